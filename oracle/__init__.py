@@ -1,0 +1,247 @@
+"""CPU oracle for paged-KV gather / scatter / transfer (ctypes wrapper of kvx_oracle.c).
+
+TEST INFRASTRUCTURE ONLY.  The test suite, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` may load this module; the library path never does.  It shares no code
+with the CUDA library: the C source computes every address on its own from the pages'
+definitions (see the header comment of ``kvx_oracle.h`` for the passages followed).
+
+Pools are described by numpy byte arrays: a :class:`Pool` holds one base array plus the byte
+offset of every plane inside it (or one array per plane), so the same numpy memory can be
+copied to the GPU and compared byte for byte afterwards.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass, field
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kvx_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libkvx_oracle.so")
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_OUT_OF_RANGE = 3
+ERR_DUPLICATE_DST = 4
+
+TOKEN_ROWS = 0
+HND_PAGES = 1
+
+OP_GATHER = 0
+OP_SCATTER = 1
+OP_TRANSFER = 2
+
+
+def build(src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the oracle with the host C compiler (plain -O2, no vectorisation flags)."""
+    cmd = ["gcc", "-O2", "-std=c99", "-Wall", "-Wextra", "-shared", "-fPIC", src, "-o", out]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+class _Pool(ctypes.Structure):
+    _fields_ = [
+        ("num_layers", ctypes.c_int32),
+        ("kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("elem_bytes", ctypes.c_int32),
+        ("kind", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("num_slots", ctypes.c_int64),
+        ("planes", ctypes.POINTER(ctypes.c_void_p)),
+        ("slot_stride", ctypes.c_int64),
+    ]
+
+
+class Request(ctypes.Structure):
+    _fields_ = [
+        ("op", ctypes.c_int32),
+        ("n_tokens", ctypes.c_int32),
+        ("src_off", ctypes.c_int64),
+        ("dst_off", ctypes.c_int64),
+        ("buf_off", ctypes.c_int64),
+    ]
+
+
+class Chunk(ctypes.Structure):
+    _fields_ = [("req", ctypes.c_int32), ("src", ctypes.c_int32), ("dst", ctypes.c_int32),
+                ("rows", ctypes.c_int32)]
+
+
+_lib_cache = {}
+
+
+def load(path: str = _LIB_PATH) -> ctypes.CDLL:
+    """Load (building first if needed) the oracle shared library at ``path``."""
+    if path in _lib_cache:
+        return _lib_cache[path]
+    if not os.path.exists(path) or (path == _LIB_PATH and
+                                    os.path.getmtime(path) < os.path.getmtime(_SRC)):
+        build(out=path)
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER
+    i32p, u8p = P(ctypes.c_int32), ctypes.c_void_p
+    lib.kvxo_bytes_per_token.restype = ctypes.c_int64
+    lib.kvxo_bytes_per_token.argtypes = [ctypes.c_int32] * 4
+    lib.kvxo_row_bytes.restype = ctypes.c_int64
+    lib.kvxo_row_bytes.argtypes = [P(_Pool)]
+    lib.kvxo_check_slots.argtypes = [P(_Pool), i32p, ctypes.c_int64]
+    lib.kvxo_has_duplicate.argtypes = [i32p, ctypes.c_int64, ctypes.c_int64]
+    lib.kvxo_gather.argtypes = [P(_Pool), i32p, ctypes.c_int64, u8p, P(ctypes.c_int64)]
+    lib.kvxo_scatter.argtypes = [P(_Pool), i32p, ctypes.c_int64, u8p, ctypes.c_int,
+                                 P(ctypes.c_int64)]
+    lib.kvxo_transfer.argtypes = [P(_Pool), i32p, P(_Pool), i32p, ctypes.c_int64, ctypes.c_int,
+                                  P(ctypes.c_int64)]
+    lib.kvxo_hnd_gather.argtypes = [P(_Pool), i32p, ctypes.c_int64, u8p]
+    lib.kvxo_hnd_rebuild.argtypes = [P(_Pool), i32p, ctypes.c_int64, u8p]
+    lib.kvxo_batch.argtypes = [P(_Pool), P(_Pool), P(Request), ctypes.c_int32, i32p,
+                               ctypes.c_int64, i32p, ctypes.c_int64, u8p, ctypes.c_int64, i32p]
+    lib.kvxo_plan.restype = ctypes.c_int64
+    lib.kvxo_plan.argtypes = [i32p, i32p, ctypes.c_int64, P(ctypes.c_int64), ctypes.c_int32,
+                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                              P(Chunk), ctypes.c_int64]
+    _lib_cache[path] = lib
+    return lib
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _i32p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+@dataclass
+class Pool:
+    """A KV pool in host memory.
+
+    ``planes`` holds, for every plane p = 2*layer + kv, a pair (array, byte_offset): the plane
+    starts ``byte_offset`` bytes into the uint8 view of ``array``.  ``kind`` is TOKEN_ROWS
+    (slot s at ``slot_stride * s``) or HND_PAGES ([page][head][page_size][dim]).
+    """
+
+    num_layers: int
+    kv_heads: int
+    head_dim: int
+    elem_bytes: int
+    kind: int
+    num_slots: int
+    planes: List[tuple]
+    slot_stride: int = 0
+    page_size: int = 1
+    _keep: list = field(default_factory=list, repr=False)
+
+    @property
+    def num_planes(self) -> int:
+        return 2 * self.num_layers
+
+    @property
+    def row_bytes(self) -> int:
+        return self.kv_heads * self.head_dim * self.elem_bytes
+
+    def _struct(self) -> _Pool:
+        ptrs = (ctypes.c_void_p * self.num_planes)()
+        for p, (arr, off) in enumerate(self.planes):
+            assert arr.flags["C_CONTIGUOUS"]
+            ptrs[p] = arr.ctypes.data + int(off)
+        s = _Pool(self.num_layers, self.kv_heads, self.head_dim, self.elem_bytes, self.kind,
+                  self.page_size, self.num_slots, ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p)),
+                  self.slot_stride)
+        self._keep = [ptrs]
+        return s
+
+
+def bytes_per_token(num_layers: int, kv_heads: int, head_dim: int, elem_bytes: int,
+                    lib: Optional[ctypes.CDLL] = None) -> int:
+    return int((lib or load()).kvxo_bytes_per_token(num_layers, kv_heads, head_dim, elem_bytes))
+
+
+def gather(pool: Pool, slots, lib=None):
+    """Returns (status, buffer bytes [P*n*R] (None on error), bytes written)."""
+    lib = lib or load()
+    slots = _i32(slots)
+    n = len(slots)
+    buf = np.zeros(max(1, pool.num_planes * n * pool.row_bytes), dtype=np.uint8)
+    written = ctypes.c_int64(0)
+    ps = pool._struct()
+    rc = lib.kvxo_gather(ctypes.byref(ps), _i32p(slots), n, buf.ctypes.data, ctypes.byref(written))
+    if rc != OK:
+        return rc, None, 0
+    return rc, buf[: pool.num_planes * n * pool.row_bytes], written.value
+
+
+def scatter(pool: Pool, slots, buf: np.ndarray, check_dup: bool = False, lib=None):
+    lib = lib or load()
+    slots = _i32(slots)
+    buf = np.ascontiguousarray(buf).view(np.uint8)
+    written = ctypes.c_int64(0)
+    ps = pool._struct()
+    rc = lib.kvxo_scatter(ctypes.byref(ps), _i32p(slots), len(slots), buf.ctypes.data,
+                          int(check_dup), ctypes.byref(written))
+    return rc, written.value
+
+
+def transfer(src: Pool, src_slots, dst: Pool, dst_slots, check_dup: bool = False, lib=None):
+    lib = lib or load()
+    a, b = _i32(src_slots), _i32(dst_slots)
+    assert len(a) == len(b)
+    written = ctypes.c_int64(0)
+    s1, s2 = src._struct(), dst._struct()
+    rc = lib.kvxo_transfer(ctypes.byref(s1), _i32p(a), ctypes.byref(s2), _i32p(b), len(a),
+                           int(check_dup), ctypes.byref(written))
+    return rc, written.value
+
+
+def hnd_gather(pool: Pool, page_table, seq_len: int, lib=None):
+    lib = lib or load()
+    pt = _i32(page_table)
+    buf = np.zeros(max(1, pool.num_planes * seq_len * pool.row_bytes), dtype=np.uint8)
+    ps = pool._struct()
+    rc = lib.kvxo_hnd_gather(ctypes.byref(ps), _i32p(pt), seq_len, buf.ctypes.data)
+    if rc != OK:
+        return rc, None
+    return rc, buf[: pool.num_planes * seq_len * pool.row_bytes]
+
+
+def hnd_rebuild(pool: Pool, page_table, seq_len: int, buf: np.ndarray, lib=None):
+    lib = lib or load()
+    pt = _i32(page_table)
+    buf = np.ascontiguousarray(buf).view(np.uint8)
+    ps = pool._struct()
+    return lib.kvxo_hnd_rebuild(ctypes.byref(ps), _i32p(pt), seq_len, buf.ctypes.data)
+
+
+def batch(src: Optional[Pool], dst: Optional[Pool], reqs: Sequence[tuple], src_slots,
+          dst_slots, buf: np.ndarray, lib=None) -> np.ndarray:
+    """reqs: sequence of (op, n_tokens, src_off, dst_off, buf_off).  Returns status[n+1]."""
+    lib = lib or load()
+    arr = (Request * max(1, len(reqs)))(*[Request(*r) for r in reqs])
+    a, b = _i32(src_slots), _i32(dst_slots)
+    status = np.zeros(len(reqs) + 1, dtype=np.int32)
+    s1 = src._struct() if src is not None else None
+    s2 = dst._struct() if dst is not None else None
+    buf = buf.view(np.uint8)
+    lib.kvxo_batch(ctypes.byref(s1) if s1 else None, ctypes.byref(s2) if s2 else None, arr,
+                   len(reqs), _i32p(a), len(a), _i32p(b), len(b), buf.ctypes.data, buf.nbytes,
+                   _i32p(status))
+    return status
+
+
+def plan(src_idx, dst_idx, req_start, src_page_size: int, dst_page_size: int,
+         tile_tokens: int, chunk_rows: int, lib=None) -> np.ndarray:
+    """Run-length plan; returns an int32 array [n_chunks][4] = (req, src, dst, rows)."""
+    lib = lib or load()
+    a, b = _i32(src_idx), _i32(dst_idx)
+    rs = np.ascontiguousarray(np.asarray(req_start, dtype=np.int64))
+    n = len(a)
+    out = (Chunk * max(1, n))()
+    cnt = lib.kvxo_plan(_i32p(a), _i32p(b), n, rs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                        len(rs), src_page_size, dst_page_size, tile_tokens, chunk_rows, out, n)
+    assert 0 <= cnt <= n
+    res = np.frombuffer(out, dtype=np.int32).reshape(-1, 4)[:cnt].copy()
+    return res

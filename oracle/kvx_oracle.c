@@ -1,0 +1,298 @@
+/*
+ * kvx_oracle.c -- the plain CPU definition of paged-KV gather / scatter / transfer.
+ *
+ * TEST INFRASTRUCTURE ONLY (see kvx_oracle.h): single-threaded, one head vector at a time,
+ * no blocking, no fusion, no reordering.  Each function says which passage it follows.
+ */
+#include "kvx_oracle.h"
+
+#include <stdlib.h>
+#include <string.h>
+
+int64_t kvxo_bytes_per_token(int32_t num_layers, int32_t kv_heads, int32_t head_dim,
+                             int32_t elem_bytes) {
+  /* [DistServe] KV Cache 跨实例传输: B_KV = 2 x L x n_layer x n_kvhead x d_head x b, here
+   * for L = 1 token.  The 2 is K and V. */
+  return (int64_t)2 * num_layers * kv_heads * head_dim * elem_bytes;
+}
+
+static int64_t head_bytes(const kvxo_pool *pool) {
+  return (int64_t)pool->head_dim * pool->elem_bytes;
+}
+
+int64_t kvxo_row_bytes(const kvxo_pool *pool) { return pool->kv_heads * head_bytes(pool); }
+
+static int32_t num_planes(const kvxo_pool *pool) { return 2 * pool->num_layers; }
+
+/* Address of head vector (plane, slot, head). */
+static uint8_t *head_vec(const kvxo_pool *pool, int32_t plane, int64_t slot, int32_t head) {
+  uint8_t *base = pool->planes[plane];
+  int64_t hb = head_bytes(pool);
+  if (pool->kind == KVXO_HND_PAGES) {
+    /* [Mooncake] 7.7: HND page = [head][page_size][dim]. */
+    int64_t page = slot / pool->page_size;
+    int64_t off = slot % pool->page_size;
+    return base + ((page * pool->kv_heads + head) * pool->page_size + off) * hb;
+  }
+  /* Token rows: one slot holds every head of one token ([PD-budget] 5090 section: the pool is
+   * paged per token). */
+  return base + slot * pool->slot_stride + head * hb;
+}
+
+/* Address of head vector (plane, token, head) in a [plane][n][head][dim] buffer. */
+static uint8_t *buf_vec(uint8_t *buf, const kvxo_pool *pool, int32_t plane, int64_t n,
+                        int64_t token, int32_t head) {
+  return buf + (((int64_t)plane * n + token) * pool->kv_heads + head) * head_bytes(pool);
+}
+
+int kvxo_check_slots(const kvxo_pool *pool, const int32_t *slots, int64_t n) {
+  for (int64_t i = 0; i < n; ++i)
+    if (slots[i] < 0 || (int64_t)slots[i] >= pool->num_slots) return KVXO_ERR_OUT_OF_RANGE;
+  return KVXO_OK;
+}
+
+int kvxo_has_duplicate(const int32_t *slots, int64_t n, int64_t num_slots) {
+  unsigned char *seen = (unsigned char *)calloc((size_t)num_slots, 1);
+  int dup = 0;
+  if (!seen) return 1;
+  for (int64_t i = 0; i < n && !dup; ++i) {
+    if (slots[i] < 0 || slots[i] >= num_slots) continue;
+    if (seen[slots[i]]) dup = 1;
+    seen[slots[i]] = 1;
+  }
+  free(seen);
+  return dup;
+}
+
+int kvxo_gather(const kvxo_pool *src, const int32_t *slots, int64_t n, uint8_t *buf,
+                int64_t *bytes_written) {
+  /* [PD-budget] 5090 section: P gathers the rows to send into one contiguous staging region.
+   * [mini-infer] KV 序列化格式选择: per layer (k, v), each [seq, kv_heads, head_dim]. */
+  int64_t hb = head_bytes(src);
+  int rc = kvxo_check_slots(src, slots, n);
+  if (rc != KVXO_OK) return rc;
+  for (int32_t p = 0; p < num_planes(src); ++p)
+    for (int64_t i = 0; i < n; ++i)
+      for (int32_t h = 0; h < src->kv_heads; ++h)
+        memcpy(buf_vec(buf, src, p, n, i, h), head_vec(src, p, slots[i], h), (size_t)hb);
+  if (bytes_written) *bytes_written = n * num_planes(src) * kvxo_row_bytes(src);
+  return KVXO_OK;
+}
+
+int kvxo_scatter(const kvxo_pool *dst, const int32_t *slots, int64_t n, const uint8_t *buf,
+                 int check_dup, int64_t *bytes_written) {
+  /* [PD-budget] 5090 section: D scatters the staged rows back into its own pages. */
+  int64_t hb = head_bytes(dst);
+  int rc = kvxo_check_slots(dst, slots, n);
+  if (rc != KVXO_OK) return rc;
+  if (check_dup && kvxo_has_duplicate(slots, n, dst->num_slots)) return KVXO_ERR_DUPLICATE_DST;
+  for (int32_t p = 0; p < num_planes(dst); ++p)
+    for (int64_t i = 0; i < n; ++i)
+      for (int32_t h = 0; h < dst->kv_heads; ++h)
+        memcpy(head_vec(dst, p, slots[i], h), buf_vec((uint8_t *)buf, dst, p, n, i, h),
+               (size_t)hb);
+  if (bytes_written) *bytes_written = n * num_planes(dst) * kvxo_row_bytes(dst);
+  return KVXO_OK;
+}
+
+static int same_row_shape(const kvxo_pool *a, const kvxo_pool *b) {
+  return a->num_layers == b->num_layers && a->kv_heads == b->kv_heads &&
+         a->head_dim == b->head_dim && a->elem_bytes == b->elem_bytes;
+}
+
+int kvxo_transfer(const kvxo_pool *src, const int32_t *src_slots, const kvxo_pool *dst,
+                  const int32_t *dst_slots, int64_t n, int check_dup, int64_t *bytes_written) {
+  /* [PD-budget] B300 section: a gather kernel on P writes the scattered source rows straight
+   * into D's pages.  [DistServe] 第三步: layer j of P goes only to layer j of D, so plane p
+   * maps to plane p. */
+  int64_t hb = head_bytes(src);
+  int rc;
+  if (!same_row_shape(src, dst)) return KVXO_ERR_INVALID_ARG;
+  rc = kvxo_check_slots(src, src_slots, n);
+  if (rc == KVXO_OK) rc = kvxo_check_slots(dst, dst_slots, n);
+  if (rc != KVXO_OK) return rc;
+  if (check_dup && kvxo_has_duplicate(dst_slots, n, dst->num_slots))
+    return KVXO_ERR_DUPLICATE_DST;
+  for (int32_t p = 0; p < num_planes(src); ++p)
+    for (int64_t i = 0; i < n; ++i)
+      for (int32_t h = 0; h < src->kv_heads; ++h)
+        memcpy(head_vec(dst, p, dst_slots[i], h), head_vec(src, p, src_slots[i], h),
+               (size_t)hb);
+  if (bytes_written) *bytes_written = n * num_planes(src) * kvxo_row_bytes(src);
+  return KVXO_OK;
+}
+
+static int check_page_table(const kvxo_pool *pool, const int32_t *page_table, int64_t seq_len) {
+  int64_t num_pages, n_pt;
+  if (pool->kind != KVXO_HND_PAGES || pool->page_size <= 0) return KVXO_ERR_INVALID_ARG;
+  num_pages = pool->num_slots / pool->page_size;
+  n_pt = (seq_len + pool->page_size - 1) / pool->page_size;
+  for (int64_t j = 0; j < n_pt; ++j)
+    if (page_table[j] < 0 || page_table[j] >= num_pages) return KVXO_ERR_OUT_OF_RANGE;
+  return KVXO_OK;
+}
+
+int kvxo_hnd_gather(const kvxo_pool *src, const int32_t *page_table, int64_t seq_len,
+                    uint8_t *buf) {
+  /* [mini-infer] KV 序列化格式选择: take the per-layer [heads, seq, dim] cache and permute
+   * (1, 0, 2) to [seq, heads, dim].  Here the [heads, seq, dim] view is read through the page
+   * table of an HND pool ([Mooncake] 7.7), materialised per plane, then permuted. */
+  int32_t H = src->kv_heads, ps = src->page_size;
+  int64_t hb = head_bytes(src);
+  uint8_t *logical;
+  int rc = check_page_table(src, page_table, seq_len);
+  if (rc != KVXO_OK) return rc;
+  logical = (uint8_t *)malloc((size_t)(H * seq_len * hb > 0 ? H * seq_len * hb : 1));
+  if (!logical) return KVXO_ERR_INVALID_ARG;
+  for (int32_t p = 0; p < num_planes(src); ++p) {
+    /* logical[h][s][:] = page page_table[s / ps], head h, offset s % ps */
+    for (int32_t h = 0; h < H; ++h)
+      for (int64_t s = 0; s < seq_len; ++s) {
+        int64_t slot = (int64_t)page_table[s / ps] * ps + s % ps;
+        memcpy(logical + ((int64_t)h * seq_len + s) * hb, head_vec(src, p, slot, h),
+               (size_t)hb);
+      }
+    /* buf[p][s][h][:] = logical[h][s][:]   (permute(1, 0, 2)) */
+    for (int64_t s = 0; s < seq_len; ++s)
+      for (int32_t h = 0; h < H; ++h)
+        memcpy(buf_vec(buf, src, p, seq_len, s, h), logical + ((int64_t)h * seq_len + s) * hb,
+               (size_t)hb);
+  }
+  free(logical);
+  return KVXO_OK;
+}
+
+int kvxo_hnd_rebuild(const kvxo_pool *dst, const int32_t *page_table, int64_t seq_len,
+                     const uint8_t *buf) {
+  /* [mini-infer] KV 序列化格式选择, rebuild direction: [seq, heads, dim] -> permute(1, 0, 2)
+   * -> [heads, seq, dim], then stored into the pages named by the page table. */
+  int32_t H = dst->kv_heads, ps = dst->page_size;
+  int64_t hb = head_bytes(dst);
+  uint8_t *logical;
+  int rc = check_page_table(dst, page_table, seq_len);
+  if (rc != KVXO_OK) return rc;
+  logical = (uint8_t *)malloc((size_t)(H * seq_len * hb > 0 ? H * seq_len * hb : 1));
+  if (!logical) return KVXO_ERR_INVALID_ARG;
+  for (int32_t p = 0; p < num_planes(dst); ++p) {
+    for (int64_t s = 0; s < seq_len; ++s)
+      for (int32_t h = 0; h < H; ++h)
+        memcpy(logical + ((int64_t)h * seq_len + s) * hb,
+               buf_vec((uint8_t *)buf, dst, p, seq_len, s, h), (size_t)hb);
+    for (int32_t h = 0; h < H; ++h)
+      for (int64_t s = 0; s < seq_len; ++s) {
+        int64_t slot = (int64_t)page_table[s / ps] * ps + s % ps;
+        memcpy(head_vec(dst, p, slot, h), logical + ((int64_t)h * seq_len + s) * hb,
+               (size_t)hb);
+      }
+  }
+  free(logical);
+  return KVXO_OK;
+}
+
+static int check_request(const kvxo_pool *src, const kvxo_pool *dst, const kvxo_request *r,
+                         int64_t n_src_slots, int64_t n_dst_slots, int64_t buf_bytes,
+                         const int32_t *src_slots, const int32_t *dst_slots) {
+  int uses_src = r->op == KVXO_OP_GATHER || r->op == KVXO_OP_TRANSFER;
+  int uses_dst = r->op == KVXO_OP_SCATTER || r->op == KVXO_OP_TRANSFER;
+  int uses_buf = r->op == KVXO_OP_GATHER || r->op == KVXO_OP_SCATTER;
+  int rc;
+  if (r->op < KVXO_OP_GATHER || r->op > KVXO_OP_TRANSFER || r->n_tokens < 0)
+    return KVXO_ERR_INVALID_ARG;
+  if (uses_src && (r->src_off < 0 || r->src_off + r->n_tokens > n_src_slots))
+    return KVXO_ERR_INVALID_ARG;
+  if (uses_dst && (r->dst_off < 0 || r->dst_off + r->n_tokens > n_dst_slots))
+    return KVXO_ERR_INVALID_ARG;
+  if (uses_buf) {
+    const kvxo_pool *pool = uses_src ? src : dst;
+    int64_t need = (int64_t)r->n_tokens * num_planes(pool) * kvxo_row_bytes(pool);
+    if (r->buf_off < 0 || r->buf_off % 16 != 0 || r->buf_off + need > buf_bytes)
+      return KVXO_ERR_INVALID_ARG;
+  }
+  if (uses_src && (rc = kvxo_check_slots(src, src_slots + r->src_off, r->n_tokens)) != KVXO_OK)
+    return rc;
+  if (uses_dst && (rc = kvxo_check_slots(dst, dst_slots + r->dst_off, r->n_tokens)) != KVXO_OK)
+    return rc;
+  return KVXO_OK;
+}
+
+int kvxo_batch(const kvxo_pool *src, const kvxo_pool *dst, const kvxo_request *reqs,
+               int32_t n_reqs, const int32_t *src_slots, int64_t n_src_slots,
+               const int32_t *dst_slots, int64_t n_dst_slots, uint8_t *buf, int64_t buf_bytes,
+               int32_t *status) {
+  /* [Mooncake] 6.1: a batch of non-contiguous transfers submitted together; each is its own
+   * request with its own status. */
+  status[0] = KVXO_OK;
+  if (src && dst && !same_row_shape(src, dst)) {
+    for (int32_t q = 0; q <= n_reqs; ++q) status[q] = KVXO_ERR_INVALID_ARG;
+    return KVXO_ERR_INVALID_ARG;
+  }
+  for (int32_t q = 0; q < n_reqs; ++q) {
+    const kvxo_request *r = &reqs[q];
+    int rc = check_request(src, dst, r, n_src_slots, n_dst_slots, buf_bytes, src_slots,
+                           dst_slots);
+    if (rc == KVXO_OK) {
+      if (r->op == KVXO_OP_GATHER)
+        rc = kvxo_gather(src, src_slots + r->src_off, r->n_tokens, buf + r->buf_off, NULL);
+      else if (r->op == KVXO_OP_SCATTER)
+        rc = kvxo_scatter(dst, dst_slots + r->dst_off, r->n_tokens, buf + r->buf_off, 0, NULL);
+      else
+        rc = kvxo_transfer(src, src_slots + r->src_off, dst, dst_slots + r->dst_off,
+                           r->n_tokens, 0, NULL);
+    }
+    status[1 + q] = rc;
+    if (rc > status[0]) status[0] = rc;
+  }
+  return status[0];
+}
+
+int64_t kvxo_plan(const int32_t *src_idx, const int32_t *dst_idx, int64_t n,
+                  const int64_t *req_start, int32_t n_reqs, int32_t src_page_size,
+                  int32_t dst_page_size, int32_t tile_tokens, int32_t chunk_rows,
+                  kvxo_chunk *out, int64_t max_chunks) {
+  /* [Mooncake] 7.6: consecutive blocks are merged into one descriptor.  Step 1 marks the
+   * tokens where a run must start; step 2 walks the runs and cuts each into pieces of at most
+   * chunk_rows rows. */
+  int32_t *req_of = NULL;
+  unsigned char *brk = NULL;
+  int64_t count = 0;
+  if (n <= 0) return 0;
+  req_of = (int32_t *)malloc((size_t)n * sizeof(int32_t));
+  brk = (unsigned char *)calloc((size_t)n, 1);
+  if (!req_of || !brk) {
+    free(req_of);
+    free(brk);
+    return -1;
+  }
+  /* request of every token, and request starts */
+  for (int32_t q = 0; q < n_reqs; ++q) {
+    int64_t end = (q + 1 < n_reqs) ? req_start[q + 1] : n;
+    for (int64_t i = req_start[q]; i < end; ++i) req_of[i] = q;
+    if (req_start[q] < n) brk[req_start[q]] = 1;
+  }
+  /* step 1: run starts */
+  for (int64_t i = 0; i < n; ++i) {
+    if (i == 0 || i % tile_tokens == 0) brk[i] = 1;
+    if (i > 0 && src_idx[i] != src_idx[i - 1] + 1) brk[i] = 1;
+    if (i > 0 && dst_idx[i] != dst_idx[i - 1] + 1) brk[i] = 1;
+    if (src_page_size > 1 && src_idx[i] % src_page_size == 0) brk[i] = 1;
+    if (dst_page_size > 1 && dst_idx[i] % dst_page_size == 0) brk[i] = 1;
+  }
+  /* step 2: each run [a, b) becomes ceil((b - a) / chunk_rows) chunks */
+  for (int64_t a = 0; a < n;) {
+    int64_t b = a + 1;
+    while (b < n && !brk[b]) ++b;
+    for (int64_t j = 0; j < b - a; j += chunk_rows) {
+      if (count < max_chunks) {
+        out[count].req = req_of[a];
+        out[count].src = src_idx[a] + (int32_t)j;
+        out[count].dst = dst_idx[a] + (int32_t)j;
+        out[count].rows = (int32_t)((b - a - j) < chunk_rows ? (b - a - j) : chunk_rows);
+      }
+      ++count;
+    }
+    a = b;
+  }
+  free(req_of);
+  free(brk);
+  return count;
+}

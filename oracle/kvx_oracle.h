@@ -1,0 +1,148 @@
+/*
+ * kvx_oracle.h -- CPU oracle for moving a finished prefill's KV cache out of a
+ * token-paged KV pool.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This library is the plain, slow, single-threaded
+ * definition of what the GPU library computes.  Only the test suite, the smoke
+ * check and the benchmark's CPU-baseline leg may load it; the product path never
+ * calls, links or imports it.  It shares no code, header, helper or constant
+ * table with the CUDA library: every address below is computed here, from the
+ * pages' definitions, independently.
+ *
+ * Sources (web pages, cited by title and section):
+ *  [PD-budget]  "穷人版 PD 分离：在消费级显卡上把 TTS 推理拆成两半" (kilerd.me/pd-on-a-budget)
+ *               sections "第一堵墙" (144 KiB/token x 2048 = 288 MiB), "B300：让 P 直接写 D 的显存"
+ *               (gather kernel writes scattered source rows straight into D's pages),
+ *               "5090：一个看得见所有卡的代理" (token-paged pool, few-KB fragments, gather to a
+ *               contiguous staging region, then scatter back into D's pages).
+ *  [DistServe]  "DistServe 完全拆解" section "KV Cache 跨实例传输" (B_KV = 2 L n_layer n_kvhead
+ *               d_head b) and "第三步：根据网络亲和性映射 stage" (layer j goes only to layer j).
+ *  [mini-infer] "mini-infer系统实战-18-PD 解耦" sections "KV 序列化格式选择" (list of per-layer
+ *               (k, v), each [seq, kv_heads, head_dim], via permute(1,0,2) of [heads, seq, dim])
+ *               and "KV 传输大小" (the KV size table).
+ *  [Mooncake]   "PD分离调研：从推理阶段拆分到Mooncake的KVCache中心架构" sections 6.1 (batch of
+ *               non-contiguous src/dst transfers), 7.4 (per-layer KV tensors registered by base
+ *               address and block length), 7.6 (contiguous blocks coalesced into fewer transfer
+ *               descriptors), 7.7 (HND layout for non-MLA KV).
+ *
+ * Conventions:
+ *  - A pool has P = 2 * num_layers planes; plane p = 2*layer + kv with K = 0, V = 1
+ *    (the (k, v) tuple order of [mini-infer] "KV 序列化格式选择").
+ *  - A row is one (plane, token): kv_heads head vectors of head_dim elements, R bytes.
+ *  - A contiguous transfer buffer is [plane][token][head][dim]
+ *    = [layer][K/V][seq][kv_heads][head_dim] ([mini-infer] transfer format).
+ *  - Values are never interpreted: every operation is a byte copy.
+ */
+#ifndef KVX_ORACLE_H
+#define KVX_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Result codes (numerically equal to the library's, written out here on their own). */
+#define KVXO_OK 0
+#define KVXO_ERR_INVALID_ARG 1
+#define KVXO_ERR_OUT_OF_RANGE 3
+#define KVXO_ERR_DUPLICATE_DST 4
+
+/* Pool kinds. */
+#define KVXO_TOKEN_ROWS 0 /* plane = [slot][head][dim]; slot rows slot_stride bytes apart */
+#define KVXO_HND_PAGES 1  /* plane = [page][head][page_size][dim]  ([Mooncake] 7.7 HND) */
+
+/* Batch request kinds. */
+#define KVXO_OP_GATHER 0
+#define KVXO_OP_SCATTER 1
+#define KVXO_OP_TRANSFER 2
+
+typedef struct kvxo_pool {
+  int32_t num_layers;
+  int32_t kv_heads;
+  int32_t head_dim;
+  int32_t elem_bytes;
+  int32_t kind;
+  int32_t page_size; /* HND pages only */
+  int64_t num_slots; /* token slots per plane (HND: pages * page_size) */
+  uint8_t **planes;  /* 2*num_layers plane base addresses, plane 2*layer + kv */
+  int64_t slot_stride; /* token rows only: bytes from slot s to slot s+1 */
+} kvxo_pool;
+
+typedef struct kvxo_request {
+  int32_t op;
+  int32_t n_tokens;
+  int64_t src_off; /* element offset into the batch's source slot list */
+  int64_t dst_off; /* element offset into the batch's destination slot list */
+  int64_t buf_off; /* byte offset of this request's [plane][token][head][dim] region */
+} kvxo_request;
+
+typedef struct kvxo_chunk {
+  int32_t req;  /* request the rows belong to */
+  int32_t src;  /* first source index (slot, or token for a buffer side) */
+  int32_t dst;  /* first destination index */
+  int32_t rows; /* consecutive rows covered */
+} kvxo_chunk;
+
+/* B_KV per token = 2 * n_layer * n_kvhead * d_head * b   ([DistServe] KV Cache 跨实例传输). */
+int64_t kvxo_bytes_per_token(int32_t num_layers, int32_t kv_heads, int32_t head_dim,
+                             int32_t elem_bytes);
+
+/* Bytes of one (plane, token) row: kv_heads * head_dim * elem_bytes. */
+int64_t kvxo_row_bytes(const kvxo_pool *pool);
+
+/* Validation shared by every operation below: every index in [0, num_slots). */
+int kvxo_check_slots(const kvxo_pool *pool, const int32_t *slots, int64_t n);
+
+/* Same slot twice among the destinations. */
+int kvxo_has_duplicate(const int32_t *slots, int64_t n, int64_t num_slots);
+
+/* Gather: buf[p][i] = row(src, p, slots[i]).  Returns a status code; nothing is written on
+ * error.  *bytes_written (may be NULL) receives n * P * R. */
+int kvxo_gather(const kvxo_pool *src, const int32_t *slots, int64_t n, uint8_t *buf,
+                int64_t *bytes_written);
+
+/* Scatter: row(dst, p, slots[i]) = buf[p][i].  check_dup != 0 rejects repeated slots. */
+int kvxo_scatter(const kvxo_pool *dst, const int32_t *slots, int64_t n, const uint8_t *buf,
+                 int check_dup, int64_t *bytes_written);
+
+/* Pool-to-pool transfer: row(dst, p, dst_slots[i]) = row(src, p, src_slots[i]). */
+int kvxo_transfer(const kvxo_pool *src, const int32_t *src_slots, const kvxo_pool *dst,
+                  const int32_t *dst_slots, int64_t n, int check_dup, int64_t *bytes_written);
+
+/* HND gather by page table, through the logical per-plane [heads][seq][dim] view, then the
+ * [heads,seq,dim] -> [seq,heads,dim] permute of [mini-infer] "KV 序列化格式选择".
+ * Token s lives in page page_table[s / page_size] at offset s % page_size. */
+int kvxo_hnd_gather(const kvxo_pool *src, const int32_t *page_table, int64_t seq_len,
+                    uint8_t *buf);
+
+/* Inverse rebuild: [seq,heads,dim] -> [heads,seq,dim] permute, then written into the pages. */
+int kvxo_hnd_rebuild(const kvxo_pool *dst, const int32_t *page_table, int64_t seq_len,
+                     const uint8_t *buf);
+
+/* Batch: every request applied in index order ([Mooncake] 6.1 BatchTransfer).
+ * status[0] = largest code of any request, status[1 + q] = code of request q.  A failing
+ * request writes nothing; the others still run.  The buffer region of request q is
+ * buf + buf_off laid out [plane][n_tokens][head][dim]. */
+int kvxo_batch(const kvxo_pool *src, const kvxo_pool *dst, const kvxo_request *reqs,
+               int32_t n_reqs, const int32_t *src_slots, int64_t n_src_slots,
+               const int32_t *dst_slots, int64_t n_dst_slots, uint8_t *buf, int64_t buf_bytes,
+               int32_t *status);
+
+/* Run-length plan ([Mooncake] 7.6: contiguous blocks coalesced into fewer descriptors).
+ * src_idx / dst_idx give each token's source and destination index (slot, or the token's own
+ * position for a buffer side).  req_start lists the first token of every request (ascending,
+ * req_start[0] = 0).  A run ends where either index sequence stops increasing by one, at a
+ * request start, at every multiple of tile_tokens, and at each page start of a side whose
+ * page_size > 1.  Each run is cut into pieces of at most chunk_rows rows.
+ * Writes up to max_chunks chunks and returns the number of chunks. */
+int64_t kvxo_plan(const int32_t *src_idx, const int32_t *dst_idx, int64_t n,
+                  const int64_t *req_start, int32_t n_reqs, int32_t src_page_size,
+                  int32_t dst_page_size, int32_t tile_tokens, int32_t chunk_rows,
+                  kvxo_chunk *out, int64_t max_chunks);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVX_ORACLE_H */

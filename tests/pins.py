@@ -1,0 +1,362 @@
+"""Pins that tie the oracle to something other than itself.
+
+Every function here takes the oracle's ctypes library and raises AssertionError when the
+oracle disagrees with: a size the pages print (tests/golden/kv_sizes.json), the
+element-by-element brute-force model (tests/bruteforce.py) on every small injective slot map
+and page table, an invariant the pages state, or a numpy routine that the method reduces to
+in a special case.  test_oracle_pins.py runs them against the real oracle;
+test_oracle_mutants.py runs them against oracle builds with a planted mistake and expects a
+failure for each one.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import os
+
+import numpy as np
+
+import oracle
+from tests import bruteforce as bf
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "kv_sizes.json")
+UNITS = {"KiB": 2 ** 10, "MiB": 2 ** 20, "GiB": 2 ** 30}
+
+# tiny shapes: 2 layers (4 planes), 2 heads, head_dim 4 -> 16-byte rows
+L, H, D = 2, 2, 4
+
+
+def _arange_fill(start):
+    return lambda n: (np.arange(n, dtype=np.int64) + start).astype(np.uint16)
+
+
+def _sentinel_fill(n):
+    return (0x7E00 | (np.arange(n) % 509)).astype(np.uint16)
+
+
+def _bytes_of(buf5d):
+    return np.ascontiguousarray(buf5d).view(np.uint8).reshape(-1)
+
+
+def pin_sizes(lib):
+    """[DistServe] B_KV and the pages' printed sizes (golden fixture)."""
+    table = json.load(open(GOLDEN))
+    for e in table["entries"]:
+        per_tok = oracle.bytes_per_token(e["layers"], e["kv_heads"], e["head_dim"],
+                                         e["elem_bytes"], lib=lib)
+        total = per_tok * e["tokens"]
+        assert total == e["bytes"], (e["name"], total, e["bytes"])
+        assert abs(total / UNITS[e["unit"]] - e["stated"]) <= e["tol"], e["name"]
+        if "per_token_bytes" in e:
+            assert per_tok == e["per_token_bytes"]
+            assert per_tok / UNITS[e["per_token_unit"]] == e["per_token_stated"]
+
+
+def pin_bytes_written(lib):
+    """The oracle reports n * P * R bytes moved, and R = kv_heads * head_dim * elem_bytes."""
+    pool = bf.make_pool("planes", L, H, D, 8, _arange_fill(0))
+    op = bf.to_oracle(pool)
+    rc, buf, written = oracle.gather(op, [3, 1, 6], lib=lib)
+    assert rc == oracle.OK
+    assert written == 3 * 2 * L * H * D * 2 == buf.nbytes
+    assert written == 3 * oracle.bytes_per_token(L, H, D, 2, lib=lib)
+
+
+def _maps(num_slots, nmax):
+    for n in range(nmax + 1):
+        yield from itertools.permutations(range(num_slots), n)
+
+
+def pin_bruteforce_gather(lib):
+    """All injective slot maps of n <= 3 tokens from 4-slot pools, every layout."""
+    for layout, ps in (("planes", 1), ("slot_major", 1), ("hnd", 2)):
+        pool = bf.make_pool(layout, L, H, D, 4, _arange_fill(1), page_size=ps)
+        op = bf.to_oracle(pool)
+        before = pool.data.copy()
+        for slots in _maps(4, 3):
+            want = _bytes_of(bf.gather(pool, slots))
+            rc, buf, _ = oracle.gather(op, list(slots), lib=lib)
+            assert rc == oracle.OK
+            assert np.array_equal(buf, want), (layout, slots)
+        assert np.array_equal(pool.data, before), "source modified"
+
+
+def pin_bruteforce_scatter(lib):
+    for layout, ps in (("planes", 1), ("slot_major", 1), ("hnd", 2)):
+        base = bf.make_pool(layout, L, H, D, 4, _sentinel_fill, page_size=ps)
+        for slots in _maps(4, 3):
+            n = len(slots)
+            buf = (np.arange(L * 2 * n * H * D) + 100).astype(np.uint16).reshape(L, 2, n, H, D)
+            want = bf.scatter(base, slots, buf)
+            buf_before = buf.copy()
+            pool = base.copy()
+            rc, _ = oracle.scatter(bf.to_oracle(pool), list(slots), buf, lib=lib)
+            assert rc == oracle.OK
+            assert np.array_equal(pool.data, want.data), (layout, slots)
+            assert np.array_equal(buf, buf_before), "buffer modified"
+
+
+def pin_bruteforce_transfer(lib):
+    """Every pair of injective maps with n <= 2 between every pair of layouts."""
+    layouts = (("planes", 1), ("slot_major", 1), ("hnd", 2))
+    for (la, pa), (lb, pb) in itertools.product(layouts, layouts):
+        src = bf.make_pool(la, L, H, D, 4, _arange_fill(1), page_size=pa)
+        base = bf.make_pool(lb, L, H, D, 4, _sentinel_fill, page_size=pb)
+        for n in range(3):
+            for s in itertools.permutations(range(4), n):
+                for d in itertools.permutations(range(4), n):
+                    want = bf.transfer(src, s, base, d)
+                    src_before = src.data.copy()
+                    dst = base.copy()
+                    rc, _ = oracle.transfer(bf.to_oracle(src), list(s), bf.to_oracle(dst),
+                                            list(d), lib=lib)
+                    assert rc == oracle.OK
+                    assert np.array_equal(dst.data, want.data), (la, lb, s, d)
+                    assert np.array_equal(src.data, src_before), "source modified"
+
+
+def pin_bruteforce_hnd(lib):
+    """Every page table of k <= 3 pages out of a 4-page pool (page size 3), every sequence
+    length that ends in page k, for the page-table gather and the inverse rebuild."""
+    ps = 3
+    src = bf.make_pool("hnd", L, H, D, 4 * ps, _arange_fill(1), page_size=ps)
+    base = bf.make_pool("hnd", L, H, D, 4 * ps, _sentinel_fill, page_size=ps)
+    for k in range(1, 4):
+        for pt in itertools.permutations(range(4), k):
+            for seq in range((k - 1) * ps + 1, k * ps + 1):
+                want = bf.hnd_gather(src, pt, seq)
+                rc, buf = oracle.hnd_gather(bf.to_oracle(src), list(pt), seq, lib=lib)
+                assert rc == oracle.OK
+                assert np.array_equal(buf, _bytes_of(want)), (pt, seq)
+                dst = base.copy()
+                assert oracle.hnd_rebuild(bf.to_oracle(dst), list(pt), seq, want,
+                                          lib=lib) == oracle.OK
+                slots = [pt[s // ps] * ps + s % ps for s in range(seq)]
+                assert np.array_equal(dst.data, bf.scatter(base, slots, want).data), (pt, seq)
+
+
+def pin_roundtrip(lib):
+    """[PD-budget] 5090 section: gather into staging, scatter back.  Scattering the gathered
+    rows to the same slots leaves the pool unchanged; into a sentinel pool those slots equal
+    the source and every other slot keeps its sentinel."""
+    g = np.random.Generator(np.random.PCG64(7))
+    for layout, ps in (("planes", 1), ("slot_major", 1), ("hnd", 4)):
+        src = bf.make_pool(layout, 3, 2, 8, 64, lambda n: g.integers(0, 0x7C00, n), ps)
+        slots = g.choice(64, 20, replace=False)
+        rc, buf, _ = oracle.gather(bf.to_oracle(src), slots, lib=lib)
+        assert rc == oracle.OK
+        same = src.copy()
+        assert oracle.scatter(bf.to_oracle(same), slots, buf, lib=lib)[0] == oracle.OK
+        assert np.array_equal(same.data, src.data)
+        sent = bf.make_pool(layout, 3, 2, 8, 64, _sentinel_fill, ps)
+        ref = sent.copy()
+        assert oracle.scatter(bf.to_oracle(sent), slots, buf, lib=lib)[0] == oracle.OK
+        touched = set(int(s) for s in slots)
+        for layer in range(3):
+            for kv in range(2):
+                for slot in range(64):
+                    a = [sent.get(layer, kv, slot, h, d) for h in range(2) for d in range(8)]
+                    b = [(src if slot in touched else ref).get(layer, kv, slot, h, d)
+                         for h in range(2) for d in range(8)]
+                    assert a == b, (layout, layer, kv, slot)
+
+
+def pin_transfer_is_scatter_of_gather(lib):
+    """[PD-budget]: the B300 direct write and the 5090 staging + scatter reach the same bytes."""
+    g = np.random.Generator(np.random.PCG64(11))
+    src = bf.make_pool("planes", 2, 2, 8, 50, lambda n: g.integers(0, 0x7C00, n))
+    s = g.choice(50, 17, replace=False)
+    d = g.choice(40, 17, replace=False)
+    a = bf.make_pool("slot_major", 2, 2, 8, 40, _sentinel_fill)
+    b = a.copy()
+    assert oracle.transfer(bf.to_oracle(src), s, bf.to_oracle(a), d, lib=lib)[0] == oracle.OK
+    rc, buf, _ = oracle.gather(bf.to_oracle(src), s, lib=lib)
+    assert rc == oracle.OK
+    assert oracle.scatter(bf.to_oracle(b), d, buf, lib=lib)[0] == oracle.OK
+    assert np.array_equal(a.data, b.data)
+
+
+def pin_hnd_roundtrip(lib):
+    """[mini-infer]: permute on extract and the inverse permute on rebuild are the identity."""
+    g = np.random.Generator(np.random.PCG64(13))
+    ps = 4
+    src = bf.make_pool("hnd", 2, 3, 8, 16 * ps, lambda n: g.integers(0, 0x7C00, n), ps)
+    pt = g.choice(16, 5, replace=False)
+    seq = 4 * ps + 2  # last page partial
+    rc, buf = oracle.hnd_gather(bf.to_oracle(src), pt, seq, lib=lib)
+    assert rc == oracle.OK
+    dst = bf.make_pool("hnd", 2, 3, 8, 16 * ps, _sentinel_fill, ps)
+    ref = dst.copy()
+    assert oracle.hnd_rebuild(bf.to_oracle(dst), pt, seq, buf, lib=lib) == oracle.OK
+    rc, buf2 = oracle.hnd_gather(bf.to_oracle(dst), pt, seq, lib=lib)
+    assert np.array_equal(buf, buf2)
+    # the tail of the last page and all other pages keep their sentinel
+    touched = {int(pt[s // ps]) * ps + s % ps for s in range(seq)}
+    for slot in range(16 * ps):
+        if slot in touched:
+            continue
+        for layer in range(2):
+            for kv in range(2):
+                for h in range(3):
+                    assert dst.get(layer, kv, slot, h, 0) == ref.get(layer, kv, slot, h, 0)
+
+
+def pin_plane_locality(lib):
+    """[DistServe] 第三步: layer j of P goes only to layer j of D (plane p only to plane p)."""
+    P = 2 * 3
+    src = bf.make_pool("planes", 3, 1, 8, 10, lambda n: np.repeat(np.arange(P) + 1, n // P))
+    dst = bf.make_pool("planes", 3, 1, 8, 10, lambda n: np.zeros(n))
+    assert oracle.transfer(bf.to_oracle(src), [1, 5, 9], bf.to_oracle(dst), [0, 2, 4],
+                           lib=lib)[0] == oracle.OK
+    for p in range(P):
+        assert set(np.unique(dst.data[p])) <= {0, p + 1}
+        assert (dst.data[p, [0, 2, 4]] == p + 1).all()
+
+
+def pin_numpy_special_cases(lib):
+    """Per-plane token rows: the gather is numpy fancy indexing pool[:, slots].  HND pages:
+    it is transpose(1, 0, 2) of the page-table view [heads, seq, dim] ([mini-infer])."""
+    g = np.random.Generator(np.random.PCG64(17))
+    pool = bf.make_pool("planes", 3, 2, 8, 40, lambda n: g.integers(0, 0x7C00, n))
+    slots = g.choice(40, 13, replace=False)
+    rc, buf, _ = oracle.gather(bf.to_oracle(pool), slots, lib=lib)
+    assert np.array_equal(buf, _bytes_of(pool.data[:, slots]))
+    ps = 4
+    hp = bf.make_pool("hnd", 3, 2, 8, 12 * ps, lambda n: g.integers(0, 0x7C00, n), ps)
+    pt = g.choice(12, 3, replace=False)
+    seq = 2 * ps + 3
+    rc, buf = oracle.hnd_gather(bf.to_oracle(hp), pt, seq, lib=lib)
+    s = np.arange(seq)
+    planes = []
+    for p in range(6):
+        view = hp.data[p][pt[s // ps], :, s % ps, :]  # [seq, heads, dim] via fancy indexing
+        hsd = np.transpose(view, (1, 0, 2))           # the [heads, seq, dim] cache view
+        planes.append(np.transpose(hsd, (1, 0, 2)))   # permute(1, 0, 2)
+    assert np.array_equal(buf, _bytes_of(np.stack(planes)))
+
+
+def pin_validation(lib):
+    """Out-of-range slots (== num_slots, negative) fail with OUT_OF_RANGE and write nothing;
+    duplicate destinations fail only when checked."""
+    pool = bf.make_pool("planes", L, H, D, 8, _sentinel_fill)
+    keep = pool.data.copy()
+    buf = np.arange(L * 2 * 3 * H * D, dtype=np.uint16)
+    for bad in ([0, 8, 1], [0, -1, 1], [2147483647]):
+        rc, _ = oracle.scatter(bf.to_oracle(pool), bad, buf[: L * 2 * len(bad) * H * D], lib=lib)
+        assert rc == oracle.ERR_OUT_OF_RANGE
+        assert np.array_equal(pool.data, keep)
+    src = bf.make_pool("planes", L, H, D, 8, _arange_fill(0))
+    assert oracle.gather(bf.to_oracle(src), [7, 8], lib=lib)[0] == oracle.ERR_OUT_OF_RANGE
+    assert oracle.gather(bf.to_oracle(src), [7, 0], lib=lib)[0] == oracle.OK
+    rc, _ = oracle.transfer(bf.to_oracle(src), [1, 2], bf.to_oracle(pool), [3, 8], lib=lib)
+    assert rc == oracle.ERR_OUT_OF_RANGE and np.array_equal(pool.data, keep)
+    rc, _ = oracle.scatter(bf.to_oracle(pool), [1, 1], buf[: L * 2 * 2 * H * D], check_dup=True,
+                           lib=lib)
+    assert rc == oracle.ERR_DUPLICATE_DST and np.array_equal(pool.data, keep)
+    rc, _ = oracle.scatter(bf.to_oracle(pool), [1, 1], buf[: L * 2 * 2 * H * D], lib=lib)
+    assert rc == oracle.OK
+    hp = bf.make_pool("hnd", L, H, D, 8, _arange_fill(0), page_size=2)
+    assert oracle.hnd_gather(bf.to_oracle(hp), [3, 4], 3, lib=lib)[0] == oracle.ERR_OUT_OF_RANGE
+    assert oracle.hnd_gather(bf.to_oracle(hp), [3, 0], 3, lib=lib)[0] == oracle.OK
+
+
+def pin_batch(lib):
+    """[Mooncake] 6.1: a batch equals its requests applied one by one; a bad request reports
+    its own status and moves nothing, the others still run."""
+    g = np.random.Generator(np.random.PCG64(19))
+    src = bf.make_pool("planes", L, H, D, 30, lambda n: g.integers(0, 0x7C00, n))
+    dst0 = bf.make_pool("planes", L, H, D, 30, _sentinel_fill)
+    R = H * D * 2
+    P = 2 * L
+    ss = g.choice(30, 12, replace=False).astype(np.int32)
+    ds = g.choice(30, 12, replace=False).astype(np.int32)
+    ss_bad = ss.copy()
+    ss_bad[5] = 30  # request 1 (tokens 4..7 of the source list) goes out of range
+    buf0 = np.zeros(2 * P * 4 * R, dtype=np.uint8)
+    reqs = [(oracle.OP_TRANSFER, 4, 0, 0, 0), (oracle.OP_TRANSFER, 4, 4, 4, 0),
+            (oracle.OP_GATHER, 4, 8, 0, 0), (oracle.OP_SCATTER, 4, 0, 8, P * 4 * R)]
+    buf = buf0.copy()
+    buf[P * 4 * R:] = g.integers(0, 255, P * 4 * R, dtype=np.uint8)
+    dst = dst0.copy()
+    st = oracle.batch(bf.to_oracle(src), bf.to_oracle(dst), reqs, ss_bad, ds, buf, lib=lib)
+    assert list(st) == [oracle.ERR_OUT_OF_RANGE, 0, oracle.ERR_OUT_OF_RANGE, 0, 0]
+    # expected: apply the good requests one by one with the element model
+    exp = bf.transfer(src, ss[0:4], dst0, ds[0:4])
+    want_gather = _bytes_of(bf.gather(src, ss[8:12]))
+    assert np.array_equal(buf[: P * 4 * R], want_gather)
+    sc = buf[P * 4 * R:].view(np.uint16).reshape(L, 2, 4, H, D)
+    exp = bf.scatter(exp, ds[8:12], sc)
+    assert np.array_equal(dst.data, exp.data)
+    # bad records
+    st = oracle.batch(bf.to_oracle(src), bf.to_oracle(dst), [(7, 1, 0, 0, 0), (0, -1, 0, 0, 0),
+                      (0, 4, 10, 0, 0), (0, 4, 0, 0, 8)], ss, ds, buf, lib=lib)
+    assert list(st) == [1, 1, 1, 1, 1]
+
+
+def _expand(chunks):
+    src, dst = [], []
+    for _, s, d, rows in chunks:
+        src.extend(range(s, s + rows))
+        dst.extend(range(d, d + rows))
+    return src, dst
+
+
+def pin_plan(lib):
+    """[Mooncake] 7.6 coalescing.  Invariants: expanding the chunks gives back the index lists;
+    a fully contiguous list within one tile is one run; the number of runs is 1 + the number of
+    places where either list stops increasing by one (plus forced breaks); no chunk crosses a
+    tile boundary, a request start, or a page start of a paged side; chunks are <= chunk_rows."""
+    g = np.random.Generator(np.random.PCG64(23))
+    # contiguous: one run, split only by chunk_rows
+    n = 100
+    ch = oracle.plan(np.arange(5, 5 + n), np.arange(n), [0], 1, 1, 4096, 16, lib=lib)
+    assert len(ch) == (n + 15) // 16 and ch[:, 3].sum() == n
+    assert ch[0].tolist() == [0, 5, 0, 16]
+    ch = oracle.plan(np.arange(5, 5 + n), np.arange(n), [0], 1, 1, 4096, 1000, lib=lib)
+    assert len(ch) == 1
+    # random fragments with several requests, pages and tiles
+    for trial in range(30):
+        n = int(g.integers(1, 300))
+        def runs_of(hi):  # independent run structure for each side
+            r = []
+            while sum(r) < n:
+                r.append(int(g.integers(1, hi)))
+            return np.concatenate([np.arange(s, s + k) for s, k in
+                                   zip(g.integers(0, 1000, len(r)), r)])[:n]
+        src = runs_of(6) if trial % 3 else np.arange(40, 40 + n)
+        dst = runs_of(6) if trial % 3 != 1 else np.arange(n)
+        reqs = sorted(set([0] + list(g.integers(0, n, int(g.integers(0, 4))))))
+        sps, dps = int(g.choice([1, 4])), int(g.choice([1, 8]))
+        tile, rows_max = int(g.choice([7, 64, 4096])), int(g.choice([1, 3, 16]))
+        ch = oracle.plan(src, dst, reqs, sps, dps, tile, rows_max, lib=lib)
+        s2, d2 = _expand(ch)
+        assert s2 == src.tolist() and d2 == dst.tolist()
+        assert (ch[:, 3] >= 1).all() and (ch[:, 3] <= rows_max).all()
+        starts = np.concatenate([[0], np.cumsum(ch[:, 3])[:-1]])
+        for (q, s, d, rows), t0 in zip(ch, starts):
+            t1 = t0 + rows
+            assert t0 // tile == (t1 - 1) // tile
+            assert not any(t0 < r < t1 for r in reqs)
+            assert q == max(i for i, r in enumerate(reqs) if r <= t0)
+            if sps > 1:
+                assert not any((s + j) % sps == 0 for j in range(1, rows))
+            if dps > 1:
+                assert not any((d + j) % dps == 0 for j in range(1, rows))
+        # count of runs: a run boundary exists exactly at forced or natural breaks
+        brk = np.zeros(n, bool)
+        brk[0] = True
+        brk[1:] |= (src[1:] != src[:-1] + 1) | (dst[1:] != dst[:-1] + 1)
+        brk[np.arange(n) % tile == 0] = True
+        brk[reqs] = True
+        if sps > 1:
+            brk |= src % sps == 0
+        if dps > 1:
+            brk |= dst % dps == 0
+        run_len = np.diff(np.concatenate([np.flatnonzero(brk), [n]]))
+        assert len(ch) == int(((run_len + rows_max - 1) // rows_max).sum())
+
+
+ALL_PINS = [pin_sizes, pin_bytes_written, pin_bruteforce_gather, pin_bruteforce_scatter,
+            pin_bruteforce_transfer, pin_bruteforce_hnd, pin_roundtrip,
+            pin_transfer_is_scatter_of_gather, pin_hnd_roundtrip, pin_plane_locality,
+            pin_numpy_special_cases, pin_validation, pin_batch, pin_plan]

@@ -1,0 +1,87 @@
+"""Planted mistakes in the oracle must fail at least one pin.
+
+Each case copies kvx_oracle.c, plants one plausible mistake (a dropped term, a wrong index, a
+transposed operand, a skipped check), builds the copy with the host compiler and runs every
+pin against it.  The real oracle source is never modified.
+"""
+import json
+import os
+import shutil
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+import oracle
+from tests import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "kvx_oracle.c")
+HDR = os.path.join(os.path.dirname(oracle.__file__), "kvx_oracle.h")
+
+MUTANTS = {
+    "kv_swapped_in_buffer": ("(((int64_t)plane * n + token) * pool->kv_heads",
+                             "(((int64_t)(plane ^ 1) * n + token) * pool->kv_heads"),
+    "hnd_page_offset_off_by_one": ("* pool->page_size + off) * hb",
+                                   "* pool->page_size + (off + 1) % pool->page_size) * hb"),
+    "hnd_heads_and_offsets_transposed": ("((page * pool->kv_heads + head) * pool->page_size + off)",
+                                         "((page * pool->page_size + off) * pool->kv_heads + head)"),
+    "nhd_head_stride_dropped": ("return base + slot * pool->slot_stride + head * hb;",
+                                "return base + slot * pool->slot_stride;"),
+    "range_check_off_by_one": ("(int64_t)slots[i] >= pool->num_slots",
+                               "(int64_t)slots[i] > pool->num_slots"),
+    "negative_slot_accepted": ("slots[i] < 0 || (int64_t)slots[i] >= pool->num_slots",
+                               "(int64_t)slots[i] >= pool->num_slots"),
+    "permute_missing": ("memcpy(buf_vec(buf, src, p, seq_len, s, h), logical + ((int64_t)h * seq_len + s) * hb,",
+                        "memcpy(buf_vec(buf, src, p, seq_len, s, h), logical + ((int64_t)s * H + h) * hb,"),
+    "factor_two_dropped": ("return (int64_t)2 * num_layers", "return (int64_t)num_layers"),
+    "plan_dst_break_dropped": ("if (i > 0 && dst_idx[i] != dst_idx[i - 1] + 1) brk[i] = 1;", ""),
+    "plan_tile_break_dropped": ("if (i == 0 || i % tile_tokens == 0) brk[i] = 1;",
+                                "if (i == 0) brk[i] = 1;"),
+    "batch_status_not_per_request": ("status[1 + q] = rc;", "status[1 + q] = 0;"),
+    "transfer_src_dst_swapped": ("memcpy(head_vec(dst, p, dst_slots[i], h), head_vec(src, p, src_slots[i], h),",
+                                 "memcpy(head_vec(src, p, src_slots[i], h), head_vec(dst, p, dst_slots[i], h),"),
+}
+
+
+def _build_mutant(name, old, new, tmp):
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation anchor for {name} not unique/missing"
+    d = os.path.join(tmp, name)
+    os.makedirs(d)
+    shutil.copy(HDR, d)
+    src = os.path.join(d, "kvx_oracle.c")
+    open(src, "w").write(text.replace(old, new))
+    return oracle.build(src=src, out=os.path.join(d, "libmut.so"))
+
+
+_CHILD = r"""
+import json, sys
+sys.path.insert(0, sys.argv[2])
+import oracle
+from tests import pins
+lib = oracle.load(sys.argv[1])
+failed = []
+for pin in pins.ALL_PINS:
+    try:
+        pin(lib)
+    except AssertionError:
+        failed.append(pin.__name__)
+print(json.dumps(failed))
+"""
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name):
+    """A mutant may write out of bounds (that is the mistake), so its pins run in a child
+    process; the child dying of the corruption also counts as caught."""
+    old, new = MUTANTS[name]
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    with tempfile.TemporaryDirectory() as tmp:
+        path = _build_mutant(name, old, new, tmp)
+        res = subprocess.run([sys.executable, "-c", _CHILD, path, root], capture_output=True,
+                             text=True, timeout=600)
+        if res.returncode != 0:
+            return  # crashed on its own planted mistake
+        failed = json.loads(res.stdout.strip().splitlines()[-1])
+        assert failed, f"planted mistake {name} passed every pin"
