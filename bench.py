@@ -1,0 +1,398 @@
+#!/usr/bin/env python
+"""Benchmark of libkvx on its headline workload.
+
+Workload (a step = one pass of the whole hot path: index validation + run-length plan + copy):
+a 2048-token prompt, 36 layers x K/V x 8 kv heads x head_dim 128 bf16 (144 KiB/token, 288 MiB),
+moved pool-to-pool between two 65,536-slot token pools (72 per-plane tensors each, 9 GiB per
+pool) in one GB300's HBM; source and destination slot lists are 2048 distinct uniformly random
+slots each.  Inputs are resident in HBM before the timed region; L2 is flushed (a write of
+2x the L2 size) before every timed step, outside the step's CUDA events.
+
+Metric: GB/s moved = (payload read + payload written + index bytes) / device time per step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (single-threaded, as it stands) on a bounded sample of
+the same workload on the host cores.  Under torchrun (N > 1) every rank runs an independent
+replica on its own GPU (no data-path collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KV transfer GB/s (read+write) & µs/request at 288 MiB; % of GB300 HBM peak"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = ("2048-token prompt, 36 layers x K/V x 8 kv heads x 128 bf16 (144 KiB/token, "
+            "288 MiB), pool-to-pool transfer between two 65536-slot per-plane token pools, "
+            "2048 + 2048 distinct uniformly random slots")
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+L, H, D, SLOTS, N_TOK = 36, 8, 128, 65536, 2048
+R = H * D * 2
+P = 2 * L
+
+
+def alg_bytes(n_tokens: int) -> int:
+    """Payload read + payload written + the two int32 slot lists."""
+    return 2 * n_tokens * P * R + 2 * 4 * n_tokens
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def profile_traffic():
+    """Per-launch DRAM bytes of the copy kernel from the committed ncu summary, if that summary
+    was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "copy_kernel_cfg2.md")
+    src = os.path.join(ROOT, "disaggregated_paged_kv_gb300", "csrc", "kvx_copy.cu")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    if not m or not h:
+        return None
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != h.group(1):
+        return None
+    return int(m.group(1))
+
+
+class Clocks:
+    def __init__(self, device_index: int, enabled: bool):
+        self.proc = None
+        self.lines = []
+        if not enabled:
+            return
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(device_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in out.splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import numpy as np
+    import torch
+
+    from disaggregated_paged_kv_gb300 import kvx
+    from tests import inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    kvx.lib()
+    stream = torch.cuda.Stream(device=dev)
+    sptr = int(stream.cuda_stream)
+
+    # inputs resident in HBM: two 9 GiB pools of 72 per-plane [65536][8][128] bf16 tensors
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(inputs.seed(2, inputs.ROLE_VALUES) + rank)
+    src = torch.randn((P, SLOTS, H, D), dtype=torch.bfloat16, device=dev, generator=gen)
+    dst = torch.empty((P, SLOTS, H, D), dtype=torch.bfloat16, device=dev)
+    dst.view(torch.int16).fill_(0x7FC1)  # quiet-NaN sentinel
+    s_np = inputs.distinct_slots(inputs.rng(2, inputs.ROLE_SRC_SLOTS), N_TOK, SLOTS)
+    d_np = inputs.distinct_slots(inputs.rng(2, inputs.ROLE_DST_SLOTS), N_TOK, SLOTS)
+    s_dev = torch.from_numpy(s_np).to(dev)
+    d_dev = torch.from_numpy(d_np).to(dev)
+    src_l = kvx.Layout(L, H, D, kvx.BF16, SLOTS, base=src, plane_stride=SLOTS * R)
+    dst_l = kvx.Layout(L, H, D, kvx.BF16, SLOTS, base=dst, plane_stride=SLOTS * R)
+    ws = torch.empty(kvx.workspace_size(N_TOK, 0), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    def step():
+        kvx.transfer(src_l, s_dev, dst_l, d_dev, N_TOK, ws, st, stream=sptr)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            step()
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvx.OK
+    # the kernel did the work: sampled rows equal on the device
+    k = torch.from_numpy(np.arange(0, N_TOK, 97)).to(dev)
+    assert torch.equal(dst[:, d_dev[k]].view(torch.int16), src[:, s_dev[k]].view(torch.int16))
+
+    # ---- timed region: K steps, each bracketed by events on the launching stream ----
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = Clocks(local_rank, not args.no_clocks)
+    time.sleep(0.3 if clocks.proc else 0)
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+
+    # ---- the copy kernel alone (plan and copy launched separately, same flushes) ----
+    ev3 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            ev3[i][0].record(stream)
+            kvx.plan(kvx.OP_TRANSFER, src_l, s_dev, dst_l, d_dev, N_TOK, ws, st, stream=sptr)
+            ev3[i][1].record(stream)
+            kvx.execute(kvx.OP_TRANSFER, src_l, dst_l, None, 0, N_TOK, None, ws, st,
+                        buf_bytes=0, stream=sptr)
+            ev3[i][2].record(stream)
+    torch.cuda.synchronize()
+    plan_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in ev3)
+    copy_ms = statistics.mean(b.elapsed_time(c) for _, b, c in ev3)
+
+    # ---- end to end through the C ABI with host buffers (kvx_submit) ----
+    e2e = None
+    if not args.no_e2e:
+        hs = torch.from_numpy(s_np).pin_memory()
+        hd = torch.from_numpy(d_np).pin_memory()
+        hst = torch.full((1,), -1, dtype=torch.int32).pin_memory()
+        ws2 = torch.empty(kvx.workspace_size(N_TOK, 0), dtype=torch.uint8, device=dev)
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                flush.fill_(i & 0xFF)
+                ev2[i][0].record(stream)
+                kvx.submit(kvx.OP_TRANSFER, src_l, hs, dst_l, hd, N_TOK, None, ws2, hst,
+                           buf_bytes=0, stream=sptr)
+                ev2[i][1].record(stream)
+        torch.cuda.synchronize()
+        assert int(hst[0]) == kvx.OK
+        e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in ev2)
+        e2e = {"value": alg_bytes(N_TOK) / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+               "us_per_request": e2e_ms * 1e3,
+               "h2d_bytes_per_step": 2 * 4 * N_TOK, "d2h_bytes_per_step": 4,
+               "how": "kvx_submit: pinned host slot lists copied in, plan + copy, status "
+                      "copied out, all inside the step's CUDA events"}
+
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return dict(step_ms=step_ms, total_ms=total_ms, plan_ms=plan_ms, copy_ms=copy_ms, e2e=e2e,
+                clocks=clk, device=torch.cuda.get_device_name(dev))
+
+
+# ---------------------------------------------------------------------------------------
+# the oracle (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------------------
+
+class OracleTransfer:
+    """The single-threaded oracle on a transfer of n_tokens rows x 72 planes between two host
+    pools of pool_slots slots per plane (both first-touched before any timing)."""
+
+    def __init__(self, n_tokens: int, pool_slots: int):
+        import numpy as np
+
+        import oracle
+        from tests import inputs
+
+        g = inputs.rng(2, inputs.ROLE_VALUES)
+        nbytes = P * pool_slots * R
+        self.src = g.integers(0, 256, nbytes, dtype=np.uint8)
+        self.dst = np.zeros(nbytes, dtype=np.uint8)
+        self.sp = oracle.Pool(L, H, D, 2, oracle.TOKEN_ROWS, pool_slots,
+                              [(self.src, p * pool_slots * R) for p in range(P)], R)
+        self.dp = oracle.Pool(L, H, D, 2, oracle.TOKEN_ROWS, pool_slots,
+                              [(self.dst, p * pool_slots * R) for p in range(P)], R)
+        self.s = inputs.distinct_slots(inputs.rng(2, inputs.ROLE_SRC_SLOTS), n_tokens, pool_slots)
+        self.d = inputs.distinct_slots(inputs.rng(2, inputs.ROLE_DST_SLOTS), n_tokens, pool_slots)
+        self.lib = oracle.load()
+        self.oracle = oracle
+        self.pool_slots = pool_slots
+
+    def run(self, reps: int = 0, budget_s: float = 0.0, min_reps: int = 1):
+        """Runs reps transfers (or, with reps=0, at least min_reps and until budget_s).
+        Returns (seconds per transfer, transfers run)."""
+        n, t0 = 0, time.perf_counter()
+        while (n < reps) if reps else (n < min_reps or time.perf_counter() - t0 < budget_s):
+            rc, _ = self.oracle.transfer(self.sp, self.s, self.dp, self.d, lib=self.lib)
+            assert rc == self.oracle.OK
+            n += 1
+        return (time.perf_counter() - t0) / max(n, 1), n
+
+
+def cpu_baseline(budget_s: float = 10.0):
+    pool_slots = 8192
+    ob = OracleTransfer(N_TOK, pool_slots)
+    ob.run(reps=1)  # warm
+    sec, reps = ob.run(budget_s=budget_s, min_reps=3)
+    return {"value": alg_bytes(N_TOK) / sec / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "us_per_request": sec * 1e6,
+            "sample": f"the full 2048-token x 72-plane transfer (288 MiB each way), repeated "
+                      f"{reps} times in {sec * reps:.1f} s; host pools reduced to {pool_slots} "
+                      f"slots per plane (2 x {P * pool_slots * R / 2**30:.2f} GiB) with the same "
+                      f"random scattering; single thread"}
+
+
+def run_reference(args, rank: int):
+    """The reference arm: the oracle, as it stands, on the host cores.  Each step is a bounded
+    sample of the workload (512 of the 2048 tokens, all 72 planes)."""
+    if rank != 0:
+        return
+    n_sample, pool_slots = 512, 8192
+    ob = OracleTransfer(n_sample, pool_slots)
+    ob.run(reps=max(1, args.warmup))
+    sec, _ = ob.run(reps=args.steps)
+    value = alg_bytes(n_sample) / sec / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "kv_dtype": "bf16", "tokens": N_TOK, "planes": P,
+                       "row_bytes": R, "pool_slots": SLOTS, "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"each step: {n_sample} of the 2048 tokens x 72 planes "
+                                       f"({n_sample * P * R / 2**20:.0f} MiB each way) between host "
+                                       f"pools reduced to {pool_slots} slots per plane; single "
+                                       "thread"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    K = args.steps
+    ms_per_step = res["total_ms"] / K
+    value = world * alg_bytes(N_TOK) * K / (res["total_ms"] * 1e-3) / 1e9
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    copy_bytes = 2 * N_TOK * P * R
+    achieved = copy_bytes / (res["copy_ms"] * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "kv_dtype": "bf16", "tokens": N_TOK, "planes": P,
+                   "row_bytes": R, "pool_slots": SLOTS,
+                   "payload_bytes_each_way": N_TOK * P * R,
+                   "alg_bytes_per_step": alg_bytes(N_TOK),
+                   "us_per_request": ms_per_step * 1e3,
+                   "frac_of_measured_hbm": value / hbm,
+                   "frac_of_nominal_8tbs": value / NOMINAL_HBM_GBS,
+                   "plan_us": res["plan_ms"] * 1e3, "copy_us": res["copy_ms"] * 1e3,
+                   "l2": "flushed before every timed step (write of 2x L2, outside the events)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "device": res["device"]},
+        "clocks": res["clocks"],
+        "e2e": res["e2e"],
+        "gpu_launches": 2 * K,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": UNIT,
+                     "frac": achieved / hbm, "traffic": profile_traffic(),
+                     "kernel": "copy_kernel<true> (linear rows)",
+                     "peak_kind": f"{peak_kind} (burst copy)",
+                     "achieved_bytes_per_launch": copy_bytes},
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

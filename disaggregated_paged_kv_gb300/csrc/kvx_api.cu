@@ -1,0 +1,675 @@
+// kvx_api.cu -- libkvx's C ABI: layout handles, host-side validation, and the launches.
+//
+// Every entry point checks what the host can see (pointers, alignment, sizes, layout
+// agreement, overlapping memory, workspace size) and returns at once with nothing enqueued
+// if it fails; data-dependent checks happen in the planner and end up in the device status
+// word ("穷人版 PD 分离", section "最难的一个问题": the client learns of a failure right away
+// and no half-written KV is left behind).
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "kvx_internal.cuh"
+
+struct kvx_layout {
+  int32_t num_layers, kv_heads, head_dim, elem, kind, page_size;
+  int32_t planes;
+  int64_t num_slots;
+  int64_t row_bytes, seg_bytes;
+  int64_t slot_stride;  // NHD
+  int64_t page_bytes;   // HND
+  int64_t extent;       // bytes one plane spans from its start
+  uintptr_t lo, hi;     // envelope of all planes
+  uintptr_t plane[KVX_MAX_PLANES];
+};
+
+namespace {
+
+thread_local int32_t g_last_cuda = 0;
+
+kvx_status cuda_fail(cudaError_t e) {
+  g_last_cuda = (int32_t)e;
+  return KVX_ERR_CUDA;
+}
+
+int elem_bytes_of(int32_t dtype) {
+  switch (dtype) {
+    case KVX_F16:
+    case KVX_BF16:
+      return 2;
+    case KVX_F32:
+      return 4;
+    case KVX_FP8:
+      return 1;
+    default:
+      return 0;
+  }
+}
+
+bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+bool ranges_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) {
+  return a0 < b1 && b0 < a1;
+}
+
+bool layout_overlaps_range(const kvx_layout *l, uintptr_t b0, uintptr_t b1) {
+  if (!ranges_overlap(l->lo, l->hi, b0, b1)) return false;
+  for (int p = 0; p < l->planes; ++p)
+    if (ranges_overlap(l->plane[p], l->plane[p] + l->extent, b0, b1)) return true;
+  return false;
+}
+
+bool layouts_overlap(const kvx_layout *a, const kvx_layout *b) {
+  if (!ranges_overlap(a->lo, a->hi, b->lo, b->hi)) return false;
+  for (int p = 0; p < a->planes; ++p)
+    if (layout_overlaps_range(b, a->plane[p], a->plane[p] + a->extent)) return true;
+  return false;
+}
+
+bool same_rows(const kvx_layout *a, const kvx_layout *b) {
+  return a->num_layers == b->num_layers && a->kv_heads == b->kv_heads &&
+         a->head_dim == b->head_dim && a->elem == b->elem;
+}
+
+kvx::Side pool_side(const kvx_layout *l) {
+  kvx::Side s = {};
+  s.is_pool = 1;
+  s.hnd = l->kind == KVX_HND_PAGED ? 1 : 0;
+  s.page_size = s.hnd ? l->page_size : 1;
+  s.seg_bytes = (int32_t)l->seg_bytes;
+  s.num_slots = l->num_slots;
+  s.slot_stride = l->slot_stride;
+  s.page_bytes = l->page_bytes;
+  return s;
+}
+
+kvx::Side buffer_side(int64_t seg_bytes) {
+  kvx::Side s = {};
+  s.is_pool = 0;
+  s.hnd = 0;
+  s.page_size = 1;
+  s.seg_bytes = (int32_t)seg_bytes;
+  return s;
+}
+
+int32_t chunk_rows_for(int64_t row_bytes) {
+  int64_t m = kvx::kDefaultChunkBytes / row_bytes;
+  if (m < 1) m = 1;
+  if (m > kvx::kTile) m = kvx::kTile;
+  return (int32_t)m;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  int bps_linear = 0;   // resident copy CTAs per SM, linear-only variant
+  int bps_general = 0;  // resident copy CTAs per SM, general variant
+};
+
+kvx_status device_info(DeviceInfo *out) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return KVX_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev].sms == 0) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int bl = kvx::copy_blocks_per_sm(true, kvx::kMaxTiles);
+    const int bg = kvx::copy_blocks_per_sm(false, kvx::kMaxTiles);
+    if (bl <= 0 || bg <= 0) {
+      e = cudaGetLastError();
+      return cuda_fail(e != cudaSuccess ? e : cudaErrorUnknown);
+    }
+    cache[dev].sms = sms;
+    cache[dev].bps_linear = bl;
+    cache[dev].bps_general = bg;
+  }
+  *out = cache[dev];
+  return KVX_OK;
+}
+
+// What a plan or a copy is about: the two sides and the token space.
+struct Call {
+  int32_t mode = kvx::kModeSlots;
+  int32_t op = KVX_OP_GATHER;
+  const kvx_layout *src = nullptr, *dst = nullptr;  // pools (nullptr = buffer side)
+  const kvx_layout *shape = nullptr;                // the layout that fixes P and R
+  int64_t n_tokens = 0;
+  int32_t n_segs = 0;
+  int32_t n_status = 1;
+};
+
+// Checks the layouts an op needs and fills call.src / call.dst / call.shape.
+kvx_status bind_layouts(Call &c, kvx_layout_t src, kvx_layout_t dst) {
+  switch (c.op) {
+    case KVX_OP_GATHER:
+      if (!src) return KVX_ERR_INVALID_ARG;
+      c.src = src;
+      c.shape = src;
+      return KVX_OK;
+    case KVX_OP_SCATTER:
+      if (!dst) return KVX_ERR_INVALID_ARG;
+      c.dst = dst;
+      c.shape = dst;
+      return KVX_OK;
+    case KVX_OP_TRANSFER:
+    case KVX_OP_BATCH:
+      if (c.op == KVX_OP_TRANSFER && (!src || !dst)) return KVX_ERR_INVALID_ARG;
+      if (!src && !dst) return KVX_ERR_INVALID_ARG;
+      if (src && dst && !same_rows(src, dst)) return KVX_ERR_INVALID_ARG;
+      if (src && dst && layouts_overlap(src, dst)) return KVX_ERR_OVERLAP;
+      c.src = src;
+      c.dst = dst;
+      c.shape = src ? src : dst;
+      return KVX_OK;
+    default:
+      return KVX_ERR_INVALID_ARG;
+  }
+}
+
+kvx::Side src_side(const Call &c) {
+  if (c.mode == kvx::kModeBatch) {
+    if (c.src) return pool_side(c.src);
+    kvx::Side s = pool_side(c.shape);
+    s.num_slots = 0;
+    return s;
+  }
+  return c.src ? pool_side(c.src) : buffer_side(c.shape->seg_bytes);
+}
+
+kvx::Side dst_side(const Call &c) {
+  if (c.mode == kvx::kModeBatch) {
+    if (c.dst) return pool_side(c.dst);
+    kvx::Side s = pool_side(c.shape);
+    s.num_slots = 0;
+    return s;
+  }
+  return c.dst ? pool_side(c.dst) : buffer_side(c.shape->seg_bytes);
+}
+
+kvx_status check_ws(const void *d_ws, size_t ws_bytes, const kvx::WsLayout &L) {
+  if (!d_ws || !aligned(d_ws, 256)) return KVX_ERR_NO_WORKSPACE;
+  if ((int64_t)ws_bytes < L.total) return KVX_ERR_NO_WORKSPACE;
+  return KVX_OK;
+}
+
+kvx_status check_buffer(const Call &c, const void *d_buf, size_t buf_bytes) {
+  if (c.mode == kvx::kModeBatch) {
+    if (buf_bytes > 0 && (!d_buf || !aligned(d_buf, 16))) return KVX_ERR_ALIGNMENT;
+  } else if (c.op == KVX_OP_GATHER || c.op == KVX_OP_SCATTER) {
+    const int64_t need = (int64_t)c.shape->planes * c.n_tokens * c.shape->row_bytes;
+    if (!d_buf) return KVX_ERR_INVALID_ARG;
+    if (!aligned(d_buf, 16)) return KVX_ERR_ALIGNMENT;
+    if ((int64_t)buf_bytes < need) return KVX_ERR_INVALID_ARG;
+    buf_bytes = (size_t)need;
+  } else {
+    return KVX_OK;
+  }
+  if (buf_bytes == 0) return KVX_OK;
+  const uintptr_t b0 = (uintptr_t)d_buf, b1 = b0 + buf_bytes;
+  if (c.src && layout_overlaps_range(c.src, b0, b1)) return KVX_ERR_OVERLAP;
+  if (c.dst && layout_overlaps_range(c.dst, b0, b1)) return KVX_ERR_OVERLAP;
+  return KVX_OK;
+}
+
+kvx::PlanArgs plan_args(const Call &c, void *d_ws, int32_t *d_status) {
+  kvx::PlanArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.mode = c.mode;
+  a.op = c.op;
+  a.n_tokens = c.n_tokens;
+  a.n_segs = c.n_segs;
+  a.chunk_rows = chunk_rows_for(c.shape->row_bytes);
+  a.planes = c.shape->planes;
+  a.row_bytes = (int32_t)c.shape->row_bytes;
+  a.src = src_side(c);
+  a.dst = dst_side(c);
+  a.has_src = c.src != nullptr;
+  a.has_dst = c.dst != nullptr;
+  a.ws = static_cast<char *>(d_ws);
+  a.L = kvx::ws_layout(c.n_tokens, c.n_segs, false);
+  a.status = d_status;
+  return a;
+}
+
+kvx_status enqueue_plan(const Call &c, kvx::PlanArgs &a, cudaStream_t s) {
+  cudaError_t e;
+  if (c.n_tokens == 0) {
+    e = cudaMemsetAsync(a.status, 0, sizeof(int32_t) * (size_t)c.n_status, s);
+    return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+  }
+  if (c.mode == kvx::kModeSlots) {
+    if (kvx::num_tiles(c.n_tokens) == 1) {
+      a.status_direct = 1;
+    } else {
+      e = cudaMemsetAsync(a.status, 0, sizeof(int32_t), s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+  } else {
+    e = kvx::launch_prefix(a, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  e = kvx::launch_plan(a, s);
+  return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+}
+
+kvx_status enqueue_copy(const Call &c, const kvx_request *d_reqs, void *d_buf, const void *d_ws,
+                        int32_t *d_status, cudaStream_t s) {
+  if (c.n_tokens == 0) return KVX_OK;
+  DeviceInfo di;
+  kvx_status st = device_info(&di);
+  if (st != KVX_OK) return st;
+  static thread_local kvx::CopyArgs a;  // ~4 KiB of plane pointers: keep it off the stack
+  std::memset(&a, 0, sizeof(a));
+  a.mode = c.mode;
+  a.op = c.op;
+  a.n_tokens = c.n_tokens;
+  a.n_segs = c.n_segs;
+  a.chunk_rows = chunk_rows_for(c.shape->row_bytes);
+  a.planes = c.shape->planes;
+  a.row_bytes = (int32_t)c.shape->row_bytes;
+  a.seg_bytes = (int32_t)c.shape->seg_bytes;
+  a.heads = c.shape->kv_heads;
+  a.src = src_side(c);
+  a.dst = dst_side(c);
+  a.buf = static_cast<char *>(d_buf);
+  a.reqs = d_reqs;
+  a.ws = static_cast<const char *>(d_ws);
+  a.L = kvx::ws_layout(c.n_tokens, c.n_segs, false);
+  a.status = d_status;
+  for (int p = 0; p < c.shape->planes; ++p) {
+    a.src_planes[p] = c.src ? reinterpret_cast<const char *>(c.src->plane[p]) : nullptr;
+    a.dst_planes[p] = c.dst ? reinterpret_cast<char *>(c.dst->plane[p]) : nullptr;
+  }
+  const int64_t warps_needed = (int64_t)c.shape->planes * c.n_tokens;
+  const int64_t wpb = kvx::kCopyThreads / 32;
+  int64_t grid = (int64_t)di.sms * (kvx::copy_is_linear(a) ? di.bps_linear : di.bps_general);
+  const int64_t need = (warps_needed + wpb - 1) / wpb;
+  if (need < grid) grid = need;
+  if (grid < 1) grid = 1;
+  cudaError_t e = kvx::launch_copy(a, (int)grid, s);
+  return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+}
+
+bool valid_n(int64_t n) { return n >= 0 && n <= KVX_MAX_TOKENS; }
+
+}  // namespace
+
+extern "C" {
+
+kvx_status kvx_layout_create(const kvx_layout_desc *d, kvx_layout_t *out) {
+  if (!d || !out) return KVX_ERR_INVALID_ARG;
+  *out = nullptr;
+  const int eb = elem_bytes_of(d->dtype);
+  if (d->num_layers < 1 || 2 * (int64_t)d->num_layers > KVX_MAX_PLANES || d->kv_heads < 1 ||
+      d->head_dim < 1 || eb == 0 || d->num_slots < 1 || d->num_slots > INT32_MAX)
+    return KVX_ERR_INVALID_ARG;
+  if (d->kind != KVX_NHD && d->kind != KVX_HND_PAGED) return KVX_ERR_INVALID_ARG;
+  const int64_t seg = (int64_t)d->head_dim * eb;
+  const int64_t R = seg * d->kv_heads;
+  if (R > (int64_t)1 << 30) return KVX_ERR_INVALID_ARG;
+  if (R % 16 != 0) return KVX_ERR_ALIGNMENT;
+  kvx_layout *l = new (std::nothrow) kvx_layout;
+  if (!l) return KVX_ERR_INVALID_ARG;
+  std::memset(l, 0, sizeof(*l));
+  l->num_layers = d->num_layers;
+  l->kv_heads = d->kv_heads;
+  l->head_dim = d->head_dim;
+  l->elem = eb;
+  l->kind = d->kind;
+  l->planes = 2 * d->num_layers;
+  l->num_slots = d->num_slots;
+  l->row_bytes = R;
+  l->seg_bytes = seg;
+  kvx_status st = KVX_OK;
+  if (d->kind == KVX_HND_PAGED) {
+    if (d->page_size < 1 || d->num_slots % d->page_size != 0 || d->slot_stride != 0)
+      st = KVX_ERR_INVALID_ARG;
+    else if (seg % 16 != 0)
+      st = KVX_ERR_ALIGNMENT;
+    l->page_size = d->page_size;
+    l->page_bytes = R * d->page_size;
+    l->extent = l->page_bytes * (d->num_slots / (d->page_size > 0 ? d->page_size : 1));
+  } else {
+    l->page_size = 1;
+    l->slot_stride = d->slot_stride == 0 ? R : d->slot_stride;
+    if (l->slot_stride < R) st = KVX_ERR_INVALID_ARG;
+    else if (l->slot_stride % 16 != 0) st = KVX_ERR_ALIGNMENT;
+    else if (l->slot_stride > ((int64_t)1 << 62) / d->num_slots) st = KVX_ERR_INVALID_ARG;
+    l->extent = (d->num_slots - 1) * l->slot_stride + R;
+  }
+  if (st == KVX_OK) {
+    l->lo = UINTPTR_MAX;
+    l->hi = 0;
+    for (int p = 0; p < l->planes; ++p) {
+      uintptr_t a;
+      if (d->plane_ptrs) {
+        a = (uintptr_t)d->plane_ptrs[p];
+      } else {
+        if (!d->base) { st = KVX_ERR_INVALID_ARG; break; }
+        a = (uintptr_t)d->base + (uintptr_t)(d->plane_stride * p);
+      }
+      if (a == 0) { st = KVX_ERR_INVALID_ARG; break; }
+      if (a % 16 != 0) { st = KVX_ERR_ALIGNMENT; break; }
+      l->plane[p] = a;
+      if (a < l->lo) l->lo = a;
+      if (a + l->extent > l->hi) l->hi = a + l->extent;
+    }
+  }
+  if (st != KVX_OK) {
+    delete l;
+    return st;
+  }
+  *out = l;
+  return KVX_OK;
+}
+
+kvx_status kvx_layout_destroy(kvx_layout_t layout) {
+  delete layout;
+  return KVX_OK;
+}
+
+int64_t kvx_layout_row_bytes(kvx_layout_t l) { return l ? l->row_bytes : -1; }
+
+int32_t kvx_layout_num_planes(kvx_layout_t l) { return l ? l->planes : -1; }
+
+size_t kvx_workspace_size(int64_t max_tokens, int32_t max_requests) {
+  if (!valid_n(max_tokens) || max_requests < 0 || max_requests > kvx::kMaxSegs) return 0;
+  return (size_t)kvx::ws_layout(max_tokens, max_requests, true).total;
+}
+
+kvx_status kvx_plan(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, kvx_layout_t dst,
+                    const int32_t *d_dst_slots, int32_t n, void *d_ws, size_t ws_bytes,
+                    int32_t *d_status, kvx_stream_t stream) {
+  if (op < KVX_OP_GATHER || op > KVX_OP_TRANSFER || !valid_n(n)) return KVX_ERR_INVALID_ARG;
+  if (!d_status || !aligned(d_status, 4)) return KVX_ERR_INVALID_ARG;
+  Call c;
+  c.mode = kvx::kModeSlots;
+  c.op = op;
+  c.n_tokens = n;
+  kvx_status st = bind_layouts(c, src, dst);
+  if (st != KVX_OK) return st;
+  if (n > 0) {
+    if (c.src && (!d_src_slots || !aligned(d_src_slots, 4))) return KVX_ERR_INVALID_ARG;
+    if (c.dst && (!d_dst_slots || !aligned(d_dst_slots, 4))) return KVX_ERR_INVALID_ARG;
+  }
+  const kvx::WsLayout L = kvx::ws_layout(n, 0, false);
+  if (n > 0 && (st = check_ws(d_ws, ws_bytes, L)) != KVX_OK) return st;
+  kvx::PlanArgs a = plan_args(c, d_ws, d_status);
+  a.src_idx = d_src_slots;
+  a.dst_idx = d_dst_slots;
+  return enqueue_plan(c, a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kvx_status kvx_plan_runs(int32_t op, kvx_layout_t src, kvx_layout_t dst, const int32_t *d_runs,
+                         int32_t n_runs, int32_t n_tokens, void *d_ws, size_t ws_bytes,
+                         int32_t *d_status, kvx_stream_t stream) {
+  if (op < KVX_OP_GATHER || op > KVX_OP_TRANSFER || !valid_n(n_tokens) || n_runs < 0 ||
+      n_runs > kvx::kMaxSegs)
+    return KVX_ERR_INVALID_ARG;
+  if (!d_status || !aligned(d_status, 4)) return KVX_ERR_INVALID_ARG;
+  if (n_runs > 0 && (!d_runs || !aligned(d_runs, 4))) return KVX_ERR_INVALID_ARG;
+  Call c;
+  c.mode = kvx::kModeRuns;
+  c.op = op;
+  c.n_tokens = n_tokens;
+  c.n_segs = n_runs;
+  kvx_status st = bind_layouts(c, src, dst);
+  if (st != KVX_OK) return st;
+  if (n_runs == 0 && n_tokens > 0) return KVX_ERR_INVALID_ARG;
+  const kvx::WsLayout L = kvx::ws_layout(n_tokens, n_runs, false);
+  if ((n_tokens > 0 || n_runs > 0) && (st = check_ws(d_ws, ws_bytes, L)) != KVX_OK) return st;
+  kvx::PlanArgs a = plan_args(c, d_ws, d_status);
+  a.runs = d_runs;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (n_tokens == 0 && n_runs > 0) {
+    // nothing to move, but the runs must still add up to zero
+    cudaError_t e = kvx::launch_prefix(a, s);
+    return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+  }
+  return enqueue_plan(c, a, s);
+}
+
+kvx_status kvx_plan_batch(kvx_layout_t src, kvx_layout_t dst, const kvx_request *d_reqs,
+                          int32_t n_reqs, int64_t total_tokens, const int32_t *d_src_slots,
+                          int64_t n_src_slots, const int32_t *d_dst_slots, int64_t n_dst_slots,
+                          size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *d_status,
+                          kvx_stream_t stream) {
+  if (!valid_n(total_tokens) || n_reqs < 0 || n_reqs > kvx::kMaxSegs || n_src_slots < 0 ||
+      n_dst_slots < 0)
+    return KVX_ERR_INVALID_ARG;
+  if (!d_status || !aligned(d_status, 4)) return KVX_ERR_INVALID_ARG;
+  if (n_reqs > 0 && (!d_reqs || !aligned(d_reqs, 8))) return KVX_ERR_INVALID_ARG;
+  if (n_src_slots > 0 && (!d_src_slots || !aligned(d_src_slots, 4))) return KVX_ERR_INVALID_ARG;
+  if (n_dst_slots > 0 && (!d_dst_slots || !aligned(d_dst_slots, 4))) return KVX_ERR_INVALID_ARG;
+  Call c;
+  c.mode = kvx::kModeBatch;
+  c.op = KVX_OP_BATCH;
+  c.n_tokens = total_tokens;
+  c.n_segs = n_reqs;
+  c.n_status = n_reqs + 1;
+  kvx_status st = bind_layouts(c, src, dst);
+  if (st != KVX_OK) return st;
+  const kvx::WsLayout L = kvx::ws_layout(total_tokens, n_reqs, false);
+  if (n_reqs > 0 && (st = check_ws(d_ws, ws_bytes, L)) != KVX_OK) return st;
+  kvx::PlanArgs a = plan_args(c, d_ws, d_status);
+  a.src_idx = d_src_slots;
+  a.dst_idx = d_dst_slots;
+  a.n_src_idx = n_src_slots;
+  a.n_dst_idx = n_dst_slots;
+  a.reqs = d_reqs;
+  a.buf_bytes = (int64_t)buf_bytes;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (n_reqs == 0) {
+    if (total_tokens != 0) return KVX_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemsetAsync(d_status, 0, sizeof(int32_t), s);
+    return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+  }
+  cudaError_t e = kvx::launch_prefix(a, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (total_tokens == 0) return KVX_OK;
+  e = kvx::launch_plan(a, s);
+  return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+}
+
+kvx_status kvx_execute(int32_t op, kvx_layout_t src, kvx_layout_t dst, const kvx_request *d_reqs,
+                       int32_t n_reqs, int64_t n_tokens, void *d_buf, size_t buf_bytes,
+                       const void *d_ws, size_t ws_bytes, int32_t *d_status,
+                       kvx_stream_t stream) {
+  if (op < KVX_OP_GATHER || op > KVX_OP_BATCH || !valid_n(n_tokens)) return KVX_ERR_INVALID_ARG;
+  if (!d_status || !aligned(d_status, 4)) return KVX_ERR_INVALID_ARG;
+  Call c;
+  c.op = op;
+  c.mode = op == KVX_OP_BATCH ? kvx::kModeBatch : kvx::kModeSlots;
+  c.n_tokens = n_tokens;
+  if (op == KVX_OP_BATCH) {
+    if (n_reqs < 0 || n_reqs > kvx::kMaxSegs || (n_reqs > 0 && !d_reqs)) return KVX_ERR_INVALID_ARG;
+    c.n_segs = n_reqs;
+  }
+  kvx_status st = bind_layouts(c, src, dst);
+  if (st != KVX_OK) return st;
+  if ((st = check_buffer(c, d_buf, buf_bytes)) != KVX_OK) return st;
+  if (n_tokens == 0) return KVX_OK;
+  if ((st = check_ws(d_ws, ws_bytes, kvx::ws_layout(n_tokens, c.n_segs, false))) != KVX_OK)
+    return st;
+  return enqueue_copy(c, d_reqs, d_buf, d_ws, d_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kvx_status kvx_gather(kvx_layout_t src, const int32_t *d_src_slots, int32_t n, void *d_buf,
+                      size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *d_status,
+                      kvx_stream_t stream) {
+  Call c;
+  c.op = KVX_OP_GATHER;
+  c.n_tokens = n;
+  kvx_status st = bind_layouts(c, src, nullptr);
+  if (st == KVX_OK && valid_n(n)) st = check_buffer(c, d_buf, buf_bytes);
+  if (st != KVX_OK) return st;
+  st = kvx_plan(KVX_OP_GATHER, src, d_src_slots, nullptr, nullptr, n, d_ws, ws_bytes, d_status,
+                stream);
+  if (st != KVX_OK) return st;
+  return kvx_execute(KVX_OP_GATHER, src, nullptr, nullptr, 0, n, d_buf, buf_bytes, d_ws,
+                     ws_bytes, d_status, stream);
+}
+
+kvx_status kvx_scatter(kvx_layout_t dst, const int32_t *d_dst_slots, int32_t n,
+                       const void *d_buf, size_t buf_bytes, void *d_ws, size_t ws_bytes,
+                       int32_t *d_status, kvx_stream_t stream) {
+  Call c;
+  c.op = KVX_OP_SCATTER;
+  c.n_tokens = n;
+  kvx_status st = bind_layouts(c, nullptr, dst);
+  if (st == KVX_OK && valid_n(n)) st = check_buffer(c, d_buf, buf_bytes);
+  if (st != KVX_OK) return st;
+  st = kvx_plan(KVX_OP_SCATTER, nullptr, nullptr, dst, d_dst_slots, n, d_ws, ws_bytes, d_status,
+                stream);
+  if (st != KVX_OK) return st;
+  return kvx_execute(KVX_OP_SCATTER, nullptr, dst, nullptr, 0, n, const_cast<void *>(d_buf),
+                     buf_bytes, d_ws, ws_bytes, d_status, stream);
+}
+
+kvx_status kvx_transfer(kvx_layout_t src, const int32_t *d_src_slots, kvx_layout_t dst,
+                        const int32_t *d_dst_slots, int32_t n, void *d_ws, size_t ws_bytes,
+                        int32_t *d_status, kvx_stream_t stream) {
+  kvx_status st = kvx_plan(KVX_OP_TRANSFER, src, d_src_slots, dst, d_dst_slots, n, d_ws,
+                           ws_bytes, d_status, stream);
+  if (st != KVX_OK) return st;
+  return kvx_execute(KVX_OP_TRANSFER, src, dst, nullptr, 0, n, nullptr, 0, d_ws, ws_bytes,
+                     d_status, stream);
+}
+
+kvx_status kvx_gather_runs(kvx_layout_t src, const int32_t *d_runs, int32_t n_runs,
+                           int32_t n_tokens, void *d_buf, size_t buf_bytes, void *d_ws,
+                           size_t ws_bytes, int32_t *d_status, kvx_stream_t stream) {
+  Call c;
+  c.op = KVX_OP_GATHER;
+  c.n_tokens = n_tokens;
+  kvx_status st = bind_layouts(c, src, nullptr);
+  if (st == KVX_OK && valid_n(n_tokens)) st = check_buffer(c, d_buf, buf_bytes);
+  if (st != KVX_OK) return st;
+  st = kvx_plan_runs(KVX_OP_GATHER, src, nullptr, d_runs, n_runs, n_tokens, d_ws, ws_bytes,
+                     d_status, stream);
+  if (st != KVX_OK) return st;
+  return kvx_execute(KVX_OP_GATHER, src, nullptr, nullptr, 0, n_tokens, d_buf, buf_bytes, d_ws,
+                     ws_bytes, d_status, stream);
+}
+
+kvx_status kvx_scatter_runs(kvx_layout_t dst, const int32_t *d_runs, int32_t n_runs,
+                            int32_t n_tokens, const void *d_buf, size_t buf_bytes, void *d_ws,
+                            size_t ws_bytes, int32_t *d_status, kvx_stream_t stream) {
+  Call c;
+  c.op = KVX_OP_SCATTER;
+  c.n_tokens = n_tokens;
+  kvx_status st = bind_layouts(c, nullptr, dst);
+  if (st == KVX_OK && valid_n(n_tokens)) st = check_buffer(c, d_buf, buf_bytes);
+  if (st != KVX_OK) return st;
+  st = kvx_plan_runs(KVX_OP_SCATTER, nullptr, dst, d_runs, n_runs, n_tokens, d_ws, ws_bytes,
+                     d_status, stream);
+  if (st != KVX_OK) return st;
+  return kvx_execute(KVX_OP_SCATTER, nullptr, dst, nullptr, 0, n_tokens,
+                     const_cast<void *>(d_buf), buf_bytes, d_ws, ws_bytes, d_status, stream);
+}
+
+kvx_status kvx_transfer_runs(kvx_layout_t src, kvx_layout_t dst, const int32_t *d_runs,
+                             int32_t n_runs, int32_t n_tokens, void *d_ws, size_t ws_bytes,
+                             int32_t *d_status, kvx_stream_t stream) {
+  kvx_status st = kvx_plan_runs(KVX_OP_TRANSFER, src, dst, d_runs, n_runs, n_tokens, d_ws,
+                                ws_bytes, d_status, stream);
+  if (st != KVX_OK) return st;
+  return kvx_execute(KVX_OP_TRANSFER, src, dst, nullptr, 0, n_tokens, nullptr, 0, d_ws, ws_bytes,
+                     d_status, stream);
+}
+
+kvx_status kvx_batch(kvx_layout_t src, kvx_layout_t dst, const kvx_request *d_reqs,
+                     int32_t n_reqs, int64_t total_tokens, const int32_t *d_src_slots,
+                     int64_t n_src_slots, const int32_t *d_dst_slots, int64_t n_dst_slots,
+                     void *d_buf, size_t buf_bytes, void *d_ws, size_t ws_bytes,
+                     int32_t *d_status, kvx_stream_t stream) {
+  Call c;
+  c.op = KVX_OP_BATCH;
+  c.mode = kvx::kModeBatch;
+  kvx_status st = bind_layouts(c, src, dst);
+  if (st == KVX_OK) st = check_buffer(c, d_buf, buf_bytes);
+  if (st != KVX_OK) return st;
+  st = kvx_plan_batch(src, dst, d_reqs, n_reqs, total_tokens, d_src_slots, n_src_slots,
+                      d_dst_slots, n_dst_slots, buf_bytes, d_ws, ws_bytes, d_status, stream);
+  if (st != KVX_OK) return st;
+  return kvx_execute(KVX_OP_BATCH, src, dst, d_reqs, n_reqs, total_tokens, d_buf, buf_bytes,
+                     d_ws, ws_bytes, d_status, stream);
+}
+
+kvx_status kvx_submit(int32_t op, kvx_layout_t src, const int32_t *h_src_slots,
+                      kvx_layout_t dst, const int32_t *h_dst_slots, int32_t n, void *d_buf,
+                      size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *h_status,
+                      kvx_stream_t stream) {
+  if (op < KVX_OP_GATHER || op > KVX_OP_TRANSFER || !valid_n(n) || !h_status)
+    return KVX_ERR_INVALID_ARG;
+  Call c;
+  c.op = op;
+  c.n_tokens = n;
+  kvx_status st = bind_layouts(c, src, dst);
+  if (st != KVX_OK) return st;
+  if ((st = check_buffer(c, d_buf, buf_bytes)) != KVX_OK) return st;
+  if (n > 0 && ((c.src && !h_src_slots) || (c.dst && !h_dst_slots))) return KVX_ERR_INVALID_ARG;
+  const kvx::WsLayout L = kvx::ws_layout(n, 0, true);
+  if ((st = check_ws(d_ws, ws_bytes, L)) != KVX_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char *stage = static_cast<char *>(d_ws) + L.stage_off;
+  int32_t *d_src = reinterpret_cast<int32_t *>(stage);
+  int32_t *d_dst = d_src + n;
+  int32_t *d_st = reinterpret_cast<int32_t *>(stage + kvx::align_up(8 * (int64_t)n, 16));
+  cudaError_t e;
+  if (n > 0 && c.src) {
+    e = cudaMemcpyAsync(d_src, h_src_slots, sizeof(int32_t) * (size_t)n, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (n > 0 && c.dst) {
+    e = cudaMemcpyAsync(d_dst, h_dst_slots, sizeof(int32_t) * (size_t)n, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  st = kvx_plan(op, src, c.src ? d_src : nullptr, dst, c.dst ? d_dst : nullptr, n, d_ws,
+                ws_bytes, d_st, stream);
+  if (st != KVX_OK) return st;
+  st = kvx_execute(op, src, dst, nullptr, 0, n, d_buf, buf_bytes, d_ws, ws_bytes, d_st, stream);
+  if (st != KVX_OK) return st;
+  e = cudaMemcpyAsync(h_status, d_st, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+}
+
+kvx_status kvx_plan_export(const void *d_ws, size_t ws_bytes, int64_t n_tokens,
+                           int32_t *d_chunks, int64_t max_chunks, int64_t *d_count,
+                           kvx_stream_t stream) {
+  if (!valid_n(n_tokens) || max_chunks < 0 || !d_count) return KVX_ERR_INVALID_ARG;
+  if (max_chunks > 0 && (!d_chunks || !aligned(d_chunks, 4))) return KVX_ERR_INVALID_ARG;
+  const kvx::WsLayout L = kvx::ws_layout(n_tokens, 0, false);
+  // the export reads only the header, tile and chunk sections, which do not depend on n_segs
+  if (!d_ws || !aligned(d_ws, 256) || (int64_t)ws_bytes < L.prefix_off) return KVX_ERR_NO_WORKSPACE;
+  cudaError_t e = kvx::launch_export(static_cast<const char *>(d_ws), L, n_tokens, d_chunks,
+                                     max_chunks, d_count, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+}
+
+const char *kvx_status_str(kvx_status s) {
+  switch (s) {
+    case KVX_OK: return "ok";
+    case KVX_ERR_INVALID_ARG: return "invalid argument";
+    case KVX_ERR_ALIGNMENT: return "misaligned pointer or row size";
+    case KVX_ERR_OUT_OF_RANGE: return "index out of range";
+    case KVX_ERR_DUPLICATE_DST: return "duplicate destination";
+    case KVX_ERR_OVERLAP: return "source and destination memory overlap";
+    case KVX_ERR_CUDA: return "CUDA error";
+    case KVX_ERR_NO_WORKSPACE: return "workspace too small or misaligned";
+    case KVX_ERR_TIMEOUT: return "timeout";
+    case KVX_ERR_CANCELLED: return "cancelled";
+    default: return "unknown status";
+  }
+}
+
+int32_t kvx_last_cuda_error(void) { return g_last_cuda; }
+
+int32_t kvx_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,160 @@
+// kvx_internal.cuh -- structures shared by libkvx's host code and its sm_103a kernels.
+//
+// The hot path is two kernels on the caller's stream:
+//   planner  one CTA per tile of KVX_PLAN_TILE consecutive tokens: checks every index, marks
+//            where a run of consecutive source and destination rows breaks, compacts the runs
+//            with block-wide prefix sums and cuts them into chunks of at most chunk_rows rows
+//            ("Mooncake" survey 7.6: contiguous blocks merged into fewer descriptors).  The
+//            chunk table of each tile goes into the workspace.
+//   copy     a persistent grid of warps; work item w is (chunk w / P, plane w % P).  A warp
+//            moves the chunk's rows for one plane with 16-byte vector loads and stores
+//            ("DistServe" 第三步: plane p only ever goes to plane p).
+// Runs and batches add a one-CTA prefix kernel in front of the planner that turns run lengths
+// or request token counts into token offsets.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kvx.h"
+
+namespace kvx {
+
+constexpr int kTile = KVX_PLAN_TILE;           // tokens per planner CTA
+constexpr int kPlanThreads = 512;
+constexpr int kPlanItems = kTile / kPlanThreads;  // consecutive tokens per planner thread
+constexpr int kMaxTiles = KVX_MAX_TOKENS / KVX_PLAN_TILE;
+constexpr int kCopyThreads = 256;
+constexpr int kPrefixThreads = 1024;
+constexpr int kPrefixItems = 4;
+constexpr int kMaxSegs = 1 << 24;              // most runs / requests per call
+constexpr uint32_t kPlanMagic = 0x4B565831u;   // "KVX1"
+constexpr int kDefaultChunkBytes = KVX_CHUNK_BYTES;  // target bytes per chunk (per plane)
+
+static_assert(kTile % kPlanThreads == 0, "tile must split evenly over planner threads");
+static_assert(kPlanItems * kPlanThreads == kTile, "one planner item per token");
+
+enum Mode : int32_t { kModeSlots = 0, kModeRuns = 1, kModeBatch = 2 };
+
+// Geometry of one side of a move.
+struct Side {
+  int32_t is_pool;     // 1: a pool (index = slot); 0: a transfer buffer (index = row)
+  int32_t hnd;         // 1: HND pages; runs break at every page start
+  int32_t page_size;   // HND tokens per page (1 otherwise)
+  int32_t seg_bytes;   // bytes of one head vector (head_dim * elem)
+  int64_t num_slots;   // pool: valid slots [0, num_slots)
+  int64_t slot_stride; // NHD pool: bytes from slot s to s+1
+  int64_t page_bytes;  // HND pool: bytes of one page of one plane (= H * page_size * seg)
+};
+
+// One chunk of the plan: rows consecutive rows starting at (src, dst) of request req.
+struct __align__(16) Chunk {
+  int32_t req;
+  int32_t src;
+  int32_t dst;
+  int32_t rows;
+};
+
+// Byte offsets of the workspace sections; a pure function of the call's sizes, so the host
+// and every kernel agree on it.
+struct WsLayout {
+  int64_t header_off;  // PlanHeader
+  int64_t tiles_off;   // int32[n_tiles]: chunks per tile
+  int64_t chunks_off;  // Chunk[n_tiles][kTile]
+  int64_t prefix_off;  // int64[n_segs + 1]: token offset of each run / request
+  int64_t stage_off;   // kvx_submit: int32 src[n], int32 dst[n], int32 status
+  int64_t total;       // bytes required
+};
+
+__host__ __device__ inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline int64_t num_tiles(int64_t n_tokens) {
+  return (n_tokens + kTile - 1) / kTile;
+}
+
+__host__ __device__ inline WsLayout ws_layout(int64_t n_tokens, int64_t n_segs, bool staging) {
+  WsLayout L;
+  int64_t tiles = num_tiles(n_tokens);
+  L.header_off = 0;
+  L.tiles_off = 256;
+  L.chunks_off = align_up(L.tiles_off + 4 * (tiles > 0 ? tiles : 1), 256);
+  L.prefix_off = align_up(L.chunks_off + (int64_t)sizeof(Chunk) * kTile * tiles, 256);
+  L.stage_off = align_up(L.prefix_off + 8 * (n_segs + 1), 256);
+  L.total = staging ? align_up(L.stage_off + 8 * n_tokens + 16, 256) : L.stage_off;
+  return L;
+}
+
+// Written by the planner (or the prefix kernel) into the workspace; the copy kernel compares
+// it with its own arguments before it moves anything.
+struct PlanHeader {
+  uint32_t magic;
+  int32_t mode;
+  int32_t op;
+  int32_t n_segs;
+  int64_t n_tokens;
+  int32_t chunk_rows;
+  int32_t planes;
+  int32_t row_bytes;
+  int32_t src_is_pool, src_hnd, src_page_size;
+  int32_t dst_is_pool, dst_hnd, dst_page_size;
+  int32_t pad;
+  int64_t src_num_slots;
+  int64_t dst_num_slots;
+};
+
+struct PlanArgs {
+  int32_t mode;
+  int32_t op;          // slots / runs modes
+  int64_t n_tokens;    // size of the planned token space
+  int32_t n_segs;      // runs: n_runs; batch: n_reqs
+  int32_t chunk_rows;
+  int32_t planes;
+  int32_t row_bytes;
+  const int32_t *src_idx;  // slots / batch: source slot list
+  const int32_t *dst_idx;  // slots / batch: destination slot list
+  int64_t n_src_idx;       // batch: elements in src_idx
+  int64_t n_dst_idx;       // batch: elements in dst_idx
+  const int32_t *runs;     // runs: [n_segs][3]
+  const kvx_request *reqs; // batch
+  int64_t buf_bytes;       // batch: capacity of the buffer for request checks
+  int32_t has_src, has_dst;
+  int32_t status_direct;   // slots mode with a single tile: the CTA stores status[0] itself
+  int32_t pad;
+  Side src, dst;           // batch: pool geometry of the two layouts (is_pool = 1)
+  char *ws;
+  WsLayout L;
+  int32_t *status;
+};
+
+struct CopyArgs {
+  int32_t mode;
+  int32_t op;
+  int64_t n_tokens;
+  int32_t n_segs;
+  int32_t chunk_rows;
+  int32_t planes;
+  int32_t row_bytes;
+  int32_t seg_bytes;
+  int32_t heads;
+  Side src, dst;           // single modes: the two sides; batch: the two pools
+  char *buf;               // single modes: the transfer buffer
+  const kvx_request *reqs; // batch
+  const char *ws;
+  WsLayout L;
+  int32_t *status;
+  const char *src_planes[KVX_MAX_PLANES];
+  char *dst_planes[KVX_MAX_PLANES];
+};
+
+// Launchers (enqueue only; return the launch's cudaError_t).
+cudaError_t launch_prefix(const PlanArgs &a, cudaStream_t s);
+cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
+cudaError_t launch_copy(const CopyArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_export(const char *ws, WsLayout L, int64_t n_tokens, int32_t *out,
+                          int64_t max_chunks, int64_t *count, cudaStream_t s);
+// Blocks per SM at which the copy kernel (linear-only or general variant) is resident on the
+// current device, and which variant a call runs.
+int copy_blocks_per_sm(bool linear, int n_tiles);
+bool copy_is_linear(const CopyArgs &a);
+
+}  // namespace kvx

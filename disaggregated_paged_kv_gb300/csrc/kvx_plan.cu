@@ -1,0 +1,419 @@
+// kvx_plan.cu -- index validation and run-length planning on the device (sm_103a).
+//
+// "PD分离调研" (Mooncake survey) 7.6: the sender merges contiguous blocks into fewer transfer
+// descriptors.  "穷人版 PD 分离", section "5090：一个看得见所有卡的代理": the cost of a KV move
+// is set by the number of fragments (72 blocks on a fresh pool, 105,660 once it fragments),
+// so fragments are found and merged on the GPU, next to the data, without a host round trip.
+//
+// Planner CTA (one per tile of kTile tokens), three phases, all in shared memory:
+//   1. each thread takes kPlanItems consecutive tokens, fetches their source and destination
+//      index, range-checks it and sets brk = "a new run starts here";
+//   2. a block-wide exclusive scan of brk numbers the runs; each run start records its token
+//      offset and first indices; run r's length is start[r+1] - start[r];
+//   3. a second scan of ceil(len / chunk_rows) gives each run's first chunk; every chunk is
+//      then written with one binary search over those chunk offsets.
+#include "kvx_internal.cuh"
+
+namespace kvx {
+namespace {
+
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Exclusive scan of one value per thread across the block; *total gets the block sum.
+// s_warp must hold THREADS / 32 elements.  Ends with a barrier, so s_warp is reusable.
+template <int THREADS, typename T>
+__device__ __forceinline__ T block_exclusive_scan(T v, T *total, T *s_warp) {
+  constexpr int kWarps = THREADS / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  T x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    T y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    T w = lane < kWarps ? s_warp[lane] : T(0);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      T y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kWarps) s_warp[lane] = w;
+  }
+  __syncthreads();
+  T res = (warp > 0 ? s_warp[warp - 1] : T(0)) + x - v;
+  *total = s_warp[kWarps - 1];
+  __syncthreads();
+  return res;
+}
+
+template <int THREADS>
+__device__ __forceinline__ int32_t block_max(int32_t v, int32_t *s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = __reduce_max_sync(0xffffffffu, v);
+  if (lane == 0) s_warp[warp] = v;
+  __syncthreads();
+  int32_t r = 0;
+  for (int i = 0; i < THREADS / 32; ++i) r = max(r, s_warp[i]);
+  __syncthreads();
+  return r;
+}
+
+// Largest q in [0, n) with pre[q] <= g (pre[0] = 0 <= g).
+__device__ __forceinline__ int32_t seg_of(const int64_t *pre, int32_t n, int64_t g) {
+  int32_t lo = 0, hi = n;  // invariant: pre[lo] <= g, answer in [lo, hi)
+  while (hi - lo > 1) {
+    int32_t mid = (lo + hi) >> 1;
+    if (pre[mid] <= g) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ bool uses_src_pool(int32_t op) {
+  return op == KVX_OP_GATHER || op == KVX_OP_TRANSFER;
+}
+__device__ __forceinline__ bool uses_dst_pool(int32_t op) {
+  return op == KVX_OP_SCATTER || op == KVX_OP_TRANSFER;
+}
+
+struct Tok {
+  int64_t s, d;     // source / destination index
+  int32_t req;      // request (batch) or 0
+  int32_t err;      // kvx_status of this token's indices
+  int32_t op;       // operation of the token's request
+  bool start;       // first token of a request
+  bool live;        // false: token of a failed request or past the planned range
+};
+
+// Indices of token g.  hint: a segment known to start at or before g (batch / runs).
+__device__ __forceinline__ Tok fetch(const PlanArgs &a, int64_t g, int32_t &seg) {
+  Tok t;
+  t.req = 0;
+  t.err = 0;
+  t.op = a.op;
+  t.start = (g == 0);
+  t.live = true;
+  if (a.mode == kModeSlots) {
+    t.s = a.src.is_pool ? (int64_t)a.src_idx[g] : g;
+    t.d = a.dst.is_pool ? (int64_t)a.dst_idx[g] : g;
+  } else {
+    const int64_t *pre = reinterpret_cast<const int64_t *>(a.ws + a.L.prefix_off);
+    if (g >= pre[a.n_segs]) {  // fewer tokens than promised: already a fatal status
+      t.s = t.d = 0;
+      t.live = false;
+      return t;
+    }
+    while (seg + 1 < a.n_segs && pre[seg + 1] <= g) ++seg;
+    const int64_t off = g - pre[seg];
+    if (a.mode == kModeRuns) {
+      t.s = a.src.is_pool ? (int64_t)a.runs[3 * (int64_t)seg] + off : g;
+      t.d = a.dst.is_pool ? (int64_t)a.runs[3 * (int64_t)seg + 1] + off : g;
+    } else {
+      t.req = seg;
+      t.start = (off == 0);
+      if (a.status[1 + seg] != KVX_OK) {  // bad record: never read its index arrays
+        t.s = t.d = off;
+        t.live = false;
+        return t;
+      }
+      const kvx_request r = a.reqs[seg];
+      t.op = r.op;
+      t.s = uses_src_pool(r.op) ? (int64_t)a.src_idx[r.src_off + off] : off;
+      t.d = uses_dst_pool(r.op) ? (int64_t)a.dst_idx[r.dst_off + off] : off;
+    }
+  }
+  const bool sp = (a.mode == kModeBatch) ? uses_src_pool(t.op) : (bool)a.src.is_pool;
+  const bool dp = (a.mode == kModeBatch) ? uses_dst_pool(t.op) : (bool)a.dst.is_pool;
+  if ((sp && (t.s < 0 || t.s >= a.src.num_slots)) || (dp && (t.d < 0 || t.d >= a.dst.num_slots)))
+    t.err = KVX_ERR_OUT_OF_RANGE;
+  return t;
+}
+
+__device__ __forceinline__ bool starts_run(const PlanArgs &a, const Tok &t, const Tok &prev,
+                                           bool first_in_tile) {
+  if (first_in_tile || t.start || t.req != prev.req) return true;
+  if (t.s != prev.s + 1 || t.d != prev.d + 1) return true;
+  const bool sp = (a.mode == kModeBatch) ? uses_src_pool(t.op) : (bool)a.src.is_pool;
+  const bool dp = (a.mode == kModeBatch) ? uses_dst_pool(t.op) : (bool)a.dst.is_pool;
+  if (sp && a.src.hnd && t.s % a.src.page_size == 0) return true;
+  if (dp && a.dst.hnd && t.d % a.dst.page_size == 0) return true;
+  return false;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanArgs a) {
+  __shared__ int32_t s_tok[kTile];   // token offset (in tile) of run r
+  __shared__ int32_t s_src[kTile];   // first source index of run r
+  __shared__ int32_t s_dst[kTile];   // first destination index of run r
+  __shared__ int32_t s_req[kTile];   // request of run r
+  __shared__ int32_t s_coff[kTile + 1];
+  __shared__ int32_t s_warp[kPlanThreads / 32];
+
+  pdl_trigger();
+  pdl_wait();  // the prefix kernel (runs / batch) must be complete
+
+  const int tile = blockIdx.x;
+  const int64_t t0 = (int64_t)tile * kTile;
+  const int64_t rem = a.n_tokens - t0;
+  const int32_t cnt = (int32_t)(rem < kTile ? rem : kTile);
+  const int tid = threadIdx.x;
+
+  // phase 1: indices, checks and run starts of this thread's tokens
+  Tok tk[kPlanItems];
+  bool brk[kPlanItems];
+  int32_t nbrk = 0, err = 0;
+  const int32_t i0 = tid * kPlanItems;
+  int32_t seg = 0;
+  if ((a.mode != kModeSlots) && i0 < cnt) {
+    const int64_t *pre = reinterpret_cast<const int64_t *>(a.ws + a.L.prefix_off);
+    const int64_t g = t0 + i0 - (i0 > 0 ? 1 : 0);
+    seg = (g < pre[a.n_segs]) ? seg_of(pre, a.n_segs, g) : 0;
+  }
+  Tok prev;
+  if (i0 > 0 && i0 < cnt) prev = fetch(a, t0 + i0 - 1, seg);
+#pragma unroll
+  for (int k = 0; k < kPlanItems; ++k) {
+    const int32_t i = i0 + k;
+    brk[k] = false;
+    if (i < cnt) {
+      tk[k] = fetch(a, t0 + i, seg);
+      err = max(err, tk[k].err);
+      brk[k] = starts_run(a, tk[k], prev, i == 0);
+      prev = tk[k];
+      nbrk += brk[k] ? 1 : 0;
+      if (tk[k].err != KVX_OK && a.mode == kModeBatch) atomicMax(&a.status[1 + tk[k].req], tk[k].err);
+    }
+  }
+  err = block_max<kPlanThreads>(err, s_warp);
+  if (tid == 0) {
+    if (a.status_direct) a.status[0] = err;
+    else if (err != KVX_OK) atomicMax(&a.status[0], err);
+  }
+
+  int32_t n_runs;
+  int32_t r = block_exclusive_scan<kPlanThreads>(nbrk, &n_runs, s_warp);
+#pragma unroll
+  for (int k = 0; k < kPlanItems; ++k) {
+    if (brk[k]) {
+      s_tok[r] = i0 + k;
+      s_src[r] = (int32_t)tk[k].s;
+      s_dst[r] = (int32_t)tk[k].d;
+      s_req[r] = tk[k].req;
+      ++r;
+    }
+  }
+  __syncthreads();
+
+  // phase 2: chunks per run, scanned into each run's first chunk
+  const int32_t m = a.chunk_rows;
+  int32_t nch[kPlanItems];
+  int32_t my_chunks = 0;
+#pragma unroll
+  for (int k = 0; k < kPlanItems; ++k) {
+    const int32_t rr = i0 + k;
+    nch[k] = 0;
+    if (rr < n_runs) {
+      const int32_t len = (rr + 1 < n_runs ? s_tok[rr + 1] : cnt) - s_tok[rr];
+      nch[k] = (len + m - 1) / m;
+    }
+    my_chunks += nch[k];
+  }
+  int32_t n_chunks;
+  int32_t c = block_exclusive_scan<kPlanThreads>(my_chunks, &n_chunks, s_warp);
+#pragma unroll
+  for (int k = 0; k < kPlanItems; ++k) {
+    if (i0 + k < n_runs) s_coff[i0 + k] = c;
+    c += nch[k];
+  }
+  if (tid == 0) s_coff[n_runs] = n_chunks;
+  __syncthreads();
+
+  if (tid == 0) {
+    reinterpret_cast<int32_t *>(a.ws + a.L.tiles_off)[tile] = n_chunks;
+    if (tile == 0) {
+      PlanHeader *h = reinterpret_cast<PlanHeader *>(a.ws + a.L.header_off);
+      h->mode = a.mode;
+      h->op = a.op;
+      h->n_segs = a.n_segs;
+      h->n_tokens = a.n_tokens;
+      h->chunk_rows = a.chunk_rows;
+      h->planes = a.planes;
+      h->row_bytes = a.row_bytes;
+      h->src_is_pool = a.src.is_pool;
+      h->src_hnd = a.src.hnd;
+      h->src_page_size = a.src.page_size;
+      h->dst_is_pool = a.dst.is_pool;
+      h->dst_hnd = a.dst.hnd;
+      h->dst_page_size = a.dst.page_size;
+      h->pad = 0;
+      h->src_num_slots = a.src.num_slots;
+      h->dst_num_slots = a.dst.num_slots;
+      h->magic = kPlanMagic;
+    }
+  }
+
+  // phase 3: write the chunks
+  Chunk *out = reinterpret_cast<Chunk *>(a.ws + a.L.chunks_off) + (int64_t)tile * kTile;
+  for (int32_t ci = tid; ci < n_chunks; ci += kPlanThreads) {
+    int32_t lo = 0, hi = n_runs;  // largest run with s_coff[run] <= ci
+    while (hi - lo > 1) {
+      const int32_t mid = (lo + hi) >> 1;
+      if (s_coff[mid] <= ci) lo = mid; else hi = mid;
+    }
+    const int32_t len = (lo + 1 < n_runs ? s_tok[lo + 1] : cnt) - s_tok[lo];
+    const int32_t j0 = (ci - s_coff[lo]) * m;
+    Chunk ch;
+    ch.req = s_req[lo];
+    ch.src = s_src[lo] + j0;
+    ch.dst = s_dst[lo] + j0;
+    ch.rows = min(m, len - j0);
+    out[ci] = ch;
+  }
+}
+
+// Checks one batch record; returns its status.
+__device__ __forceinline__ int32_t check_request(const PlanArgs &a, const kvx_request &r) {
+  if (r.op < KVX_OP_GATHER || r.op > KVX_OP_TRANSFER) return KVX_ERR_INVALID_ARG;
+  if (r.n_tokens < 0 || r.n_tokens > KVX_MAX_TOKENS) return KVX_ERR_INVALID_ARG;
+  const bool us = uses_src_pool(r.op), ud = uses_dst_pool(r.op);
+  if (us && (!a.has_src || r.src_off < 0 || r.src_off + r.n_tokens > a.n_src_idx))
+    return KVX_ERR_INVALID_ARG;
+  if (ud && (!a.has_dst || r.dst_off < 0 || r.dst_off + r.n_tokens > a.n_dst_idx))
+    return KVX_ERR_INVALID_ARG;
+  if (r.op != KVX_OP_TRANSFER) {
+    const int64_t need = (int64_t)a.planes * r.n_tokens * a.row_bytes;
+    if (r.buf_off < 0 || (r.buf_off & 15) != 0 || r.buf_off + need > a.buf_bytes)
+      return KVX_ERR_INVALID_ARG;
+  }
+  return KVX_OK;
+}
+
+// One CTA: token offset of every run / request, their checks, and status words.
+__global__ void __launch_bounds__(kPrefixThreads) prefix_kernel(const __grid_constant__ PlanArgs a) {
+  __shared__ int64_t s_warp64[kPrefixThreads / 32];
+  __shared__ int32_t s_warp32[kPrefixThreads / 32];
+  pdl_trigger();
+  pdl_wait();
+  int64_t *pre = reinterpret_cast<int64_t *>(a.ws + a.L.prefix_off);
+  const int tid = threadIdx.x;
+  int64_t carry = 0;
+  int32_t err = 0;
+  for (int64_t base = 0; base < a.n_segs; base += (int64_t)kPrefixThreads * kPrefixItems) {
+    int64_t len[kPrefixItems];
+    int64_t sum = 0;
+#pragma unroll
+    for (int k = 0; k < kPrefixItems; ++k) {
+      const int64_t q = base + (int64_t)tid * kPrefixItems + k;
+      len[k] = 0;
+      if (q < a.n_segs) {
+        int32_t e = KVX_OK;
+        if (a.mode == kModeRuns) {
+          len[k] = a.runs[3 * q + 2];
+          if (len[k] < 0) { e = KVX_ERR_INVALID_ARG; len[k] = 0; }
+        } else {
+          const kvx_request r = a.reqs[q];
+          e = check_request(a, r);
+          len[k] = r.n_tokens > 0 && r.n_tokens <= KVX_MAX_TOKENS ? r.n_tokens : 0;
+          a.status[1 + q] = e;
+        }
+        err = max(err, e);
+      }
+      sum += len[k];
+    }
+    int64_t total;
+    int64_t run = carry + block_exclusive_scan<kPrefixThreads>(sum, &total, s_warp64);
+#pragma unroll
+    for (int k = 0; k < kPrefixItems; ++k) {
+      const int64_t q = base + (int64_t)tid * kPrefixItems + k;
+      if (q < a.n_segs) pre[q] = run;
+      run += len[k];
+    }
+    carry += total;
+  }
+  if (tid == 0) pre[a.n_segs] = carry;
+  const int32_t fatal = (carry != a.n_tokens) ? KVX_ERR_INVALID_ARG : KVX_OK;
+  err = block_max<kPrefixThreads>(err, s_warp32);
+  if (fatal != KVX_OK && a.mode == kModeBatch) {
+    for (int64_t q = tid; q < a.n_segs; q += kPrefixThreads) a.status[1 + q] = fatal;
+  }
+  if (tid == 0) a.status[0] = max(err, fatal);
+}
+
+// Flattens the per-tile chunk tables (one CTA).
+__global__ void __launch_bounds__(1024) export_kernel(const char *ws, WsLayout L, int64_t n_tokens,
+                                                      int32_t *out, int64_t max_chunks,
+                                                      int64_t *count) {
+  __shared__ int64_t s_warp[32];
+  const int32_t *tiles = reinterpret_cast<const int32_t *>(ws + L.tiles_off);
+  const Chunk *chunks = reinterpret_cast<const Chunk *>(ws + L.chunks_off);
+  const int64_t nt = num_tiles(n_tokens);
+  int64_t carry = 0;
+  for (int64_t base = 0; base < nt; base += 1024) {
+    const int64_t t = base + threadIdx.x;
+    int64_t mine = t < nt ? tiles[t] : 0;
+    mine = mine < 0 ? 0 : (mine > kTile ? kTile : mine);  // never read past a tile's table
+    int64_t total;
+    const int64_t at = carry + block_exclusive_scan<1024>(mine, &total, s_warp);
+    carry += total;
+    if (t < nt) {
+      for (int64_t k = 0; k < mine; ++k) {
+        if (at + k < max_chunks) {
+          const Chunk c = chunks[t * kTile + k];
+          int32_t *o = out + 4 * (at + k);
+          o[0] = c.req;
+          o[1] = c.src;
+          o[2] = c.dst;
+          o[3] = c.rows;
+        }
+      }
+    }
+  }
+  if (threadIdx.x == 0) *count = carry;
+}
+
+cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, void **args, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) {
+    // programmatic dependent launch refused on this stream: launch in plain stream order
+    (void)cudaGetLastError();
+    cfg.numAttrs = 0;
+    e = cudaLaunchKernelExC(&cfg, fn, args);
+  }
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_prefix(const PlanArgs &a, cudaStream_t s) {
+  void *args[] = {const_cast<PlanArgs *>(&a)};
+  return launch_pdl(reinterpret_cast<const void *>(prefix_kernel), dim3(1), dim3(kPrefixThreads),
+                    args, s);
+}
+
+cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s) {
+  void *args[] = {const_cast<PlanArgs *>(&a)};
+  return launch_pdl(reinterpret_cast<const void *>(plan_kernel),
+                    dim3((unsigned)num_tiles(a.n_tokens)), dim3(kPlanThreads), args, s);
+}
+
+cudaError_t launch_export(const char *ws, WsLayout L, int64_t n_tokens, int32_t *out,
+                          int64_t max_chunks, int64_t *count, cudaStream_t s) {
+  export_kernel<<<1, 1024, 0, s>>>(ws, L, n_tokens, out, max_chunks, count);
+  return cudaGetLastError();
+}
+
+}  // namespace kvx

@@ -1,0 +1,352 @@
+"""Thin Python binding of libkvx (include/kvx.h).
+
+Argument marshalling only: every step of a move runs in libkvx's kernels.  Each function here
+maps one to one onto the C entry point of the same name without the ``kvx_`` prefix
+(``gather`` -> ``kvx_gather``).  Device buffers may be given as torch tensors (their
+``data_ptr()`` is passed) or as plain integer addresses; ``stream=None`` means torch's current
+stream.  A non-OK return code raises :class:`KvxError`; device-side results land in the status
+tensor the caller passes.
+
+There is no fallback: if ``libkvx.so`` is missing the first call raises, telling the user to
+build it (``python -m disaggregated_paged_kv_gb300.build`` or ``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkvx.so")
+
+# ---- constants (kvx.h) ------------------------------------------------------------------
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_ALIGNMENT = 2
+ERR_OUT_OF_RANGE = 3
+ERR_DUPLICATE_DST = 4
+ERR_OVERLAP = 5
+ERR_CUDA = 6
+ERR_NO_WORKSPACE = 7
+ERR_TIMEOUT = 8
+ERR_CANCELLED = 9
+
+F16, BF16, F32, FP8 = 1, 2, 3, 4
+NHD, HND_PAGED = 0, 1
+OP_GATHER, OP_SCATTER, OP_TRANSFER, OP_BATCH = 0, 1, 2, 3
+
+MAX_PLANES = 256
+PLAN_TILE = 2048
+MAX_TOKENS = PLAN_TILE * 4096
+CHUNK_BYTES = 8192
+
+ELEM_BYTES = {F16: 2, BF16: 2, F32: 4, FP8: 1}
+
+
+class KvxError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = status_str(code)
+        if code == ERR_CUDA:
+            msg += f" (cudaError {last_cuda_error()})"
+        super().__init__(f"{where}: {msg} [{code}]")
+
+
+class LayoutDesc(ctypes.Structure):
+    _fields_ = [
+        ("num_layers", ctypes.c_int32),
+        ("kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("kind", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("num_slots", ctypes.c_int64),
+        ("plane_ptrs", ctypes.POINTER(ctypes.c_void_p)),
+        ("base", ctypes.c_void_p),
+        ("plane_stride", ctypes.c_int64),
+        ("slot_stride", ctypes.c_int64),
+    ]
+
+
+class Request(ctypes.Structure):
+    _fields_ = [
+        ("op", ctypes.c_int32),
+        ("n_tokens", ctypes.c_int32),
+        ("src_off", ctypes.c_int64),
+        ("dst_off", ctypes.c_int64),
+        ("buf_off", ctypes.c_int64),
+    ]
+
+
+assert ctypes.sizeof(Request) == 32
+
+_lib: Optional[ctypes.CDLL] = None
+
+_VP = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+_SIGS = {
+    "kvx_layout_create": (_I32, [ctypes.POINTER(LayoutDesc), ctypes.POINTER(_VP)]),
+    "kvx_layout_destroy": (_I32, [_VP]),
+    "kvx_layout_row_bytes": (_I64, [_VP]),
+    "kvx_layout_num_planes": (_I32, [_VP]),
+    "kvx_workspace_size": (_SZ, [_I64, _I32]),
+    "kvx_gather": (_I32, [_VP, _VP, _I32, _VP, _SZ, _VP, _SZ, _VP, _VP]),
+    "kvx_scatter": (_I32, [_VP, _VP, _I32, _VP, _SZ, _VP, _SZ, _VP, _VP]),
+    "kvx_transfer": (_I32, [_VP, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _VP]),
+    "kvx_gather_runs": (_I32, [_VP, _VP, _I32, _I32, _VP, _SZ, _VP, _SZ, _VP, _VP]),
+    "kvx_scatter_runs": (_I32, [_VP, _VP, _I32, _I32, _VP, _SZ, _VP, _SZ, _VP, _VP]),
+    "kvx_transfer_runs": (_I32, [_VP, _VP, _VP, _I32, _I32, _VP, _SZ, _VP, _VP]),
+    "kvx_batch": (_I32, [_VP, _VP, _VP, _I32, _I64, _VP, _I64, _VP, _I64, _VP, _SZ, _VP, _SZ,
+                         _VP, _VP]),
+    "kvx_submit": (_I32, [_I32, _VP, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _SZ, _VP, _VP]),
+    "kvx_plan": (_I32, [_I32, _VP, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _VP]),
+    "kvx_plan_runs": (_I32, [_I32, _VP, _VP, _VP, _I32, _I32, _VP, _SZ, _VP, _VP]),
+    "kvx_plan_batch": (_I32, [_VP, _VP, _VP, _I32, _I64, _VP, _I64, _VP, _I64, _SZ, _VP, _SZ,
+                              _VP, _VP]),
+    "kvx_execute": (_I32, [_I32, _VP, _VP, _VP, _I32, _I64, _VP, _SZ, _VP, _SZ, _VP, _VP]),
+    "kvx_plan_export": (_I32, [_VP, _SZ, _I64, _VP, _I64, _VP, _VP]),
+    "kvx_status_str": (ctypes.c_char_p, [_I32]),
+    "kvx_last_cuda_error": (_I32, []),
+    "kvx_version": (_I32, []),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libkvx.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libkvx.so not found at {LIB_PATH}; build it with "
+                "`python -m disaggregated_paged_kv_gb300.build`")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(l, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = l
+    return _lib
+
+
+def exported_names() -> Sequence[str]:
+    return tuple(_SIGS)
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _nbytes(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        raise TypeError("give the byte size explicitly for a raw address")
+    return int(x.numel() * x.element_size())
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream) or None
+    if isinstance(stream, int):
+        return stream or None
+    return int(stream.cuda_stream) or None
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != OK:
+        raise KvxError(rc, where)
+
+
+def status_str(code: int) -> str:
+    return lib().kvx_status_str(code).decode()
+
+
+def last_cuda_error() -> int:
+    return int(lib().kvx_last_cuda_error())
+
+
+def version() -> int:
+    return int(lib().kvx_version())
+
+
+def workspace_size(max_tokens: int, max_requests: int = 0) -> int:
+    return int(lib().kvx_workspace_size(max_tokens, max_requests))
+
+
+class Layout:
+    """Owns a kvx_layout_t.  Plane addresses come either from ``plane_ptrs`` (a sequence of
+    tensors or integer addresses, one per plane) or from ``base`` + p * ``plane_stride``."""
+
+    def __init__(self, num_layers: int, kv_heads: int, head_dim: int, dtype: int,
+                 num_slots: int, kind: int = NHD, page_size: int = 1, plane_ptrs=None,
+                 base=None, plane_stride: int = 0, slot_stride: int = 0, keepalive=None):
+        d = LayoutDesc()
+        d.num_layers, d.kv_heads, d.head_dim, d.dtype = num_layers, kv_heads, head_dim, dtype
+        d.kind, d.page_size, d.num_slots = kind, page_size, num_slots
+        self._ptr_array = None
+        if plane_ptrs is not None:
+            arr = (ctypes.c_void_p * len(plane_ptrs))(*[_ptr(p) for p in plane_ptrs])
+            self._ptr_array = arr
+            d.plane_ptrs = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+        d.base = _ptr(base)
+        d.plane_stride, d.slot_stride = plane_stride, slot_stride
+        h = ctypes.c_void_p()
+        _check(lib().kvx_layout_create(ctypes.byref(d), ctypes.byref(h)), "kvx_layout_create")
+        self.handle = h.value
+        self.num_layers, self.kv_heads, self.head_dim = num_layers, kv_heads, head_dim
+        self.dtype, self.kind, self.page_size, self.num_slots = dtype, kind, page_size, num_slots
+        self._keepalive = keepalive  # tensors whose memory the planes point into
+
+    @property
+    def row_bytes(self) -> int:
+        return int(lib().kvx_layout_row_bytes(self.handle))
+
+    @property
+    def num_planes(self) -> int:
+        return int(lib().kvx_layout_num_planes(self.handle))
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            lib().kvx_layout_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _h(layout: Optional[Layout]) -> Optional[int]:
+    return None if layout is None else layout.handle
+
+
+def gather(src: Layout, src_slots, n: int, buf, ws, status, buf_bytes=None, ws_bytes=None,
+           stream=None) -> None:
+    rc = lib().kvx_gather(_h(src), _ptr(src_slots), n, _ptr(buf),
+                          _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
+                          _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
+                          _stream(stream))
+    _check(rc, "kvx_gather")
+
+
+def scatter(dst: Layout, dst_slots, n: int, buf, ws, status, buf_bytes=None, ws_bytes=None,
+            stream=None) -> None:
+    rc = lib().kvx_scatter(_h(dst), _ptr(dst_slots), n, _ptr(buf),
+                           _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
+                           _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
+                           _stream(stream))
+    _check(rc, "kvx_scatter")
+
+
+def transfer(src: Layout, src_slots, dst: Layout, dst_slots, n: int, ws, status,
+             ws_bytes=None, stream=None) -> None:
+    rc = lib().kvx_transfer(_h(src), _ptr(src_slots), _h(dst), _ptr(dst_slots), n, _ptr(ws),
+                            _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
+                            _stream(stream))
+    _check(rc, "kvx_transfer")
+
+
+def gather_runs(src: Layout, runs, n_runs: int, n_tokens: int, buf, ws, status, buf_bytes=None,
+                ws_bytes=None, stream=None) -> None:
+    rc = lib().kvx_gather_runs(_h(src), _ptr(runs), n_runs, n_tokens, _ptr(buf),
+                               _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
+                               _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
+                               _stream(stream))
+    _check(rc, "kvx_gather_runs")
+
+
+def scatter_runs(dst: Layout, runs, n_runs: int, n_tokens: int, buf, ws, status,
+                 buf_bytes=None, ws_bytes=None, stream=None) -> None:
+    rc = lib().kvx_scatter_runs(_h(dst), _ptr(runs), n_runs, n_tokens, _ptr(buf),
+                                _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
+                                _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
+                                _stream(stream))
+    _check(rc, "kvx_scatter_runs")
+
+
+def transfer_runs(src: Layout, dst: Layout, runs, n_runs: int, n_tokens: int, ws, status,
+                  ws_bytes=None, stream=None) -> None:
+    rc = lib().kvx_transfer_runs(_h(src), _h(dst), _ptr(runs), n_runs, n_tokens, _ptr(ws),
+                                 _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
+                                 _stream(stream))
+    _check(rc, "kvx_transfer_runs")
+
+
+def batch(src: Optional[Layout], dst: Optional[Layout], reqs, n_reqs: int, total_tokens: int,
+          src_slots, n_src_slots: int, dst_slots, n_dst_slots: int, buf, ws, status,
+          buf_bytes=None, ws_bytes=None, stream=None) -> None:
+    rc = lib().kvx_batch(_h(src), _h(dst), _ptr(reqs), n_reqs, total_tokens, _ptr(src_slots),
+                         n_src_slots, _ptr(dst_slots), n_dst_slots, _ptr(buf),
+                         _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
+                         _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
+                         _stream(stream))
+    _check(rc, "kvx_batch")
+
+
+def submit(op: int, src: Optional[Layout], h_src_slots, dst: Optional[Layout], h_dst_slots,
+           n: int, buf, ws, h_status, buf_bytes=None, ws_bytes=None, stream=None) -> None:
+    """Host slot lists (pinned tensors or numpy arrays) and a host status word."""
+    rc = lib().kvx_submit(op, _h(src), _host_ptr(h_src_slots), _h(dst), _host_ptr(h_dst_slots),
+                          n, _ptr(buf), _nbytes(buf) if buf_bytes is None else buf_bytes,
+                          _ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
+                          _host_ptr(h_status), _stream(stream))
+    _check(rc, "kvx_submit")
+
+
+def _host_ptr(x) -> Optional[int]:
+    if x is None or isinstance(x, int):
+        return x
+    if hasattr(x, "ctypes"):  # numpy
+        return int(x.ctypes.data)
+    return int(x.data_ptr())
+
+
+def plan(op: int, src: Optional[Layout], src_slots, dst: Optional[Layout], dst_slots, n: int,
+         ws, status, ws_bytes=None, stream=None) -> None:
+    rc = lib().kvx_plan(op, _h(src), _ptr(src_slots), _h(dst), _ptr(dst_slots), n, _ptr(ws),
+                        _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
+                        _stream(stream))
+    _check(rc, "kvx_plan")
+
+
+def plan_runs(op: int, src: Optional[Layout], dst: Optional[Layout], runs, n_runs: int,
+              n_tokens: int, ws, status, ws_bytes=None, stream=None) -> None:
+    rc = lib().kvx_plan_runs(op, _h(src), _h(dst), _ptr(runs), n_runs, n_tokens, _ptr(ws),
+                             _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
+                             _stream(stream))
+    _check(rc, "kvx_plan_runs")
+
+
+def plan_batch(src: Optional[Layout], dst: Optional[Layout], reqs, n_reqs: int,
+               total_tokens: int, src_slots, n_src_slots: int, dst_slots, n_dst_slots: int,
+               buf_bytes: int, ws, status, ws_bytes=None, stream=None) -> None:
+    rc = lib().kvx_plan_batch(_h(src), _h(dst), _ptr(reqs), n_reqs, total_tokens,
+                              _ptr(src_slots), n_src_slots, _ptr(dst_slots), n_dst_slots,
+                              buf_bytes, _ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
+                              _ptr(status), _stream(stream))
+    _check(rc, "kvx_plan_batch")
+
+
+def execute(op: int, src: Optional[Layout], dst: Optional[Layout], reqs, n_reqs: int,
+            n_tokens: int, buf, ws, status, buf_bytes=None, ws_bytes=None, stream=None) -> None:
+    rc = lib().kvx_execute(op, _h(src), _h(dst), _ptr(reqs), n_reqs, n_tokens, _ptr(buf),
+                           _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
+                           _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
+                           _stream(stream))
+    _check(rc, "kvx_execute")
+
+
+def plan_export(ws, n_tokens: int, out, max_chunks: int, count, ws_bytes=None,
+                stream=None) -> None:
+    rc = lib().kvx_plan_export(_ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
+                               n_tokens, _ptr(out), max_chunks, _ptr(count), _stream(stream))
+    _check(rc, "kvx_plan_export")

@@ -1,0 +1,286 @@
+/*
+ * kvx.h -- libkvx: move a finished prefill's KV cache out of a token-paged KV pool on one
+ * GB300 (sm_103a).
+ *
+ * A request's K/V rows sit scattered across a paged pool, often as thousands of few-KB
+ * fragments.  libkvx gathers them by slot index into a contiguous transfer buffer (optionally
+ * turning per-page [heads][tokens][dim] into [tokens][heads][dim]), scatters a buffer back into
+ * a pool, or moves rows straight from one pool into another pool in the same HBM.
+ *
+ * Sources (web pages, cited by title and section):
+ *  [PD-budget]  "穷人版 PD 分离：在消费级显卡上把 TTS 推理拆成两半" (kilerd.me/pd-on-a-budget):
+ *               "B300：让 P 直接写 D 的显存" (a gather kernel writes scattered source rows
+ *               straight into the decode side's pages), "5090：一个看得见所有卡的代理" (token-paged
+ *               pool, ~7,660 few-KB fragments per request, gather into a contiguous staging
+ *               region then scatter back; fragment count, not bytes, sets the cost), "最难的一个
+ *               问题" (a failed transfer must be reported to the client at once).
+ *  [DistServe]  "DistServe 完全拆解": "KV Cache 跨实例传输" (B_KV = 2 L n_layer n_kvhead d_head b,
+ *               T = B_KV / BW_eff + T_setup), "一次请求如何穿过 DistServe" (per-layer pulls, no
+ *               contiguous buffer needed).
+ *  [mini-infer] "mini-infer系统实战-18-PD 解耦": "KV 序列化格式选择" (per-layer (k, v), each
+ *               [seq, kv_heads, head_dim]; permute(1,0,2) on extract and on rebuild).
+ *  [Mooncake]   "PD分离调研：从推理阶段拆分到Mooncake的KVCache中心架构": 6.1 (TransferEngine:
+ *               registered memory, batches of non-contiguous src/dst, asynchronous status),
+ *               7.4 (per-layer KV tensors registered as base address + block length),
+ *               7.6 (src_ptrs/dst_ptrs/lengths, contiguous blocks coalesced),
+ *               7.7 (HND layout for non-MLA KV).
+ *
+ * Conventions used by every call:
+ *  - A layout has P = 2 * num_layers planes, plane p = 2*layer + kv with K = 0, V = 1.
+ *  - A row is one (plane, token): kv_heads * head_dim elements, R bytes.  R must be a multiple
+ *    of 16.  Values are never interpreted: every operation is an exact byte copy, so NaN
+ *    payloads and any bit pattern survive.
+ *  - A contiguous transfer buffer holding n tokens is [plane][n][kv_heads][head_dim], i.e.
+ *    [layer][K/V][seq][head][dim]: row (p, i) starts at byte (p * n + i) * R.
+ *  - Slots and page-table entries are int32.  Byte offsets are 64-bit.
+ *
+ * Ownership: the caller owns every device buffer (pools, index arrays, transfer buffers,
+ * workspace, status words).  The library owns only the host-side layout handle.  No call
+ * allocates memory or synchronises the host; work is enqueued on the caller's stream and the
+ * call returns.
+ *
+ * Errors come in two kinds ([PD-budget] "最难的一个问题": the client learns of a failure at
+ * once, and nothing is half-written):
+ *  - Problems visible on the host (null or misaligned pointers, bad sizes, mismatched
+ *    layouts, overlapping memory, short workspace) return a kvx_status immediately and enqueue
+ *    nothing.
+ *  - Problems in device-resident data (an index out of range, a bad request record) are
+ *    written by the planner into the device status word(s).  The copy then moves nothing for
+ *    the affected call (or, in kvx_batch, the affected request): all or nothing.  Read the
+ *    status after synchronising the stream.
+ */
+#ifndef KVX_H
+#define KVX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVX_API __attribute__((visibility("default")))
+#else
+#define KVX_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *kvx_stream_t;
+
+typedef enum kvx_status {
+  KVX_OK = 0,
+  KVX_ERR_INVALID_ARG = 1,   /* bad size, null pointer, inconsistent layouts or request */
+  KVX_ERR_ALIGNMENT = 2,     /* pointer or row size not 16-byte aligned */
+  KVX_ERR_OUT_OF_RANGE = 3,  /* a slot / page index outside the pool (device status) */
+  KVX_ERR_DUPLICATE_DST = 4, /* reserved: a destination slot named twice */
+  KVX_ERR_OVERLAP = 5,       /* source and destination memory overlap */
+  KVX_ERR_CUDA = 6,          /* a CUDA runtime call failed; see kvx_last_cuda_error() */
+  KVX_ERR_NO_WORKSPACE = 7,  /* workspace too small or misaligned */
+  KVX_ERR_TIMEOUT = 8,       /* reserved */
+  KVX_ERR_CANCELLED = 9      /* reserved */
+} kvx_status;
+
+typedef enum kvx_dtype {
+  KVX_F16 = 1,  /* 2-byte elements */
+  KVX_BF16 = 2, /* 2-byte elements */
+  KVX_F32 = 3,  /* 4-byte elements */
+  KVX_FP8 = 4   /* 1-byte elements */
+} kvx_dtype;
+
+typedef enum kvx_kind {
+  /* Token rows: each plane is [num_slots][kv_heads][head_dim]; slot s starts at
+   * plane + s * slot_stride.  Covers per-plane pools ([Mooncake] 7.4: one tensor per layer,
+   * block length = row bytes) and slot-major pools [slot][layer][K/V][head][dim]
+   * (plane_stride = R, slot_stride = P * R). */
+  KVX_NHD = 0,
+  /* HND pages ([Mooncake] 7.7): each plane is [num_slots / page_size][kv_heads][page_size]
+   * [head_dim].  Slot s is token s % page_size of page s / page_size. */
+  KVX_HND_PAGED = 1
+} kvx_kind;
+
+typedef enum kvx_op {
+  KVX_OP_GATHER = 0,   /* pool rows -> contiguous buffer */
+  KVX_OP_SCATTER = 1,  /* contiguous buffer -> pool rows */
+  KVX_OP_TRANSFER = 2, /* pool rows -> pool rows */
+  KVX_OP_BATCH = 3     /* kvx_execute only: the plan came from kvx_plan_batch */
+} kvx_op;
+
+/* Most planes a layout may have (128 layers x K/V). */
+#define KVX_MAX_PLANES 256
+/* The planner works on tiles of this many consecutive tokens; a run never crosses a multiple
+ * of it. */
+#define KVX_PLAN_TILE 2048
+/* Most tokens (or rows) one call may move per plane. */
+#define KVX_MAX_TOKENS (KVX_PLAN_TILE * 4096)
+/* The planner cuts every run into chunks of at most max(1, KVX_CHUNK_BYTES / R) rows; one
+ * warp moves one chunk of one plane. */
+#define KVX_CHUNK_BYTES 8192
+
+typedef struct kvx_layout_desc {
+  int32_t num_layers; /* L >= 1, 2L <= KVX_MAX_PLANES */
+  int32_t kv_heads;   /* H >= 1 */
+  int32_t head_dim;   /* D >= 1 (elements) */
+  int32_t dtype;      /* kvx_dtype; only its byte width is used */
+  int32_t kind;       /* kvx_kind */
+  int32_t page_size;  /* KVX_HND_PAGED: tokens per page (>= 1).  KVX_NHD: ignored. */
+  int64_t num_slots;  /* token slots per plane; HND: a multiple of page_size */
+  /* Plane addresses: either plane_ptrs (host array of 2L device pointers, read during
+   * kvx_layout_create and not kept) or, when plane_ptrs is NULL, plane p at
+   * base + p * plane_stride.  Every plane address must be 16-byte aligned. */
+  void *const *plane_ptrs;
+  void *base;
+  int64_t plane_stride;
+  /* KVX_NHD: bytes from slot s to slot s+1 within a plane; 0 means R (dense rows).  Must be a
+   * multiple of 16 and >= R.  KVX_HND_PAGED: must be 0. */
+  int64_t slot_stride;
+} kvx_layout_desc;
+
+typedef struct kvx_layout *kvx_layout_t;
+
+/* One request of a batch ([Mooncake] 6.1 BatchTransfer entry).  32 bytes, device-resident.
+ *  op        KVX_OP_GATHER, KVX_OP_SCATTER or KVX_OP_TRANSFER
+ *  n_tokens  rows per plane moved by this request (>= 0)
+ *  src_off   first element of this request's source slots in the batch's source slot list
+ *            (GATHER, TRANSFER)
+ *  dst_off   first element of its destination slots in the destination slot list
+ *            (SCATTER, TRANSFER)
+ *  buf_off   byte offset (multiple of 16) of its buffer region, laid out
+ *            [plane][n_tokens][head][dim] (GATHER, SCATTER) */
+typedef struct kvx_request {
+  int32_t op;
+  int32_t n_tokens;
+  int64_t src_off;
+  int64_t dst_off;
+  int64_t buf_off;
+} kvx_request;
+
+/* ---- layouts ------------------------------------------------------------------------ */
+
+/* Validates desc and creates a host-only handle (no device memory).  Errors:
+ * KVX_ERR_INVALID_ARG (bad field), KVX_ERR_ALIGNMENT (R, head bytes for HND, slot stride or a
+ * plane address not a multiple of 16). */
+KVX_API kvx_status kvx_layout_create(const kvx_layout_desc *desc, kvx_layout_t *out);
+KVX_API kvx_status kvx_layout_destroy(kvx_layout_t layout);
+/* R, the bytes of one (plane, token) row; -1 for a NULL handle. */
+KVX_API int64_t kvx_layout_row_bytes(kvx_layout_t layout);
+/* P = 2 * num_layers; -1 for a NULL handle. */
+KVX_API int32_t kvx_layout_num_planes(kvx_layout_t layout);
+
+/* ---- workspace ---------------------------------------------------------------------- */
+
+/* Bytes of device workspace (256-byte aligned) that any call moving up to max_tokens rows per
+ * plane, with up to max_requests requests (kvx_batch) or runs (kvx_*_runs), needs.  The
+ * workspace holds the plan between the planner and the copy; its contents need no
+ * initialisation.  Returns 0 if the arguments are out of range. */
+KVX_API size_t kvx_workspace_size(int64_t max_tokens, int32_t max_requests);
+
+/* ---- one-shot calls: plan + copy on `stream` ----------------------------------------- */
+
+/* Gather ([PD-budget] 5090 section; [mini-infer] KV 序列化格式选择):
+ *   buf[p][i] = row(src, p, src_slots[i]) for every plane p and i < n.
+ * d_src_slots: device int32[n].  d_buf: device, 16-byte aligned, >= P*n*R bytes.
+ * With a KVX_HND_PAGED source the buffer row is [head][dim], so the call is the fused
+ * [heads,tokens,dim] -> [tokens,heads,dim] permute.
+ * d_status: device int32[1]; KVX_OK or KVX_ERR_OUT_OF_RANGE after the stream reaches it. */
+KVX_API kvx_status kvx_gather(kvx_layout_t src, const int32_t *d_src_slots, int32_t n, void *d_buf,
+                      size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *d_status,
+                      kvx_stream_t stream);
+
+/* Scatter ([PD-budget] 5090 section: D scatters the staged rows into its own pages):
+ *   row(dst, p, dst_slots[i]) = buf[p][i].  Slots not named keep their bytes.  Naming a slot
+ * twice leaves either of the two rows there (unspecified which). */
+KVX_API kvx_status kvx_scatter(kvx_layout_t dst, const int32_t *d_dst_slots, int32_t n,
+                       const void *d_buf, size_t buf_bytes, void *d_ws, size_t ws_bytes,
+                       int32_t *d_status, kvx_stream_t stream);
+
+/* Pool-to-pool transfer ([PD-budget] B300 section; [Mooncake] 7.6):
+ *   row(dst, p, dst_slots[i]) = row(src, p, src_slots[i]).
+ * src and dst must have the same num_layers, kv_heads, head_dim and element size and must
+ * not share memory (KVX_ERR_OVERLAP). */
+KVX_API kvx_status kvx_transfer(kvx_layout_t src, const int32_t *d_src_slots, kvx_layout_t dst,
+                        const int32_t *d_dst_slots, int32_t n, void *d_ws, size_t ws_bytes,
+                        int32_t *d_status, kvx_stream_t stream);
+
+/* Run-list forms ([Mooncake] 7.6 src/dst/length descriptors).  d_runs: device int32[n_runs][3]
+ * = {src_start, dst_start, len}; run r names rows src_start .. src_start+len-1 and
+ * dst_start .. dst_start+len-1.  A buffer side ignores its start field: runs fill (or drain)
+ * consecutive buffer rows in run order.  n_tokens must equal the sum of len (checked on the
+ * device: KVX_ERR_INVALID_ARG in the status word). */
+KVX_API kvx_status kvx_gather_runs(kvx_layout_t src, const int32_t *d_runs, int32_t n_runs,
+                           int32_t n_tokens, void *d_buf, size_t buf_bytes, void *d_ws,
+                           size_t ws_bytes, int32_t *d_status, kvx_stream_t stream);
+KVX_API kvx_status kvx_scatter_runs(kvx_layout_t dst, const int32_t *d_runs, int32_t n_runs,
+                            int32_t n_tokens, const void *d_buf, size_t buf_bytes, void *d_ws,
+                            size_t ws_bytes, int32_t *d_status, kvx_stream_t stream);
+KVX_API kvx_status kvx_transfer_runs(kvx_layout_t src, kvx_layout_t dst, const int32_t *d_runs,
+                             int32_t n_runs, int32_t n_tokens, void *d_ws, size_t ws_bytes,
+                             int32_t *d_status, kvx_stream_t stream);
+
+/* Batch of requests in one plan + one copy launch ([Mooncake] 6.1).  d_reqs: device
+ * kvx_request[n_reqs].  total_tokens must equal the sum of n_tokens.  src / dst may be NULL
+ * if no request uses them.  d_src_slots / d_dst_slots: device int32 arrays of n_src_slots /
+ * n_dst_slots elements.  d_status: device int32[n_reqs + 1]: [1 + q] is request q's code,
+ * [0] the largest of all.  A failing request moves nothing; the others still run. */
+KVX_API kvx_status kvx_batch(kvx_layout_t src, kvx_layout_t dst, const kvx_request *d_reqs,
+                     int32_t n_reqs, int64_t total_tokens, const int32_t *d_src_slots,
+                     int64_t n_src_slots, const int32_t *d_dst_slots, int64_t n_dst_slots,
+                     void *d_buf, size_t buf_bytes, void *d_ws, size_t ws_bytes,
+                     int32_t *d_status, kvx_stream_t stream);
+
+/* Host-index submission ([Mooncake] 6.1 submitTransfer + getTransferStatus): like
+ * kvx_gather / kvx_scatter / kvx_transfer, but the slot lists are host arrays (pinned memory
+ * makes the copy asynchronous) staged into the workspace, and the final status is copied
+ * back into *h_status.  *h_status is valid once the stream has reached this call. */
+KVX_API kvx_status kvx_submit(int32_t op, kvx_layout_t src, const int32_t *h_src_slots,
+                      kvx_layout_t dst, const int32_t *h_dst_slots, int32_t n, void *d_buf,
+                      size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *h_status,
+                      kvx_stream_t stream);
+
+/* ---- two-phase form: the plan (validation + run-length planning) and the copy -------- */
+
+/* Validates the indices and writes the plan into d_ws; the status word(s) get the result.
+ * op is KVX_OP_GATHER, KVX_OP_SCATTER or KVX_OP_TRANSFER; unused side arguments are NULL. */
+KVX_API kvx_status kvx_plan(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, kvx_layout_t dst,
+                    const int32_t *d_dst_slots, int32_t n, void *d_ws, size_t ws_bytes,
+                    int32_t *d_status, kvx_stream_t stream);
+KVX_API kvx_status kvx_plan_runs(int32_t op, kvx_layout_t src, kvx_layout_t dst, const int32_t *d_runs,
+                         int32_t n_runs, int32_t n_tokens, void *d_ws, size_t ws_bytes,
+                         int32_t *d_status, kvx_stream_t stream);
+KVX_API kvx_status kvx_plan_batch(kvx_layout_t src, kvx_layout_t dst, const kvx_request *d_reqs,
+                          int32_t n_reqs, int64_t total_tokens, const int32_t *d_src_slots,
+                          int64_t n_src_slots, const int32_t *d_dst_slots, int64_t n_dst_slots,
+                          size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *d_status,
+                          kvx_stream_t stream);
+
+/* Runs the copy the plan in d_ws describes.  op, layouts, n_tokens (the planned token count:
+ * n, the runs' total, or total_tokens) and, for KVX_OP_BATCH, d_reqs / n_reqs must be those
+ * the plan was made with; the device checks them against the plan and writes
+ * KVX_ERR_INVALID_ARG on a mismatch.  d_status is the array given to the planner; nothing
+ * moves where it holds an error.  A plan may be executed more than once (for instance with
+ * other layouts of the same geometry). */
+KVX_API kvx_status kvx_execute(int32_t op, kvx_layout_t src, kvx_layout_t dst, const kvx_request *d_reqs,
+                       int32_t n_reqs, int64_t n_tokens, void *d_buf, size_t buf_bytes,
+                       const void *d_ws, size_t ws_bytes, int32_t *d_status,
+                       kvx_stream_t stream);
+
+/* Copies the plan's chunks out of the workspace, in plan order, as device int32[4] records
+ * {request, src_index, dst_index, rows}; *d_count (device int64) gets the total, and at most
+ * max_chunks records are written.  n_tokens as for kvx_execute.  For tests and inspection. */
+KVX_API kvx_status kvx_plan_export(const void *d_ws, size_t ws_bytes, int64_t n_tokens,
+                           int32_t *d_chunks, int64_t max_chunks, int64_t *d_count,
+                           kvx_stream_t stream);
+
+/* ---- misc ---------------------------------------------------------------------------- */
+
+KVX_API const char *kvx_status_str(kvx_status status);
+/* The cudaError_t of the last failing CUDA call made by this thread inside libkvx. */
+KVX_API int32_t kvx_last_cuda_error(void);
+/* Library version, major * 10000 + minor * 100 + patch. */
+KVX_API int32_t kvx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVX_H */

@@ -1,0 +1,127 @@
+"""The C ABI on the CPU: the library loads, exports every entry point include/kvx.h declares,
+and rejects bad host-visible arguments before touching CUDA (no GPU is needed for any of
+these: each call returns before its first CUDA call)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from disaggregated_paged_kv_gb300 import build as kbuild
+from disaggregated_paged_kv_gb300 import kvx
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvx.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(kvx.LIB_PATH):
+        kbuild.build()
+    return kvx.lib()
+
+
+def declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^KVX_API\s+[\w\s\*]+?\*?(kvx_\w+)\(", text, re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared()
+    assert len(names) >= 20
+    out = subprocess.run(["nm", "-D", "--defined-only", kvx.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    # the binding covers the same set
+    assert sorted(kvx.exported_names()) == names
+
+
+def test_misc(lib):
+    assert kvx.version() == 100
+    assert kvx.status_str(kvx.OK) == "ok"
+    assert "range" in kvx.status_str(kvx.ERR_OUT_OF_RANGE)
+    ws = kvx.workspace_size(2048, 0)
+    assert ws > 2048 * 16 and ws % 256 == 0
+    assert kvx.workspace_size(kvx.MAX_TOKENS + 1, 0) == 0
+    assert kvx.workspace_size(-1, 0) == 0
+    assert kvx.workspace_size(10, -1) == 0
+
+
+FAKE = 1 << 40  # a 16-byte-aligned address that is never dereferenced on the host
+
+
+def test_layout_validation(lib):
+    L = kvx.Layout(36, 8, 128, kvx.BF16, 65536, base=FAKE, plane_stride=65536 * 2048)
+    assert L.row_bytes == 2048 and L.num_planes == 72
+    L.close()
+    bad = [
+        dict(num_layers=0),
+        dict(num_layers=129),
+        dict(kv_heads=0),
+        dict(dtype=9),
+        dict(num_slots=0),
+        dict(num_slots=2 ** 31),
+        dict(kind=5),
+        dict(base=None),
+        dict(slot_stride=128),  # smaller than a row
+    ]
+    for kw in bad:
+        args = dict(num_layers=2, kv_heads=2, head_dim=64, dtype=kvx.F16, num_slots=100,
+                    base=FAKE, plane_stride=100 * 256)
+        args.update(kw)
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.Layout(**args)
+        assert e.value.code == kvx.ERR_INVALID_ARG, kw
+    for kw in [dict(head_dim=3), dict(base=FAKE + 8), dict(slot_stride=264)]:
+        args = dict(num_layers=2, kv_heads=2, head_dim=64, dtype=kvx.F16, num_slots=100,
+                    base=FAKE, plane_stride=100 * 256)
+        args.update(kw)
+        with pytest.raises(kvx.KvxError) as e:
+            kvx.Layout(**args)
+        assert e.value.code == kvx.ERR_ALIGNMENT, kw
+    with pytest.raises(kvx.KvxError):  # HND: slots must fill whole pages
+        kvx.Layout(2, 2, 64, kvx.F16, 100, kind=kvx.HND_PAGED, page_size=16, base=FAKE,
+                   plane_stride=1 << 20)
+    with pytest.raises(kvx.KvxError) as e:  # HND head vector must be 16-byte aligned
+        kvx.Layout(2, 4, 4, kvx.F16, 32, kind=kvx.HND_PAGED, page_size=16, base=FAKE,
+                   plane_stride=1 << 20)
+    assert e.value.code == kvx.ERR_ALIGNMENT
+    # explicit plane pointers
+    ptrs = [FAKE + (1 << 30) * p for p in range(4)]
+    L = kvx.Layout(2, 2, 64, kvx.F16, 100, plane_ptrs=ptrs)
+    assert L.num_planes == 4
+    with pytest.raises(kvx.KvxError):
+        kvx.Layout(2, 2, 64, kvx.F16, 100, plane_ptrs=ptrs[:3] + [0])
+
+
+def test_call_validation_before_cuda(lib):
+    src = kvx.Layout(2, 2, 64, kvx.F16, 1000, base=FAKE, plane_stride=1000 * 256)
+    dst = kvx.Layout(2, 2, 64, kvx.F16, 1000, base=FAKE * 2, plane_stride=1000 * 256)
+    other = kvx.Layout(3, 2, 64, kvx.F16, 1000, base=FAKE * 3, plane_stride=1000 * 256)
+    WS, ST, SL, BUF = FAKE * 4, FAKE * 5, FAKE * 6, FAKE * 7
+    big = 1 << 30
+    l = kvx.lib()
+    # transfer: mismatched shapes, overlap, null status, negative n
+    assert l.kvx_transfer(src.handle, SL, other.handle, SL, 10, WS, big, ST, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_transfer(src.handle, SL, src.handle, SL, 10, WS, big, ST, None) == kvx.ERR_OVERLAP
+    assert l.kvx_transfer(src.handle, SL, dst.handle, SL, 10, WS, big, None, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_transfer(src.handle, SL, dst.handle, SL, -1, WS, big, ST, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_transfer(src.handle, None, dst.handle, SL, 10, WS, big, ST, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_transfer(src.handle, SL, dst.handle, SL, 10, WS + 16, big, ST, None) == kvx.ERR_NO_WORKSPACE
+    assert l.kvx_transfer(src.handle, SL, dst.handle, SL, 10, WS, 512, ST, None) == kvx.ERR_NO_WORKSPACE
+    assert l.kvx_transfer(None, SL, dst.handle, SL, 10, WS, big, ST, None) == kvx.ERR_INVALID_ARG
+    # gather: buffer checks
+    need = 4 * 10 * 256
+    assert l.kvx_gather(src.handle, SL, 10, None, need, WS, big, ST, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_gather(src.handle, SL, 10, BUF + 4, need, WS, big, ST, None) == kvx.ERR_ALIGNMENT
+    assert l.kvx_gather(src.handle, SL, 10, BUF, need - 16, WS, big, ST, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_gather(src.handle, SL, 10, FAKE + 256, need, WS, big, ST, None) == kvx.ERR_OVERLAP
+    # execute / plan argument checks
+    assert l.kvx_execute(9, src.handle, dst.handle, None, 0, 10, None, 0, WS, big, ST, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_plan(kvx.OP_BATCH, src.handle, SL, dst.handle, SL, 10, WS, big, ST, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_plan_runs(kvx.OP_TRANSFER, src.handle, dst.handle, None, 3, 10, WS, big, ST, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_plan_batch(src.handle, dst.handle, None, 2, 10, SL, 10, SL, 10, 0, WS, big, ST, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_submit(kvx.OP_TRANSFER, src.handle, None, dst.handle, None, 10, None, 0, WS, big, ctypes.c_void_p(0), None) == kvx.ERR_INVALID_ARG
