@@ -299,6 +299,8 @@ bool valid_n(int64_t n) { return n >= 0 && n <= KVX_MAX_TOKENS; }
 
 }  // namespace
 
+void kvx::record_cuda_error(cudaError_t e) { g_last_cuda = (int32_t)e; }
+
 extern "C" {
 
 kvx_status kvx_layout_create(const kvx_layout_desc *d, kvx_layout_t *out) {

@@ -156,5 +156,7 @@ cudaError_t launch_export(const char *ws, WsLayout L, int64_t n_tokens, int32_t 
 // current device, and which variant a call runs.
 int copy_blocks_per_sm(bool linear, int n_tiles);
 bool copy_is_linear(const CopyArgs &a);
+// Records e as this thread's kvx_last_cuda_error().
+void record_cuda_error(cudaError_t e);
 
 }  // namespace kvx

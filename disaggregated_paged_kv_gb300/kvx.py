@@ -39,6 +39,7 @@ MAX_PLANES = 256
 PLAN_TILE = 2048
 MAX_TOKENS = PLAN_TILE * 4096
 CHUNK_BYTES = 8192
+NOALLOC_MAX_TOKENS = 16384
 
 ELEM_BYTES = {F16: 2, BF16: 2, F32: 4, FP8: 1}
 
@@ -96,6 +97,7 @@ _SIGS = {
     "kvx_gather": (_I32, [_VP, _VP, _I32, _VP, _SZ, _VP, _SZ, _VP, _VP]),
     "kvx_scatter": (_I32, [_VP, _VP, _I32, _VP, _SZ, _VP, _SZ, _VP, _VP]),
     "kvx_transfer": (_I32, [_VP, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _VP]),
+    "kvx_transfer_noalloc": (_I32, [_VP, _VP, _VP, _VP, _I32, _VP, _VP]),
     "kvx_gather_runs": (_I32, [_VP, _VP, _I32, _I32, _VP, _SZ, _VP, _SZ, _VP, _VP]),
     "kvx_scatter_runs": (_I32, [_VP, _VP, _I32, _I32, _VP, _SZ, _VP, _SZ, _VP, _VP]),
     "kvx_transfer_runs": (_I32, [_VP, _VP, _VP, _I32, _I32, _VP, _SZ, _VP, _VP]),
@@ -253,6 +255,16 @@ def transfer(src: Layout, src_slots, dst: Layout, dst_slots, n: int, ws, status,
                             _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
                             _stream(stream))
     _check(rc, "kvx_transfer")
+
+
+def transfer_noalloc(src: Layout, src_slots, dst: Layout, dst_slots, n: int, status,
+                     stream=None) -> None:
+    """kvx_transfer without a workspace, for callers that cannot allocate device memory when
+    KV has to move (the planner's scratch is a fixed array inside libkvx; n is at most
+    NOALLOC_MAX_TOKENS, and calls that overlap on the GPU must not share it)."""
+    rc = lib().kvx_transfer_noalloc(_h(src), _ptr(src_slots), _h(dst), _ptr(dst_slots), n,
+                                    _ptr(status), _stream(stream))
+    _check(rc, "kvx_transfer_noalloc")
 
 
 def gather_runs(src: Layout, runs, n_runs: int, n_tokens: int, buf, ws, status, buf_bytes=None,

@@ -237,6 +237,25 @@ KVX_API kvx_status kvx_submit(int32_t op, kvx_layout_t src, const int32_t *h_src
                       size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *h_status,
                       kvx_stream_t stream);
 
+/* Pool-to-pool transfer without a workspace argument.  The pages have no counterpart to this
+ * call: it exists for callers that cannot allocate device memory when KV has to move -- an
+ * engine that reserved nearly all HBM for its KV pool at start-up has none left for a
+ * workspace, and cudaMalloc would synchronise the device between decode steps.  Same
+ * arguments, results and errors as kvx_transfer, except that the planner's scratch is one
+ * fixed array per device inside libkvx:
+ *  - n may be at most KVX_NOALLOC_MAX_TOKENS; a larger n returns KVX_ERR_NO_WORKSPACE with
+ *    nothing enqueued;
+ *  - the array's device address is looked up on the first call made while a device is
+ *    current; make that first call on each device before any stream capture;
+ *  - all calls share the array, so calls whose work overlaps on the GPU (other streams, other
+ *    host threads without ordering) race and may corrupt each other; calls in one stream are
+ *    safe.  Nothing in it needs to be cleared between calls.
+ * It allocates nothing and calls no allocating library routine. */
+#define KVX_NOALLOC_MAX_TOKENS 16384
+KVX_API kvx_status kvx_transfer_noalloc(kvx_layout_t src, const int32_t *d_src_slots,
+                                        kvx_layout_t dst, const int32_t *d_dst_slots, int32_t n,
+                                        int32_t *d_status, kvx_stream_t stream);
+
 /* ---- two-phase form: the plan (validation + run-length planning) and the copy -------- */
 
 /* Validates the indices and writes the plan into d_ws; the status word(s) get the result.
