@@ -382,7 +382,7 @@ def main():
         "gpu_launches": 2 * K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": UNIT,
                      "frac": achieved / hbm, "traffic": profile_traffic(),
-                     "kernel": "copy_kernel<true> (linear rows)",
+                     "kernel": "copy_row_kernel (one warp per 2 KiB row)",
                      "peak_kind": f"{peak_kind} (burst copy)",
                      "achieved_bytes_per_launch": copy_bytes},
     }

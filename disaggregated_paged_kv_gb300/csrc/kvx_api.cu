@@ -5,6 +5,7 @@
 // if it fails; data-dependent checks happen in the planner and end up in the device status
 // word ("穷人版 PD 分离", section "最难的一个问题": the client learns of a failure right away
 // and no half-written KV is left behind).
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -93,6 +94,12 @@ kvx::Side buffer_side(int64_t seg_bytes) {
   return s;
 }
 
+// A pool side whose chunk rows are contiguous (token rows with dense slots); a buffer side
+// (nullptr) always is.
+bool side_linear(const kvx_layout *l, const kvx_layout *shape) {
+  return !l || (l->kind == KVX_NHD && l->slot_stride == shape->row_bytes);
+}
+
 int32_t chunk_rows_for(int64_t row_bytes) {
   int64_t m = kvx::kDefaultChunkBytes / row_bytes;
   if (m < 1) m = 1;
@@ -102,9 +109,13 @@ int32_t chunk_rows_for(int64_t row_bytes) {
 
 struct DeviceInfo {
   int sms = 0;
-  int bps_linear = 0;   // resident copy CTAs per SM, linear-only variant
-  int bps_general = 0;  // resident copy CTAs per SM, general variant
+  int bps[kvx::kNumVariants] = {};        // resident CTAs per SM per copy variant (largest plan)
+  int bps_small[kvx::kNumVariants] = {};  // the same for plans of <= kBulkSmallTiles tiles
+  int bps_fused_linear = 0;               // one-launch path, linear rows
+  int bps_fused_general = 0;              // one-launch path, general placement
 };
+
+std::atomic<int32_t> g_fused_max{KVX_FUSED_MAX_TOKENS};
 
 kvx_status device_info(DeviceInfo *out) {
   static std::mutex mu;
@@ -118,15 +129,23 @@ kvx_status device_info(DeviceInfo *out) {
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e);
-    const int bl = kvx::copy_blocks_per_sm(true, kvx::kMaxTiles);
-    const int bg = kvx::copy_blocks_per_sm(false, kvx::kMaxTiles);
-    if (bl <= 0 || bg <= 0) {
+    DeviceInfo d;
+    d.sms = sms;
+    for (int v = 0; v < kvx::kNumVariants; ++v) {
+      d.bps[v] = kvx::variant_blocks_per_sm((kvx::CopyVariant)v, kvx::kMaxTiles);
+      d.bps_small[v] = kvx::variant_blocks_per_sm((kvx::CopyVariant)v, kvx::kBulkSmallTiles);
+      if (d.bps[v] <= 0 || d.bps_small[v] <= 0) {
+        e = cudaGetLastError();
+        return cuda_fail(e != cudaSuccess ? e : cudaErrorUnknown);
+      }
+    }
+    d.bps_fused_linear = kvx::fused_blocks_per_sm(true);
+    d.bps_fused_general = kvx::fused_blocks_per_sm(false);
+    if (d.bps_fused_linear <= 0 || d.bps_fused_general <= 0) {
       e = cudaGetLastError();
       return cuda_fail(e != cudaSuccess ? e : cudaErrorUnknown);
     }
-    cache[dev].sms = sms;
-    cache[dev].bps_linear = bl;
-    cache[dev].bps_general = bg;
+    cache[dev] = d;
   }
   *out = cache[dev];
   return KVX_OK;
@@ -257,13 +276,8 @@ kvx_status enqueue_plan(const Call &c, kvx::PlanArgs &a, cudaStream_t s) {
   return e == cudaSuccess ? KVX_OK : cuda_fail(e);
 }
 
-kvx_status enqueue_copy(const Call &c, const kvx_request *d_reqs, void *d_buf, const void *d_ws,
-                        int32_t *d_status, cudaStream_t s) {
-  if (c.n_tokens == 0) return KVX_OK;
-  DeviceInfo di;
-  kvx_status st = device_info(&di);
-  if (st != KVX_OK) return st;
-  static thread_local kvx::CopyArgs a;  // ~4 KiB of plane pointers: keep it off the stack
+void fill_copy_args(kvx::CopyArgs &a, const Call &c, const kvx_request *d_reqs, void *d_buf,
+                    const void *d_ws, int32_t *d_status) {
   std::memset(&a, 0, sizeof(a));
   a.mode = c.mode;
   a.op = c.op;
@@ -285,13 +299,47 @@ kvx_status enqueue_copy(const Call &c, const kvx_request *d_reqs, void *d_buf, c
     a.src_planes[p] = c.src ? reinterpret_cast<const char *>(c.src->plane[p]) : nullptr;
     a.dst_planes[p] = c.dst ? reinterpret_cast<char *>(c.dst->plane[p]) : nullptr;
   }
-  const int64_t warps_needed = (int64_t)c.shape->planes * c.n_tokens;
-  const int64_t wpb = kvx::kCopyThreads / 32;
-  int64_t grid = (int64_t)di.sms * (kvx::copy_is_linear(a) ? di.bps_linear : di.bps_general);
-  const int64_t need = (warps_needed + wpb - 1) / wpb;
+}
+
+kvx_status enqueue_copy(const Call &c, const kvx_request *d_reqs, void *d_buf, const void *d_ws,
+                        int32_t *d_status, cudaStream_t s, const int32_t *spec_src = nullptr,
+                        const int32_t *spec_dst = nullptr) {
+  if (c.n_tokens == 0) return KVX_OK;
+  DeviceInfo di;
+  kvx_status st = device_info(&di);
+  if (st != KVX_OK) return st;
+  static thread_local kvx::CopyArgs a;  // ~4 KiB of plane pointers: keep it off the stack
+  fill_copy_args(a, c, d_reqs, d_buf, d_ws, d_status);
+  if (kvx::copy_variant(a) == kvx::kVariantRow) {
+    a.spec_src = spec_src;
+    a.spec_dst = spec_dst;
+    const cudaError_t e = kvx::launch_copy(a, (int)kvx::row_grid(c.n_tokens, c.shape->planes), s);
+    return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+  }
+  // one warp (register paths) or one thread (bulk path) per work item; at most n*P items
+  const int64_t items = (int64_t)c.shape->planes * c.n_tokens;
+  const kvx::CopyVariant v = kvx::copy_variant(a);
+  const int64_t per_cta = v == kvx::kVariantBulk ? kvx::variant_threads(v) : kvx::kCopyThreads / 32;
+  const bool small = kvx::num_tiles(c.n_tokens) <= kvx::kBulkSmallTiles;
+  int64_t grid = (int64_t)di.sms * (small ? di.bps_small[v] : di.bps[v]);
+  const int64_t need = (items + per_cta - 1) / per_cta;
   if (need < grid) grid = need;
   if (grid < 1) grid = 1;
   cudaError_t e = kvx::launch_copy(a, (int)grid, s);
+  return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+}
+
+// The one-launch path of a single request (see kvx_set_fused_max_tokens).
+kvx_status enqueue_fused(const Call &c, const int32_t *d_src, const int32_t *d_dst, void *d_buf,
+                         int32_t *d_status, cudaStream_t s) {
+  DeviceInfo di;
+  kvx_status st = device_info(&di);
+  if (st != KVX_OK) return st;
+  static thread_local kvx::CopyArgs a;
+  fill_copy_args(a, c, nullptr, d_buf, nullptr, d_status);
+  const int bps = kvx::copy_is_linear(a) ? di.bps_fused_linear : di.bps_fused_general;
+  cudaError_t e = kvx::launch_fused(a, d_src, d_dst, (int32_t)c.n_tokens,
+                                    chunk_rows_for(c.shape->row_bytes), di.sms, bps, s);
   return e == cudaSuccess ? KVX_OK : cuda_fail(e);
 }
 
@@ -501,46 +549,58 @@ kvx_status kvx_execute(int32_t op, kvx_layout_t src, kvx_layout_t dst, const kvx
   return enqueue_copy(c, d_reqs, d_buf, d_ws, d_status, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// gather / scatter / transfer of one slot-list request: one launch up to the fused limit,
+// otherwise the planner + copy launches.
+static kvx_status run_slots(int32_t op, kvx_layout_t src, const int32_t *d_src_slots,
+                            kvx_layout_t dst, const int32_t *d_dst_slots, int32_t n, void *d_buf,
+                            size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *d_status,
+                            kvx_stream_t stream) {
+  if (!valid_n(n)) return KVX_ERR_INVALID_ARG;
+  Call c;
+  c.op = op;
+  c.n_tokens = n;
+  kvx_status st = bind_layouts(c, src, dst);
+  if (st == KVX_OK) st = check_buffer(c, d_buf, buf_bytes);
+  if (st != KVX_OK) return st;
+  // Rows of >= KVX_CHUNK_BYTES on linear layouts take the planner + row kernel (the row kernel
+  // overlaps the planner); other requests of up to the fused limit take the one-launch path.
+  const bool row_path = chunk_rows_for(c.shape->row_bytes) == 1 && side_linear(c.src, c.shape) &&
+                        side_linear(c.dst, c.shape);
+  if (n == 0 || row_path || n > g_fused_max.load(std::memory_order_relaxed)) {
+    st = kvx_plan(op, src, d_src_slots, dst, d_dst_slots, n, d_ws, ws_bytes, d_status, stream);
+    if (st != KVX_OK || n == 0) return st;
+    // the copy may read the slot lists itself (see CopyArgs::spec_src)
+    return enqueue_copy(c, nullptr, d_buf, d_ws, d_status, reinterpret_cast<cudaStream_t>(stream),
+                        c.src ? d_src_slots : nullptr, c.dst ? d_dst_slots : nullptr);
+  }
+  // the same host checks as kvx_plan
+  if (!d_status || !aligned(d_status, 4)) return KVX_ERR_INVALID_ARG;
+  if (c.src && (!d_src_slots || !aligned(d_src_slots, 4))) return KVX_ERR_INVALID_ARG;
+  if (c.dst && (!d_dst_slots || !aligned(d_dst_slots, 4))) return KVX_ERR_INVALID_ARG;
+  if ((st = check_ws(d_ws, ws_bytes, kvx::ws_layout(n, 0, false))) != KVX_OK) return st;
+  return enqueue_fused(c, c.src ? d_src_slots : nullptr, c.dst ? d_dst_slots : nullptr, d_buf,
+                       d_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
 kvx_status kvx_gather(kvx_layout_t src, const int32_t *d_src_slots, int32_t n, void *d_buf,
                       size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *d_status,
                       kvx_stream_t stream) {
-  Call c;
-  c.op = KVX_OP_GATHER;
-  c.n_tokens = n;
-  kvx_status st = bind_layouts(c, src, nullptr);
-  if (st == KVX_OK && valid_n(n)) st = check_buffer(c, d_buf, buf_bytes);
-  if (st != KVX_OK) return st;
-  st = kvx_plan(KVX_OP_GATHER, src, d_src_slots, nullptr, nullptr, n, d_ws, ws_bytes, d_status,
-                stream);
-  if (st != KVX_OK) return st;
-  return kvx_execute(KVX_OP_GATHER, src, nullptr, nullptr, 0, n, d_buf, buf_bytes, d_ws,
-                     ws_bytes, d_status, stream);
+  return run_slots(KVX_OP_GATHER, src, d_src_slots, nullptr, nullptr, n, d_buf, buf_bytes, d_ws,
+                   ws_bytes, d_status, stream);
 }
 
 kvx_status kvx_scatter(kvx_layout_t dst, const int32_t *d_dst_slots, int32_t n,
                        const void *d_buf, size_t buf_bytes, void *d_ws, size_t ws_bytes,
                        int32_t *d_status, kvx_stream_t stream) {
-  Call c;
-  c.op = KVX_OP_SCATTER;
-  c.n_tokens = n;
-  kvx_status st = bind_layouts(c, nullptr, dst);
-  if (st == KVX_OK && valid_n(n)) st = check_buffer(c, d_buf, buf_bytes);
-  if (st != KVX_OK) return st;
-  st = kvx_plan(KVX_OP_SCATTER, nullptr, nullptr, dst, d_dst_slots, n, d_ws, ws_bytes, d_status,
-                stream);
-  if (st != KVX_OK) return st;
-  return kvx_execute(KVX_OP_SCATTER, nullptr, dst, nullptr, 0, n, const_cast<void *>(d_buf),
-                     buf_bytes, d_ws, ws_bytes, d_status, stream);
+  return run_slots(KVX_OP_SCATTER, nullptr, nullptr, dst, d_dst_slots, n,
+                   const_cast<void *>(d_buf), buf_bytes, d_ws, ws_bytes, d_status, stream);
 }
 
 kvx_status kvx_transfer(kvx_layout_t src, const int32_t *d_src_slots, kvx_layout_t dst,
                         const int32_t *d_dst_slots, int32_t n, void *d_ws, size_t ws_bytes,
                         int32_t *d_status, kvx_stream_t stream) {
-  kvx_status st = kvx_plan(KVX_OP_TRANSFER, src, d_src_slots, dst, d_dst_slots, n, d_ws,
-                           ws_bytes, d_status, stream);
-  if (st != KVX_OK) return st;
-  return kvx_execute(KVX_OP_TRANSFER, src, dst, nullptr, 0, n, nullptr, 0, d_ws, ws_bytes,
-                     d_status, stream);
+  return run_slots(KVX_OP_TRANSFER, src, d_src_slots, dst, d_dst_slots, n, nullptr, 0, d_ws,
+                   ws_bytes, d_status, stream);
 }
 
 kvx_status kvx_gather_runs(kvx_layout_t src, const int32_t *d_runs, int32_t n_runs,
@@ -632,10 +692,8 @@ kvx_status kvx_submit(int32_t op, kvx_layout_t src, const int32_t *h_src_slots,
     e = cudaMemcpyAsync(d_dst, h_dst_slots, sizeof(int32_t) * (size_t)n, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  st = kvx_plan(op, src, c.src ? d_src : nullptr, dst, c.dst ? d_dst : nullptr, n, d_ws,
-                ws_bytes, d_st, stream);
-  if (st != KVX_OK) return st;
-  st = kvx_execute(op, src, dst, nullptr, 0, n, d_buf, buf_bytes, d_ws, ws_bytes, d_st, stream);
+  st = run_slots(op, src, c.src ? d_src : nullptr, dst, c.dst ? d_dst : nullptr, n, d_buf,
+                 buf_bytes, d_ws, ws_bytes, d_st, stream);
   if (st != KVX_OK) return st;
   e = cudaMemcpyAsync(h_status, d_st, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
   return e == cudaSuccess ? KVX_OK : cuda_fail(e);
@@ -671,6 +729,14 @@ const char *kvx_status_str(kvx_status s) {
 }
 
 int32_t kvx_last_cuda_error(void) { return g_last_cuda; }
+
+kvx_status kvx_set_fused_max_tokens(int32_t max_tokens) {
+  if (max_tokens < 0 || max_tokens > KVX_FUSED_MAX_TOKENS) return KVX_ERR_INVALID_ARG;
+  g_fused_max.store(max_tokens, std::memory_order_relaxed);
+  return KVX_OK;
+}
+
+int32_t kvx_get_fused_max_tokens(void) { return g_fused_max.load(std::memory_order_relaxed); }
 
 int32_t kvx_version(void) { return 100; }
 

@@ -17,93 +17,14 @@
 // (row j, head h, piece w) = (v / vps / H, v / vps % H, v % vps) on each side, vps = 16-byte
 // pieces per head vector; on an HND side that turns [head][token] into [token][head], which
 // is the fused permute of "mini-infer系统实战-18-PD 解耦" (KV 序列化格式选择).
-#include "kvx_internal.cuh"
+#include <atomic>
+
+#include "kvx_copy_ops.cuh"
 
 namespace kvx {
 namespace {
 
-constexpr int kUnroll = 4;
-
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-__device__ __forceinline__ uint4 ld_stream(const void *p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
-__device__ __forceinline__ void st_stream(void *p, const uint4 &v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
-struct Addr {
-  const char *base;  // row 0, head 0
-  int64_t row;       // bytes between consecutive rows of the chunk
-  int64_t head;      // bytes between consecutive head vectors of a row
-};
-
-// Address of the chunk's first row on one side.  idx: slot (pool) or row (buffer).  The
-// side's geometry stays in the kernel's parameter space (read by reference, not copied).
-__device__ __forceinline__ Addr side_addr(const Side &s, bool is_pool, const char *plane,
-                                          int64_t idx, const char *buf_plane, int32_t row_bytes) {
-  Addr a;
-  if (!is_pool) {
-    a.base = buf_plane + idx * row_bytes;
-    a.row = row_bytes;
-    a.head = s.seg_bytes;
-  } else if (s.hnd) {
-    const int64_t page = idx / s.page_size, off = idx - page * s.page_size;
-    a.base = plane + page * s.page_bytes + off * s.seg_bytes;
-    a.row = s.seg_bytes;
-    a.head = (int64_t)s.page_size * s.seg_bytes;
-  } else {
-    a.base = plane + idx * s.slot_stride;
-    a.row = s.slot_stride;
-    a.head = s.seg_bytes;
-  }
-  return a;
-}
-
-__device__ __forceinline__ void copy_linear(const char *src, char *dst, int32_t nvec, int lane) {
-  const uint4 *s = reinterpret_cast<const uint4 *>(src);
-  uint4 *d = reinterpret_cast<uint4 *>(dst);
-  for (int32_t v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
-    uint4 r[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (v0 + 32 * u < nvec) r[u] = ld_stream(s + v0 + 32 * u);
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (v0 + 32 * u < nvec) st_stream(d + v0 + 32 * u, r[u]);
-  }
-}
-
-__device__ __forceinline__ int64_t vec_off(const Addr &a, int32_t v, int32_t vps, int32_t heads) {
-  const int32_t q = v / vps, w = v - q * vps;
-  const int32_t j = q / heads, h = q - j * heads;
-  return j * a.row + h * a.head + (int64_t)w * 16;
-}
-
-__device__ __forceinline__ void copy_pieces(const Addr &s, const Addr &d, int32_t nvec,
-                                            int32_t vps, int32_t heads, int lane) {
-  for (int32_t v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
-    uint4 r[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int32_t v = v0 + 32 * u;
-      if (v < nvec) r[u] = ld_stream(s.base + vec_off(s, v, vps, heads));
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int32_t v = v0 + 32 * u;
-      if (v < nvec) st_stream(const_cast<char *>(d.base) + vec_off(d, v, vps, heads), r[u]);
-    }
-  }
-}
+using namespace ops;
 
 __device__ __forceinline__ bool header_matches(const CopyArgs &a) {
   const PlanHeader *h = reinterpret_cast<const PlanHeader *>(a.ws + a.L.header_off);
@@ -119,35 +40,29 @@ __device__ __forceinline__ bool header_matches(const CopyArgs &a) {
          h->src_num_slots == a.src.num_slots && h->dst_num_slots == a.dst.num_slots;
 }
 
-// kLinear: the host has seen that every chunk is linear on both sides (token-row pools with
-// dense rows, and buffers), so the per-vector placement path is compiled out.
-template <bool kLinear>
-__global__ void __launch_bounds__(kCopyThreads, 4) copy_kernel(const __grid_constant__ CopyArgs a) {
-  extern __shared__ int32_t s_tile_base[];  // n_tiles + 1 entries
-  __shared__ int32_t s_warp[kCopyThreads / 32];
-  __shared__ int32_t s_ok;
-
-  pdl_wait();  // the planner's tables must be complete
-
+// Common start of every copy kernel: checks the plan header (and, for single calls, the
+// status word) and turns the per-tile chunk counts into each tile's first chunk in shared
+// memory.  Returns the plan's chunk count, or -1 if this CTA must not move anything.
+template <int THREADS>
+__device__ __forceinline__ int32_t copy_prologue(const CopyArgs &a, int32_t *s_tile_base,
+                                                 int32_t *s_warp, int32_t *s_ok) {
+  constexpr int kWarps = THREADS / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     int32_t ok = header_matches(a) ? 1 : 0;
     if (!ok && blockIdx.x == 0) atomicMax(&a.status[0], (int32_t)KVX_ERR_INVALID_ARG);
     if (ok && a.mode != kModeBatch && a.status[0] != KVX_OK) ok = 0;
-    s_ok = ok;
+    *s_ok = ok;
   }
   __syncthreads();
-  if (!s_ok) return;
-
-  // chunk counts of every tile -> first chunk of every tile
+  if (!*s_ok) return -1;
   const int32_t nt = (int32_t)num_tiles(a.n_tokens);
   const int32_t *tiles = reinterpret_cast<const int32_t *>(a.ws + a.L.tiles_off);
   int32_t carry = 0;
-  for (int32_t base = 0; base < nt; base += kCopyThreads) {
+  for (int32_t base = 0; base < nt; base += THREADS) {
     const int32_t t = base + tid;
     int32_t v = t < nt ? tiles[t] : 0;
     v = v < 0 ? 0 : (v > kTile ? kTile : v);  // never index past a tile's table
-    // block exclusive scan
     int32_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -157,7 +72,7 @@ __global__ void __launch_bounds__(kCopyThreads, 4) copy_kernel(const __grid_cons
     if (lane == 31) s_warp[warp] = x;
     __syncthreads();
     int32_t wex = 0, tot = 0;
-    for (int i = 0; i < kCopyThreads / 32; ++i) {
+    for (int i = 0; i < kWarps; ++i) {
       if (i < warp) wex += s_warp[i];
       tot += s_warp[i];
     }
@@ -167,66 +82,300 @@ __global__ void __launch_bounds__(kCopyThreads, 4) copy_kernel(const __grid_cons
   }
   if (tid == 0) s_tile_base[nt] = carry;
   __syncthreads();
+  return carry;
+}
 
-  const uint32_t total = (uint32_t)carry * (uint32_t)a.planes;
+// Work item w = (chunk w / P, plane w % P): both sides' addresses and the row count.  False
+// if the item belongs to a failed request of a batch.
+__device__ __forceinline__ bool decode_item(const CopyArgs &a, uint32_t w,
+                                            const int32_t *s_tile_base, int32_t nt, Addr &sa,
+                                            Addr &da, int32_t &rows) {
+  const uint32_t c = w / (uint32_t)a.planes;
+  const int32_t p = (int32_t)(w - c * (uint32_t)a.planes);
+  int32_t lo = 0, hi = nt;  // tile holding chunk c
+  while (hi - lo > 1) {
+    const int32_t mid = (lo + hi) >> 1;
+    if ((uint32_t)s_tile_base[mid] <= c) lo = mid; else hi = mid;
+  }
   const Chunk *chunks = reinterpret_cast<const Chunk *>(a.ws + a.L.chunks_off);
+  const Chunk ch = chunks[(int64_t)lo * kTile + (c - (uint32_t)s_tile_base[lo])];
+  int32_t op = a.op;
+  const char *bufp = a.buf;
+  int64_t nreq = a.n_tokens;
+  bool src_pool = a.src.is_pool, dst_pool = a.dst.is_pool;
+  if (a.mode == kModeBatch) {
+    if (a.status[1 + ch.req] != KVX_OK) return false;
+    const kvx_request rq = a.reqs[ch.req];
+    op = rq.op;
+    bufp = a.buf + rq.buf_off;
+    nreq = rq.n_tokens;
+    src_pool = (op == KVX_OP_GATHER || op == KVX_OP_TRANSFER);
+    dst_pool = (op == KVX_OP_SCATTER || op == KVX_OP_TRANSFER);
+  }
   const int32_t R = a.row_bytes;
-  const int32_t vps = a.seg_bytes >> 4;
-  const int32_t *st = a.status;
-  const uint32_t nwarps = gridDim.x * (kCopyThreads / 32);
+  const char *buf_plane = bufp + (int64_t)p * nreq * R;
+  sa = side_addr(a.src, src_pool, a.src_planes[p], ch.src, buf_plane, R);
+  da = side_addr(a.dst, dst_pool, a.dst_planes[p], ch.dst, buf_plane, R);
+  rows = ch.rows;
+  return true;
+}
 
+// Register path: one warp per work item.  kLinear: the host has seen that every chunk is
+// linear on both sides (token-row pools with dense rows, and buffers), so the per-vector
+// placement path is compiled out.
+template <bool kLinear>
+__global__ void __launch_bounds__(kCopyThreads, 4) copy_kernel(const __grid_constant__ CopyArgs a) {
+  extern __shared__ int32_t s_tile_base[];  // n_tiles + 1 entries
+  __shared__ int32_t s_warp[kCopyThreads / 32];
+  __shared__ int32_t s_ok;
+
+  pdl_wait();  // the planner's tables must be complete
+  const int32_t C = copy_prologue<kCopyThreads>(a, s_tile_base, s_warp, &s_ok);
+  if (C < 0) return;
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int32_t nt = (int32_t)num_tiles(a.n_tokens);
+  const uint32_t total = (uint32_t)C * (uint32_t)a.planes;
+  const int32_t R = a.row_bytes;
+  const uint32_t nwarps = gridDim.x * (kCopyThreads / 32);
   for (uint32_t w = blockIdx.x * (kCopyThreads / 32) + warp; w < total; w += nwarps) {
-    const uint32_t c = w / (uint32_t)a.planes;
-    const int32_t p = (int32_t)(w - c * (uint32_t)a.planes);
-    int32_t lo = 0, hi = nt;  // tile holding chunk c
+    Addr sa, da;
+    int32_t rows;
+    if (!decode_item(a, w, s_tile_base, nt, sa, da, rows)) continue;
+    const int32_t nvec = rows * (R >> 4);
+    if (kLinear) {
+      copy_linear(sa.base, const_cast<char *>(da.base), nvec, lane);
+    } else {
+      const bool linear = sa.head == a.seg_bytes && da.head == a.seg_bytes &&
+                          (rows == 1 || (sa.row == R && da.row == R));
+      if (linear)
+        copy_linear(sa.base, const_cast<char *>(da.base), nvec, lane);
+      else
+        copy_pieces(sa, da, nvec, a.seg_bytes >> 4, a.heads, lane);
+    }
+  }
+}
+
+// Lean register path for the common case: one request (gather, scatter or transfer, from a
+// slot list or a run list) whose chunks are all linear.  Only base pointers are kept per side
+// (no row / head strides, no batch records), so the kernel fits in 32 registers and an SM holds
+// 8 CTAs = 64 warps: twice the 16-byte loads in flight of the general kernel.
+__device__ __forceinline__ const char *lin_addr(const Side &s, bool pool, const char *plane,
+                                                int32_t idx, const char *buf_plane,
+                                                int32_t row_bytes) {
+  return pool ? plane + (int64_t)idx * s.slot_stride : buf_plane + (int64_t)idx * row_bytes;
+}
+
+__global__ void __launch_bounds__(kCopyThreads, 8)
+    copy_lean_kernel(const __grid_constant__ CopyArgs a) {
+  extern __shared__ int32_t s_tile_base[];  // n_tiles + 1 entries
+  __shared__ int32_t s_warp[kCopyThreads / 32];
+  __shared__ int32_t s_ok;
+
+  pdl_wait();
+  const int32_t C = copy_prologue<kCopyThreads>(a, s_tile_base, s_warp, &s_ok);
+  if (C < 0) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int32_t nt = (int32_t)num_tiles(a.n_tokens);
+  const uint32_t P = (uint32_t)a.planes;
+  const uint32_t total = (uint32_t)C * P;
+  const int32_t R = a.row_bytes;
+  const bool sp = a.src.is_pool != 0, dp = a.dst.is_pool != 0;
+  const Chunk *chunks = reinterpret_cast<const Chunk *>(a.ws + a.L.chunks_off);
+  const uint32_t nwarps = gridDim.x * (kCopyThreads / 32);
+  for (uint32_t w = blockIdx.x * (kCopyThreads / 32) + warp; w < total; w += nwarps) {
+    const uint32_t c = w / P;
+    const int32_t p = (int32_t)(w - c * P);
+    int32_t lo = 0, hi = nt;
     while (hi - lo > 1) {
       const int32_t mid = (lo + hi) >> 1;
       if ((uint32_t)s_tile_base[mid] <= c) lo = mid; else hi = mid;
     }
     const Chunk ch = chunks[(int64_t)lo * kTile + (c - (uint32_t)s_tile_base[lo])];
+    const char *buf_plane = a.buf + (int64_t)p * a.n_tokens * R;
+    const char *src = lin_addr(a.src, sp, a.src_planes[p], ch.src, buf_plane, R);
+    char *dst = const_cast<char *>(lin_addr(a.dst, dp, a.dst_planes[p], ch.dst, buf_plane, R));
+    copy_linear(src, dst, ch.rows * (R >> 4), lane);
+  }
+}
 
-    int32_t op = a.op;
-    const char *bufp = a.buf;
-    int64_t nreq = a.n_tokens;
-    if (a.mode == kModeBatch) {
-      if (st[1 + ch.req] != KVX_OK) continue;
-      const kvx_request rq = a.reqs[ch.req];
-      op = rq.op;
-      bufp = a.buf + rq.buf_off;
-      nreq = rq.n_tokens;
+// Row path: one request, linear rows of >= KVX_CHUNK_BYTES, so the plan is one chunk per
+// token.  Non-persistent: the grid holds one warp per (token, plane) row, token-major, and
+// the hardware keeps every SM full of short-lived warps (25-32 registers, 64 warps per SM).
+// With the slot lists at hand (one-shot calls) a warp range-checks its own row and issues its
+// loads before griddepcontrol.wait, so the planner runs under the first wave of loads; the
+// stores wait for the planner's verdict, which keeps the move all-or-nothing.
+__global__ void __launch_bounds__(kCopyThreads, 8) copy_row_kernel(const __grid_constant__ CopyArgs a) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t w = blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
+  const uint32_t P = (uint32_t)a.planes;
+  const uint32_t t = w / P;
+  const int32_t p = (int32_t)(w - t * P);
+  if (t >= (uint32_t)a.n_tokens) return;
+  const int32_t R = a.row_bytes;
+  const bool sp = a.src.is_pool != 0, dp = a.dst.is_pool != 0;
+  const bool spec = a.spec_src != nullptr || a.spec_dst != nullptr;
+  int32_t s, d;
+  bool ok;
+  if (spec) {
+    s = sp ? a.spec_src[t] : (int32_t)t;
+    d = dp ? a.spec_dst[t] : (int32_t)t;
+    ok = (!sp || (s >= 0 && (int64_t)s < a.src.num_slots)) &&
+         (!dp || (d >= 0 && (int64_t)d < a.dst.num_slots));
+  } else {
+    pdl_wait();
+    ok = header_matches(a);
+    if (!ok) {
+      if (w == 0 && lane == 0) atomicMax(&a.status[0], (int32_t)KVX_ERR_INVALID_ARG);
+      return;
     }
-    bool src_pool = a.src.is_pool, dst_pool = a.dst.is_pool;
-    if (a.mode == kModeBatch) {
-      src_pool = (op == KVX_OP_GATHER || op == KVX_OP_TRANSFER);
-      dst_pool = (op == KVX_OP_SCATTER || op == KVX_OP_TRANSFER);
-    }
-    const char *buf_plane = bufp + (int64_t)p * nreq * R;
-    const Addr sa = side_addr(a.src, src_pool, a.src_planes[p], ch.src, buf_plane, R);
-    const Addr da = side_addr(a.dst, dst_pool, a.dst_planes[p], ch.dst, buf_plane, R);
-    const int32_t nvec = ch.rows * (R >> 4);
-    if (kLinear) {
-      copy_linear(sa.base, const_cast<char *>(da.base), nvec, lane);
-    } else {
-      const bool linear = sa.head == a.seg_bytes && da.head == a.seg_bytes &&
-                          (ch.rows == 1 || (sa.row == R && da.row == R));
-      if (linear)
-        copy_linear(sa.base, const_cast<char *>(da.base), nvec, lane);
-      else
-        copy_pieces(sa, da, nvec, vps, a.heads, lane);
+    if (a.status[0] != KVX_OK) return;
+    const Chunk ch = reinterpret_cast<const Chunk *>(a.ws + a.L.chunks_off)[t];
+    s = ch.src;
+    d = ch.dst;
+  }
+  const char *buf_plane = a.buf + (int64_t)p * a.n_tokens * R;
+  const uint4 *src = reinterpret_cast<const uint4 *>(lin_addr(a.src, sp, a.src_planes[p], s, buf_plane, R));
+  uint4 *dst = reinterpret_cast<uint4 *>(const_cast<char *>(lin_addr(a.dst, dp, a.dst_planes[p], d, buf_plane, R)));
+  const int32_t nv = R >> 4;
+  uint4 r[kUnroll];
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u)
+    if (ok && lane + 32 * u < nv) r[u] = ld_stream(src + lane + 32 * u);
+  if (spec) {
+    pdl_wait();  // the planner has checked every index of the request
+    if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK) return;
+  }
+  if (!ok) return;
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u)
+    if (lane + 32 * u < nv) st_stream(dst + lane + 32 * u, r[u]);
+  if (nv > 32 * kUnroll)  // rows longer than 2 KiB: the rest in the ordinary loop
+    copy_linear(reinterpret_cast<const char *>(src + 32 * kUnroll),
+                reinterpret_cast<char *>(dst + 32 * kUnroll), nv - 32 * kUnroll, lane);
+}
+
+// ---- bulk (TMA) path ----------------------------------------------------------------------
+// For linear chunks only.  Every thread owns one kBulkStage-byte shared-memory stage and one
+// mbarrier: cp.async.bulk global -> shared (completion counted in bytes on the mbarrier), then
+// cp.async.bulk shared -> global, and the stage is reused once that store has read it.  Data
+// never passes through registers, so an SM keeps as many 2 KiB moves in flight as it has
+// stages.  Waits are bounded by %globaltimer: a wait that exceeds kWaitLimitNs (never expected)
+// sets KVX_ERR_TIMEOUT, drains this thread's transfers and ends the thread.
+
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.b32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return false;
+}
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
+                                          uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_store(void *gdst, const void *smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_u32(smem_src)), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+template <int kThreads, int kStage>
+__global__ void __launch_bounds__(kThreads) copy_bulk_kernel(const __grid_constant__ CopyArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem[];  // stages | mbarriers | tile bases
+  __shared__ int32_t s_warp[kThreads / 32];
+  __shared__ int32_t s_ok;
+  unsigned char *stage = smem + threadIdx.x * kStage;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kThreads * kStage) + threadIdx.x;
+  int32_t *s_tile_base = reinterpret_cast<int32_t *>(smem + kThreads * kStage + 8 * kThreads);
+
+  pdl_wait();
+  const int32_t C = copy_prologue<kThreads>(a, s_tile_base, s_warp, &s_ok);
+  if (C < 0) return;
+  mbar_init(bar);
+
+  const int32_t nt = (int32_t)num_tiles(a.n_tokens);
+  const uint32_t total = (uint32_t)C * (uint32_t)a.planes;
+  const uint32_t R = (uint32_t)a.row_bytes;
+  uint32_t parity = 0;
+  bool failed = false;
+  for (uint32_t w = blockIdx.x * kThreads + threadIdx.x; w < total && !failed;
+       w += gridDim.x * kThreads) {
+    Addr sa, da;
+    int32_t rows;
+    if (!decode_item(a, w, s_tile_base, nt, sa, da, rows)) continue;
+    const uint32_t bytes = (uint32_t)rows * R;
+    for (uint32_t off = 0; off < bytes; off += kStage) {
+      const uint32_t n = bytes - off < (uint32_t)kStage ? bytes - off : (uint32_t)kStage;
+      bulk_wait_read_all();  // the previous store has finished reading this stage
+      mbar_expect_tx(bar, n);
+      bulk_load(stage, sa.base + off, n, bar);
+      if (!mbar_wait_bounded(bar, parity)) {
+        failed = true;
+        break;
+      }
+      parity ^= 1u;
+      bulk_store(const_cast<char *>(da.base) + off, stage, n);
     }
   }
+  if (failed) {
+    atomicMax(&a.status[0], (int32_t)KVX_ERR_TIMEOUT);
+    (void)mbar_wait_bounded(bar, parity);  // let the outstanding load land before leaving
+  }
+  bulk_wait_all();  // every store complete before the kernel ends
+}
+
+constexpr int kBulkThreads = kBulkThreadsPerCta;
+constexpr int kBulkStage = 2048;
+
+size_t bulk_smem_bytes(int32_t n_tiles) {
+  return (size_t)kBulkThreads * kBulkStage + 8 * kBulkThreads + 4 * (size_t)(n_tiles + 1);
 }
 
 }  // namespace
 
-int copy_blocks_per_sm(bool linear, int n_tiles) {
-  int nb = 0;
-  const size_t smem = sizeof(int32_t) * (size_t)(n_tiles + 1);
-  const cudaError_t e =
-      linear ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, copy_kernel<true>, kCopyThreads, smem)
-             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, copy_kernel<false>, kCopyThreads, smem);
-  return e == cudaSuccess ? nb : 0;
-}
+std::atomic<int32_t> g_engine{KVX_ENGINE_AUTO};
 
 bool side_is_linear(const Side &s, int32_t row_bytes) {
   return !s.is_pool || (!s.hnd && s.slot_stride == row_bytes);
@@ -240,22 +389,65 @@ bool copy_is_linear(const CopyArgs &a) {
   return side_is_linear(a.src, a.row_bytes) && side_is_linear(a.dst, a.row_bytes);
 }
 
+CopyVariant copy_variant(const CopyArgs &a) {
+  if (!copy_is_linear(a)) return kVariantGeneral;
+  if (g_engine.load(std::memory_order_relaxed) == KVX_ENGINE_BULK) return kVariantBulk;
+  if (a.mode == kModeBatch) return kVariantLinear;
+  return a.chunk_rows == 1 ? kVariantRow : kVariantLean;
+}
+
+int64_t row_grid(int64_t n_tokens, int32_t planes) {
+  const int64_t warps = n_tokens * planes, wpb = kCopyThreads / 32;
+  return (warps + wpb - 1) / wpb;
+}
+
+bool use_bulk(const CopyArgs &a) { return copy_variant(a) == kVariantBulk; }
+
+int variant_threads(CopyVariant v) { return v == kVariantBulk ? kBulkThreads : kCopyThreads; }
+
+size_t variant_smem(CopyVariant v, int32_t n_tiles) {
+  if (v == kVariantRow) return 0;
+  return v == kVariantBulk ? bulk_smem_bytes(n_tiles) : sizeof(int32_t) * (size_t)(n_tiles + 1);
+}
+
+const void *variant_fn(CopyVariant v) {
+  switch (v) {
+    case kVariantLean: return reinterpret_cast<const void *>(copy_lean_kernel);
+    case kVariantLinear: return reinterpret_cast<const void *>(copy_kernel<true>);
+    case kVariantGeneral: return reinterpret_cast<const void *>(copy_kernel<false>);
+    case kVariantRow: return reinterpret_cast<const void *>(copy_row_kernel);
+    default: return reinterpret_cast<const void *>(copy_bulk_kernel<kBulkThreads, kBulkStage>);
+  }
+}
+
+int variant_blocks_per_sm(CopyVariant v, int32_t n_tiles) {
+  const void *fn = variant_fn(v);
+  if (v == kVariantBulk &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)bulk_smem_bytes(kMaxTiles)) != cudaSuccess)
+    return 0;
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, variant_threads(v),
+                                                    variant_smem(v, n_tiles)) != cudaSuccess)
+    return 0;
+  return nb;
+}
+
 cudaError_t launch_copy(const CopyArgs &a, int grid, cudaStream_t s) {
   const int32_t nt = (int32_t)num_tiles(a.n_tokens);
-  const bool lin = copy_is_linear(a);
+  const CopyVariant v = copy_variant(a);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kCopyThreads);
-  cfg.dynamicSmemBytes = sizeof(int32_t) * (size_t)(nt + 1);
+  cfg.blockDim = dim3(variant_threads(v));
+  cfg.dynamicSmemBytes = variant_smem(v, nt);
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void *args[] = {const_cast<CopyArgs *>(&a)};
-  const void *fn = lin ? reinterpret_cast<const void *>(copy_kernel<true>)
-                       : reinterpret_cast<const void *>(copy_kernel<false>);
+  const void *fn = variant_fn(v);
   cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) {
     // programmatic dependent launch refused on this stream: launch in plain stream order
@@ -267,3 +459,13 @@ cudaError_t launch_copy(const CopyArgs &a, int grid, cudaStream_t s) {
 }
 
 }  // namespace kvx
+
+extern "C" kvx_status kvx_set_copy_engine(int32_t engine) {
+  if (engine < KVX_ENGINE_AUTO || engine > KVX_ENGINE_BULK) return KVX_ERR_INVALID_ARG;
+  kvx::g_engine.store(engine, std::memory_order_relaxed);
+  return KVX_OK;
+}
+
+extern "C" int32_t kvx_get_copy_engine(void) {
+  return kvx::g_engine.load(std::memory_order_relaxed);
+}

@@ -1,0 +1,95 @@
+// kvx_copy_ops.cuh -- device helpers shared by libkvx's copy kernels (sm_103a): 16-byte
+// streaming loads and stores, the address of a chunk's first row on either side of a move, and
+// the two ways a warp moves a chunk (flat byte range, or 16-byte pieces placed by row / head).
+#pragma once
+
+#include "kvx_internal.cuh"
+
+namespace kvx {
+namespace ops {
+
+constexpr int kUnroll = 4;  // independent 16-byte loads in flight per lane
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_stream(void *p, const uint4 &v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+struct Addr {
+  const char *base;  // row 0, head 0
+  int64_t row;       // bytes between consecutive rows of the chunk
+  int64_t head;      // bytes between consecutive head vectors of a row
+};
+
+// Address of the chunk's first row on one side.  idx: slot (pool) or row (buffer).  The
+// side's geometry stays in the kernel's parameter space (read by reference, not copied).
+__device__ __forceinline__ Addr side_addr(const Side &s, bool is_pool, const char *plane,
+                                          int64_t idx, const char *buf_plane, int32_t row_bytes) {
+  Addr a;
+  if (!is_pool) {
+    a.base = buf_plane + idx * row_bytes;
+    a.row = row_bytes;
+    a.head = s.seg_bytes;
+  } else if (s.hnd) {
+    const int64_t page = idx / s.page_size, off = idx - page * s.page_size;
+    a.base = plane + page * s.page_bytes + off * s.seg_bytes;
+    a.row = s.seg_bytes;
+    a.head = (int64_t)s.page_size * s.seg_bytes;
+  } else {
+    a.base = plane + idx * s.slot_stride;
+    a.row = s.slot_stride;
+    a.head = s.seg_bytes;
+  }
+  return a;
+}
+
+__device__ __forceinline__ void copy_linear(const char *src, char *dst, int32_t nvec, int lane) {
+  const uint4 *s = reinterpret_cast<const uint4 *>(src);
+  uint4 *d = reinterpret_cast<uint4 *>(dst);
+  for (int32_t v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
+    uint4 r[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (v0 + 32 * u < nvec) r[u] = ld_stream(s + v0 + 32 * u);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (v0 + 32 * u < nvec) st_stream(d + v0 + 32 * u, r[u]);
+  }
+}
+
+__device__ __forceinline__ int64_t vec_off(const Addr &a, int32_t v, int32_t vps, int32_t heads) {
+  const int32_t q = v / vps, w = v - q * vps;
+  const int32_t j = q / heads, h = q - j * heads;
+  return j * a.row + h * a.head + (int64_t)w * 16;
+}
+
+__device__ __forceinline__ void copy_pieces(const Addr &s, const Addr &d, int32_t nvec,
+                                            int32_t vps, int32_t heads, int lane) {
+  for (int32_t v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
+    uint4 r[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int32_t v = v0 + 32 * u;
+      if (v < nvec) r[u] = ld_stream(s.base + vec_off(s, v, vps, heads));
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int32_t v = v0 + 32 * u;
+      if (v < nvec) st_stream(const_cast<char *>(d.base) + vec_off(d, v, vps, heads), r[u]);
+    }
+  }
+}
+
+}  // namespace ops
+}  // namespace kvx

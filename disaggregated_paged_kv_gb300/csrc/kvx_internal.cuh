@@ -142,6 +142,11 @@ struct CopyArgs {
   const char *ws;
   WsLayout L;
   int32_t *status;
+  // One-shot calls with one-row chunks also pass the slot lists themselves: the row kernel
+  // then range-checks and loads its row before the planner has finished, and stores only
+  // once the planner's status word says every index is valid.  nullptr: read the plan.
+  const int32_t *spec_src;
+  const int32_t *spec_dst;
   const char *src_planes[KVX_MAX_PLANES];
   char *dst_planes[KVX_MAX_PLANES];
 };
@@ -152,11 +157,32 @@ cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
 cudaError_t launch_copy(const CopyArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_export(const char *ws, WsLayout L, int64_t n_tokens, int32_t *out,
                           int64_t max_chunks, int64_t *count, cudaStream_t s);
-// Blocks per SM at which the copy kernel (linear-only or general variant) is resident on the
-// current device, and which variant a call runs.
-int copy_blocks_per_sm(bool linear, int n_tiles);
+// Copy kernel variants: row (one request, linear one-row chunks: a non-persistent grid with one
+// warp per (token, plane) row), lean (one request, linear multi-row chunks, persistent, 32
+// registers), linear (batches of linear chunks), general (per-16-byte placement: HND pages,
+// slot-major pools) and bulk (TMA, linear chunks, chosen with kvx_set_copy_engine).
+enum CopyVariant : int {
+  kVariantLean = 0,
+  kVariantLinear,
+  kVariantGeneral,
+  kVariantBulk,
+  kVariantRow,
+  kNumVariants
+};
+CopyVariant copy_variant(const CopyArgs &a);
 bool copy_is_linear(const CopyArgs &a);
+bool use_bulk(const CopyArgs &a);
+int variant_threads(CopyVariant v);
+int variant_blocks_per_sm(CopyVariant v, int32_t n_tiles);
+// Grid of the row variant: one warp per (token, plane) row.
+int64_t row_grid(int64_t n_tokens, int32_t planes);
+constexpr int kBulkThreadsPerCta = 32;
+constexpr int kBulkSmallTiles = 256;  // occupancy is cached for <= this many tiles and for the max
 // Records e as this thread's kvx_last_cuda_error().
 void record_cuda_error(cudaError_t e);
+// One-launch path for single requests of up to KVX_FUSED_MAX_TOKENS tokens (kvx_fused.cu).
+int fused_blocks_per_sm(bool linear);
+cudaError_t launch_fused(const CopyArgs &c, const int32_t *src_idx, const int32_t *dst_idx,
+                         int32_t n, int32_t chunk_rows, int sms, int bps, cudaStream_t s);
 
 }  // namespace kvx

@@ -145,6 +145,27 @@ __device__ __forceinline__ bool starts_run(const PlanArgs &a, const Tok &t, cons
   return false;
 }
 
+__device__ __forceinline__ void write_header(const PlanArgs &a) {
+  PlanHeader *h = reinterpret_cast<PlanHeader *>(a.ws + a.L.header_off);
+  h->mode = a.mode;
+  h->op = a.op;
+  h->n_segs = a.n_segs;
+  h->n_tokens = a.n_tokens;
+  h->chunk_rows = a.chunk_rows;
+  h->planes = a.planes;
+  h->row_bytes = a.row_bytes;
+  h->src_is_pool = a.src.is_pool;
+  h->src_hnd = a.src.hnd;
+  h->src_page_size = a.src.page_size;
+  h->dst_is_pool = a.dst.is_pool;
+  h->dst_hnd = a.dst.hnd;
+  h->dst_page_size = a.dst.page_size;
+  h->pad = 0;
+  h->src_num_slots = a.src.num_slots;
+  h->dst_num_slots = a.dst.num_slots;
+  h->magic = kPlanMagic;
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanArgs a) {
   __shared__ int32_t s_tok[kTile];   // token offset (in tile) of run r
   __shared__ int32_t s_src[kTile];   // first source index of run r
@@ -174,24 +195,86 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     seg = (g < pre[a.n_segs]) ? seg_of(pre, a.n_segs, g) : 0;
   }
   Tok prev;
-  if (i0 > 0 && i0 < cnt) prev = fetch(a, t0 + i0 - 1, seg);
+  if (a.mode == kModeSlots) {
+    // Slot lists: issue every index load of this thread (and its predecessor token) before
+    // using any of them, so they cost one memory round trip instead of one per token.
+    int32_t sraw[kPlanItems + 1], draw[kPlanItems + 1];
 #pragma unroll
-  for (int k = 0; k < kPlanItems; ++k) {
-    const int32_t i = i0 + k;
-    brk[k] = false;
-    if (i < cnt) {
-      tk[k] = fetch(a, t0 + i, seg);
-      err = max(err, tk[k].err);
-      brk[k] = starts_run(a, tk[k], prev, i == 0);
-      prev = tk[k];
-      nbrk += brk[k] ? 1 : 0;
-      if (tk[k].err != KVX_OK && a.mode == kModeBatch) atomicMax(&a.status[1 + tk[k].req], tk[k].err);
+    for (int k = 0; k <= kPlanItems; ++k) {
+      const int32_t i = i0 + k - 1;
+      const bool in = i >= 0 && i < cnt;
+      sraw[k] = (in && a.src.is_pool) ? __ldg(a.src_idx + t0 + i) : (int32_t)(t0 + i);
+      draw[k] = (in && a.dst.is_pool) ? __ldg(a.dst_idx + t0 + i) : (int32_t)(t0 + i);
+    }
+    prev.s = sraw[0];
+    prev.d = draw[0];
+    prev.req = 0;
+    prev.op = a.op;
+#pragma unroll
+    for (int k = 0; k < kPlanItems; ++k) {
+      const int32_t i = i0 + k;
+      brk[k] = false;
+      if (i < cnt) {
+        Tok &t = tk[k];
+        t.s = sraw[k + 1];
+        t.d = draw[k + 1];
+        t.req = 0;
+        t.op = a.op;
+        t.start = (t0 + i == 0);
+        t.live = true;
+        t.err = ((a.src.is_pool && (t.s < 0 || t.s >= a.src.num_slots)) ||
+                 (a.dst.is_pool && (t.d < 0 || t.d >= a.dst.num_slots)))
+                    ? KVX_ERR_OUT_OF_RANGE
+                    : KVX_OK;
+        err = max(err, t.err);
+        brk[k] = starts_run(a, t, prev, i == 0);
+        prev = t;
+        nbrk += brk[k] ? 1 : 0;
+      }
+    }
+  } else {
+    if (i0 > 0 && i0 < cnt) prev = fetch(a, t0 + i0 - 1, seg);
+#pragma unroll
+    for (int k = 0; k < kPlanItems; ++k) {
+      const int32_t i = i0 + k;
+      brk[k] = false;
+      if (i < cnt) {
+        tk[k] = fetch(a, t0 + i, seg);
+        err = max(err, tk[k].err);
+        brk[k] = starts_run(a, tk[k], prev, i == 0);
+        prev = tk[k];
+        nbrk += brk[k] ? 1 : 0;
+        if (tk[k].err != KVX_OK && a.mode == kModeBatch)
+          atomicMax(&a.status[1 + tk[k].req], tk[k].err);
+      }
     }
   }
   err = block_max<kPlanThreads>(err, s_warp);
   if (tid == 0) {
     if (a.status_direct) a.status[0] = err;
     else if (err != KVX_OK) atomicMax(&a.status[0], err);
+  }
+  Chunk *out = reinterpret_cast<Chunk *>(a.ws + a.L.chunks_off) + (int64_t)tile * kTile;
+
+  if (a.chunk_rows == 1) {
+    // Every chunk is one row, so the plan is one chunk per token in token order whatever the
+    // runs are: no scans needed.
+#pragma unroll
+    for (int k = 0; k < kPlanItems; ++k) {
+      if (i0 + k < cnt) {
+        Chunk ch;
+        ch.req = tk[k].req;
+        ch.src = (int32_t)tk[k].s;
+        ch.dst = (int32_t)tk[k].d;
+        ch.rows = 1;
+        out[i0 + k] = ch;
+      }
+    }
+    if (tid == 0) {
+      reinterpret_cast<int32_t *>(a.ws + a.L.tiles_off)[tile] = cnt;
+      if (tile == 0) write_header(a);
+    }
+    return;
   }
 
   int32_t n_runs;
@@ -234,30 +317,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
 
   if (tid == 0) {
     reinterpret_cast<int32_t *>(a.ws + a.L.tiles_off)[tile] = n_chunks;
-    if (tile == 0) {
-      PlanHeader *h = reinterpret_cast<PlanHeader *>(a.ws + a.L.header_off);
-      h->mode = a.mode;
-      h->op = a.op;
-      h->n_segs = a.n_segs;
-      h->n_tokens = a.n_tokens;
-      h->chunk_rows = a.chunk_rows;
-      h->planes = a.planes;
-      h->row_bytes = a.row_bytes;
-      h->src_is_pool = a.src.is_pool;
-      h->src_hnd = a.src.hnd;
-      h->src_page_size = a.src.page_size;
-      h->dst_is_pool = a.dst.is_pool;
-      h->dst_hnd = a.dst.hnd;
-      h->dst_page_size = a.dst.page_size;
-      h->pad = 0;
-      h->src_num_slots = a.src.num_slots;
-      h->dst_num_slots = a.dst.num_slots;
-      h->magic = kPlanMagic;
-    }
+    if (tile == 0) write_header(a);
   }
 
   // phase 3: write the chunks
-  Chunk *out = reinterpret_cast<Chunk *>(a.ws + a.L.chunks_off) + (int64_t)tile * kTile;
   for (int32_t ci = tid; ci < n_chunks; ci += kPlanThreads) {
     int32_t lo = 0, hi = n_runs;  // largest run with s_coff[run] <= ci
     while (hi - lo > 1) {

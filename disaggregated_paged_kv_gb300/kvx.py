@@ -38,7 +38,7 @@ OP_GATHER, OP_SCATTER, OP_TRANSFER, OP_BATCH = 0, 1, 2, 3
 MAX_PLANES = 256
 PLAN_TILE = 2048
 MAX_TOKENS = PLAN_TILE * 4096
-CHUNK_BYTES = 8192
+CHUNK_BYTES = 2048
 NOALLOC_MAX_TOKENS = 16384
 
 ELEM_BYTES = {F16: 2, BF16: 2, F32: 4, FP8: 1}
@@ -113,6 +113,10 @@ _SIGS = {
     "kvx_status_str": (ctypes.c_char_p, [_I32]),
     "kvx_last_cuda_error": (_I32, []),
     "kvx_version": (_I32, []),
+    "kvx_set_copy_engine": (_I32, [_I32]),
+    "kvx_get_copy_engine": (_I32, []),
+    "kvx_set_fused_max_tokens": (_I32, [_I32]),
+    "kvx_get_fused_max_tokens": (_I32, []),
 }
 
 
@@ -177,6 +181,28 @@ def last_cuda_error() -> int:
 
 def version() -> int:
     return int(lib().kvx_version())
+
+
+ENGINE_AUTO, ENGINE_REGISTERS, ENGINE_BULK = 0, 1, 2
+
+
+def set_copy_engine(engine: int) -> None:
+    _check(lib().kvx_set_copy_engine(engine), "kvx_set_copy_engine")
+
+
+def get_copy_engine() -> int:
+    return int(lib().kvx_get_copy_engine())
+
+
+FUSED_MAX_TOKENS = 8192
+
+
+def set_fused_max_tokens(max_tokens: int) -> None:
+    _check(lib().kvx_set_fused_max_tokens(max_tokens), "kvx_set_fused_max_tokens")
+
+
+def get_fused_max_tokens() -> int:
+    return int(lib().kvx_get_fused_max_tokens())
 
 
 def workspace_size(max_tokens: int, max_requests: int = 0) -> int:

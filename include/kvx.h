@@ -77,7 +77,8 @@ typedef enum kvx_status {
   KVX_ERR_OVERLAP = 5,       /* source and destination memory overlap */
   KVX_ERR_CUDA = 6,          /* a CUDA runtime call failed; see kvx_last_cuda_error() */
   KVX_ERR_NO_WORKSPACE = 7,  /* workspace too small or misaligned */
-  KVX_ERR_TIMEOUT = 8,       /* reserved */
+  KVX_ERR_TIMEOUT = 8,       /* a copy's wait on its own bulk transfer exceeded 200 ms; the
+                                copy stopped instead of hanging (never expected) */
   KVX_ERR_CANCELLED = 9      /* reserved */
 } kvx_status;
 
@@ -115,7 +116,7 @@ typedef enum kvx_op {
 #define KVX_MAX_TOKENS (KVX_PLAN_TILE * 4096)
 /* The planner cuts every run into chunks of at most max(1, KVX_CHUNK_BYTES / R) rows; one
  * warp moves one chunk of one plane. */
-#define KVX_CHUNK_BYTES 8192
+#define KVX_CHUNK_BYTES 2048
 
 typedef struct kvx_layout_desc {
   int32_t num_layers; /* L >= 1, 2L <= KVX_MAX_PLANES */
@@ -291,6 +292,27 @@ KVX_API kvx_status kvx_plan_export(const void *d_ws, size_t ws_bytes, int64_t n_
                            kvx_stream_t stream);
 
 /* ---- misc ---------------------------------------------------------------------------- */
+
+/* Which kernel moves linear chunks (rows contiguous on both sides).  KVX_ENGINE_AUTO (default)
+ * and KVX_ENGINE_BULK use the TMA bulk-copy kernel (cp.async.bulk through shared memory);
+ * KVX_ENGINE_REGISTERS uses 16-byte register loads and stores, one warp per chunk.  Both move
+ * the same bytes; chunks that are not linear always take the register path.  Process-wide;
+ * returns KVX_ERR_INVALID_ARG for an unknown value. */
+#define KVX_ENGINE_AUTO 0
+#define KVX_ENGINE_REGISTERS 1
+#define KVX_ENGINE_BULK 2
+KVX_API kvx_status kvx_set_copy_engine(int32_t engine);
+KVX_API int32_t kvx_get_copy_engine(void);
+
+/* kvx_gather, kvx_scatter and kvx_transfer (and kvx_submit, kvx_transfer_noalloc) move a
+ * request of n <= this limit in one launch: every CTA checks all n indices itself (the move
+ * stays all-or-nothing), plans the runs of its own slice and copies it; larger requests use
+ * the planner + copy launches of kvx_plan / kvx_execute.  Both reach the same bytes.  The
+ * default and the most is KVX_FUSED_MAX_TOKENS; 0 sends every request through the planner.
+ * Process-wide. */
+#define KVX_FUSED_MAX_TOKENS 8192
+KVX_API kvx_status kvx_set_fused_max_tokens(int32_t max_tokens);
+KVX_API int32_t kvx_get_fused_max_tokens(void);
 
 KVX_API const char *kvx_status_str(kvx_status status);
 /* The cudaError_t of the last failing CUDA call made by this thread inside libkvx. */

@@ -30,6 +30,33 @@ def _cuda():
     torch.cuda.synchronize()
 
 
+PATHS = {
+    # one launch (every CTA validates and plans its own slice)
+    "fused": (kvx.FUSED_MAX_TOKENS, kvx.ENGINE_AUTO),
+    # planner launch + register-path copy
+    "planned": (0, kvx.ENGINE_REGISTERS),
+    # planner launch + TMA bulk copy (linear chunks)
+    "planned_bulk": (0, kvx.ENGINE_BULK),
+}
+
+
+@pytest.fixture(params=sorted(PATHS))
+def path(request):
+    fused_max, engine = PATHS[request.param]
+    kvx.set_fused_max_tokens(fused_max)
+    kvx.set_copy_engine(engine)
+    yield request.param
+    kvx.set_fused_max_tokens(kvx.FUSED_MAX_TOKENS)
+    kvx.set_copy_engine(kvx.ENGINE_AUTO)
+
+
+@pytest.fixture(params=["registers", "bulk"])
+def engine(request):
+    kvx.set_copy_engine(kvx.ENGINE_REGISTERS if request.param == "registers" else kvx.ENGINE_BULK)
+    yield request.param
+    kvx.set_copy_engine(kvx.ENGINE_AUTO)
+
+
 def _rng(k):
     return np.random.Generator(np.random.PCG64(1000 + k))
 
@@ -75,7 +102,7 @@ def _slot_lists(k, n, num_slots):
 
 @pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("n", [0, 1, 7, 2047, 2048, 2049, 4500])
-def test_gather(kind, n):
+def test_gather(kind, n, path):
     g = _rng(n)
     src = _pool(kind, "normal", g)
     slots = inputs.distinct_slots(g, n, src.num_slots) if n % 2 else _slot_lists(n, n, 8192)
@@ -92,7 +119,7 @@ def test_gather(kind, n):
 
 @pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("n", [1, 2048, 3001])
-def test_scatter(kind, n):
+def test_scatter(kind, n, path):
     g = _rng(100 + n)
     dst = _pool(kind, "sentinel", salt=3)
     slots = _slot_lists(100 + n, n, dst.num_slots)
@@ -115,7 +142,7 @@ def test_scatter(kind, n):
                                                ("hnd", "planes_separate"), ("planes", "slot_major"),
                                                ("hnd", "hnd")])
 @pytest.mark.parametrize("n", [5, 3000])
-def test_transfer(src_kind, dst_kind, n):
+def test_transfer(src_kind, dst_kind, n, path):
     g = _rng(200 + n)
     src = _pool(src_kind, "normal", g)
     dst = _pool(dst_kind, "sentinel", salt=5)
@@ -132,7 +159,7 @@ def test_transfer(src_kind, dst_kind, n):
     hz.assert_same_bytes(src.readback(), src.host, "source pool")
 
 
-def test_cfg1_gather_scatter_back_full_size():
+def test_cfg1_gather_scatter_back_full_size(path):
     """Qwen2.5-1.5B shape (28 x 2 x 128 fp16), slot-major pool of 4096 slots, 128 random
     slots: gather, then scatter back into a sentinel copy and in place."""
     w = inputs.WORKLOADS[1]
@@ -170,7 +197,7 @@ def test_cfg1_gather_scatter_back_full_size():
     hz.assert_same_bytes(src.readback(), src.host, "cfg1 in-place scatter-back")
 
 
-def test_hnd_page_table_gather_and_rebuild():
+def test_hnd_page_table_gather_and_rebuild(path):
     """Fused [heads, seq, dim] -> [seq, heads, dim] gather through a page table, last page
     partial, then the inverse rebuild into a second pool under an independent page table."""
     g = _rng(77)
@@ -218,7 +245,7 @@ def _runs_from_slots(s, d):
     return runs
 
 
-def test_runs_gather_scatter_transfer():
+def test_runs_gather_scatter_transfer(engine):
     g = _rng(500)
     n = 5000
     src = _pool("planes", "normal", g, num_slots=16384)
@@ -265,7 +292,7 @@ def test_runs_gather_scatter_transfer():
 # batch
 # ---------------------------------------------------------------------------------------
 
-def test_batch_mixed_ops_and_failing_request():
+def test_batch_mixed_ops_and_failing_request(engine):
     g = _rng(600)
     src = _pool("planes", "normal", g, num_slots=20000)
     dst = _pool("planes_separate", "sentinel", num_slots=20000, salt=8)
@@ -376,7 +403,7 @@ def test_plan_batch_matches_oracle():
 # ---------------------------------------------------------------------------------------
 
 @pytest.mark.parametrize("bad", [8192, -1, 2 ** 31 - 1])
-def test_out_of_range_moves_nothing(bad):
+def test_out_of_range_moves_nothing(bad, path):
     g = _rng(800)
     n = 5000
     src = _pool("planes", "normal", g)
@@ -423,7 +450,7 @@ def test_host_side_errors():
     assert e.value.code == kvx.ERR_INVALID_ARG
 
 
-def test_plan_once_execute_twice():
+def test_plan_once_execute_twice(engine):
     """A plan depends on indices and geometry only: one plan serves two destination pools."""
     g = _rng(1000)
     n = 3000
@@ -451,7 +478,7 @@ def test_plan_once_execute_twice():
     hz.assert_same_bytes(c.readback(), c.host, "no move on plan mismatch")
 
 
-def test_submit_with_host_slot_lists():
+def test_submit_with_host_slot_lists(path):
     g = _rng(1100)
     n = 2500
     src = _pool("planes", "normal", g)
@@ -468,3 +495,63 @@ def test_submit_with_host_slot_lists():
                          salt=1)
     assert oracle.transfer(hz.oracle_pool(src), s.numpy(), hz.oracle_pool(exp), d.numpy())[0] == 0
     hz.assert_same_bytes(dst.readback(), exp.host, "submit")
+
+
+# ---------------------------------------------------------------------------------------
+# 2 KiB rows (the 144 KiB/token shape): one-row chunks, so the planned path runs the row
+# kernel, which loads its rows before the planner's verdict and stores only after it
+# ---------------------------------------------------------------------------------------
+
+SH2K = dict(L=4, H=8, D=128, dtype="bf16")
+
+
+@pytest.mark.parametrize("op", ["gather", "scatter", "transfer"])
+@pytest.mark.parametrize("n", [1, 2048, 5000])
+def test_rows_2k(op, n, path):
+    g = _rng(3000 + n)
+    num = 8192
+    src = _pool("planes", "normal", g, num_slots=num, **SH2K)
+    s = _slot_lists(3001 + n, n, num)
+    d = _slot_lists(3002 + n, n, num)
+    ws, st = hz.workspace(n), hz.status()
+    P, R = 2 * SH2K["L"], SH2K["H"] * SH2K["D"] * 2
+    if op == "gather":
+        rc, want, _ = oracle.gather(hz.oracle_pool(src), s)
+        buf = _buffer(n, **SH2K)
+        kvx.gather(hz.kvx_layout(src), hz.dev_i32(s), n, hz.GUARD + buf.dev.data_ptr(), ws, st,
+                   buf_bytes=n * P * R)
+        exp = buf.host.copy()
+        exp[hz.GUARD:hz.GUARD + len(want)] = want
+        assert _sync_status(st) == [0]
+        hz.assert_same_bytes(buf.readback(), exp, f"gather 2k {path}")
+        return
+    dst = _pool("planes_separate", "sentinel", num_slots=num, salt=4, **SH2K)
+    exp = hz.make_mirror("planes_separate", SH2K["L"], SH2K["H"], SH2K["D"], SH2K["dtype"], num,
+                         1, "sentinel", salt=4)
+    if op == "scatter":
+        buf = _buffer(n, fill="normal", g=g, **SH2K)
+        assert oracle.scatter(hz.oracle_pool(exp), d, hz.buffer_body_bytes(buf))[0] == 0
+        kvx.scatter(hz.kvx_layout(dst), hz.dev_i32(d), n, hz.GUARD + buf.dev.data_ptr(), ws, st,
+                    buf_bytes=n * P * R)
+    else:
+        assert oracle.transfer(hz.oracle_pool(src), s, hz.oracle_pool(exp), d)[0] == 0
+        kvx.transfer(hz.kvx_layout(src), hz.dev_i32(s), hz.kvx_layout(dst), hz.dev_i32(d), n, ws, st)
+    assert _sync_status(st) == [0]
+    hz.assert_same_bytes(dst.readback(), exp.host, f"{op} 2k {path}")
+
+
+@pytest.mark.parametrize("where", [0, 2047, 4999])
+def test_rows_2k_out_of_range_moves_nothing(where, path):
+    """The row kernel may load rows before the planner's verdict; it must store none of them
+    when any index of the request (here in the first, a middle or the last tile) is bad."""
+    g = _rng(4000 + where)
+    n, num = 5000, 8192
+    src = _pool("planes", "normal", g, num_slots=num, **SH2K)
+    dst = _pool("planes", "sentinel", num_slots=num, salt=2, **SH2K)
+    s = _slot_lists(4001, n, num)
+    d = _slot_lists(4002, n, num)
+    s[where] = num  # one source index out of range
+    ws, st = hz.workspace(n), hz.status()
+    kvx.transfer(hz.kvx_layout(src), hz.dev_i32(s), hz.kvx_layout(dst), hz.dev_i32(d), n, ws, st)
+    assert _sync_status(st) == [kvx.ERR_OUT_OF_RANGE]
+    hz.assert_same_bytes(dst.readback(), dst.host, "destination untouched")
