@@ -63,6 +63,11 @@ def parse_args():
                     help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--pool-slots", type=int, default=SLOTS,
+                    help="slots per plane of both pools (smaller pools for profiler captures; "
+                         "the request itself is unchanged)")
+    ap.add_argument("--workload", type=int, default=2,
+                    help="2 (default): the headline transfer; 1, 3, 4, 5: the other workloads")
     return ap.parse_args()
 
 
@@ -81,7 +86,7 @@ def measured_peaks():
 def profile_traffic():
     """Per-launch DRAM bytes of the copy kernel from the committed ncu summary, if that summary
     was taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "copy_kernel_cfg2.md")
+    path = os.path.join(ROOT, "profiles", "copy_row_kernel_cfg2_transfer.md")
     src = os.path.join(ROOT, "disaggregated_paged_kv_gb300", "csrc", "kvx_copy.cu")
     if not os.path.exists(path):
         return None
@@ -150,6 +155,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     from tests import inputs
 
     torch.cuda.set_device(local_rank)
+    NS = args.pool_slots
     dev = torch.device("cuda", local_rank)
     kvx.lib()
     stream = torch.cuda.Stream(device=dev)
@@ -158,15 +164,15 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     # inputs resident in HBM: two 9 GiB pools of 72 per-plane [65536][8][128] bf16 tensors
     gen = torch.Generator(device=dev)
     gen.manual_seed(inputs.seed(2, inputs.ROLE_VALUES) + rank)
-    src = torch.randn((P, SLOTS, H, D), dtype=torch.bfloat16, device=dev, generator=gen)
-    dst = torch.empty((P, SLOTS, H, D), dtype=torch.bfloat16, device=dev)
+    src = torch.randn((P, NS, H, D), dtype=torch.bfloat16, device=dev, generator=gen)
+    dst = torch.empty((P, NS, H, D), dtype=torch.bfloat16, device=dev)
     dst.view(torch.int16).fill_(0x7FC1)  # quiet-NaN sentinel
-    s_np = inputs.distinct_slots(inputs.rng(2, inputs.ROLE_SRC_SLOTS), N_TOK, SLOTS)
-    d_np = inputs.distinct_slots(inputs.rng(2, inputs.ROLE_DST_SLOTS), N_TOK, SLOTS)
+    s_np = inputs.distinct_slots(inputs.rng(2, inputs.ROLE_SRC_SLOTS), N_TOK, NS)
+    d_np = inputs.distinct_slots(inputs.rng(2, inputs.ROLE_DST_SLOTS), N_TOK, NS)
     s_dev = torch.from_numpy(s_np).to(dev)
     d_dev = torch.from_numpy(d_np).to(dev)
-    src_l = kvx.Layout(L, H, D, kvx.BF16, SLOTS, base=src, plane_stride=SLOTS * R)
-    dst_l = kvx.Layout(L, H, D, kvx.BF16, SLOTS, base=dst, plane_stride=SLOTS * R)
+    src_l = kvx.Layout(L, H, D, kvx.BF16, NS, base=src, plane_stride=NS * R)
+    dst_l = kvx.Layout(L, H, D, kvx.BF16, NS, base=dst, plane_stride=NS * R)
     ws = torch.empty(kvx.workspace_size(N_TOK, 0), dtype=torch.uint8, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -257,6 +263,161 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
 
 # ---------------------------------------------------------------------------------------
+# the other workloads (--workload 1, 3, 4, 5): same timing rules, one JSON line each
+# ---------------------------------------------------------------------------------------
+
+def run_workload(args, cfg: int):
+    """Times every leg of workload cfg (gather + scatter-back, fragmented gather + scatter,
+    batch, fused-permute gather + rebuild).  Pools, slot lists and page tables come from the
+    same seeded recipe as the tests."""
+    import numpy as np
+    import torch
+
+    from disaggregated_paged_kv_gb300 import kvx
+    from tests import inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kvx.lib()
+    stream = torch.cuda.Stream(device=dev)
+    sp = int(stream.cuda_stream)
+    w = inputs.WORKLOADS[cfg]
+    Pw, Hw, Dw, Rw = w.planes, w.kv_heads, w.head_dim, w.row_bytes
+    tdt = torch.float16 if w.dtype == "fp16" else torch.bfloat16
+    kdt = kvx.F16 if w.dtype == "fp16" else kvx.BF16
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(inputs.seed(cfg, inputs.ROLE_VALUES))
+    sentinel = 0x7E01 if w.dtype == "fp16" else 0x7FC1
+
+    def randn(shape):
+        return torch.randn(shape, dtype=tdt, device=dev, generator=gen)
+
+    def sentinel_pool(shape):
+        t = torch.empty(shape, dtype=tdt, device=dev)
+        t.view(torch.int16).fill_(sentinel)
+        return t
+
+    st = torch.zeros(65, dtype=torch.int32, device=dev)
+    legs = []  # (name, fn, algorithmic bytes)
+    requests = 1
+    if cfg == 1:
+        pool = randn((w.num_slots, w.num_layers, 2, Hw, Dw))
+        lay = kvx.Layout(w.num_layers, Hw, Dw, kdt, w.num_slots, base=pool, plane_stride=Rw,
+                         slot_stride=Pw * Rw)
+        slots = torch.from_numpy(inputs.distinct_slots(inputs.rng(1, 1), w.n_tokens, w.num_slots)).to(dev)
+        buf = torch.empty((Pw, w.n_tokens, Hw, Dw), dtype=tdt, device=dev)
+        ws = torch.empty(kvx.workspace_size(w.n_tokens), dtype=torch.uint8, device=dev)
+        nb = 2 * w.payload_bytes + 4 * w.n_tokens
+        legs = [("gather", lambda: kvx.gather(lay, slots, w.n_tokens, buf, ws, st, stream=sp), nb),
+                ("scatter_back_in_place",
+                 lambda: kvx.scatter(lay, slots, w.n_tokens, buf, ws, st, stream=sp), nb)]
+        desc = ("Qwen2.5-1.5B-shaped KV (28 x K/V x 2 x 128 fp16), slot-major pool of 4096 slots, "
+                "128 random slots: gather to a 3.5 MiB [layer][K/V][seq][head][dim] buffer, then "
+                "scatter back in place")
+    elif cfg == 3:
+        src_planes = [randn((w.num_slots, Hw, Dw)) for _ in range(Pw)]
+        dst_planes = [sentinel_pool((w.num_slots, Hw, Dw)) for _ in range(Pw)]
+        s_np, runs = inputs.fragmented_slots(inputs.rng(3, 1), w.n_tokens, w.num_slots, 1.6)
+        d_np, _ = inputs.fragmented_slots(inputs.rng(3, 2), w.n_tokens, w.num_slots, 1.6)
+        s_d, d_d = torch.from_numpy(s_np).to(dev), torch.from_numpy(d_np).to(dev)
+        sl = kvx.Layout(w.num_layers, Hw, Dw, kdt, w.num_slots, plane_ptrs=src_planes)
+        dl = kvx.Layout(w.num_layers, Hw, Dw, kdt, w.num_slots, plane_ptrs=dst_planes)
+        buf = torch.empty((Pw, w.n_tokens, Hw, Dw), dtype=tdt, device=dev)
+        ws = torch.empty(kvx.workspace_size(w.n_tokens), dtype=torch.uint8, device=dev)
+        nb = 2 * w.payload_bytes + 4 * w.n_tokens
+        legs = [("gather", lambda: kvx.gather(sl, s_d, w.n_tokens, buf, ws, st, stream=sp), nb),
+                ("scatter", lambda: kvx.scatter(dl, d_d, w.n_tokens, buf, ws, st, stream=sp), nb)]
+        desc = (f"fragmented pools: 72 per-plane [131072][8][128] bf16 pools, 1536 tokens in "
+                f"{len(runs)} runs ~Geometric(1.6): gather to a 216 MiB buffer, then scatter into a "
+                f"fresh run layout")
+    elif cfg == 4:
+        lens = inputs.batch_lengths()
+        s_np, offs = inputs.paged_request_slots(inputs.rng(4, 1), lens, w.page_size, w.num_slots)
+        d_np, _ = inputs.paged_request_slots(inputs.rng(4, 2), lens, w.page_size, w.num_slots)
+        src = randn((Pw, w.num_slots, Hw, Dw))
+        dst = sentinel_pool((Pw, w.num_slots, Hw, Dw))
+        sl = kvx.Layout(w.num_layers, Hw, Dw, kdt, w.num_slots, base=src, plane_stride=w.num_slots * Rw)
+        dl = kvx.Layout(w.num_layers, Hw, Dw, kdt, w.num_slots, base=dst, plane_stride=w.num_slots * Rw)
+        reqs = [kvx.Request(kvx.OP_TRANSFER, L, int(o), int(o), 0) for L, o in zip(lens, offs[:-1])]
+        dreq = torch.from_numpy(np.frombuffer(b"".join(bytes(r) for r in reqs), dtype=np.uint8).copy()).to(dev)
+        total = int(sum(lens))
+        s_d, d_d = torch.from_numpy(s_np).to(dev), torch.from_numpy(d_np).to(dev)
+        ws = torch.empty(kvx.workspace_size(total, len(reqs)), dtype=torch.uint8, device=dev)
+        nb = 2 * total * Pw * Rw + 8 * total + 32 * len(reqs)
+        requests = len(reqs)
+        legs = [("batch", lambda: kvx.batch(sl, dl, dreq, len(reqs), total, s_d, total, d_d, total,
+                                             None, ws, st, buf_bytes=0, stream=sp), nb)]
+        desc = (f"64 requests of U{{1000..2000}} tokens ({total} total), 36 x K/V x 8 x 128 bf16, "
+                f"token-paged pools of 262144 slots with page size 16: one kvx_batch")
+    elif cfg == 5:
+        ps = w.page_size
+        pages = w.num_slots // ps
+        n_pages = w.n_tokens // ps
+        src = randn((Pw, pages, Hw, ps, Dw))
+        dst = sentinel_pool((Pw, pages, Hw, ps, Dw))
+        pt = inputs.random_pages(inputs.rng(5, 1), n_pages, pages)
+        pt2 = inputs.random_pages(inputs.rng(5, 2), n_pages, pages)
+        s_d = torch.from_numpy(inputs.page_table_slots(pt, w.n_tokens, ps)).to(dev)
+        d_d = torch.from_numpy(inputs.page_table_slots(pt2, w.n_tokens, ps)).to(dev)
+        sl = kvx.Layout(w.num_layers, Hw, Dw, kdt, w.num_slots, kind=kvx.HND_PAGED, page_size=ps,
+                        base=src, plane_stride=w.num_slots * Rw)
+        dl = kvx.Layout(w.num_layers, Hw, Dw, kdt, w.num_slots, kind=kvx.HND_PAGED, page_size=ps,
+                        base=dst, plane_stride=w.num_slots * Rw)
+        buf = torch.empty((Pw, w.n_tokens, Hw, Dw), dtype=tdt, device=dev)
+        ws = torch.empty(kvx.workspace_size(w.n_tokens), dtype=torch.uint8, device=dev)
+        nb = 2 * w.payload_bytes + 4 * w.n_tokens
+        legs = [("gather_permute", lambda: kvx.gather(sl, s_d, w.n_tokens, buf, ws, st, stream=sp), nb),
+                ("rebuild", lambda: kvx.scatter(dl, d_d, w.n_tokens, buf, ws, st, stream=sp), nb)]
+        desc = ("Qwen2.5-7B-shaped KV (28 x K/V x 4 x 128 bf16), seq 32768 in HND pages of 16 "
+                "(65536-page pools, random page tables): fused [heads,seq,dim] -> [seq,heads,dim] "
+                "gather to a 1.75 GiB buffer, then the inverse rebuild")
+    else:
+        raise SystemExit(f"unknown workload {cfg}")
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def timed(K, flush_l2=True):
+        evs = []
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(len(legs) + 1)]
+                if flush_l2:
+                    flush.fill_(i & 0xFF)
+                e[0].record(stream)
+                for j, (_, fn, _) in enumerate(legs):
+                    fn()
+                    e[j + 1].record(stream)
+                evs.append(e)
+        torch.cuda.synchronize()
+        return [[e[j].elapsed_time(e[j + 1]) for j in range(len(legs))] for e in evs]
+
+    timed(max(3, args.warmup))
+    assert int(st[0].item()) == kvx.OK, int(st[0].item())
+    K = max(3, min(args.steps, 200 if cfg in (4, 5) else args.steps))
+    res = timed(K)
+    total_bytes = sum(b for _, _, b in legs)
+    step_ms = statistics.mean(sum(r) for r in res)
+    line = {"metric": METRIC, "value": total_bytes / (step_ms * 1e-3) / 1e9, "unit": UNIT,
+            "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "dtype": "u8", "data": "synthetic",
+            "config": {"workload": f"cfg {cfg}: {desc}", "kv_dtype": w.dtype,
+                       "alg_bytes_per_step": total_bytes, "requests_per_step": requests,
+                       "us_per_request": step_ms * 1e3 / requests,
+                       "l2": "flushed before every timed step (write of 2x L2, outside the events)"},
+            "legs": {name: {"us": statistics.mean(r[j] for r in res) * 1e3,
+                            "GBs": b / (statistics.mean(r[j] for r in res) * 1e-3) / 1e9}
+                     for j, (name, _, b) in enumerate(legs)}}
+    peaks, _ = measured_peaks()
+    line["config"]["frac_of_measured_hbm"] = line["value"] / float(peaks["hbm_gbs"])
+    line["config"]["frac_of_nominal_8tbs"] = line["value"] / NOMINAL_HBM_GBS
+    if cfg == 1:  # launch-bound and L2-resident when not flushed: report the warm figure too
+        warm = timed(K, flush_l2=False)
+        wm = statistics.mean(sum(r) for r in warm)
+        line["warm_l2"] = {"value": total_bytes / (wm * 1e-3) / 1e9, "us_per_step": wm * 1e3}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------
 # the oracle (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------------------
 
@@ -343,6 +504,9 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank)
         return
+    if args.workload != 2:
+        run_workload(args, args.workload)
+        return
     if world > 1:
         import torch
         import torch.distributed as dist
@@ -367,7 +531,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": {"workload": WORKLOAD, "kv_dtype": "bf16", "tokens": N_TOK, "planes": P,
-                   "row_bytes": R, "pool_slots": SLOTS,
+                   "row_bytes": R, "pool_slots": args.pool_slots,
                    "payload_bytes_each_way": N_TOK * P * R,
                    "alg_bytes_per_step": alg_bytes(N_TOK),
                    "us_per_request": ms_per_step * 1e3,
