@@ -66,6 +66,8 @@ def parse_args():
     ap.add_argument("--pool-slots", type=int, default=SLOTS,
                     help="slots per plane of both pools (smaller pools for profiler captures; "
                          "the request itself is unchanged)")
+    ap.add_argument("--fused-max", type=int, default=None,
+                    help="kvx_set_fused_max_tokens for this run (0: planner + copy launches only)")
     ap.add_argument("--workload", type=int, default=2,
                     help="2 (default): the headline transfer; 1, 3, 4, 5: the other workloads")
     return ap.parse_args()
@@ -504,6 +506,9 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank)
         return
+    if args.fused_max is not None:
+        from disaggregated_paged_kv_gb300 import kvx
+        kvx.set_fused_max_tokens(args.fused_max)
     if args.workload != 2:
         run_workload(args, args.workload)
         return

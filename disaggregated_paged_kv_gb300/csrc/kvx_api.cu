@@ -73,6 +73,13 @@ bool same_rows(const kvx_layout *a, const kvx_layout *b) {
          a->head_dim == b->head_dim && a->elem == b->elem;
 }
 
+int32_t log2_exact(int64_t v) {
+  if (v <= 0 || (v & (v - 1)) != 0) return -1;
+  int32_t sh = 0;
+  while ((int64_t)1 << sh < v) ++sh;
+  return sh;
+}
+
 kvx::Side pool_side(const kvx_layout *l) {
   kvx::Side s = {};
   s.is_pool = 1;
@@ -82,6 +89,8 @@ kvx::Side pool_side(const kvx_layout *l) {
   s.num_slots = l->num_slots;
   s.slot_stride = l->slot_stride;
   s.page_bytes = l->page_bytes;
+  s.seg_shift = log2_exact(s.seg_bytes);
+  s.ps_shift = log2_exact(s.page_size);
   return s;
 }
 
@@ -91,13 +100,9 @@ kvx::Side buffer_side(int64_t seg_bytes) {
   s.hnd = 0;
   s.page_size = 1;
   s.seg_bytes = (int32_t)seg_bytes;
+  s.seg_shift = log2_exact(seg_bytes);
+  s.ps_shift = 0;
   return s;
-}
-
-// A pool side whose chunk rows are contiguous (token rows with dense slots); a buffer side
-// (nullptr) always is.
-bool side_linear(const kvx_layout *l, const kvx_layout *shape) {
-  return !l || (l->kind == KVX_NHD && l->slot_stride == shape->row_bytes);
 }
 
 int32_t chunk_rows_for(int64_t row_bytes) {
@@ -115,7 +120,7 @@ struct DeviceInfo {
   int bps_fused_general = 0;              // one-launch path, general placement
 };
 
-std::atomic<int32_t> g_fused_max{KVX_FUSED_MAX_TOKENS};
+std::atomic<int32_t> g_fused_max{0};  // measured: planner + row kernel is faster
 
 kvx_status device_info(DeviceInfo *out) {
   static std::mutex mu;
@@ -310,12 +315,15 @@ kvx_status enqueue_copy(const Call &c, const kvx_request *d_reqs, void *d_buf, c
   if (st != KVX_OK) return st;
   static thread_local kvx::CopyArgs a;  // ~4 KiB of plane pointers: keep it off the stack
   fill_copy_args(a, c, d_reqs, d_buf, d_ws, d_status);
+  a.spec_src = spec_src;
+  a.spec_dst = spec_dst;
   if (kvx::copy_variant(a) == kvx::kVariantRow) {
-    a.spec_src = spec_src;
-    a.spec_dst = spec_dst;
-    const cudaError_t e = kvx::launch_copy(a, (int)kvx::row_grid(c.n_tokens, c.shape->planes), s);
+    a.row_group_shift = kvx::row_group_shift(a);
+    const cudaError_t e = kvx::launch_copy(
+        a, (int)kvx::row_grid(c.n_tokens, c.shape->planes, a.row_group_shift), s);
     return e == cudaSuccess ? KVX_OK : cuda_fail(e);
   }
+  a.spec_src = a.spec_dst = nullptr;  // the other kernels read the plan
   // one warp (register paths) or one thread (bulk path) per work item; at most n*P items
   const int64_t items = (int64_t)c.shape->planes * c.n_tokens;
   const kvx::CopyVariant v = kvx::copy_variant(a);
@@ -562,11 +570,11 @@ static kvx_status run_slots(int32_t op, kvx_layout_t src, const int32_t *d_src_s
   kvx_status st = bind_layouts(c, src, dst);
   if (st == KVX_OK) st = check_buffer(c, d_buf, buf_bytes);
   if (st != KVX_OK) return st;
-  // Rows of >= KVX_CHUNK_BYTES on linear layouts take the planner + row kernel (the row kernel
-  // overlaps the planner); other requests of up to the fused limit take the one-launch path.
-  const bool row_path = chunk_rows_for(c.shape->row_bytes) == 1 && side_linear(c.src, c.shape) &&
-                        side_linear(c.dst, c.shape);
-  if (n == 0 || row_path || n > g_fused_max.load(std::memory_order_relaxed)) {
+  // Requests of up to the fused limit with rows under KVX_CHUNK_BYTES take the one-launch
+  // path; the rest take the planner + row kernel (the row kernel overlaps the planner).
+  const bool fused = chunk_rows_for(c.shape->row_bytes) > 1 &&
+                     n <= g_fused_max.load(std::memory_order_relaxed);
+  if (n == 0 || !fused) {
     st = kvx_plan(op, src, d_src_slots, dst, d_dst_slots, n, d_ws, ws_bytes, d_status, stream);
     if (st != KVX_OK || n == 0) return st;
     // the copy may read the slot lists itself (see CopyArgs::spec_src)

@@ -199,60 +199,121 @@ __global__ void __launch_bounds__(kCopyThreads, 8)
   }
 }
 
-// Row path: one request, linear rows of >= KVX_CHUNK_BYTES, so the plan is one chunk per
-// token.  Non-persistent: the grid holds one warp per (token, plane) row, token-major, and
-// the hardware keeps every SM full of short-lived warps (25-32 registers, 64 warps per SM).
-// With the slot lists at hand (one-shot calls) a warp range-checks its own row and issues its
-// loads before griddepcontrol.wait, so the planner runs under the first wave of loads; the
-// stores wait for the planner's verdict, which keeps the move all-or-nothing.
+// Row path.  Non-persistent grid: one warp per (group of g consecutive tokens, plane), token
+// major; g is a power of two with g * R <= KVX_CHUNK_BYTES where rows are small, so a warp moves
+// up to 2 KiB, and each token gets 32 / g lanes (so every lane serves exactly one token).  The
+// hardware keeps every SM full of short-lived 32-register warps (64 per SM).  Two sources of
+// indices:
+//  - speculative (one-shot calls, slot lists at hand): a lane range-checks its token and issues
+//    its loads before griddepcontrol.wait, so the planner runs under the first wave of loads;
+//    the stores wait for the planner's verdict, so the move stays all-or-nothing;
+//  - plan (g == 1, one-row chunks): after griddepcontrol.wait a warp reads chunk t of the plan
+//    (one chunk per token), including the request record of a batch.
+// Byte x of a token's row: on a token-row side the row is contiguous; on an HND side it sits at
+// head x / seg, offset x % seg of the token's page -- the fused [heads, tokens, dim] <->
+// [tokens, heads, dim] permute.
+__device__ __forceinline__ int32_t div_p2(int32_t v, int32_t d, int32_t shift) {
+  return shift >= 0 ? v >> shift : v / d;
+}
+
+// Start of a token's row (head 0) on one side.
+template <bool kHnd>
+__device__ __forceinline__ const char *row_base(const Side &s, bool pool, const char *plane,
+                                                const char *buf_plane, int32_t idx, int32_t R) {
+  if (!pool) return buf_plane + (int64_t)idx * R;
+  if (!kHnd) return plane + (int64_t)idx * s.slot_stride;
+  const int32_t page = div_p2(idx, s.page_size, s.ps_shift), off = idx - page * s.page_size;
+  return plane + (int64_t)page * s.page_bytes + (int64_t)off * s.seg_bytes;
+}
+
+// Byte x of the row: contiguous, except on an HND pool side where head h = x / seg sits
+// page_size * seg bytes after head h - 1.
+template <bool kHnd>
+__device__ __forceinline__ const char *row_byte(const Side &s, bool pool, const char *row,
+                                                int32_t x) {
+  if (!kHnd || !pool) return row + x;
+  const int32_t h = div_p2(x, s.seg_bytes, s.seg_shift);
+  return row + (int64_t)h * s.page_size * s.seg_bytes + (x - h * s.seg_bytes);
+}
+
+// kSpec: indices from the slot lists (one-shot, single request); otherwise from the plan.
+template <bool kSrcHnd, bool kDstHnd, bool kSpec>
 __global__ void __launch_bounds__(kCopyThreads, 8) copy_row_kernel(const __grid_constant__ CopyArgs a) {
   const int lane = threadIdx.x & 31;
   const uint32_t w = blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
   const uint32_t P = (uint32_t)a.planes;
-  const uint32_t t = w / P;
-  const int32_t p = (int32_t)(w - t * P);
-  if (t >= (uint32_t)a.n_tokens) return;
-  const int32_t R = a.row_bytes;
-  const bool sp = a.src.is_pool != 0, dp = a.dst.is_pool != 0;
-  const bool spec = a.spec_src != nullptr || a.spec_dst != nullptr;
-  int32_t s, d;
-  bool ok;
-  if (spec) {
-    s = sp ? a.spec_src[t] : (int32_t)t;
-    d = dp ? a.spec_dst[t] : (int32_t)t;
-    ok = (!sp || (s >= 0 && (int64_t)s < a.src.num_slots)) &&
-         (!dp || (d >= 0 && (int64_t)d < a.dst.num_slots));
+  const uint32_t q = w / P;
+  const int32_t p = (int32_t)(w - q * P);
+  const int32_t gsh = a.row_group_shift;   // g = 1 << gsh tokens per warp
+  const int32_t lsh = 5 - gsh;             // 1 << lsh lanes per token
+  const int64_t t0 = (int64_t)q << gsh;
+  if (t0 >= a.n_tokens) return;
+  const int64_t t = t0 + (lane >> lsh);
+  const int32_t li = lane & ((1 << lsh) - 1);
+  const int32_t R = a.row_bytes, vpr = R >> 4;
+  bool sp = a.src.is_pool != 0, dp = a.dst.is_pool != 0;
+  const char *bufp = a.buf;
+  int64_t nreq = a.n_tokens;
+  int32_t si, di;
+  bool ok = t < a.n_tokens;
+  if constexpr (kSpec) {
+    const int64_t tt = ok ? t : t0;
+    si = sp ? a.spec_src[tt] : (int32_t)tt;
+    di = dp ? a.spec_dst[tt] : (int32_t)tt;
+    ok = ok && (!sp || (si >= 0 && (int64_t)si < a.src.num_slots)) &&
+         (!dp || (di >= 0 && (int64_t)di < a.dst.num_slots));
   } else {
     pdl_wait();
-    ok = header_matches(a);
-    if (!ok) {
+    if (!header_matches(a)) {
       if (w == 0 && lane == 0) atomicMax(&a.status[0], (int32_t)KVX_ERR_INVALID_ARG);
       return;
     }
-    if (a.status[0] != KVX_OK) return;
-    const Chunk ch = reinterpret_cast<const Chunk *>(a.ws + a.L.chunks_off)[t];
-    s = ch.src;
-    d = ch.dst;
+    const Chunk ch = reinterpret_cast<const Chunk *>(a.ws + a.L.chunks_off)[t0];  // g == 1
+    if (a.mode == kModeBatch) {
+      if (a.status[1 + ch.req] != KVX_OK) return;
+      const kvx_request rq = a.reqs[ch.req];
+      sp = (rq.op == KVX_OP_GATHER || rq.op == KVX_OP_TRANSFER);
+      dp = (rq.op == KVX_OP_SCATTER || rq.op == KVX_OP_TRANSFER);
+      bufp = a.buf + rq.buf_off;
+      nreq = rq.n_tokens;
+    } else if (a.status[0] != KVX_OK) {
+      return;
+    }
+    si = ch.src;
+    di = ch.dst;
   }
-  const char *buf_plane = a.buf + (int64_t)p * a.n_tokens * R;
-  const uint4 *src = reinterpret_cast<const uint4 *>(lin_addr(a.src, sp, a.src_planes[p], s, buf_plane, R));
-  uint4 *dst = reinterpret_cast<uint4 *>(const_cast<char *>(lin_addr(a.dst, dp, a.dst_planes[p], d, buf_plane, R)));
-  const int32_t nv = R >> 4;
+  const char *buf_plane = bufp + (int64_t)p * nreq * R;
+  const char *srow = row_base<kSrcHnd>(a.src, sp, a.src_planes[p], buf_plane, si, R);
+  char *drow = const_cast<char *>(row_base<kDstHnd>(a.dst, dp, a.dst_planes[p], buf_plane, di, R));
   uint4 r[kUnroll];
 #pragma unroll
-  for (int u = 0; u < kUnroll; ++u)
-    if (ok && lane + 32 * u < nv) r[u] = ld_stream(src + lane + 32 * u);
-  if (spec) {
+  for (int u = 0; u < kUnroll; ++u) {
+    const int32_t xv = li + (u << lsh);
+    if (ok && xv < vpr) r[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
+  }
+  if constexpr (kSpec) {
     pdl_wait();  // the planner has checked every index of the request
     if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK) return;
   }
   if (!ok) return;
 #pragma unroll
-  for (int u = 0; u < kUnroll; ++u)
-    if (lane + 32 * u < nv) st_stream(dst + lane + 32 * u, r[u]);
-  if (nv > 32 * kUnroll)  // rows longer than 2 KiB: the rest in the ordinary loop
-    copy_linear(reinterpret_cast<const char *>(src + 32 * kUnroll),
-                reinterpret_cast<char *>(dst + 32 * kUnroll), nv - 32 * kUnroll, lane);
+  for (int u = 0; u < kUnroll; ++u) {
+    const int32_t xv = li + (u << lsh);
+    if (xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), r[u]);
+  }
+  // rows longer than kUnroll vectors per lane (over 2 KiB): the rest, after the verdict
+  for (int32_t x0 = kUnroll << lsh; x0 < vpr; x0 += kUnroll << lsh) {
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int32_t xv = x0 + li + (u << lsh);
+      if (xv < vpr) r[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int32_t xv = x0 + li + (u << lsh);
+      if (xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), r[u]);
+    }
+  }
 }
 
 // ---- bulk (TMA) path ----------------------------------------------------------------------
@@ -390,18 +451,46 @@ bool copy_is_linear(const CopyArgs &a) {
 }
 
 CopyVariant copy_variant(const CopyArgs &a) {
-  if (!copy_is_linear(a)) return kVariantGeneral;
-  if (g_engine.load(std::memory_order_relaxed) == KVX_ENGINE_BULK) return kVariantBulk;
-  if (a.mode == kModeBatch) return kVariantLinear;
-  return a.chunk_rows == 1 ? kVariantRow : kVariantLean;
+  const bool linear = copy_is_linear(a);
+  if (linear && g_engine.load(std::memory_order_relaxed) == KVX_ENGINE_BULK) return kVariantBulk;
+  // the row kernel takes every one-shot request (slot lists at hand) and every plan with
+  // one-row chunks; multi-row plans keep the persistent kernels
+  const bool spec = a.spec_src != nullptr || a.spec_dst != nullptr;
+  if ((spec && a.mode == kModeSlots) || a.chunk_rows == 1) return kVariantRow;
+  if (!linear) return kVariantGeneral;
+  return a.mode == kModeBatch ? kVariantLinear : kVariantLean;
 }
 
-int64_t row_grid(int64_t n_tokens, int32_t planes) {
-  const int64_t warps = n_tokens * planes, wpb = kCopyThreads / 32;
+int32_t row_group_shift(const CopyArgs &a) {
+  // plans are read one chunk (= one token) per warp; speculative calls group small rows
+  if (!(a.spec_src != nullptr || a.spec_dst != nullptr)) return 0;
+  int32_t sh = 0;
+  while (sh < 5 && ((int64_t)a.row_bytes << (sh + 1)) <= KVX_CHUNK_BYTES) ++sh;
+  return sh;
+}
+
+int64_t row_grid(int64_t n_tokens, int32_t planes, int32_t group_shift) {
+  const int64_t tokens_per_warp = (int64_t)1 << group_shift;
+  const int64_t warps = (n_tokens + tokens_per_warp - 1) / tokens_per_warp * planes;
+  const int64_t wpb = kCopyThreads / 32;
   return (warps + wpb - 1) / wpb;
 }
 
-bool use_bulk(const CopyArgs &a) { return copy_variant(a) == kVariantBulk; }
+template <bool kSpec>
+const void *row_fn_of(bool sh, bool dh) {
+  if (sh && dh) return reinterpret_cast<const void *>(copy_row_kernel<true, true, kSpec>);
+  if (sh) return reinterpret_cast<const void *>(copy_row_kernel<true, false, kSpec>);
+  if (dh) return reinterpret_cast<const void *>(copy_row_kernel<false, true, kSpec>);
+  return reinterpret_cast<const void *>(copy_row_kernel<false, false, kSpec>);
+}
+
+const void *row_fn(const CopyArgs &a) {
+  // an HND side only matters where the request uses it as a pool
+  const bool sh = a.src.hnd && (a.src.is_pool || a.mode == kModeBatch);
+  const bool dh = a.dst.hnd && (a.dst.is_pool || a.mode == kModeBatch);
+  const bool spec = a.spec_src != nullptr || a.spec_dst != nullptr;
+  return spec ? row_fn_of<true>(sh, dh) : row_fn_of<false>(sh, dh);
+}
 
 int variant_threads(CopyVariant v) { return v == kVariantBulk ? kBulkThreads : kCopyThreads; }
 
@@ -415,7 +504,7 @@ const void *variant_fn(CopyVariant v) {
     case kVariantLean: return reinterpret_cast<const void *>(copy_lean_kernel);
     case kVariantLinear: return reinterpret_cast<const void *>(copy_kernel<true>);
     case kVariantGeneral: return reinterpret_cast<const void *>(copy_kernel<false>);
-    case kVariantRow: return reinterpret_cast<const void *>(copy_row_kernel);
+    case kVariantRow: return reinterpret_cast<const void *>(copy_row_kernel<false, false, true>);
     default: return reinterpret_cast<const void *>(copy_bulk_kernel<kBulkThreads, kBulkStage>);
   }
 }
@@ -447,7 +536,7 @@ cudaError_t launch_copy(const CopyArgs &a, int grid, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void *args[] = {const_cast<CopyArgs *>(&a)};
-  const void *fn = variant_fn(v);
+  const void *fn = v == kVariantRow ? row_fn(a) : variant_fn(v);
   cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) {
     // programmatic dependent launch refused on this stream: launch in plain stream order

@@ -45,6 +45,8 @@ struct Side {
   int64_t num_slots;   // pool: valid slots [0, num_slots)
   int64_t slot_stride; // NHD pool: bytes from slot s to s+1
   int64_t page_bytes;  // HND pool: bytes of one page of one plane (= H * page_size * seg)
+  int32_t seg_shift;   // log2(seg_bytes) if a power of two, else -1
+  int32_t ps_shift;    // log2(page_size) if a power of two, else -1
 };
 
 // One chunk of the plan: rows consecutive rows starting at (src, dst) of request req.
@@ -147,6 +149,8 @@ struct CopyArgs {
   // once the planner's status word says every index is valid.  nullptr: read the plan.
   const int32_t *spec_src;
   const int32_t *spec_dst;
+  int32_t row_group_shift;  // row kernel: log2 of the tokens one warp moves
+  int32_t pad2;
   const char *src_planes[KVX_MAX_PLANES];
   char *dst_planes[KVX_MAX_PLANES];
 };
@@ -157,10 +161,11 @@ cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
 cudaError_t launch_copy(const CopyArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_export(const char *ws, WsLayout L, int64_t n_tokens, int32_t *out,
                           int64_t max_chunks, int64_t *count, cudaStream_t s);
-// Copy kernel variants: row (one request, linear one-row chunks: a non-persistent grid with one
-// warp per (token, plane) row), lean (one request, linear multi-row chunks, persistent, 32
-// registers), linear (batches of linear chunks), general (per-16-byte placement: HND pages,
-// slot-major pools) and bulk (TMA, linear chunks, chosen with kvx_set_copy_engine).
+// Copy kernel variants: row (non-persistent, one warp per group of tokens of one plane: every
+// one-shot request, and every plan with one-row chunks), lean (one request, linear multi-row
+// chunks, persistent, 32 registers), linear (batches of linear multi-row chunks), general
+// (per-16-byte placement of multi-row chunks: HND pages, slot-major pools) and bulk (TMA,
+// linear chunks, chosen with kvx_set_copy_engine).
 enum CopyVariant : int {
   kVariantLean = 0,
   kVariantLinear,
@@ -175,7 +180,8 @@ bool use_bulk(const CopyArgs &a);
 int variant_threads(CopyVariant v);
 int variant_blocks_per_sm(CopyVariant v, int32_t n_tiles);
 // Grid of the row variant: one warp per (token, plane) row.
-int64_t row_grid(int64_t n_tokens, int32_t planes);
+int64_t row_grid(int64_t n_tokens, int32_t planes, int32_t group_shift);
+int32_t row_group_shift(const CopyArgs &a);
 constexpr int kBulkThreadsPerCta = 32;
 constexpr int kBulkSmallTiles = 256;  // occupancy is cached for <= this many tiles and for the max
 // Records e as this thread's kvx_last_cuda_error().

@@ -304,12 +304,13 @@ KVX_API kvx_status kvx_plan_export(const void *d_ws, size_t ws_bytes, int64_t n_
 KVX_API kvx_status kvx_set_copy_engine(int32_t engine);
 KVX_API int32_t kvx_get_copy_engine(void);
 
-/* kvx_gather, kvx_scatter and kvx_transfer (and kvx_submit, kvx_transfer_noalloc) move a
- * request of n <= this limit in one launch: every CTA checks all n indices itself (the move
- * stays all-or-nothing), plans the runs of its own slice and copies it; larger requests use
- * the planner + copy launches of kvx_plan / kvx_execute.  Both reach the same bytes.  The
- * default and the most is KVX_FUSED_MAX_TOKENS; 0 sends every request through the planner.
- * Process-wide. */
+/* Optional one-launch path for kvx_gather, kvx_scatter and kvx_transfer (and kvx_submit,
+ * kvx_transfer_noalloc): a request whose rows are shorter than KVX_CHUNK_BYTES and whose n is
+ * at most this limit moves in one launch, every CTA checking all n indices itself (the move
+ * stays all-or-nothing), planning the runs of its own slice and copying it.  Otherwise the
+ * planner launch and the row copy kernel run (the copy overlaps the planner).  Both reach the
+ * same bytes.  The default is 0 (off: on GB300 the two launches measured faster at every size);
+ * the most is KVX_FUSED_MAX_TOKENS.  Process-wide. */
 #define KVX_FUSED_MAX_TOKENS 8192
 KVX_API kvx_status kvx_set_fused_max_tokens(int32_t max_tokens);
 KVX_API int32_t kvx_get_fused_max_tokens(void);

@@ -31,10 +31,10 @@ def _cuda():
 
 
 PATHS = {
-    # one launch (every CTA validates and plans its own slice)
+    # default routing: planner launch + row copy kernel (loads overlap the planner)
+    "default": (0, kvx.ENGINE_AUTO),
+    # one launch where it applies (rows under 2 KiB; every CTA validates and plans its slice)
     "fused": (kvx.FUSED_MAX_TOKENS, kvx.ENGINE_AUTO),
-    # planner launch + register-path copy
-    "planned": (0, kvx.ENGINE_REGISTERS),
     # planner launch + TMA bulk copy (linear chunks)
     "planned_bulk": (0, kvx.ENGINE_BULK),
 }
@@ -46,7 +46,7 @@ def path(request):
     kvx.set_fused_max_tokens(fused_max)
     kvx.set_copy_engine(engine)
     yield request.param
-    kvx.set_fused_max_tokens(kvx.FUSED_MAX_TOKENS)
+    kvx.set_fused_max_tokens(0)
     kvx.set_copy_engine(kvx.ENGINE_AUTO)
 
 
