@@ -85,19 +85,28 @@ def measured_peaks():
     return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
+COPY_SOURCES = ("kvx_copy.cu", "kvx_copy_ops.cuh", "kvx_internal.cuh")
+
+
+def copy_source_sha256() -> str:
+    """Hash of the sources the copy kernel is compiled from."""
+    h = hashlib.sha256()
+    for name in COPY_SOURCES:
+        with open(os.path.join(ROOT, "disaggregated_paged_kv_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def profile_traffic():
     """Per-launch DRAM bytes of the copy kernel from the committed ncu summary, if that summary
-    was taken on the current kernel source (else None)."""
+    was taken on the current kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", "copy_row_kernel_cfg2_transfer.md")
-    src = os.path.join(ROOT, "disaggregated_paged_kv_gb300", "csrc", "kvx_copy.cu")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
     h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    if not m or not h:
-        return None
-    if hashlib.sha256(open(src, "rb").read()).hexdigest() != h.group(1):
+    if not m or not h or copy_source_sha256() != h.group(1):
         return None
     return int(m.group(1))
 

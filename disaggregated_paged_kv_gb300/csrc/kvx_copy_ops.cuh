@@ -12,9 +12,12 @@ constexpr int kUnroll = 4;  // independent 16-byte loads in flight per lane
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Plain 16-byte global load.  Measured on the 288 MiB transfer: 1.7 us per step faster than the
+// read-only path (ld.global.nc with L1::no_allocate), and .L2::256B prefetch hints only added
+// L2 traffic past the end of every row.
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
   return r;
