@@ -154,6 +154,24 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest x over all ranks (x itself without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step: int, steps: int, world: int, max_total_ms: float) -> float:
+    """Whole-job throughput: every rank moved bytes_per_step per step; the slowest rank's time
+    counts."""
+    return world * bytes_per_step * steps / (max_total_ms * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------------------
@@ -265,10 +283,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                "how": "kvx_submit: pinned host slot lists copied in, plan + copy, status "
                       "copied out, all inside the step's CUDA events"}
 
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, device=dev)
     return dict(step_ms=step_ms, total_ms=total_ms, plan_ms=plan_ms, copy_ms=copy_ms, e2e=e2e,
                 clocks=clk, device=torch.cuda.get_device_name(dev))
 
@@ -535,7 +550,7 @@ def main():
         return
     K = args.steps
     ms_per_step = res["total_ms"] / K
-    value = world * alg_bytes(N_TOK) * K / (res["total_ms"] * 1e-3) / 1e9
+    value = whole_job_gbs(alg_bytes(N_TOK), K, world, res["total_ms"])
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
     copy_bytes = 2 * N_TOK * P * R
