@@ -280,8 +280,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         e2e = {"value": alg_bytes(N_TOK) / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                "us_per_request": e2e_ms * 1e3,
                "h2d_bytes_per_step": 2 * 4 * N_TOK, "d2h_bytes_per_step": 4,
-               "how": "kvx_submit: pinned host slot lists copied in, plan + copy, status "
-                      "copied out, all inside the step's CUDA events"}
+               "how": "kvx_submit with pinned host slot lists and status word: the planner "
+                      "and the copy read the 16 KiB of slot lists from host memory over "
+                      "NVLink-C2C and the copy writes the 4-byte status back, all inside the "
+                      "step's CUDA events"}
 
     total_ms = max_over_ranks(total_ms, device=dev)
     return dict(step_ms=step_ms, total_ms=total_ms, plan_ms=plan_ms, copy_ms=copy_ms, e2e=e2e,

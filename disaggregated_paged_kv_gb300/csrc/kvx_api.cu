@@ -308,7 +308,9 @@ void fill_copy_args(kvx::CopyArgs &a, const Call &c, const kvx_request *d_reqs, 
 
 kvx_status enqueue_copy(const Call &c, const kvx_request *d_reqs, void *d_buf, const void *d_ws,
                         int32_t *d_status, cudaStream_t s, const int32_t *spec_src = nullptr,
-                        const int32_t *spec_dst = nullptr) {
+                        const int32_t *spec_dst = nullptr, int32_t *host_status = nullptr,
+                        bool *host_status_written = nullptr) {
+  if (host_status_written) *host_status_written = false;
   if (c.n_tokens == 0) return KVX_OK;
   DeviceInfo di;
   kvx_status st = device_info(&di);
@@ -318,6 +320,8 @@ kvx_status enqueue_copy(const Call &c, const kvx_request *d_reqs, void *d_buf, c
   a.spec_src = spec_src;
   a.spec_dst = spec_dst;
   if (kvx::copy_variant(a) == kvx::kVariantRow) {
+    a.host_status = host_status;
+    if (host_status_written) *host_status_written = host_status != nullptr;
     a.row_group_shift = kvx::row_group_shift(a);
     const cudaError_t e = kvx::launch_copy(
         a, (int)kvx::row_grid(c.n_tokens, c.shape->planes, a.row_group_shift), s);
@@ -562,7 +566,9 @@ kvx_status kvx_execute(int32_t op, kvx_layout_t src, kvx_layout_t dst, const kvx
 static kvx_status run_slots(int32_t op, kvx_layout_t src, const int32_t *d_src_slots,
                             kvx_layout_t dst, const int32_t *d_dst_slots, int32_t n, void *d_buf,
                             size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *d_status,
-                            kvx_stream_t stream) {
+                            kvx_stream_t stream, int32_t *host_status = nullptr,
+                            bool *host_status_written = nullptr) {
+  if (host_status_written) *host_status_written = false;
   if (!valid_n(n)) return KVX_ERR_INVALID_ARG;
   Call c;
   c.op = op;
@@ -579,7 +585,8 @@ static kvx_status run_slots(int32_t op, kvx_layout_t src, const int32_t *d_src_s
     if (st != KVX_OK || n == 0) return st;
     // the copy may read the slot lists itself (see CopyArgs::spec_src)
     return enqueue_copy(c, nullptr, d_buf, d_ws, d_status, reinterpret_cast<cudaStream_t>(stream),
-                        c.src ? d_src_slots : nullptr, c.dst ? d_dst_slots : nullptr);
+                        c.src ? d_src_slots : nullptr, c.dst ? d_dst_slots : nullptr,
+                        host_status, host_status_written);
   }
   // the same host checks as kvx_plan
   if (!d_status || !aligned(d_status, 4)) return KVX_ERR_INVALID_ARG;
@@ -671,6 +678,17 @@ kvx_status kvx_batch(kvx_layout_t src, kvx_layout_t dst, const kvx_request *d_re
                      d_ws, ws_bytes, d_status, stream);
 }
 
+// Device address of a pinned (page-locked) host buffer, or nullptr for pageable memory.
+static const void *pinned_alias(const void *h) {
+  if (!h) return nullptr;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 kvx_status kvx_submit(int32_t op, kvx_layout_t src, const int32_t *h_src_slots,
                       kvx_layout_t dst, const int32_t *h_dst_slots, int32_t n, void *d_buf,
                       size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *h_status,
@@ -688,21 +706,31 @@ kvx_status kvx_submit(int32_t op, kvx_layout_t src, const int32_t *h_src_slots,
   if ((st = check_ws(d_ws, ws_bytes, L)) != KVX_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char *stage = static_cast<char *>(d_ws) + L.stage_off;
-  int32_t *d_src = reinterpret_cast<int32_t *>(stage);
-  int32_t *d_dst = d_src + n;
   int32_t *d_st = reinterpret_cast<int32_t *>(stage + kvx::align_up(8 * (int64_t)n, 16));
   cudaError_t e;
-  if (n > 0 && c.src) {
+  // Pinned host memory is reachable from the GPU (over NVLink-C2C on GB300): the kernels then
+  // read the slot lists and write the status word in place.  Pageable memory is staged with
+  // copies into the workspace.
+  const int32_t *z_src = static_cast<const int32_t *>(pinned_alias(h_src_slots));
+  const int32_t *z_dst = static_cast<const int32_t *>(pinned_alias(h_dst_slots));
+  int32_t *z_status = static_cast<int32_t *>(const_cast<void *>(pinned_alias(h_status)));
+  const int32_t *use_src = z_src, *use_dst = z_dst;
+  if (n > 0 && c.src && !z_src) {
+    int32_t *d_src = reinterpret_cast<int32_t *>(stage);
     e = cudaMemcpyAsync(d_src, h_src_slots, sizeof(int32_t) * (size_t)n, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e);
+    use_src = d_src;
   }
-  if (n > 0 && c.dst) {
+  if (n > 0 && c.dst && !z_dst) {
+    int32_t *d_dst = reinterpret_cast<int32_t *>(stage) + n;
     e = cudaMemcpyAsync(d_dst, h_dst_slots, sizeof(int32_t) * (size_t)n, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e);
+    use_dst = d_dst;
   }
-  st = run_slots(op, src, c.src ? d_src : nullptr, dst, c.dst ? d_dst : nullptr, n, d_buf,
-                 buf_bytes, d_ws, ws_bytes, d_st, stream);
-  if (st != KVX_OK) return st;
+  bool written = false;
+  st = run_slots(op, src, c.src ? use_src : nullptr, dst, c.dst ? use_dst : nullptr, n, d_buf,
+                 buf_bytes, d_ws, ws_bytes, d_st, stream, z_status, &written);
+  if (st != KVX_OK || written) return st;
   e = cudaMemcpyAsync(h_status, d_st, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
   return e == cudaSuccess ? KVX_OK : cuda_fail(e);
 }

@@ -216,6 +216,18 @@ __device__ __forceinline__ int32_t div_p2(int32_t v, int32_t d, int32_t shift) {
   return shift >= 0 ? v >> shift : v / d;
 }
 
+// The final status into the caller's pinned host word (kvx_submit), visible to the host once
+// the stream has reached the end of the call.
+__device__ __forceinline__ void report_host_status(int32_t *host_status, int32_t v) {
+  *reinterpret_cast<volatile int32_t *>(host_status) = v;
+  __threadfence_system();
+}
+
+// Whether this thread (the first of the grid) reports to the host status word.
+__device__ __forceinline__ bool reports(const CopyArgs &a) {
+  return a.host_status != nullptr && blockIdx.x == 0 && threadIdx.x == 0;
+}
+
 // Start of a token's row (head 0) on one side.
 template <bool kHnd>
 __device__ __forceinline__ const char *row_base(const Side &s, bool pool, const char *plane,
@@ -237,8 +249,10 @@ __device__ __forceinline__ const char *row_byte(const Side &s, bool pool, const 
 }
 
 // kSpec: indices from the slot lists (one-shot, single request); otherwise from the plan.
-template <bool kSrcHnd, bool kDstHnd, bool kSpec>
-__global__ void __launch_bounds__(kCopyThreads, 8) copy_row_kernel(const __grid_constant__ CopyArgs a) {
+// kTail: rows longer than kUnroll vectors per lane (over 2 KiB), moved in further passes; a
+// separate instance so that the common short-row kernels keep every value in registers.
+template <bool kSrcHnd, bool kDstHnd, bool kSpec, bool kTail>
+__global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8) copy_row_kernel(const __grid_constant__ CopyArgs a) {
   const int lane = threadIdx.x & 31;
   const uint32_t w = blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
   const uint32_t P = (uint32_t)a.planes;
@@ -293,25 +307,33 @@ __global__ void __launch_bounds__(kCopyThreads, 8) copy_row_kernel(const __grid_
   }
   if constexpr (kSpec) {
     pdl_wait();  // the planner has checked every index of the request
-    if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK) return;
+    const int32_t verdict = *reinterpret_cast<volatile const int32_t *>(a.status);
+    if (verdict != KVX_OK) {
+      if (reports(a)) report_host_status(a.host_status, verdict);
+      return;
+    }
   }
+  if (kSpec && reports(a) && !ok) report_host_status(a.host_status, KVX_OK);
   if (!ok) return;
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u) {
     const int32_t xv = li + (u << lsh);
     if (xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), r[u]);
   }
-  // rows longer than kUnroll vectors per lane (over 2 KiB): the rest, after the verdict
-  for (int32_t x0 = kUnroll << lsh; x0 < vpr; x0 += kUnroll << lsh) {
+  if (kSpec && reports(a)) report_host_status(a.host_status, KVX_OK);
+  if constexpr (kTail) {
+    // the rest of a long row, after the verdict
+    for (int32_t x0 = kUnroll << lsh; x0 < vpr; x0 += kUnroll << lsh) {
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int32_t xv = x0 + li + (u << lsh);
-      if (xv < vpr) r[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
-    }
+      for (int u = 0; u < kUnroll; ++u) {
+        const int32_t xv = x0 + li + (u << lsh);
+        if (xv < vpr) r[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
+      }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int32_t xv = x0 + li + (u << lsh);
-      if (xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), r[u]);
+      for (int u = 0; u < kUnroll; ++u) {
+        const int32_t xv = x0 + li + (u << lsh);
+        if (xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), r[u]);
+      }
     }
   }
 }
@@ -476,12 +498,12 @@ int64_t row_grid(int64_t n_tokens, int32_t planes, int32_t group_shift) {
   return (warps + wpb - 1) / wpb;
 }
 
-template <bool kSpec>
+template <bool kSpec, bool kTail>
 const void *row_fn_of(bool sh, bool dh) {
-  if (sh && dh) return reinterpret_cast<const void *>(copy_row_kernel<true, true, kSpec>);
-  if (sh) return reinterpret_cast<const void *>(copy_row_kernel<true, false, kSpec>);
-  if (dh) return reinterpret_cast<const void *>(copy_row_kernel<false, true, kSpec>);
-  return reinterpret_cast<const void *>(copy_row_kernel<false, false, kSpec>);
+  if (sh && dh) return reinterpret_cast<const void *>(copy_row_kernel<true, true, kSpec, kTail>);
+  if (sh) return reinterpret_cast<const void *>(copy_row_kernel<true, false, kSpec, kTail>);
+  if (dh) return reinterpret_cast<const void *>(copy_row_kernel<false, true, kSpec, kTail>);
+  return reinterpret_cast<const void *>(copy_row_kernel<false, false, kSpec, kTail>);
 }
 
 const void *row_fn(const CopyArgs &a) {
@@ -489,7 +511,9 @@ const void *row_fn(const CopyArgs &a) {
   const bool sh = a.src.hnd && (a.src.is_pool || a.mode == kModeBatch);
   const bool dh = a.dst.hnd && (a.dst.is_pool || a.mode == kModeBatch);
   const bool spec = a.spec_src != nullptr || a.spec_dst != nullptr;
-  return spec ? row_fn_of<true>(sh, dh) : row_fn_of<false>(sh, dh);
+  const bool tail = a.row_bytes > kUnroll * 32 * 16;  // more than one pass of the warp
+  if (spec) return tail ? row_fn_of<true, true>(sh, dh) : row_fn_of<true, false>(sh, dh);
+  return tail ? row_fn_of<false, true>(sh, dh) : row_fn_of<false, false>(sh, dh);
 }
 
 int variant_threads(CopyVariant v) { return v == kVariantBulk ? kBulkThreads : kCopyThreads; }
@@ -504,7 +528,7 @@ const void *variant_fn(CopyVariant v) {
     case kVariantLean: return reinterpret_cast<const void *>(copy_lean_kernel);
     case kVariantLinear: return reinterpret_cast<const void *>(copy_kernel<true>);
     case kVariantGeneral: return reinterpret_cast<const void *>(copy_kernel<false>);
-    case kVariantRow: return reinterpret_cast<const void *>(copy_row_kernel<false, false, true>);
+    case kVariantRow: return reinterpret_cast<const void *>(copy_row_kernel<false, false, true, false>);
     default: return reinterpret_cast<const void *>(copy_bulk_kernel<kBulkThreads, kBulkStage>);
   }
 }

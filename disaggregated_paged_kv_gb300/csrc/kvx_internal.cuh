@@ -151,6 +151,9 @@ struct CopyArgs {
   const int32_t *spec_dst;
   int32_t row_group_shift;  // row kernel: log2 of the tokens one warp moves
   int32_t pad2;
+  // kvx_submit with a pinned host status word: the row kernel stores the final status there
+  // itself (through its device mapping) instead of a device-to-host copy.  nullptr: none.
+  int32_t *host_status;
   const char *src_planes[KVX_MAX_PLANES];
   char *dst_planes[KVX_MAX_PLANES];
 };

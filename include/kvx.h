@@ -230,9 +230,11 @@ KVX_API kvx_status kvx_batch(kvx_layout_t src, kvx_layout_t dst, const kvx_reque
                      int32_t *d_status, kvx_stream_t stream);
 
 /* Host-index submission ([Mooncake] 6.1 submitTransfer + getTransferStatus): like
- * kvx_gather / kvx_scatter / kvx_transfer, but the slot lists are host arrays (pinned memory
- * makes the copy asynchronous) staged into the workspace, and the final status is copied
- * back into *h_status.  *h_status is valid once the stream has reached this call. */
+ * kvx_gather / kvx_scatter / kvx_transfer, but the slot lists and the status word are host
+ * memory.  Pinned (page-locked) host memory is read and written by the kernels in place, over
+ * the CPU-GPU link; pageable memory is staged through the workspace with copies on the
+ * stream.  *h_status is valid once the stream has reached the end of this call, not before
+ * (it may show KVX_OK while rows are still moving). */
 KVX_API kvx_status kvx_submit(int32_t op, kvx_layout_t src, const int32_t *h_src_slots,
                       kvx_layout_t dst, const int32_t *h_dst_slots, int32_t n, void *d_buf,
                       size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *h_status,
@@ -293,11 +295,11 @@ KVX_API kvx_status kvx_plan_export(const void *d_ws, size_t ws_bytes, int64_t n_
 
 /* ---- misc ---------------------------------------------------------------------------- */
 
-/* Which kernel moves linear chunks (rows contiguous on both sides).  KVX_ENGINE_AUTO (default)
- * and KVX_ENGINE_BULK use the TMA bulk-copy kernel (cp.async.bulk through shared memory);
- * KVX_ENGINE_REGISTERS uses 16-byte register loads and stores, one warp per chunk.  Both move
- * the same bytes; chunks that are not linear always take the register path.  Process-wide;
- * returns KVX_ERR_INVALID_ARG for an unknown value. */
+/* Which kernel moves linear chunks (rows contiguous on both sides).  KVX_ENGINE_BULK uses the
+ * TMA bulk-copy kernel (cp.async.bulk through shared memory); KVX_ENGINE_AUTO (default) and
+ * KVX_ENGINE_REGISTERS use 16-byte register loads and stores.  Both move the same bytes;
+ * chunks that are not linear always take the register path.  Process-wide; returns
+ * KVX_ERR_INVALID_ARG for an unknown value. */
 #define KVX_ENGINE_AUTO 0
 #define KVX_ENGINE_REGISTERS 1
 #define KVX_ENGINE_BULK 2

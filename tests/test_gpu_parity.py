@@ -497,6 +497,79 @@ def test_submit_with_host_slot_lists(path):
     hz.assert_same_bytes(dst.readback(), exp.host, "submit")
 
 
+# kvx_submit with the 2 KiB rows of the 144 KiB/token shape: the row kernel reads pinned slot
+# lists in place and writes the status word itself; pageable lists / status are staged.
+SUBMIT_MEM = ["pinned", "pageable", "pinned_lists_pageable_status"]
+
+
+@pytest.mark.parametrize("mem", SUBMIT_MEM)
+@pytest.mark.parametrize("op", ["gather", "scatter", "transfer"])
+def test_submit_rows_2k(op, mem, path):
+    sh = dict(L=4, H=8, D=128, dtype="bf16")
+    n, num = 3000, 8192
+    g = _rng(1200)
+    src = _pool("planes", "normal", g, num_slots=num, **sh)
+    s_np = _slot_lists(1201, n, num).astype(np.int32)
+    d_np = _slot_lists(1202, n, num).astype(np.int32)
+    pin_lists = mem != "pageable"
+    s = torch.from_numpy(s_np).pin_memory() if pin_lists else s_np.copy()
+    d = torch.from_numpy(d_np).pin_memory() if pin_lists else d_np.copy()
+    hst = torch.full((1,), -1, dtype=torch.int32)
+    hst = hst.pin_memory() if mem == "pinned" else hst
+    ws = hz.workspace(n)
+    if op == "gather":
+        rc, want, _ = oracle.gather(hz.oracle_pool(src), s_np)
+        buf = _buffer(n, **sh)
+        kvx.submit(kvx.OP_GATHER, hz.kvx_layout(src), s, None, None, n,
+                   hz.GUARD + buf.dev.data_ptr(), ws, hst, buf_bytes=n * buf.P * buf.R)
+        torch.cuda.synchronize()
+        got = buf.readback()
+        exp = buf.host.copy()
+        exp[hz.GUARD:hz.GUARD + want.size] = want
+    else:
+        dst = _pool("planes", "sentinel", num_slots=num, salt=2, **sh)
+        exp_m = hz.make_mirror("planes", sh["L"], sh["H"], sh["D"], sh["dtype"], num, 1,
+                               "sentinel", salt=2)
+        if op == "scatter":
+            buf = _buffer(n, "normal", g, **sh)
+            rc = oracle.scatter(hz.oracle_pool(exp_m), d_np, hz.buffer_body_bytes(buf))[0]
+            kvx.submit(kvx.OP_SCATTER, None, None, hz.kvx_layout(dst), d, n,
+                       hz.GUARD + buf.dev.data_ptr(), ws, hst, buf_bytes=n * buf.P * buf.R)
+        else:
+            rc = oracle.transfer(hz.oracle_pool(src), s_np, hz.oracle_pool(exp_m), d_np)[0]
+            kvx.submit(kvx.OP_TRANSFER, hz.kvx_layout(src), s, hz.kvx_layout(dst), d, n, None,
+                       ws, hst, buf_bytes=0)
+        torch.cuda.synchronize()
+        got, exp = dst.readback(), exp_m.host
+    assert rc == 0
+    assert int(hst[0]) == kvx.OK
+    hz.assert_same_bytes(got, exp, f"submit {op} {mem}")
+    hz.assert_same_bytes(src.readback(), src.host, "source pool")
+
+
+@pytest.mark.parametrize("mem", SUBMIT_MEM)
+def test_submit_rows_2k_out_of_range(mem, path):
+    sh = dict(L=4, H=8, D=128, dtype="bf16")
+    n, num = 3000, 8192
+    g = _rng(1300)
+    src = _pool("planes", "normal", g, num_slots=num, **sh)
+    dst = _pool("planes", "sentinel", num_slots=num, salt=2, **sh)
+    s_np = _slot_lists(1301, n, num).astype(np.int32)
+    d_np = _slot_lists(1302, n, num).astype(np.int32)
+    d_np[n - 5] = num  # one past the end: the whole request must move nothing
+    pin = mem != "pageable"
+    s = torch.from_numpy(s_np).pin_memory() if pin else s_np
+    d = torch.from_numpy(d_np).pin_memory() if pin else d_np
+    hst = torch.full((1,), -1, dtype=torch.int32)
+    hst = hst.pin_memory() if mem == "pinned" else hst
+    before = dst.readback()
+    kvx.submit(kvx.OP_TRANSFER, hz.kvx_layout(src), s, hz.kvx_layout(dst), d, n, None,
+               hz.workspace(n), hst, buf_bytes=0)
+    torch.cuda.synchronize()
+    assert int(hst[0]) == kvx.ERR_OUT_OF_RANGE
+    hz.assert_same_bytes(dst.readback(), before, "nothing moved")
+
+
 # ---------------------------------------------------------------------------------------
 # 2 KiB rows (the 144 KiB/token shape): one-row chunks, so the planned path runs the row
 # kernel, which loads its rows before the planner's verdict and stores only after it
