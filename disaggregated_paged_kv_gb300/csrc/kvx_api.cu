@@ -118,6 +118,7 @@ struct DeviceInfo {
   int bps_small[kvx::kNumVariants] = {};  // the same for plans of <= kBulkSmallTiles tiles
   int bps_fused_linear = 0;               // one-launch path, linear rows
   int bps_fused_general = 0;              // one-launch path, general placement
+  int bps_stream = 0;                     // layer-streamed copy
 };
 
 std::atomic<int32_t> g_fused_max{0};  // measured: planner + row kernel is faster
@@ -146,7 +147,8 @@ kvx_status device_info(DeviceInfo *out) {
     }
     d.bps_fused_linear = kvx::fused_blocks_per_sm(true);
     d.bps_fused_general = kvx::fused_blocks_per_sm(false);
-    if (d.bps_fused_linear <= 0 || d.bps_fused_general <= 0) {
+    d.bps_stream = kvx::stream_blocks_per_sm();
+    if (d.bps_fused_linear <= 0 || d.bps_fused_general <= 0 || d.bps_stream <= 0) {
       e = cudaGetLastError();
       return cuda_fail(e != cudaSuccess ? e : cudaErrorUnknown);
     }
@@ -732,6 +734,99 @@ kvx_status kvx_submit(int32_t op, kvx_layout_t src, const int32_t *h_src_slots,
                  buf_bytes, d_ws, ws_bytes, d_st, stream, z_status, &written);
   if (st != KVX_OK || written) return st;
   e = cudaMemcpyAsync(h_status, d_st, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+}
+
+// Device address of a control word: device memory as is, pinned host memory through its
+// device mapping; anything else (pageable memory, unknown pointers) gives nullptr.
+// Tags the mirror words of each kvx_stream call: an odd 64-bit start, one step per call.
+std::atomic<uint64_t> g_stream_gen{0xD1B54A32D192ED03ull};
+static_assert(sizeof(kvx::Chunk) * kvx::kTile >= 8 * (1 + KVX_MAX_PLANES / 2),
+              "the stream mirror fits in one tile's chunk table");
+
+static const void *device_word(const void *p) {
+  if (!p) return nullptr;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return at.devicePointer;
+  if (at.type == cudaMemoryTypeHost) return at.devicePointer;
+  return nullptr;
+}
+
+kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, kvx_layout_t dst,
+                      const int32_t *d_dst_slots, int32_t n, void *d_buf, size_t buf_bytes,
+                      const kvx_stream_ctl *ctl, void *d_ws, size_t ws_bytes, int32_t *d_status,
+                      kvx_stream_t stream) {
+  if (op < KVX_OP_GATHER || op > KVX_OP_TRANSFER || !valid_n(n)) return KVX_ERR_INVALID_ARG;
+  if (!ctl || ctl->wait_ns < 1 || ctl->wait_ns > KVX_MAX_WAIT_NS || ctl->max_ctas < 0 ||
+      ctl->reserved != 0)
+    return KVX_ERR_INVALID_ARG;
+  if (!d_status || !aligned(d_status, 16)) return KVX_ERR_INVALID_ARG;
+  Call c;
+  c.op = op;
+  c.n_tokens = n;
+  kvx_status st = bind_layouts(c, src, dst);
+  if (st == KVX_OK) st = check_buffer(c, d_buf, buf_bytes);
+  if (st != KVX_OK) return st;
+  const int32_t layers = c.shape->planes / 2;
+  kvx::StreamCtl k = {};
+  k.layer_ready = static_cast<const int32_t *>(device_word(ctl->layer_ready));
+  k.epoch_word = static_cast<const int32_t *>(device_word(ctl->epoch_word));
+  k.host_done = static_cast<int32_t *>(const_cast<void *>(pinned_alias(ctl->host_done)));
+  if ((ctl->layer_ready && (!k.layer_ready || !aligned(ctl->layer_ready, 4))) ||
+      (ctl->epoch_word && (!k.epoch_word || !aligned(ctl->epoch_word, 4))) ||
+      (ctl->host_done && (!k.host_done || !aligned(ctl->host_done, 4))))
+    return KVX_ERR_INVALID_ARG;
+  k.wait_ns = ctl->wait_ns;
+  k.ready_value = ctl->ready_value;
+  k.epoch = ctl->epoch;
+  k.layers = layers;
+  if (n > 0) {
+    if (c.src && (!d_src_slots || !aligned(d_src_slots, 4))) return KVX_ERR_INVALID_ARG;
+    if (c.dst && (!d_dst_slots || !aligned(d_dst_slots, 4))) return KVX_ERR_INVALID_ARG;
+    if ((st = check_ws(d_ws, ws_bytes, kvx::ws_layout(n, 0, false))) != KVX_OK) return st;
+  }
+  DeviceInfo di;
+  if ((st = device_info(&di)) != KVX_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  // status[0..3]: verdict, layers pending, CTAs finished, done.  A single-tile planner
+  // writes all four itself; otherwise they are zeroed first and the planner's tiles raise [0].
+  const bool direct = n > 0 && kvx::num_tiles(n) == 1;
+  if (!direct) {
+    e = cudaMemsetAsync(d_status, 0, 4 * sizeof(int32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (n > 0) {
+    kvx::PlanArgs pa = plan_args(c, d_ws, d_status);
+    pa.src_idx = d_src_slots;
+    pa.dst_idx = d_dst_slots;
+    pa.validate_only = 1;  // the streamed copy reads the slot lists itself
+    if (direct) pa.status_direct = 4;
+    e = kvx::launch_plan(pa, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    // the mirror lives where a plan's chunk table would be (unused by a validate-only plan)
+    k.mirror = reinterpret_cast<uint64_t *>(static_cast<char *>(d_ws) +
+                                            kvx::ws_layout(n, 0, false).chunks_off);
+  }
+  k.gen = g_stream_gen.fetch_add(1, std::memory_order_relaxed);
+  static thread_local kvx::CopyArgs a;  // ~4 KiB of plane pointers: keep it off the stack
+  fill_copy_args(a, c, nullptr, d_buf, d_ws, d_status);
+  a.spec_src = c.src ? d_src_slots : nullptr;
+  a.spec_dst = c.dst ? d_dst_slots : nullptr;
+  a.row_group_shift = kvx::row_group_shift(a);
+  // one warp per item at most; a grid of at least one CTA also runs the exit protocol for n = 0
+  kvx::stream_sizes(k, n, a.row_group_shift);
+  const int64_t warps = k.items;
+  int64_t grid = (int64_t)di.sms * di.bps_stream;
+  if (ctl->max_ctas > 0 && ctl->max_ctas < grid) grid = ctl->max_ctas;
+  const int64_t need = (warps + kvx::kCopyThreads / 32 - 1) / (kvx::kCopyThreads / 32);
+  if (need < grid) grid = need;
+  if (grid < 1) grid = 1;
+  e = kvx::launch_stream(a, k, (int)grid, s);
   return e == cudaSuccess ? KVX_OK : cuda_fail(e);
 }
 

@@ -211,10 +211,7 @@ __global__ void __launch_bounds__(kCopyThreads, 8)
 //    (one chunk per token), including the request record of a batch.
 // Byte x of a token's row: on a token-row side the row is contiguous; on an HND side it sits at
 // head x / seg, offset x % seg of the token's page -- the fused [heads, tokens, dim] <->
-// [tokens, heads, dim] permute.
-__device__ __forceinline__ int32_t div_p2(int32_t v, int32_t d, int32_t shift) {
-  return shift >= 0 ? v >> shift : v / d;
-}
+// [tokens, heads, dim] permute (row_base / row_byte).
 
 // The final status into the caller's pinned host word (kvx_submit), visible to the host once
 // the stream has reached the end of the call.
@@ -226,26 +223,6 @@ __device__ __forceinline__ void report_host_status(int32_t *host_status, int32_t
 // Whether this thread (the first of the grid) reports to the host status word.
 __device__ __forceinline__ bool reports(const CopyArgs &a) {
   return a.host_status != nullptr && blockIdx.x == 0 && threadIdx.x == 0;
-}
-
-// Start of a token's row (head 0) on one side.
-template <bool kHnd>
-__device__ __forceinline__ const char *row_base(const Side &s, bool pool, const char *plane,
-                                                const char *buf_plane, int32_t idx, int32_t R) {
-  if (!pool) return buf_plane + (int64_t)idx * R;
-  if (!kHnd) return plane + (int64_t)idx * s.slot_stride;
-  const int32_t page = div_p2(idx, s.page_size, s.ps_shift), off = idx - page * s.page_size;
-  return plane + (int64_t)page * s.page_bytes + (int64_t)off * s.seg_bytes;
-}
-
-// Byte x of the row: contiguous, except on an HND pool side where head h = x / seg sits
-// page_size * seg bytes after head h - 1.
-template <bool kHnd>
-__device__ __forceinline__ const char *row_byte(const Side &s, bool pool, const char *row,
-                                                int32_t x) {
-  if (!kHnd || !pool) return row + x;
-  const int32_t h = div_p2(x, s.seg_bytes, s.seg_shift);
-  return row + (int64_t)h * s.page_size * s.seg_bytes + (x - h * s.seg_bytes);
 }
 
 // kSpec: indices from the slot lists (one-shot, single request); otherwise from the plan.
@@ -350,11 +327,6 @@ constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 __device__ __forceinline__ void mbar_init(uint64_t *bar) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");

@@ -1,6 +1,7 @@
 // kvx_copy_ops.cuh -- device helpers shared by libkvx's copy kernels (sm_103a): 16-byte
-// streaming loads and stores, the address of a chunk's first row on either side of a move, and
-// the two ways a warp moves a chunk (flat byte range, or 16-byte pieces placed by row / head).
+// streaming loads and stores, the address of a chunk's first row (or of byte x of one token's
+// row) on either side of a move, and the two ways a warp moves a chunk (flat byte range, or
+// 16-byte pieces placed by row / head).
 #pragma once
 
 #include "kvx_internal.cuh"
@@ -11,6 +12,13 @@ namespace ops {
 constexpr int kUnroll = 4;  // independent 16-byte loads in flight per lane
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Nanoseconds of the GPU's global timer (bounds every wait in libkvx's kernels).
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 // Plain 16-byte global load.  Measured on the 288 MiB transfer: 1.7 us per step faster than the
 // read-only path (ld.global.nc with L1::no_allocate), and .L2::256B prefetch hints only added
@@ -55,6 +63,31 @@ __device__ __forceinline__ Addr side_addr(const Side &s, bool is_pool, const cha
     a.head = s.seg_bytes;
   }
   return a;
+}
+
+// v / d, by a shift where d is a power of two (shift >= 0).
+__device__ __forceinline__ int32_t div_p2(int32_t v, int32_t d, int32_t shift) {
+  return shift >= 0 ? v >> shift : v / d;
+}
+
+// Start of a token's row (head 0) on one side.
+template <bool kHnd>
+__device__ __forceinline__ const char *row_base(const Side &s, bool pool, const char *plane,
+                                                const char *buf_plane, int32_t idx, int32_t R) {
+  if (!pool) return buf_plane + (int64_t)idx * R;
+  if (!kHnd) return plane + (int64_t)idx * s.slot_stride;
+  const int32_t page = div_p2(idx, s.page_size, s.ps_shift), off = idx - page * s.page_size;
+  return plane + (int64_t)page * s.page_bytes + (int64_t)off * s.seg_bytes;
+}
+
+// Byte x of the row: contiguous, except on an HND pool side where head h = x / seg sits
+// page_size * seg bytes after head h - 1.
+template <bool kHnd>
+__device__ __forceinline__ const char *row_byte(const Side &s, bool pool, const char *row,
+                                                int32_t x) {
+  if (!kHnd || !pool) return row + x;
+  const int32_t h = div_p2(x, s.seg_bytes, s.seg_shift);
+  return row + (int64_t)h * s.page_size * s.seg_bytes + (x - h * s.seg_bytes);
 }
 
 __device__ __forceinline__ void copy_linear(const char *src, char *dst, int32_t nvec, int lane) {

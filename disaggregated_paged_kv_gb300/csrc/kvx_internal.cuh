@@ -120,8 +120,9 @@ struct PlanArgs {
   const kvx_request *reqs; // batch
   int64_t buf_bytes;       // batch: capacity of the buffer for request checks
   int32_t has_src, has_dst;
-  int32_t status_direct;   // slots mode with a single tile: the CTA stores status[0] itself
-  int32_t pad;
+  int32_t status_direct;   // slots mode with a single tile: the CTA stores status[0] itself,
+                           // and zeroes status[1 .. status_direct - 1]
+  int32_t validate_only;   // check the indices and write the status only (kvx_stream)
   Side src, dst;           // batch: pool geometry of the two layouts (is_pool = 1)
   char *ws;
   WsLayout L;
@@ -158,6 +159,27 @@ struct CopyArgs {
   char *dst_planes[KVX_MAX_PLANES];
 };
 
+// kvx_stream's control words, as device addresses (pinned host words through their device
+// mapping).
+struct StreamCtl {
+  const int32_t *layer_ready;  // [layers] or nullptr (all ready)
+  const int32_t *epoch_word;   // nullptr: never cancelled
+  int32_t *host_done;          // nullptr: none
+  // Device-memory copy of what some CTA has seen in the words above, in the workspace:
+  // [0] == gen: cancelled; [1 + l] == gen: layer l ready.  gen is a 64-bit tag new for every
+  // call, so words left by earlier calls (or any stale workspace bytes) do not match it and
+  // nothing needs resetting.
+  uint64_t *mirror;
+  uint64_t gen;
+  int64_t wait_ns;
+  int32_t ready_value;
+  int32_t epoch;
+  int32_t layers;
+  uint32_t groups;     // row groups of 1 << row_group_shift tokens per plane
+  uint32_t per_layer;  // items per layer: 2 * groups
+  uint32_t items;      // per_layer * layers (< 2^32 for every legal size)
+};
+
 // Launchers (enqueue only; return the launch's cudaError_t).
 cudaError_t launch_prefix(const PlanArgs &a, cudaStream_t s);
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
@@ -189,6 +211,10 @@ constexpr int kBulkThreadsPerCta = 32;
 constexpr int kBulkSmallTiles = 256;  // occupancy is cached for <= this many tiles and for the max
 // Records e as this thread's kvx_last_cuda_error().
 void record_cuda_error(cudaError_t e);
+// Layer-streamed copy (kvx_stream.cu): persistent grid over layer-major row groups.
+int stream_blocks_per_sm();
+void stream_sizes(StreamCtl &k, int64_t n_tokens, int32_t group_shift);
+cudaError_t launch_stream(const CopyArgs &c, const StreamCtl &k, int grid, cudaStream_t s);
 // One-launch path for single requests of up to KVX_FUSED_MAX_TOKENS tokens (kvx_fused.cu).
 int fused_blocks_per_sm(bool linear);
 cudaError_t launch_fused(const CopyArgs &c, const int32_t *src_idx, const int32_t *dst_idx,

@@ -251,9 +251,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   }
   err = block_max<kPlanThreads>(err, s_warp);
   if (tid == 0) {
-    if (a.status_direct) a.status[0] = err;
-    else if (err != KVX_OK) atomicMax(&a.status[0], err);
+    if (a.status_direct) {
+      a.status[0] = err;
+      for (int k = 1; k < a.status_direct; ++k) a.status[k] = 0;
+    } else if (err != KVX_OK) {
+      atomicMax(&a.status[0], err);
+    }
   }
+  if (a.validate_only) return;
   Chunk *out = reinterpret_cast<Chunk *>(a.ws + a.L.chunks_off) + (int64_t)tile * kTile;
 
   if (a.chunk_rows == 1) {

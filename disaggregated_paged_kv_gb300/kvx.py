@@ -81,6 +81,22 @@ class Request(ctypes.Structure):
 
 assert ctypes.sizeof(Request) == 32
 
+MAX_WAIT_NS = 10_000_000_000
+
+
+class StreamCtl(ctypes.Structure):
+    """kvx_stream_ctl: pointers are device or pinned host addresses (or None)."""
+    _fields_ = [
+        ("layer_ready", ctypes.c_void_p),
+        ("ready_value", ctypes.c_int32),
+        ("epoch_word", ctypes.c_void_p),
+        ("epoch", ctypes.c_int32),
+        ("wait_ns", ctypes.c_int64),
+        ("max_ctas", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("host_done", ctypes.c_void_p),
+    ]
+
 _lib: Optional[ctypes.CDLL] = None
 
 _VP = ctypes.c_void_p
@@ -104,6 +120,8 @@ _SIGS = {
     "kvx_batch": (_I32, [_VP, _VP, _VP, _I32, _I64, _VP, _I64, _VP, _I64, _VP, _SZ, _VP, _SZ,
                          _VP, _VP]),
     "kvx_submit": (_I32, [_I32, _VP, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _SZ, _VP, _VP]),
+    "kvx_stream": (_I32, [_I32, _VP, _VP, _VP, _VP, _I32, _VP, _SZ, ctypes.POINTER(StreamCtl),
+                          _VP, _SZ, _VP, _VP]),
     "kvx_plan": (_I32, [_I32, _VP, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _VP]),
     "kvx_plan_runs": (_I32, [_I32, _VP, _VP, _VP, _I32, _I32, _VP, _SZ, _VP, _VP]),
     "kvx_plan_batch": (_I32, [_VP, _VP, _VP, _I32, _I64, _VP, _I64, _VP, _I64, _SZ, _VP, _SZ,
@@ -388,3 +406,36 @@ def plan_export(ws, n_tokens: int, out, max_chunks: int, count, ws_bytes=None,
     rc = lib().kvx_plan_export(_ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
                                n_tokens, _ptr(out), max_chunks, _ptr(count), _stream(stream))
     _check(rc, "kvx_plan_export")
+
+
+def stream(op: int, src: Optional[Layout], src_slots, dst: Optional[Layout], dst_slots, n: int,
+           buf, ws, status, layer_ready=None, ready_value: int = 1, epoch_word=None,
+           epoch: int = 0, wait_ns: int = 100_000_000, max_ctas: int = 0, host_done=None,
+           buf_bytes=None, ws_bytes=None, stream=None) -> None:
+    """kvx_stream: a gather / scatter / transfer that moves layer l once
+    ``layer_ready[l] >= ready_value`` and stops when ``epoch_word`` no longer holds ``epoch``
+    or a layer's wait exceeds ``wait_ns``.  ``status`` is a device int32[4] (verdict, layers
+    pending, internal, done).  Control words may be device tensors or pinned host tensors."""
+    ctl = StreamCtl()
+    ctl.layer_ready = _any_ptr(layer_ready)
+    ctl.ready_value = ready_value
+    ctl.epoch_word = _any_ptr(epoch_word)
+    ctl.epoch = epoch
+    ctl.wait_ns = wait_ns
+    ctl.max_ctas = max_ctas
+    ctl.reserved = 0
+    ctl.host_done = _any_ptr(host_done)
+    rc = lib().kvx_stream(op, _h(src), _ptr(src_slots), _h(dst), _ptr(dst_slots), n, _ptr(buf),
+                          _nbytes(buf) if buf_bytes is None else buf_bytes, ctypes.byref(ctl),
+                          _ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
+                          _ptr(status), _stream(stream))
+    _check(rc, "kvx_stream")
+
+
+def _any_ptr(x) -> Optional[int]:
+    """Address of a tensor (device or pinned host), a numpy array or an integer."""
+    if x is None or isinstance(x, int):
+        return x
+    if hasattr(x, "ctypes"):
+        return int(x.ctypes.data)
+    return int(x.data_ptr())

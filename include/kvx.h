@@ -77,9 +77,11 @@ typedef enum kvx_status {
   KVX_ERR_OVERLAP = 5,       /* source and destination memory overlap */
   KVX_ERR_CUDA = 6,          /* a CUDA runtime call failed; see kvx_last_cuda_error() */
   KVX_ERR_NO_WORKSPACE = 7,  /* workspace too small or misaligned */
-  KVX_ERR_TIMEOUT = 8,       /* a copy's wait on its own bulk transfer exceeded 200 ms; the
-                                copy stopped instead of hanging (never expected) */
-  KVX_ERR_CANCELLED = 9      /* reserved */
+  KVX_ERR_TIMEOUT = 8,       /* a bounded device wait ran out: kvx_stream's wait for a layer
+                                (ctl->wait_ns), or the bulk engine's wait on its own transfer
+                                (200 ms, never expected); the kernel stopped instead of hanging */
+  KVX_ERR_CANCELLED = 9      /* kvx_stream: the request's epoch word changed; the rest of the
+                                request was dropped */
 } kvx_status;
 
 typedef enum kvx_dtype {
@@ -292,6 +294,63 @@ KVX_API kvx_status kvx_execute(int32_t op, kvx_layout_t src, kvx_layout_t dst, c
 KVX_API kvx_status kvx_plan_export(const void *d_ws, size_t ws_bytes, int64_t n_tokens,
                            int32_t *d_chunks, int64_t max_chunks, int64_t *d_count,
                            kvx_stream_t stream);
+
+/* ---- layer-streamed, cancellable copy ------------------------------------------------- */
+
+/* Longest a kvx_stream wait for one layer may be bounded to (ctl->wait_ns): 10 s. */
+#define KVX_MAX_WAIT_NS 10000000000LL
+
+/* Control block of kvx_stream (read on the host at the call; the words it points to are read
+ * by the kernel while it runs).  Pointers may be device memory or pinned (page-locked) host
+ * memory; pageable host memory is rejected (KVX_ERR_INVALID_ARG). */
+typedef struct kvx_stream_ctl {
+  /* int32[num_layers] or NULL.  Layer l (planes 2l and 2l+1) is moved once
+   * layer_ready[l] >= ready_value; the producer raises the word after the layer's rows are
+   * written ([DistServe] "一次请求如何穿过 DistServe": prefill writes the prompt's KV layer by
+   * layer, decode pulls layer j as soon as it exists).  NULL: every layer is ready. */
+  const int32_t *layer_ready;
+  int32_t ready_value;
+  /* int32 or NULL.  The request is live while *epoch_word == epoch.  The receiving side
+   * cancels it (gives up on the transfer, reassigns its pages) by changing the word; the copy
+   * then drops every layer it has not started ([PD-budget] "最难的一个问题": each request
+   * carries an identity, late data for a dead request is discarded). */
+  const int32_t *epoch_word;
+  int32_t epoch;
+  /* Bound on each wait for one layer, 1 .. KVX_MAX_WAIT_NS nanoseconds.  A layer not ready in
+   * time ends the copy with KVX_ERR_TIMEOUT ([DistServe] "一次请求如何穿过 DistServe": every
+   * abnormal path needs a lease or a timeout). */
+  int64_t wait_ns;
+  /* Most CTAs (of 256 threads) the copy occupies for its whole duration; 0: as many as fit on
+   * the GPU.  A producer running on the same GPU needs SMs to make progress: leave it room. */
+  int32_t max_ctas;
+  int32_t reserved;  /* must be 0 */
+  /* Pinned host int32 or NULL: set to 1 when d_status[3] is (see kvx_stream). */
+  int32_t *host_done;
+} kvx_stream_ctl;
+
+/* Gather / scatter / transfer of one request (op and arguments as kvx_gather / kvx_scatter /
+ * kvx_transfer; d_buf / buf_bytes are ignored by a transfer) that moves layer by layer as the
+ * producer marks layers ready, and stops early on cancellation or a wait running out.
+ *
+ * d_status: device int32[4], written by the call (no initialisation needed):
+ *   [0] KVX_OK, or the first error: KVX_ERR_OUT_OF_RANGE (nothing moved, as kvx_transfer),
+ *       KVX_ERR_TIMEOUT or KVX_ERR_CANCELLED (the larger code if both happened).
+ *   [1] layers pending: the trailing layers not guaranteed moved.  Layers
+ *       0 .. num_layers - [1] - 1 hold every row of the request; rows of later layers may or
+ *       may not have been written.  0 when [0] is KVX_OK.
+ *   [2] internal (CTAs finished).
+ *   [3] 1 once every CTA of the copy has finished and its writes are visible system-wide: no
+ *       further write of this call can land ([PD-budget] "最难的一个问题": the sender may only
+ *       acknowledge an aborted transfer once it can prove no late write is still in flight).
+ *       The receiving side may reuse cancelled pages after seeing it (or after the stream has
+ *       passed the call).
+ * The copy occupies up to ctl->max_ctas CTAs while it waits; every wait polls with back-off
+ * and ends by ctl->wait_ns, so the kernel always finishes. */
+KVX_API kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots,
+                              kvx_layout_t dst, const int32_t *d_dst_slots, int32_t n,
+                              void *d_buf, size_t buf_bytes, const kvx_stream_ctl *ctl,
+                              void *d_ws, size_t ws_bytes, int32_t *d_status,
+                              kvx_stream_t stream);
 
 /* ---- misc ---------------------------------------------------------------------------- */
 

@@ -125,3 +125,34 @@ def test_call_validation_before_cuda(lib):
     assert l.kvx_plan_runs(kvx.OP_TRANSFER, src.handle, dst.handle, None, 3, 10, WS, big, ST, None) == kvx.ERR_INVALID_ARG
     assert l.kvx_plan_batch(src.handle, dst.handle, None, 2, 10, SL, 10, SL, 10, 0, WS, big, ST, None) == kvx.ERR_INVALID_ARG
     assert l.kvx_submit(kvx.OP_TRANSFER, src.handle, None, dst.handle, None, 10, None, 0, WS, big, ctypes.c_void_p(0), None) == kvx.ERR_INVALID_ARG
+
+
+def test_stream_validation_before_cuda(lib):
+    """kvx_stream's control block and arguments are checked on the host, nothing enqueued."""
+    src = kvx.Layout(2, 2, 64, kvx.F16, 1000, base=FAKE, plane_stride=1000 * 256)
+    dst = kvx.Layout(2, 2, 64, kvx.F16, 1000, base=FAKE * 2, plane_stride=1000 * 256)
+    WS, ST, SL = FAKE * 4, FAKE * 5, FAKE * 6
+    big = 1 << 30
+    l = kvx.lib()
+
+    def call(ctl, status=ST, op=kvx.OP_TRANSFER, n=10, s=src, d=dst):
+        return l.kvx_stream(op, s.handle, SL, d.handle, SL, n, None, 0,
+                            None if ctl is None else ctypes.byref(ctl), WS, big, status, None)
+
+    def ctl(**kw):
+        c = kvx.StreamCtl()
+        c.wait_ns = 1000
+        for k, v in kw.items():
+            setattr(c, k, v)
+        return c
+
+    assert call(None) == kvx.ERR_INVALID_ARG                             # no control block
+    assert call(ctl(wait_ns=0)) == kvx.ERR_INVALID_ARG                   # unbounded wait
+    assert call(ctl(wait_ns=kvx.MAX_WAIT_NS + 1)) == kvx.ERR_INVALID_ARG
+    assert call(ctl(max_ctas=-1)) == kvx.ERR_INVALID_ARG
+    assert call(ctl(reserved=1)) == kvx.ERR_INVALID_ARG
+    assert call(ctl(), status=ST + 4) == kvx.ERR_INVALID_ARG             # status not 16-aligned
+    assert call(ctl(), status=None) == kvx.ERR_INVALID_ARG
+    assert call(ctl(), op=kvx.OP_BATCH) == kvx.ERR_INVALID_ARG
+    assert call(ctl(), n=-1) == kvx.ERR_INVALID_ARG
+    assert call(ctl(), d=src) == kvx.ERR_OVERLAP
