@@ -550,6 +550,24 @@ def run_stream(args):
     clk = clocks.stop()
     step_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
 
+    def timed(**kw):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                flush.fill_(i & 0xFF)
+                evs[i][0].record(stream)
+                launch(**kw)
+                evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        assert st.tolist()[:2] == [kvx.OK, 0], st.tolist()
+        return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    # every layer ready, through device ready words already raised; and on a persistent grid
+    words = torch.ones(L, dtype=torch.int32, device=dev)
+    words_ms = timed(layer_ready=words, ready_value=1)
+    persistent_ms = timed(max_ctas=2 * torch.cuda.get_device_properties(dev).multi_processor_count)
+
     # (2) layers raised by the host at a fixed cadence; (3) the move started after the last one
     cadence = args.layer_us * 1e-6
     trials = 30
@@ -602,7 +620,9 @@ def run_stream(args):
         "all_ready": {"us_per_request": step_ms * 1e3, "GBs": gbs,
                       "frac_of_measured_hbm": gbs / float(peaks["hbm_gbs"]),
                       "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
-                      "includes": "status memset + planner + streamed copy"},
+                      "includes": "planner + streamed copy + epilogue"},
+        "all_ready_device_words_us": words_ms * 1e3,
+        "all_ready_persistent_2_per_sm_us": persistent_ms * 1e3,
         "streamed_tail_us": pct(tails),
         "unstreamed_us": pct(unstreamed),
         "producer": f"host raises one layer every {args.layer_us:g} us into pinned ready words; "

@@ -5,6 +5,7 @@
 // if it fails; data-dependent checks happen in the planner and end up in the device status
 // word ("穷人版 PD 分离", section "最难的一个问题": the client learns of a failure right away
 // and no half-written KV is left behind).
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -741,7 +742,7 @@ kvx_status kvx_submit(int32_t op, kvx_layout_t src, const int32_t *h_src_slots,
 // device mapping; anything else (pageable memory, unknown pointers) gives nullptr.
 // Tags the mirror words of each kvx_stream call: an odd 64-bit start, one step per call.
 std::atomic<uint64_t> g_stream_gen{0xD1B54A32D192ED03ull};
-static_assert(sizeof(kvx::Chunk) * kvx::kTile >= 8 * (1 + KVX_MAX_PLANES / 2),
+static_assert(sizeof(kvx::Chunk) * kvx::kTile >= 8 * (2 + KVX_MAX_PLANES / 2),
               "the stream mirror fits in one tile's chunk table");
 
 static const void *device_word(const void *p) {
@@ -818,14 +819,22 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
   a.spec_src = c.src ? d_src_slots : nullptr;
   a.spec_dst = c.dst ? d_dst_slots : nullptr;
   a.row_group_shift = kvx::row_group_shift(a);
-  // one warp per item at most; a grid of at least one CTA also runs the exit protocol for n = 0
   kvx::stream_sizes(k, n, a.row_group_shift);
+  if (ctl->max_ctas == 0) {  // one warp per item, then the epilogue
+    e = kvx::launch_stream_rows(a, k, s);
+    return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+  }
+  // persistent grid of at most max_ctas CTAs (at least one: it also runs the exit protocol)
   const int64_t warps = k.items;
   int64_t grid = (int64_t)di.sms * di.bps_stream;
-  if (ctl->max_ctas > 0 && ctl->max_ctas < grid) grid = ctl->max_ctas;
+  if (ctl->max_ctas < grid) grid = ctl->max_ctas;
   const int64_t need = (warps + kvx::kCopyThreads / 32 - 1) / (kvx::kCopyThreads / 32);
   if (need < grid) grid = need;
   if (grid < 1) grid = 1;
+  // about four blocks per warp: few layer entries per warp, yet each layer's items spread
+  // over many warps (a late layer moves in a few row latencies)
+  const int64_t per_warp = (warps + grid * (kvx::kCopyThreads / 32) - 1) / (grid * (kvx::kCopyThreads / 32));
+  k.block = (uint32_t)std::min<int64_t>(std::max<int64_t>(per_warp / 4, 1), 8);
   e = kvx::launch_stream(a, k, (int)grid, s);
   return e == cudaSuccess ? KVX_OK : cuda_fail(e);
 }

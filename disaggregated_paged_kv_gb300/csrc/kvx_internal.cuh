@@ -166,7 +166,8 @@ struct StreamCtl {
   const int32_t *epoch_word;   // nullptr: never cancelled
   int32_t *host_done;          // nullptr: none
   // Device-memory copy of what some CTA has seen in the words above, in the workspace:
-  // [0] == gen: cancelled; [1 + l] == gen: layer l ready.  gen is a 64-bit tag new for every
+  // [0] == gen: cancelled (persistent grid); [1 + l] == gen: layer l ready;
+  // [1 + KVX_MAX_PLANES / 2]: the row grid's stop word.  gen is a 64-bit tag new for every
   // call, so words left by earlier calls (or any stale workspace bytes) do not match it and
   // nothing needs resetting.
   uint64_t *mirror;
@@ -178,6 +179,8 @@ struct StreamCtl {
   uint32_t groups;     // row groups of 1 << row_group_shift tokens per plane
   uint32_t per_layer;  // items per layer: 2 * groups
   uint32_t items;      // per_layer * layers (< 2^32 for every legal size)
+  uint32_t block;      // consecutive items a warp takes per block (see kvx_stream.cu)
+  uint32_t pad2;
 };
 
 // Launchers (enqueue only; return the launch's cudaError_t).
@@ -215,6 +218,8 @@ void record_cuda_error(cudaError_t e);
 int stream_blocks_per_sm();
 void stream_sizes(StreamCtl &k, int64_t n_tokens, int32_t group_shift);
 cudaError_t launch_stream(const CopyArgs &c, const StreamCtl &k, int grid, cudaStream_t s);
+// Row grid (one warp per item) and the epilogue that sets the "no further write" words.
+cudaError_t launch_stream_rows(const CopyArgs &c, const StreamCtl &k, cudaStream_t s);
 // One-launch path for single requests of up to KVX_FUSED_MAX_TOKENS tokens (kvx_fused.cu).
 int fused_blocks_per_sm(bool linear);
 cudaError_t launch_fused(const CopyArgs &c, const int32_t *src_idx, const int32_t *dst_idx,

@@ -7,23 +7,35 @@
 // another request, and the sender may only acknowledge the abort once it can prove that no
 // write is still in flight.
 //
-// One persistent grid walks the request's rows in layer-major order: item i is
-// (layer l, K/V, group of g tokens) with l = i / (2 * groups); warp w takes items w, w + W,
-// w + 2W, ... (W warps in the grid), so every warp reaches the layers in increasing order and
-// all warps stay busy however few tokens a layer has.  A warp entering layer l checks, once
-// per CTA and layer (the first warp to arrive polls, the others read the CTA's shared bit of
-// layer l):
-//   - the request's epoch word: changed -> the CTA stops before layer l (KVX_ERR_CANCELLED);
-//   - the producer's ready word of layer l: below ready_value -> poll with back-off, bounded
-//     by wait_ns of %globaltimer and an iteration cap -> the CTA stops before layer l
-//     (KVX_ERR_TIMEOUT).
-// A CTA that stops still finishes the layers its warps had already entered, so every layer
-// below the smallest stop layer of all CTAs holds every row.  On exit each CTA publishes its
-// stop layer and code, and the last CTA to finish sets the "no further write" word with a
-// system-scope release after all CTAs' writes.
+// Items are (layer l, K/V, group of g tokens) in layer-major order: item i has
+// l = i / (2 * groups).  Two grids move them:
 //
-// Waits only ever poll memory that the host or another engine writes; the kernel never waits
-// for another CTA or another kernel.
+// Row grid (the default): one warp per item, one CTA per kWarps consecutive items, as the
+// row kernel of kvx_copy.cu.  Thread 0 of a CTA waits for the CTA's layer (usually one) while
+// its warps load their slot indices; the rows are loaded once the layer is ready, and stored
+// once the planner's verdict says every index is valid.  A CTA that gives up on a layer
+// (the epoch word changed, or the wait ran past wait_ns) writes a tagged stop word into the
+// device-memory mirror, so every CTA that starts later stops at once instead of waiting its
+// own wait_ns again; CTAs below the stop layer still move their rows.  A one-thread epilogue
+// kernel, launched behind the grid, folds the stop codes into the status and sets the
+// "no further write" words once every CTA has finished.
+//
+// Persistent grid (kvx_stream_ctl::max_ctas > 0): at most max_ctas CTAs, so that a producer
+// running on the same GPU keeps the rest of it.  Blocks of kWarps * block consecutive items
+// go to the CTAs in turn, so every warp reaches the layers in increasing order.  A warp
+// entering layer l checks, once per CTA and layer (the first warp to arrive polls, the others
+// read the CTA's shared bit of layer l), the epoch word and the ready word of layer l.  A CTA
+// that stops still finishes the layers its warps had already entered, so every layer below
+// the smallest stop layer of all CTAs holds every row.  On exit each CTA publishes its stop
+// layer and code, and the last CTA to finish sets the "no further write" words.
+//
+// In both, polling is shared out so that the words of a slow producer (often pinned host
+// memory, read over the CPU-GPU link) see few readers: pollers read the device-memory mirror
+// of what some CTA has already seen on every round and the producer's words only on their
+// first round and every 16th, except in the CTA that owns the layer's first item, which reads
+// them on every round and copies what it sees into the mirror.  Every wait is bounded by
+// wait_ns of %globaltimer and an iteration cap.  Waits only ever poll memory that the host or
+// another engine writes: no CTA waits for another CTA or another kernel.
 #include "kvx_copy_ops.cuh"
 
 namespace kvx {
@@ -162,13 +174,21 @@ __global__ void __launch_bounds__(kCopyThreads, 6) stream_kernel(const __grid_co
   const int32_t li = lane & ((1 << lsh) - 1);
   const int32_t R = a.row_bytes, vpr = R >> 4;
   const bool sp = a.src.is_pool != 0, dp = a.dst.is_pool != 0;
-  const uint32_t W = gridDim.x * kWarps;
+  // Blocks of kWarps * k.block consecutive items go to the CTAs in turn; warp w of a CTA takes
+  // items w, w + kWarps, ... of each of its blocks.  A warp's items still increase, and it
+  // enters a new layer about once per block rather than once per item.
+  const uint32_t bs = kWarps * k.block;
+  const uint32_t stride = gridDim.x * bs;
   int32_t lcur = -1;
   bool verdict_ok = false;  // this warp has seen the planner's verdict (every index valid)
-  for (uint32_t i = blockIdx.x * kWarps + warp; i < k.items; i += W) {
+  uint32_t base = blockIdx.x * bs, j = 0;
+  for (;; (++j == k.block) ? (j = 0, base += stride) : 0) {
+    const uint32_t i = base + j * kWarps + warp;
+    if (i >= k.items) break;
     const int32_t l = (int32_t)(i / k.per_layer);
     if (l != lcur) {
-      const bool owner = blockIdx.x == ((uint64_t)l * k.per_layer % W) / kWarps;
+      // the CTA whose block holds the layer's first item
+      const bool owner = blockIdx.x == ((uint64_t)l * k.per_layer / bs) % gridDim.x;
       int32_t go = lane == 0 ? wait_layer(k, l, owner, &cs) : 0;
       go = __shfl_sync(0xffffffffu, go, 0);
       __syncwarp();  // lane 0's acquire orders every lane's loads of the layer
@@ -231,6 +251,201 @@ __global__ void __launch_bounds__(kCopyThreads, 6) stream_kernel(const __grid_co
   }
 }
 
+// ---- row grid ------------------------------------------------------------------------
+
+// The stop word (mirror[kStopWord]) of the row grid: gen ^ (code << 56 | layer << 40).  Any
+// value whose low 40 bits differ from gen's -- stale words of earlier calls, never-written
+// workspace -- decodes as "no stop".
+constexpr int kStopWord = 1 + KVX_MAX_PLANES / 2;
+
+__device__ __forceinline__ uint64_t ld_relaxed_gpu(const uint64_t *p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int32_t ld_relaxed_sys(const int32_t *p) {
+  int32_t v;
+  asm volatile("ld.relaxed.sys.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+struct Stop {
+  int32_t layer;  // first layer not to move
+  int32_t code;   // KVX_ERR_TIMEOUT / KVX_ERR_CANCELLED; 0: no stop
+};
+
+__device__ __forceinline__ Stop decode_stop(uint64_t v, uint64_t gen) {
+  const uint64_t d = v ^ gen;
+  Stop st = {0, 0};
+  if (d != 0 && (d & ((1ull << 40) - 1)) == 0) {
+    st.code = (int32_t)(d >> 56);
+    st.layer = (int32_t)((d >> 40) & 0xFFFF);
+  }
+  return st;
+}
+
+// Records a stop unless one is recorded already (the first one stays).
+__device__ __forceinline__ void publish_stop(const StreamCtl &k, uint64_t seen, int32_t layer,
+                                             int32_t code) {
+  const uint64_t v = k.gen ^ (((uint64_t)code << 56) | ((uint64_t)layer << 40));
+  atomicCAS(reinterpret_cast<unsigned long long *>(k.mirror + kStopWord),
+            (unsigned long long)seen, (unsigned long long)v);
+}
+
+// Thread 0 of a CTA: waits until layer l may move.  Returns 0 to go on, else the stop code.
+__device__ int32_t row_wait(const StreamCtl &k, int32_t l, bool owner) {
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t sleep_ns = 32;
+  for (uint32_t it = 0;; ++it) {
+    const uint64_t sw = ld_relaxed_gpu(k.mirror + kStopWord);
+    const uint64_t m = ld_acquire_gpu(k.mirror + 1 + l);
+    const Stop st = decode_stop(sw, k.gen);
+    if (st.code && l >= st.layer) return st.code;
+    if (m == k.gen) return 0;
+    if (owner || it == 0 || (it & 15) == 15) {
+      const int32_t e = k.epoch_word ? ld_relaxed_sys(k.epoch_word) : k.epoch;
+      if (e != k.epoch) {  // cancelled: every layer not started is dropped
+        publish_stop(k, sw, 0, KVX_ERR_CANCELLED);
+        return KVX_ERR_CANCELLED;
+      }
+      if (!k.layer_ready || ld_acquire_sys(k.layer_ready + l) >= k.ready_value) {
+        st_release_gpu(k.mirror + 1 + l, k.gen);
+        return 0;
+      }
+    }
+    if (globaltimer_ns() - t0 >= (uint64_t)k.wait_ns || it >= kMaxPolls) {
+      publish_stop(k, sw, l, KVX_ERR_TIMEOUT);
+      return KVX_ERR_TIMEOUT;
+    }
+    __nanosleep(sleep_ns);
+    if (sleep_ns < kMaxSleepNs) sleep_ns <<= 1;
+  }
+}
+
+// kTail: rows over 2 KiB (more than one pass of the warp), a separate instance as in the row
+// kernel so that the common instances keep every value in registers.
+template <bool kSrcHnd, bool kDstHnd, bool kTail>
+__global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8)
+    stream_row_kernel(const __grid_constant__ StreamArgs s) {
+  __shared__ int32_t s_stop;  // first layer this CTA does not move
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the epilogue may queue
+  const CopyArgs &a = s.c;
+  const StreamCtl &k = s.k;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t i0 = blockIdx.x * kWarps;  // the CTA's first item (< k.items)
+  const uint32_t i = i0 + warp;
+  const int32_t gsh = a.row_group_shift, lsh = 5 - gsh;
+  const uint32_t ic = i < k.items ? i : i0;
+  const int32_t l = (int32_t)(ic / k.per_layer);
+  const uint32_t r = ic - (uint32_t)l * k.per_layer;
+  const int32_t kv = r >= k.groups ? 1 : 0;
+  const int64_t t = ((int64_t)(r - kv * k.groups) << gsh) + (lane >> lsh);
+  const bool sp = a.src.is_pool != 0, dp = a.dst.is_pool != 0;
+  // slot indices and their range checks go out before the wait
+  bool ok = i < k.items && t < a.n_tokens;
+  const int64_t tt = ok ? t : 0;
+  const int32_t si = sp ? a.spec_src[tt] : (int32_t)tt;
+  const int32_t di = dp ? a.spec_dst[tt] : (int32_t)tt;
+  ok = ok && (!sp || (si >= 0 && (int64_t)si < a.src.num_slots)) &&
+       (!dp || (di >= 0 && (int64_t)di < a.dst.num_slots));
+  if (threadIdx.x == 0) {
+    int32_t stop = 1 << 30;
+    if (k.layer_ready || k.epoch_word) {
+      const uint32_t i1 = min(i0 + kWarps, k.items) - 1;
+      const int32_t l0 = (int32_t)(i0 / k.per_layer), l1 = (int32_t)(i1 / k.per_layer);
+      for (int32_t ll = l0; ll <= l1; ++ll) {
+        const uint32_t bs = (uint32_t)kWarps;
+        const bool owner = blockIdx.x == (uint32_t)(((uint64_t)ll * k.per_layer) / bs);
+        const int32_t code = row_wait(k, ll, owner);
+        if (code) {  // layers of this CTA below ll passed their wait: they still move
+          stop = ll;
+          atomicMax(&a.status[2], code);
+          atomicMax(&a.status[1], k.layers - stop);
+          break;
+        }
+      }
+    }
+    s_stop = stop;
+  }
+  __syncthreads();  // thread 0's acquire of the layer orders every thread's row loads
+  if (l >= s_stop) ok = false;
+  const int32_t p = 2 * l + kv;
+  const int32_t R = a.row_bytes, vpr = R >> 4;
+  const int32_t li = lane & ((1 << lsh) - 1);
+  const char *buf_plane = a.buf + (int64_t)p * a.n_tokens * R;
+  const char *srow = row_base<kSrcHnd>(a.src, sp, a.src_planes[p], buf_plane, si, R);
+  char *drow = const_cast<char *>(row_base<kDstHnd>(a.dst, dp, a.dst_planes[p], buf_plane, di, R));
+  uint4 v[kUnroll];
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const int32_t xv = li + (u << lsh);
+    if (ok && xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
+  }
+  pdl_wait();  // the planner has checked every index and written status[0]
+  if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK || !ok) return;
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const int32_t xv = li + (u << lsh);
+    if (xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), v[u]);
+  }
+  if constexpr (kTail) {
+    for (int32_t x0 = kUnroll << lsh; x0 < vpr; x0 += kUnroll << lsh) {
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int32_t xv = x0 + li + (u << lsh);
+        if (xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int32_t xv = x0 + li + (u << lsh);
+        if (xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), v[u]);
+      }
+    }
+  }
+}
+
+// Behind the row grid: once every CTA has finished (griddepcontrol.wait), the stop code joins
+// the verdict and the "no further write" words are set.
+__global__ void stream_done_kernel(int32_t *status, int32_t *host_done, int32_t layers) {
+  pdl_wait();
+  if (status[0] != KVX_OK) status[1] = layers;  // the planner refused the request: nothing moved
+  const int32_t code = status[2];
+  if (code) atomicMax(&status[0], code);
+  status[2] = 0;
+  __threadfence_system();
+  st_release_sys(&status[3], 1);
+  if (host_done) st_release_sys(host_done, 1);
+}
+
+template <bool kTail>
+const void *stream_row_fn_of(bool sh, bool dh) {
+  if (sh && dh) return reinterpret_cast<const void *>(stream_row_kernel<true, true, kTail>);
+  if (sh) return reinterpret_cast<const void *>(stream_row_kernel<true, false, kTail>);
+  if (dh) return reinterpret_cast<const void *>(stream_row_kernel<false, true, kTail>);
+  return reinterpret_cast<const void *>(stream_row_kernel<false, false, kTail>);
+}
+
+cudaError_t launch_pdl_ex(const void *fn, unsigned grid, unsigned block, void **params,
+                          cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, params);
+  if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) {
+    (void)cudaGetLastError();  // no programmatic dependent launch here: plain stream order
+    cfg.numAttrs = 0;
+    e = cudaLaunchKernelExC(&cfg, fn, params);
+  }
+  return e;
+}
+
 const void *stream_fn(bool sh, bool dh) {
   if (sh && dh) return reinterpret_cast<const void *>(stream_kernel<true, true>);
   if (sh) return reinterpret_cast<const void *>(stream_kernel<true, false>);
@@ -259,24 +474,27 @@ cudaError_t launch_stream(const CopyArgs &c, const StreamCtl &k, int grid, cudaS
   args.c = c;
   args.k = k;
   const bool sh = c.src.hnd && c.src.is_pool, dh = c.dst.hnd && c.dst.is_pool;
-  const void *fn = stream_fn(sh, dh);
   void *params[] = {&args};
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kCopyThreads);
-  cfg.stream = s;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr.val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, params);
-  if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) {
-    (void)cudaGetLastError();  // no programmatic dependent launch here: plain stream order
-    cfg.numAttrs = 0;
-    e = cudaLaunchKernelExC(&cfg, fn, params);
+  return launch_pdl_ex(stream_fn(sh, dh), (unsigned)grid, kCopyThreads, params, s);
+}
+
+cudaError_t launch_stream_rows(const CopyArgs &c, const StreamCtl &k, cudaStream_t s) {
+  static thread_local StreamArgs args;
+  args.c = c;
+  args.k = k;
+  const bool sh = c.src.hnd && c.src.is_pool, dh = c.dst.hnd && c.dst.is_pool;
+  const bool tail = c.row_bytes > kUnroll * 32 * 16;
+  const void *fn = tail ? stream_row_fn_of<true>(sh, dh) : stream_row_fn_of<false>(sh, dh);
+  void *params[] = {&args};
+  cudaError_t e = cudaSuccess;
+  if (k.items > 0) {
+    e = launch_pdl_ex(fn, (k.items + kWarps - 1) / kWarps, kCopyThreads, params, s);
+    if (e != cudaSuccess) return e;
   }
-  return e;
+  int32_t *status = c.status, *done = k.host_done;
+  int32_t layers = k.layers;
+  void *dparams[] = {&status, &done, &layers};
+  return launch_pdl_ex(reinterpret_cast<const void *>(stream_done_kernel), 1, 1, dparams, s);
 }
 
 }  // namespace kvx

@@ -320,8 +320,10 @@ typedef struct kvx_stream_ctl {
    * time ends the copy with KVX_ERR_TIMEOUT ([DistServe] "一次请求如何穿过 DistServe": every
    * abnormal path needs a lease or a timeout). */
   int64_t wait_ns;
-  /* Most CTAs (of 256 threads) the copy occupies for its whole duration; 0: as many as fit on
-   * the GPU.  A producer running on the same GPU needs SMs to make progress: leave it room. */
+  /* 0: one warp per row (group) on as many CTAs as the request needs; CTAs waiting for a
+   * layer hold their SM slots.  > 0: a persistent grid of at most max_ctas CTAs (of 256
+   * threads) for the whole move, leaving the rest of the GPU to a producer running on the
+   * same GPU, which needs SMs to make progress. */
   int32_t max_ctas;
   int32_t reserved;  /* must be 0 */
   /* Pinned host int32 or NULL: set to 1 when d_status[3] is (see kvx_stream). */
@@ -338,7 +340,7 @@ typedef struct kvx_stream_ctl {
  *   [1] layers pending: the trailing layers not guaranteed moved.  Layers
  *       0 .. num_layers - [1] - 1 hold every row of the request; rows of later layers may or
  *       may not have been written.  0 when [0] is KVX_OK.
- *   [2] internal (CTAs finished).
+ *   [2] internal.
  *   [3] 1 once every CTA of the copy has finished and its writes are visible system-wide: no
  *       further write of this call can land ([PD-budget] "最难的一个问题": the sender may only
  *       acknowledge an aborted transfer once it can prove no late write is still in flight).

@@ -41,6 +41,12 @@ def _cuda():
     yield
 
 
+# max_ctas: 0 = one warp per row group (default grid); 40 = a persistent grid of 40 CTAs
+@pytest.fixture(params=[0, 40], ids=["rowgrid", "persistent40"])
+def grid(request):
+    return request.param
+
+
 def _rng(k):
     return np.random.Generator(np.random.PCG64(5000 + k))
 
@@ -96,13 +102,13 @@ def _run_transfer(src, dst, s, d, n, st, **kw):
 @pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("n", [1, 777, 2500])
 @pytest.mark.parametrize("ready", ["none", "device_words"])
-def test_stream_transfer_all_ready(kind, n, ready):
+def test_stream_transfer_all_ready(kind, n, ready, grid):
     src, dst, s, d, exp = _transfer_case(kind, n, seed=n)
     st = _status()
     rw = None
     if ready == "device_words":
         rw = torch.full((SH["L"],), 3, dtype=torch.int32, device="cuda")
-    _run_transfer(src, dst, s, d, n, st, layer_ready=rw, ready_value=3)
+    _run_transfer(src, dst, s, d, n, st, layer_ready=rw, ready_value=3, max_ctas=grid)
     torch.cuda.synchronize()
     v = st.cpu().tolist()
     assert v[0] == kvx.OK and v[1] == 0 and v[3] == 1, v
@@ -111,7 +117,7 @@ def test_stream_transfer_all_ready(kind, n, ready):
 
 
 @pytest.mark.parametrize("kind", KINDS)
-def test_stream_gather_and_scatter(kind):
+def test_stream_gather_and_scatter(kind, grid):
     n = 1500
     g = _rng(77)
     src = _pool(kind, "normal", g)
@@ -122,7 +128,8 @@ def test_stream_gather_and_scatter(kind):
                          fill="sentinel").to_device()
     st = _status()
     kvx.stream(kvx.OP_GATHER, hz.kvx_layout(src), hz.dev_i32(s), None, None, n,
-               hz.GUARD + buf.dev.data_ptr(), hz.workspace(n), st, buf_bytes=len(want))
+               hz.GUARD + buf.dev.data_ptr(), hz.workspace(n), st, buf_bytes=len(want),
+               max_ctas=grid)
     torch.cuda.synchronize()
     assert st.cpu().tolist()[0:2] == [kvx.OK, 0]
     exp_buf = buf.host.copy()
@@ -136,7 +143,8 @@ def test_stream_gather_and_scatter(kind):
     assert oracle.scatter(hz.oracle_pool(exp), d, want)[0] == oracle.OK
     st2 = _status()
     kvx.stream(kvx.OP_SCATTER, None, None, hz.kvx_layout(dst), hz.dev_i32(d), n,
-               hz.GUARD + buf.dev.data_ptr(), hz.workspace(n), st2, buf_bytes=len(want))
+               hz.GUARD + buf.dev.data_ptr(), hz.workspace(n), st2, buf_bytes=len(want),
+               max_ctas=grid)
     torch.cuda.synchronize()
     assert st2.cpu().tolist()[0:2] == [kvx.OK, 0]
     hz.assert_same_bytes(dst.readback(), exp.host, f"stream scatter {kind}")
@@ -156,10 +164,10 @@ def test_stream_2k_rows_few_ctas():
     hz.assert_same_bytes(dst.readback(), exp.host, "stream 2k rows, 3 CTAs")
 
 
-def test_stream_n0_and_out_of_range():
+def test_stream_n0_and_out_of_range(grid):
     src, dst, s, d, exp = _transfer_case("planes", 300, seed=120)
     st = _status()
-    _run_transfer(src, dst, s, d, 0, st)
+    _run_transfer(src, dst, s, d, 0, st, max_ctas=grid)
     torch.cuda.synchronize()
     v = st.cpu().tolist()
     assert v[0] == kvx.OK and v[1] == 0 and v[3] == 1, v
@@ -168,7 +176,7 @@ def test_stream_n0_and_out_of_range():
     d_bad = d.copy()
     d_bad[-1] = dst.num_slots  # one past the end: nothing may move
     st = _status()
-    _run_transfer(src, dst, s, d_bad, 300, st)
+    _run_transfer(src, dst, s, d_bad, 300, st, max_ctas=grid)
     torch.cuda.synchronize()
     v = st.cpu().tolist()
     assert v[0] == kvx.ERR_OUT_OF_RANGE and v[1] == SH["L"] and v[3] == 1, v
@@ -178,7 +186,7 @@ def test_stream_n0_and_out_of_range():
 # ---- layers raised by the host after the launch --------------------------------------------
 
 @pytest.mark.parametrize("sh", [SH, SH2K], ids=["256B", "2KiB"])
-def test_stream_layers_raised_late(sh):
+def test_stream_layers_raised_late(sh, grid):
     n = 1024
     src, dst, s, d, exp = _transfer_case("planes", n, sh=sh, seed=140)
     ready = _pinned_i32([0] * sh["L"])
@@ -188,7 +196,7 @@ def test_stream_layers_raised_late(sh):
     torch.cuda.synchronize()
     kvx.stream(kvx.OP_TRANSFER, hz.kvx_layout(src), sd, hz.kvx_layout(dst), dd, n, None, ws, st,
                layer_ready=ready, ready_value=1, wait_ns=2_000_000_000, host_done=done,
-               buf_bytes=0)
+               max_ctas=grid, buf_bytes=0)
     for layer in range(sh["L"]):
         time.sleep(0.01)
         assert int(done[0]) == 0, f"finished before layer {layer} was raised"
@@ -204,7 +212,7 @@ def test_stream_layers_raised_late(sh):
 
 @pytest.mark.parametrize("kind", ["planes", "slot_major"])
 @pytest.mark.parametrize("k", [0, 4])
-def test_stream_timeout_at_layer(kind, k):
+def test_stream_timeout_at_layer(kind, k, grid):
     n = 900
     src, dst, s, d, exp = _transfer_case(kind, n, seed=160 + k)
     orig = _expected_pool(kind, dst.num_slots, 5)
@@ -214,7 +222,7 @@ def test_stream_timeout_at_layer(kind, k):
     st = _status()
     t0 = time.perf_counter()
     _run_transfer(src, dst, s, d, n, st, layer_ready=ready, ready_value=1, wait_ns=30_000_000,
-                  host_done=done)
+                  host_done=done, max_ctas=grid)
     torch.cuda.synchronize()
     elapsed = time.perf_counter() - t0
     v = st.cpu().tolist()
@@ -226,7 +234,7 @@ def test_stream_timeout_at_layer(kind, k):
 
 # ---- cancellation through the epoch word ---------------------------------------------------
 
-def test_stream_cancel_while_waiting():
+def test_stream_cancel_while_waiting(grid):
     n, k = 1200, 3
     src, dst, s, d, exp = _transfer_case("planes", n, seed=180)
     orig = _expected_pool("planes", dst.num_slots, 5)
@@ -240,7 +248,7 @@ def test_stream_cancel_while_waiting():
     t0 = time.perf_counter()
     kvx.stream(kvx.OP_TRANSFER, hz.kvx_layout(src), sd, hz.kvx_layout(dst), dd, n, None, ws, st,
                layer_ready=ready, ready_value=1, epoch_word=epoch, epoch=41,
-               wait_ns=5_000_000_000, host_done=done, buf_bytes=0)
+               wait_ns=5_000_000_000, host_done=done, max_ctas=grid, buf_bytes=0)
     time.sleep(0.05)
     assert int(done[0]) == 0  # still waiting for layer k
     epoch[0] = 42             # the receiver gives up on the request
@@ -256,13 +264,13 @@ def test_stream_cancel_while_waiting():
     hz.assert_same_bytes(dst.readback(), exp.host, "cancelled while waiting")
 
 
-def test_stream_cancelled_before_launch():
+def test_stream_cancelled_before_launch(grid):
     n = 500
     src, dst, s, d, _ = _transfer_case("hnd", n, seed=200)
     before = dst.readback()
     epoch = torch.tensor([7], dtype=torch.int32, device="cuda")  # device epoch word
     st = _status()
-    _run_transfer(src, dst, s, d, n, st, epoch_word=epoch, epoch=6)
+    _run_transfer(src, dst, s, d, n, st, epoch_word=epoch, epoch=6, max_ctas=grid)
     torch.cuda.synchronize()
     v = st.cpu().tolist()
     assert v[0] == kvx.ERR_CANCELLED and v[1] == SH["L"] and v[3] == 1, v
