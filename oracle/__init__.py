@@ -96,6 +96,8 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
                                  P(ctypes.c_int64)]
     lib.kvxo_transfer.argtypes = [P(_Pool), i32p, P(_Pool), i32p, ctypes.c_int64, ctypes.c_int,
                                   P(ctypes.c_int64)]
+    lib.kvxo_transfer_layers.argtypes = [P(_Pool), i32p, P(_Pool), i32p, ctypes.c_int64,
+                                         ctypes.c_int32, P(ctypes.c_int64)]
     lib.kvxo_hnd_gather.argtypes = [P(_Pool), i32p, ctypes.c_int64, u8p]
     lib.kvxo_hnd_rebuild.argtypes = [P(_Pool), i32p, ctypes.c_int64, u8p]
     lib.kvxo_batch.argtypes = [P(_Pool), P(_Pool), P(Request), ctypes.c_int32, i32p,
@@ -194,6 +196,18 @@ def transfer(src: Pool, src_slots, dst: Pool, dst_slots, check_dup: bool = False
     s1, s2 = src._struct(), dst._struct()
     rc = lib.kvxo_transfer(ctypes.byref(s1), _i32p(a), ctypes.byref(s2), _i32p(b), len(a),
                            int(check_dup), ctypes.byref(written))
+    return rc, written.value
+
+
+def transfer_layers(src: Pool, src_slots, dst: Pool, dst_slots, stop: int, lib=None):
+    """kvxo_transfer_layers: the transfer of layers 0 .. stop-1 only."""
+    lib = lib or load()
+    a, b = _i32(src_slots), _i32(dst_slots)
+    assert len(a) == len(b)
+    written = ctypes.c_int64(0)
+    s1, s2 = src._struct(), dst._struct()
+    rc = lib.kvxo_transfer_layers(ctypes.byref(s1), _i32p(a), ctypes.byref(s2), _i32p(b), len(a),
+                                  int(stop), ctypes.byref(written))
     return rc, written.value
 
 

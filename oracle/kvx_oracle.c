@@ -132,6 +132,30 @@ static int check_page_table(const kvxo_pool *pool, const int32_t *page_table, in
   return KVXO_OK;
 }
 
+int kvxo_transfer_layers(const kvxo_pool *src, const int32_t *src_slots, const kvxo_pool *dst,
+                         const int32_t *dst_slots, int64_t n, int32_t stop,
+                         int64_t *bytes_written) {
+  /* [DistServe] 一次请求如何穿过 DistServe: prefill writes the prompt's KV layer by layer and
+   * decode pulls layer j once it exists.  A layer-streamed move that stopped before layer
+   * `stop` has moved exactly the rows of layers 0 .. stop-1 (planes 2l and 2l+1), as
+   * kvxo_transfer moves them; the planes of later layers are untouched. */
+  int64_t hb = head_bytes(src);
+  int rc;
+  if (!same_row_shape(src, dst) || stop < 0 || stop > src->num_layers)
+    return KVXO_ERR_INVALID_ARG;
+  rc = kvxo_check_slots(src, src_slots, n);
+  if (rc == KVXO_OK) rc = kvxo_check_slots(dst, dst_slots, n);
+  if (rc != KVXO_OK) return rc;
+  for (int32_t layer = 0; layer < stop; ++layer)
+    for (int32_t kv = 0; kv < 2; ++kv)
+      for (int64_t i = 0; i < n; ++i)
+        for (int32_t h = 0; h < src->kv_heads; ++h)
+          memcpy(head_vec(dst, 2 * layer + kv, dst_slots[i], h),
+                 head_vec(src, 2 * layer + kv, src_slots[i], h), (size_t)hb);
+  if (bytes_written) *bytes_written = n * 2 * (int64_t)stop * kvxo_row_bytes(src);
+  return KVXO_OK;
+}
+
 int kvxo_hnd_gather(const kvxo_pool *src, const int32_t *page_table, int64_t seq_len,
                     uint8_t *buf) {
   /* [mini-infer] KV 序列化格式选择: take the per-layer [heads, seq, dim] cache and permute

@@ -110,6 +110,13 @@ int kvxo_scatter(const kvxo_pool *dst, const int32_t *slots, int64_t n, const ui
 int kvxo_transfer(const kvxo_pool *src, const int32_t *src_slots, const kvxo_pool *dst,
                   const int32_t *dst_slots, int64_t n, int check_dup, int64_t *bytes_written);
 
+/* kvxo_transfer restricted to the layers before `stop` (0 <= stop <= num_layers): what a
+ * layer-streamed move that stopped before layer `stop` has written.  Planes 2l and 2l+1 of
+ * every layer l < stop are moved; later planes are untouched.  Written bytes: n * 2 * stop * R. */
+int kvxo_transfer_layers(const kvxo_pool *src, const int32_t *src_slots, const kvxo_pool *dst,
+                         const int32_t *dst_slots, int64_t n, int32_t stop,
+                         int64_t *bytes_written);
+
 /* HND gather by page table, through the logical per-plane [heads][seq][dim] view, then the
  * [heads,seq,dim] -> [seq,heads,dim] permute of [mini-infer] "KV 序列化格式选择".
  * Token s lives in page page_table[s / page_size] at offset s % page_size. */

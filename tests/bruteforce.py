@@ -123,6 +123,19 @@ def transfer(src: BFPool, src_slots, dst: BFPool, dst_slots) -> BFPool:
     return res
 
 
+def transfer_layers(src: BFPool, src_slots, dst: BFPool, dst_slots, stop: int) -> BFPool:
+    """transfer() of the layers before `stop` only."""
+    res = dst.copy()
+    for layer in range(stop):
+        for kv in range(2):
+            for i in range(len(src_slots)):
+                for h in range(src.H):
+                    for d in range(src.D):
+                        res.set(layer, kv, int(dst_slots[i]), h, d,
+                                src.get(layer, kv, int(src_slots[i]), h, d))
+    return res
+
+
 def hnd_gather(pool: BFPool, page_table, seq_len) -> np.ndarray:
     """[layer][kv][s][h][d] = element (h, s, d) of the page-table view."""
     out = np.zeros((pool.L, 2, seq_len, pool.H, pool.D), np.uint16)

@@ -115,6 +115,32 @@ def pin_bruteforce_transfer(lib):
                     assert np.array_equal(src.data, src_before), "source modified"
 
 
+def pin_bruteforce_transfer_layers(lib):
+    """Every stop layer (0 .. L) of a layer-streamed transfer, for every pair of layouts and
+    every injective map with n <= 2; bytes written = n * 2 * stop * R; stop outside [0, L]
+    refused with nothing written."""
+    layouts = (("planes", 1), ("slot_major", 1), ("hnd", 2))
+    R = H * D * 2
+    for (la, pa), (lb, pb) in itertools.product(layouts, layouts):
+        src = bf.make_pool(la, L, H, D, 4, _arange_fill(3), page_size=pa)
+        base = bf.make_pool(lb, L, H, D, 4, _sentinel_fill, page_size=pb)
+        for n in range(3):
+            for s in itertools.permutations(range(4), n):
+                d = tuple(reversed(range(4)))[:n]
+                for stop in range(L + 1):
+                    want = bf.transfer_layers(src, s, base, d, stop)
+                    dst = base.copy()
+                    rc, written = oracle.transfer_layers(bf.to_oracle(src), list(s),
+                                                         bf.to_oracle(dst), list(d), stop, lib=lib)
+                    assert rc == oracle.OK and written == n * 2 * stop * R
+                    assert np.array_equal(dst.data, want.data), (la, lb, s, stop)
+        for bad in (-1, L + 1):
+            dst = base.copy()
+            rc, _ = oracle.transfer_layers(bf.to_oracle(src), [0], bf.to_oracle(dst), [1], bad,
+                                           lib=lib)
+            assert rc == oracle.ERR_INVALID_ARG and np.array_equal(dst.data, base.data)
+
+
 def pin_bruteforce_hnd(lib):
     """Every page table of k <= 3 pages out of a 4-page pool (page size 3), every sequence
     length that ends in page k, for the page-table gather and the inverse rebuild."""
@@ -357,6 +383,7 @@ def pin_plan(lib):
 
 
 ALL_PINS = [pin_sizes, pin_bytes_written, pin_bruteforce_gather, pin_bruteforce_scatter,
-            pin_bruteforce_transfer, pin_bruteforce_hnd, pin_roundtrip,
+            pin_bruteforce_transfer, pin_bruteforce_transfer_layers, pin_bruteforce_hnd,
+            pin_roundtrip,
             pin_transfer_is_scatter_of_gather, pin_hnd_roundtrip, pin_plane_locality,
             pin_numpy_special_cases, pin_validation, pin_batch, pin_plan]

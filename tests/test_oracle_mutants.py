@@ -39,6 +39,10 @@ MUTANTS = {
     "plan_tile_break_dropped": ("if (i == 0 || i % tile_tokens == 0) brk[i] = 1;",
                                 "if (i == 0) brk[i] = 1;"),
     "batch_status_not_per_request": ("status[1 + q] = rc;", "status[1 + q] = 0;"),
+    "layers_one_short": ("for (int32_t layer = 0; layer < stop; ++layer)",
+                         "for (int32_t layer = 0; layer + 1 < stop; ++layer)"),
+    "layers_v_plane_dropped": ("    for (int32_t kv = 0; kv < 2; ++kv)\n      for (int64_t i = 0; i < n; ++i)\n        for (int32_t h = 0; h < src->kv_heads; ++h)\n          memcpy(head_vec(dst, 2 * layer + kv",
+                               "    for (int32_t kv = 0; kv < 1; ++kv)\n      for (int64_t i = 0; i < n; ++i)\n        for (int32_t h = 0; h < src->kv_heads; ++h)\n          memcpy(head_vec(dst, 2 * layer + kv"),
     "transfer_src_dst_swapped": ("memcpy(head_vec(dst, p, dst_slots[i], h), head_vec(src, p, src_slots[i], h),",
                                  "memcpy(head_vec(src, p, src_slots[i], h), head_vec(dst, p, dst_slots[i], h),"),
 }
