@@ -73,22 +73,20 @@ def _status():
     return torch.full((4,), -1, dtype=torch.int32, device="cuda")
 
 
-def _keep_layers_below(exp, orig, k):
-    """exp with every plane of layer >= k put back to orig's bytes."""
-    if exp.kind == "slot_major":
-        exp.body[:, k:] = orig.body[:, k:]
-    else:
-        exp.body[2 * k:] = orig.body[2 * k:]
-
-
-def _transfer_case(kind, n, sh=SH, seed=0):
+def _transfer_case(kind, n, sh=SH, seed=0, stop=None):
+    """Pools, slot lists and the oracle's expected destination: the whole transfer, or (stop)
+    the transfer of the layers before `stop` only."""
     g = _rng(seed)
     src = _pool(kind, "normal", g, sh=sh)
     dst = _pool(kind, "sentinel", salt=5, sh=sh)
     s = _slots(seed + 1, n, src.num_slots)
     d = _slots(seed + 2, n, dst.num_slots)
     exp = _expected_pool(kind, dst.num_slots, 5, sh=sh)
-    assert oracle.transfer(hz.oracle_pool(src), s, hz.oracle_pool(exp), d)[0] == oracle.OK
+    if stop is None:
+        rc, _ = oracle.transfer(hz.oracle_pool(src), s, hz.oracle_pool(exp), d)
+    else:
+        rc, _ = oracle.transfer_layers(hz.oracle_pool(src), s, hz.oracle_pool(exp), d, stop)
+    assert rc == oracle.OK
     return src, dst, s, d, exp
 
 
@@ -214,9 +212,7 @@ def test_stream_layers_raised_late(sh, grid):
 @pytest.mark.parametrize("k", [0, 4])
 def test_stream_timeout_at_layer(kind, k, grid):
     n = 900
-    src, dst, s, d, exp = _transfer_case(kind, n, seed=160 + k)
-    orig = _expected_pool(kind, dst.num_slots, 5)
-    _keep_layers_below(exp, orig, k)
+    src, dst, s, d, exp = _transfer_case(kind, n, seed=160 + k, stop=k)
     ready = _pinned_i32([1 if layer < k else 0 for layer in range(SH["L"])])
     done = _pinned_i32([0])
     st = _status()
@@ -236,9 +232,7 @@ def test_stream_timeout_at_layer(kind, k, grid):
 
 def test_stream_cancel_while_waiting(grid):
     n, k = 1200, 3
-    src, dst, s, d, exp = _transfer_case("planes", n, seed=180)
-    orig = _expected_pool("planes", dst.num_slots, 5)
-    _keep_layers_below(exp, orig, k)
+    src, dst, s, d, exp = _transfer_case("planes", n, seed=180, stop=k)
     ready = _pinned_i32([1 if layer < k else 0 for layer in range(SH["L"])])
     epoch = _pinned_i32([41])
     done = _pinned_i32([0])
