@@ -98,6 +98,10 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
                                   P(ctypes.c_int64)]
     lib.kvxo_transfer_layers.argtypes = [P(_Pool), i32p, P(_Pool), i32p, ctypes.c_int64,
                                          ctypes.c_int32, P(ctypes.c_int64)]
+    lib.kvxo_move_heads.argtypes = [ctypes.c_int32, P(_Pool), i32p, ctypes.c_int32, P(_Pool),
+                                    i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, u8p,
+                                    P(ctypes.c_int64)]
+    lib.kvxo_tp_slice.argtypes = [ctypes.c_int32] * 5 + [P(ctypes.c_int32)] * 3
     lib.kvxo_hnd_gather.argtypes = [P(_Pool), i32p, ctypes.c_int64, u8p]
     lib.kvxo_hnd_rebuild.argtypes = [P(_Pool), i32p, ctypes.c_int64, u8p]
     lib.kvxo_batch.argtypes = [P(_Pool), P(_Pool), P(Request), ctypes.c_int32, i32p,
@@ -209,6 +213,38 @@ def transfer_layers(src: Pool, src_slots, dst: Pool, dst_slots, stop: int, lib=N
     rc = lib.kvxo_transfer_layers(ctypes.byref(s1), _i32p(a), ctypes.byref(s2), _i32p(b), len(a),
                                   int(stop), ctypes.byref(written))
     return rc, written.value
+
+
+def move_heads(op: int, src: Optional[Pool], src_slots, src_head0: int, dst: Optional[Pool],
+               dst_slots, dst_head0: int, n_heads: int, n: int, buf: Optional[np.ndarray] = None,
+               lib=None):
+    """kvxo_move_heads.  op 0 gather returns (status, buffer bytes); 1 scatter reads ``buf``;
+    2 transfer.  Returns (status, buffer or None, bytes written)."""
+    lib = lib or load()
+    a = _i32(src_slots if src_slots is not None else [])
+    b = _i32(dst_slots if dst_slots is not None else [])
+    shape = dst if op == 1 else src
+    if op == 0:
+        buf = np.zeros(max(1, shape.num_planes * n * n_heads * shape.head_dim * shape.elem_bytes),
+                       dtype=np.uint8)
+    written = ctypes.c_int64(0)
+    s1 = src._struct() if src is not None else None
+    s2 = dst._struct() if dst is not None else None
+    bp = np.ascontiguousarray(buf).view(np.uint8) if buf is not None else None
+    rc = lib.kvxo_move_heads(op, ctypes.byref(s1) if s1 is not None else None, _i32p(a),
+                             src_head0, ctypes.byref(s2) if s2 is not None else None, _i32p(b),
+                             dst_head0, n_heads, n, bp.ctypes.data if bp is not None else None,
+                             ctypes.byref(written))
+    return rc, (bp if op == 0 else None), written.value
+
+
+def tp_slice(heads: int, p_tp: int, p_rank: int, d_tp: int, d_rank: int, lib=None):
+    """kvxo_tp_slice: (status, src_head0, dst_head0, n_heads)."""
+    lib = lib or load()
+    a, b, c = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    rc = lib.kvxo_tp_slice(heads, p_tp, p_rank, d_tp, d_rank, ctypes.byref(a), ctypes.byref(b),
+                           ctypes.byref(c))
+    return rc, a.value, b.value, c.value
 
 
 def hnd_gather(pool: Pool, page_table, seq_len: int, lib=None):

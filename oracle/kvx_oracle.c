@@ -156,6 +156,83 @@ int kvxo_transfer_layers(const kvxo_pool *src, const int32_t *src_slots, const k
   return KVXO_OK;
 }
 
+int kvxo_move_heads(int32_t op, const kvxo_pool *src, const int32_t *src_slots,
+                    int32_t src_head0, const kvxo_pool *dst, const int32_t *dst_slots,
+                    int32_t dst_head0, int32_t n_heads, int64_t n, uint8_t *buf,
+                    int64_t *bytes_written) {
+  /* [Mooncake] 7.7 异构TP: with different tensor-parallel sizes on the two sides, one rank's
+   * KV shard is a range of kv heads of the other side's shard; the move takes, for every plane
+   * and token, head vectors src_head0 .. src_head0 + n_heads - 1 of the source row to head
+   * vectors dst_head0 .. dst_head0 + n_heads - 1 of the destination row. */
+  const kvxo_pool *shape = op == 1 ? dst : src;
+  int64_t hb;
+  int rc;
+  if (op < 0 || op > 2 || n_heads < 1 || !shape) return KVXO_ERR_INVALID_ARG;
+  if (op == 2 && (src->num_layers != dst->num_layers || src->head_dim != dst->head_dim ||
+                  src->elem_bytes != dst->elem_bytes))
+    return KVXO_ERR_INVALID_ARG;
+  if (op != 1 && (src_head0 < 0 || src_head0 + n_heads > src->kv_heads))
+    return KVXO_ERR_INVALID_ARG;
+  if (op != 0 && (dst_head0 < 0 || dst_head0 + n_heads > dst->kv_heads))
+    return KVXO_ERR_INVALID_ARG;
+  rc = op != 1 ? kvxo_check_slots(src, src_slots, n) : KVXO_OK;
+  if (rc == KVXO_OK && op != 0) rc = kvxo_check_slots(dst, dst_slots, n);
+  if (rc != KVXO_OK) return rc;
+  hb = head_bytes(shape);
+  for (int32_t p = 0; p < num_planes(shape); ++p)
+    for (int64_t i = 0; i < n; ++i)
+      for (int32_t j = 0; j < n_heads; ++j) {
+        /* the buffer holds the n_heads moved heads: [plane][n][n_heads][dim] */
+        uint8_t *b = buf + (((int64_t)p * n + i) * n_heads + j) * hb;
+        if (op == 0)
+          memcpy(b, head_vec(src, p, src_slots[i], src_head0 + j), (size_t)hb);
+        else if (op == 1)
+          memcpy(head_vec(dst, p, dst_slots[i], dst_head0 + j), b, (size_t)hb);
+        else
+          memcpy(head_vec(dst, p, dst_slots[i], dst_head0 + j),
+                 head_vec(src, p, src_slots[i], src_head0 + j), (size_t)hb);
+      }
+  if (bytes_written) *bytes_written = n * num_planes(shape) * n_heads * hb;
+  return KVXO_OK;
+}
+
+/* Heads [*first, *first + *count) held by rank r of a tensor-parallel group of size t. */
+static int tp_heads(int32_t heads, int32_t t, int32_t r, int32_t *first, int32_t *count) {
+  if (heads < 1 || t < 1 || r < 0 || r >= t) return KVXO_ERR_INVALID_ARG;
+  if (t <= heads) {
+    if (heads % t != 0) return KVXO_ERR_INVALID_ARG;
+    *first = r * (heads / t);
+    *count = heads / t;
+  } else {
+    if (t % heads != 0) return KVXO_ERR_INVALID_ARG;
+    *first = r / (t / heads); /* replicated: t / heads ranks hold the same head */
+    *count = 1;
+  }
+  return KVXO_OK;
+}
+
+int kvxo_tp_slice(int32_t heads, int32_t p_tp, int32_t p_rank, int32_t d_tp, int32_t d_rank,
+                  int32_t *src_head0, int32_t *dst_head0, int32_t *n_heads) {
+  /* [Mooncake] 7.7 异构TP: the sender's transfer plan -- whether this P rank sends to this D
+   * rank, where in its own shard the heads start, where they start in the D rank's shard and
+   * how many.  Of the P ranks holding the same (replicated) head, the lowest-numbered sends. */
+  int32_t pf, pc, df, dc, lo, hi;
+  int rc = tp_heads(heads, p_tp, p_rank, &pf, &pc);
+  if (rc == KVXO_OK) rc = tp_heads(heads, d_tp, d_rank, &df, &dc);
+  if (rc != KVXO_OK) return rc;
+  lo = pf > df ? pf : df;
+  hi = (pf + pc) < (df + dc) ? (pf + pc) : (df + dc);
+  *src_head0 = 0;
+  *dst_head0 = 0;
+  *n_heads = 0;
+  if (hi <= lo) return KVXO_OK;
+  if (p_tp > heads && p_rank % (p_tp / heads) != 0) return KVXO_OK; /* another replica sends */
+  *src_head0 = lo - pf;
+  *dst_head0 = lo - df;
+  *n_heads = hi - lo;
+  return KVXO_OK;
+}
+
 int kvxo_hnd_gather(const kvxo_pool *src, const int32_t *page_table, int64_t seq_len,
                     uint8_t *buf) {
   /* [mini-infer] KV 序列化格式选择: take the per-layer [heads, seq, dim] cache and permute

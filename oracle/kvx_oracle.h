@@ -117,6 +117,26 @@ int kvxo_transfer_layers(const kvxo_pool *src, const int32_t *src_slots, const k
                          const int32_t *dst_slots, int64_t n, int32_t stop,
                          int64_t *bytes_written);
 
+/* Head-range move between pools whose kv_heads differ ([Mooncake] 7.7 异构TP).  op: 0 gather
+ * (src -> buf [plane][n][n_heads][head_dim]), 1 scatter (buf -> dst), 2 transfer (src ->
+ * dst).  For every plane and token i, heads src_head0 .. src_head0 + n_heads - 1 of source
+ * row i go to heads dst_head0 .. of destination row i.  The pools share num_layers, head_dim
+ * and elem_bytes.  Errors: KVXO_ERR_INVALID_ARG (bad op, geometry or head range),
+ * KVXO_ERR_OUT_OF_RANGE; nothing written on error. */
+int kvxo_move_heads(int32_t op, const kvxo_pool *src, const int32_t *src_slots,
+                    int32_t src_head0, const kvxo_pool *dst, const int32_t *dst_slots,
+                    int32_t dst_head0, int32_t n_heads, int64_t n, uint8_t *buf,
+                    int64_t *bytes_written);
+
+/* The transfer plan between P rank p_rank of a tensor-parallel group of size p_tp and D rank
+ * d_rank of a group of size d_tp, for a model with `heads` kv heads ([Mooncake] 7.7 异构TP).
+ * Rank r of a group of size t holds heads [r*heads/t, (r+1)*heads/t) (t <= heads, t divides
+ * heads) or the single head r/(t/heads) (t > heads, heads divides t).  Output: the first
+ * head to send in the P rank's shard, the first head in the D rank's shard, and the count
+ * (0: nothing to send; of P ranks holding the same head only the lowest-numbered sends). */
+int kvxo_tp_slice(int32_t heads, int32_t p_tp, int32_t p_rank, int32_t d_tp, int32_t d_rank,
+                  int32_t *src_head0, int32_t *dst_head0, int32_t *n_heads);
+
 /* HND gather by page table, through the logical per-plane [heads][seq][dim] view, then the
  * [heads,seq,dim] -> [seq,heads,dim] permute of [mini-infer] "KV 序列化格式选择".
  * Token s lives in page page_table[s / page_size] at offset s % page_size. */

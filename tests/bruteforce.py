@@ -136,6 +136,30 @@ def transfer_layers(src: BFPool, src_slots, dst: BFPool, dst_slots, stop: int) -
     return res
 
 
+def move_heads(op, src: BFPool, src_slots, h0, dst: BFPool, dst_slots, g0, nh, buf=None):
+    """Head-range move, element by element.  op 0: returns the buffer [layer][kv][n][nh][D];
+    op 1 (buffer -> dst) and op 2 (src -> dst): return the new destination pool."""
+    shape = dst if op == 1 else src
+    n = len(dst_slots) if op == 1 else len(src_slots)
+    if op == 0:
+        out = np.zeros((shape.L, 2, n, nh, shape.D), np.uint16)
+    else:
+        out = dst.copy()
+    for layer in range(shape.L):
+        for kv in range(2):
+            for i in range(n):
+                for j in range(nh):
+                    for d in range(shape.D):
+                        if op == 0:
+                            out[layer, kv, i, j, d] = src.get(layer, kv, int(src_slots[i]), h0 + j, d)
+                        elif op == 1:
+                            out.set(layer, kv, int(dst_slots[i]), g0 + j, d, buf[layer, kv, i, j, d])
+                        else:
+                            out.set(layer, kv, int(dst_slots[i]), g0 + j, d,
+                                    src.get(layer, kv, int(src_slots[i]), h0 + j, d))
+    return out
+
+
 def hnd_gather(pool: BFPool, page_table, seq_len) -> np.ndarray:
     """[layer][kv][s][h][d] = element (h, s, d) of the page-table view."""
     out = np.zeros((pool.L, 2, seq_len, pool.H, pool.D), np.uint16)

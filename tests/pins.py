@@ -141,6 +141,101 @@ def pin_bruteforce_transfer_layers(lib):
             assert rc == oracle.ERR_INVALID_ARG and np.array_equal(dst.data, base.data)
 
 
+def pin_bruteforce_move_heads(lib):
+    """Head-range gather / scatter / transfer between pools with different kv_heads, for every
+    pair of layouts, every valid (src_head0, dst_head0, n_heads) and n <= 2; bad head ranges
+    refused with nothing written."""
+    layouts = (("planes", 1), ("slot_major", 1), ("hnd", 2))
+    for (la, pa), (lb, pb) in itertools.product(layouts, layouts):
+        for hs, hd in ((3, 2), (2, 3), (1, 2)):
+            src = bf.make_pool(la, L, hs, D, 4, _arange_fill(5), page_size=pa)
+            base = bf.make_pool(lb, L, hd, D, 4, _sentinel_fill, page_size=pb)
+            for nh in range(1, min(hs, hd) + 1):
+                for h0 in range(hs - nh + 1):
+                    for g0 in range(hd - nh + 1):
+                        for n in (1, 2):
+                            s_, d_ = [3, 0][:n], [1, 2][:n]
+                            want = bf.move_heads(2, src, s_, h0, base, d_, g0, nh)
+                            dst = base.copy()
+                            rc, _, w = oracle.move_heads(2, bf.to_oracle(src), s_, h0,
+                                                         bf.to_oracle(dst), d_, g0, nh, n, lib=lib)
+                            assert rc == oracle.OK and w == n * 2 * L * nh * D * 2
+                            assert np.array_equal(dst.data, want.data), (la, lb, hs, hd, h0, g0, nh)
+                            rc, got, _ = oracle.move_heads(0, bf.to_oracle(src), s_, h0, None, None,
+                                                           0, nh, n, lib=lib)
+                            gb = bf.move_heads(0, src, s_, h0, None, None, 0, nh)
+                            assert rc == oracle.OK
+                            assert np.array_equal(got[: gb.size * 2].view(np.uint16), gb.ravel())
+                            dst = base.copy()
+                            rc, _, _ = oracle.move_heads(1, None, None, 0, bf.to_oracle(dst), d_,
+                                                         g0, nh, n, buf=gb.view(np.uint8), lib=lib)
+                            want = bf.move_heads(1, None, None, 0, base, d_, g0, nh, buf=gb)
+                            assert rc == oracle.OK and np.array_equal(dst.data, want.data)
+            for h0, g0, nh in ((hs, 0, 1), (0, hd, 1), (0, 0, 0), (-1, 0, 1)):
+                dst = base.copy()
+                rc, _, _ = oracle.move_heads(2, bf.to_oracle(src), [0], h0, bf.to_oracle(dst), [1],
+                                             g0, nh, 1, lib=lib)
+                assert rc == oracle.ERR_INVALID_ARG and np.array_equal(dst.data, base.data)
+
+
+def pin_move_heads_full_range_is_transfer(lib):
+    """Moving every head (same kv_heads on both sides) is the plain transfer."""
+    src = bf.make_pool("planes", L, H, D, 4, _arange_fill(7))
+    a = bf.make_pool("hnd", L, H, D, 4, _sentinel_fill, page_size=2)
+    b = a.copy()
+    rc1, _, _ = oracle.move_heads(2, bf.to_oracle(src), [2, 1], 0, bf.to_oracle(a), [0, 3], 0, H, 2,
+                                  lib=lib)
+    rc2, _ = oracle.transfer(bf.to_oracle(src), [2, 1], bf.to_oracle(b), [0, 3], lib=lib)
+    assert rc1 == rc2 == oracle.OK and np.array_equal(a.data, b.data)
+
+
+def pin_tp_slice(lib):
+    """The heterogeneous-TP transfer plan.  Worked cases of the passage (8 kv heads): P TP 4 ->
+    D TP 2 merges two P shards into each D shard; P TP 2 -> D TP 4 splits each P shard over two
+    D ranks.  Exhaustively for small sizes: every D rank receives each of its heads exactly
+    once, from a P rank that holds it, at the matching offsets."""
+    # P TP 4 (2 heads each) -> D TP 2 (4 heads each): D rank 0 <- P ranks 0, 1
+    assert oracle.tp_slice(8, 4, 0, 2, 0, lib=lib) == (oracle.OK, 0, 0, 2)
+    assert oracle.tp_slice(8, 4, 1, 2, 0, lib=lib) == (oracle.OK, 0, 2, 2)
+    assert oracle.tp_slice(8, 4, 2, 2, 0, lib=lib)[3] == 0
+    assert oracle.tp_slice(8, 4, 3, 2, 1, lib=lib) == (oracle.OK, 0, 2, 2)
+    # P TP 2 (4 heads each) -> D TP 4 (2 heads each): P rank 1 -> D ranks 2, 3
+    assert oracle.tp_slice(8, 2, 1, 4, 2, lib=lib) == (oracle.OK, 0, 0, 2)
+    assert oracle.tp_slice(8, 2, 1, 4, 3, lib=lib) == (oracle.OK, 2, 0, 2)
+    assert oracle.tp_slice(8, 2, 1, 4, 0, lib=lib)[3] == 0
+    # replicated producer (2 kv heads, P TP 4): ranks 0 and 2 send, 1 and 3 are replicas
+    assert oracle.tp_slice(2, 4, 0, 1, 0, lib=lib) == (oracle.OK, 0, 0, 1)
+    assert oracle.tp_slice(2, 4, 1, 1, 0, lib=lib)[3] == 0
+    assert oracle.tp_slice(2, 4, 2, 1, 0, lib=lib) == (oracle.OK, 0, 1, 1)
+
+    def held(heads, t, r):
+        if t <= heads:
+            return list(range(r * heads // t, (r + 1) * heads // t))
+        return [r // (t // heads)]
+
+    sizes = (1, 2, 4, 8, 16)
+    for heads in (1, 2, 4, 8):
+        for p_tp in sizes:
+            for d_tp in sizes:
+                ok = lambda t: (heads % t == 0) if t <= heads else (t % heads == 0)
+                if not (ok(p_tp) and ok(d_tp)):
+                    assert oracle.tp_slice(heads, p_tp, 0, d_tp, 0, lib=lib)[0] == oracle.ERR_INVALID_ARG
+                    continue
+                for dr in range(d_tp):
+                    got = []
+                    for pr in range(p_tp):
+                        rc, sh0, dh0, nh = oracle.tp_slice(heads, p_tp, pr, d_tp, dr, lib=lib)
+                        assert rc == oracle.OK
+                        for j in range(nh):
+                            g_src = held(heads, p_tp, pr)[sh0 + j]
+                            g_dst = held(heads, d_tp, dr)[dh0 + j]
+                            assert g_src == g_dst
+                            got.append(g_dst)
+                    assert sorted(got) == held(heads, d_tp, dr), (heads, p_tp, d_tp, dr)
+    for bad in ((0, 1, 0, 1, 0), (8, 3, 0, 1, 0), (8, 2, 2, 1, 0), (8, 1, 0, 2, -1), (2, 3, 0, 1, 0)):
+        assert oracle.tp_slice(*bad, lib=lib)[0] == oracle.ERR_INVALID_ARG
+
+
 def pin_bruteforce_hnd(lib):
     """Every page table of k <= 3 pages out of a 4-page pool (page size 3), every sequence
     length that ends in page k, for the page-table gather and the inverse rebuild."""
@@ -383,7 +478,8 @@ def pin_plan(lib):
 
 
 ALL_PINS = [pin_sizes, pin_bytes_written, pin_bruteforce_gather, pin_bruteforce_scatter,
-            pin_bruteforce_transfer, pin_bruteforce_transfer_layers, pin_bruteforce_hnd,
+            pin_bruteforce_transfer, pin_bruteforce_transfer_layers, pin_bruteforce_move_heads,
+            pin_move_heads_full_range_is_transfer, pin_tp_slice, pin_bruteforce_hnd,
             pin_roundtrip,
             pin_transfer_is_scatter_of_gather, pin_hnd_roundtrip, pin_plane_locality,
             pin_numpy_special_cases, pin_validation, pin_batch, pin_plan]

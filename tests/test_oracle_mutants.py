@@ -43,6 +43,12 @@ MUTANTS = {
                          "for (int32_t layer = 0; layer + 1 < stop; ++layer)"),
     "layers_v_plane_dropped": ("    for (int32_t kv = 0; kv < 2; ++kv)\n      for (int64_t i = 0; i < n; ++i)\n        for (int32_t h = 0; h < src->kv_heads; ++h)\n          memcpy(head_vec(dst, 2 * layer + kv",
                                "    for (int32_t kv = 0; kv < 1; ++kv)\n      for (int64_t i = 0; i < n; ++i)\n        for (int32_t h = 0; h < src->kv_heads; ++h)\n          memcpy(head_vec(dst, 2 * layer + kv"),
+    "tp_replicas_all_send": ("  if (p_tp > heads && p_rank % (p_tp / heads) != 0) return KVXO_OK; /* another replica sends */\n", ""),
+    "tp_dst_offset_from_p_side": ("  *dst_head0 = lo - df;", "  *dst_head0 = lo - pf;"),
+    "heads_dst_offset_ignored": ("        else\n          memcpy(head_vec(dst, p, dst_slots[i], dst_head0 + j),",
+                                 "        else\n          memcpy(head_vec(dst, p, dst_slots[i], j),"),
+    "heads_buffer_row_of_whole_pool": ("uint8_t *b = buf + (((int64_t)p * n + i) * n_heads + j) * hb;",
+                                       "uint8_t *b = buf + (((int64_t)p * n + i) * shape->kv_heads + j) * hb;"),
     "transfer_src_dst_swapped": ("memcpy(head_vec(dst, p, dst_slots[i], h), head_vec(src, p, src_slots[i], h),",
                                  "memcpy(head_vec(src, p, src_slots[i], h), head_vec(dst, p, dst_slots[i], h),"),
 }
