@@ -168,7 +168,21 @@ struct Call {
   int64_t n_tokens = 0;
   int32_t n_segs = 0;
   int32_t n_status = 1;
+  // Geometry of the rows moved: the shape layout's whole rows, or (kvx_move_heads) a range of
+  // heads of each side, reached by offsetting every plane base of that side.
+  int32_t planes = 0;
+  int32_t heads = 0;
+  int64_t row_bytes = 0, seg_bytes = 0;
+  int64_t src_head_off = 0, dst_head_off = 0;
 };
+
+void set_whole_rows(Call &c) {
+  c.planes = c.shape->planes;
+  c.heads = c.shape->kv_heads;
+  c.row_bytes = c.shape->row_bytes;
+  c.seg_bytes = c.shape->seg_bytes;
+  c.src_head_off = c.dst_head_off = 0;
+}
 
 // Checks the layouts an op needs and fills call.src / call.dst / call.shape.
 kvx_status bind_layouts(Call &c, kvx_layout_t src, kvx_layout_t dst) {
@@ -177,11 +191,13 @@ kvx_status bind_layouts(Call &c, kvx_layout_t src, kvx_layout_t dst) {
       if (!src) return KVX_ERR_INVALID_ARG;
       c.src = src;
       c.shape = src;
+      set_whole_rows(c);
       return KVX_OK;
     case KVX_OP_SCATTER:
       if (!dst) return KVX_ERR_INVALID_ARG;
       c.dst = dst;
       c.shape = dst;
+      set_whole_rows(c);
       return KVX_OK;
     case KVX_OP_TRANSFER:
     case KVX_OP_BATCH:
@@ -192,6 +208,7 @@ kvx_status bind_layouts(Call &c, kvx_layout_t src, kvx_layout_t dst) {
       c.src = src;
       c.dst = dst;
       c.shape = src ? src : dst;
+      set_whole_rows(c);
       return KVX_OK;
     default:
       return KVX_ERR_INVALID_ARG;
@@ -205,7 +222,7 @@ kvx::Side src_side(const Call &c) {
     s.num_slots = 0;
     return s;
   }
-  return c.src ? pool_side(c.src) : buffer_side(c.shape->seg_bytes);
+  return c.src ? pool_side(c.src) : buffer_side(c.seg_bytes);
 }
 
 kvx::Side dst_side(const Call &c) {
@@ -215,7 +232,7 @@ kvx::Side dst_side(const Call &c) {
     s.num_slots = 0;
     return s;
   }
-  return c.dst ? pool_side(c.dst) : buffer_side(c.shape->seg_bytes);
+  return c.dst ? pool_side(c.dst) : buffer_side(c.seg_bytes);
 }
 
 kvx_status check_ws(const void *d_ws, size_t ws_bytes, const kvx::WsLayout &L) {
@@ -228,7 +245,7 @@ kvx_status check_buffer(const Call &c, const void *d_buf, size_t buf_bytes) {
   if (c.mode == kvx::kModeBatch) {
     if (buf_bytes > 0 && (!d_buf || !aligned(d_buf, 16))) return KVX_ERR_ALIGNMENT;
   } else if (c.op == KVX_OP_GATHER || c.op == KVX_OP_SCATTER) {
-    const int64_t need = (int64_t)c.shape->planes * c.n_tokens * c.shape->row_bytes;
+    const int64_t need = (int64_t)c.planes * c.n_tokens * c.row_bytes;
     if (!d_buf) return KVX_ERR_INVALID_ARG;
     if (!aligned(d_buf, 16)) return KVX_ERR_ALIGNMENT;
     if ((int64_t)buf_bytes < need) return KVX_ERR_INVALID_ARG;
@@ -250,9 +267,9 @@ kvx::PlanArgs plan_args(const Call &c, void *d_ws, int32_t *d_status) {
   a.op = c.op;
   a.n_tokens = c.n_tokens;
   a.n_segs = c.n_segs;
-  a.chunk_rows = chunk_rows_for(c.shape->row_bytes);
-  a.planes = c.shape->planes;
-  a.row_bytes = (int32_t)c.shape->row_bytes;
+  a.chunk_rows = chunk_rows_for(c.row_bytes);
+  a.planes = c.planes;
+  a.row_bytes = (int32_t)c.row_bytes;
   a.src = src_side(c);
   a.dst = dst_side(c);
   a.has_src = c.src != nullptr;
@@ -291,11 +308,11 @@ void fill_copy_args(kvx::CopyArgs &a, const Call &c, const kvx_request *d_reqs, 
   a.op = c.op;
   a.n_tokens = c.n_tokens;
   a.n_segs = c.n_segs;
-  a.chunk_rows = chunk_rows_for(c.shape->row_bytes);
-  a.planes = c.shape->planes;
-  a.row_bytes = (int32_t)c.shape->row_bytes;
-  a.seg_bytes = (int32_t)c.shape->seg_bytes;
-  a.heads = c.shape->kv_heads;
+  a.chunk_rows = chunk_rows_for(c.row_bytes);
+  a.planes = c.planes;
+  a.row_bytes = (int32_t)c.row_bytes;
+  a.seg_bytes = (int32_t)c.seg_bytes;
+  a.heads = c.heads;
   a.src = src_side(c);
   a.dst = dst_side(c);
   a.buf = static_cast<char *>(d_buf);
@@ -303,9 +320,10 @@ void fill_copy_args(kvx::CopyArgs &a, const Call &c, const kvx_request *d_reqs, 
   a.ws = static_cast<const char *>(d_ws);
   a.L = kvx::ws_layout(c.n_tokens, c.n_segs, false);
   a.status = d_status;
-  for (int p = 0; p < c.shape->planes; ++p) {
-    a.src_planes[p] = c.src ? reinterpret_cast<const char *>(c.src->plane[p]) : nullptr;
-    a.dst_planes[p] = c.dst ? reinterpret_cast<char *>(c.dst->plane[p]) : nullptr;
+  for (int p = 0; p < c.planes; ++p) {
+    a.src_planes[p] = c.src ? reinterpret_cast<const char *>(c.src->plane[p]) + c.src_head_off
+                            : nullptr;
+    a.dst_planes[p] = c.dst ? reinterpret_cast<char *>(c.dst->plane[p]) + c.dst_head_off : nullptr;
   }
 }
 
@@ -327,12 +345,12 @@ kvx_status enqueue_copy(const Call &c, const kvx_request *d_reqs, void *d_buf, c
     if (host_status_written) *host_status_written = host_status != nullptr;
     a.row_group_shift = kvx::row_group_shift(a);
     const cudaError_t e = kvx::launch_copy(
-        a, (int)kvx::row_grid(c.n_tokens, c.shape->planes, a.row_group_shift), s);
+        a, (int)kvx::row_grid(c.n_tokens, c.planes, a.row_group_shift), s);
     return e == cudaSuccess ? KVX_OK : cuda_fail(e);
   }
   a.spec_src = a.spec_dst = nullptr;  // the other kernels read the plan
   // one warp (register paths) or one thread (bulk path) per work item; at most n*P items
-  const int64_t items = (int64_t)c.shape->planes * c.n_tokens;
+  const int64_t items = (int64_t)c.planes * c.n_tokens;
   const kvx::CopyVariant v = kvx::copy_variant(a);
   const int64_t per_cta = v == kvx::kVariantBulk ? kvx::variant_threads(v) : kvx::kCopyThreads / 32;
   const bool small = kvx::num_tiles(c.n_tokens) <= kvx::kBulkSmallTiles;
@@ -354,7 +372,7 @@ kvx_status enqueue_fused(const Call &c, const int32_t *d_src, const int32_t *d_d
   fill_copy_args(a, c, nullptr, d_buf, nullptr, d_status);
   const int bps = kvx::copy_is_linear(a) ? di.bps_fused_linear : di.bps_fused_general;
   cudaError_t e = kvx::launch_fused(a, d_src, d_dst, (int32_t)c.n_tokens,
-                                    chunk_rows_for(c.shape->row_bytes), di.sms, bps, s);
+                                    chunk_rows_for(c.row_bytes), di.sms, bps, s);
   return e == cudaSuccess ? KVX_OK : cuda_fail(e);
 }
 
@@ -566,6 +584,41 @@ kvx_status kvx_execute(int32_t op, kvx_layout_t src, kvx_layout_t dst, const kvx
 
 // gather / scatter / transfer of one slot-list request: one launch up to the fused limit,
 // otherwise the planner + copy launches.
+// The one-shot path of a bound call: planner + copy (the copy reading the slot lists itself),
+// or the one-launch fused path.
+static kvx_status run_call(const Call &c, const int32_t *d_src_slots, const int32_t *d_dst_slots,
+                           void *d_buf, void *d_ws, size_t ws_bytes, int32_t *d_status,
+                           kvx_stream_t stream, int32_t *host_status = nullptr,
+                           bool *host_status_written = nullptr) {
+  if (host_status_written) *host_status_written = false;
+  const int64_t n = c.n_tokens;
+  if (!d_status || !aligned(d_status, 4)) return KVX_ERR_INVALID_ARG;
+  if (n > 0) {
+    if (c.src && (!d_src_slots || !aligned(d_src_slots, 4))) return KVX_ERR_INVALID_ARG;
+    if (c.dst && (!d_dst_slots || !aligned(d_dst_slots, 4))) return KVX_ERR_INVALID_ARG;
+  }
+  const kvx::WsLayout L = kvx::ws_layout(n, 0, false);
+  kvx_status st;
+  if (n > 0 && (st = check_ws(d_ws, ws_bytes, L)) != KVX_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // Requests of up to the fused limit with rows under KVX_CHUNK_BYTES take the one-launch
+  // path; the rest take the planner + row kernel (the row kernel overlaps the planner).
+  const bool fused = chunk_rows_for(c.row_bytes) > 1 &&
+                     n <= g_fused_max.load(std::memory_order_relaxed);
+  if (n == 0 || !fused) {
+    kvx::PlanArgs a = plan_args(c, d_ws, d_status);
+    a.src_idx = d_src_slots;
+    a.dst_idx = d_dst_slots;
+    st = enqueue_plan(c, a, s);
+    if (st != KVX_OK || n == 0) return st;
+    // the copy may read the slot lists itself (see CopyArgs::spec_src)
+    return enqueue_copy(c, nullptr, d_buf, d_ws, d_status, s, c.src ? d_src_slots : nullptr,
+                        c.dst ? d_dst_slots : nullptr, host_status, host_status_written);
+  }
+  return enqueue_fused(c, c.src ? d_src_slots : nullptr, c.dst ? d_dst_slots : nullptr, d_buf,
+                       d_status, s);
+}
+
 static kvx_status run_slots(int32_t op, kvx_layout_t src, const int32_t *d_src_slots,
                             kvx_layout_t dst, const int32_t *d_dst_slots, int32_t n, void *d_buf,
                             size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *d_status,
@@ -579,25 +632,8 @@ static kvx_status run_slots(int32_t op, kvx_layout_t src, const int32_t *d_src_s
   kvx_status st = bind_layouts(c, src, dst);
   if (st == KVX_OK) st = check_buffer(c, d_buf, buf_bytes);
   if (st != KVX_OK) return st;
-  // Requests of up to the fused limit with rows under KVX_CHUNK_BYTES take the one-launch
-  // path; the rest take the planner + row kernel (the row kernel overlaps the planner).
-  const bool fused = chunk_rows_for(c.shape->row_bytes) > 1 &&
-                     n <= g_fused_max.load(std::memory_order_relaxed);
-  if (n == 0 || !fused) {
-    st = kvx_plan(op, src, d_src_slots, dst, d_dst_slots, n, d_ws, ws_bytes, d_status, stream);
-    if (st != KVX_OK || n == 0) return st;
-    // the copy may read the slot lists itself (see CopyArgs::spec_src)
-    return enqueue_copy(c, nullptr, d_buf, d_ws, d_status, reinterpret_cast<cudaStream_t>(stream),
-                        c.src ? d_src_slots : nullptr, c.dst ? d_dst_slots : nullptr,
-                        host_status, host_status_written);
-  }
-  // the same host checks as kvx_plan
-  if (!d_status || !aligned(d_status, 4)) return KVX_ERR_INVALID_ARG;
-  if (c.src && (!d_src_slots || !aligned(d_src_slots, 4))) return KVX_ERR_INVALID_ARG;
-  if (c.dst && (!d_dst_slots || !aligned(d_dst_slots, 4))) return KVX_ERR_INVALID_ARG;
-  if ((st = check_ws(d_ws, ws_bytes, kvx::ws_layout(n, 0, false))) != KVX_OK) return st;
-  return enqueue_fused(c, c.src ? d_src_slots : nullptr, c.dst ? d_dst_slots : nullptr, d_buf,
-                       d_status, reinterpret_cast<cudaStream_t>(stream));
+  return run_call(c, d_src_slots, d_dst_slots, d_buf, d_ws, ws_bytes, d_status, stream,
+                  host_status, host_status_written);
 }
 
 kvx_status kvx_gather(kvx_layout_t src, const int32_t *d_src_slots, int32_t n, void *d_buf,
@@ -772,7 +808,7 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
   kvx_status st = bind_layouts(c, src, dst);
   if (st == KVX_OK) st = check_buffer(c, d_buf, buf_bytes);
   if (st != KVX_OK) return st;
-  const int32_t layers = c.shape->planes / 2;
+  const int32_t layers = c.planes / 2;
   kvx::StreamCtl k = {};
   k.layer_ready = static_cast<const int32_t *>(device_word(ctl->layer_ready));
   k.epoch_word = static_cast<const int32_t *>(device_word(ctl->epoch_word));
@@ -837,6 +873,84 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
   k.block = (uint32_t)std::min<int64_t>(std::max<int64_t>(per_warp / 4, 1), 8);
   e = kvx::launch_stream(a, k, (int)grid, s);
   return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+}
+
+// Heads [*first, *first + *count) held by rank r of a tensor-parallel group of size t.
+static kvx_status tp_heads(int32_t heads, int32_t t, int32_t r, int32_t *first, int32_t *count) {
+  if (heads < 1 || t < 1 || r < 0 || r >= t) return KVX_ERR_INVALID_ARG;
+  if (t <= heads) {
+    if (heads % t != 0) return KVX_ERR_INVALID_ARG;
+    *first = r * (heads / t);
+    *count = heads / t;
+  } else {
+    if (t % heads != 0) return KVX_ERR_INVALID_ARG;
+    *first = r / (t / heads);  // t / heads ranks hold the same head
+    *count = 1;
+  }
+  return KVX_OK;
+}
+
+kvx_status kvx_tp_slice(int32_t kv_heads, int32_t src_tp, int32_t src_rank, int32_t dst_tp,
+                        int32_t dst_rank, int32_t *src_head0, int32_t *dst_head0,
+                        int32_t *n_heads) {
+  if (!src_head0 || !dst_head0 || !n_heads) return KVX_ERR_INVALID_ARG;
+  int32_t sf, sc, df, dc;
+  kvx_status st = tp_heads(kv_heads, src_tp, src_rank, &sf, &sc);
+  if (st == KVX_OK) st = tp_heads(kv_heads, dst_tp, dst_rank, &df, &dc);
+  if (st != KVX_OK) return st;
+  *src_head0 = *dst_head0 = *n_heads = 0;
+  const int32_t lo = std::max(sf, df), hi = std::min(sf + sc, df + dc);
+  if (hi <= lo) return KVX_OK;
+  if (src_tp > kv_heads && src_rank % (src_tp / kv_heads) != 0) return KVX_OK;  // a replica
+  *src_head0 = lo - sf;
+  *dst_head0 = lo - df;
+  *n_heads = hi - lo;
+  return KVX_OK;
+}
+
+// Byte offset of head h within a plane's token row (token-row pool) or page (HND pool).
+static int64_t head_offset(const kvx_layout *l, int32_t h) {
+  return l->kind == KVX_HND_PAGED ? (int64_t)h * l->page_size * l->seg_bytes
+                                  : (int64_t)h * l->seg_bytes;
+}
+
+kvx_status kvx_move_heads(int32_t op, kvx_layout_t src, const int32_t *d_src_slots,
+                          int32_t src_head0, kvx_layout_t dst, const int32_t *d_dst_slots,
+                          int32_t dst_head0, int32_t n_heads, int32_t n, void *d_buf,
+                          size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *d_status,
+                          kvx_stream_t stream) {
+  if (op < KVX_OP_GATHER || op > KVX_OP_TRANSFER || !valid_n(n) || n_heads < 1)
+    return KVX_ERR_INVALID_ARG;
+  const bool uses_src = op != KVX_OP_SCATTER, uses_dst = op != KVX_OP_GATHER;
+  if ((uses_src && !src) || (uses_dst && !dst)) return KVX_ERR_INVALID_ARG;
+  Call c;
+  c.op = op;
+  c.n_tokens = n;
+  c.src = uses_src ? src : nullptr;
+  c.dst = uses_dst ? dst : nullptr;
+  c.shape = uses_src ? src : dst;
+  if (c.src && c.dst) {
+    if (src->num_layers != dst->num_layers || src->head_dim != dst->head_dim ||
+        src->elem != dst->elem)
+      return KVX_ERR_INVALID_ARG;
+    if (layouts_overlap(src, dst)) return KVX_ERR_OVERLAP;
+  }
+  if (c.src && (src_head0 < 0 || (int64_t)src_head0 + n_heads > src->kv_heads))
+    return KVX_ERR_INVALID_ARG;
+  if (c.dst && (dst_head0 < 0 || (int64_t)dst_head0 + n_heads > dst->kv_heads))
+    return KVX_ERR_INVALID_ARG;
+  c.planes = c.shape->planes;
+  c.heads = n_heads;
+  c.seg_bytes = c.shape->seg_bytes;
+  c.row_bytes = (int64_t)n_heads * c.seg_bytes;
+  c.src_head_off = c.src ? head_offset(src, src_head0) : 0;
+  c.dst_head_off = c.dst ? head_offset(dst, dst_head0) : 0;
+  // every 16-byte vector of the slice stays inside one head (HND) and starts 16-byte aligned
+  if (c.row_bytes % 16 != 0 || c.src_head_off % 16 != 0 || c.dst_head_off % 16 != 0)
+    return KVX_ERR_ALIGNMENT;
+  kvx_status st = check_buffer(c, d_buf, buf_bytes);
+  if (st != KVX_OK) return st;
+  return run_call(c, d_src_slots, d_dst_slots, d_buf, d_ws, ws_bytes, d_status, stream);
 }
 
 kvx_status kvx_plan_export(const void *d_ws, size_t ws_bytes, int64_t n_tokens,

@@ -122,6 +122,10 @@ _SIGS = {
     "kvx_submit": (_I32, [_I32, _VP, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _SZ, _VP, _VP]),
     "kvx_stream": (_I32, [_I32, _VP, _VP, _VP, _VP, _I32, _VP, _SZ, ctypes.POINTER(StreamCtl),
                           _VP, _SZ, _VP, _VP]),
+    "kvx_tp_slice": (_I32, [_I32, _I32, _I32, _I32, _I32, ctypes.POINTER(_I32),
+                            ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
+    "kvx_move_heads": (_I32, [_I32, _VP, _VP, _I32, _VP, _VP, _I32, _I32, _I32, _VP, _SZ, _VP,
+                              _SZ, _VP, _VP]),
     "kvx_plan": (_I32, [_I32, _VP, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _VP]),
     "kvx_plan_runs": (_I32, [_I32, _VP, _VP, _VP, _I32, _I32, _VP, _SZ, _VP, _VP]),
     "kvx_plan_batch": (_I32, [_VP, _VP, _VP, _I32, _I64, _VP, _I64, _VP, _I64, _SZ, _VP, _SZ,
@@ -439,3 +443,24 @@ def _any_ptr(x) -> Optional[int]:
     if hasattr(x, "ctypes"):
         return int(x.ctypes.data)
     return int(x.data_ptr())
+
+
+def tp_slice(kv_heads: int, src_tp: int, src_rank: int, dst_tp: int, dst_rank: int):
+    """kvx_tp_slice: (src_head0, dst_head0, n_heads) a source rank sends a destination rank."""
+    a, b, c = _I32(0), _I32(0), _I32(0)
+    _check(lib().kvx_tp_slice(kv_heads, src_tp, src_rank, dst_tp, dst_rank, ctypes.byref(a),
+                              ctypes.byref(b), ctypes.byref(c)), "kvx_tp_slice")
+    return a.value, b.value, c.value
+
+
+def move_heads(op: int, src: Optional[Layout], src_slots, src_head0: int, dst: Optional[Layout],
+               dst_slots, dst_head0: int, n_heads: int, n: int, buf, ws, status, buf_bytes=None,
+               ws_bytes=None, stream=None) -> None:
+    """kvx_move_heads: heads [src_head0, src_head0 + n_heads) of each source row to heads
+    [dst_head0, ...) of each destination row (layouts may have different kv_heads)."""
+    rc = lib().kvx_move_heads(op, _h(src), _ptr(src_slots), src_head0, _h(dst), _ptr(dst_slots),
+                              dst_head0, n_heads, n, _ptr(buf),
+                              _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
+                              _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
+                              _stream(stream))
+    _check(rc, "kvx_move_heads")

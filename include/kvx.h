@@ -295,6 +295,41 @@ KVX_API kvx_status kvx_plan_export(const void *d_ws, size_t ws_bytes, int64_t n_
                            int32_t *d_chunks, int64_t max_chunks, int64_t *d_count,
                            kvx_stream_t stream);
 
+/* ---- head ranges: heterogeneous tensor parallelism ------------------------------------- */
+
+/* Which kv heads a rank of one tensor-parallel group sends to a rank of another ([Mooncake] 7.7
+ * 异构TP: with different TP sizes on the two sides, one D rank may merge the shards of several
+ * P ranks, or one P rank's shard is split over several D ranks; the sender computes whether it
+ * sends, the source offset, the destination offset and the length).  A model has kv_heads kv
+ * heads; rank r of a group of size t holds heads [r*kv_heads/t, (r+1)*kv_heads/t) when
+ * t <= kv_heads (t must divide kv_heads), and the single head r/(t/kv_heads) when
+ * t > kv_heads (kv_heads must divide t; the head is replicated over t/kv_heads ranks).
+ * Outputs (host memory): the first head to send in the source rank's own shard, the first head
+ * it lands on in the destination rank's shard, and the count; *n_heads = 0 when the pair
+ * exchanges nothing.  Of source ranks holding the same replicated head, only the
+ * lowest-numbered sends it.  Host-only arithmetic; KVX_ERR_INVALID_ARG for sizes that do not
+ * divide, ranks out of range or null outputs. */
+KVX_API kvx_status kvx_tp_slice(int32_t kv_heads, int32_t src_tp, int32_t src_rank,
+                                int32_t dst_tp, int32_t dst_rank, int32_t *src_head0,
+                                int32_t *dst_head0, int32_t *n_heads);
+
+/* Gather / scatter / transfer of a range of kv heads between layouts whose kv_heads differ
+ * ([Mooncake] 7.7 异构TP).  For every plane and token i, heads src_head0 .. src_head0 +
+ * n_heads - 1 of source row i go to heads dst_head0 .. dst_head0 + n_heads - 1 of destination
+ * row i.  Both layouts (where the op uses them) have the same num_layers, head_dim and dtype;
+ * kv_heads may differ.  A gather's buffer holds the moved heads only: [plane][n][n_heads]
+ * [head_dim] (buf_bytes >= P * n * n_heads * head_dim * elem); a scatter reads that form.
+ * Arguments, workspace, status and errors otherwise as kvx_gather / kvx_scatter /
+ * kvx_transfer (src_head0 is ignored by a scatter, dst_head0 by a gather); a head range outside
+ * a layout's kv_heads is KVX_ERR_INVALID_ARG, and a range whose bytes do not start and end on
+ * 16-byte boundaries within a row is KVX_ERR_ALIGNMENT. */
+KVX_API kvx_status kvx_move_heads(int32_t op, kvx_layout_t src, const int32_t *d_src_slots,
+                                  int32_t src_head0, kvx_layout_t dst,
+                                  const int32_t *d_dst_slots, int32_t dst_head0,
+                                  int32_t n_heads, int32_t n, void *d_buf, size_t buf_bytes,
+                                  void *d_ws, size_t ws_bytes, int32_t *d_status,
+                                  kvx_stream_t stream);
+
 /* ---- layer-streamed, cancellable copy ------------------------------------------------- */
 
 /* Longest a kvx_stream wait for one layer may be bounded to (ctl->wait_ns): 10 s. */

@@ -10,6 +10,7 @@ import pytest
 
 from disaggregated_paged_kv_gb300 import build as kbuild
 from disaggregated_paged_kv_gb300 import kvx
+import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "kvx.h")
@@ -156,3 +157,47 @@ def test_stream_validation_before_cuda(lib):
     assert call(ctl(), op=kvx.OP_BATCH) == kvx.ERR_INVALID_ARG
     assert call(ctl(), n=-1) == kvx.ERR_INVALID_ARG
     assert call(ctl(), d=src) == kvx.ERR_OVERLAP
+
+
+def test_tp_slice_matches_oracle(lib):
+    """kvx_tp_slice (host arithmetic in libkvx) against the oracle's plan, exhaustively for
+    small sizes, including the refusals."""
+    sizes = (1, 2, 3, 4, 6, 8, 16)
+    for heads in (1, 2, 4, 6, 8):
+        for st in sizes:
+            for dt in sizes:
+                for sr in range(-1, st + 1):
+                    for dr in (0, dt - 1, dt):
+                        want = oracle.tp_slice(heads, st, sr, dt, dr)
+                        a, b, c = ctypes.c_int32(-7), ctypes.c_int32(-7), ctypes.c_int32(-7)
+                        rc = kvx.lib().kvx_tp_slice(heads, st, sr, dt, dr, ctypes.byref(a),
+                                                    ctypes.byref(b), ctypes.byref(c))
+                        assert rc == want[0], (heads, st, sr, dt, dr)
+                        if rc == kvx.OK:
+                            assert (a.value, b.value, c.value) == want[1:], (heads, st, sr, dt, dr)
+
+
+def test_move_heads_validation_before_cuda(lib):
+    src = kvx.Layout(2, 4, 64, kvx.F16, 1000, base=FAKE, plane_stride=1000 * 512)
+    dst = kvx.Layout(2, 2, 64, kvx.F16, 1000, base=FAKE * 2, plane_stride=1000 * 256)
+    odd = kvx.Layout(2, 2, 4, kvx.F16, 1000, base=FAKE * 3, plane_stride=1000 * 16)
+    other = kvx.Layout(3, 2, 64, kvx.F16, 1000, base=FAKE * 3, plane_stride=1000 * 256)
+    WS, ST, SL = FAKE * 4, FAKE * 5, FAKE * 6
+    big = 1 << 30
+    l = kvx.lib()
+
+    def mv(op, s, h0, d, g0, nh, n=10, buf=None, bb=0):
+        return l.kvx_move_heads(op, s and s.handle, SL, h0, d and d.handle, SL, g0, nh, n, buf, bb,
+                                WS, big, ST, None)
+
+    T, G, S = kvx.OP_TRANSFER, kvx.OP_GATHER, kvx.OP_SCATTER
+    assert mv(T, src, 3, dst, 0, 2) == kvx.ERR_INVALID_ARG      # source range past kv_heads
+    assert mv(T, src, 0, dst, 1, 2) == kvx.ERR_INVALID_ARG      # destination range past kv_heads
+    assert mv(T, src, 0, dst, 0, 0) == kvx.ERR_INVALID_ARG      # no heads
+    assert mv(T, src, -1, dst, 0, 1) == kvx.ERR_INVALID_ARG
+    assert mv(T, src, 0, other, 0, 2) == kvx.ERR_INVALID_ARG    # layer counts differ
+    assert mv(T, src, 0, src, 0, 2) == kvx.ERR_OVERLAP
+    assert mv(T, None, 0, dst, 0, 1) == kvx.ERR_INVALID_ARG
+    assert mv(S, None, 0, odd, 1, 1) == kvx.ERR_ALIGNMENT       # 8-byte heads: no 16-byte vectors
+    assert mv(G, src, 0, None, 0, 2, buf=None, bb=0) == kvx.ERR_INVALID_ARG   # gather needs a buffer
+    assert mv(G, src, 0, None, 0, 2, buf=FAKE * 7, bb=4 * 10 * 256 - 16) == kvx.ERR_INVALID_ARG
