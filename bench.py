@@ -70,7 +70,8 @@ def parse_args():
                     help="kvx_set_fused_max_tokens for this run (0: planner + copy launches only)")
     ap.add_argument("--workload", default="2",
                     help="2 (default): the headline transfer; 1, 3, 4, 5: the other workloads; "
-                         "stream: the headline transfer through kvx_stream (layer-streamed)")
+                         "stream: the headline transfer through kvx_stream (layer-streamed); "
+                         "tp: the headline request resharded between TP groups (kvx_move_heads)")
     ap.add_argument("--layer-us", type=float, default=100.0,
                     help="--workload stream: host cadence of the emulated producer, us/layer")
     return ap.parse_args()
@@ -487,6 +488,105 @@ class OracleTransfer:
         return (time.perf_counter() - t0) / max(n, 1), n
 
 
+def run_tp(args):
+    """The headline request (2048 random tokens, 36 layers x K/V x 8 kv heads x 128 bf16) moved
+    between tensor-parallel groups of different sizes: for every (P rank, D rank) pair the heads
+    kvx_tp_slice assigns it, one kvx_move_heads transfer each, all on one stream.  A step is
+    the whole reshard (every pair); L2 flushed before each step.  P pools are HND pages of 16
+    tokens, D pools per-plane token rows."""
+    import numpy as np
+    import torch
+
+    from disaggregated_paged_kv_gb300 import kvx
+    from tests import inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kvx.lib()
+    stream = torch.cuda.Stream(device=dev)
+    sp = int(stream.cuda_stream)
+    NS = min(args.pool_slots, 32768)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(inputs.seed(2, inputs.ROLE_VALUES))
+    s_dev = torch.from_numpy(inputs.distinct_slots(inputs.rng(2, inputs.ROLE_SRC_SLOTS), N_TOK, NS)).to(dev)
+    d_dev = torch.from_numpy(inputs.distinct_slots(inputs.rng(2, inputs.ROLE_DST_SLOTS), N_TOK, NS)).to(dev)
+    ws = torch.empty(kvx.workspace_size(N_TOK, 0), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    peaks, _ = measured_peaks()
+    results = {}
+    for p_tp, d_tp in ((1, 2), (2, 1), (4, 2), (2, 4), (8, 1)):
+        hp, hd = H // p_tp, H // d_tp
+        p_pools = [torch.randn((P, NS // 16, hp, 16, D), dtype=torch.bfloat16, device=dev,
+                               generator=gen) for _ in range(p_tp)]
+        d_pools = [torch.empty((P, NS, hd, D), dtype=torch.bfloat16, device=dev) for _ in range(d_tp)]
+        p_l = [kvx.Layout(L, hp, D, kvx.BF16, NS, kind=kvx.HND_PAGED, page_size=16, base=t,
+                          plane_stride=NS * hp * D * 2) for t in p_pools]
+        d_l = [kvx.Layout(L, hd, D, kvx.BF16, NS, base=t, plane_stride=NS * hd * D * 2)
+               for t in d_pools]
+        plan = []
+        for dr in range(d_tp):
+            for pr in range(p_tp):
+                sh0, dh0, nh = kvx.tp_slice(H, p_tp, pr, d_tp, dr)
+                if nh:
+                    plan.append((pr, dr, sh0, dh0, nh))
+
+        def step():
+            for pr, dr, sh0, dh0, nh in plan:
+                kvx.move_heads(kvx.OP_TRANSFER, p_l[pr], s_dev, sh0, d_l[dr], d_dev, dh0, nh,
+                               N_TOK, None, ws, st, buf_bytes=0, stream=sp)
+
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                flush.fill_(1)
+                step()
+        torch.cuda.synchronize()
+        assert int(st.item()) == kvx.OK
+        # spot check: token k, plane 0, first moved head of the first pair
+        pr, dr, sh0, dh0, nh = plan[0]
+        k = 97
+        sslot, dslot = int(s_dev[k]), int(d_dev[k])
+        got = d_pools[dr][0, dslot, dh0:dh0 + nh]
+        want = p_pools[pr][0, sslot // 16, sh0:sh0 + nh, sslot % 16]
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+        K = args.steps
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                flush.fill_(i & 0xFF)
+                ev[i][0].record(stream)
+                step()
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        alg = alg_bytes(N_TOK) + 8 * N_TOK * (len(plan) - 1)  # every pair reads both lists
+        gbs = alg / (ms * 1e-3) / 1e9
+        results[f"p{p_tp}_to_d{d_tp}"] = {
+            "pairs": len(plan), "launches_per_reshard": 2 * len(plan),
+            "us_per_reshard": ms * 1e3, "GBs": gbs,
+            "frac_of_measured_hbm": gbs / float(peaks["hbm_gbs"]),
+            "slice_bytes": plan[0][4] * D * 2}
+        del p_pools, d_pools, p_l, d_l
+        torch.cuda.empty_cache()
+    head = results["p1_to_d2"]
+    line = {
+        "metric": "KV reshard between TP groups (kvx_move_heads) at 288 MiB: GB/s (read+write)",
+        "value": head["GBs"], "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["us_per_reshard"] * 1e-3,
+        "higher_is_better": True, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": "2048-token prompt, 36 layers x K/V x 8 kv heads x 128 bf16 "
+                               "(288 MiB) moved from the HND pools (page 16) of a P TP group to "
+                               "the token-row pools of a D TP group; value = P TP 1 -> D TP 2",
+                   "pool_slots": NS,
+                   "l2": "flushed before every timed step (write of 2x L2, outside the events)"},
+        "reshards": results,
+        "gpu_launches": head["launches_per_reshard"] * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_stream(args):
     """The headline transfer through kvx_stream.  (1) Every layer ready: device time of
     memset + planner + streamed copy per step, L2 flushed before each step.  (2) Layers raised
@@ -687,6 +787,9 @@ def main():
         kvx.set_fused_max_tokens(args.fused_max)
     if args.workload == "stream":
         run_stream(args)
+        return
+    if args.workload == "tp":
+        run_tp(args)
         return
     if int(args.workload) != 2:
         run_workload(args, int(args.workload))
