@@ -54,6 +54,7 @@ class _Pool(ctypes.Structure):
         ("num_slots", ctypes.c_int64),
         ("planes", ctypes.POINTER(ctypes.c_void_p)),
         ("slot_stride", ctypes.c_int64),
+        ("kv_planes", ctypes.c_int32),
     ]
 
 
@@ -87,6 +88,8 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
     i32p, u8p = P(ctypes.c_int32), ctypes.c_void_p
     lib.kvxo_bytes_per_token.restype = ctypes.c_int64
     lib.kvxo_bytes_per_token.argtypes = [ctypes.c_int32] * 4
+    lib.kvxo_mla_bytes_per_token.restype = ctypes.c_int64
+    lib.kvxo_mla_bytes_per_token.argtypes = [ctypes.c_int32] * 4
     lib.kvxo_row_bytes.restype = ctypes.c_int64
     lib.kvxo_row_bytes.argtypes = [P(_Pool)]
     lib.kvxo_check_slots.argtypes = [P(_Pool), i32p, ctypes.c_int64]
@@ -126,9 +129,10 @@ def _i32p(a: np.ndarray):
 class Pool:
     """A KV pool in host memory.
 
-    ``planes`` holds, for every plane p = 2*layer + kv, a pair (array, byte_offset): the plane
-    starts ``byte_offset`` bytes into the uint8 view of ``array``.  ``kind`` is TOKEN_ROWS
-    (slot s at ``slot_stride * s``) or HND_PAGES ([page][head][page_size][dim]).
+    ``planes`` holds, for every plane p = kv_planes*layer + kv, a pair (array, byte_offset):
+    the plane starts ``byte_offset`` bytes into the uint8 view of ``array``.  ``kind`` is
+    TOKEN_ROWS (slot s at ``slot_stride * s``) or HND_PAGES ([page][head][page_size][dim]).
+    ``kv_planes`` is 2 (K and V) or 1 (one latent plane per layer, MLA).
     """
 
     num_layers: int
@@ -140,11 +144,12 @@ class Pool:
     planes: List[tuple]
     slot_stride: int = 0
     page_size: int = 1
+    kv_planes: int = 2
     _keep: list = field(default_factory=list, repr=False)
 
     @property
     def num_planes(self) -> int:
-        return 2 * self.num_layers
+        return self.kv_planes * self.num_layers
 
     @property
     def row_bytes(self) -> int:
@@ -157,9 +162,15 @@ class Pool:
             ptrs[p] = arr.ctypes.data + int(off)
         s = _Pool(self.num_layers, self.kv_heads, self.head_dim, self.elem_bytes, self.kind,
                   self.page_size, self.num_slots, ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p)),
-                  self.slot_stride)
+                  self.slot_stride, self.kv_planes)
         self._keep = [ptrs]
         return s
+
+
+def mla_bytes_per_token(num_layers: int, latent_dim: int, rope_dim: int, elem_bytes: int,
+                        lib=None) -> int:
+    return int((lib or load()).kvxo_mla_bytes_per_token(num_layers, latent_dim, rope_dim,
+                                                         elem_bytes))
 
 
 def bytes_per_token(num_layers: int, kv_heads: int, head_dim: int, elem_bytes: int,

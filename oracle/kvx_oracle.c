@@ -22,7 +22,19 @@ static int64_t head_bytes(const kvxo_pool *pool) {
 
 int64_t kvxo_row_bytes(const kvxo_pool *pool) { return pool->kv_heads * head_bytes(pool); }
 
-static int32_t num_planes(const kvxo_pool *pool) { return 2 * pool->num_layers; }
+int64_t kvxo_mla_bytes_per_token(int32_t num_layers, int32_t latent_dim, int32_t rope_dim,
+                                 int32_t elem_bytes) {
+  /* [mini-infer] KV 传输大小: MLA stores a single compressed vector (latent + rope) per layer
+   * and token instead of a K and a V row. */
+  return (int64_t)num_layers * (latent_dim + rope_dim) * elem_bytes;
+}
+
+/* Planes per layer: K and V, or (MLA) one latent plane. */
+static int32_t planes_per_layer(const kvxo_pool *pool) { return pool->kv_planes == 1 ? 1 : 2; }
+
+static int32_t num_planes(const kvxo_pool *pool) {
+  return planes_per_layer(pool) * pool->num_layers;
+}
 
 /* Address of head vector (plane, slot, head). */
 static uint8_t *head_vec(const kvxo_pool *pool, int32_t plane, int64_t slot, int32_t head) {
@@ -97,7 +109,8 @@ int kvxo_scatter(const kvxo_pool *dst, const int32_t *slots, int64_t n, const ui
 
 static int same_row_shape(const kvxo_pool *a, const kvxo_pool *b) {
   return a->num_layers == b->num_layers && a->kv_heads == b->kv_heads &&
-         a->head_dim == b->head_dim && a->elem_bytes == b->elem_bytes;
+         a->head_dim == b->head_dim && a->elem_bytes == b->elem_bytes &&
+         planes_per_layer(a) == planes_per_layer(b);
 }
 
 int kvxo_transfer(const kvxo_pool *src, const int32_t *src_slots, const kvxo_pool *dst,
@@ -137,8 +150,9 @@ int kvxo_transfer_layers(const kvxo_pool *src, const int32_t *src_slots, const k
                          int64_t *bytes_written) {
   /* [DistServe] 一次请求如何穿过 DistServe: prefill writes the prompt's KV layer by layer and
    * decode pulls layer j once it exists.  A layer-streamed move that stopped before layer
-   * `stop` has moved exactly the rows of layers 0 .. stop-1 (planes 2l and 2l+1), as
-   * kvxo_transfer moves them; the planes of later layers are untouched. */
+   * `stop` has moved exactly the rows of layers 0 .. stop-1 (planes 2l and 2l+1; plane l for
+   * one latent plane per layer), as kvxo_transfer moves them; later planes are untouched. */
+  const int32_t ppl = planes_per_layer(src);
   int64_t hb = head_bytes(src);
   int rc;
   if (!same_row_shape(src, dst) || stop < 0 || stop > src->num_layers)
@@ -147,12 +161,12 @@ int kvxo_transfer_layers(const kvxo_pool *src, const int32_t *src_slots, const k
   if (rc == KVXO_OK) rc = kvxo_check_slots(dst, dst_slots, n);
   if (rc != KVXO_OK) return rc;
   for (int32_t layer = 0; layer < stop; ++layer)
-    for (int32_t kv = 0; kv < 2; ++kv)
+    for (int32_t kv = 0; kv < ppl; ++kv)
       for (int64_t i = 0; i < n; ++i)
         for (int32_t h = 0; h < src->kv_heads; ++h)
-          memcpy(head_vec(dst, 2 * layer + kv, dst_slots[i], h),
-                 head_vec(src, 2 * layer + kv, src_slots[i], h), (size_t)hb);
-  if (bytes_written) *bytes_written = n * 2 * (int64_t)stop * kvxo_row_bytes(src);
+          memcpy(head_vec(dst, ppl * layer + kv, dst_slots[i], h),
+                 head_vec(src, ppl * layer + kv, src_slots[i], h), (size_t)hb);
+  if (bytes_written) *bytes_written = n * ppl * (int64_t)stop * kvxo_row_bytes(src);
   return KVXO_OK;
 }
 
@@ -169,7 +183,8 @@ int kvxo_move_heads(int32_t op, const kvxo_pool *src, const int32_t *src_slots,
   int rc;
   if (op < 0 || op > 2 || n_heads < 1 || !shape) return KVXO_ERR_INVALID_ARG;
   if (op == 2 && (src->num_layers != dst->num_layers || src->head_dim != dst->head_dim ||
-                  src->elem_bytes != dst->elem_bytes))
+                  src->elem_bytes != dst->elem_bytes ||
+                  planes_per_layer(src) != planes_per_layer(dst)))
     return KVXO_ERR_INVALID_ARG;
   if (op != 1 && (src_head0 < 0 || src_head0 + n_heads > src->kv_heads))
     return KVXO_ERR_INVALID_ARG;

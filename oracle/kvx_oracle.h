@@ -67,6 +67,8 @@ typedef struct kvxo_pool {
   int64_t num_slots; /* token slots per plane (HND: pages * page_size) */
   uint8_t **planes;  /* 2*num_layers plane base addresses, plane 2*layer + kv */
   int64_t slot_stride; /* token rows only: bytes from slot s to slot s+1 */
+  int32_t kv_planes;   /* planes per layer: 2 (K then V; 0 also means 2) or 1 (one latent
+                        * vector per layer, MLA: [mini-infer] "KV 传输大小") */
 } kvxo_pool;
 
 typedef struct kvxo_request {
@@ -87,6 +89,11 @@ typedef struct kvxo_chunk {
 /* B_KV per token = 2 * n_layer * n_kvhead * d_head * b   ([DistServe] KV Cache 跨实例传输). */
 int64_t kvxo_bytes_per_token(int32_t num_layers, int32_t kv_heads, int32_t head_dim,
                              int32_t elem_bytes);
+
+/* MLA bytes per token ([mini-infer] "KV 传输大小": MLA keeps one compressed vector per layer,
+ * latent + rope, so there is no factor 2): num_layers * (latent_dim + rope_dim) * elem_bytes. */
+int64_t kvxo_mla_bytes_per_token(int32_t num_layers, int32_t latent_dim, int32_t rope_dim,
+                                 int32_t elem_bytes);
 
 /* Bytes of one (plane, token) row: kv_heads * head_dim * elem_bytes. */
 int64_t kvxo_row_bytes(const kvxo_pool *pool);

@@ -4,10 +4,11 @@ Independent of the oracle: no byte arithmetic and no memcpy.  A pool is a numpy 
 axes name the multi-index of every element, and each element is moved on its own in Python
 loops.  Layout axes:
 
-  planes      [plane][slot][head][dim]            (plane = 2*layer + kv)
+  planes      [plane][slot][head][dim]            (plane = kvp*layer + kv)
   slot_major  [slot][layer][kv][head][dim]
   hnd         [plane][page][head][page_size][dim]
 
+kvp is the number of planes per layer: 2 (K, V) or 1 (one latent vector per layer, MLA).
 The transfer buffer is [layer][kv][token][head][dim].
 """
 from __future__ import annotations
@@ -28,39 +29,40 @@ class BFPool:
     num_slots: int
     data: np.ndarray  # uint16 elements
     page_size: int = 1
+    kvp: int = 2
 
     def copy(self) -> "BFPool":
         return BFPool(self.layout, self.L, self.H, self.D, self.num_slots, self.data.copy(),
-                      self.page_size)
+                      self.page_size, self.kvp)
 
     def get(self, layer, kv, slot, h, d):
         if self.layout == "planes":
-            return self.data[2 * layer + kv, slot, h, d]
+            return self.data[self.kvp * layer + kv, slot, h, d]
         if self.layout == "slot_major":
             return self.data[slot, layer, kv, h, d]
-        return self.data[2 * layer + kv, slot // self.page_size, h, slot % self.page_size, d]
+        return self.data[self.kvp * layer + kv, slot // self.page_size, h, slot % self.page_size, d]
 
     def set(self, layer, kv, slot, h, d, v):
         if self.layout == "planes":
-            self.data[2 * layer + kv, slot, h, d] = v
+            self.data[self.kvp * layer + kv, slot, h, d] = v
         elif self.layout == "slot_major":
             self.data[slot, layer, kv, h, d] = v
         else:
-            self.data[2 * layer + kv, slot // self.page_size, h, slot % self.page_size, d] = v
+            self.data[self.kvp * layer + kv, slot // self.page_size, h, slot % self.page_size, d] = v
 
 
-def make_pool(layout, L, H, D, num_slots, fill, page_size=1) -> BFPool:
+def make_pool(layout, L, H, D, num_slots, fill, page_size=1, kvp=2) -> BFPool:
     """fill: callable(n) -> uint16 values, used in C order of the layout's axes."""
     if layout == "planes":
-        shape = (2 * L, num_slots, H, D)
+        shape = (kvp * L, num_slots, H, D)
     elif layout == "slot_major":
-        shape = (num_slots, L, 2, H, D)
+        shape = (num_slots, L, kvp, H, D)
     else:
         assert num_slots % page_size == 0
-        shape = (2 * L, num_slots // page_size, H, page_size, D)
+        shape = (kvp * L, num_slots // page_size, H, page_size, D)
     n = int(np.prod(shape))
     return BFPool(layout, L, H, D, num_slots, np.asarray(fill(n), np.uint16).reshape(shape),
-                  page_size)
+                  page_size, kvp)
 
 
 def to_oracle(pool: BFPool) -> oracle.Pool:
@@ -69,13 +71,13 @@ def to_oracle(pool: BFPool) -> oracle.Pool:
     base = pool.data
     planes = []
     for layer in range(pool.L):
-        for kv in range(2):
+        for kv in range(pool.kvp):
             if pool.layout == "planes":
-                view = base[2 * layer + kv]
+                view = base[pool.kvp * layer + kv]
             elif pool.layout == "slot_major":
                 view = base[:, layer, kv]
             else:
-                view = base[2 * layer + kv]
+                view = base[pool.kvp * layer + kv]
             off = view.__array_interface__["data"][0] - base.__array_interface__["data"][0]
             planes.append((base, off))
     if pool.layout == "planes":
@@ -85,14 +87,14 @@ def to_oracle(pool: BFPool) -> oracle.Pool:
     else:
         kind, stride = oracle.HND_PAGES, 0
     return oracle.Pool(pool.L, pool.H, pool.D, 2, kind, pool.num_slots, planes, stride,
-                       pool.page_size)
+                       pool.page_size, pool.kvp)
 
 
 def gather(pool: BFPool, slots) -> np.ndarray:
     n = len(slots)
-    out = np.zeros((pool.L, 2, n, pool.H, pool.D), np.uint16)
+    out = np.zeros((pool.L, pool.kvp, n, pool.H, pool.D), np.uint16)
     for layer in range(pool.L):
-        for kv in range(2):
+        for kv in range(pool.kvp):
             for i in range(n):
                 for h in range(pool.H):
                     for d in range(pool.D):
@@ -103,7 +105,7 @@ def gather(pool: BFPool, slots) -> np.ndarray:
 def scatter(pool: BFPool, slots, buf: np.ndarray) -> BFPool:
     res = pool.copy()
     for layer in range(pool.L):
-        for kv in range(2):
+        for kv in range(pool.kvp):
             for i in range(len(slots)):
                 for h in range(pool.H):
                     for d in range(pool.D):
@@ -114,7 +116,7 @@ def scatter(pool: BFPool, slots, buf: np.ndarray) -> BFPool:
 def transfer(src: BFPool, src_slots, dst: BFPool, dst_slots) -> BFPool:
     res = dst.copy()
     for layer in range(src.L):
-        for kv in range(2):
+        for kv in range(src.kvp):
             for i in range(len(src_slots)):
                 for h in range(src.H):
                     for d in range(src.D):
@@ -127,7 +129,7 @@ def transfer_layers(src: BFPool, src_slots, dst: BFPool, dst_slots, stop: int) -
     """transfer() of the layers before `stop` only."""
     res = dst.copy()
     for layer in range(stop):
-        for kv in range(2):
+        for kv in range(src.kvp):
             for i in range(len(src_slots)):
                 for h in range(src.H):
                     for d in range(src.D):
@@ -142,11 +144,11 @@ def move_heads(op, src: BFPool, src_slots, h0, dst: BFPool, dst_slots, g0, nh, b
     shape = dst if op == 1 else src
     n = len(dst_slots) if op == 1 else len(src_slots)
     if op == 0:
-        out = np.zeros((shape.L, 2, n, nh, shape.D), np.uint16)
+        out = np.zeros((shape.L, shape.kvp, n, nh, shape.D), np.uint16)
     else:
         out = dst.copy()
     for layer in range(shape.L):
-        for kv in range(2):
+        for kv in range(shape.kvp):
             for i in range(n):
                 for j in range(nh):
                     for d in range(shape.D):
@@ -162,10 +164,10 @@ def move_heads(op, src: BFPool, src_slots, h0, dst: BFPool, dst_slots, g0, nh, b
 
 def hnd_gather(pool: BFPool, page_table, seq_len) -> np.ndarray:
     """[layer][kv][s][h][d] = element (h, s, d) of the page-table view."""
-    out = np.zeros((pool.L, 2, seq_len, pool.H, pool.D), np.uint16)
+    out = np.zeros((pool.L, pool.kvp, seq_len, pool.H, pool.D), np.uint16)
     ps = pool.page_size
     for layer in range(pool.L):
-        for kv in range(2):
+        for kv in range(pool.kvp):
             for s in range(seq_len):
                 slot = int(page_table[s // ps]) * ps + s % ps
                 for h in range(pool.H):

@@ -236,6 +236,51 @@ def pin_tp_slice(lib):
         assert oracle.tp_slice(*bad, lib=lib)[0] == oracle.ERR_INVALID_ARG
 
 
+def pin_mla(lib):
+    """One latent plane per layer (MLA).  Sizes from the pages' table ([mini-infer] KV 传输大小):
+    DeepSeek-V2-Lite (27 layers, latent 512 + rope 64, 2-byte elements) 3.80 MB at 128 tokens
+    and 30.38 MB at 1024, about 54 % of Qwen2.5-7B's 7.00 MB.  Brute force: gather, scatter,
+    transfer and the layer-range transfer of kv_planes = 1 pools for every pair of layouts."""
+    gold = json.load(open(os.path.join(os.path.dirname(GOLDEN), "mla_sizes.json")))
+    for e in gold["entries"]:
+        got = oracle.mla_bytes_per_token(e["layers"], e["latent_dim"], e["rope_dim"],
+                                         e["elem_bytes"], lib=lib) * e["tokens"]
+        assert got == e["bytes"], e["name"]
+        assert abs(got / 2**20 - e["stated"]) <= e["tol"], e["name"]
+    mla = oracle.mla_bytes_per_token(27, 512, 64, 2, lib=lib)
+    gqa7b = oracle.bytes_per_token(28, 4, 128, 2, lib=lib)
+    r = gold["ratio_to_qwen25_7b"]
+    assert abs(mla / gqa7b - r["stated"]) <= r["tol"]
+    layouts = (("planes", 1), ("slot_major", 1), ("hnd", 2))
+    R = H * D * 2
+    for (la, pa), (lb, pb) in itertools.product(layouts, layouts):
+        src = bf.make_pool(la, L, H, D, 4, _arange_fill(11), page_size=pa, kvp=1)
+        base = bf.make_pool(lb, L, H, D, 4, _sentinel_fill, page_size=pb, kvp=1)
+        s_, d_ = [2, 0, 3], [1, 3, 0]
+        dst = base.copy()
+        rc, w = oracle.transfer(bf.to_oracle(src), s_, bf.to_oracle(dst), d_, lib=lib)
+        assert rc == oracle.OK and w == 3 * L * R
+        assert np.array_equal(dst.data, bf.transfer(src, s_, base, d_).data), (la, lb)
+        for stop in range(L + 1):
+            dst = base.copy()
+            rc, w = oracle.transfer_layers(bf.to_oracle(src), s_, bf.to_oracle(dst), d_, stop,
+                                           lib=lib)
+            assert rc == oracle.OK and w == 3 * stop * R
+            assert np.array_equal(dst.data, bf.transfer_layers(src, s_, base, d_, stop).data)
+        rc, got, w = oracle.gather(bf.to_oracle(src), s_, lib=lib)
+        want = bf.gather(src, s_)
+        assert rc == oracle.OK and w == want.size * 2
+        assert np.array_equal(got.view(np.uint16), want.ravel())
+        dst = base.copy()
+        rc, _ = oracle.scatter(bf.to_oracle(dst), d_, want.view(np.uint8), lib=lib)
+        assert rc == oracle.OK and np.array_equal(dst.data, bf.scatter(base, d_, want).data)
+    # K/V pools and latent pools do not mix
+    a = bf.make_pool("planes", L, H, D, 4, _arange_fill(1))
+    b = bf.make_pool("planes", L, H, D, 4, _sentinel_fill, kvp=1)
+    rc, _ = oracle.transfer(bf.to_oracle(a), [0], bf.to_oracle(b), [1], lib=lib)
+    assert rc == oracle.ERR_INVALID_ARG
+
+
 def pin_bruteforce_hnd(lib):
     """Every page table of k <= 3 pages out of a 4-page pool (page size 3), every sequence
     length that ends in page k, for the page-table gather and the inverse rebuild."""
@@ -479,7 +524,7 @@ def pin_plan(lib):
 
 ALL_PINS = [pin_sizes, pin_bytes_written, pin_bruteforce_gather, pin_bruteforce_scatter,
             pin_bruteforce_transfer, pin_bruteforce_transfer_layers, pin_bruteforce_move_heads,
-            pin_move_heads_full_range_is_transfer, pin_tp_slice, pin_bruteforce_hnd,
+            pin_move_heads_full_range_is_transfer, pin_tp_slice, pin_mla, pin_bruteforce_hnd,
             pin_roundtrip,
             pin_transfer_is_scatter_of_gather, pin_hnd_roundtrip, pin_plane_locality,
             pin_numpy_special_cases, pin_validation, pin_batch, pin_plan]

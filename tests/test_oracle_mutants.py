@@ -49,6 +49,9 @@ MUTANTS = {
                                  "        else\n          memcpy(head_vec(dst, p, dst_slots[i], j),"),
     "heads_buffer_row_of_whole_pool": ("uint8_t *b = buf + (((int64_t)p * n + i) * n_heads + j) * hb;",
                                        "uint8_t *b = buf + (((int64_t)p * n + i) * shape->kv_heads + j) * hb;"),
+    "mla_latent_plane_ignored": ("return pool->kv_planes == 1 ? 1 : 2;", "return 2;"),
+    "mla_counted_as_k_and_v": ("return (int64_t)num_layers * (latent_dim + rope_dim) * elem_bytes;",
+                               "return (int64_t)2 * num_layers * (latent_dim + rope_dim) * elem_bytes;"),
     "transfer_src_dst_swapped": ("memcpy(head_vec(dst, p, dst_slots[i], h), head_vec(src, p, src_slots[i], h),",
                                  "memcpy(head_vec(src, p, src_slots[i], h), head_vec(dst, p, dst_slots[i], h),"),
 }
