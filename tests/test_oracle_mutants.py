@@ -41,8 +41,7 @@ MUTANTS = {
     "batch_status_not_per_request": ("status[1 + q] = rc;", "status[1 + q] = 0;"),
     "layers_one_short": ("for (int32_t layer = 0; layer < stop; ++layer)",
                          "for (int32_t layer = 0; layer + 1 < stop; ++layer)"),
-    "layers_v_plane_dropped": ("    for (int32_t kv = 0; kv < 2; ++kv)\n      for (int64_t i = 0; i < n; ++i)\n        for (int32_t h = 0; h < src->kv_heads; ++h)\n          memcpy(head_vec(dst, 2 * layer + kv",
-                               "    for (int32_t kv = 0; kv < 1; ++kv)\n      for (int64_t i = 0; i < n; ++i)\n        for (int32_t h = 0; h < src->kv_heads; ++h)\n          memcpy(head_vec(dst, 2 * layer + kv"),
+    "layers_v_plane_dropped": ("    for (int32_t kv = 0; kv < ppl; ++kv)", "    for (int32_t kv = 0; kv < 1; ++kv)"),
     "tp_replicas_all_send": ("  if (p_tp > heads && p_rank % (p_tp / heads) != 0) return KVXO_OK; /* another replica sends */\n", ""),
     "tp_dst_offset_from_p_side": ("  *dst_head0 = lo - df;", "  *dst_head0 = lo - pf;"),
     "heads_dst_offset_ignored": ("        else\n          memcpy(head_vec(dst, p, dst_slots[i], dst_head0 + j),",
