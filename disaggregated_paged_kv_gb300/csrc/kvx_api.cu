@@ -16,6 +16,7 @@
 
 struct kvx_layout {
   int32_t num_layers, kv_heads, head_dim, elem, kind, page_size;
+  int32_t kv_planes;  // planes per layer: 2 (K, V) or 1 (MLA latent)
   int32_t planes;
   int64_t num_slots;
   int64_t row_bytes, seg_bytes;
@@ -70,8 +71,8 @@ bool layouts_overlap(const kvx_layout *a, const kvx_layout *b) {
 }
 
 bool same_rows(const kvx_layout *a, const kvx_layout *b) {
-  return a->num_layers == b->num_layers && a->kv_heads == b->kv_heads &&
-         a->head_dim == b->head_dim && a->elem == b->elem;
+  return a->num_layers == b->num_layers && a->kv_planes == b->kv_planes &&
+         a->kv_heads == b->kv_heads && a->head_dim == b->head_dim && a->elem == b->elem;
 }
 
 int32_t log2_exact(int64_t v) {
@@ -388,7 +389,9 @@ kvx_status kvx_layout_create(const kvx_layout_desc *d, kvx_layout_t *out) {
   if (!d || !out) return KVX_ERR_INVALID_ARG;
   *out = nullptr;
   const int eb = elem_bytes_of(d->dtype);
-  if (d->num_layers < 1 || 2 * (int64_t)d->num_layers > KVX_MAX_PLANES || d->kv_heads < 1 ||
+  const int32_t kvp = d->kv_planes == 0 ? 2 : d->kv_planes;
+  if ((kvp != 1 && kvp != 2) || d->reserved != 0) return KVX_ERR_INVALID_ARG;
+  if (d->num_layers < 1 || kvp * (int64_t)d->num_layers > KVX_MAX_PLANES || d->kv_heads < 1 ||
       d->head_dim < 1 || eb == 0 || d->num_slots < 1 || d->num_slots > INT32_MAX)
     return KVX_ERR_INVALID_ARG;
   if (d->kind != KVX_NHD && d->kind != KVX_HND_PAGED) return KVX_ERR_INVALID_ARG;
@@ -404,7 +407,8 @@ kvx_status kvx_layout_create(const kvx_layout_desc *d, kvx_layout_t *out) {
   l->head_dim = d->head_dim;
   l->elem = eb;
   l->kind = d->kind;
-  l->planes = 2 * d->num_layers;
+  l->kv_planes = kvp;
+  l->planes = kvp * d->num_layers;
   l->num_slots = d->num_slots;
   l->row_bytes = R;
   l->seg_bytes = seg;
@@ -808,7 +812,7 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
   kvx_status st = bind_layouts(c, src, dst);
   if (st == KVX_OK) st = check_buffer(c, d_buf, buf_bytes);
   if (st != KVX_OK) return st;
-  const int32_t layers = c.planes / 2;
+  const int32_t layers = c.shape->num_layers;
   kvx::StreamCtl k = {};
   k.layer_ready = static_cast<const int32_t *>(device_word(ctl->layer_ready));
   k.epoch_word = static_cast<const int32_t *>(device_word(ctl->epoch_word));
@@ -821,6 +825,7 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
   k.ready_value = ctl->ready_value;
   k.epoch = ctl->epoch;
   k.layers = layers;
+  k.kv_planes = c.shape->kv_planes;
   if (n > 0) {
     if (c.src && (!d_src_slots || !aligned(d_src_slots, 4))) return KVX_ERR_INVALID_ARG;
     if (c.dst && (!d_dst_slots || !aligned(d_dst_slots, 4))) return KVX_ERR_INVALID_ARG;
@@ -930,8 +935,8 @@ kvx_status kvx_move_heads(int32_t op, kvx_layout_t src, const int32_t *d_src_slo
   c.dst = uses_dst ? dst : nullptr;
   c.shape = uses_src ? src : dst;
   if (c.src && c.dst) {
-    if (src->num_layers != dst->num_layers || src->head_dim != dst->head_dim ||
-        src->elem != dst->elem)
+    if (src->num_layers != dst->num_layers || src->kv_planes != dst->kv_planes ||
+        src->head_dim != dst->head_dim || src->elem != dst->elem)
       return KVX_ERR_INVALID_ARG;
     if (layouts_overlap(src, dst)) return KVX_ERR_OVERLAP;
   }
@@ -992,6 +997,6 @@ kvx_status kvx_set_fused_max_tokens(int32_t max_tokens) {
 
 int32_t kvx_get_fused_max_tokens(void) { return g_fused_max.load(std::memory_order_relaxed); }
 
-int32_t kvx_version(void) { return 100; }
+int32_t kvx_version(void) { return 200; }
 
 }  // extern "C"

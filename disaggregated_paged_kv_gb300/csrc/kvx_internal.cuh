@@ -177,10 +177,10 @@ struct StreamCtl {
   int32_t epoch;
   int32_t layers;
   uint32_t groups;     // row groups of 1 << row_group_shift tokens per plane
-  uint32_t per_layer;  // items per layer: 2 * groups
+  uint32_t per_layer;  // items per layer: kv_planes * groups
   uint32_t items;      // per_layer * layers (< 2^32 for every legal size)
   uint32_t block;      // consecutive items a warp takes per block (see kvx_stream.cu)
-  uint32_t pad2;
+  int32_t kv_planes;   // planes per layer: 2 (K, V) or 1 (MLA latent); plane = kv_planes*l + kv
 };
 
 // Launchers (enqueue only; return the launch's cudaError_t).

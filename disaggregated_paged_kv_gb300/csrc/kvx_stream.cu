@@ -8,7 +8,8 @@
 // write is still in flight.
 //
 // Items are (layer l, K/V, group of g tokens) in layer-major order: item i has
-// l = i / (2 * groups).  Two grids move them:
+// l = i / (kv_planes * groups); with one latent plane per layer (MLA) there is no K/V split.
+// Two grids move them:
 //
 // Row grid (the default): one warp per item, one CTA per kWarps consecutive items, as the
 // row kernel of kvx_copy.cu.  Thread 0 of a CTA waits for the CTA's layer (usually one) while
@@ -196,9 +197,9 @@ __global__ void __launch_bounds__(kCopyThreads, 6) stream_kernel(const __grid_co
       lcur = l;
     }
     const uint32_t r = i - (uint32_t)l * k.per_layer;
-    const int32_t kv = r >= k.groups ? 1 : 0;
+    const int32_t kv = r >= k.groups ? 1 : 0;  // K or V (always 0 with one latent plane)
     const int64_t t = ((int64_t)(r - kv * k.groups) << gsh) + (lane >> lsh);
-    const int32_t p = 2 * l + kv;
+    const int32_t p = k.kv_planes * l + kv;
     // The first item's loads go out before the planner's verdict, like the row kernel's; a
     // lane range-checks its own indices first so that it never reads outside a pool.
     bool ok = t < a.n_tokens;
@@ -339,7 +340,7 @@ __global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8)
   const uint32_t ic = i < k.items ? i : i0;
   const int32_t l = (int32_t)(ic / k.per_layer);
   const uint32_t r = ic - (uint32_t)l * k.per_layer;
-  const int32_t kv = r >= k.groups ? 1 : 0;
+  const int32_t kv = r >= k.groups ? 1 : 0;  // K or V (always 0 with one latent plane)
   const int64_t t = ((int64_t)(r - kv * k.groups) << gsh) + (lane >> lsh);
   const bool sp = a.src.is_pool != 0, dp = a.dst.is_pool != 0;
   // slot indices and their range checks go out before the wait
@@ -370,7 +371,7 @@ __global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8)
   }
   __syncthreads();  // thread 0's acquire of the layer orders every thread's row loads
   if (l >= s_stop) ok = false;
-  const int32_t p = 2 * l + kv;
+  const int32_t p = k.kv_planes * l + kv;
   const int32_t R = a.row_bytes, vpr = R >> 4;
   const int32_t li = lane & ((1 << lsh) - 1);
   const char *buf_plane = a.buf + (int64_t)p * a.n_tokens * R;
@@ -465,8 +466,8 @@ int stream_blocks_per_sm() {
 void stream_sizes(StreamCtl &k, int64_t n_tokens, int32_t group_shift) {
   const int64_t groups = (n_tokens + (1 << group_shift) - 1) >> group_shift;
   k.groups = (uint32_t)groups;
-  k.per_layer = (uint32_t)(2 * groups);
-  k.items = (uint32_t)(2 * groups * k.layers);
+  k.per_layer = (uint32_t)(k.kv_planes * groups);
+  k.items = (uint32_t)(k.kv_planes * groups * k.layers);
 }
 
 cudaError_t launch_stream(const CopyArgs &c, const StreamCtl &k, int grid, cudaStream_t s) {

@@ -66,6 +66,8 @@ class LayoutDesc(ctypes.Structure):
         ("base", ctypes.c_void_p),
         ("plane_stride", ctypes.c_int64),
         ("slot_stride", ctypes.c_int64),
+        ("kv_planes", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
 
@@ -237,8 +239,10 @@ class Layout:
 
     def __init__(self, num_layers: int, kv_heads: int, head_dim: int, dtype: int,
                  num_slots: int, kind: int = NHD, page_size: int = 1, plane_ptrs=None,
-                 base=None, plane_stride: int = 0, slot_stride: int = 0, keepalive=None):
+                 base=None, plane_stride: int = 0, slot_stride: int = 0, keepalive=None,
+                 kv_planes: int = 2):
         d = LayoutDesc()
+        d.kv_planes = kv_planes
         d.num_layers, d.kv_heads, d.head_dim, d.dtype = num_layers, kv_heads, head_dim, dtype
         d.kind, d.page_size, d.num_slots = kind, page_size, num_slots
         self._ptr_array = None
@@ -253,6 +257,7 @@ class Layout:
         self.handle = h.value
         self.num_layers, self.kv_heads, self.head_dim = num_layers, kv_heads, head_dim
         self.dtype, self.kind, self.page_size, self.num_slots = dtype, kind, page_size, num_slots
+        self.kv_planes = kv_planes
         self._keepalive = keepalive  # tensors whose memory the planes point into
 
     @property

@@ -26,7 +26,8 @@
  *               7.7 (HND layout for non-MLA KV).
  *
  * Conventions used by every call:
- *  - A layout has P = 2 * num_layers planes, plane p = 2*layer + kv with K = 0, V = 1.
+ *  - A layout has P = 2 * num_layers planes, plane p = 2*layer + kv with K = 0, V = 1 (or, with
+ *    kv_planes = 1 for MLA, P = num_layers latent planes, plane p = layer).
  *  - A row is one (plane, token): kv_heads * head_dim elements, R bytes.  R must be a multiple
  *    of 16.  Values are never interpreted: every operation is an exact byte copy, so NaN
  *    payloads and any bit pattern survive.
@@ -121,15 +122,15 @@ typedef enum kvx_op {
 #define KVX_CHUNK_BYTES 2048
 
 typedef struct kvx_layout_desc {
-  int32_t num_layers; /* L >= 1, 2L <= KVX_MAX_PLANES */
+  int32_t num_layers; /* L >= 1, kv_planes * L <= KVX_MAX_PLANES */
   int32_t kv_heads;   /* H >= 1 */
   int32_t head_dim;   /* D >= 1 (elements) */
   int32_t dtype;      /* kvx_dtype; only its byte width is used */
   int32_t kind;       /* kvx_kind */
   int32_t page_size;  /* KVX_HND_PAGED: tokens per page (>= 1).  KVX_NHD: ignored. */
   int64_t num_slots;  /* token slots per plane; HND: a multiple of page_size */
-  /* Plane addresses: either plane_ptrs (host array of 2L device pointers, read during
-   * kvx_layout_create and not kept) or, when plane_ptrs is NULL, plane p at
+  /* Plane addresses: either plane_ptrs (host array of P = kv_planes * L device pointers, read
+   * during kvx_layout_create and not kept) or, when plane_ptrs is NULL, plane p at
    * base + p * plane_stride.  Every plane address must be 16-byte aligned. */
   void *const *plane_ptrs;
   void *base;
@@ -137,6 +138,11 @@ typedef struct kvx_layout_desc {
   /* KVX_NHD: bytes from slot s to slot s+1 within a plane; 0 means R (dense rows).  Must be a
    * multiple of 16 and >= R.  KVX_HND_PAGED: must be 0. */
   int64_t slot_stride;
+  /* Planes per layer: 2 (K and V; 0 also means 2) or 1 -- one latent vector per layer and
+   * token (MLA: [mini-infer] "KV 传输大小", latent + rope in a single plane).  With 1, plane p
+   * is layer p and a transfer buffer is [layer][seq][head][dim]. */
+  int32_t kv_planes;
+  int32_t reserved; /* must be 0 */
 } kvx_layout_desc;
 
 typedef struct kvx_layout *kvx_layout_t;

@@ -19,14 +19,14 @@ from tests import inputs
 GUARD = 64 * 1024
 
 
-def _shape(kind: str, L: int, H: int, D: int, num_slots: int, ps: int):
+def _shape(kind: str, L: int, H: int, D: int, num_slots: int, ps: int, kvp: int = 2):
     if kind in ("planes", "planes_separate"):
-        return (2 * L, num_slots, H, D)
+        return (kvp * L, num_slots, H, D)
     if kind == "slot_major":
-        return (num_slots, L, 2, H, D)
+        return (num_slots, L, kvp, H, D)
     if kind == "hnd":
         assert num_slots % ps == 0
-        return (2 * L, num_slots // ps, H, ps, D)
+        return (kvp * L, num_slots // ps, H, ps, D)
     raise ValueError(kind)
 
 
@@ -40,8 +40,9 @@ class Mirror:
     num_slots: int
     page_size: int
     host: np.ndarray       # uint8, guard + body + guard
-    body: np.ndarray       # uint16 view of the body with the layout's axes
+    body: np.ndarray       # element view (uint16, or uint8 for fp8) with the layout's axes
     dev: object = None     # torch uint8 tensor mirroring host
+    kvp: int = 2           # planes per layer: 2 (K, V) or 1 (MLA latent)
 
     @property
     def elem(self) -> int:
@@ -53,7 +54,7 @@ class Mirror:
 
     @property
     def P(self) -> int:
-        return 2 * self.L
+        return self.kvp * self.L
 
     def to_device(self):
         import torch
@@ -69,22 +70,23 @@ class Mirror:
 
 def make_mirror(kind: str, L: int, H: int, D: int, dtype: str, num_slots: int = 0,
                 page_size: int = 1, fill: str = "normal", g: Optional[np.random.Generator] = None,
-                n_tokens: int = 0, salt: int = 0) -> Mirror:
+                n_tokens: int = 0, salt: int = 0, kvp: int = 2) -> Mirror:
     """fill: 'normal' (N(0,1) values from g) or 'sentinel' (quiet-NaN payloads)."""
     if kind == "buffer":
-        shape = (2 * L, n_tokens, H, D)
+        shape = (kvp * L, n_tokens, H, D)
     else:
-        shape = _shape(kind, L, H, D, num_slots, page_size)
+        shape = _shape(kind, L, H, D, num_slots, page_size, kvp)
+    e = inputs.ELEM_BYTES[dtype]
     n_el = int(np.prod(shape))
-    host = np.empty(2 * GUARD + 2 * n_el, dtype=np.uint8)
-    host[:GUARD] = inputs.sentinel_bits(GUARD // 2, dtype, salt + 1).view(np.uint8)
-    host[GUARD + 2 * n_el:] = inputs.sentinel_bits(GUARD // 2, dtype, salt + 2).view(np.uint8)
-    body = host[GUARD:GUARD + 2 * n_el].view(np.uint16).reshape(shape)
+    host = np.empty(2 * GUARD + e * n_el, dtype=np.uint8)
+    host[:GUARD] = inputs.sentinel_bits(GUARD // e, dtype, salt + 1).view(np.uint8)
+    host[GUARD + e * n_el:] = inputs.sentinel_bits(GUARD // e, dtype, salt + 2).view(np.uint8)
+    body = host[GUARD:GUARD + e * n_el].view(np.uint16 if e == 2 else np.uint8).reshape(shape)
     if fill == "normal":
         body.reshape(-1)[:] = inputs.normal_bits(g, n_el, dtype)
     else:
         body.reshape(-1)[:] = inputs.sentinel_bits(n_el, dtype, salt)
-    return Mirror(kind, L, H, D, dtype, num_slots, page_size, host, body)
+    return Mirror(kind, L, H, D, dtype, num_slots, page_size, host, body, kvp=kvp)
 
 
 def oracle_pool(m: Mirror) -> oracle.Pool:
@@ -92,25 +94,25 @@ def oracle_pool(m: Mirror) -> oracle.Pool:
     base_addr = m.host.__array_interface__["data"][0]
     planes = []
     for layer in range(m.L):
-        for kv in range(2):
+        for kv in range(m.kvp):
             if m.kind == "slot_major":
                 view = m.body[:, layer, kv]
             elif m.kind == "planes_separate":  # plane p stored in block P-1-p
-                view = m.body[m.P - 1 - (2 * layer + kv)]
+                view = m.body[m.P - 1 - (m.kvp * layer + kv)]
             else:
-                view = m.body[2 * layer + kv]
+                view = m.body[m.kvp * layer + kv]
             planes.append((m.host, view.__array_interface__["data"][0] - base_addr))
     if m.kind == "slot_major":
         return oracle.Pool(m.L, m.H, m.D, m.elem, oracle.TOKEN_ROWS, m.num_slots, planes,
-                           m.body.strides[0])
+                           m.body.strides[0], kv_planes=m.kvp)
     if m.kind == "hnd":
         return oracle.Pool(m.L, m.H, m.D, m.elem, oracle.HND_PAGES, m.num_slots, planes, 0,
-                           m.page_size)
+                           m.page_size, kv_planes=m.kvp)
     return oracle.Pool(m.L, m.H, m.D, m.elem, oracle.TOKEN_ROWS, m.num_slots, planes,
-                       m.body.strides[1])
+                       m.body.strides[1], kv_planes=m.kvp)
 
 
-KVX_DTYPE = {"fp16": 1, "bf16": 2}
+KVX_DTYPE = {"fp16": 1, "bf16": 2, "fp8": 4}
 
 
 def kvx_layout(m: Mirror):
@@ -119,19 +121,21 @@ def kvx_layout(m: Mirror):
     base = m.dev_body_ptr()
     R, P = m.R, m.P
     dt = KVX_DTYPE[m.dtype]
+    kvp = m.kvp
     if m.kind == "planes":
         return kvx.Layout(m.L, m.H, m.D, dt, m.num_slots, base=base,
-                          plane_stride=m.num_slots * R, keepalive=m.dev)
+                          plane_stride=m.num_slots * R, keepalive=m.dev, kv_planes=kvp)
     if m.kind == "planes_separate":
         ptrs = [base + (P - 1 - p) * m.num_slots * R for p in range(P)]
-        return kvx.Layout(m.L, m.H, m.D, dt, m.num_slots, plane_ptrs=ptrs, keepalive=m.dev)
+        return kvx.Layout(m.L, m.H, m.D, dt, m.num_slots, plane_ptrs=ptrs, keepalive=m.dev,
+                          kv_planes=kvp)
     if m.kind == "slot_major":
         return kvx.Layout(m.L, m.H, m.D, dt, m.num_slots, base=base, plane_stride=R,
-                          slot_stride=P * R, keepalive=m.dev)
+                          slot_stride=P * R, keepalive=m.dev, kv_planes=kvp)
     if m.kind == "hnd":
         return kvx.Layout(m.L, m.H, m.D, dt, m.num_slots, kind=kvx.HND_PAGED,
                           page_size=m.page_size, base=base, plane_stride=m.num_slots * R,
-                          keepalive=m.dev)
+                          keepalive=m.dev, kv_planes=kvp)
     raise ValueError(m.kind)
 
 

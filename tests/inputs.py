@@ -50,7 +50,20 @@ def rng(cfg: int, role: int) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(seed(cfg, role)))
 
 
-ELEM_BYTES = {"fp16": 2, "bf16": 2}
+ELEM_BYTES = {"fp16": 2, "bf16": 2, "fp8": 1}
+
+
+def _e4m3_table() -> np.ndarray:
+    """Every finite fp8 E4M3 value by code (NaN codes 0x7F / 0xFF excluded): sign, 4 exponent
+    bits with bias 7, 3 mantissa bits, subnormals at exponent 0."""
+    vals = np.full(256, np.nan)
+    for code in range(256):
+        if code & 0x7F == 0x7F:
+            continue
+        s, e, m = code >> 7, (code >> 3) & 0xF, code & 0x7
+        mag = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+        vals[code] = -mag if s else mag
+    return vals
 
 
 # ---------------------------------------------------------------------------------------
@@ -58,8 +71,21 @@ ELEM_BYTES = {"fp16": 2, "bf16": 2}
 # ---------------------------------------------------------------------------------------
 
 def normal_bits(g: np.random.Generator, n_elems: int, dtype: str) -> np.ndarray:
-    """n_elems N(0,1) values as raw 16-bit patterns (uint16) of fp16 or bf16."""
+    """n_elems N(0,1) values as raw bit patterns: uint16 of fp16 or bf16, uint8 of fp8 E4M3
+    (nearest code, ties to the even code)."""
     x = g.standard_normal(n_elems).astype(np.float32)
+    if dtype == "fp8":
+        table = _e4m3_table()
+        codes = np.flatnonzero(~np.isnan(table))
+        order = codes[np.argsort(table[codes], kind="stable")]
+        vals = table[order]
+        xd = np.clip(x.astype(np.float64), vals[0], vals[-1])
+        hi = np.clip(np.searchsorted(vals, xd), 1, len(vals) - 1)
+        lo = hi - 1
+        dlo, dhi = xd - vals[lo], vals[hi] - xd
+        pick = np.where(dhi < dlo, hi, np.where(dlo < dhi, lo,
+                        np.where(order[lo] % 2 == 0, lo, hi)))
+        return order[pick].astype(np.uint8)
     if dtype == "fp16":
         return x.astype(np.float16).view(np.uint16)
     if dtype == "bf16":
@@ -70,9 +96,12 @@ def normal_bits(g: np.random.Generator, n_elems: int, dtype: str) -> np.ndarray:
 
 
 def sentinel_bits(n_elems: int, dtype: str, salt: int = 0) -> np.ndarray:
-    """Quiet-NaN payload patterns: fp16 0x7E00 | 9-bit payload, bf16 0x7FC0 | 6-bit payload."""
+    """Quiet-NaN payload patterns: fp16 0x7E00 | 9-bit payload, bf16 0x7FC0 | 6-bit payload;
+    fp8 E4M3 has two NaN codes only, 0x7F and 0xFF."""
     e = np.arange(n_elems, dtype=np.uint64) + np.uint64(salt) * np.uint64(0x9E3779B1)
     h = (e * np.uint64(0x9E3779B97F4A7C15)) >> np.uint64(40)
+    if dtype == "fp8":
+        return (np.uint8(0x7F) | ((h & np.uint64(1)) << np.uint64(7)).astype(np.uint8)).astype(np.uint8)
     if dtype == "fp16":
         return (np.uint16(0x7E00) | (h & np.uint64(0x1FF)).astype(np.uint16)).astype(np.uint16)
     if dtype == "bf16":

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_misc(lib):
-    assert kvx.version() == 100
+    assert kvx.version() == 200
     assert kvx.status_str(kvx.OK) == "ok"
     assert "range" in kvx.status_str(kvx.ERR_OUT_OF_RANGE)
     ws = kvx.workspace_size(2048, 0)
@@ -201,3 +201,20 @@ def test_move_heads_validation_before_cuda(lib):
     assert mv(S, None, 0, odd, 1, 1) == kvx.ERR_ALIGNMENT       # 8-byte heads: no 16-byte vectors
     assert mv(G, src, 0, None, 0, 2, buf=None, bb=0) == kvx.ERR_INVALID_ARG   # gather needs a buffer
     assert mv(G, src, 0, None, 0, 2, buf=FAKE * 7, bb=4 * 10 * 256 - 16) == kvx.ERR_INVALID_ARG
+
+
+def test_latent_plane_layouts(lib):
+    """kv_planes: 1 (MLA latent, P = L) or 2 (default, P = 2L); anything else refused; latent
+    and K/V layouts do not mix in one move."""
+    mla = kvx.Layout(27, 1, 576, kvx.BF16, 1000, base=FAKE, plane_stride=1000 * 1152, kv_planes=1)
+    assert mla.num_planes == 27 and mla.row_bytes == 1152
+    kv = kvx.Layout(27, 1, 576, kvx.BF16, 1000, base=FAKE * 2, plane_stride=1000 * 1152)
+    assert kv.num_planes == 54
+    with pytest.raises(kvx.KvxError):
+        kvx.Layout(2, 1, 64, kvx.BF16, 10, base=FAKE, plane_stride=4096, kv_planes=3)
+    with pytest.raises(kvx.KvxError):
+        kvx.Layout(200, 1, 64, kvx.BF16, 10, base=FAKE, plane_stride=4096)  # 400 planes
+    kvx.Layout(200, 1, 64, kvx.BF16, 10, base=FAKE, plane_stride=4096, kv_planes=1).close()
+    l = kvx.lib()
+    assert l.kvx_transfer(mla.handle, FAKE * 6, kv.handle, FAKE * 6, 10, FAKE * 4, 1 << 30,
+                          FAKE * 5, None) == kvx.ERR_INVALID_ARG
