@@ -17,6 +17,7 @@
 struct kvx_layout {
   int32_t num_layers, kv_heads, head_dim, elem, kind, page_size;
   int32_t kv_planes;  // planes per layer: 2 (K, V) or 1 (MLA latent)
+  int32_t vec;        // widest access (16, 8, 4, 2, 1 bytes) every row and head vector allows
   int32_t planes;
   int64_t num_slots;
   int64_t row_bytes, seg_bytes;
@@ -80,6 +81,13 @@ int32_t log2_exact(int64_t v) {
   int32_t sh = 0;
   while ((int64_t)1 << sh < v) ++sh;
   return sh;
+}
+
+// Largest power of two, at most 16, that divides x (x > 0).
+int32_t pow2_align(int64_t x) {
+  int32_t a = 16;
+  while (a > 1 && x % a != 0) a >>= 1;
+  return a;
 }
 
 kvx::Side pool_side(const kvx_layout *l) {
@@ -175,7 +183,16 @@ struct Call {
   int32_t heads = 0;
   int64_t row_bytes = 0, seg_bytes = 0;
   int64_t src_head_off = 0, dst_head_off = 0;
+  // Widest access every row, head vector and plane of the call allows.  Below 16 bytes the
+  // call takes the narrow row kernel with one row per plan chunk.
+  int32_t vec = 16;
 };
+
+// The access width a pool side allows: its own, and its head vectors' (the per-head
+// placement of the fast kernels moves 16-byte pieces of head vectors).
+int32_t side_vec(const kvx_layout *l) {
+  return l ? std::min(l->vec, pow2_align(l->seg_bytes)) : 16;
+}
 
 void set_whole_rows(Call &c) {
   c.planes = c.shape->planes;
@@ -183,6 +200,12 @@ void set_whole_rows(Call &c) {
   c.row_bytes = c.shape->row_bytes;
   c.seg_bytes = c.shape->seg_bytes;
   c.src_head_off = c.dst_head_off = 0;
+  c.vec = std::min(std::min(side_vec(c.src), side_vec(c.dst)), pow2_align(c.row_bytes));
+}
+
+// Rows per plan chunk: runs cut into chunks of up to KVX_CHUNK_BYTES, one row for narrow rows.
+int32_t call_chunk_rows(const Call &c) {
+  return c.vec < 16 ? 1 : chunk_rows_for(c.row_bytes);
 }
 
 // Checks the layouts an op needs and fills call.src / call.dst / call.shape.
@@ -268,7 +291,7 @@ kvx::PlanArgs plan_args(const Call &c, void *d_ws, int32_t *d_status) {
   a.op = c.op;
   a.n_tokens = c.n_tokens;
   a.n_segs = c.n_segs;
-  a.chunk_rows = chunk_rows_for(c.row_bytes);
+  a.chunk_rows = call_chunk_rows(c);
   a.planes = c.planes;
   a.row_bytes = (int32_t)c.row_bytes;
   a.src = src_side(c);
@@ -309,11 +332,12 @@ void fill_copy_args(kvx::CopyArgs &a, const Call &c, const kvx_request *d_reqs, 
   a.op = c.op;
   a.n_tokens = c.n_tokens;
   a.n_segs = c.n_segs;
-  a.chunk_rows = chunk_rows_for(c.row_bytes);
+  a.chunk_rows = call_chunk_rows(c);
   a.planes = c.planes;
   a.row_bytes = (int32_t)c.row_bytes;
   a.seg_bytes = (int32_t)c.seg_bytes;
   a.heads = c.heads;
+  a.vec_bytes = c.vec;
   a.src = src_side(c);
   a.dst = dst_side(c);
   a.buf = static_cast<char *>(d_buf);
@@ -341,6 +365,10 @@ kvx_status enqueue_copy(const Call &c, const kvx_request *d_reqs, void *d_buf, c
   fill_copy_args(a, c, d_reqs, d_buf, d_ws, d_status);
   a.spec_src = spec_src;
   a.spec_dst = spec_dst;
+  if (c.vec < 16) {  // narrow rows: one warp per row, read after the planner
+    const cudaError_t e = kvx::launch_narrow(a, s);
+    return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+  }
   if (kvx::copy_variant(a) == kvx::kVariantRow) {
     a.host_status = host_status;
     if (host_status_written) *host_status_written = host_status != nullptr;
@@ -398,7 +426,6 @@ kvx_status kvx_layout_create(const kvx_layout_desc *d, kvx_layout_t *out) {
   const int64_t seg = (int64_t)d->head_dim * eb;
   const int64_t R = seg * d->kv_heads;
   if (R > (int64_t)1 << 30) return KVX_ERR_INVALID_ARG;
-  if (R % 16 != 0) return KVX_ERR_ALIGNMENT;
   kvx_layout *l = new (std::nothrow) kvx_layout;
   if (!l) return KVX_ERR_INVALID_ARG;
   std::memset(l, 0, sizeof(*l));
@@ -413,11 +440,13 @@ kvx_status kvx_layout_create(const kvx_layout_desc *d, kvx_layout_t *out) {
   l->row_bytes = R;
   l->seg_bytes = seg;
   kvx_status st = KVX_OK;
+  // Rows move in the widest accesses that every row start, head vector and plane allows:
+  // 16 bytes for the usual shapes, narrower for rows that are not 16-byte multiples.
+  l->vec = pow2_align(R);
   if (d->kind == KVX_HND_PAGED) {
     if (d->page_size < 1 || d->num_slots % d->page_size != 0 || d->slot_stride != 0)
       st = KVX_ERR_INVALID_ARG;
-    else if (seg % 16 != 0)
-      st = KVX_ERR_ALIGNMENT;
+    l->vec = std::min(l->vec, pow2_align(seg));  // a head vector is contiguous, not a row
     l->page_size = d->page_size;
     l->page_bytes = R * d->page_size;
     l->extent = l->page_bytes * (d->num_slots / (d->page_size > 0 ? d->page_size : 1));
@@ -425,8 +454,8 @@ kvx_status kvx_layout_create(const kvx_layout_desc *d, kvx_layout_t *out) {
     l->page_size = 1;
     l->slot_stride = d->slot_stride == 0 ? R : d->slot_stride;
     if (l->slot_stride < R) st = KVX_ERR_INVALID_ARG;
-    else if (l->slot_stride % 16 != 0) st = KVX_ERR_ALIGNMENT;
     else if (l->slot_stride > ((int64_t)1 << 62) / d->num_slots) st = KVX_ERR_INVALID_ARG;
+    l->vec = std::min(l->vec, pow2_align(l->slot_stride));
     l->extent = (d->num_slots - 1) * l->slot_stride + R;
   }
   if (st == KVX_OK) {
@@ -441,7 +470,8 @@ kvx_status kvx_layout_create(const kvx_layout_desc *d, kvx_layout_t *out) {
         a = (uintptr_t)d->base + (uintptr_t)(d->plane_stride * p);
       }
       if (a == 0) { st = KVX_ERR_INVALID_ARG; break; }
-      if (a % 16 != 0) { st = KVX_ERR_ALIGNMENT; break; }
+      if (a % l->elem != 0) { st = KVX_ERR_ALIGNMENT; break; }  // elements stay aligned
+      l->vec = std::min(l->vec, pow2_align((int64_t)a));
       l->plane[p] = a;
       if (a < l->lo) l->lo = a;
       if (a + l->extent > l->hi) l->hi = a + l->extent;
@@ -607,8 +637,7 @@ static kvx_status run_call(const Call &c, const int32_t *d_src_slots, const int3
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // Requests of up to the fused limit with rows under KVX_CHUNK_BYTES take the one-launch
   // path; the rest take the planner + row kernel (the row kernel overlaps the planner).
-  const bool fused = chunk_rows_for(c.row_bytes) > 1 &&
-                     n <= g_fused_max.load(std::memory_order_relaxed);
+  const bool fused = call_chunk_rows(c) > 1 && n <= g_fused_max.load(std::memory_order_relaxed);
   if (n == 0 || !fused) {
     kvx::PlanArgs a = plan_args(c, d_ws, d_status);
     a.src_idx = d_src_slots;
@@ -812,6 +841,7 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
   kvx_status st = bind_layouts(c, src, dst);
   if (st == KVX_OK) st = check_buffer(c, d_buf, buf_bytes);
   if (st != KVX_OK) return st;
+  if (c.vec < 16) return KVX_ERR_ALIGNMENT;  // the streamed kernels move 16-byte vectors
   const int32_t layers = c.shape->num_layers;
   kvx::StreamCtl k = {};
   k.layer_ready = static_cast<const int32_t *>(device_word(ctl->layer_ready));
@@ -950,9 +980,10 @@ kvx_status kvx_move_heads(int32_t op, kvx_layout_t src, const int32_t *d_src_slo
   c.row_bytes = (int64_t)n_heads * c.seg_bytes;
   c.src_head_off = c.src ? head_offset(src, src_head0) : 0;
   c.dst_head_off = c.dst ? head_offset(dst, dst_head0) : 0;
-  // every 16-byte vector of the slice stays inside one head (HND) and starts 16-byte aligned
-  if (c.row_bytes % 16 != 0 || c.src_head_off % 16 != 0 || c.dst_head_off % 16 != 0)
-    return KVX_ERR_ALIGNMENT;
+  // accesses no wider than the slice's length and start on either side allow
+  c.vec = std::min(std::min(side_vec(c.src), side_vec(c.dst)), pow2_align(c.row_bytes));
+  if (c.src_head_off) c.vec = std::min(c.vec, pow2_align(c.src_head_off));
+  if (c.dst_head_off) c.vec = std::min(c.vec, pow2_align(c.dst_head_off));
   kvx_status st = check_buffer(c, d_buf, buf_bytes);
   if (st != KVX_OK) return st;
   return run_call(c, d_src_slots, d_dst_slots, d_buf, d_ws, ws_bytes, d_status, stream);

@@ -26,19 +26,6 @@ namespace {
 
 using namespace ops;
 
-__device__ __forceinline__ bool header_matches(const CopyArgs &a) {
-  const PlanHeader *h = reinterpret_cast<const PlanHeader *>(a.ws + a.L.header_off);
-  // slot-list and run-list plans share one chunk format; a batch plan must be run as a batch
-  const bool batch = a.mode == kModeBatch;
-  return h->magic == kPlanMagic && (h->mode == kModeBatch) == batch && h->op == a.op &&
-         (!batch || h->n_segs == a.n_segs) && h->n_tokens == a.n_tokens &&
-         h->chunk_rows == a.chunk_rows &&
-         h->planes == a.planes && h->row_bytes == a.row_bytes &&
-         h->src_is_pool == a.src.is_pool && h->src_hnd == a.src.hnd &&
-         h->src_page_size == a.src.page_size && h->dst_is_pool == a.dst.is_pool &&
-         h->dst_hnd == a.dst.hnd && h->dst_page_size == a.dst.page_size &&
-         h->src_num_slots == a.src.num_slots && h->dst_num_slots == a.dst.num_slots;
-}
 
 // Common start of every copy kernel: checks the plan header (and, for single calls, the
 // status word) and turns the per-tile chunk counts into each tile's first chunk in shared

@@ -13,6 +13,21 @@ constexpr int kUnroll = 4;  // independent 16-byte loads in flight per lane
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Whether the plan in the workspace was made for this call's sizes and sides.
+__device__ __forceinline__ bool header_matches(const CopyArgs &a) {
+  const PlanHeader *h = reinterpret_cast<const PlanHeader *>(a.ws + a.L.header_off);
+  // slot-list and run-list plans share one chunk format; a batch plan must be run as a batch
+  const bool batch = a.mode == kModeBatch;
+  return h->magic == kPlanMagic && (h->mode == kModeBatch) == batch && h->op == a.op &&
+         (!batch || h->n_segs == a.n_segs) && h->n_tokens == a.n_tokens &&
+         h->chunk_rows == a.chunk_rows &&
+         h->planes == a.planes && h->row_bytes == a.row_bytes &&
+         h->src_is_pool == a.src.is_pool && h->src_hnd == a.src.hnd &&
+         h->src_page_size == a.src.page_size && h->dst_is_pool == a.dst.is_pool &&
+         h->dst_hnd == a.dst.hnd && h->dst_page_size == a.dst.page_size &&
+         h->src_num_slots == a.src.num_slots && h->dst_num_slots == a.dst.num_slots;
+}
+
 // Nanoseconds of the GPU's global timer (bounds every wait in libkvx's kernels).
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;

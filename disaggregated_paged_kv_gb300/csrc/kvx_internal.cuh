@@ -151,7 +151,7 @@ struct CopyArgs {
   const int32_t *spec_src;
   const int32_t *spec_dst;
   int32_t row_group_shift;  // row kernel: log2 of the tokens one warp moves
-  int32_t pad2;
+  int32_t vec_bytes;        // widest access the call's rows allow: 16, or 8/4/2/1 (kvx_narrow.cu)
   // kvx_submit with a pinned host status word: the row kernel stores the final status there
   // itself (through its device mapping) instead of a device-to-host copy.  nullptr: none.
   int32_t *host_status;
@@ -214,6 +214,8 @@ constexpr int kBulkThreadsPerCta = 32;
 constexpr int kBulkSmallTiles = 256;  // occupancy is cached for <= this many tiles and for the max
 // Records e as this thread's kvx_last_cuda_error().
 void record_cuda_error(cudaError_t e);
+// Rows that do not allow 16-byte accesses (kvx_narrow.cu): one warp per (token, plane) row.
+cudaError_t launch_narrow(const CopyArgs &a, cudaStream_t s);
 // Layer-streamed copy (kvx_stream.cu): persistent grid over layer-major row groups.
 int stream_blocks_per_sm();
 void stream_sizes(StreamCtl &k, int64_t n_tokens, int32_t group_shift);

@@ -50,7 +50,7 @@ def _rng(k):
     return np.random.Generator(np.random.PCG64(9000 + k))
 
 
-def _mirror(kind, shape, fill, g=None, num=2048, salt=0):
+def _mirror(kind, shape, fill, g=None, num=1024, salt=0):
     L, H, D, dt, kvp = SHAPES[shape]
     return hz.make_mirror(kind, L, H, D, dt, num, 16 if kind == "hnd" else 1, fill, g, salt=salt,
                           kvp=kvp)
@@ -64,7 +64,7 @@ def _slots(k, n, num):
 @pytest.mark.parametrize("src_kind", KINDS)
 @pytest.mark.parametrize("dst_kind", KINDS)
 def test_transfer_formats(shape, src_kind, dst_kind, path):
-    n = 700
+    n = 500
     src = _mirror(src_kind, shape, "normal", _rng(1)).to_device()
     dst = _mirror(dst_kind, shape, "sentinel", salt=2).to_device()
     exp = _mirror(dst_kind, shape, "sentinel", salt=2)
@@ -82,7 +82,7 @@ def test_transfer_formats(shape, src_kind, dst_kind, path):
 
 @pytest.mark.parametrize("shape", sorted(SHAPES))
 @pytest.mark.parametrize("kind", KINDS)
-@pytest.mark.parametrize("n", [1, 128, 2048])
+@pytest.mark.parametrize("n", [1, 128, 1000])
 def test_gather_scatter_formats(shape, kind, n, path):
     L, H, D, dt, kvp = SHAPES[shape]
     src = _mirror(kind, shape, "normal", _rng(n)).to_device()
@@ -117,7 +117,7 @@ def test_stream_latent_layers(shape, max_ctas):
     """kvx_stream over one latent plane per layer: layers below a never-raised layer k move,
     the rest stay untouched (the oracle's layer-range transfer)."""
     L, H, D, dt, kvp = SHAPES[shape]
-    n, k = 900, 11
+    n, k = 700, 11
     src = _mirror("planes", shape, "normal", _rng(30)).to_device()
     dst = _mirror("hnd", shape, "sentinel", salt=6).to_device()
     exp = _mirror("hnd", shape, "sentinel", salt=6)
