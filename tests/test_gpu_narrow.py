@@ -83,7 +83,7 @@ def test_gather_scatter_plan_execute_narrow(shape, kind, path):
     """Gather by kvx_gather, then scatter through a separate kvx_plan + kvx_execute."""
     L, H, D, dt = SHAPES[shape]
     n = 2500
-    src = _mirror(kind, shape, "normal", _rng(5)).to_device()
+    src = _mirror(kind, shape, "normal", _rng(5), num=4096).to_device()
     s = _slots(6, n, src.num_slots)
     rc, want, w = oracle.gather(hz.oracle_pool(src), s)
     assert rc == oracle.OK
@@ -97,8 +97,8 @@ def test_gather_scatter_plan_execute_narrow(shape, kind, path):
     exp_buf[hz.GUARD:hz.GUARD + w] = want
     hz.assert_same_bytes(buf.readback(), exp_buf, f"gather {shape} {kind}")
 
-    dst = _mirror(kind, shape, "sentinel", salt=7).to_device()
-    exp = _mirror(kind, shape, "sentinel", salt=7)
+    dst = _mirror(kind, shape, "sentinel", num=4096, salt=7).to_device()
+    exp = _mirror(kind, shape, "sentinel", num=4096, salt=7)
     d = _slots(8, n, dst.num_slots)
     assert oracle.scatter(hz.oracle_pool(exp), d, want)[0] == oracle.OK
     ws, st = hz.workspace(n), hz.status()
