@@ -71,7 +71,8 @@ def parse_args():
     ap.add_argument("--workload", default="2",
                     help="2 (default): the headline transfer; 1, 3, 4, 5: the other workloads; "
                          "stream: the headline transfer through kvx_stream (layer-streamed); "
-                         "tp: the headline request resharded between TP groups (kvx_move_heads)")
+                         "tp: the headline request resharded between TP groups (kvx_move_heads); "
+                         "formats: MLA, fp8, narrow rows and cross-kind transcoding")
     ap.add_argument("--layer-us", type=float, default=100.0,
                     help="--workload stream: host cadence of the emulated producer, us/layer")
     return ap.parse_args()
@@ -488,6 +489,101 @@ class OracleTransfer:
         return (time.perf_counter() - t0) / max(n, 1), n
 
 
+def run_formats(args):
+    """Pool-to-pool transfers of one request of random slots in other layouts and dtypes, each
+    timed like the headline (L2 flushed before every step, CUDA events around kvx_transfer):
+      mla_bf16   DeepSeek-V2-Lite-shaped MLA latent rows (27 layers x 576 bf16 = 1152 B),
+                 16384 tokens, one plane per layer
+      mla_fp8    the same latent rows in fp8 (576 B)
+      gqa_fp8    the headline shape in fp8 (36 x K/V x 8 x 128: 1 KiB rows), 2048 tokens
+      narrow     200-byte rows (one head of head_dim 100 fp16) through 8-byte accesses
+      transcode  the headline shape from a slot-major pool into per-plane pools"""
+    import numpy as np
+    import torch
+
+    from disaggregated_paged_kv_gb300 import kvx
+    from tests import inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kvx.lib()
+    stream = torch.cuda.Stream(device=dev)
+    sp = int(stream.cuda_stream)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    peaks, _ = measured_peaks()
+    # name: (layers, heads, head_dim, elem bytes, kv_planes, tokens, pool slots, src slot-major)
+    cases = {
+        "mla_bf16": (27, 1, 576, 2, 1, 16384, 65536, False),
+        "mla_fp8": (27, 1, 576, 1, 1, 16384, 65536, False),
+        "gqa_fp8": (36, 8, 128, 1, 2, 2048, 65536, False),
+        "narrow": (36, 1, 100, 2, 2, 16384, 65536, False),
+        "transcode": (36, 8, 128, 2, 2, 2048, 32768, True),
+    }
+    dts = {1: kvx.FP8, 2: kvx.BF16}
+    results = {}
+    for name, (Lc, Hc, Dc, e, kvp, n, NS, slot_major) in cases.items():
+        Pc, Rc = kvp * Lc, Hc * Dc * e
+        src = torch.randint(0, 255, (Pc * NS * Rc,), dtype=torch.uint8, device=dev)
+        dst = torch.zeros(Pc * NS * Rc, dtype=torch.uint8, device=dev)
+        if slot_major:
+            sl = kvx.Layout(Lc, Hc, Dc, dts[e], NS, base=src, plane_stride=Rc,
+                            slot_stride=Pc * Rc, kv_planes=kvp)
+        else:
+            sl = kvx.Layout(Lc, Hc, Dc, dts[e], NS, base=src, plane_stride=NS * Rc, kv_planes=kvp)
+        dl = kvx.Layout(Lc, Hc, Dc, dts[e], NS, base=dst, plane_stride=NS * Rc, kv_planes=kvp)
+        s_d = torch.from_numpy(inputs.distinct_slots(inputs.rng(2, inputs.ROLE_SRC_SLOTS), n, NS)).to(dev)
+        d_d = torch.from_numpy(inputs.distinct_slots(inputs.rng(2, inputs.ROLE_DST_SLOTS), n, NS)).to(dev)
+        ws = torch.empty(kvx.workspace_size(n, 0), dtype=torch.uint8, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def step():
+            kvx.transfer(sl, s_d, dl, d_d, n, ws, st, stream=sp)
+
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                flush.fill_(1)
+                step()
+        torch.cuda.synchronize()
+        assert int(st.item()) == kvx.OK
+        # spot check token 7, plane 1: bytes equal
+        k = 7
+        so = (int(s_d[k]) * Pc + 1) * Rc if slot_major else (NS + int(s_d[k])) * Rc
+        do = (NS + int(d_d[k])) * Rc
+        assert torch.equal(dst[do:do + Rc], src[so:so + Rc])
+        K = args.steps
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                flush.fill_(i & 0xFF)
+                ev[i][0].record(stream)
+                step()
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        alg = 2 * n * Pc * Rc + 8 * n
+        gbs = alg / (ms * 1e-3) / 1e9
+        results[name] = {"row_bytes": Rc, "planes": Pc, "tokens": n,
+                         "payload_bytes_each_way": n * Pc * Rc, "us_per_request": ms * 1e3,
+                         "GBs": gbs, "frac_of_measured_hbm": gbs / float(peaks["hbm_gbs"])}
+        del src, dst, sl, dl
+        torch.cuda.empty_cache()
+    head = results["mla_bf16"]
+    line = {
+        "metric": "KV transfer GB/s (read+write) in other layouts and dtypes",
+        "value": head["GBs"], "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["us_per_request"] * 1e-3,
+        "higher_is_better": True, "dtype": "u8", "data": "synthetic (random bytes)",
+        "config": {"workload": "pool-to-pool transfers of random slots; value = MLA bf16 "
+                               "(27 latent planes x 1152 B, 16384 tokens)",
+                   "l2": "flushed before every timed step (write of 2x L2, outside the events)"},
+        "formats": results,
+        "gpu_launches": 2 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_tp(args):
     """The headline request (2048 random tokens, 36 layers x K/V x 8 kv heads x 128 bf16) moved
     between tensor-parallel groups of different sizes: for every (P rank, D rank) pair the heads
@@ -790,6 +886,9 @@ def main():
         return
     if args.workload == "tp":
         run_tp(args)
+        return
+    if args.workload == "formats":
+        run_formats(args)
         return
     if int(args.workload) != 2:
         run_workload(args, int(args.workload))

@@ -365,7 +365,8 @@ kvx_status enqueue_copy(const Call &c, const kvx_request *d_reqs, void *d_buf, c
   fill_copy_args(a, c, d_reqs, d_buf, d_ws, d_status);
   a.spec_src = spec_src;
   a.spec_dst = spec_dst;
-  if (c.vec < 16) {  // narrow rows: one warp per row, read after the planner
+  if (c.vec < 16) {  // narrow rows: read after the planner, several rows per warp
+    a.row_group_shift = kvx::narrow_group_shift(a.row_bytes, a.vec_bytes);
     const cudaError_t e = kvx::launch_narrow(a, s);
     return e == cudaSuccess ? KVX_OK : cuda_fail(e);
   }

@@ -216,6 +216,8 @@ constexpr int kBulkSmallTiles = 256;  // occupancy is cached for <= this many ti
 void record_cuda_error(cudaError_t e);
 // Rows that do not allow 16-byte accesses (kvx_narrow.cu): one warp per (token, plane) row.
 cudaError_t launch_narrow(const CopyArgs &a, cudaStream_t s);
+// log2 of the tokens one warp of the narrow kernel moves (CopyArgs::row_group_shift).
+int32_t narrow_group_shift(int32_t row_bytes, int32_t vec_bytes);
 // Layer-streamed copy (kvx_stream.cu): persistent grid over layer-major row groups.
 int stream_blocks_per_sm();
 void stream_sizes(StreamCtl &k, int64_t n_tokens, int32_t group_shift);
