@@ -815,15 +815,19 @@ std::atomic<uint64_t> g_stream_gen{0xD1B54A32D192ED03ull};
 static_assert(sizeof(kvx::Chunk) * kvx::kTile >= 8 * (2 + KVX_MAX_PLANES / 2),
               "the stream mirror fits in one tile's chunk table");
 
-static const void *device_word(const void *p) {
+static const void *device_word(const void *p, bool *in_device_memory = nullptr) {
+  if (in_device_memory) *in_device_memory = false;
   if (!p) return nullptr;
   cudaPointerAttributes at;
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
     (void)cudaGetLastError();
     return nullptr;
   }
-  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return at.devicePointer;
-  if (at.type == cudaMemoryTypeHost) return at.devicePointer;
+  if (at.type == cudaMemoryTypeDevice) {
+    if (in_device_memory) *in_device_memory = true;
+    return at.devicePointer;
+  }
+  if (at.type == cudaMemoryTypeManaged || at.type == cudaMemoryTypeHost) return at.devicePointer;
   return nullptr;
 }
 
@@ -845,8 +849,10 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
   if (c.vec < 16) return KVX_ERR_ALIGNMENT;  // the streamed kernels move 16-byte vectors
   const int32_t layers = c.shape->num_layers;
   kvx::StreamCtl k = {};
-  k.layer_ready = static_cast<const int32_t *>(device_word(ctl->layer_ready));
-  k.epoch_word = static_cast<const int32_t *>(device_word(ctl->epoch_word));
+  bool ready_local = false, epoch_local = false;
+  k.layer_ready = static_cast<const int32_t *>(device_word(ctl->layer_ready, &ready_local));
+  k.epoch_word = static_cast<const int32_t *>(device_word(ctl->epoch_word, &epoch_local));
+  k.words_local = (!ctl->layer_ready || ready_local) && (!ctl->epoch_word || epoch_local);
   k.host_done = static_cast<int32_t *>(const_cast<void *>(pinned_alias(ctl->host_done)));
   if ((ctl->layer_ready && (!k.layer_ready || !aligned(ctl->layer_ready, 4))) ||
       (ctl->epoch_word && (!k.epoch_word || !aligned(ctl->epoch_word, 4))) ||

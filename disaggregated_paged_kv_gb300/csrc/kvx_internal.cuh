@@ -181,6 +181,10 @@ struct StreamCtl {
   uint32_t items;      // per_layer * layers (< 2^32 for every legal size)
   uint32_t block;      // consecutive items a warp takes per block (see kvx_stream.cu)
   int32_t kv_planes;   // planes per layer: 2 (K, V) or 1 (MLA latent); plane = kv_planes*l + kv
+  // The producer's words all live in this GPU's memory (or are absent): a direct read costs
+  // what a mirror read costs, so the waits read them first and skip the mirror.
+  int32_t words_local;
+  int32_t pad3;
 };
 
 // Launchers (enqueue only; return the launch's cudaError_t).

@@ -59,6 +59,18 @@ __device__ __forceinline__ int32_t ld_acquire_sys(const int32_t *p) {
   return v;
 }
 
+__device__ __forceinline__ uint64_t ld_relaxed_gpu(const uint64_t *p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int32_t ld_relaxed_sys(const int32_t *p) {
+  int32_t v;
+  asm volatile("ld.relaxed.sys.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void st_release_sys(int32_t *p, int32_t v) {
   asm volatile("st.release.sys.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -122,6 +134,14 @@ __device__ int32_t wait_layer(const StreamCtl &k, int32_t l, bool owner, CtaStat
   if (!k.layer_ready && !k.epoch_word) {  // nothing to wait for
     or_release_cta(&cs->ready[l >> 5], bit);
     return 1;
+  }
+  if (k.words_local) {  // one round trip: the epoch and the ready word together
+    const int32_t e = k.epoch_word ? ld_relaxed_sys(k.epoch_word) : k.epoch;
+    const bool ready = !k.layer_ready || ld_acquire_sys(k.layer_ready + l) >= k.ready_value;
+    if (e == k.epoch && ready) {
+      or_release_cta(&cs->ready[l >> 5], bit);
+      return 1;
+    }
   }
   const bool poller = !(atomicOr(&cs->polling[l >> 5], bit) & bit);
   const uint64_t t0 = globaltimer_ns();
@@ -259,18 +279,6 @@ __global__ void __launch_bounds__(kCopyThreads, 6) stream_kernel(const __grid_co
 // workspace -- decodes as "no stop".
 constexpr int kStopWord = 1 + KVX_MAX_PLANES / 2;
 
-__device__ __forceinline__ uint64_t ld_relaxed_gpu(const uint64_t *p) {
-  uint64_t v;
-  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ int32_t ld_relaxed_sys(const int32_t *p) {
-  int32_t v;
-  asm volatile("ld.relaxed.sys.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 struct Stop {
   int32_t layer;  // first layer not to move
   int32_t code;   // KVX_ERR_TIMEOUT / KVX_ERR_CANCELLED; 0: no stop
@@ -296,6 +304,11 @@ __device__ __forceinline__ void publish_stop(const StreamCtl &k, uint64_t seen, 
 
 // Thread 0 of a CTA: waits until layer l may move.  Returns 0 to go on, else the stop code.
 __device__ int32_t row_wait(const StreamCtl &k, int32_t l, bool owner) {
+  if (k.words_local) {  // one round trip: the epoch and the ready word together
+    const int32_t e = k.epoch_word ? ld_relaxed_sys(k.epoch_word) : k.epoch;
+    const bool ready = !k.layer_ready || ld_acquire_sys(k.layer_ready + l) >= k.ready_value;
+    if (e == k.epoch && ready) return 0;
+  }
   const uint64_t t0 = globaltimer_ns();
   uint32_t sleep_ns = 32;
   for (uint32_t it = 0;; ++it) {
