@@ -587,8 +587,9 @@ def run_formats(args):
 def run_tp(args):
     """The headline request (2048 random tokens, 36 layers x K/V x 8 kv heads x 128 bf16) moved
     between tensor-parallel groups of different sizes: for every (P rank, D rank) pair the heads
-    kvx_tp_slice assigns it, one kvx_move_heads transfer each, all on one stream.  A step is
-    the whole reshard (every pair); L2 flushed before each step.  P pools are HND pages of 16
+    kvx_tp_slice assigns it, one kvx_move_heads transfer each, each pair on its own stream
+    (forked from and joined back into the timed stream; also timed with every pair on one
+    stream).  A step is the whole reshard (every pair); L2 flushed before each step.  P pools are HND pages of 16
     tokens, D pools per-plane token rows."""
     import numpy as np
     import torch
@@ -628,7 +629,26 @@ def run_tp(args):
                 if nh:
                     plan.append((pr, dr, sh0, dh0, nh))
 
+        # one stream, workspace and status per pair: independent pairs overlap on the GPU
+        side = [torch.cuda.Stream(device=dev) for _ in plan]
+        wss = [torch.empty(kvx.workspace_size(N_TOK, 0), dtype=torch.uint8, device=dev)
+               for _ in plan]
+        sts = [torch.zeros(1, dtype=torch.int32, device=dev) for _ in plan]
+        fork = torch.cuda.Event()
+        joins = [torch.cuda.Event() for _ in plan]
+
         def step():
+            fork.record(stream)
+            for j, (pr, dr, sh0, dh0, nh) in enumerate(plan):
+                side[j].wait_event(fork)
+                kvx.move_heads(kvx.OP_TRANSFER, p_l[pr], s_dev, sh0, d_l[dr], d_dev, dh0, nh,
+                               N_TOK, None, wss[j], sts[j], buf_bytes=0,
+                               stream=int(side[j].cuda_stream))
+                joins[j].record(side[j])
+            for ev_j in joins:
+                stream.wait_event(ev_j)
+
+        def step_serial():
             for pr, dr, sh0, dh0, nh in plan:
                 kvx.move_heads(kvx.OP_TRANSFER, p_l[pr], s_dev, sh0, d_l[dr], d_dev, dh0, nh,
                                N_TOK, None, ws, st, buf_bytes=0, stream=sp)
@@ -637,8 +657,9 @@ def run_tp(args):
             for _ in range(args.warmup):
                 flush.fill_(1)
                 step()
+                step_serial()
         torch.cuda.synchronize()
-        assert int(st.item()) == kvx.OK
+        assert int(st.item()) == kvx.OK and all(int(x.item()) == kvx.OK for x in sts)
         # spot check: token k, plane 0, first moved head of the first pair
         pr, dr, sh0, dh0, nh = plan[0]
         k = 97
@@ -647,22 +668,28 @@ def run_tp(args):
         want = p_pools[pr][0, sslot // 16, sh0:sh0 + nh, sslot % 16]
         assert torch.equal(got.view(torch.int16), want.view(torch.int16))
         K = args.steps
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(K)]
-        with torch.cuda.stream(stream):
-            for i in range(K):
-                flush.fill_(i & 0xFF)
-                ev[i][0].record(stream)
-                step()
-                ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+        def timed(fn):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(K)]
+            with torch.cuda.stream(stream):
+                for i in range(K):
+                    flush.fill_(i & 0xFF)
+                    ev[i][0].record(stream)
+                    fn()
+                    ev[i][1].record(stream)
+            torch.cuda.synchronize()
+            return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+        ms = timed(step)
+        ms_serial = timed(step_serial)
         alg = alg_bytes(N_TOK) + 8 * N_TOK * (len(plan) - 1)  # every pair reads both lists
         gbs = alg / (ms * 1e-3) / 1e9
         results[f"p{p_tp}_to_d{d_tp}"] = {
             "pairs": len(plan), "launches_per_reshard": 2 * len(plan),
             "us_per_reshard": ms * 1e3, "GBs": gbs,
             "frac_of_measured_hbm": gbs / float(peaks["hbm_gbs"]),
+            "us_per_reshard_one_stream": ms_serial * 1e3,
             "slice_bytes": plan[0][4] * D * 2}
         del p_pools, d_pools, p_l, d_l
         torch.cuda.empty_cache()
