@@ -72,7 +72,8 @@ def parse_args():
                     help="2 (default): the headline transfer; 1, 3, 4, 5: the other workloads; "
                          "stream: the headline transfer through kvx_stream (layer-streamed); "
                          "tp: the headline request resharded between TP groups (kvx_move_heads); "
-                         "formats: MLA, fp8, narrow rows and cross-kind transcoding")
+                         "formats: MLA, fp8, narrow rows and cross-kind transcoding; "
+                         "comparators: other ways to move the headline bytes (context)")
     ap.add_argument("--layer-us", type=float, default=100.0,
                     help="--workload stream: host cadence of the emulated producer, us/layer")
     return ap.parse_args()
@@ -157,6 +158,14 @@ class Clocks:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def step_percentiles(step_ms):
+    """p10, median and p90 of per-step times, in us (CUDA event timestamps tick in ~1-2 us
+    steps on this GPU, so these are coarse; the mean is the headline)."""
+    xs = sorted(step_ms)
+    n = len(xs)
+    return [xs[n // 10] * 1e3, xs[n // 2] * 1e3, xs[(9 * n) // 10] * 1e3]
 
 
 def max_over_ranks(x: float, device=None) -> float:
@@ -487,6 +496,107 @@ class OracleTransfer:
             assert rc == self.oracle.OK
             n += 1
         return (time.perf_counter() - t0) / max(n, 1), n
+
+
+def _cudart():
+    """The CUDA runtime library of the toolkit, for plain cudaMemcpyAsync calls."""
+    import ctypes
+    import glob
+    cands = (glob.glob("/usr/local/cuda/lib64/libcudart.so*") +
+             glob.glob("/usr/local/cuda/targets/*/lib/libcudart.so*"))
+    for c in sorted(cands):
+        try:
+            lib = ctypes.CDLL(c)
+            lib.cudaMemcpyAsync.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                            ctypes.c_int, ctypes.c_void_p]
+            lib.cudaMemcpyAsync.restype = ctypes.c_int
+            return lib
+        except OSError:
+            continue
+    return None
+
+
+def run_comparators(args):
+    """Other ways to move the headline request's bytes on the same GB300 (context, not shipped):
+    a contiguous device-to-device copy of the same byte count (the streaming ceiling), one
+    cudaMemcpyAsync per 2 KiB fragment (the per-block path of the pages' first design, 147,456
+    copies), and torch index_select + index_copy_ over the [72][slots][8][128] pools.  L2 flushed
+    before each step; CUDA events on the launching stream."""
+    import torch
+
+    from disaggregated_paged_kv_gb300 import kvx
+    from tests import inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    NS = args.pool_slots
+    stream = torch.cuda.Stream(device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(inputs.seed(2, inputs.ROLE_VALUES))
+    src = torch.randn((P, NS, H, D), dtype=torch.bfloat16, device=dev, generator=gen)
+    dst = torch.empty((P, NS, H, D), dtype=torch.bfloat16, device=dev)
+    s_np = inputs.distinct_slots(inputs.rng(2, inputs.ROLE_SRC_SLOTS), N_TOK, NS)
+    d_np = inputs.distinct_slots(inputs.rng(2, inputs.ROLE_DST_SLOTS), N_TOK, NS)
+    s_dev = torch.from_numpy(s_np).to(dev).long()
+    d_dev = torch.from_numpy(d_np).to(dev).long()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flat_src = src.view(-1)[: N_TOK * P * H * D]
+    flat_dst = dst.view(-1)[: N_TOK * P * H * D]
+
+    def timed(fn, K):
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                flush.fill_(1)
+                fn()
+            torch.cuda.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(K)]
+            for i in range(K):
+                flush.fill_(i & 0xFF)
+                ev[i][0].record(stream)
+                fn()
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+
+    res = {}
+    res["contiguous_d2d_copy_us"] = timed(lambda: flat_dst.copy_(flat_src), args.steps)
+
+    def index_path():
+        dst.index_copy_(1, d_dev, src.index_select(1, s_dev))
+
+    res["torch_index_select_index_copy_us"] = timed(index_path, max(3, args.steps // 20))
+
+    rt = _cudart()
+    if rt is not None:
+        sp = stream.cuda_stream
+        base_s, base_d = src.data_ptr(), dst.data_ptr()
+        offs = [(p * NS + int(si)) * R for p in range(P) for si in s_np]
+        offd = [(p * NS + int(di)) * R for p in range(P) for di in d_np]
+        pairs = list(zip(offs, offd))
+
+        def per_fragment():
+            for a, b in pairs:
+                rt.cudaMemcpyAsync(base_d + b, base_s + a, R, 3, sp)  # device to device
+
+        res["per_fragment_memcpy_us"] = timed(per_fragment, 2)
+        res["per_fragment_copies"] = len(pairs)
+    else:
+        res["per_fragment_memcpy_us"] = None
+    kvx.lib()
+    nb = alg_bytes(N_TOK)
+    line = {
+        "metric": "other ways to move the headline request's 288 MiB on the same GPU (context)",
+        "value": res["contiguous_d2d_copy_us"], "unit": "us", "n_gpus": 1, "steps": args.steps,
+        "warmup": 2, "higher_is_better": False, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "value": "contiguous D2D copy of the same bytes, us",
+                   "l2": "flushed before every timed step (write of 2x L2, outside the events)"},
+        "comparators": res,
+        "GBs": {k: (nb / (v * 1e-6) / 1e9 if isinstance(v, float) and k.endswith("_us") else None)
+                for k, v in res.items()},
+    }
+    print(json.dumps(line), flush=True)
 
 
 def run_formats(args):
@@ -917,6 +1027,9 @@ def main():
     if args.workload == "formats":
         run_formats(args)
         return
+    if args.workload == "comparators":
+        run_comparators(args)
+        return
     if int(args.workload) != 2:
         run_workload(args, int(args.workload))
         return
@@ -948,6 +1061,7 @@ def main():
                    "payload_bytes_each_way": N_TOK * P * R,
                    "alg_bytes_per_step": alg_bytes(N_TOK),
                    "us_per_request": ms_per_step * 1e3,
+                   "us_per_request_p10_median_p90": step_percentiles(res["step_ms"]),
                    "frac_of_measured_hbm": value / hbm,
                    "frac_of_nominal_8tbs": value / NOMINAL_HBM_GBS,
                    "plan_us": res["plan_ms"] * 1e3, "copy_us": res["copy_ms"] * 1e3,
@@ -959,6 +1073,8 @@ def main():
         "gpu_launches": 2 * K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": UNIT,
                      "frac": achieved / hbm, "traffic": profile_traffic(),
+                     "traffic_over_alg": (profile_traffic() / copy_bytes
+                                          if profile_traffic() else None),
                      "kernel": "copy_row_kernel (one warp per 2 KiB row)",
                      "peak_kind": f"{peak_kind} (burst copy)",
                      "achieved_bytes_per_launch": copy_bytes},
