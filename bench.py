@@ -74,6 +74,9 @@ def parse_args():
                          "tp: the headline request resharded between TP groups (kvx_move_heads); "
                          "formats: MLA, fp8, narrow rows and cross-kind transcoding; "
                          "comparators: other ways to move the headline bytes (context)")
+    ap.add_argument("--check-duplicates", action="store_true",
+                    help="kvx_set_check_duplicates(1) for this run (the planner also checks "
+                         "every destination slot for repeats)")
     ap.add_argument("--layer-us", type=float, default=100.0,
                     help="--workload stream: host cadence of the emulated producer, us/layer")
     return ap.parse_args()
@@ -1018,6 +1021,9 @@ def main():
     if args.fused_max is not None:
         from disaggregated_paged_kv_gb300 import kvx
         kvx.set_fused_max_tokens(args.fused_max)
+    if args.check_duplicates:
+        from disaggregated_paged_kv_gb300 import kvx
+        kvx.set_check_duplicates(True)
     if args.workload == "stream":
         run_stream(args)
         return
@@ -1067,6 +1073,7 @@ def main():
                    "plan_us": res["plan_ms"] * 1e3, "copy_us": res["copy_ms"] * 1e3,
                    "l2": "flushed before every timed step (write of 2x L2, outside the events)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
+                   "duplicate_check": bool(args.check_duplicates),
                    "device": res["device"]},
         "clocks": res["clocks"],
         "e2e": res["e2e"],

@@ -132,6 +132,7 @@ struct DeviceInfo {
 };
 
 std::atomic<int32_t> g_fused_max{0};  // measured: planner + row kernel is faster
+std::atomic<int32_t> g_check_dup{0};  // kvx_set_check_duplicates
 
 kvx_status device_info(DeviceInfo *out) {
   static std::mutex mu;
@@ -207,6 +208,16 @@ void set_whole_rows(Call &c) {
 int32_t call_chunk_rows(const Call &c) {
   return c.vec < 16 ? 1 : chunk_rows_for(c.row_bytes);
 }
+
+// Whether the planner checks this call's destination slots for repeats: slot-list calls into
+// a pool, with kvx_set_check_duplicates on.
+bool dup_check(const Call &c) {
+  return g_check_dup.load(std::memory_order_relaxed) != 0 && c.mode == kvx::kModeSlots &&
+         c.dst != nullptr && c.n_tokens > 0;
+}
+
+// The workspace a slot-list call needs (the duplicate table included when it is checked).
+kvx::WsLayout slots_ws(const Call &c) { return kvx::ws_layout(c.n_tokens, 0, false, dup_check(c)); }
 
 // Checks the layouts an op needs and fills call.src / call.dst / call.shape.
 kvx_status bind_layouts(Call &c, kvx_layout_t src, kvx_layout_t dst) {
@@ -299,8 +310,15 @@ kvx::PlanArgs plan_args(const Call &c, void *d_ws, int32_t *d_status) {
   a.has_src = c.src != nullptr;
   a.has_dst = c.dst != nullptr;
   a.ws = static_cast<char *>(d_ws);
-  a.L = kvx::ws_layout(c.n_tokens, c.n_segs, false);
+  a.L = kvx::ws_layout(c.n_tokens, c.n_segs, false, dup_check(c));
   a.status = d_status;
+  if (dup_check(c)) {
+    a.dup_table = reinterpret_cast<uint32_t *>(static_cast<char *>(d_ws) + a.L.dup_off);
+    a.dup_mask = (uint32_t)(a.L.dup_slots - 1);
+    int32_t bits = 0;
+    while (((int64_t)1 << bits) < a.L.dup_slots) ++bits;
+    a.dup_bits = bits;
+  }
   return a;
 }
 
@@ -309,6 +327,10 @@ kvx_status enqueue_plan(const Call &c, kvx::PlanArgs &a, cudaStream_t s) {
   if (c.n_tokens == 0) {
     e = cudaMemsetAsync(a.status, 0, sizeof(int32_t) * (size_t)c.n_status, s);
     return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+  }
+  if (a.dup_table) {  // an empty duplicate table
+    e = cudaMemsetAsync(a.dup_table, 0, sizeof(uint32_t) * ((size_t)a.dup_mask + 1), s);
+    if (e != cudaSuccess) return cuda_fail(e);
   }
   if (c.mode == kvx::kModeSlots) {
     if (kvx::num_tiles(c.n_tokens) == 1) {
@@ -497,7 +519,7 @@ int32_t kvx_layout_num_planes(kvx_layout_t l) { return l ? l->planes : -1; }
 
 size_t kvx_workspace_size(int64_t max_tokens, int32_t max_requests) {
   if (!valid_n(max_tokens) || max_requests < 0 || max_requests > kvx::kMaxSegs) return 0;
-  return (size_t)kvx::ws_layout(max_tokens, max_requests, true).total;
+  return (size_t)kvx::ws_layout(max_tokens, max_requests, true, true).total;
 }
 
 kvx_status kvx_plan(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, kvx_layout_t dst,
@@ -515,7 +537,7 @@ kvx_status kvx_plan(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, kv
     if (c.src && (!d_src_slots || !aligned(d_src_slots, 4))) return KVX_ERR_INVALID_ARG;
     if (c.dst && (!d_dst_slots || !aligned(d_dst_slots, 4))) return KVX_ERR_INVALID_ARG;
   }
-  const kvx::WsLayout L = kvx::ws_layout(n, 0, false);
+  const kvx::WsLayout L = slots_ws(c);
   if (n > 0 && (st = check_ws(d_ws, ws_bytes, L)) != KVX_OK) return st;
   kvx::PlanArgs a = plan_args(c, d_ws, d_status);
   a.src_idx = d_src_slots;
@@ -632,13 +654,14 @@ static kvx_status run_call(const Call &c, const int32_t *d_src_slots, const int3
     if (c.src && (!d_src_slots || !aligned(d_src_slots, 4))) return KVX_ERR_INVALID_ARG;
     if (c.dst && (!d_dst_slots || !aligned(d_dst_slots, 4))) return KVX_ERR_INVALID_ARG;
   }
-  const kvx::WsLayout L = kvx::ws_layout(n, 0, false);
+  const kvx::WsLayout L = slots_ws(c);
   kvx_status st;
   if (n > 0 && (st = check_ws(d_ws, ws_bytes, L)) != KVX_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // Requests of up to the fused limit with rows under KVX_CHUNK_BYTES take the one-launch
   // path; the rest take the planner + row kernel (the row kernel overlaps the planner).
-  const bool fused = call_chunk_rows(c) > 1 && n <= g_fused_max.load(std::memory_order_relaxed);
+  const bool fused = call_chunk_rows(c) > 1 && !dup_check(c) &&
+                     n <= g_fused_max.load(std::memory_order_relaxed);
   if (n == 0 || !fused) {
     kvx::PlanArgs a = plan_args(c, d_ws, d_status);
     a.src_idx = d_src_slots;
@@ -775,7 +798,7 @@ kvx_status kvx_submit(int32_t op, kvx_layout_t src, const int32_t *h_src_slots,
   if (st != KVX_OK) return st;
   if ((st = check_buffer(c, d_buf, buf_bytes)) != KVX_OK) return st;
   if (n > 0 && ((c.src && !h_src_slots) || (c.dst && !h_dst_slots))) return KVX_ERR_INVALID_ARG;
-  const kvx::WsLayout L = kvx::ws_layout(n, 0, true);
+  const kvx::WsLayout L = kvx::ws_layout(n, 0, true, dup_check(c));
   if ((st = check_ws(d_ws, ws_bytes, L)) != KVX_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char *stage = static_cast<char *>(d_ws) + L.stage_off;
@@ -866,7 +889,7 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
   if (n > 0) {
     if (c.src && (!d_src_slots || !aligned(d_src_slots, 4))) return KVX_ERR_INVALID_ARG;
     if (c.dst && (!d_dst_slots || !aligned(d_dst_slots, 4))) return KVX_ERR_INVALID_ARG;
-    if ((st = check_ws(d_ws, ws_bytes, kvx::ws_layout(n, 0, false))) != KVX_OK) return st;
+    if ((st = check_ws(d_ws, ws_bytes, slots_ws(c))) != KVX_OK) return st;
   }
   DeviceInfo di;
   if ((st = device_info(&di)) != KVX_OK) return st;
@@ -885,6 +908,10 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
     pa.dst_idx = d_dst_slots;
     pa.validate_only = 1;  // the streamed copy reads the slot lists itself
     if (direct) pa.status_direct = 4;
+    if (pa.dup_table) {
+      e = cudaMemsetAsync(pa.dup_table, 0, sizeof(uint32_t) * ((size_t)pa.dup_mask + 1), s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
     e = kvx::launch_plan(pa, s);
     if (e != cudaSuccess) return cuda_fail(e);
     // the mirror lives where a plan's chunk table would be (unused by a validate-only plan)
@@ -1034,6 +1061,14 @@ kvx_status kvx_set_fused_max_tokens(int32_t max_tokens) {
 }
 
 int32_t kvx_get_fused_max_tokens(void) { return g_fused_max.load(std::memory_order_relaxed); }
+
+kvx_status kvx_set_check_duplicates(int32_t on) {
+  if (on != 0 && on != 1) return KVX_ERR_INVALID_ARG;
+  g_check_dup.store(on, std::memory_order_relaxed);
+  return KVX_OK;
+}
+
+int32_t kvx_get_check_duplicates(void) { return g_check_dup.load(std::memory_order_relaxed); }
 
 int32_t kvx_version(void) { return 200; }
 

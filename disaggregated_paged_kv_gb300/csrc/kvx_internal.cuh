@@ -65,6 +65,8 @@ struct WsLayout {
   int64_t chunks_off;  // Chunk[n_tiles][kTile]
   int64_t prefix_off;  // int64[n_segs + 1]: token offset of each run / request
   int64_t stage_off;   // kvx_submit: int32 src[n], int32 dst[n], int32 status
+  int64_t dup_off;     // duplicate-destination check: uint32[dup_slots] hash table
+  int64_t dup_slots;   // power of two >= 2n
   int64_t total;       // bytes required
 };
 
@@ -74,7 +76,10 @@ __host__ __device__ inline int64_t num_tiles(int64_t n_tokens) {
   return (n_tokens + kTile - 1) / kTile;
 }
 
-__host__ __device__ inline WsLayout ws_layout(int64_t n_tokens, int64_t n_segs, bool staging) {
+// staging: kvx_submit's copies of host slot lists; dup: the duplicate-destination table
+// (after the staging area whether or not that is used, so every call agrees on its place).
+__host__ __device__ inline WsLayout ws_layout(int64_t n_tokens, int64_t n_segs, bool staging,
+                                              bool dup = false) {
   WsLayout L;
   int64_t tiles = num_tiles(n_tokens);
   L.header_off = 0;
@@ -82,7 +87,11 @@ __host__ __device__ inline WsLayout ws_layout(int64_t n_tokens, int64_t n_segs, 
   L.chunks_off = align_up(L.tiles_off + 4 * (tiles > 0 ? tiles : 1), 256);
   L.prefix_off = align_up(L.chunks_off + (int64_t)sizeof(Chunk) * kTile * tiles, 256);
   L.stage_off = align_up(L.prefix_off + 8 * (n_segs + 1), 256);
-  L.total = staging ? align_up(L.stage_off + 8 * n_tokens + 16, 256) : L.stage_off;
+  L.dup_off = align_up(L.stage_off + 8 * n_tokens + 16, 256);
+  L.dup_slots = 64;
+  while (L.dup_slots < 2 * n_tokens) L.dup_slots <<= 1;
+  if (dup) L.total = L.dup_off + 4 * L.dup_slots;
+  else L.total = staging ? L.dup_off : L.stage_off;
   return L;
 }
 
@@ -123,6 +132,11 @@ struct PlanArgs {
   int32_t status_direct;   // slots mode with a single tile: the CTA stores status[0] itself,
                            // and zeroes status[1 .. status_direct - 1]
   int32_t validate_only;   // check the indices and write the status only (kvx_stream)
+  // Duplicate-destination check (slots mode, destination pool): open-addressing table of
+  // dup_mask + 1 words in the workspace, zeroed before the planner; entry = slot + 1.
+  uint32_t *dup_table;     // nullptr: no check
+  uint32_t dup_mask;
+  int32_t dup_bits;        // log2 of the table size
   Side src, dst;           // batch: pool geometry of the two layouts (is_pool = 1)
   char *ws;
   WsLayout L;

@@ -145,6 +145,23 @@ __device__ __forceinline__ bool starts_run(const PlanArgs &a, const Tok &t, cons
   return false;
 }
 
+// Inserts a destination slot into the duplicate table; true if the slot was there already.
+// Entries only ever go from empty (0) to a slot, so a bucket changes under a thread at most
+// once; probes are bounded by the table size, and the table holds at most n < size entries.
+__device__ bool dup_insert(const PlanArgs &a, int32_t slot) {
+  const uint32_t tag = (uint32_t)slot + 1u;
+  uint32_t h = ((uint32_t)slot * 2654435761u) >> (32 - a.dup_bits);
+  for (uint32_t probe = 0; probe <= a.dup_mask; ++probe, h = (h + 1) & a.dup_mask) {
+    uint32_t cur = *reinterpret_cast<volatile uint32_t *>(a.dup_table + h);
+    if (cur == 0) {
+      cur = atomicCAS(a.dup_table + h, 0u, tag);
+      if (cur == 0) return false;  // claimed
+    }
+    if (cur == tag) return true;
+  }
+  return false;
+}
+
 __device__ __forceinline__ void write_header(const PlanArgs &a) {
   PlanHeader *h = reinterpret_cast<PlanHeader *>(a.ws + a.L.header_off);
   h->mode = a.mode;
@@ -226,6 +243,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
                  (a.dst.is_pool && (t.d < 0 || t.d >= a.dst.num_slots)))
                     ? KVX_ERR_OUT_OF_RANGE
                     : KVX_OK;
+        if (t.err == KVX_OK && a.dup_table && dup_insert(a, (int32_t)t.d))
+          t.err = KVX_ERR_DUPLICATE_DST;
         err = max(err, t.err);
         brk[k] = starts_run(a, t, prev, i == 0);
         prev = t;

@@ -141,6 +141,8 @@ _SIGS = {
     "kvx_get_copy_engine": (_I32, []),
     "kvx_set_fused_max_tokens": (_I32, [_I32]),
     "kvx_get_fused_max_tokens": (_I32, []),
+    "kvx_set_check_duplicates": (_I32, [_I32]),
+    "kvx_get_check_duplicates": (_I32, []),
 }
 
 
@@ -227,6 +229,14 @@ def set_fused_max_tokens(max_tokens: int) -> None:
 
 def get_fused_max_tokens() -> int:
     return int(lib().kvx_get_fused_max_tokens())
+
+
+def set_check_duplicates(on: bool) -> None:
+    _check(lib().kvx_set_check_duplicates(1 if on else 0), "kvx_set_check_duplicates")
+
+
+def get_check_duplicates() -> bool:
+    return bool(lib().kvx_get_check_duplicates())
 
 
 def workspace_size(max_tokens: int, max_requests: int = 0) -> int:

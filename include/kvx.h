@@ -74,7 +74,8 @@ typedef enum kvx_status {
   KVX_ERR_INVALID_ARG = 1,   /* bad size, null pointer, inconsistent layouts or request */
   KVX_ERR_ALIGNMENT = 2,     /* pointer or row size not 16-byte aligned */
   KVX_ERR_OUT_OF_RANGE = 3,  /* a slot / page index outside the pool (device status) */
-  KVX_ERR_DUPLICATE_DST = 4, /* reserved: a destination slot named twice */
+  KVX_ERR_DUPLICATE_DST = 4, /* a destination slot named twice (device status; only checked
+                                with kvx_set_check_duplicates(1)) */
   KVX_ERR_OVERLAP = 5,       /* source and destination memory overlap */
   KVX_ERR_CUDA = 6,          /* a CUDA runtime call failed; see kvx_last_cuda_error() */
   KVX_ERR_NO_WORKSPACE = 7,  /* workspace too small or misaligned */
@@ -418,6 +419,20 @@ KVX_API int32_t kvx_get_copy_engine(void);
 #define KVX_FUSED_MAX_TOKENS 8192
 KVX_API kvx_status kvx_set_fused_max_tokens(int32_t max_tokens);
 KVX_API int32_t kvx_get_fused_max_tokens(void);
+
+/* Duplicate-destination check (process-wide, off by default).  With 1, every slot-list call
+ * that writes into a pool (kvx_scatter, kvx_transfer, kvx_submit, kvx_stream,
+ * kvx_move_heads, kvx_plan for those ops) also makes the planner insert each destination slot
+ * into a hash table in the workspace; a slot named twice gives KVX_ERR_DUPLICATE_DST in the
+ * status and nothing moves.  (Without the check a repeated destination ends up holding one of
+ * its source rows, which one unspecified.)  The table needs the workspace kvx_workspace_size
+ * returns (4 bytes per slot of a power of two >= 2n, beyond the plan), and a memset per call;
+ * the one-launch fused path is not used while the check is on.  Run lists and batches are not
+ * checked, and kvx_transfer_noalloc's fixed scratch holds the table only for requests of up to
+ * about half its token limit (KVX_ERR_NO_WORKSPACE beyond that while the check is on).  A list with both a repeated and an
+ * out-of-range slot may report either error.  KVX_ERR_INVALID_ARG for values other than 0 / 1. */
+KVX_API kvx_status kvx_set_check_duplicates(int32_t on);
+KVX_API int32_t kvx_get_check_duplicates(void);
 
 KVX_API const char *kvx_status_str(kvx_status status);
 /* The cudaError_t of the last failing CUDA call made by this thread inside libkvx. */

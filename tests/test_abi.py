@@ -230,3 +230,12 @@ def test_stream_refuses_narrow_rows(lib):
     rc = kvx.lib().kvx_stream(kvx.OP_TRANSFER, src.handle, FAKE * 6, dst.handle, FAKE * 6, 10,
                               None, 0, ctypes.byref(c), FAKE * 4, 1 << 30, FAKE * 5, None)
     assert rc == kvx.ERR_ALIGNMENT
+
+
+def test_check_duplicates_switch(lib):
+    assert kvx.get_check_duplicates() is False
+    kvx.set_check_duplicates(True)
+    assert kvx.get_check_duplicates() is True
+    kvx.set_check_duplicates(False)
+    assert kvx.lib().kvx_set_check_duplicates(2) == kvx.ERR_INVALID_ARG
+    assert kvx.get_check_duplicates() is False
