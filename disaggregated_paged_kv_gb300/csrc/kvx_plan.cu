@@ -145,23 +145,6 @@ __device__ __forceinline__ bool starts_run(const PlanArgs &a, const Tok &t, cons
   return false;
 }
 
-// Inserts a destination slot into the duplicate table; true if the slot was there already.
-// Entries only ever go from empty (0) to a slot, so a bucket changes under a thread at most
-// once; probes are bounded by the table size, and the table holds at most n < size entries.
-__device__ bool dup_insert(const PlanArgs &a, int32_t slot) {
-  const uint32_t tag = (uint32_t)slot + 1u;
-  uint32_t h = ((uint32_t)slot * 2654435761u) >> (32 - a.dup_bits);
-  for (uint32_t probe = 0; probe <= a.dup_mask; ++probe, h = (h + 1) & a.dup_mask) {
-    uint32_t cur = *reinterpret_cast<volatile uint32_t *>(a.dup_table + h);
-    if (cur == 0) {
-      cur = atomicCAS(a.dup_table + h, 0u, tag);
-      if (cur == 0) return false;  // claimed
-    }
-    if (cur == tag) return true;
-  }
-  return false;
-}
-
 __device__ __forceinline__ void write_header(const PlanArgs &a) {
   PlanHeader *h = reinterpret_cast<PlanHeader *>(a.ws + a.L.header_off);
   h->mode = a.mode;
@@ -243,8 +226,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
                  (a.dst.is_pool && (t.d < 0 || t.d >= a.dst.num_slots)))
                     ? KVX_ERR_OUT_OF_RANGE
                     : KVX_OK;
-        if (t.err == KVX_OK && a.dup_table && dup_insert(a, (int32_t)t.d))
-          t.err = KVX_ERR_DUPLICATE_DST;
+
         err = max(err, t.err);
         brk[k] = starts_run(a, t, prev, i == 0);
         prev = t;
@@ -483,6 +465,39 @@ cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, void **args, cudaS
   return e;
 }
 
+// Duplicate-destination check (kvx_set_check_duplicates), behind the planner: one thread per
+// destination slot inserts it into an open-addressing table in the workspace (entry = slot + 1,
+// home bucket from a multiplicative hash, linear probing bounded by the table size; entries
+// only ever go from empty to a slot, and the table holds at most n < size of them).  Spread
+// over many CTAs because one SM keeps only a limited number of atomics in flight.  The inserts
+// go out before griddepcontrol.wait; the verdict is raised only once the planner, which writes
+// the status word, has finished.
+constexpr int kDupThreads = 128;
+
+__global__ void __launch_bounds__(kDupThreads) dup_kernel(const __grid_constant__ PlanArgs a) {
+  pdl_trigger();
+  const int64_t i = (int64_t)blockIdx.x * kDupThreads + threadIdx.x;
+  bool dup = false;
+  if (i < a.n_tokens) {
+    const int32_t slot = __ldg(a.dst_idx + i);
+    if (slot >= 0 && (int64_t)slot < a.dst.num_slots) {  // the planner reports the others
+      const uint32_t tag = (uint32_t)slot + 1u;
+      uint32_t h = ((uint32_t)slot * 2654435761u) >> (32 - a.dup_bits);
+      for (uint32_t probe = 0; probe <= a.dup_mask; ++probe, h = (h + 1) & a.dup_mask) {
+        const uint32_t cur = atomicCAS(a.dup_table + h, 0u, tag);
+        if (cur == 0) break;  // claimed
+        if (cur == tag) {
+          dup = true;
+          break;
+        }
+      }
+    }
+  }
+  dup = __syncthreads_or(dup);
+  pdl_wait();  // the planner's status words are written
+  if (dup && threadIdx.x == 0) atomicMax(&a.status[0], (int32_t)KVX_ERR_DUPLICATE_DST);
+}
+
 }  // namespace
 
 cudaError_t launch_prefix(const PlanArgs &a, cudaStream_t s) {
@@ -493,8 +508,12 @@ cudaError_t launch_prefix(const PlanArgs &a, cudaStream_t s) {
 
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s) {
   void *args[] = {const_cast<PlanArgs *>(&a)};
-  return launch_pdl(reinterpret_cast<const void *>(plan_kernel),
-                    dim3((unsigned)num_tiles(a.n_tokens)), dim3(kPlanThreads), args, s);
+  cudaError_t e = launch_pdl(reinterpret_cast<const void *>(plan_kernel),
+                             dim3((unsigned)num_tiles(a.n_tokens)), dim3(kPlanThreads), args, s);
+  if (e != cudaSuccess || !a.dup_table) return e;
+  const int64_t grid = (a.n_tokens + kDupThreads - 1) / kDupThreads;
+  return launch_pdl(reinterpret_cast<const void *>(dup_kernel), dim3((unsigned)grid),
+                    dim3(kDupThreads), args, s);
 }
 
 cudaError_t launch_export(const char *ws, WsLayout L, int64_t n_tokens, int32_t *out,
