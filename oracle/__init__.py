@@ -101,6 +101,9 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
                                   P(ctypes.c_int64)]
     lib.kvxo_transfer_layers.argtypes = [P(_Pool), i32p, P(_Pool), i32p, ctypes.c_int64,
                                          ctypes.c_int32, P(ctypes.c_int64)]
+    lib.kvxo_transfer_owned.argtypes = [P(_Pool), i32p, P(_Pool), i32p, ctypes.c_int64,
+                                        ctypes.c_int32, i32p, ctypes.c_int32, ctypes.c_int32,
+                                        P(ctypes.c_int64)]
     lib.kvxo_move_heads.argtypes = [ctypes.c_int32, P(_Pool), i32p, ctypes.c_int32, P(_Pool),
                                     i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, u8p,
                                     P(ctypes.c_int64)]
@@ -223,6 +226,20 @@ def transfer_layers(src: Pool, src_slots, dst: Pool, dst_slots, stop: int, lib=N
     s1, s2 = src._struct(), dst._struct()
     rc = lib.kvxo_transfer_layers(ctypes.byref(s1), _i32p(a), ctypes.byref(s2), _i32p(b), len(a),
                                   int(stop), ctypes.byref(written))
+    return rc, written.value
+
+
+def transfer_owned(src: Pool, src_slots, dst: Pool, dst_slots, stop: int, page_epochs,
+                   epoch_page: int, epoch: int, lib=None):
+    """kvxo_transfer_owned: rows of layers < stop whose destination page still holds epoch."""
+    lib = lib or load()
+    a, b, e = _i32(src_slots), _i32(dst_slots), _i32(page_epochs)
+    assert len(a) == len(b)
+    written = ctypes.c_int64(0)
+    s1, s2 = src._struct(), dst._struct()
+    rc = lib.kvxo_transfer_owned(ctypes.byref(s1), _i32p(a), ctypes.byref(s2), _i32p(b), len(a),
+                                 int(stop), _i32p(e), int(epoch_page), int(epoch),
+                                 ctypes.byref(written))
     return rc, written.value
 
 

@@ -170,6 +170,37 @@ int kvxo_transfer_layers(const kvxo_pool *src, const int32_t *src_slots, const k
   return KVXO_OK;
 }
 
+int kvxo_transfer_owned(const kvxo_pool *src, const int32_t *src_slots, const kvxo_pool *dst,
+                        const int32_t *dst_slots, int64_t n, int32_t stop,
+                        const int32_t *page_epochs, int32_t epoch_page, int32_t epoch,
+                        int64_t *bytes_written) {
+  /* [PD-budget] 最难的一个问题: once the receiver hands a page to another request, late data
+   * of the old request must not land in it.  Every destination page (epoch_page consecutive
+   * slots) carries the epoch of the request that owns it; a row is written only while its
+   * page still holds this request's epoch.  With the layer-streamed stop as in
+   * kvxo_transfer_layers. */
+  const int32_t ppl = planes_per_layer(src);
+  int64_t hb = head_bytes(src), rows = 0;
+  int rc;
+  if (!same_row_shape(src, dst) || stop < 0 || stop > src->num_layers || epoch_page < 1 ||
+      !page_epochs)
+    return KVXO_ERR_INVALID_ARG;
+  rc = kvxo_check_slots(src, src_slots, n);
+  if (rc == KVXO_OK) rc = kvxo_check_slots(dst, dst_slots, n);
+  if (rc != KVXO_OK) return rc;
+  for (int32_t layer = 0; layer < stop; ++layer)
+    for (int32_t kv = 0; kv < ppl; ++kv)
+      for (int64_t i = 0; i < n; ++i) {
+        if (page_epochs[dst_slots[i] / epoch_page] != epoch) continue; /* page reassigned */
+        for (int32_t h = 0; h < src->kv_heads; ++h)
+          memcpy(head_vec(dst, ppl * layer + kv, dst_slots[i], h),
+                 head_vec(src, ppl * layer + kv, src_slots[i], h), (size_t)hb);
+        ++rows;
+      }
+  if (bytes_written) *bytes_written = rows * kvxo_row_bytes(src);
+  return KVXO_OK;
+}
+
 int kvxo_move_heads(int32_t op, const kvxo_pool *src, const int32_t *src_slots,
                     int32_t src_head0, const kvxo_pool *dst, const int32_t *dst_slots,
                     int32_t dst_head0, int32_t n_heads, int64_t n, uint8_t *buf,

@@ -124,6 +124,14 @@ int kvxo_transfer_layers(const kvxo_pool *src, const int32_t *src_slots, const k
                          const int32_t *dst_slots, int64_t n, int32_t stop,
                          int64_t *bytes_written);
 
+/* kvxo_transfer_layers restricted to rows whose destination page is still owned by the
+ * request: page_epochs[slot / epoch_page] must equal epoch for row (slot) to be written.
+ * Bytes written: the rows written * R. */
+int kvxo_transfer_owned(const kvxo_pool *src, const int32_t *src_slots, const kvxo_pool *dst,
+                        const int32_t *dst_slots, int64_t n, int32_t stop,
+                        const int32_t *page_epochs, int32_t epoch_page, int32_t epoch,
+                        int64_t *bytes_written);
+
 /* Head-range move between pools whose kv_heads differ ([Mooncake] 7.7 异构TP).  op: 0 gather
  * (src -> buf [plane][n][n_heads][head_dim]), 1 scatter (buf -> dst), 2 transfer (src ->
  * dst).  For every plane and token i, heads src_head0 .. src_head0 + n_heads - 1 of source

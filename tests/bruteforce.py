@@ -138,6 +138,22 @@ def transfer_layers(src: BFPool, src_slots, dst: BFPool, dst_slots, stop: int) -
     return res
 
 
+def transfer_owned(src: BFPool, src_slots, dst: BFPool, dst_slots, stop: int, page_epochs,
+                   epoch_page: int, epoch: int) -> BFPool:
+    """transfer_layers() of the rows whose destination page still holds epoch."""
+    res = dst.copy()
+    for layer in range(stop):
+        for kv in range(src.kvp):
+            for i in range(len(src_slots)):
+                if page_epochs[int(dst_slots[i]) // epoch_page] != epoch:
+                    continue
+                for h in range(src.H):
+                    for d in range(src.D):
+                        res.set(layer, kv, int(dst_slots[i]), h, d,
+                                src.get(layer, kv, int(src_slots[i]), h, d))
+    return res
+
+
 def move_heads(op, src: BFPool, src_slots, h0, dst: BFPool, dst_slots, g0, nh, buf=None):
     """Head-range move, element by element.  op 0: returns the buffer [layer][kv][n][nh][D];
     op 1 (buffer -> dst) and op 2 (src -> dst): return the new destination pool."""

@@ -141,6 +141,39 @@ def pin_bruteforce_transfer_layers(lib):
             assert rc == oracle.ERR_INVALID_ARG and np.array_equal(dst.data, base.data)
 
 
+def pin_bruteforce_transfer_owned(lib):
+    """Rows whose destination page changed owner are never written: every owner pattern of a
+    4-slot pool in pages of 1 and 2 slots, every stop layer, every layout pair, n <= 2 maps;
+    every page owned gives the layer-range transfer, no page owned leaves the pool alone."""
+    layouts = (("planes", 1), ("slot_major", 1), ("hnd", 2))
+    R = H * D * 2
+    for (la, pa), (lb, pb) in itertools.product(layouts, layouts):
+        src = bf.make_pool(la, L, H, D, 4, _arange_fill(9), page_size=pa)
+        base = bf.make_pool(lb, L, H, D, 4, _sentinel_fill, page_size=pb)
+        for ep in (1, 2):
+            for owners in itertools.product((5, 6), repeat=4 // ep):
+                for n in (1, 2):
+                    s_, d_ = [2, 0][:n], [3, 1][:n]
+                    for stop in range(L + 1):
+                        want = bf.transfer_owned(src, s_, base, d_, stop, owners, ep, 5)
+                        dst = base.copy()
+                        rc, w = oracle.transfer_owned(bf.to_oracle(src), s_, bf.to_oracle(dst),
+                                                      d_, stop, list(owners), ep, 5, lib=lib)
+                        moved = sum(owners[x // ep] == 5 for x in d_)
+                        assert rc == oracle.OK and w == moved * 2 * stop * R
+                        assert np.array_equal(dst.data, want.data), (la, lb, ep, owners, stop)
+        full = base.copy()
+        oracle.transfer_layers(bf.to_oracle(src), [2, 0], bf.to_oracle(full), [3, 1], L, lib=lib)
+        dst = base.copy()
+        oracle.transfer_owned(bf.to_oracle(src), [2, 0], bf.to_oracle(dst), [3, 1], L, [5] * 4, 1, 5,
+                              lib=lib)
+        assert np.array_equal(dst.data, full.data)
+        dst = base.copy()
+        oracle.transfer_owned(bf.to_oracle(src), [2, 0], bf.to_oracle(dst), [3, 1], L, [6] * 4, 1, 5,
+                              lib=lib)
+        assert np.array_equal(dst.data, base.data)
+
+
 def pin_bruteforce_move_heads(lib):
     """Head-range gather / scatter / transfer between pools with different kv_heads, for every
     pair of layouts, every valid (src_head0, dst_head0, n_heads) and n <= 2; bad head ranges
@@ -523,7 +556,8 @@ def pin_plan(lib):
 
 
 ALL_PINS = [pin_sizes, pin_bytes_written, pin_bruteforce_gather, pin_bruteforce_scatter,
-            pin_bruteforce_transfer, pin_bruteforce_transfer_layers, pin_bruteforce_move_heads,
+            pin_bruteforce_transfer, pin_bruteforce_transfer_layers, pin_bruteforce_transfer_owned,
+            pin_bruteforce_move_heads,
             pin_move_heads_full_range_is_transfer, pin_tp_slice, pin_mla, pin_bruteforce_hnd,
             pin_roundtrip,
             pin_transfer_is_scatter_of_gather, pin_hnd_roundtrip, pin_plane_locality,

@@ -39,9 +39,10 @@ MUTANTS = {
     "plan_tile_break_dropped": ("if (i == 0 || i % tile_tokens == 0) brk[i] = 1;",
                                 "if (i == 0) brk[i] = 1;"),
     "batch_status_not_per_request": ("status[1 + q] = rc;", "status[1 + q] = 0;"),
-    "layers_one_short": ("for (int32_t layer = 0; layer < stop; ++layer)",
-                         "for (int32_t layer = 0; layer + 1 < stop; ++layer)"),
-    "layers_v_plane_dropped": ("    for (int32_t kv = 0; kv < ppl; ++kv)", "    for (int32_t kv = 0; kv < 1; ++kv)"),
+    "layers_one_short": ("for (int32_t layer = 0; layer < stop; ++layer)\n    for (int32_t kv = 0; kv < ppl; ++kv)\n      for (int64_t i = 0; i < n; ++i)\n        for",
+                         "for (int32_t layer = 0; layer + 1 < stop; ++layer)\n    for (int32_t kv = 0; kv < ppl; ++kv)\n      for (int64_t i = 0; i < n; ++i)\n        for"),
+    "layers_v_plane_dropped": ("    for (int32_t kv = 0; kv < ppl; ++kv)\n      for (int64_t i = 0; i < n; ++i)\n        for",
+                               "    for (int32_t kv = 0; kv < 1; ++kv)\n      for (int64_t i = 0; i < n; ++i)\n        for"),
     "tp_replicas_all_send": ("  if (p_tp > heads && p_rank % (p_tp / heads) != 0) return KVXO_OK; /* another replica sends */\n", ""),
     "tp_dst_offset_from_p_side": ("  *dst_head0 = lo - df;", "  *dst_head0 = lo - pf;"),
     "heads_dst_offset_ignored": ("        else\n          memcpy(head_vec(dst, p, dst_slots[i], dst_head0 + j),",
@@ -51,6 +52,9 @@ MUTANTS = {
     "mla_latent_plane_ignored": ("return pool->kv_planes == 1 ? 1 : 2;", "return 2;"),
     "mla_counted_as_k_and_v": ("return (int64_t)num_layers * (latent_dim + rope_dim) * elem_bytes;",
                                "return (int64_t)2 * num_layers * (latent_dim + rope_dim) * elem_bytes;"),
+    "owner_check_on_source_page": ("if (page_epochs[dst_slots[i] / epoch_page] != epoch) continue;",
+                                   "if (page_epochs[src_slots[i] / epoch_page] != epoch) continue;"),
+    "owner_check_dropped": ("if (page_epochs[dst_slots[i] / epoch_page] != epoch) continue;", ""),
     "transfer_src_dst_swapped": ("memcpy(head_vec(dst, p, dst_slots[i], h), head_vec(src, p, src_slots[i], h),",
                                  "memcpy(head_vec(src, p, src_slots[i], h), head_vec(dst, p, dst_slots[i], h),"),
 }
