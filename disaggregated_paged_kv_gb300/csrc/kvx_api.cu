@@ -860,7 +860,9 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
                       kvx_stream_t stream) {
   if (op < KVX_OP_GATHER || op > KVX_OP_TRANSFER || !valid_n(n)) return KVX_ERR_INVALID_ARG;
   if (!ctl || ctl->wait_ns < 1 || ctl->wait_ns > KVX_MAX_WAIT_NS || ctl->max_ctas < 0 ||
-      ctl->reserved != 0)
+      ctl->reserved != 0 || ctl->reserved2 != 0)
+    return KVX_ERR_INVALID_ARG;
+  if (ctl->dst_page_epochs && (op == KVX_OP_GATHER || ctl->epoch_page < 1))
     return KVX_ERR_INVALID_ARG;
   if (!d_status || !aligned(d_status, 16)) return KVX_ERR_INVALID_ARG;
   Call c;
@@ -877,7 +879,10 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
   k.epoch_word = static_cast<const int32_t *>(device_word(ctl->epoch_word, &epoch_local));
   k.words_local = (!ctl->layer_ready || ready_local) && (!ctl->epoch_word || epoch_local);
   k.host_done = static_cast<int32_t *>(const_cast<void *>(pinned_alias(ctl->host_done)));
-  if ((ctl->layer_ready && (!k.layer_ready || !aligned(ctl->layer_ready, 4))) ||
+  k.page_epochs = static_cast<const int32_t *>(device_word(ctl->dst_page_epochs));
+  k.epoch_page = ctl->epoch_page;
+  if ((ctl->dst_page_epochs && (!k.page_epochs || !aligned(ctl->dst_page_epochs, 4))) ||
+      (ctl->layer_ready && (!k.layer_ready || !aligned(ctl->layer_ready, 4))) ||
       (ctl->epoch_word && (!k.epoch_word || !aligned(ctl->epoch_word, 4))) ||
       (ctl->host_done && (!k.host_done || !aligned(ctl->host_done, 4))))
     return KVX_ERR_INVALID_ARG;
@@ -1070,6 +1075,6 @@ kvx_status kvx_set_check_duplicates(int32_t on) {
 
 int32_t kvx_get_check_duplicates(void) { return g_check_dup.load(std::memory_order_relaxed); }
 
-int32_t kvx_version(void) { return 200; }
+int32_t kvx_version(void) { return 201; }
 
 }  // extern "C"

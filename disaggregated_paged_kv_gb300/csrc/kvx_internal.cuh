@@ -193,12 +193,16 @@ struct StreamCtl {
   uint32_t groups;     // row groups of 1 << row_group_shift tokens per plane
   uint32_t per_layer;  // items per layer: kv_planes * groups
   uint32_t items;      // per_layer * layers (< 2^32 for every legal size)
+  uint32_t per_layer_pad;  // row grid: per_layer rounded up to whole CTAs
   uint32_t block;      // consecutive items a warp takes per block (see kvx_stream.cu)
   int32_t kv_planes;   // planes per layer: 2 (K, V) or 1 (MLA latent); plane = kv_planes*l + kv
   // The producer's words all live in this GPU's memory (or are absent): a direct read costs
   // what a mirror read costs, so the waits read them first and skip the mirror.
   int32_t words_local;
-  int32_t pad3;
+  // Owner epoch of every destination page (page = slot / epoch_page), or nullptr: a row is
+  // stored only while its page's word holds `epoch`.
+  int32_t epoch_page;
+  const int32_t *page_epochs;
 };
 
 // Launchers (enqueue only; return the launch's cudaError_t).

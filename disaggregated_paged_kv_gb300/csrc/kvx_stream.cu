@@ -11,10 +11,12 @@
 // l = i / (kv_planes * groups); with one latent plane per layer (MLA) there is no K/V split.
 // Two grids move them:
 //
-// Row grid (the default): one warp per item, one CTA per kWarps consecutive items, as the
-// row kernel of kvx_copy.cu.  Thread 0 of a CTA waits for the CTA's layer (usually one) while
-// its warps load their slot indices; the rows are loaded once the layer is ready, and stored
-// once the planner's verdict says every index is valid.  A CTA that gives up on a layer
+// Row grid (the default): one warp per item, one CTA per kWarps consecutive items of one
+// layer (each layer's items padded to whole CTAs), as the row kernel of kvx_copy.cu.  Thread 0
+// of a CTA waits for the CTA's layer while its warps load their slot indices; the rows are
+// loaded once the layer is ready, and stored once the planner's verdict says every index is
+// valid (and, with owner epochs, while the row's destination page still belongs to the
+// request).  A CTA that gives up on a layer
 // (the epoch word changed, or the wait ran past wait_ns) writes a tagged stop word into the
 // device-memory mirror, so every CTA that starts later stops at once instead of waiting its
 // own wait_ns again; CTAs below the stop layer still move their rows.  A one-thread epilogue
@@ -69,6 +71,11 @@ __device__ __forceinline__ int32_t ld_relaxed_sys(const int32_t *p) {
   int32_t v;
   asm volatile("ld.relaxed.sys.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+// Whether destination slot di still belongs to the request (its page's owner epoch).
+__device__ __forceinline__ bool page_owned(const StreamCtl &k, int32_t di) {
+  return ld_relaxed_sys(k.page_epochs + di / k.epoch_page) == k.epoch;
 }
 
 __device__ __forceinline__ void st_release_sys(int32_t *p, int32_t v) {
@@ -247,6 +254,12 @@ __global__ void __launch_bounds__(kCopyThreads, 6) stream_kernel(const __grid_co
         }
         verdict_ok = true;
       }
+      if (x0 == 0 && ok && dp && k.page_epochs && !page_owned(k, di)) {
+        // the page went to another request: the row is dropped and reported
+        ok = false;
+        atomicMax(&cs.code, (int32_t)KVX_ERR_CANCELLED);
+        atomicMax(&a.status[1], layers - l);
+      }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int32_t xv = x0 + li + (u << lsh);
@@ -342,48 +355,45 @@ __device__ int32_t row_wait(const StreamCtl &k, int32_t l, bool owner) {
 template <bool kSrcHnd, bool kDstHnd, bool kTail>
 __global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8)
     stream_row_kernel(const __grid_constant__ StreamArgs s) {
-  __shared__ int32_t s_stop;  // first layer this CTA does not move
+  __shared__ int32_t s_stop;  // 1: the CTA's layer moves, 0: it stopped
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the epilogue may queue
   const CopyArgs &a = s.c;
   const StreamCtl &k = s.k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t i0 = blockIdx.x * kWarps;  // the CTA's first item (< k.items)
-  const uint32_t i = i0 + warp;
+  // Each layer's items are padded to a multiple of kWarps, so the CTA's items all belong to
+  // one layer: a layer that is late never holds back rows of an earlier one.
+  const uint32_t i0 = blockIdx.x * kWarps;  // the CTA's first (padded) item
+  const int32_t l = (int32_t)(i0 / k.per_layer_pad);
+  const uint32_t r = i0 - (uint32_t)l * k.per_layer_pad + warp;
+  const bool has = r < k.per_layer;
+  const uint32_t rc = has ? r : 0;
   const int32_t gsh = a.row_group_shift, lsh = 5 - gsh;
-  const uint32_t ic = i < k.items ? i : i0;
-  const int32_t l = (int32_t)(ic / k.per_layer);
-  const uint32_t r = ic - (uint32_t)l * k.per_layer;
-  const int32_t kv = r >= k.groups ? 1 : 0;  // K or V (always 0 with one latent plane)
-  const int64_t t = ((int64_t)(r - kv * k.groups) << gsh) + (lane >> lsh);
+  const int32_t kv = rc >= k.groups ? 1 : 0;  // K or V (always 0 with one latent plane)
+  const int64_t t = ((int64_t)(rc - kv * k.groups) << gsh) + (lane >> lsh);
   const bool sp = a.src.is_pool != 0, dp = a.dst.is_pool != 0;
   // slot indices and their range checks go out before the wait
-  bool ok = i < k.items && t < a.n_tokens;
+  bool ok = has && t < a.n_tokens;
   const int64_t tt = ok ? t : 0;
   const int32_t si = sp ? a.spec_src[tt] : (int32_t)tt;
   const int32_t di = dp ? a.spec_dst[tt] : (int32_t)tt;
   ok = ok && (!sp || (si >= 0 && (int64_t)si < a.src.num_slots)) &&
        (!dp || (di >= 0 && (int64_t)di < a.dst.num_slots));
   if (threadIdx.x == 0) {
-    int32_t stop = 1 << 30;
+    int32_t go = 1;
     if (k.layer_ready || k.epoch_word) {
-      const uint32_t i1 = min(i0 + kWarps, k.items) - 1;
-      const int32_t l0 = (int32_t)(i0 / k.per_layer), l1 = (int32_t)(i1 / k.per_layer);
-      for (int32_t ll = l0; ll <= l1; ++ll) {
-        const uint32_t bs = (uint32_t)kWarps;
-        const bool owner = blockIdx.x == (uint32_t)(((uint64_t)ll * k.per_layer) / bs);
-        const int32_t code = row_wait(k, ll, owner);
-        if (code) {  // layers of this CTA below ll passed their wait: they still move
-          stop = ll;
-          atomicMax(&a.status[2], code);
-          atomicMax(&a.status[1], k.layers - stop);
-          break;
-        }
+      // the CTA holding the layer's first items polls the producer on every round
+      const bool owner = blockIdx.x == (uint32_t)((uint64_t)l * k.per_layer_pad / kWarps);
+      const int32_t code = row_wait(k, l, owner);
+      if (code) {
+        go = 0;
+        atomicMax(&a.status[2], code);
+        atomicMax(&a.status[1], k.layers - l);
       }
     }
-    s_stop = stop;
+    s_stop = go;
   }
   __syncthreads();  // thread 0's acquire of the layer orders every thread's row loads
-  if (l >= s_stop) ok = false;
+  if (!s_stop) ok = false;
   const int32_t p = k.kv_planes * l + kv;
   const int32_t R = a.row_bytes, vpr = R >> 4;
   const int32_t li = lane & ((1 << lsh) - 1);
@@ -398,6 +408,12 @@ __global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8)
   }
   pdl_wait();  // the planner has checked every index and written status[0]
   if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK || !ok) return;
+  if (dp && k.page_epochs && !page_owned(k, di)) {
+    // the page went to another request: the row is dropped and reported
+    atomicMax(&a.status[2], (int32_t)KVX_ERR_CANCELLED);
+    atomicMax(&a.status[1], k.layers - l);
+    return;
+  }
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u) {
     const int32_t xv = li + (u << lsh);
@@ -481,6 +497,7 @@ void stream_sizes(StreamCtl &k, int64_t n_tokens, int32_t group_shift) {
   k.groups = (uint32_t)groups;
   k.per_layer = (uint32_t)(k.kv_planes * groups);
   k.items = (uint32_t)(k.kv_planes * groups * k.layers);
+  k.per_layer_pad = (k.per_layer + kWarps - 1) / kWarps * kWarps;
 }
 
 cudaError_t launch_stream(const CopyArgs &c, const StreamCtl &k, int grid, cudaStream_t s) {
@@ -502,7 +519,7 @@ cudaError_t launch_stream_rows(const CopyArgs &c, const StreamCtl &k, cudaStream
   void *params[] = {&args};
   cudaError_t e = cudaSuccess;
   if (k.items > 0) {
-    e = launch_pdl_ex(fn, (k.items + kWarps - 1) / kWarps, kCopyThreads, params, s);
+    e = launch_pdl_ex(fn, k.per_layer_pad / kWarps * k.layers, kCopyThreads, params, s);
     if (e != cudaSuccess) return e;
   }
   int32_t *status = c.status, *done = k.host_done;

@@ -97,6 +97,9 @@ class StreamCtl(ctypes.Structure):
         ("max_ctas", ctypes.c_int32),
         ("reserved", ctypes.c_int32),
         ("host_done", ctypes.c_void_p),
+        ("dst_page_epochs", ctypes.c_void_p),
+        ("epoch_page", ctypes.c_int32),
+        ("reserved2", ctypes.c_int32),
     ]
 
 _lib: Optional[ctypes.CDLL] = None
@@ -430,7 +433,8 @@ def plan_export(ws, n_tokens: int, out, max_chunks: int, count, ws_bytes=None,
 def stream(op: int, src: Optional[Layout], src_slots, dst: Optional[Layout], dst_slots, n: int,
            buf, ws, status, layer_ready=None, ready_value: int = 1, epoch_word=None,
            epoch: int = 0, wait_ns: int = 100_000_000, max_ctas: int = 0, host_done=None,
-           buf_bytes=None, ws_bytes=None, stream=None) -> None:
+           dst_page_epochs=None, epoch_page: int = 1, buf_bytes=None, ws_bytes=None,
+           stream=None) -> None:
     """kvx_stream: a gather / scatter / transfer that moves layer l once
     ``layer_ready[l] >= ready_value`` and stops when ``epoch_word`` no longer holds ``epoch``
     or a layer's wait exceeds ``wait_ns``.  ``status`` is a device int32[4] (verdict, layers
@@ -444,6 +448,9 @@ def stream(op: int, src: Optional[Layout], src_slots, dst: Optional[Layout], dst
     ctl.max_ctas = max_ctas
     ctl.reserved = 0
     ctl.host_done = _any_ptr(host_done)
+    ctl.dst_page_epochs = _any_ptr(dst_page_epochs)
+    ctl.epoch_page = epoch_page if dst_page_epochs is not None else 0
+    ctl.reserved2 = 0
     rc = lib().kvx_stream(op, _h(src), _ptr(src_slots), _h(dst), _ptr(dst_slots), n, _ptr(buf),
                           _nbytes(buf) if buf_bytes is None else buf_bytes, ctypes.byref(ctl),
                           _ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,

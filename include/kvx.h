@@ -370,6 +370,15 @@ typedef struct kvx_stream_ctl {
   int32_t reserved;  /* must be 0 */
   /* Pinned host int32 or NULL: set to 1 when d_status[3] is (see kvx_stream). */
   int32_t *host_done;
+  /* int32[ceil(num_slots / epoch_page)] or NULL: the owner epoch of every destination page
+   * (page = slot / epoch_page).  A row is stored only while its page's word holds `epoch`;
+   * rows of pages the receiver has handed to another request are dropped and reported
+   * (KVX_ERR_CANCELLED), the rest of the request still moves ([PD-budget] "最难的一个问题":
+   * late data must not land in reassigned pages).  Needs a destination pool (not a gather).
+   * Device memory keeps the per-row check cheap; pinned host memory is read over the link. */
+  const int32_t *dst_page_epochs;
+  int32_t epoch_page; /* slots per epoch page, >= 1 when dst_page_epochs is set */
+  int32_t reserved2;  /* must be 0 */
 } kvx_stream_ctl;
 
 /* Gather / scatter / transfer of one request (op and arguments as kvx_gather / kvx_scatter /
@@ -378,10 +387,12 @@ typedef struct kvx_stream_ctl {
  *
  * d_status: device int32[4], written by the call (no initialisation needed):
  *   [0] KVX_OK, or the first error: KVX_ERR_OUT_OF_RANGE (nothing moved, as kvx_transfer),
- *       KVX_ERR_TIMEOUT or KVX_ERR_CANCELLED (the larger code if both happened).
+ *       KVX_ERR_TIMEOUT or KVX_ERR_CANCELLED (the larger code if both happened; CANCELLED
+ *       also when rows were dropped for pages that changed owner).
  *   [1] layers pending: the trailing layers not guaranteed moved.  Layers
  *       0 .. num_layers - [1] - 1 hold every row of the request; rows of later layers may or
- *       may not have been written.  0 when [0] is KVX_OK.
+ *       may not have been written (except rows dropped for a changed page owner, never
+ *       written once the change was seen).  0 when [0] is KVX_OK.
  *   [2] internal.
  *   [3] 1 once every CTA of the copy has finished and its writes are visible system-wide: no
  *       further write of this call can land ([PD-budget] "最难的一个问题": the sender may only

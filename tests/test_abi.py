@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_misc(lib):
-    assert kvx.version() == 200
+    assert kvx.version() == 201
     assert kvx.status_str(kvx.OK) == "ok"
     assert "range" in kvx.status_str(kvx.ERR_OUT_OF_RANGE)
     ws = kvx.workspace_size(2048, 0)
@@ -239,3 +239,20 @@ def test_check_duplicates_switch(lib):
     kvx.set_check_duplicates(False)
     assert kvx.lib().kvx_set_check_duplicates(2) == kvx.ERR_INVALID_ARG
     assert kvx.get_check_duplicates() is False
+
+
+def test_stream_page_epochs_validation(lib):
+    src = kvx.Layout(2, 2, 64, kvx.F16, 1000, base=FAKE, plane_stride=1000 * 256)
+    dst = kvx.Layout(2, 2, 64, kvx.F16, 1000, base=FAKE * 2, plane_stride=1000 * 256)
+    c = kvx.StreamCtl()
+    c.wait_ns = 1000
+    c.dst_page_epochs = FAKE * 8
+    c.epoch_page = 0  # page size missing
+    l = kvx.lib()
+    args = lambda op, s, d: (op, s and s.handle, FAKE * 6, d and d.handle, FAKE * 6, 10, FAKE * 7,
+                             10 * 4 * 256, ctypes.byref(c), FAKE * 4, 1 << 30, FAKE * 5, None)
+    assert l.kvx_stream(*args(kvx.OP_TRANSFER, src, dst)) == kvx.ERR_INVALID_ARG
+    c.epoch_page = 16
+    assert l.kvx_stream(*args(kvx.OP_GATHER, src, None)) == kvx.ERR_INVALID_ARG  # no destination pool
+    c.reserved2 = 1
+    assert l.kvx_stream(*args(kvx.OP_TRANSFER, src, dst)) == kvx.ERR_INVALID_ARG

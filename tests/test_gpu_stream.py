@@ -278,3 +278,79 @@ def test_stream_pageable_control_word_refused():
     with pytest.raises(kvx.KvxError) as e:
         _run_transfer(src, dst, s, d, n, _status(), layer_ready=ready)
     assert e.value.code == kvx.ERR_INVALID_ARG
+
+
+# ---- destination pages handed to another request (per-page owner epochs) -------------------
+
+EP = 8  # slots per epoch page
+
+
+def _owners(num_slots, taken, epoch=41, other=77):
+    """Owner epoch per destination page: `epoch`, except the pages in `taken`."""
+    e = np.full((num_slots + EP - 1) // EP, epoch, dtype=np.int32)
+    e[list(taken)] = other
+    return e
+
+
+def test_stream_pages_reassigned_before_launch(grid):
+    n = 1200
+    src, dst, s, d, _ = _transfer_case("planes", n, seed=240)
+    taken = sorted(set((d[[3, 500, 999, 1199]] // EP).tolist()))
+    owners = _owners(dst.num_slots, taken)
+    exp = _expected_pool("planes", dst.num_slots, 5)
+    rc, w = oracle.transfer_owned(hz.oracle_pool(src), s, hz.oracle_pool(exp), d, SH["L"], owners,
+                                  EP, 41)
+    dropped = int(np.isin(d // EP, taken).sum())
+    assert rc == oracle.OK and w == (n - dropped) * 2 * SH["L"] * src.R
+    st = _status()
+    _run_transfer(src, dst, s, d, n, st, dst_page_epochs=torch.from_numpy(owners).cuda(),
+                  epoch_page=EP, epoch=41, max_ctas=grid)
+    torch.cuda.synchronize()
+    v = st.cpu().tolist()
+    assert v[0] == kvx.ERR_CANCELLED and v[1] == SH["L"] and v[3] == 1, v
+    hz.assert_same_bytes(dst.readback(), exp.host, "rows of reassigned pages dropped")
+
+
+def test_stream_pages_reassigned_while_waiting(grid):
+    """Layers below k are raised; while the kernel waits for layer k the receiver hands some
+    destination pages to another request (pinned host owner words), then the producer raises the
+    rest: rows of layers < k are all written, rows of later layers only into owned pages."""
+    n, k = 1000, 3
+    src, dst, s, d, _ = _transfer_case("planes", n, seed=260)
+    taken = sorted(set((d[[0, 17, 640, 999]] // EP).tolist()))
+    owners = torch.from_numpy(_owners(dst.num_slots, [])).pin_memory()
+    ready = _pinned_i32([1 if l < k else 0 for l in range(SH["L"])])
+    done = _pinned_i32([0])
+    st = _status()
+    ws, sd, dd = hz.workspace(n), hz.dev_i32(s), hz.dev_i32(d)
+    torch.cuda.synchronize()
+    kvx.stream(kvx.OP_TRANSFER, hz.kvx_layout(src), sd, hz.kvx_layout(dst), dd, n, None, ws, st,
+               layer_ready=ready, ready_value=1, epoch=41, dst_page_epochs=owners, epoch_page=EP,
+               wait_ns=5_000_000_000, host_done=done, max_ctas=grid, buf_bytes=0)
+    time.sleep(0.05)
+    assert int(done[0]) == 0  # still waiting for layer k
+    for pg in taken:
+        owners[pg] = 77
+    for layer in range(k, SH["L"]):
+        ready[layer] = 1
+    torch.cuda.synchronize()
+    v = st.cpu().tolist()
+    assert v[0] == kvx.ERR_CANCELLED and v[1] == SH["L"] - k and v[3] == 1, v
+    exp = _expected_pool("planes", dst.num_slots, 5)
+    assert oracle.transfer_owned(hz.oracle_pool(src), s, hz.oracle_pool(exp), d, SH["L"],
+                                 owners.numpy(), EP, 41)[0] == oracle.OK
+    assert oracle.transfer_layers(hz.oracle_pool(src), s, hz.oracle_pool(exp), d, k)[0] == oracle.OK
+    hz.assert_same_bytes(dst.readback(), exp.host, "late rows of reassigned pages dropped")
+
+
+def test_stream_all_pages_owned_moves_everything(grid):
+    n = 700
+    src, dst, s, d, exp = _transfer_case("hnd", n, seed=280)
+    owners = torch.from_numpy(_owners(dst.num_slots, [])).cuda()
+    st = _status()
+    _run_transfer(src, dst, s, d, n, st, dst_page_epochs=owners, epoch_page=EP, epoch=41,
+                  max_ctas=grid)
+    torch.cuda.synchronize()
+    v = st.cpu().tolist()
+    assert v[0] == kvx.OK and v[1] == 0 and v[3] == 1, v
+    hz.assert_same_bytes(dst.readback(), exp.host, "every page owned")
