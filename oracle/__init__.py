@@ -73,6 +73,13 @@ class Chunk(ctypes.Structure):
                 ("rows", ctypes.c_int32)]
 
 
+class Part(ctypes.Structure):
+    """kvxo_part: heads [src_head0, src_head0 + n_heads) of srcs[src] -> heads from dst_head0
+    of dsts[dst]."""
+    _fields_ = [("src", ctypes.c_int32), ("dst", ctypes.c_int32), ("src_head0", ctypes.c_int32),
+                ("dst_head0", ctypes.c_int32), ("n_heads", ctypes.c_int32)]
+
+
 _lib_cache = {}
 
 
@@ -108,6 +115,9 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
                                     i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, u8p,
                                     P(ctypes.c_int64)]
     lib.kvxo_tp_slice.argtypes = [ctypes.c_int32] * 5 + [P(ctypes.c_int32)] * 3
+    lib.kvxo_reshard.argtypes = [P(P(_Pool)), ctypes.c_int32, i32p, P(P(_Pool)), ctypes.c_int32,
+                                 i32p, P(Part), ctypes.c_int32, ctypes.c_int64,
+                                 P(ctypes.c_int64)]
     lib.kvxo_hnd_gather.argtypes = [P(_Pool), i32p, ctypes.c_int64, u8p]
     lib.kvxo_hnd_rebuild.argtypes = [P(_Pool), i32p, ctypes.c_int64, u8p]
     lib.kvxo_batch.argtypes = [P(_Pool), P(_Pool), P(Request), ctypes.c_int32, i32p,
@@ -264,6 +274,24 @@ def move_heads(op: int, src: Optional[Pool], src_slots, src_head0: int, dst: Opt
                              dst_head0, n_heads, n, bp.ctypes.data if bp is not None else None,
                              ctypes.byref(written))
     return rc, (bp if op == 0 else None), written.value
+
+
+def reshard(srcs: Sequence[Optional[Pool]], src_slots, dsts: Sequence[Optional[Pool]], dst_slots,
+            parts, n: int, lib=None):
+    """kvxo_reshard.  parts: sequence of (src, dst, src_head0, dst_head0, n_heads).  The
+    destination pools are written in place.  Returns (status, bytes written)."""
+    lib = lib or load()
+    a = _i32(src_slots if src_slots is not None else [])
+    b = _i32(dst_slots if dst_slots is not None else [])
+    keep = [p._struct() if p is not None else None for p in list(srcs) + list(dsts)]
+    ptr = lambda s: ctypes.pointer(s) if s is not None else ctypes.POINTER(_Pool)()
+    sa = (ctypes.POINTER(_Pool) * max(1, len(srcs)))(*[ptr(s) for s in keep[:len(srcs)]])
+    da = (ctypes.POINTER(_Pool) * max(1, len(dsts)))(*[ptr(s) for s in keep[len(srcs):]])
+    pa = (Part * max(1, len(parts)))(*[Part(*map(int, q)) for q in parts])
+    written = ctypes.c_int64(0)
+    rc = lib.kvxo_reshard(sa, len(srcs), _i32p(a), da, len(dsts), _i32p(b), pa, len(parts), n,
+                          ctypes.byref(written))
+    return rc, written.value
 
 
 def tp_slice(heads: int, p_tp: int, p_rank: int, d_tp: int, d_rank: int, lib=None):

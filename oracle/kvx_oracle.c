@@ -242,6 +242,55 @@ int kvxo_move_heads(int32_t op, const kvxo_pool *src, const int32_t *src_slots,
   return KVXO_OK;
 }
 
+/* Same planes and head vectors (kv_heads may differ): what a head-range transfer between a
+ * and b needs. */
+static int same_geometry(const kvxo_pool *a, const kvxo_pool *b) {
+  return a->num_layers == b->num_layers && a->head_dim == b->head_dim &&
+         a->elem_bytes == b->elem_bytes && planes_per_layer(a) == planes_per_layer(b);
+}
+
+int kvxo_reshard(const kvxo_pool *const *srcs, int32_t n_srcs, const int32_t *src_slots,
+                 const kvxo_pool *const *dsts, int32_t n_dsts, const int32_t *dst_slots,
+                 const kvxo_part *parts, int32_t n_parts, int64_t n, int64_t *bytes_written) {
+  /* [Mooncake] 7.7 异构TP: when the two tensor-parallel sizes differ, a D rank assembles its
+   * shard from pieces of several P ranks (or a P rank's shard goes out in pieces to several
+   * D ranks).  Each piece is one head-range transfer; a reshard is all of them. */
+  int64_t total = 0, w;
+  int rc;
+  if (n_srcs < 1 || n_dsts < 1 || n_parts < 1 || !srcs || !dsts || !parts)
+    return KVXO_ERR_INVALID_ARG;
+  for (int32_t k = 0; k < n_srcs; ++k)
+    if (!srcs[k] || !same_geometry(srcs[k], srcs[0])) return KVXO_ERR_INVALID_ARG;
+  for (int32_t k = 0; k < n_dsts; ++k)
+    if (!dsts[k] || !same_geometry(dsts[k], srcs[0])) return KVXO_ERR_INVALID_ARG;
+  for (int32_t k = 0; k < n_parts; ++k) {
+    const kvxo_part *q = &parts[k];
+    if (q->src < 0 || q->src >= n_srcs || q->dst < 0 || q->dst >= n_dsts || q->n_heads < 1)
+      return KVXO_ERR_INVALID_ARG;
+    if (q->src_head0 < 0 || q->src_head0 + q->n_heads > srcs[q->src]->kv_heads)
+      return KVXO_ERR_INVALID_ARG;
+    if (q->dst_head0 < 0 || q->dst_head0 + q->n_heads > dsts[q->dst]->kv_heads)
+      return KVXO_ERR_INVALID_ARG;
+    for (int32_t m = 0; m < k; ++m) /* one writer per destination head */
+      if (parts[m].dst == q->dst && parts[m].dst_head0 < q->dst_head0 + q->n_heads &&
+          q->dst_head0 < parts[m].dst_head0 + parts[m].n_heads)
+        return KVXO_ERR_INVALID_ARG;
+  }
+  for (int32_t k = 0; k < n_srcs; ++k)
+    if ((rc = kvxo_check_slots(srcs[k], src_slots, n)) != KVXO_OK) return rc;
+  for (int32_t k = 0; k < n_dsts; ++k)
+    if ((rc = kvxo_check_slots(dsts[k], dst_slots, n)) != KVXO_OK) return rc;
+  for (int32_t k = 0; k < n_parts; ++k) {
+    const kvxo_part *q = &parts[k];
+    rc = kvxo_move_heads(2, srcs[q->src], src_slots, q->src_head0, dsts[q->dst], dst_slots,
+                         q->dst_head0, q->n_heads, n, NULL, &w);
+    if (rc != KVXO_OK) return rc; /* not reached: every check above has passed */
+    total += w;
+  }
+  if (bytes_written) *bytes_written = total;
+  return KVXO_OK;
+}
+
 /* Heads [*first, *first + *count) held by rank r of a tensor-parallel group of size t. */
 static int tp_heads(int32_t heads, int32_t t, int32_t r, int32_t *first, int32_t *count) {
   if (heads < 1 || t < 1 || r < 0 || r >= t) return KVXO_ERR_INVALID_ARG;

@@ -143,6 +143,32 @@ int kvxo_move_heads(int32_t op, const kvxo_pool *src, const int32_t *src_slots,
                     int32_t dst_head0, int32_t n_heads, int64_t n, uint8_t *buf,
                     int64_t *bytes_written);
 
+/* One part of a reshard: heads src_head0 .. src_head0 + n_heads - 1 of source pool `src`
+ * go to heads dst_head0 .. dst_head0 + n_heads - 1 of destination pool `dst` (indices into
+ * the srcs / dsts arrays of kvxo_reshard). */
+typedef struct kvxo_part {
+  int32_t src;
+  int32_t dst;
+  int32_t src_head0;
+  int32_t dst_head0;
+  int32_t n_heads;
+} kvxo_part;
+
+/* A whole reshard between two tensor-parallel groups ([Mooncake] 7.7 异构TP: one D rank may
+ * merge the shards of several P ranks; one P rank's shard may be split over several D ranks).
+ * Every part is a head-range transfer (kvxo_move_heads, op 2) from srcs[part.src] to
+ * dsts[part.dst] with the one source slot list and the one destination slot list (the ranks
+ * of one instance share its block table).  The result is that of the parts' transfers done
+ * one after another; no two parts may write the same head of the same destination pool, so
+ * their order does not matter.  Every pool listed shares num_layers, kv_planes, head_dim
+ * and elem_bytes, and every slot is checked against every pool of its side.  Errors:
+ * KVXO_ERR_INVALID_ARG (no part, a pool index or head range outside its pool, differing
+ * geometry, two parts writing one destination head), then KVXO_ERR_OUT_OF_RANGE; nothing
+ * written on error.  Bytes written: the sum over parts of n * P * n_heads * head bytes. */
+int kvxo_reshard(const kvxo_pool *const *srcs, int32_t n_srcs, const int32_t *src_slots,
+                 const kvxo_pool *const *dsts, int32_t n_dsts, const int32_t *dst_slots,
+                 const kvxo_part *parts, int32_t n_parts, int64_t n, int64_t *bytes_written);
+
 /* The transfer plan between P rank p_rank of a tensor-parallel group of size p_tp and D rank
  * d_rank of a group of size d_tp, for a model with `heads` kv heads ([Mooncake] 7.7 异构TP).
  * Rank r of a group of size t holds heads [r*heads/t, (r+1)*heads/t) (t <= heads, t divides

@@ -178,6 +178,22 @@ def move_heads(op, src: BFPool, src_slots, h0, dst: BFPool, dst_slots, g0, nh, b
     return out
 
 
+def reshard(srcs, src_slots, dsts, dst_slots, parts):
+    """Every part (src, dst, h0, g0, nh) as its own element-by-element head transfer into a
+    copy of its destination pool; returns the new destination pools."""
+    out = [d.copy() for d in dsts]
+    for si, di, h0, g0, nh in parts:
+        src, res = srcs[si], out[di]
+        for layer in range(src.L):
+            for kv in range(src.kvp):
+                for i in range(len(src_slots)):
+                    for j in range(nh):
+                        for d in range(src.D):
+                            res.set(layer, kv, int(dst_slots[i]), g0 + j, d,
+                                    src.get(layer, kv, int(src_slots[i]), h0 + j, d))
+    return out
+
+
 def hnd_gather(pool: BFPool, page_table, seq_len) -> np.ndarray:
     """[layer][kv][s][h][d] = element (h, s, d) of the page-table view."""
     out = np.zeros((pool.L, pool.kvp, seq_len, pool.H, pool.D), np.uint16)

@@ -269,6 +269,106 @@ def pin_tp_slice(lib):
         assert oracle.tp_slice(*bad, lib=lib)[0] == oracle.ERR_INVALID_ARG
 
 
+def _tp_parts(heads, p_tp, d_tp, lib):
+    """(pr, dr, h0, g0, nh) for every pair the oracle's tp_slice plan connects."""
+    parts = []
+    for dr in range(d_tp):
+        for pr in range(p_tp):
+            rc, h0, g0, nh = oracle.tp_slice(heads, p_tp, pr, d_tp, dr, lib=lib)
+            assert rc == oracle.OK
+            if nh:
+                parts.append((pr, dr, h0, g0, nh))
+    return parts
+
+
+def pin_bruteforce_reshard(lib):
+    """A whole TP reshard in one call against the element-by-element model of its parts, for
+    merges (4 -> 2, 2 -> 1), splits (1 -> 2, 2 -> 4), replicated heads (2 -> 4 with 2 heads)
+    and layout pairs; then the refusals: two parts writing one destination head, a part
+    naming no pool, a head range past a pool, and a slot valid in one pool of a side but not
+    in another -- each with nothing written."""
+    heads = 4
+    layouts = (("planes", 1), ("hnd", 2), ("slot_major", 1))
+    for (la, pa), (lb, pb) in itertools.product(layouts, layouts):
+        for p_tp, d_tp, hh in ((4, 2, 4), (2, 1, 4), (1, 2, 4), (2, 4, 4), (2, 4, 2)):
+            parts = _tp_parts(hh, p_tp, d_tp, lib)
+            srcs = [bf.make_pool(la, L, max(1, hh // p_tp), D, 4, _arange_fill(11 + r),
+                                 page_size=pa) for r in range(p_tp)]
+            base = [bf.make_pool(lb, L, max(1, hh // d_tp), D, 4, _sentinel_fill, page_size=pb)
+                    for _ in range(d_tp)]
+            for s_, d_ in (([3], [1]), ([3, 0], [1, 2]), ([], [])):
+                want = bf.reshard(srcs, s_, base, d_, parts)
+                got = [b.copy() for b in base]
+                rc, w = oracle.reshard([bf.to_oracle(x) for x in srcs], s_,
+                                       [bf.to_oracle(x) for x in got], d_, parts, len(s_), lib=lib)
+                assert rc == oracle.OK, (la, lb, p_tp, d_tp)
+                assert w == sum(len(s_) * 2 * L * q[4] * D * 2 for q in parts)
+                for g, e in zip(got, want):
+                    assert np.array_equal(g.data, e.data), (la, lb, p_tp, d_tp, hh, s_)
+    srcs = [bf.make_pool("planes", L, 2, D, 4, _arange_fill(3 + r)) for r in range(2)]
+    small = bf.make_pool("planes", L, 2, D, 3, _sentinel_fill)
+    base = [bf.make_pool("hnd", L, 4, D, 4, _sentinel_fill, page_size=2) for _ in range(2)]
+    bad = {
+        "one head written twice": ([(0, 0, 0, 0, 2), (1, 0, 1, 1, 1)], base),
+        "no such source": ([(2, 0, 0, 0, 1)], base),
+        "no such destination": ([(0, 2, 0, 0, 1)], base),
+        "head past the source": ([(0, 0, 1, 0, 2)], base),
+        "head past the destination": ([(0, 1, 0, 3, 2)], base),
+        "no heads": ([(0, 0, 0, 0, 0)], base),
+        "no parts": ([], base),
+    }
+    for name, (parts, dsts) in bad.items():
+        got = [b.copy() for b in dsts]
+        rc, _ = oracle.reshard([bf.to_oracle(x) for x in srcs], [1], [bf.to_oracle(x) for x in got],
+                               [0], parts, 1, lib=lib)
+        assert rc == oracle.ERR_INVALID_ARG, name
+        assert all(np.array_equal(g.data, b.data) for g, b in zip(got, dsts)), name
+    # slot 3 is valid in the first destination pool, not in the second (3 slots): refused,
+    # although only the first pool is written by the part
+    got = [base[0].copy(), small.copy()]
+    rc, _ = oracle.reshard([bf.to_oracle(x) for x in srcs], [0, 1],
+                           [bf.to_oracle(x) for x in got], [0, 3], [(0, 0, 0, 0, 2)], 2, lib=lib)
+    assert rc == oracle.ERR_OUT_OF_RANGE
+    assert np.array_equal(got[0].data, base[0].data) and np.array_equal(got[1].data, small.data)
+    got = [b.copy() for b in base]
+    rc, _ = oracle.reshard([bf.to_oracle(srcs[0]), bf.to_oracle(small)], [3, 0],
+                           [bf.to_oracle(x) for x in got], [0, 1], [(0, 0, 0, 0, 2)], 2, lib=lib)
+    assert rc == oracle.ERR_OUT_OF_RANGE
+    assert all(np.array_equal(g.data, b.data) for g, b in zip(got, base))
+
+
+def pin_reshard_reassembles_model(lib):
+    """What a reshard must achieve, stated without parts: a model's KV (8 kv heads) split by
+    heads over the pools of a P TP group and resharded with the tp_slice plan leaves in every
+    D rank's pool, at each destination slot, exactly that rank's heads of the model's rows at
+    the matching source slot (numpy slicing of the whole-model pool, replicated heads
+    included); every other slot keeps its bytes."""
+    heads, L2, D2, ns = 8, 2, 4, 6
+    full = np.arange(2 * L2 * ns * heads * D2, dtype=np.uint16).reshape(2 * L2, ns, heads, D2)
+    full = (full * 7 + 3).astype(np.uint16)
+    s_, d_ = [5, 0, 2], [1, 4, 3]
+
+    def shard(t, r):  # heads of rank r in a group of size t
+        if t <= heads:
+            return list(range(r * heads // t, (r + 1) * heads // t))
+        return [r // (t // heads)]
+
+    for p_tp, d_tp in ((1, 8), (8, 1), (2, 4), (4, 2), (16, 2), (2, 16), (8, 8), (1, 1)):
+        srcs = [bf.BFPool("planes", L2, len(shard(p_tp, r)), D2, ns,
+                          np.ascontiguousarray(full[:, :, shard(p_tp, r)])) for r in range(p_tp)]
+        dsts = [bf.make_pool("planes", L2, len(shard(d_tp, r)), D2, ns, _sentinel_fill)
+                for r in range(d_tp)]
+        before = [x.data.copy() for x in dsts]
+        parts = _tp_parts(heads, p_tp, d_tp, lib)
+        rc, _ = oracle.reshard([bf.to_oracle(x) for x in srcs], s_, [bf.to_oracle(x) for x in dsts],
+                               d_, parts, len(s_), lib=lib)
+        assert rc == oracle.OK
+        for r, x in enumerate(dsts):
+            want = before[r].copy()
+            want[:, d_] = full[:, s_][:, :, shard(d_tp, r)]
+            assert np.array_equal(x.data, want), (p_tp, d_tp, r)
+
+
 def pin_mla(lib):
     """One latent plane per layer (MLA).  Sizes from the pages' table ([mini-infer] KV 传输大小):
     DeepSeek-V2-Lite (27 layers, latent 512 + rope 64, 2-byte elements) 3.80 MB at 128 tokens
@@ -557,7 +657,7 @@ def pin_plan(lib):
 
 ALL_PINS = [pin_sizes, pin_bytes_written, pin_bruteforce_gather, pin_bruteforce_scatter,
             pin_bruteforce_transfer, pin_bruteforce_transfer_layers, pin_bruteforce_transfer_owned,
-            pin_bruteforce_move_heads,
+            pin_bruteforce_move_heads, pin_bruteforce_reshard, pin_reshard_reassembles_model,
             pin_move_heads_full_range_is_transfer, pin_tp_slice, pin_mla, pin_bruteforce_hnd,
             pin_roundtrip,
             pin_transfer_is_scatter_of_gather, pin_hnd_roundtrip, pin_plane_locality,

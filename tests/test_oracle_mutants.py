@@ -55,6 +55,14 @@ MUTANTS = {
     "owner_check_on_source_page": ("if (page_epochs[dst_slots[i] / epoch_page] != epoch) continue;",
                                    "if (page_epochs[src_slots[i] / epoch_page] != epoch) continue;"),
     "owner_check_dropped": ("if (page_epochs[dst_slots[i] / epoch_page] != epoch) continue;", ""),
+    "reshard_adjacent_parts_refused": ("q->dst_head0 < parts[m].dst_head0 + parts[m].n_heads)",
+                                       "q->dst_head0 <= parts[m].dst_head0 + parts[m].n_heads)"),
+    "reshard_one_writer_check_dropped": ("for (int32_t m = 0; m < k; ++m) /* one writer",
+                                         "for (int32_t m = 0; m < 0; ++m) /* one writer"),
+    "reshard_first_dst_pool_checked_only": ("for (int32_t k = 0; k < n_dsts; ++k)\n    if ((rc = kvxo_check_slots(dsts[k]",
+                                            "for (int32_t k = 0; k < 1; ++k)\n    if ((rc = kvxo_check_slots(dsts[k]"),
+    "reshard_head_offsets_swapped": ("src_slots, q->src_head0, dsts[q->dst], dst_slots,\n                         q->dst_head0,",
+                                     "src_slots, q->dst_head0, dsts[q->dst], dst_slots,\n                         q->src_head0,"),
     "transfer_src_dst_swapped": ("memcpy(head_vec(dst, p, dst_slots[i], h), head_vec(src, p, src_slots[i], h),",
                                  "memcpy(head_vec(src, p, src_slots[i], h), head_vec(dst, p, dst_slots[i], h),"),
 }
