@@ -13,6 +13,7 @@
 #include <new>
 
 #include "kvx_internal.cuh"
+#include "kvx_reshard.cuh"
 
 struct kvx_layout {
   int32_t num_layers, kv_heads, head_dim, elem, kind, page_size;
@@ -1028,6 +1029,157 @@ kvx_status kvx_move_heads(int32_t op, kvx_layout_t src, const int32_t *d_src_slo
   return run_call(c, d_src_slots, d_dst_slots, d_buf, d_ws, ws_bytes, d_status, stream);
 }
 
+kvx_status kvx_tp_plan(int32_t kv_heads, int32_t src_tp, int32_t dst_tp, kvx_head_part *parts,
+                       int32_t max_parts, int32_t *n_parts) {
+  if (!n_parts || max_parts < 0 || (max_parts > 0 && !parts)) return KVX_ERR_INVALID_ARG;
+  if (src_tp < 1 || dst_tp < 1 || src_tp > 1024 || dst_tp > 1024) return KVX_ERR_INVALID_ARG;
+  int32_t count = 0;
+  for (int32_t dr = 0; dr < dst_tp; ++dr)
+    for (int32_t sr = 0; sr < src_tp; ++sr) {
+      int32_t h0 = 0, g0 = 0, nh = 0;
+      const kvx_status st = kvx_tp_slice(kv_heads, src_tp, sr, dst_tp, dr, &h0, &g0, &nh);
+      if (st != KVX_OK) return st;
+      if (nh == 0) continue;
+      if (count < max_parts) parts[count] = kvx_head_part{sr, dr, h0, g0, nh, 0};
+      ++count;
+    }
+  *n_parts = count;
+  return count > max_parts ? KVX_ERR_INVALID_ARG : KVX_OK;
+}
+
+// The same pool apart from its plane addresses: the ranks of one tensor-parallel group.
+static bool same_pool(const kvx_layout *a, const kvx_layout *b) {
+  return same_rows(a, b) && a->kind == b->kind && a->page_size == b->page_size &&
+         a->num_slots == b->num_slots && a->slot_stride == b->slot_stride &&
+         a->page_bytes == b->page_bytes;
+}
+
+// Layout l of a reshard in device terms: first plane and stride, or (planes not evenly
+// spaced) a run of the call's plane table.  False if the table is full.
+static bool reshard_layout(kvx::ReshardCall &rc, int32_t idx, const kvx_layout *l) {
+  const int64_t stride = l->planes > 1 ? (int64_t)(l->plane[1] - l->plane[0]) : 0;
+  bool even = true;
+  for (int p = 2; p < l->planes && even; ++p)
+    even = l->plane[p] == l->plane[0] + (uintptr_t)((int64_t)p * stride);
+  rc.base[idx] = reinterpret_cast<const char *>(l->plane[0]);
+  rc.stride[idx] = stride;
+  rc.tab[idx] = -1;
+  if (even) return true;
+  if (rc.n_ptrs + l->planes > kvx::kReshardMaxPtrs) return false;
+  rc.tab[idx] = rc.n_ptrs;
+  for (int p = 0; p < l->planes; ++p)
+    rc.ptrs[rc.n_ptrs++] = reinterpret_cast<const char *>(l->plane[p]);
+  return true;
+}
+
+kvx_status kvx_reshard(const kvx_layout_t *srcs, int32_t n_srcs, const int32_t *d_src_slots,
+                       const kvx_layout_t *dsts, int32_t n_dsts, const int32_t *d_dst_slots,
+                       const kvx_head_part *parts, int32_t n_parts, int32_t n, void *d_ws,
+                       size_t ws_bytes, int32_t *d_status, kvx_stream_t stream) {
+  if (!srcs || !dsts || !parts || n_srcs < 1 || n_dsts < 1 ||
+      n_srcs + n_dsts > KVX_RESHARD_MAX_LAYOUTS || n_parts < 1 ||
+      n_parts > KVX_RESHARD_MAX_PARTS || !valid_n(n) || !d_status || !aligned(d_status, 4))
+    return KVX_ERR_INVALID_ARG;
+  const kvx_layout *s0 = srcs[0], *d0 = dsts[0];
+  if (!s0 || !d0) return KVX_ERR_INVALID_ARG;
+  for (int32_t k = 1; k < n_srcs; ++k)
+    if (!srcs[k] || !same_pool(srcs[k], s0)) return KVX_ERR_INVALID_ARG;
+  for (int32_t k = 1; k < n_dsts; ++k)
+    if (!dsts[k] || !same_pool(dsts[k], d0)) return KVX_ERR_INVALID_ARG;
+  if (s0->num_layers != d0->num_layers || s0->kv_planes != d0->kv_planes ||
+      s0->head_dim != d0->head_dim || s0->elem != d0->elem)
+    return KVX_ERR_INVALID_ARG;
+  const int32_t nh = parts[0].n_heads;
+  for (int32_t k = 0; k < n_parts; ++k) {
+    const kvx_head_part &q = parts[k];
+    if (q.reserved != 0 || q.n_heads != nh || nh < 1 || q.src < 0 || q.src >= n_srcs ||
+        q.dst < 0 || q.dst >= n_dsts)
+      return KVX_ERR_INVALID_ARG;
+    if (q.src_head0 < 0 || (int64_t)q.src_head0 + nh > s0->kv_heads || q.dst_head0 < 0 ||
+        (int64_t)q.dst_head0 + nh > d0->kv_heads)
+      return KVX_ERR_INVALID_ARG;
+    for (int32_t m = 0; m < k; ++m)  // one writer per destination head
+      if (parts[m].dst == q.dst && parts[m].dst_head0 < q.dst_head0 + nh &&
+          q.dst_head0 < parts[m].dst_head0 + nh)
+        return KVX_ERR_INVALID_ARG;
+  }
+  for (int32_t k = 0; k < n_dsts; ++k) {
+    for (int32_t m = 0; m < n_srcs; ++m)
+      if (layouts_overlap(srcs[m], dsts[k])) return KVX_ERR_OVERLAP;
+    for (int32_t m = 0; m < k; ++m)
+      if (layouts_overlap(dsts[m], dsts[k])) return KVX_ERR_OVERLAP;
+  }
+  Call c;
+  c.op = KVX_OP_TRANSFER;
+  c.n_tokens = n;
+  c.src = s0;
+  c.dst = d0;
+  c.shape = s0;
+  c.planes = s0->planes;
+  c.heads = nh;
+  c.seg_bytes = s0->seg_bytes;
+  c.row_bytes = (int64_t)nh * c.seg_bytes;
+  // the reshard kernel moves 16-byte vectors: every piece must start and end on 16 bytes
+  int32_t vec = std::min(std::min(side_vec(s0), side_vec(d0)), pow2_align(c.row_bytes));
+  for (int32_t k = 0; k < n_parts; ++k) {
+    const int64_t so = head_offset(s0, parts[k].src_head0), dof = head_offset(d0, parts[k].dst_head0);
+    if (so) vec = std::min(vec, pow2_align(so));
+    if (dof) vec = std::min(vec, pow2_align(dof));
+  }
+  if (vec < 16) return KVX_ERR_ALIGNMENT;
+  c.vec = 16;
+  static thread_local kvx::ReshardCall rc;  // ~30 KB: keep it off the stack
+  std::memset(&rc, 0, sizeof(rc));
+  for (int32_t k = 0; k < n_srcs; ++k)
+    if (!reshard_layout(rc, k, srcs[k])) return KVX_ERR_INVALID_ARG;
+  for (int32_t k = 0; k < n_dsts; ++k)
+    if (!reshard_layout(rc, n_srcs + k, dsts[k])) return KVX_ERR_INVALID_ARG;
+  for (int32_t k = 0; k < n_parts; ++k)
+    rc.parts[k] = kvx::ReshardPart{parts[k].src, n_srcs + parts[k].dst,
+                                   head_offset(s0, parts[k].src_head0),
+                                   head_offset(d0, parts[k].dst_head0)};
+  kvx_status st;
+  if (n > 0) {
+    if (!d_src_slots || !aligned(d_src_slots, 4) || !d_dst_slots || !aligned(d_dst_slots, 4))
+      return KVX_ERR_INVALID_ARG;
+    if ((st = check_ws(d_ws, ws_bytes, slots_ws(c))) != KVX_OK) return st;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (n == 0) {
+    e = cudaMemsetAsync(d_status, 0, sizeof(int32_t), s);
+    return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+  }
+  // the validating planner: a single tile writes the verdict itself, more tiles raise it
+  const bool direct = kvx::num_tiles(n) == 1;
+  if (!direct) {
+    e = cudaMemsetAsync(d_status, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  kvx::PlanArgs pa = plan_args(c, d_ws, d_status);
+  pa.src_idx = d_src_slots;
+  pa.dst_idx = d_dst_slots;
+  pa.validate_only = 1;
+  if (direct) pa.status_direct = 1;
+  if (pa.dup_table) {
+    e = cudaMemsetAsync(pa.dup_table, 0, sizeof(uint32_t) * ((size_t)pa.dup_mask + 1), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  e = kvx::launch_plan(pa, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  rc.n_tokens = n;
+  rc.planes = c.planes;
+  rc.n_parts = n_parts;
+  rc.row_bytes = (int32_t)c.row_bytes;
+  rc.src = pool_side(s0);
+  rc.dst = pool_side(d0);
+  rc.status = d_status;
+  rc.src_slots = d_src_slots;
+  rc.dst_slots = d_dst_slots;
+  e = kvx::launch_reshard(rc, s);
+  return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+}
+
 kvx_status kvx_plan_export(const void *d_ws, size_t ws_bytes, int64_t n_tokens,
                            int32_t *d_chunks, int64_t max_chunks, int64_t *d_count,
                            kvx_stream_t stream) {
@@ -1075,6 +1227,6 @@ kvx_status kvx_set_check_duplicates(int32_t on) {
 
 int32_t kvx_get_check_duplicates(void) { return g_check_dup.load(std::memory_order_relaxed); }
 
-int32_t kvx_version(void) { return 201; }
+int32_t kvx_version(void) { return 202; }
 
 }  // extern "C"

@@ -13,6 +13,7 @@
 //   3. a second scan of ceil(len / chunk_rows) gives each run's first chunk; every chunk is
 //      then written with one binary search over those chunk offsets.
 #include "kvx_internal.cuh"
+#include "kvx_launch.cuh"
 
 namespace kvx {
 namespace {
@@ -444,6 +445,8 @@ __global__ void __launch_bounds__(1024) export_kernel(const char *ws, WsLayout L
   if (threadIdx.x == 0) *count = carry;
 }
 
+}  // namespace
+
 cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, void **args, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -464,6 +467,8 @@ cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, void **args, cudaS
   }
   return e;
 }
+
+namespace {
 
 // Duplicate-destination check (kvx_set_check_duplicates), behind the planner: one thread per
 // destination slot inserts it into an open-addressing table in the workspace (entry = slot + 1,

@@ -102,6 +102,25 @@ class StreamCtl(ctypes.Structure):
         ("reserved2", ctypes.c_int32),
     ]
 
+class HeadPart(ctypes.Structure):
+    """kvx_head_part: heads [src_head0, src_head0 + n_heads) of srcs[src] -> heads from
+    dst_head0 of dsts[dst]."""
+    _fields_ = [
+        ("src", ctypes.c_int32),
+        ("dst", ctypes.c_int32),
+        ("src_head0", ctypes.c_int32),
+        ("dst_head0", ctypes.c_int32),
+        ("n_heads", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+assert ctypes.sizeof(HeadPart) == 24
+
+RESHARD_MAX_LAYOUTS = 64
+RESHARD_MAX_PARTS = 128
+RESHARD_MAX_PLANE_TABLE = 3072
+
 _lib: Optional[ctypes.CDLL] = None
 
 _VP = ctypes.c_void_p
@@ -131,6 +150,10 @@ _SIGS = {
                             ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "kvx_move_heads": (_I32, [_I32, _VP, _VP, _I32, _VP, _VP, _I32, _I32, _I32, _VP, _SZ, _VP,
                               _SZ, _VP, _VP]),
+    "kvx_tp_plan": (_I32, [_I32, _I32, _I32, ctypes.POINTER(HeadPart), _I32,
+                           ctypes.POINTER(_I32)]),
+    "kvx_reshard": (_I32, [ctypes.POINTER(_VP), _I32, _VP, ctypes.POINTER(_VP), _I32, _VP,
+                           ctypes.POINTER(HeadPart), _I32, _I32, _VP, _SZ, _VP, _VP]),
     "kvx_plan": (_I32, [_I32, _VP, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _VP]),
     "kvx_plan_runs": (_I32, [_I32, _VP, _VP, _VP, _I32, _I32, _VP, _SZ, _VP, _VP]),
     "kvx_plan_batch": (_I32, [_VP, _VP, _VP, _I32, _I64, _VP, _I64, _VP, _I64, _SZ, _VP, _SZ,
@@ -473,6 +496,35 @@ def tp_slice(kv_heads: int, src_tp: int, src_rank: int, dst_tp: int, dst_rank: i
     _check(lib().kvx_tp_slice(kv_heads, src_tp, src_rank, dst_tp, dst_rank, ctypes.byref(a),
                               ctypes.byref(b), ctypes.byref(c)), "kvx_tp_slice")
     return a.value, b.value, c.value
+
+
+def tp_plan(kv_heads: int, src_tp: int, dst_tp: int):
+    """kvx_tp_plan: the whole reshard plan between TP groups of sizes src_tp and dst_tp, as a
+    list of (src rank, dst rank, src_head0, dst_head0, n_heads)."""
+    n = _I32(0)
+    rc = lib().kvx_tp_plan(kv_heads, src_tp, dst_tp, None, 0, ctypes.byref(n))
+    if rc != OK and n.value == 0:
+        _check(rc, "kvx_tp_plan")
+    arr = (HeadPart * max(1, n.value))()
+    _check(lib().kvx_tp_plan(kv_heads, src_tp, dst_tp, arr, n.value, ctypes.byref(n)),
+           "kvx_tp_plan")
+    return [(q.src, q.dst, q.src_head0, q.dst_head0, q.n_heads) for q in arr[:n.value]]
+
+
+def reshard(srcs: Sequence[Optional[Layout]], src_slots, dsts: Sequence[Optional[Layout]],
+            dst_slots, parts, n: int, ws, status, ws_bytes=None, stream=None) -> None:
+    """kvx_reshard: every part (src, dst, src_head0, dst_head0, n_heads) of a reshard between
+    the pools of two TP groups, in one planner + one copy launch."""
+    sa = (_VP * max(1, len(srcs)))(*[_h(x) for x in srcs])
+    da = (_VP * max(1, len(dsts)))(*[_h(x) for x in dsts])
+    pa = (HeadPart * max(1, len(parts)))()
+    for k, q in enumerate(parts):
+        vals = tuple(int(x) for x in q)
+        pa[k] = HeadPart(*(vals + (0,) * (6 - len(vals))))
+    rc = lib().kvx_reshard(sa, len(srcs), _ptr(src_slots), da, len(dsts), _ptr(dst_slots), pa,
+                           len(parts), n, _ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
+                           _ptr(status), _stream(stream))
+    _check(rc, "kvx_reshard")
 
 
 def move_heads(op: int, src: Optional[Layout], src_slots, src_head0: int, dst: Optional[Layout],

@@ -337,6 +337,66 @@ KVX_API kvx_status kvx_move_heads(int32_t op, kvx_layout_t src, const int32_t *d
                                   void *d_ws, size_t ws_bytes, int32_t *d_status,
                                   kvx_stream_t stream);
 
+/* One part of a reshard (kvx_reshard): heads src_head0 .. src_head0 + n_heads - 1 of layout
+ * srcs[src] go to heads dst_head0 .. dst_head0 + n_heads - 1 of layout dsts[dst].  Host
+ * memory, 24 bytes. */
+typedef struct kvx_head_part {
+  int32_t src;
+  int32_t dst;
+  int32_t src_head0;
+  int32_t dst_head0;
+  int32_t n_heads;
+  int32_t reserved; /* must be 0 */
+} kvx_head_part;
+
+/* Most layouts (sources plus destinations) and most parts of one kvx_reshard, and most plane
+ * addresses its layouts whose planes are not evenly spaced (plane_ptrs not a constant stride
+ * apart) may bring together; evenly spaced layouts count nothing towards the last. */
+#define KVX_RESHARD_MAX_LAYOUTS 64
+#define KVX_RESHARD_MAX_PARTS 128
+#define KVX_RESHARD_MAX_PLANE_TABLE 3072
+
+/* The whole transfer plan between a tensor-parallel group of size src_tp and one of size
+ * dst_tp ([Mooncake] 7.7 异构TP): kvx_tp_slice for every (source rank, destination rank)
+ * pair, the pairs that exchange nothing left out, destination rank major and source rank
+ * minor, with part.src = the source rank and part.dst = the destination rank.  Writes at most
+ * max_parts parts (host memory; parts may be NULL when max_parts is 0) and sets *n_parts to
+ * the plan's count.  KVX_ERR_INVALID_ARG for sizes kvx_tp_slice refuses, a group size above
+ * 1024, a null n_parts, or a plan of more than max_parts parts (*n_parts still says how many
+ * it needs).  Host-only. */
+KVX_API kvx_status kvx_tp_plan(int32_t kv_heads, int32_t src_tp, int32_t dst_tp,
+                               kvx_head_part *parts, int32_t max_parts, int32_t *n_parts);
+
+/* A whole reshard between two tensor-parallel groups in one call ([Mooncake] 7.7 异构TP: a D
+ * rank merges the shards of several P ranks; a P rank's shard is split over several D ranks).
+ * For every part, plane p and token i < n, heads part.src_head0 .. + n_heads - 1 of
+ * row(srcs[part.src], p, d_src_slots[i]) go to heads part.dst_head0 .. + n_heads - 1 of
+ * row(dsts[part.dst], p, d_dst_slots[i]): the result of the parts' kvx_move_heads transfers,
+ * done by one planner and one copy launch.  The ranks of one instance share its block table,
+ * so one slot list (device int32[n]) serves every source and one every destination.
+ *  - srcs: host array of n_srcs >= 1 layouts, the pools of one group's ranks: identical
+ *    descriptors apart from their plane addresses.  dsts likewise (n_dsts >= 1), with
+ *    n_srcs + n_dsts <= KVX_RESHARD_MAX_LAYOUTS.  Both sides share num_layers, kv_planes,
+ *    head_dim and dtype; kv_heads may differ between the sides.
+ *  - parts: host array of 1 .. KVX_RESHARD_MAX_PARTS parts, all with the same n_heads (every
+ *    plan kvx_tp_plan makes has this form), head ranges inside their layouts, and no two parts
+ *    writing the same head of the same destination.
+ *  - layouts given by uneven plane_ptrs bring at most KVX_RESHARD_MAX_PLANE_TABLE plane
+ *    addresses together.
+ * Errors before anything is enqueued: KVX_ERR_INVALID_ARG (the conditions above, null
+ * pointers); KVX_ERR_OVERLAP (a source's memory overlaps a destination's, or two
+ * destinations' memory overlaps, the same layout listed twice included); KVX_ERR_ALIGNMENT
+ * (a part's bytes do not start and end on 16-byte boundaries within rows); KVX_ERR_NO_WORKSPACE
+ * (d_ws as kvx_transfer: kvx_workspace_size(n, 0) bytes).  On the stream: *d_status = KVX_OK,
+ * or KVX_ERR_OUT_OF_RANGE (a slot outside [0, num_slots)) or KVX_ERR_DUPLICATE_DST (with
+ * kvx_set_check_duplicates on), with nothing written. */
+KVX_API kvx_status kvx_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
+                               const int32_t *d_src_slots, const kvx_layout_t *dsts,
+                               int32_t n_dsts, const int32_t *d_dst_slots,
+                               const kvx_head_part *parts, int32_t n_parts, int32_t n,
+                               void *d_ws, size_t ws_bytes, int32_t *d_status,
+                               kvx_stream_t stream);
+
 /* ---- layer-streamed, cancellable copy ------------------------------------------------- */
 
 /* Longest a kvx_stream wait for one layer may be bounded to (ctl->wait_ns): 10 s. */

@@ -20,7 +20,7 @@ GUARD = 64 * 1024
 
 
 def _shape(kind: str, L: int, H: int, D: int, num_slots: int, ps: int, kvp: int = 2):
-    if kind in ("planes", "planes_separate"):
+    if kind in ("planes", "planes_separate", "planes_rotated"):
         return (kvp * L, num_slots, H, D)
     if kind == "slot_major":
         return (num_slots, L, kvp, H, D)
@@ -32,7 +32,7 @@ def _shape(kind: str, L: int, H: int, D: int, num_slots: int, ps: int, kvp: int 
 
 @dataclass
 class Mirror:
-    kind: str  # planes | planes_separate | slot_major | hnd | buffer
+    kind: str  # planes | planes_separate | planes_rotated | slot_major | hnd | buffer
     L: int
     H: int
     D: int
@@ -99,6 +99,8 @@ def oracle_pool(m: Mirror) -> oracle.Pool:
                 view = m.body[:, layer, kv]
             elif m.kind == "planes_separate":  # plane p stored in block P-1-p
                 view = m.body[m.P - 1 - (m.kvp * layer + kv)]
+            elif m.kind == "planes_rotated":  # plane p stored in block (p + P/2) % P
+                view = m.body[(m.kvp * layer + kv + m.P // 2) % m.P]
             else:
                 view = m.body[m.kvp * layer + kv]
             planes.append((m.host, view.__array_interface__["data"][0] - base_addr))
@@ -127,6 +129,10 @@ def kvx_layout(m: Mirror):
                           plane_stride=m.num_slots * R, keepalive=m.dev, kv_planes=kvp)
     if m.kind == "planes_separate":
         ptrs = [base + (P - 1 - p) * m.num_slots * R for p in range(P)]
+        return kvx.Layout(m.L, m.H, m.D, dt, m.num_slots, plane_ptrs=ptrs, keepalive=m.dev,
+                          kv_planes=kvp)
+    if m.kind == "planes_rotated":  # plane addresses not a constant stride apart
+        ptrs = [base + ((p + P // 2) % P) * m.num_slots * R for p in range(P)]
         return kvx.Layout(m.L, m.H, m.D, dt, m.num_slots, plane_ptrs=ptrs, keepalive=m.dev,
                           kv_planes=kvp)
     if m.kind == "slot_major":

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_misc(lib):
-    assert kvx.version() == 201
+    assert kvx.version() == 202
     assert kvx.status_str(kvx.OK) == "ok"
     assert "range" in kvx.status_str(kvx.ERR_OUT_OF_RANGE)
     ws = kvx.workspace_size(2048, 0)
@@ -201,6 +201,86 @@ def test_move_heads_validation_before_cuda(lib):
     assert mv(T, None, 0, dst, 0, 1) == kvx.ERR_INVALID_ARG
     assert mv(G, src, 0, None, 0, 2, buf=None, bb=0) == kvx.ERR_INVALID_ARG   # gather needs a buffer
     assert mv(G, src, 0, None, 0, 2, buf=FAKE * 7, bb=4 * 10 * 256 - 16) == kvx.ERR_INVALID_ARG
+
+
+def test_tp_plan_matches_oracle(lib):
+    """kvx_tp_plan is kvx_tp_slice over every rank pair (the oracle's), pairs with nothing to
+    send left out, destination rank major; too small an output array is refused but reports
+    the count; sizes the slice refuses are refused."""
+    for heads in (1, 2, 8):
+        for p_tp in (1, 2, 4, 8, 16):
+            for d_tp in (1, 2, 4, 8, 16):
+                ok = oracle.tp_slice(heads, p_tp, 0, d_tp, 0)[0] == oracle.OK
+                if not ok:
+                    with pytest.raises(kvx.KvxError):
+                        kvx.tp_plan(heads, p_tp, d_tp)
+                    continue
+                want = []
+                for dr in range(d_tp):
+                    for pr in range(p_tp):
+                        rc, h0, g0, nh = oracle.tp_slice(heads, p_tp, pr, d_tp, dr)
+                        if nh:
+                            want.append((pr, dr, h0, g0, nh))
+                assert kvx.tp_plan(heads, p_tp, d_tp) == want
+    n = ctypes.c_int32(-1)
+    arr = (kvx.HeadPart * 3)()
+    assert kvx.lib().kvx_tp_plan(8, 8, 1, arr, 3, ctypes.byref(n)) == kvx.ERR_INVALID_ARG
+    assert n.value == 8
+    assert kvx.lib().kvx_tp_plan(8, 8, 1, None, 0, None) == kvx.ERR_INVALID_ARG
+    assert kvx.lib().kvx_tp_plan(8, 2048, 1, None, 0, ctypes.byref(n)) == kvx.ERR_INVALID_ARG
+
+
+def test_reshard_validation_before_cuda(lib):
+    """kvx_reshard refuses, before any CUDA call, every malformed reshard: counts and limits,
+    sources (or destinations) that are not the same pool shape, geometry differing between the
+    sides, parts with bad indices, head ranges or unequal sizes, two parts writing one
+    destination head, overlapping memory, pieces not 16-byte aligned, missing workspace."""
+    mk = lambda k, h, ns=1000, **kw: kvx.Layout(2, h, 64, kvx.F16, ns, base=FAKE * k,
+                                               plane_stride=ns * h * 128, **kw)
+    p = [mk(1, 2), mk(2, 2)]            # P TP 2 of a 4-head model
+    d = [mk(3, 4)]                      # D TP 1
+    WS, ST, SL = FAKE * 6, FAKE * 7, FAKE * 8
+    big = 1 << 30
+    l = kvx.lib()
+    good = [(0, 0, 0, 0, 2), (1, 0, 0, 2, 2)]
+
+    def rs(srcs, dsts, parts, n=10, ws=WS, wsb=big, st=ST, sl=SL):
+        sa = (ctypes.c_void_p * max(1, len(srcs)))(*[x.handle for x in srcs])
+        da = (ctypes.c_void_p * max(1, len(dsts)))(*[x.handle for x in dsts])
+        pa = (kvx.HeadPart * max(1, len(parts)))(*[kvx.HeadPart(*q) for q in parts])
+        return l.kvx_reshard(sa, len(srcs), sl, da, len(dsts), sl, pa, len(parts), n, ws, wsb, st,
+                             None)
+
+    E, O, A = kvx.ERR_INVALID_ARG, kvx.ERR_OVERLAP, kvx.ERR_ALIGNMENT
+    assert rs(p, d, []) == E                                         # no parts
+    assert rs([], d, good) == E and rs(p, [], good) == E
+    assert rs(p, d, [(0, 0, 0, 0, 2)] * 129) == E                    # over KVX_RESHARD_MAX_PARTS
+    many = [mk(10 + k, 2) for k in range(64)]
+    assert rs(many, d, good) == E                                    # over KVX_RESHARD_MAX_LAYOUTS
+    assert rs([p[0], mk(4, 2, ns=999)], d, good) == E                # sources of different shape
+    assert rs([p[0], mk(4, 4)], d, good) == E
+    assert rs(p, [d[0], mk(4, 2)], good) == E                        # destinations of different shape
+    three = kvx.Layout(3, 4, 64, kvx.F16, 1000, base=FAKE * 5, plane_stride=1000 * 512)
+    assert rs(p, [three], good) == E                                 # layer counts differ
+    assert rs(p, d, [(0, 0, 0, 0, 2), (1, 0, 0, 2, 1)]) == E         # unequal n_heads
+    assert rs(p, d, [(2, 0, 0, 0, 2)]) == E                          # no source 2
+    assert rs(p, d, [(0, 1, 0, 0, 2)]) == E                          # no destination 1
+    assert rs(p, d, [(0, 0, 1, 0, 2)]) == E                          # past the source's heads
+    assert rs(p, d, [(0, 0, 0, 3, 2)]) == E                          # past the destination's heads
+    assert rs(p, d, [(0, 0, 0, 0, 2), (1, 0, 0, 1, 2)]) == E         # head 1 written twice
+    assert rs(p, d, [(0, 0, 0, 0, 2, 1)]) == E                       # reserved not 0
+    assert rs(p, d, [(0, 0, 0, 0, 0)]) == E                          # no heads
+    assert rs(p, d, good, st=None) == E
+    assert rs(p, d, good, n=-1) == E
+    assert rs(p, [p[0]], [(0, 0, 0, 0, 2)]) == O                     # a source is a destination
+    assert rs(p, [d[0], d[0]], [(0, 0, 0, 0, 2), (1, 1, 0, 0, 2)]) == O   # one pool twice
+    narrow = [kvx.Layout(2, 2, 4, kvx.F16, 1000, base=FAKE * (20 + k), plane_stride=1000 * 16)
+              for k in range(2)]
+    nd = kvx.Layout(2, 4, 4, kvx.F16, 1000, base=FAKE * 30, plane_stride=1000 * 32)
+    assert rs(narrow, [nd], [(0, 0, 0, 0, 1), (1, 0, 0, 1, 1)]) == A  # 8-byte pieces
+    assert rs(p, d, good, ws=None) == kvx.ERR_NO_WORKSPACE
+    assert rs(p, d, good, wsb=16) == kvx.ERR_NO_WORKSPACE
+    assert rs(p, d, good, sl=None) == E
 
 
 def test_latent_plane_layouts(lib):
