@@ -368,6 +368,8 @@ void fill_copy_args(kvx::CopyArgs &a, const Call &c, const kvx_request *d_reqs, 
   a.ws = static_cast<const char *>(d_ws);
   a.L = kvx::ws_layout(c.n_tokens, c.n_segs, false);
   a.status = d_status;
+  a.row_lanes = 32;  // one token per warp unless the call's row shape says otherwise
+  a.rows_per_warp = 1;
   for (int p = 0; p < c.planes; ++p) {
     a.src_planes[p] = c.src ? reinterpret_cast<const char *>(c.src->plane[p]) + c.src_head_off
                             : nullptr;
@@ -396,9 +398,9 @@ kvx_status enqueue_copy(const Call &c, const kvx_request *d_reqs, void *d_buf, c
   if (kvx::copy_variant(a) == kvx::kVariantRow) {
     a.host_status = host_status;
     if (host_status_written) *host_status_written = host_status != nullptr;
-    a.row_group_shift = kvx::row_group_shift(a);
+    kvx::row_shape(a, &a.row_lanes, &a.rows_per_warp);
     const cudaError_t e = kvx::launch_copy(
-        a, (int)kvx::row_grid(c.n_tokens, c.planes, a.row_group_shift), s);
+        a, (int)kvx::row_grid(c.n_tokens, c.planes, a.rows_per_warp), s);
     return e == cudaSuccess ? KVX_OK : cuda_fail(e);
   }
   a.spec_src = a.spec_dst = nullptr;  // the other kernels read the plan

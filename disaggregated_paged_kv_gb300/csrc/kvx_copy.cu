@@ -186,15 +186,18 @@ __global__ void __launch_bounds__(kCopyThreads, 8)
   }
 }
 
-// Row path.  Non-persistent grid: one warp per (group of g consecutive tokens, plane), token
-// major; g is a power of two with g * R <= KVX_CHUNK_BYTES where rows are small, so a warp moves
-// up to 2 KiB, and each token gets 32 / g lanes (so every lane serves exactly one token).  The
-// hardware keeps every SM full of short-lived 32-register warps (64 per SM).  Two sources of
-// indices:
+// Row path.  Non-persistent grid: one warp per (group of G consecutive tokens, plane), token
+// major, with m lanes per token (m * G <= 32; lanes past m * G idle).  Each lane moves vectors
+// li, li + m, li + 2m, ... of its token's row, kUnroll of them in flight per pass.  The host
+// picks (m, G) for the row length (row_shape): as many row bytes in flight per pass as the
+// lanes allow, in as few passes as possible -- a 2 KiB row takes a whole warp (m = 32, one
+// pass), 576-byte rows go three to a warp with nine lanes each (one pass; sixteen lanes for
+// two rows would leave 44 % of the slots empty).  The hardware keeps every SM full of
+// short-lived 32-register warps (64 per SM).  Two sources of indices:
 //  - speculative (one-shot calls, slot lists at hand): a lane range-checks its token and issues
 //    its loads before griddepcontrol.wait, so the planner runs under the first wave of loads;
 //    the stores wait for the planner's verdict, so the move stays all-or-nothing;
-//  - plan (g == 1, one-row chunks): after griddepcontrol.wait a warp reads chunk t of the plan
+//  - plan (G == 1, one-row chunks): after griddepcontrol.wait a warp reads chunk t of the plan
 //    (one chunk per token), including the request record of a batch.
 // Byte x of a token's row: on a token-row side the row is contiguous; on an HND side it sits at
 // head x / seg, offset x % seg of the token's page -- the fused [heads, tokens, dim] <->
@@ -213,27 +216,29 @@ __device__ __forceinline__ bool reports(const CopyArgs &a) {
 }
 
 // kSpec: indices from the slot lists (one-shot, single request); otherwise from the plan.
-// kTail: rows longer than kUnroll vectors per lane (over 2 KiB), moved in further passes; a
-// separate instance so that the common short-row kernels keep every value in registers.
+// kTail: rows of more than kUnroll * m vectors, moved in further passes; a separate instance so
+// that the one-pass kernels keep every value in registers.
 template <bool kSrcHnd, bool kDstHnd, bool kSpec, bool kTail>
-__global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8) copy_row_kernel(const __grid_constant__ CopyArgs a) {
+__global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 6 : 8)
+    copy_row_kernel(const __grid_constant__ CopyArgs a) {
   const int lane = threadIdx.x & 31;
   const uint32_t w = blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
   const uint32_t P = (uint32_t)a.planes;
   const uint32_t q = w / P;
   const int32_t p = (int32_t)(w - q * P);
-  const int32_t gsh = a.row_group_shift;   // g = 1 << gsh tokens per warp
-  const int32_t lsh = 5 - gsh;             // 1 << lsh lanes per token
-  const int64_t t0 = (int64_t)q << gsh;
+  const int32_t m = a.row_lanes;      // lanes per token
+  const int32_t G = a.rows_per_warp;  // tokens per warp
+  const int64_t t0 = (int64_t)q * G;
   if (t0 >= a.n_tokens) return;
-  const int64_t t = t0 + (lane >> lsh);
-  const int32_t li = lane & ((1 << lsh) - 1);
+  const int32_t rl = lane / m;        // this lane's token within the group
+  const int32_t li = lane - rl * m;
+  const int64_t t = t0 + rl;
   const int32_t R = a.row_bytes, vpr = R >> 4;
   bool sp = a.src.is_pool != 0, dp = a.dst.is_pool != 0;
   const char *bufp = a.buf;
   int64_t nreq = a.n_tokens;
   int32_t si, di;
-  bool ok = t < a.n_tokens;
+  bool ok = rl < G && t < a.n_tokens;
   if constexpr (kSpec) {
     const int64_t tt = ok ? t : t0;
     si = sp ? a.spec_src[tt] : (int32_t)tt;
@@ -246,7 +251,7 @@ __global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8) copy_row_kernel(c
       if (w == 0 && lane == 0) atomicMax(&a.status[0], (int32_t)KVX_ERR_INVALID_ARG);
       return;
     }
-    const Chunk ch = reinterpret_cast<const Chunk *>(a.ws + a.L.chunks_off)[t0];  // g == 1
+    const Chunk ch = reinterpret_cast<const Chunk *>(a.ws + a.L.chunks_off)[t0];  // G == 1
     if (a.mode == kModeBatch) {
       if (a.status[1 + ch.req] != KVX_OK) return;
       const kvx_request rq = a.reqs[ch.req];
@@ -266,7 +271,7 @@ __global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8) copy_row_kernel(c
   uint4 r[kUnroll];
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u) {
-    const int32_t xv = li + (u << lsh);
+    const int32_t xv = li + u * m;
     if (ok && xv < vpr) r[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
   }
   if constexpr (kSpec) {
@@ -279,27 +284,25 @@ __global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8) copy_row_kernel(c
   }
   if (kSpec && reports(a) && !ok) report_host_status(a.host_status, KVX_OK);
   if (!ok) return;
+  // the stores of each pass, then (kTail) the next pass's loads
+  const int32_t step = kUnroll * m;
+#pragma unroll 1
+  for (int32_t x0 = 0;;) {
 #pragma unroll
-  for (int u = 0; u < kUnroll; ++u) {
-    const int32_t xv = li + (u << lsh);
-    if (xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), r[u]);
-  }
-  if (kSpec && reports(a)) report_host_status(a.host_status, KVX_OK);
-  if constexpr (kTail) {
-    // the rest of a long row, after the verdict
-    for (int32_t x0 = kUnroll << lsh; x0 < vpr; x0 += kUnroll << lsh) {
+    for (int u = 0; u < kUnroll; ++u) {
+      const int32_t xv = x0 + li + u * m;
+      if (xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), r[u]);
+    }
+    if constexpr (!kTail) break;
+    x0 += step;
+    if (x0 >= vpr) break;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int32_t xv = x0 + li + (u << lsh);
-        if (xv < vpr) r[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int32_t xv = x0 + li + (u << lsh);
-        if (xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), r[u]);
-      }
+    for (int u = 0; u < kUnroll; ++u) {
+      const int32_t xv = x0 + li + u * m;
+      if (xv < vpr) r[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
     }
   }
+  if (kSpec && reports(a)) report_host_status(a.host_status, KVX_OK);
 }
 
 // ---- bulk (TMA) path ----------------------------------------------------------------------
@@ -450,9 +453,47 @@ int32_t row_group_shift(const CopyArgs &a) {
   return sh;
 }
 
-int64_t row_grid(int64_t n_tokens, int32_t planes, int32_t group_shift) {
-  const int64_t tokens_per_warp = (int64_t)1 << group_shift;
-  const int64_t warps = (n_tokens + tokens_per_warp - 1) / tokens_per_warp * planes;
+// Most passes row_shape lets a warp make over its rows.  Measured on 16,384 random tokens x 27
+// planes: 1152-byte rows move at 80 % of the copy peak in one pass of a whole warp and at 90 %
+// three to a warp with ten lanes each in two passes; three or more passes (fewer lanes, more
+// rows) fell to 71 % and below, as did 576-byte rows (76 % in one pass, 45 % in three).
+constexpr int32_t kMaxRowPasses = 2;
+
+void row_shape(const CopyArgs &a, int32_t *lanes, int32_t *rows) {
+  *lanes = 32;
+  *rows = 1;
+  // plans are read one chunk (= one token) per warp
+  if (!(a.spec_src != nullptr || a.spec_dst != nullptr)) return;
+  row_shape_for(a.row_bytes, lanes, rows);
+}
+
+void row_shape_for(int64_t row_bytes, int32_t *lanes, int32_t *rows) {
+  *lanes = 32;
+  *rows = 1;
+  // m lanes per token, G = 32 / m tokens per warp, passes = ceil(vpr / (kUnroll m)): the most
+  // row vectors per pass (G vpr / passes), then the fewest passes, then the most lanes.  A
+  // shape of several passes needs m >= 8 (each pass takes at least 128 bytes of every row).
+  const int64_t vpr = row_bytes >> 4;
+  int64_t best_num = 0, best_den = 1, best_passes = 0;
+  for (int32_t m = 32; m >= 1; --m) {
+    const int64_t G = 32 / m;
+    const int64_t passes = (vpr + (int64_t)kUnroll * m - 1) / ((int64_t)kUnroll * m);
+    if (m < 32 && (passes > kMaxRowPasses || (passes > 1 && m < 8))) continue;
+    const int64_t num = G * vpr;  // vectors per pass = num / passes
+    const bool better = num * best_den > best_num * passes ||
+                        (num * best_den == best_num * passes && passes < best_passes);
+    if (best_passes == 0 || better) {
+      best_num = num;
+      best_den = passes;
+      best_passes = passes;
+      *lanes = m;
+      *rows = (int32_t)G;
+    }
+  }
+}
+
+int64_t row_grid(int64_t n_tokens, int32_t planes, int32_t rows_per_warp) {
+  const int64_t warps = (n_tokens + rows_per_warp - 1) / rows_per_warp * planes;
   const int64_t wpb = kCopyThreads / 32;
   return (warps + wpb - 1) / wpb;
 }
@@ -470,7 +511,7 @@ const void *row_fn(const CopyArgs &a) {
   const bool sh = a.src.hnd && (a.src.is_pool || a.mode == kModeBatch);
   const bool dh = a.dst.hnd && (a.dst.is_pool || a.mode == kModeBatch);
   const bool spec = a.spec_src != nullptr || a.spec_dst != nullptr;
-  const bool tail = a.row_bytes > kUnroll * 32 * 16;  // more than one pass of the warp
+  const bool tail = (a.row_bytes >> 4) > kUnroll * a.row_lanes;  // more than one pass
   if (spec) return tail ? row_fn_of<true, true>(sh, dh) : row_fn_of<true, false>(sh, dh);
   return tail ? row_fn_of<false, true>(sh, dh) : row_fn_of<false, false>(sh, dh);
 }

@@ -164,7 +164,9 @@ struct CopyArgs {
   // once the planner's status word says every index is valid.  nullptr: read the plan.
   const int32_t *spec_src;
   const int32_t *spec_dst;
-  int32_t row_group_shift;  // row kernel: log2 of the tokens one warp moves
+  int32_t row_group_shift;  // streamed row grid: log2 of the tokens one warp moves
+  int32_t row_lanes;        // row kernel: lanes per token (1 .. 32)
+  int32_t rows_per_warp;    // row kernel: tokens per warp (row_lanes * rows_per_warp <= 32)
   int32_t vec_bytes;        // widest access the call's rows allow: 16, or 8/4/2/1 (kvx_narrow.cu)
   // kvx_submit with a pinned host status word: the row kernel stores the final status there
   // itself (through its device mapping) instead of a device-to-host copy.  nullptr: none.
@@ -229,8 +231,13 @@ bool copy_is_linear(const CopyArgs &a);
 bool use_bulk(const CopyArgs &a);
 int variant_threads(CopyVariant v);
 int variant_blocks_per_sm(CopyVariant v, int32_t n_tiles);
-// Grid of the row variant: one warp per (token, plane) row.
-int64_t row_grid(int64_t n_tokens, int32_t planes, int32_t group_shift);
+// Grid of the row variant: one warp per (group of rows_per_warp tokens, plane).
+int64_t row_grid(int64_t n_tokens, int32_t planes, int32_t rows_per_warp);
+// Lanes per token and tokens per warp of the row variant (CopyArgs::row_lanes, rows_per_warp).
+void row_shape(const CopyArgs &a, int32_t *lanes, int32_t *rows);
+// The same for any kernel whose warps each move whole rows of row_bytes (a multiple of 16).
+void row_shape_for(int64_t row_bytes, int32_t *lanes, int32_t *rows);
+// log2 of the tokens one warp of the streamed row grid moves.
 int32_t row_group_shift(const CopyArgs &a);
 constexpr int kBulkThreadsPerCta = 32;
 constexpr int kBulkSmallTiles = 256;  // occupancy is cached for <= this many tiles and for the max

@@ -7,7 +7,8 @@
 // launch pairs over 256-byte pieces, each with its own ramp and tail.  Here one validating
 // planner checks the two slot lists once and one row grid moves every part of the plan.
 //
-// Warp w of grid row y moves 1 << g tokens of one (plane, part) pair, parts fastest:
+// Warp w of grid row y moves G tokens of one (plane, part) pair with m lanes per token (the
+// row kernel's shape for the piece length, row_shape_for), parts fastest:
 // w = (q * P + p) * J + j for token group q, plane p, part j.  The J parts that fill one
 // destination row therefore run in neighbouring warps of one CTA, and the pieces of a row
 // reach L2 together.  Grid rows (blockIdx.y) of 4096 token groups keep w small.
@@ -32,9 +33,9 @@ struct ReshardArgs {
   int32_t planes;
   int32_t n_parts;
   int32_t row_bytes;
-  int32_t group_shift;  // 1 << group_shift tokens per warp
+  int32_t lanes;        // m lanes per token
+  int32_t rows;         // G tokens per warp
   uint32_t groups_per_y;
-  int32_t pad;
   Side src, dst;
   int32_t *status;
   const int32_t *src_slots;
@@ -58,9 +59,9 @@ __device__ __forceinline__ const char *plane_addr(const ReshardArgs<kPtrs> &a, i
   return a.base[l] + (int64_t)p * a.stride[l];
 }
 
-// kTail: rows longer than kUnroll vectors per lane (over 2 KiB), moved in further passes.
+// kTail: rows of more than kUnroll * m vectors, moved in further passes.
 template <bool kSrcHnd, bool kDstHnd, bool kTail, int kPtrs>
-__global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8)
+__global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 6 : 8)
     reshard_kernel(const __grid_constant__ ReshardArgs<kPtrs> a) {
   const int lane = threadIdx.x & 31;
   const uint32_t w = blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
@@ -70,18 +71,19 @@ __global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8)
   const uint32_t qy = r / P;
   const int32_t p = (int32_t)(r - qy * P);
   if (qy >= a.groups_per_y) return;
-  const int32_t gsh = a.group_shift;
-  const int32_t lsh = 5 - gsh;  // 1 << lsh lanes per token
+  const int32_t m = a.lanes, G = a.rows;
   // n_tokens <= KVX_MAX_TOKENS (2^23): token indices fit in 32 bits
   const int32_t nt = (int32_t)a.n_tokens;
-  const int32_t t0 = (int32_t)((blockIdx.y * a.groups_per_y + qy) << gsh);
+  const int32_t t0 = (int32_t)((blockIdx.y * a.groups_per_y + qy) * G);
   if (t0 >= nt) return;
-  const int32_t t = t0 + (lane >> lsh);
-  const int32_t li = lane & ((1 << lsh) - 1);
+  const int32_t rl = lane / m;
+  const int32_t li = lane - rl * m;
+  const int32_t t = t0 + rl;
   const int32_t R = a.row_bytes, vpr = R >> 4;
-  const int32_t tt = t < nt ? t : t0;
+  const bool in = rl < G && t < nt;
+  const int32_t tt = in ? t : t0;
   const int32_t si = a.src_slots[tt], di = a.dst_slots[tt];
-  const bool ok = t < nt && si >= 0 && (int64_t)si < a.src.num_slots && di >= 0 &&
+  const bool ok = in && si >= 0 && (int64_t)si < a.src.num_slots && di >= 0 &&
                   (int64_t)di < a.dst.num_slots;
   const ReshardPart &pt = a.parts[j];
   const char *srow =
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8)
   uint4 v[kUnroll];
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u) {
-    const int32_t xv = li + (u << lsh);
+    const int32_t xv = li + u * m;
     if (ok && xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, true, srow, xv << 4));
   }
   pdl_wait();  // the planner has checked both slot lists
@@ -97,24 +99,22 @@ __global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8)
   if (!ok) return;
   char *drow = const_cast<char *>(row_base<kDstHnd>(
       a.dst, true, plane_addr(a, a.parts[j].dst, p) + a.parts[j].dst_off, nullptr, di, R));
+  const int32_t step = kUnroll * m;
+#pragma unroll 1
+  for (int32_t x0 = 0;;) {
 #pragma unroll
-  for (int u = 0; u < kUnroll; ++u) {
-    const int32_t xv = li + (u << lsh);
-    if (xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, true, drow, xv << 4)), v[u]);
-  }
-  if constexpr (kTail) {
-    for (int32_t x0 = kUnroll << lsh; x0 < vpr; x0 += kUnroll << lsh) {
+    for (int u = 0; u < kUnroll; ++u) {
+      const int32_t xv = x0 + li + u * m;
+      if (xv < vpr)
+        st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, true, drow, xv << 4)), v[u]);
+    }
+    if constexpr (!kTail) break;
+    x0 += step;
+    if (x0 >= vpr) break;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int32_t xv = x0 + li + (u << lsh);
-        if (xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, true, srow, xv << 4));
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int32_t xv = x0 + li + (u << lsh);
-        if (xv < vpr)
-          st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, true, drow, xv << 4)), v[u]);
-      }
+    for (int u = 0; u < kUnroll; ++u) {
+      const int32_t xv = x0 + li + u * m;
+      if (xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, true, srow, xv << 4));
     }
   }
 }
@@ -128,16 +128,16 @@ const void *reshard_fn(bool sh, bool dh) {
 }
 
 template <int kPtrs>
-cudaError_t launch_with(const ReshardCall &c, int32_t gsh, uint32_t per_y, dim3 grid,
+cudaError_t launch_with(const ReshardCall &c, int32_t m, int32_t G, uint32_t per_y, dim3 grid,
                         cudaStream_t s) {
   static thread_local ReshardArgs<kPtrs> a;  // up to ~29 KB: keep it off the stack
   a.n_tokens = c.n_tokens;
   a.planes = c.planes;
   a.n_parts = c.n_parts;
   a.row_bytes = c.row_bytes;
-  a.group_shift = gsh;
+  a.lanes = m;
+  a.rows = G;
   a.groups_per_y = per_y;
-  a.pad = 0;
   a.src = c.src;
   a.dst = c.dst;
   a.status = c.status;
@@ -151,7 +151,7 @@ cudaError_t launch_with(const ReshardCall &c, int32_t gsh, uint32_t per_y, dim3 
   for (int k = 0; k < KVX_RESHARD_MAX_PARTS; ++k) a.parts[k] = c.parts[k];
   for (int k = 0; k < kPtrs; ++k) a.ptrs[k] = k < c.n_ptrs ? c.ptrs[k] : nullptr;
   const bool sh = c.src.hnd != 0, dh = c.dst.hnd != 0;
-  const bool tail = c.row_bytes > kUnroll * 32 * 16;
+  const bool tail = (c.row_bytes >> 4) > kUnroll * m;  // more than one pass
   const void *fn = tail ? reshard_fn<true, kPtrs>(sh, dh) : reshard_fn<false, kPtrs>(sh, dh);
   void *params[] = {&a};
   return launch_pdl(fn, grid, dim3(kCopyThreads), params, s);
@@ -160,10 +160,10 @@ cudaError_t launch_with(const ReshardCall &c, int32_t gsh, uint32_t per_y, dim3 
 }  // namespace
 
 cudaError_t launch_reshard(const ReshardCall &c, cudaStream_t s) {
-  // tokens per warp: as the row kernel, up to 2 KiB per warp for short rows
-  int32_t gsh = 0;
-  while (gsh < 5 && ((int64_t)c.row_bytes << (gsh + 1)) <= KVX_CHUNK_BYTES) ++gsh;
-  const int64_t groups = (c.n_tokens + (1 << gsh) - 1) >> gsh;
+  // lanes per token and tokens per warp: the row kernel's shape for this piece length
+  int32_t m = 32, G = 1;
+  row_shape_for(c.row_bytes, &m, &G);
+  const int64_t groups = (c.n_tokens + G - 1) / G;
   const int64_t pj = (int64_t)c.planes * c.n_parts;  // at most 256 x 128 = 2^15
   // grid rows of at most 4096 token groups: warp indices of a row stay below 2^27, and the
   // rows number at most 2^23 / 4096 = 2048
@@ -172,8 +172,8 @@ cudaError_t launch_reshard(const ReshardCall &c, cudaStream_t s) {
   const int64_t gx = (warps + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
   const int64_t gy = (groups + per_y - 1) / per_y;
   const dim3 grid((unsigned)gx, (unsigned)gy);
-  return c.n_ptrs > 0 ? launch_with<kReshardMaxPtrs>(c, gsh, (uint32_t)per_y, grid, s)
-                      : launch_with<0>(c, gsh, (uint32_t)per_y, grid, s);
+  return c.n_ptrs > 0 ? launch_with<kReshardMaxPtrs>(c, m, G, (uint32_t)per_y, grid, s)
+                      : launch_with<0>(c, m, G, (uint32_t)per_y, grid, s);
 }
 
 }  // namespace kvx
