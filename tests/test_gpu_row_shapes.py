@@ -27,7 +27,7 @@ def _cuda():
     yield
 
 
-# row bytes (fp16, one head of R / 2 elements, or two heads where noted by the kind)
+# row bytes (fp16: two heads of R / 4 elements where those are whole 16-byte vectors, else one)
 ROWS = [16, 32, 64, 80, 112, 192, 400, 576, 800, 1152, 1280, 1600, 2048, 2304, 4112]
 L = 2
 
@@ -37,7 +37,7 @@ def _rng(k):
 
 
 def _mirror(kind, R, fill, g=None, num_slots=2048, salt=0, n_tokens=0):
-    H = 2 if (R % 32 == 0 and kind == "hnd") else 1
+    H = 2 if R % 32 == 0 else 1
     D = R // (2 * H)
     return hz.make_mirror(kind, L, H, D, "fp16", num_slots, 16 if kind == "hnd" else 1, fill, g,
                           salt=salt, n_tokens=n_tokens)
