@@ -678,7 +678,8 @@ def run_formats(args):
       mla_fp8    the same latent rows in fp8 (576 B)
       gqa_fp8    the headline shape in fp8 (36 x K/V x 8 x 128: 1 KiB rows), 2048 tokens
       narrow     200-byte rows (one head of head_dim 100 fp16) through 8-byte accesses
-      transcode  the headline shape from a slot-major pool into per-plane pools"""
+      transcode  the headline shape from a slot-major pool into per-plane pools
+    and, except the narrow rows, the same transfer through kvx_stream with every layer ready."""
     import numpy as np
     import torch
 
@@ -733,21 +734,41 @@ def run_formats(args):
         do = (NS + int(d_d[k])) * Rc
         assert torch.equal(dst[do:do + Rc], src[so:so + Rc])
         K = args.steps
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(K)]
-        with torch.cuda.stream(stream):
-            for i in range(K):
-                flush.fill_(i & 0xFF)
-                ev[i][0].record(stream)
-                step()
-                ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+        def timed(fn):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(K)]
+            with torch.cuda.stream(stream):
+                for i in range(K):
+                    flush.fill_(i & 0xFF)
+                    ev[i][0].record(stream)
+                    fn()
+                    ev[i][1].record(stream)
+            torch.cuda.synchronize()
+            return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+        ms = timed(step)
         alg = 2 * n * Pc * Rc + 8 * n
         gbs = alg / (ms * 1e-3) / 1e9
         results[name] = {"row_bytes": Rc, "planes": Pc, "tokens": n,
                          "payload_bytes_each_way": n * Pc * Rc, "us_per_request": ms * 1e3,
                          "GBs": gbs, "frac_of_measured_hbm": gbs / float(peaks["hbm_gbs"])}
+        if name != "narrow":  # the streamed kernels move 16-byte vectors only
+            st4 = torch.zeros(4, dtype=torch.int32, device=dev)
+
+            def step_stream():
+                kvx.stream(kvx.OP_TRANSFER, sl, s_d, dl, d_d, n, None, ws, st4, buf_bytes=0,
+                           stream=sp)
+
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    flush.fill_(1)
+                    step_stream()
+            ms_s = timed(step_stream)
+            assert st4.tolist()[:2] == [kvx.OK, 0], st4.tolist()
+            gbs_s = alg / (ms_s * 1e-3) / 1e9
+            results[name]["streamed_us_per_request"] = ms_s * 1e3
+            results[name]["streamed_frac_of_measured_hbm"] = gbs_s / float(peaks["hbm_gbs"])
         del src, dst, sl, dl
         torch.cuda.empty_cache()
     head = results["mla_bf16"]
@@ -927,7 +948,9 @@ def run_stream(args):
     by the host at a fixed cadence (an emulated prefill producing one layer every --layer-us):
     host time from raising the last layer to seeing the kernel's pinned "done" word.  (3) The
     same move started only after the last layer (no streaming): host time from the launch to
-    the same word."""
+    the same word.  (4) Epoch-fenced writes: every layer ready with the request's epoch word or
+    every destination page's owner word checked (device time), and a cancellation after half
+    the layers (host time from changing the pinned epoch word to the "done" word)."""
     import numpy as np
     import torch
 
@@ -1002,6 +1025,13 @@ def run_stream(args):
     words_ms = timed(layer_ready=words, ready_value=1)
     persistent_ms = timed(max_ctas=2 * torch.cuda.get_device_properties(dev).multi_processor_count)
 
+    # epoch-fenced writes: the request's epoch word checked, or every destination page's owner
+    # word checked (nothing cancelled or reassigned: the cost of the checks alone)
+    ep_word = torch.full((1,), 7, dtype=torch.int32, device=dev)
+    epoch_ms = timed(epoch_word=ep_word, epoch=7)
+    page_ep = torch.full(((NS + 15) // 16,), 7, dtype=torch.int32, device=dev)
+    pages_ms = timed(dst_page_epochs=page_ep, epoch_page=16, epoch=7)
+
     # (2) layers raised by the host at a fixed cadence; (3) the move started after the last one
     cadence = args.layer_us * 1e-6
     trials = 30
@@ -1038,6 +1068,32 @@ def run_stream(args):
         torch.cuda.synchronize()
         assert st.tolist()[:2] == [kvx.OK, 0], st.tolist()
 
+    # (4) a cancellation: half the layers raised at the cadence, then the host changes the
+    # request's epoch word (pinned); host time from the change to the "no further write" word
+    ep_host = torch.zeros(1, dtype=torch.int32).pin_memory()
+    cancels, pending = [], []
+    for trial in range(trials):
+        v = 1000 + trial  # above every ready value used so far
+        ep_host[0] = v
+        done[0] = 0
+        flush.fill_(trial & 0xFF)
+        torch.cuda.synchronize()
+        launch(layer_ready=ready, ready_value=v, epoch_word=ep_host, epoch=v,
+               wait_ns=1_000_000_000, host_done=done)
+        t0 = time.perf_counter()
+        for layer in range(L // 2):
+            target = t0 + (layer + 1) * cadence
+            while time.perf_counter() < target:
+                pass
+            ready[layer] = v
+        t_c = time.perf_counter()
+        ep_host[0] = v + 1
+        cancels.append((wait_done(t_c) - t_c) * 1e6)
+        torch.cuda.synchronize()
+        s_ = st.tolist()
+        assert s_[0] == kvx.ERR_CANCELLED and s_[3] == 1 and L - L // 2 <= s_[1] <= L, s_
+        pending.append(s_[1])
+
     def pct(xs):
         xs = sorted(xs)
         return {"median": xs[len(xs) // 2], "p10": xs[len(xs) // 10], "p90": xs[(9 * len(xs)) // 10]}
@@ -1057,13 +1113,18 @@ def run_stream(args):
                       "includes": "planner + streamed copy + epilogue"},
         "all_ready_device_words_us": words_ms * 1e3,
         "all_ready_persistent_2_per_sm_us": persistent_ms * 1e3,
+        "all_ready_request_epoch_checked_us": epoch_ms * 1e3,
+        "all_ready_page_owners_checked_us": pages_ms * 1e3,
+        "cancel_to_no_further_write_us": pct(cancels),
+        "cancel_layers_pending": {"min": min(pending), "max": max(pending),
+                                  "of": L, "raised_before_cancel": L // 2},
         "streamed_tail_us": pct(tails),
         "unstreamed_us": pct(unstreamed),
         "producer": f"host raises one layer every {args.layer_us:g} us into pinned ready words; "
                     f"{trials} trials; times on the host clock (time.perf_counter), the kernel's "
                     "done word polled in pinned memory",
         "clocks": clk,
-        "gpu_launches": 2 * K,
+        "gpu_launches": 3 * K,  # validating planner, streamed row grid, epilogue
     }
     print(json.dumps(line), flush=True)
 

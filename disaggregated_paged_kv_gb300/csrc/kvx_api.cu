@@ -931,8 +931,8 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
   fill_copy_args(a, c, nullptr, d_buf, d_ws, d_status);
   a.spec_src = c.src ? d_src_slots : nullptr;
   a.spec_dst = c.dst ? d_dst_slots : nullptr;
-  a.row_group_shift = kvx::row_group_shift(a);
-  kvx::stream_sizes(k, n, a.row_group_shift);
+  kvx::row_shape(a, &a.row_lanes, &a.rows_per_warp);
+  kvx::stream_sizes(k, n, a.rows_per_warp);
   if (ctl->max_ctas == 0) {  // one warp per item, then the epilogue
     e = kvx::launch_stream_rows(a, k, s);
     return e == cudaSuccess ? KVX_OK : cuda_fail(e);

@@ -445,14 +445,6 @@ CopyVariant copy_variant(const CopyArgs &a) {
   return a.mode == kModeBatch ? kVariantLinear : kVariantLean;
 }
 
-int32_t row_group_shift(const CopyArgs &a) {
-  // plans are read one chunk (= one token) per warp; speculative calls group small rows
-  if (!(a.spec_src != nullptr || a.spec_dst != nullptr)) return 0;
-  int32_t sh = 0;
-  while (sh < 5 && ((int64_t)a.row_bytes << (sh + 1)) <= KVX_CHUNK_BYTES) ++sh;
-  return sh;
-}
-
 // Most passes row_shape lets a warp make over its rows.  Measured on 16,384 random tokens x 27
 // planes: 1152-byte rows move at 80 % of the copy peak in one pass of a whole warp and at 90 %
 // three to a warp with ten lanes each in two passes; three or more passes (fewer lanes, more

@@ -164,9 +164,9 @@ struct CopyArgs {
   // once the planner's status word says every index is valid.  nullptr: read the plan.
   const int32_t *spec_src;
   const int32_t *spec_dst;
-  int32_t row_group_shift;  // streamed row grid: log2 of the tokens one warp moves
-  int32_t row_lanes;        // row kernel: lanes per token (1 .. 32)
-  int32_t rows_per_warp;    // row kernel: tokens per warp (row_lanes * rows_per_warp <= 32)
+  int32_t row_group_shift;  // narrow kernel: log2 of the tokens one warp moves
+  int32_t row_lanes;        // row and streamed kernels: lanes per token (1 .. 32)
+  int32_t rows_per_warp;    // tokens per warp (row_lanes * rows_per_warp <= 32)
   int32_t vec_bytes;        // widest access the call's rows allow: 16, or 8/4/2/1 (kvx_narrow.cu)
   // kvx_submit with a pinned host status word: the row kernel stores the final status there
   // itself (through its device mapping) instead of a device-to-host copy.  nullptr: none.
@@ -192,7 +192,7 @@ struct StreamCtl {
   int32_t ready_value;
   int32_t epoch;
   int32_t layers;
-  uint32_t groups;     // row groups of 1 << row_group_shift tokens per plane
+  uint32_t groups;     // row groups of rows_per_warp tokens per plane
   uint32_t per_layer;  // items per layer: kv_planes * groups
   uint32_t items;      // per_layer * layers (< 2^32 for every legal size)
   uint32_t per_layer_pad;  // row grid: per_layer rounded up to whole CTAs
@@ -237,8 +237,6 @@ int64_t row_grid(int64_t n_tokens, int32_t planes, int32_t rows_per_warp);
 void row_shape(const CopyArgs &a, int32_t *lanes, int32_t *rows);
 // The same for any kernel whose warps each move whole rows of row_bytes (a multiple of 16).
 void row_shape_for(int64_t row_bytes, int32_t *lanes, int32_t *rows);
-// log2 of the tokens one warp of the streamed row grid moves.
-int32_t row_group_shift(const CopyArgs &a);
 constexpr int kBulkThreadsPerCta = 32;
 constexpr int kBulkSmallTiles = 256;  // occupancy is cached for <= this many tiles and for the max
 // Records e as this thread's kvx_last_cuda_error().
@@ -249,7 +247,7 @@ cudaError_t launch_narrow(const CopyArgs &a, cudaStream_t s);
 int32_t narrow_group_shift(int32_t row_bytes, int32_t vec_bytes);
 // Layer-streamed copy (kvx_stream.cu): persistent grid over layer-major row groups.
 int stream_blocks_per_sm();
-void stream_sizes(StreamCtl &k, int64_t n_tokens, int32_t group_shift);
+void stream_sizes(StreamCtl &k, int64_t n_tokens, int32_t rows_per_warp);
 cudaError_t launch_stream(const CopyArgs &c, const StreamCtl &k, int grid, cudaStream_t s);
 // Row grid (one warp per item) and the epilogue that sets the "no further write" words.
 cudaError_t launch_stream_rows(const CopyArgs &c, const StreamCtl &k, cudaStream_t s);

@@ -182,7 +182,7 @@ __device__ int32_t wait_layer(const StreamCtl &k, int32_t l, bool owner, CtaStat
 }
 
 template <bool kSrcHnd, bool kDstHnd>
-__global__ void __launch_bounds__(kCopyThreads, 6) stream_kernel(const __grid_constant__ StreamArgs s) {
+__global__ void __launch_bounds__(kCopyThreads, 5) stream_kernel(const __grid_constant__ StreamArgs s) {
   __shared__ CtaState cs;
   const CopyArgs &a = s.c;
   const StreamCtl &k = s.k;
@@ -198,8 +198,8 @@ __global__ void __launch_bounds__(kCopyThreads, 6) stream_kernel(const __grid_co
   }
   __syncthreads();
 
-  const int32_t gsh = a.row_group_shift, lsh = 5 - gsh;
-  const int32_t li = lane & ((1 << lsh) - 1);
+  const int32_t m = a.row_lanes, G = a.rows_per_warp;  // lanes per token, tokens per warp
+  const int32_t rl = lane / m, li = lane - rl * m;
   const int32_t R = a.row_bytes, vpr = R >> 4;
   const bool sp = a.src.is_pool != 0, dp = a.dst.is_pool != 0;
   // Blocks of kWarps * k.block consecutive items go to the CTAs in turn; warp w of a CTA takes
@@ -225,11 +225,11 @@ __global__ void __launch_bounds__(kCopyThreads, 6) stream_kernel(const __grid_co
     }
     const uint32_t r = i - (uint32_t)l * k.per_layer;
     const int32_t kv = r >= k.groups ? 1 : 0;  // K or V (always 0 with one latent plane)
-    const int64_t t = ((int64_t)(r - kv * k.groups) << gsh) + (lane >> lsh);
+    const int64_t t = (int64_t)(r - kv * k.groups) * G + rl;
     const int32_t p = k.kv_planes * l + kv;
     // The first item's loads go out before the planner's verdict, like the row kernel's; a
     // lane range-checks its own indices first so that it never reads outside a pool.
-    bool ok = t < a.n_tokens;
+    bool ok = rl < G && t < a.n_tokens;
     const int64_t tt = ok ? t : 0;
     const int32_t si = sp ? a.spec_src[tt] : (int32_t)tt;
     const int32_t di = dp ? a.spec_dst[tt] : (int32_t)tt;
@@ -239,11 +239,11 @@ __global__ void __launch_bounds__(kCopyThreads, 6) stream_kernel(const __grid_co
     const char *srow = row_base<kSrcHnd>(a.src, sp, a.src_planes[p], buf_plane, si, R);
     char *drow = const_cast<char *>(row_base<kDstHnd>(a.dst, dp, a.dst_planes[p], buf_plane, di, R));
 #pragma unroll 1
-    for (int32_t x0 = 0; x0 < vpr; x0 += kUnroll << lsh) {
+    for (int32_t x0 = 0; x0 < vpr; x0 += kUnroll * m) {
       uint4 v[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
-        const int32_t xv = x0 + li + (u << lsh);
+        const int32_t xv = x0 + li + u * m;
         if (ok && xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
       }
       if (!verdict_ok) {
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kCopyThreads, 6) stream_kernel(const __grid_co
       }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
-        const int32_t xv = x0 + li + (u << lsh);
+        const int32_t xv = x0 + li + u * m;
         if (ok && xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), v[u]);
       }
     }
@@ -350,10 +350,10 @@ __device__ int32_t row_wait(const StreamCtl &k, int32_t l, bool owner) {
   }
 }
 
-// kTail: rows over 2 KiB (more than one pass of the warp), a separate instance as in the row
-// kernel so that the common instances keep every value in registers.
+// kTail: rows of more than kUnroll * m vectors (more than one pass of the warp), a separate
+// instance as in the row kernel so that the one-pass instances keep every value in registers.
 template <bool kSrcHnd, bool kDstHnd, bool kTail>
-__global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8)
+__global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 6 : 8)
     stream_row_kernel(const __grid_constant__ StreamArgs s) {
   __shared__ int32_t s_stop;  // 1: the CTA's layer moves, 0: it stopped
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the epilogue may queue
@@ -367,12 +367,13 @@ __global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8)
   const uint32_t r = i0 - (uint32_t)l * k.per_layer_pad + warp;
   const bool has = r < k.per_layer;
   const uint32_t rc = has ? r : 0;
-  const int32_t gsh = a.row_group_shift, lsh = 5 - gsh;
+  const int32_t m = a.row_lanes, G = a.rows_per_warp;  // lanes per token, tokens per warp
+  const int32_t rl = lane / m;
   const int32_t kv = rc >= k.groups ? 1 : 0;  // K or V (always 0 with one latent plane)
-  const int64_t t = ((int64_t)(rc - kv * k.groups) << gsh) + (lane >> lsh);
+  const int64_t t = (int64_t)(rc - kv * k.groups) * G + rl;
   const bool sp = a.src.is_pool != 0, dp = a.dst.is_pool != 0;
   // slot indices and their range checks go out before the wait
-  bool ok = has && t < a.n_tokens;
+  bool ok = has && rl < G && t < a.n_tokens;
   const int64_t tt = ok ? t : 0;
   const int32_t si = sp ? a.spec_src[tt] : (int32_t)tt;
   const int32_t di = dp ? a.spec_dst[tt] : (int32_t)tt;
@@ -396,14 +397,14 @@ __global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8)
   if (!s_stop) ok = false;
   const int32_t p = k.kv_planes * l + kv;
   const int32_t R = a.row_bytes, vpr = R >> 4;
-  const int32_t li = lane & ((1 << lsh) - 1);
+  const int32_t li = lane - rl * m;
   const char *buf_plane = a.buf + (int64_t)p * a.n_tokens * R;
   const char *srow = row_base<kSrcHnd>(a.src, sp, a.src_planes[p], buf_plane, si, R);
   char *drow = const_cast<char *>(row_base<kDstHnd>(a.dst, dp, a.dst_planes[p], buf_plane, di, R));
   uint4 v[kUnroll];
 #pragma unroll
   for (int u = 0; u < kUnroll; ++u) {
-    const int32_t xv = li + (u << lsh);
+    const int32_t xv = li + u * m;
     if (ok && xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
   }
   pdl_wait();  // the planner has checked every index and written status[0]
@@ -414,23 +415,22 @@ __global__ void __launch_bounds__(kCopyThreads, kTail ? 6 : 8)
     atomicMax(&a.status[1], k.layers - l);
     return;
   }
+  // the stores of each pass, then (kTail) the next pass's loads
+  const int32_t step = kUnroll * m;
+#pragma unroll 1
+  for (int32_t x0 = 0;;) {
 #pragma unroll
-  for (int u = 0; u < kUnroll; ++u) {
-    const int32_t xv = li + (u << lsh);
-    if (xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), v[u]);
-  }
-  if constexpr (kTail) {
-    for (int32_t x0 = kUnroll << lsh; x0 < vpr; x0 += kUnroll << lsh) {
+    for (int u = 0; u < kUnroll; ++u) {
+      const int32_t xv = x0 + li + u * m;
+      if (xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), v[u]);
+    }
+    if constexpr (!kTail) break;
+    x0 += step;
+    if (x0 >= vpr) break;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int32_t xv = x0 + li + (u << lsh);
-        if (xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int32_t xv = x0 + li + (u << lsh);
-        if (xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), v[u]);
-      }
+    for (int u = 0; u < kUnroll; ++u) {
+      const int32_t xv = x0 + li + u * m;
+      if (xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
     }
   }
 }
@@ -492,8 +492,8 @@ int stream_blocks_per_sm() {
   return e == cudaSuccess ? nb : 0;
 }
 
-void stream_sizes(StreamCtl &k, int64_t n_tokens, int32_t group_shift) {
-  const int64_t groups = (n_tokens + (1 << group_shift) - 1) >> group_shift;
+void stream_sizes(StreamCtl &k, int64_t n_tokens, int32_t rows_per_warp) {
+  const int64_t groups = (n_tokens + rows_per_warp - 1) / rows_per_warp;
   k.groups = (uint32_t)groups;
   k.per_layer = (uint32_t)(k.kv_planes * groups);
   k.items = (uint32_t)(k.kv_planes * groups * k.layers);
@@ -514,7 +514,7 @@ cudaError_t launch_stream_rows(const CopyArgs &c, const StreamCtl &k, cudaStream
   args.c = c;
   args.k = k;
   const bool sh = c.src.hnd && c.src.is_pool, dh = c.dst.hnd && c.dst.is_pool;
-  const bool tail = c.row_bytes > kUnroll * 32 * 16;
+  const bool tail = (c.row_bytes >> 4) > kUnroll * c.row_lanes;  // more than one pass
   const void *fn = tail ? stream_row_fn_of<true>(sh, dh) : stream_row_fn_of<false>(sh, dh);
   void *params[] = {&args};
   cudaError_t e = cudaSuccess;
