@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
     s_stop = go;
   }
   __syncthreads();  // thread 0's acquire of the layer orders every thread's row loads
-  if (!s_stop) ok = false;
+  if (!s_stop) return;  // stopped: this CTA writes nothing, so it need not wait for the planner
   const int32_t p = k.kv_planes * l + kv;
   const int32_t R = a.row_bytes, vpr = R >> 4;
   const int32_t li = lane - rl * m;
