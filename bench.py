@@ -261,6 +261,47 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(step_ms)
 
+    # ---- steady state without the flush: inputs larger than L2 (288 MiB each way per step),
+    # consecutive steps moving two different sets of random rows in turn, so that no step finds
+    # its rows in L2 and no flush buffer's dirty lines are written back inside a step ----
+    s2 = torch.from_numpy(inputs.distinct_slots(inputs.rng(2, 100 + inputs.ROLE_SRC_SLOTS), N_TOK, NS)).to(dev)
+    d2 = torch.from_numpy(inputs.distinct_slots(inputs.rng(2, 100 + inputs.ROLE_DST_SLOTS), N_TOK, NS)).to(dev)
+    sets = [(s_dev, d_dev), (s2, d2)]
+    ev4 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for i in range(K + 2):
+            if i >= 2:
+                ev4[i - 2][0].record(stream)
+            ss, dd = sets[i & 1]
+            kvx.transfer(src_l, ss, dst_l, dd, N_TOK, ws, st, stream=sptr)
+            if i >= 2:
+                ev4[i - 2][1].record(stream)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvx.OK
+    noflush_ms = statistics.mean(a.elapsed_time(b) for a, b in ev4)
+
+    # ---- the same step captured once into a CUDA graph and replayed (same flushes) ----
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+    torch.cuda.synchronize()
+    ev5 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for i in range(K + 3):
+            flush.fill_(i & 0xFF)
+            if i >= 3:
+                ev5[i - 3][0].record(stream)
+            graph.replay()
+            if i >= 3:
+                ev5[i - 3][1].record(stream)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvx.OK
+    graph_ms = statistics.mean(a.elapsed_time(b) for a, b in ev5)
+    del graph
+
     # ---- the copy kernel alone (plan and copy launched separately, same flushes) ----
     ev3 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
     with torch.cuda.stream(stream):
@@ -305,7 +346,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     total_ms = max_over_ranks(total_ms, device=dev)
     return dict(step_ms=step_ms, total_ms=total_ms, plan_ms=plan_ms, copy_ms=copy_ms, e2e=e2e,
-                clocks=clk, device=torch.cuda.get_device_name(dev))
+                clocks=clk, device=torch.cuda.get_device_name(dev), noflush_ms=noflush_ms,
+                graph_ms=graph_ms)
 
 
 # ---------------------------------------------------------------------------------------
@@ -1251,6 +1293,18 @@ def main():
                    "frac_of_nominal_8tbs": value / NOMINAL_HBM_GBS,
                    "plan_us": res["plan_ms"] * 1e3, "copy_us": res["copy_ms"] * 1e3,
                    "l2": "flushed before every timed step (write of 2x L2, outside the events)",
+                   "steady_state_no_flush": {
+                       "us_per_request": res["noflush_ms"] * 1e3,
+                       "GBs": alg_bytes(N_TOK) / (res["noflush_ms"] * 1e-3) / 1e9,
+                       "frac_of_measured_hbm": alg_bytes(N_TOK) / (res["noflush_ms"] * 1e-3)
+                       / 1e9 / hbm,
+                       "how": "back-to-back requests, no flush: inputs larger than L2 (288 MiB "
+                              "each way per step), two sets of random slot lists in turn"},
+                   "cuda_graph_replay": {
+                       "us_per_request": res["graph_ms"] * 1e3,
+                       "GBs": alg_bytes(N_TOK) / (res["graph_ms"] * 1e-3) / 1e9,
+                       "how": "the one kvx_transfer call (planner + copy) captured once into a "
+                              "CUDA graph and replayed each step, L2 flushed as above"},
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "duplicate_check": bool(args.check_duplicates),
                    "device": res["device"]},
