@@ -80,6 +80,9 @@ def parse_args():
                          "every destination slot for repeats)")
     ap.add_argument("--layer-us", type=float, default=100.0,
                     help="--workload stream: host cadence of the emulated producer, us/layer")
+    ap.add_argument("--device-only", action="store_true",
+                    help="--workload stream: only the device-timed parts (no host-raised "
+                         "layers, no cancellation trials), e.g. for a profiler")
     return ap.parse_args()
 
 
@@ -1076,7 +1079,7 @@ def run_stream(args):
 
     # (2) layers raised by the host at a fixed cadence; (3) the move started after the last one
     cadence = args.layer_us * 1e-6
-    trials = 30
+    trials = 0 if args.device_only else 30
 
     def wait_done(t_from):
         while int(done[0]) == 0 and time.perf_counter() < t_from + 2.0:
@@ -1137,6 +1140,8 @@ def run_stream(args):
         pending.append(s_[1])
 
     def pct(xs):
+        if not xs:
+            return None
         xs = sorted(xs)
         return {"median": xs[len(xs) // 2], "p10": xs[len(xs) // 10], "p90": xs[(9 * len(xs)) // 10]}
 
@@ -1158,8 +1163,8 @@ def run_stream(args):
         "all_ready_request_epoch_checked_us": epoch_ms * 1e3,
         "all_ready_page_owners_checked_us": pages_ms * 1e3,
         "cancel_to_no_further_write_us": pct(cancels),
-        "cancel_layers_pending": {"min": min(pending), "max": max(pending),
-                                  "of": L, "raised_before_cancel": L // 2},
+        "cancel_layers_pending": ({"min": min(pending), "max": max(pending),
+                                   "of": L, "raised_before_cancel": L // 2} if pending else None),
         "streamed_tail_us": pct(tails),
         "unstreamed_us": pct(unstreamed),
         "producer": f"host raises one layer every {args.layer_us:g} us into pinned ready words; "
