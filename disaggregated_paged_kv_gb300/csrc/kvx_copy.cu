@@ -20,6 +20,7 @@
 #include <atomic>
 
 #include "kvx_copy_ops.cuh"
+#include "kvx_launch.cuh"
 
 namespace kvx {
 namespace {
@@ -541,26 +542,10 @@ int variant_blocks_per_sm(CopyVariant v, int32_t n_tiles) {
 cudaError_t launch_copy(const CopyArgs &a, int grid, cudaStream_t s) {
   const int32_t nt = (int32_t)num_tiles(a.n_tokens);
   const CopyVariant v = copy_variant(a);
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(variant_threads(v));
-  cfg.dynamicSmemBytes = variant_smem(v, nt);
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   void *args[] = {const_cast<CopyArgs *>(&a)};
   const void *fn = v == kVariantRow ? row_fn(a) : variant_fn(v);
-  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
-  if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) {
-    // programmatic dependent launch refused on this stream: launch in plain stream order
-    (void)cudaGetLastError();
-    cfg.numAttrs = 0;
-    e = cudaLaunchKernelExC(&cfg, fn, args);
-  }
-  return e;
+  return launch_pdl(fn, dim3((unsigned)grid), dim3(variant_threads(v)), args, s,
+                    variant_smem(v, nt));
 }
 
 }  // namespace kvx

@@ -5,9 +5,11 @@
 
 namespace kvx {
 
-// Launches fn with programmatic stream serialization: the kernel may start while its
-// predecessor on the stream drains, and orders itself after it with griddepcontrol.wait.
-// Where the attribute is refused, the kernel is launched in plain stream order.
-cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, void **args, cudaStream_t s);
+// Launches fn (smem bytes of dynamic shared memory) with programmatic stream serialization:
+// the kernel may start while its predecessor on the stream drains, and orders itself after it
+// with griddepcontrol.wait.  Where the attribute is refused, the kernel is launched in plain
+// stream order.
+cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, void **args, cudaStream_t s,
+                       size_t smem = 0);
 
 }  // namespace kvx

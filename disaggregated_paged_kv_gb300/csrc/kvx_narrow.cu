@@ -12,6 +12,7 @@
 // before the planner's verdict; plans (one row per chunk, including a batch's request
 // records, lane by lane) are read after the planner.
 #include "kvx_copy_ops.cuh"
+#include "kvx_launch.cuh"
 
 namespace kvx {
 namespace {
@@ -150,23 +151,8 @@ cudaError_t launch_narrow(const CopyArgs &a, cudaStream_t s) {
   const int64_t groups = (a.n_tokens + (1 << a.row_group_shift) - 1) >> a.row_group_shift;
   const int64_t warps = groups * a.planes;
   const int64_t grid = (warps + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kCopyThreads);
-  cfg.stream = s;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr.val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
   void *args[] = {const_cast<CopyArgs *>(&a)};
-  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
-  if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) {
-    (void)cudaGetLastError();  // no programmatic dependent launch here: plain stream order
-    cfg.numAttrs = 0;
-    e = cudaLaunchKernelExC(&cfg, fn, args);
-  }
-  return e;
+  return launch_pdl(fn, dim3((unsigned)grid), dim3(kCopyThreads), args, s);
 }
 
 }  // namespace kvx

@@ -40,6 +40,7 @@
 // wait_ns of %globaltimer and an iteration cap.  Waits only ever poll memory that the host or
 // another engine writes: no CTA waits for another CTA or another kernel.
 #include "kvx_copy_ops.cuh"
+#include "kvx_launch.cuh"
 
 namespace kvx {
 namespace {
@@ -456,25 +457,6 @@ const void *stream_row_fn_of(bool sh, bool dh) {
   return reinterpret_cast<const void *>(stream_row_kernel<false, false, kTail>);
 }
 
-cudaError_t launch_pdl_ex(const void *fn, unsigned grid, unsigned block, void **params,
-                          cudaStream_t st) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(block);
-  cfg.stream = st;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr.val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, params);
-  if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) {
-    (void)cudaGetLastError();  // no programmatic dependent launch here: plain stream order
-    cfg.numAttrs = 0;
-    e = cudaLaunchKernelExC(&cfg, fn, params);
-  }
-  return e;
-}
 
 const void *stream_fn(bool sh, bool dh) {
   if (sh && dh) return reinterpret_cast<const void *>(stream_kernel<true, true>);
@@ -506,7 +488,7 @@ cudaError_t launch_stream(const CopyArgs &c, const StreamCtl &k, int grid, cudaS
   args.k = k;
   const bool sh = c.src.hnd && c.src.is_pool, dh = c.dst.hnd && c.dst.is_pool;
   void *params[] = {&args};
-  return launch_pdl_ex(stream_fn(sh, dh), (unsigned)grid, kCopyThreads, params, s);
+  return launch_pdl(stream_fn(sh, dh), dim3((unsigned)grid), dim3(kCopyThreads), params, s);
 }
 
 cudaError_t launch_stream_rows(const CopyArgs &c, const StreamCtl &k, cudaStream_t s) {
@@ -519,13 +501,13 @@ cudaError_t launch_stream_rows(const CopyArgs &c, const StreamCtl &k, cudaStream
   void *params[] = {&args};
   cudaError_t e = cudaSuccess;
   if (k.items > 0) {
-    e = launch_pdl_ex(fn, k.per_layer_pad / kWarps * k.layers, kCopyThreads, params, s);
+    e = launch_pdl(fn, dim3(k.per_layer_pad / kWarps * k.layers), dim3(kCopyThreads), params, s);
     if (e != cudaSuccess) return e;
   }
   int32_t *status = c.status, *done = k.host_done;
   int32_t layers = k.layers;
   void *dparams[] = {&status, &done, &layers};
-  return launch_pdl_ex(reinterpret_cast<const void *>(stream_done_kernel), 1, 1, dparams, s);
+  return launch_pdl(reinterpret_cast<const void *>(stream_done_kernel), dim3(1), dim3(1), dparams, s);
 }
 
 }  // namespace kvx

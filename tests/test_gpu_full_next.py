@@ -135,6 +135,48 @@ def test_tp_reshard_full_size():
         assert torch.equal(_changed(d_pools[dr], NS), want), f"D rank {dr}: other rows changed"
 
 
+def test_reshard_one_call_full_size():
+    """The headline request resharded from P TP 8 (eight 1-head HND pools, page 16) to D TP 1
+    (one 8-head token-row pool) in one kvx_reshard call with the kvx_tp_plan plan, as the
+    bench's tp workload times it: sampled rows against the oracle's kvxo_reshard of the same
+    parts on the sampled source rows, exact changed-row mask."""
+    NS = 32768
+    p_pools = [_pool((P, NS // 16, 1, 16, D), "normal", inputs.seed(2, 0) + r) for r in range(8)]
+    d_pool = _pool((P, NS, H, D), "sentinel")
+    pls = [kvx.Layout(L, 1, D, kvx.BF16, NS, kind=kvx.HND_PAGED, page_size=16, base=t,
+                      plane_stride=NS * D * 2) for t in p_pools]
+    dl = kvx.Layout(L, H, D, kvx.BF16, NS, base=d_pool, plane_stride=NS * R)
+    parts = kvx.tp_plan(H, 8, 1)
+    assert parts == [(r, 0, 0, r, 1) for r in range(8)]
+    s = inputs.distinct_slots(inputs.rng(2, inputs.ROLE_SRC_SLOTS), N, NS)
+    d = inputs.distinct_slots(inputs.rng(2, inputs.ROLE_DST_SLOTS), N, NS)
+    s_d, d_d = torch.from_numpy(s).cuda(), torch.from_numpy(d).cuda()
+    ws = torch.empty(kvx.workspace_size(N), dtype=torch.uint8, device="cuda")
+    st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    kvx.reshard(pls, s_d, [dl], d_d, parts, N, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvx.OK
+    samp = _sample(N, 126, 13)
+    m = len(samp)
+    spage = torch.from_numpy(s[samp] // 16).long().cuda()
+    soff = torch.from_numpy(s[samp] % 16).long().cuda()
+    minis = []
+    for t in p_pools:  # the sampled tokens' source rows, [P][m][1][D] per P rank
+        minis.append(np.ascontiguousarray(_host(t[:, spage, :, soff]).transpose(1, 0, 2, 3)))
+    srcs = [oracle.Pool(L, 1, D, 2, oracle.TOKEN_ROWS, m, [(x, p * m * D * 2) for p in range(P)],
+                        D * 2) for x in minis]
+    dst_host = np.full((P, m, H, D), SENT, dtype=np.uint16)
+    dst = oracle.Pool(L, H, D, 2, oracle.TOKEN_ROWS, m, [(dst_host, p * m * R) for p in range(P)],
+                      R)
+    rc, _ = oracle.reshard(srcs, np.arange(m), [dst], np.arange(m), parts, m)
+    assert rc == oracle.OK
+    got = _host(d_pool[:, torch.from_numpy(d[samp]).long().cuda()])
+    assert np.array_equal(got, dst_host), "sampled rows differ from the oracle"
+    want = torch.zeros((P, NS), dtype=torch.bool, device="cuda")
+    want[:, d_d.long()] = True
+    assert torch.equal(_changed(d_pool, NS), want), "other rows changed"
+
+
 @pytest.mark.parametrize("elem", [2, 1], ids=["bf16", "fp8"])
 def test_mla_full_size(elem):
     """DeepSeek-V2-Lite-shaped latent rows (27 planes x 576 elements), 16,384 tokens, the
