@@ -533,7 +533,8 @@ def run_workload(args, cfg: int):
         line["cuda_graph"] = {"us_per_step": gf, "value": total_bytes / (gf * 1e-6) / 1e9,
                               "warm_l2_us_per_step": gw,
                               "warm_l2_value": total_bytes / (gw * 1e-6) / 1e9,
-                              "how": "both legs (4 kernel launches) captured once, replayed"}
+                              "how": "both legs captured once (one launch each: requests of up to 512 "
+                                     "tokens skip the planner), replayed"}
     print(json.dumps(line), flush=True)
 
 

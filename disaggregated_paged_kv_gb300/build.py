@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libkvx.so")
 SOURCES = ["kvx_api.cu", "kvx_plan.cu", "kvx_copy.cu", "kvx_fused.cu", "kvx_noalloc.cu",
-           "kvx_stream.cu", "kvx_narrow.cu", "kvx_reshard.cu"]
+           "kvx_stream.cu", "kvx_narrow.cu", "kvx_reshard.cu", "kvx_small.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -665,6 +665,21 @@ static kvx_status run_call(const Call &c, const int32_t *d_src_slots, const int3
   // path; the rest take the planner + row kernel (the row kernel overlaps the planner).
   const bool fused = call_chunk_rows(c) > 1 && !dup_check(c) &&
                      n <= g_fused_max.load(std::memory_order_relaxed);
+  // small requests: one launch whose every CTA checks every index (no planner), unless the
+  // duplicate check or the bulk engine was asked for
+  const bool small = n > 0 && n <= kvx::kSmallMaxTokens && !fused && !dup_check(c) &&
+                     c.vec == 16 && kvx_get_copy_engine() != KVX_ENGINE_BULK;
+  if (small) {
+    static thread_local kvx::CopyArgs a;  // ~4 KiB of plane pointers: keep it off the stack
+    fill_copy_args(a, c, nullptr, d_buf, d_ws, d_status);
+    a.spec_src = c.src ? d_src_slots : nullptr;
+    a.spec_dst = c.dst ? d_dst_slots : nullptr;
+    a.host_status = host_status;
+    if (host_status_written) *host_status_written = host_status != nullptr;
+    kvx::row_shape(a, &a.row_lanes, &a.rows_per_warp);
+    const cudaError_t e = kvx::launch_small(a, s);
+    return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+  }
   if (n == 0 || !fused) {
     kvx::PlanArgs a = plan_args(c, d_ws, d_status);
     a.src_idx = d_src_slots;

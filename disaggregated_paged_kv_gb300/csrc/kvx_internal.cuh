@@ -245,6 +245,9 @@ void record_cuda_error(cudaError_t e);
 cudaError_t launch_narrow(const CopyArgs &a, cudaStream_t s);
 // log2 of the tokens one warp of the narrow kernel moves (CopyArgs::row_group_shift).
 int32_t narrow_group_shift(int32_t row_bytes, int32_t vec_bytes);
+// One-launch path of small one-shot requests (kvx_small.cu): every CTA checks every index.
+constexpr int32_t kSmallMaxTokens = 512;
+cudaError_t launch_small(const CopyArgs &a, cudaStream_t s);
 // Layer-streamed copy (kvx_stream.cu): persistent grid over layer-major row groups.
 int stream_blocks_per_sm();
 void stream_sizes(StreamCtl &k, int64_t n_tokens, int32_t rows_per_warp);

@@ -175,8 +175,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   __shared__ int32_t s_coff[kTile + 1];
   __shared__ int32_t s_warp[kPlanThreads / 32];
 
+  // the kernel before (the prefix kernel, or whatever the caller ran last) must be complete
+  // before the kernels behind may start: they read slot lists and rows before they wait
+  pdl_wait();
   pdl_trigger();
-  pdl_wait();  // the prefix kernel (runs / batch) must be complete
 
   const int tile = blockIdx.x;
   const int64_t t0 = (int64_t)tile * kTile;
@@ -366,8 +368,8 @@ __device__ __forceinline__ int32_t check_request(const PlanArgs &a, const kvx_re
 __global__ void __launch_bounds__(kPrefixThreads) prefix_kernel(const __grid_constant__ PlanArgs a) {
   __shared__ int64_t s_warp64[kPrefixThreads / 32];
   __shared__ int32_t s_warp32[kPrefixThreads / 32];
+  pdl_wait();  // the caller's last kernel is complete before the planner behind may start
   pdl_trigger();
-  pdl_wait();
   int64_t *pre = reinterpret_cast<int64_t *>(a.ws + a.L.prefix_off);
   const int tid = threadIdx.x;
   int64_t carry = 0;
