@@ -955,6 +955,21 @@ def run_tp(args):
                 step_one()
         ms_one = timed(step_one)
         assert int(st.item()) == kvx.OK
+
+        # the same plan layer-streamed (kvx_stream_reshard), every layer's ready word raised
+        words = torch.ones(L, dtype=torch.int32, device=dev)
+        st4 = torch.zeros(4, dtype=torch.int32, device=dev)
+
+        def step_streamed():
+            kvx.stream_reshard(p_l, s_dev, d_l, d_dev, plan, N_TOK, ws, st4, layer_ready=words,
+                               ready_value=1, stream=sp)
+
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                flush.fill_(1)
+                step_streamed()
+        ms_streamed = timed(step_streamed)
+        assert st4.tolist() == [kvx.OK, 0, 0, 1], st4.tolist()
         alg = alg_bytes(N_TOK) + 8 * N_TOK * (len(plan) - 1)  # every pair reads both lists
         gbs = alg / (ms * 1e-3) / 1e9
         gbs_one = alg_bytes(N_TOK) / (ms_one * 1e-3) / 1e9
@@ -965,6 +980,7 @@ def run_tp(args):
             "us_per_reshard_one_stream": ms_serial * 1e3,
             "us_per_reshard_one_call": ms_one * 1e3, "GBs_one_call": gbs_one,
             "frac_of_measured_hbm_one_call": gbs_one / float(peaks["hbm_gbs"]),
+            "us_per_reshard_streamed_all_ready": ms_streamed * 1e3,
             "slice_bytes": plan[0][4] * D * 2}
         del p_pools, d_pools, p_l, d_l
         torch.cuda.empty_cache()

@@ -872,25 +872,15 @@ static const void *device_word(const void *p, bool *in_device_memory = nullptr) 
   return nullptr;
 }
 
-kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, kvx_layout_t dst,
-                      const int32_t *d_dst_slots, int32_t n, void *d_buf, size_t buf_bytes,
-                      const kvx_stream_ctl *ctl, void *d_ws, size_t ws_bytes, int32_t *d_status,
-                      kvx_stream_t stream) {
-  if (op < KVX_OP_GATHER || op > KVX_OP_TRANSFER || !valid_n(n)) return KVX_ERR_INVALID_ARG;
+// The device form of a kvx_stream_ctl for a move of op over layouts shaped like shape (the
+// fields every streamed move shares); KVX_ERR_INVALID_ARG for a malformed control block.
+static kvx_status stream_ctl_of(const kvx_stream_ctl *ctl, int32_t op, const kvx_layout *shape,
+                                kvx::StreamCtl *out) {
   if (!ctl || ctl->wait_ns < 1 || ctl->wait_ns > KVX_MAX_WAIT_NS || ctl->max_ctas < 0 ||
       ctl->reserved != 0 || ctl->reserved2 != 0)
     return KVX_ERR_INVALID_ARG;
   if (ctl->dst_page_epochs && (op == KVX_OP_GATHER || ctl->epoch_page < 1))
     return KVX_ERR_INVALID_ARG;
-  if (!d_status || !aligned(d_status, 16)) return KVX_ERR_INVALID_ARG;
-  Call c;
-  c.op = op;
-  c.n_tokens = n;
-  kvx_status st = bind_layouts(c, src, dst);
-  if (st == KVX_OK) st = check_buffer(c, d_buf, buf_bytes);
-  if (st != KVX_OK) return st;
-  if (c.vec < 16) return KVX_ERR_ALIGNMENT;  // the streamed kernels move 16-byte vectors
-  const int32_t layers = c.shape->num_layers;
   kvx::StreamCtl k = {};
   bool ready_local = false, epoch_local = false;
   k.layer_ready = static_cast<const int32_t *>(device_word(ctl->layer_ready, &ready_local));
@@ -907,8 +897,27 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
   k.wait_ns = ctl->wait_ns;
   k.ready_value = ctl->ready_value;
   k.epoch = ctl->epoch;
-  k.layers = layers;
-  k.kv_planes = c.shape->kv_planes;
+  k.layers = shape->num_layers;
+  k.kv_planes = shape->kv_planes;
+  *out = k;
+  return KVX_OK;
+}
+
+kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, kvx_layout_t dst,
+                      const int32_t *d_dst_slots, int32_t n, void *d_buf, size_t buf_bytes,
+                      const kvx_stream_ctl *ctl, void *d_ws, size_t ws_bytes, int32_t *d_status,
+                      kvx_stream_t stream) {
+  if (op < KVX_OP_GATHER || op > KVX_OP_TRANSFER || !valid_n(n)) return KVX_ERR_INVALID_ARG;
+  if (!d_status || !aligned(d_status, 16)) return KVX_ERR_INVALID_ARG;
+  Call c;
+  c.op = op;
+  c.n_tokens = n;
+  kvx_status st = bind_layouts(c, src, dst);
+  if (st == KVX_OK) st = check_buffer(c, d_buf, buf_bytes);
+  if (st != KVX_OK) return st;
+  if (c.vec < 16) return KVX_ERR_ALIGNMENT;  // the streamed kernels move 16-byte vectors
+  kvx::StreamCtl k = {};
+  if ((st = stream_ctl_of(ctl, op, c.shape, &k)) != KVX_OK) return st;
   if (n > 0) {
     if (c.src && (!d_src_slots || !aligned(d_src_slots, 4))) return KVX_ERR_INVALID_ARG;
     if (c.dst && (!d_dst_slots || !aligned(d_dst_slots, 4))) return KVX_ERR_INVALID_ARG;
@@ -1089,13 +1098,16 @@ static bool reshard_layout(kvx::ReshardCall &rc, int32_t idx, const kvx_layout *
   return true;
 }
 
-kvx_status kvx_reshard(const kvx_layout_t *srcs, int32_t n_srcs, const int32_t *d_src_slots,
-                       const kvx_layout_t *dsts, int32_t n_dsts, const int32_t *d_dst_slots,
-                       const kvx_head_part *parts, int32_t n_parts, int32_t n, void *d_ws,
-                       size_t ws_bytes, int32_t *d_status, kvx_stream_t stream) {
+// Every host-side check of a reshard, and its device form in rc (the call's Call in c); the
+// planner and the copy are not enqueued.
+static kvx_status prepare_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
+                                  const int32_t *d_src_slots, const kvx_layout_t *dsts,
+                                  int32_t n_dsts, const int32_t *d_dst_slots,
+                                  const kvx_head_part *parts, int32_t n_parts, int32_t n,
+                                  void *d_ws, size_t ws_bytes, Call &c, kvx::ReshardCall &rc) {
   if (!srcs || !dsts || !parts || n_srcs < 1 || n_dsts < 1 ||
       n_srcs + n_dsts > KVX_RESHARD_MAX_LAYOUTS || n_parts < 1 ||
-      n_parts > KVX_RESHARD_MAX_PARTS || !valid_n(n) || !d_status || !aligned(d_status, 4))
+      n_parts > KVX_RESHARD_MAX_PARTS || !valid_n(n))
     return KVX_ERR_INVALID_ARG;
   const kvx_layout *s0 = srcs[0], *d0 = dsts[0];
   if (!s0 || !d0) return KVX_ERR_INVALID_ARG;
@@ -1126,7 +1138,6 @@ kvx_status kvx_reshard(const kvx_layout_t *srcs, int32_t n_srcs, const int32_t *
     for (int32_t m = 0; m < k; ++m)
       if (layouts_overlap(dsts[m], dsts[k])) return KVX_ERR_OVERLAP;
   }
-  Call c;
   c.op = KVX_OP_TRANSFER;
   c.n_tokens = n;
   c.src = s0;
@@ -1145,7 +1156,6 @@ kvx_status kvx_reshard(const kvx_layout_t *srcs, int32_t n_srcs, const int32_t *
   }
   if (vec < 16) return KVX_ERR_ALIGNMENT;
   c.vec = 16;
-  static thread_local kvx::ReshardCall rc;  // ~30 KB: keep it off the stack
   std::memset(&rc, 0, sizeof(rc));
   for (int32_t k = 0; k < n_srcs; ++k)
     if (!reshard_layout(rc, k, srcs[k])) return KVX_ERR_INVALID_ARG;
@@ -1161,6 +1171,27 @@ kvx_status kvx_reshard(const kvx_layout_t *srcs, int32_t n_srcs, const int32_t *
       return KVX_ERR_INVALID_ARG;
     if ((st = check_ws(d_ws, ws_bytes, slots_ws(c))) != KVX_OK) return st;
   }
+  rc.n_tokens = n;
+  rc.planes = c.planes;
+  rc.n_parts = n_parts;
+  rc.row_bytes = (int32_t)c.row_bytes;
+  rc.src = pool_side(s0);
+  rc.dst = pool_side(d0);
+  rc.src_slots = d_src_slots;
+  rc.dst_slots = d_dst_slots;
+  return KVX_OK;
+}
+
+kvx_status kvx_reshard(const kvx_layout_t *srcs, int32_t n_srcs, const int32_t *d_src_slots,
+                       const kvx_layout_t *dsts, int32_t n_dsts, const int32_t *d_dst_slots,
+                       const kvx_head_part *parts, int32_t n_parts, int32_t n, void *d_ws,
+                       size_t ws_bytes, int32_t *d_status, kvx_stream_t stream) {
+  if (!d_status || !aligned(d_status, 4)) return KVX_ERR_INVALID_ARG;
+  Call c;
+  static thread_local kvx::ReshardCall rc;  // ~30 KB: keep it off the stack
+  kvx_status st = prepare_reshard(srcs, n_srcs, d_src_slots, dsts, n_dsts, d_dst_slots, parts,
+                                  n_parts, n, d_ws, ws_bytes, c, rc);
+  if (st != KVX_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (n == 0) {
@@ -1184,16 +1215,54 @@ kvx_status kvx_reshard(const kvx_layout_t *srcs, int32_t n_srcs, const int32_t *
   }
   e = kvx::launch_plan(pa, s);
   if (e != cudaSuccess) return cuda_fail(e);
-  rc.n_tokens = n;
-  rc.planes = c.planes;
-  rc.n_parts = n_parts;
-  rc.row_bytes = (int32_t)c.row_bytes;
-  rc.src = pool_side(s0);
-  rc.dst = pool_side(d0);
   rc.status = d_status;
-  rc.src_slots = d_src_slots;
-  rc.dst_slots = d_dst_slots;
   e = kvx::launch_reshard(rc, s);
+  return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+}
+
+kvx_status kvx_stream_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
+                              const int32_t *d_src_slots, const kvx_layout_t *dsts,
+                              int32_t n_dsts, const int32_t *d_dst_slots,
+                              const kvx_head_part *parts, int32_t n_parts, int32_t n,
+                              const kvx_stream_ctl *ctl, void *d_ws, size_t ws_bytes,
+                              int32_t *d_status, kvx_stream_t stream) {
+  if (!d_status || !aligned(d_status, 16)) return KVX_ERR_INVALID_ARG;
+  if (ctl && ctl->max_ctas != 0) return KVX_ERR_INVALID_ARG;  // the row grid only
+  Call c;
+  static thread_local kvx::ReshardCall rc;  // ~30 KB: keep it off the stack
+  kvx_status st = prepare_reshard(srcs, n_srcs, d_src_slots, dsts, n_dsts, d_dst_slots, parts,
+                                  n_parts, n, d_ws, ws_bytes, c, rc);
+  if (st != KVX_OK) return st;
+  kvx::StreamCtl k = {};
+  if ((st = stream_ctl_of(ctl, KVX_OP_TRANSFER, c.shape, &k)) != KVX_OK) return st;
+  if (!kvx::reshard_stream_fits(rc, k)) return KVX_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  // status[0..3]: verdict, layers pending, stop code, done; as kvx_stream
+  const bool direct = n > 0 && kvx::num_tiles(n) == 1;
+  if (!direct) {
+    e = cudaMemsetAsync(d_status, 0, 4 * sizeof(int32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (n > 0) {
+    kvx::PlanArgs pa = plan_args(c, d_ws, d_status);
+    pa.src_idx = d_src_slots;
+    pa.dst_idx = d_dst_slots;
+    pa.validate_only = 1;
+    if (direct) pa.status_direct = 4;
+    if (pa.dup_table) {
+      e = cudaMemsetAsync(pa.dup_table, 0, sizeof(uint32_t) * ((size_t)pa.dup_mask + 1), s);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    e = kvx::launch_plan(pa, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    // the mirror lives where a plan's chunk table would be (unused by a validate-only plan)
+    k.mirror = reinterpret_cast<uint64_t *>(static_cast<char *>(d_ws) +
+                                            kvx::ws_layout(n, 0, false).chunks_off);
+  }
+  k.gen = g_stream_gen.fetch_add(1, std::memory_order_relaxed);
+  rc.status = d_status;
+  e = kvx::launch_reshard_stream(rc, k, s);
   return e == cudaSuccess ? KVX_OK : cuda_fail(e);
 }
 
@@ -1244,6 +1313,6 @@ kvx_status kvx_set_check_duplicates(int32_t on) {
 
 int32_t kvx_get_check_duplicates(void) { return g_check_dup.load(std::memory_order_relaxed); }
 
-int32_t kvx_version(void) { return 202; }
+int32_t kvx_version(void) { return 203; }
 
 }  // extern "C"

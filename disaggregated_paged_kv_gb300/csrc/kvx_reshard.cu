@@ -8,15 +8,18 @@
 // planner checks the two slot lists once and one row grid moves every part of the plan.
 //
 // Warp w of grid row y moves G tokens of one (plane, part) pair with m lanes per token (the
-// row kernel's shape for the piece length, row_shape_for), parts fastest:
-// w = (q * P + p) * J + j for token group q, plane p, part j.  The J parts that fill one
-// destination row therefore run in neighbouring warps of one CTA, and the pieces of a row
-// reach L2 together.  Grid rows (blockIdx.y) of 4096 token groups keep w small.
+// row kernel's shape for the piece length, row_shape_for), parts fastest and planes slowest:
+// w = (p * Q + q) * J + j for plane p, token group q of the row's Q, part j.  The J parts
+// that fill one destination row run in neighbouring warps of one CTA, so the pieces of a row
+// reach L2 together, and the warps in flight at any time cover few planes (measured on a
+// TP 8 -> 1 reshard of 2048 tokens x 72 planes: 107.2 us against 111.5 us token-major).
+// Grid rows (blockIdx.y) of 4096 token groups keep w small.
 // As in the row kernel of kvx_copy.cu, each lane range-checks its token and issues its loads
 // before the planner's verdict, and stores only after it (all-or-nothing).
 #include "kvx_copy_ops.cuh"
 #include "kvx_launch.cuh"
 #include "kvx_reshard.cuh"
+#include "kvx_stream_ops.cuh"
 
 namespace kvx {
 namespace {
@@ -68,9 +71,9 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
   const uint32_t J = (uint32_t)a.n_parts, P = (uint32_t)a.planes;
   const uint32_t r = w / J;
   const int32_t j = (int32_t)(w - r * J);
-  const uint32_t qy = r / P;
-  const int32_t p = (int32_t)(r - qy * P);
-  if (qy >= a.groups_per_y) return;
+  const int32_t p = (int32_t)(r / a.groups_per_y);
+  const uint32_t qy = r - (uint32_t)p * a.groups_per_y;
+  if ((uint32_t)p >= P || qy >= a.groups_per_y) return;
   const int32_t m = a.lanes, G = a.rows;
   // n_tokens <= KVX_MAX_TOKENS (2^23): token indices fit in 32 bits
   const int32_t nt = (int32_t)a.n_tokens;
@@ -119,6 +122,143 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
   }
 }
 
+// ---- layer-streamed reshard ---------------------------------------------------------------
+// The grid of kvx_stream's row grid over (layer, K/V, token group, part): each layer's items
+// padded to whole CTAs, parts fastest within a layer; thread 0 of a CTA waits for the CTA's
+// layer (sops::row_wait: the producer's ready word, the request's epoch word, the tagged stop
+// word), the rows load once it may go on and store once the planner's verdict is in and, with
+// owner epochs, while the destination page still belongs to the request.  The epilogue of
+// kvx_stream follows the grid.
+
+template <int kPtrs>
+struct ReshardStreamArgs {
+  ReshardArgs<kPtrs> r;
+  StreamCtl k;
+};
+static_assert(sizeof(ReshardStreamArgs<kReshardMaxPtrs>) <= 32764, "parameters too large");
+
+constexpr int kRsWarps = kCopyThreads / 32;
+
+template <bool kSrcHnd, bool kDstHnd, bool kTail, int kPtrs>
+__global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 6 : 8)
+    reshard_stream_kernel(const __grid_constant__ ReshardStreamArgs<kPtrs> s) {
+  __shared__ int32_t s_go;  // 1: the CTA's layer moves, 0: it stopped
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the epilogue may queue
+  const ReshardArgs<kPtrs> &a = s.r;
+  const StreamCtl &k = s.k;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t i0 = blockIdx.x * kRsWarps;  // the CTA's first (padded) item
+  const int32_t l = (int32_t)(i0 / k.per_layer_pad);
+  const uint32_t r = i0 - (uint32_t)l * k.per_layer_pad + warp;
+  const bool has = r < k.per_layer;
+  const uint32_t rc = has ? r : 0;
+  const uint32_t J = (uint32_t)a.n_parts;
+  const uint32_t qq = rc / J;
+  const int32_t j = (int32_t)(rc - qq * J);
+  const int32_t kv = qq >= k.groups ? 1 : 0;  // K or V (always 0 with one latent plane)
+  const int32_t q = (int32_t)(qq - (uint32_t)kv * k.groups);
+  const int32_t m = a.lanes, G = a.rows;
+  const int32_t rl = lane / m, li = lane - rl * m;
+  const int32_t nt = (int32_t)a.n_tokens;
+  const int32_t t = q * G + rl;
+  bool ok = has && rl < G && t < nt;
+  const int32_t tt = ok ? t : 0;
+  const int32_t si = a.src_slots[tt], di = a.dst_slots[tt];
+  ok = ok && si >= 0 && (int64_t)si < a.src.num_slots && di >= 0 && (int64_t)di < a.dst.num_slots;
+  if (threadIdx.x == 0) {
+    int32_t go = 1;
+    if (k.layer_ready || k.epoch_word) {
+      const bool owner = blockIdx.x == (uint32_t)((uint64_t)l * k.per_layer_pad / kRsWarps);
+      const int32_t code = sops::row_wait(k, l, owner);
+      if (code) {
+        go = 0;
+        atomicMax(&a.status[2], code);
+        atomicMax(&a.status[1], k.layers - l);
+      }
+    }
+    s_go = go;
+  }
+  __syncthreads();  // thread 0's acquire of the layer orders every thread's row loads
+  if (!s_go) return;  // stopped: this CTA writes nothing
+  const int32_t p = k.kv_planes * l + kv;
+  const ReshardPart &pt = a.parts[j];
+  const int32_t R = a.row_bytes, vpr = R >> 4;
+  const char *srow =
+      row_base<kSrcHnd>(a.src, true, plane_addr(a, pt.src, p) + pt.src_off, nullptr, si, R);
+  uint4 v[kUnroll];
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const int32_t xv = li + u * m;
+    if (ok && xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, true, srow, xv << 4));
+  }
+  pdl_wait();  // the planner has checked both slot lists and written status[0]
+  if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK || !ok) return;
+  if (k.page_epochs && !sops::page_owned(k, di)) {
+    // the page went to another request: the row is dropped and reported
+    atomicMax(&a.status[2], (int32_t)KVX_ERR_CANCELLED);
+    atomicMax(&a.status[1], k.layers - l);
+    return;
+  }
+  char *drow = const_cast<char *>(row_base<kDstHnd>(
+      a.dst, true, plane_addr(a, a.parts[j].dst, p) + a.parts[j].dst_off, nullptr, di, R));
+  const int32_t step = kUnroll * m;
+#pragma unroll 1
+  for (int32_t x0 = 0;;) {
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int32_t xv = x0 + li + u * m;
+      if (xv < vpr)
+        st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, true, drow, xv << 4)), v[u]);
+    }
+    if constexpr (!kTail) break;
+    x0 += step;
+    if (x0 >= vpr) break;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int32_t xv = x0 + li + u * m;
+      if (xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, true, srow, xv << 4));
+    }
+  }
+}
+
+template <bool kTail, int kPtrs>
+const void *reshard_stream_fn(bool sh, bool dh) {
+  if (sh && dh) return reinterpret_cast<const void *>(reshard_stream_kernel<true, true, kTail, kPtrs>);
+  if (sh) return reinterpret_cast<const void *>(reshard_stream_kernel<true, false, kTail, kPtrs>);
+  if (dh) return reinterpret_cast<const void *>(reshard_stream_kernel<false, true, kTail, kPtrs>);
+  return reinterpret_cast<const void *>(reshard_stream_kernel<false, false, kTail, kPtrs>);
+}
+
+// Items of one layer of a streamed reshard (padded to whole CTAs), and the row shape.
+struct RsSizes {
+  int32_t m, G;
+  int64_t groups, per_layer, per_layer_pad;
+};
+
+RsSizes rs_sizes(const ReshardCall &c, const StreamCtl &k) {
+  RsSizes z;
+  row_shape_for(c.row_bytes, &z.m, &z.G);
+  z.groups = (c.n_tokens + z.G - 1) / z.G;
+  z.per_layer = (int64_t)k.kv_planes * z.groups * c.n_parts;
+  z.per_layer_pad = (z.per_layer + kRsWarps - 1) / kRsWarps * kRsWarps;
+  return z;
+}
+
+template <int kPtrs>
+cudaError_t launch_stream_with(const ReshardCall &c, const StreamCtl &k, const RsSizes &z,
+                               cudaStream_t s) {
+  static thread_local ReshardStreamArgs<kPtrs> args;  // up to ~29 KB: keep it off the stack
+  fill_args(args.r, c, z.m, z.G, 0);
+  args.k = k;
+  const bool sh = c.src.hnd != 0, dh = c.dst.hnd != 0;
+  const bool tail = (c.row_bytes >> 4) > kUnroll * z.m;
+  const void *fn = tail ? reshard_stream_fn<true, kPtrs>(sh, dh)
+                        : reshard_stream_fn<false, kPtrs>(sh, dh);
+  void *params[] = {&args};
+  return launch_pdl(fn, dim3((unsigned)(k.per_layer_pad / kRsWarps * k.layers)),
+                    dim3(kCopyThreads), params, s);
+}
+
 template <bool kTail, int kPtrs>
 const void *reshard_fn(bool sh, bool dh) {
   if (sh && dh) return reinterpret_cast<const void *>(reshard_kernel<true, true, kTail, kPtrs>);
@@ -128,9 +268,7 @@ const void *reshard_fn(bool sh, bool dh) {
 }
 
 template <int kPtrs>
-cudaError_t launch_with(const ReshardCall &c, int32_t m, int32_t G, uint32_t per_y, dim3 grid,
-                        cudaStream_t s) {
-  static thread_local ReshardArgs<kPtrs> a;  // up to ~29 KB: keep it off the stack
+void fill_args(ReshardArgs<kPtrs> &a, const ReshardCall &c, int32_t m, int32_t G, uint32_t per_y) {
   a.n_tokens = c.n_tokens;
   a.planes = c.planes;
   a.n_parts = c.n_parts;
@@ -150,6 +288,13 @@ cudaError_t launch_with(const ReshardCall &c, int32_t m, int32_t G, uint32_t per
   }
   for (int k = 0; k < KVX_RESHARD_MAX_PARTS; ++k) a.parts[k] = c.parts[k];
   for (int k = 0; k < kPtrs; ++k) a.ptrs[k] = k < c.n_ptrs ? c.ptrs[k] : nullptr;
+}
+
+template <int kPtrs>
+cudaError_t launch_with(const ReshardCall &c, int32_t m, int32_t G, uint32_t per_y, dim3 grid,
+                        cudaStream_t s) {
+  static thread_local ReshardArgs<kPtrs> a;  // up to ~29 KB: keep it off the stack
+  fill_args(a, c, m, G, per_y);
   const bool sh = c.src.hnd != 0, dh = c.dst.hnd != 0;
   const bool tail = (c.row_bytes >> 4) > kUnroll * m;  // more than one pass
   const void *fn = tail ? reshard_fn<true, kPtrs>(sh, dh) : reshard_fn<false, kPtrs>(sh, dh);
@@ -158,6 +303,25 @@ cudaError_t launch_with(const ReshardCall &c, int32_t m, int32_t G, uint32_t per
 }
 
 }  // namespace
+
+bool reshard_stream_fits(const ReshardCall &c, const StreamCtl &k) {
+  const RsSizes z = rs_sizes(c, k);
+  return z.per_layer_pad * k.layers <= (int64_t)0x7fffffff;  // 32-bit item indices
+}
+
+cudaError_t launch_reshard_stream(const ReshardCall &c, StreamCtl k, cudaStream_t s) {
+  const RsSizes z = rs_sizes(c, k);
+  k.groups = (uint32_t)z.groups;
+  k.per_layer = (uint32_t)z.per_layer;
+  k.per_layer_pad = (uint32_t)z.per_layer_pad;
+  k.items = (uint32_t)(z.per_layer * k.layers);
+  cudaError_t e = cudaSuccess;
+  if (c.n_tokens > 0)
+    e = c.n_ptrs > 0 ? launch_stream_with<kReshardMaxPtrs>(c, k, z, s)
+                     : launch_stream_with<0>(c, k, z, s);
+  if (e != cudaSuccess) return e;
+  return launch_stream_done(c.status, k.host_done, k.layers, s);
+}
 
 cudaError_t launch_reshard(const ReshardCall &c, cudaStream_t s) {
   // lanes per token and tokens per warp: the row kernel's shape for this piece length

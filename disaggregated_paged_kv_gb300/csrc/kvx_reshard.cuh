@@ -38,4 +38,10 @@ struct ReshardCall {
 // Enqueues the copy of a validated reshard behind its planner (programmatic dependent launch).
 cudaError_t launch_reshard(const ReshardCall &c, cudaStream_t s);
 
+// Layer-streamed reshard (kvx_stream_reshard): whether its layer-major grid fits 32-bit item
+// indices, and the grid plus its epilogue behind the validating planner.  k holds the parsed
+// control block, the mirror and its tag; the item counts are filled in here.
+bool reshard_stream_fits(const ReshardCall &c, const StreamCtl &k);
+cudaError_t launch_reshard_stream(const ReshardCall &c, StreamCtl k, cudaStream_t s);
+
 }  // namespace kvx

@@ -41,47 +41,19 @@
 // another engine writes: no CTA waits for another CTA or another kernel.
 #include "kvx_copy_ops.cuh"
 #include "kvx_launch.cuh"
+#include "kvx_stream_ops.cuh"
 
 namespace kvx {
 namespace {
 
 using namespace ops;
+using namespace sops;
 
 constexpr int kWarps = kCopyThreads / 32;
-constexpr uint32_t kMaxPolls = 1u << 24;  // backstop behind the %globaltimer bound
-constexpr uint32_t kMaxSleepNs = 1024;
-
 struct StreamArgs {
   CopyArgs c;   // sides, planes, buffer, status, slot lists (spec_src / spec_dst)
   StreamCtl k;
 };
-
-__device__ __forceinline__ int32_t ld_acquire_sys(const int32_t *p) {
-  int32_t v;
-  asm volatile("ld.acquire.sys.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ uint64_t ld_relaxed_gpu(const uint64_t *p) {
-  uint64_t v;
-  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ int32_t ld_relaxed_sys(const int32_t *p) {
-  int32_t v;
-  asm volatile("ld.relaxed.sys.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Whether destination slot di still belongs to the request (its page's owner epoch).
-__device__ __forceinline__ bool page_owned(const StreamCtl &k, int32_t di) {
-  return ld_relaxed_sys(k.page_epochs + di / k.epoch_page) == k.epoch;
-}
-
-__device__ __forceinline__ void st_release_sys(int32_t *p, int32_t v) {
-  asm volatile("st.release.sys.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 __device__ __forceinline__ int32_t ld_acquire_cta(const int32_t *smem) {
   int32_t v;
@@ -111,16 +83,6 @@ __device__ __forceinline__ bool known_ready(CtaState *cs, int32_t l) {
 
 __device__ __forceinline__ int32_t stopped_before(CtaState *cs, int32_t l) {
   return *reinterpret_cast<volatile int32_t *>(&cs->stop) <= l;
-}
-
-__device__ __forceinline__ uint64_t ld_acquire_gpu(const uint64_t *p) {
-  uint64_t v;
-  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_release_gpu(uint64_t *p, uint64_t v) {
-  asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ int32_t give_up(CtaState *cs, int32_t l, int32_t code) {
@@ -288,69 +250,6 @@ __global__ void __launch_bounds__(kCopyThreads, 5) stream_kernel(const __grid_co
 
 // ---- row grid ------------------------------------------------------------------------
 
-// The stop word (mirror[kStopWord]) of the row grid: gen ^ (code << 56 | layer << 40).  Any
-// value whose low 40 bits differ from gen's -- stale words of earlier calls, never-written
-// workspace -- decodes as "no stop".
-constexpr int kStopWord = 1 + KVX_MAX_PLANES / 2;
-
-struct Stop {
-  int32_t layer;  // first layer not to move
-  int32_t code;   // KVX_ERR_TIMEOUT / KVX_ERR_CANCELLED; 0: no stop
-};
-
-__device__ __forceinline__ Stop decode_stop(uint64_t v, uint64_t gen) {
-  const uint64_t d = v ^ gen;
-  Stop st = {0, 0};
-  if (d != 0 && (d & ((1ull << 40) - 1)) == 0) {
-    st.code = (int32_t)(d >> 56);
-    st.layer = (int32_t)((d >> 40) & 0xFFFF);
-  }
-  return st;
-}
-
-// Records a stop unless one is recorded already (the first one stays).
-__device__ __forceinline__ void publish_stop(const StreamCtl &k, uint64_t seen, int32_t layer,
-                                             int32_t code) {
-  const uint64_t v = k.gen ^ (((uint64_t)code << 56) | ((uint64_t)layer << 40));
-  atomicCAS(reinterpret_cast<unsigned long long *>(k.mirror + kStopWord),
-            (unsigned long long)seen, (unsigned long long)v);
-}
-
-// Thread 0 of a CTA: waits until layer l may move.  Returns 0 to go on, else the stop code.
-__device__ int32_t row_wait(const StreamCtl &k, int32_t l, bool owner) {
-  if (k.words_local) {  // one round trip: the epoch and the ready word together
-    const int32_t e = k.epoch_word ? ld_relaxed_sys(k.epoch_word) : k.epoch;
-    const bool ready = !k.layer_ready || ld_acquire_sys(k.layer_ready + l) >= k.ready_value;
-    if (e == k.epoch && ready) return 0;
-  }
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t sleep_ns = 32;
-  for (uint32_t it = 0;; ++it) {
-    const uint64_t sw = ld_relaxed_gpu(k.mirror + kStopWord);
-    const uint64_t m = ld_acquire_gpu(k.mirror + 1 + l);
-    const Stop st = decode_stop(sw, k.gen);
-    if (st.code && l >= st.layer) return st.code;
-    if (m == k.gen) return 0;
-    if (owner || it == 0 || (it & 15) == 15) {
-      const int32_t e = k.epoch_word ? ld_relaxed_sys(k.epoch_word) : k.epoch;
-      if (e != k.epoch) {  // cancelled: every layer not started is dropped
-        publish_stop(k, sw, 0, KVX_ERR_CANCELLED);
-        return KVX_ERR_CANCELLED;
-      }
-      if (!k.layer_ready || ld_acquire_sys(k.layer_ready + l) >= k.ready_value) {
-        st_release_gpu(k.mirror + 1 + l, k.gen);
-        return 0;
-      }
-    }
-    if (globaltimer_ns() - t0 >= (uint64_t)k.wait_ns || it >= kMaxPolls) {
-      publish_stop(k, sw, l, KVX_ERR_TIMEOUT);
-      return KVX_ERR_TIMEOUT;
-    }
-    __nanosleep(sleep_ns);
-    if (sleep_ns < kMaxSleepNs) sleep_ns <<= 1;
-  }
-}
-
 // kTail: rows of more than kUnroll * m vectors (more than one pass of the warp), a separate
 // instance as in the row kernel so that the one-pass instances keep every value in registers.
 template <bool kSrcHnd, bool kDstHnd, bool kTail>
@@ -504,9 +403,12 @@ cudaError_t launch_stream_rows(const CopyArgs &c, const StreamCtl &k, cudaStream
     e = launch_pdl(fn, dim3(k.per_layer_pad / kWarps * k.layers), dim3(kCopyThreads), params, s);
     if (e != cudaSuccess) return e;
   }
-  int32_t *status = c.status, *done = k.host_done;
-  int32_t layers = k.layers;
-  void *dparams[] = {&status, &done, &layers};
+  return launch_stream_done(c.status, k.host_done, k.layers, s);
+}
+
+cudaError_t launch_stream_done(int32_t *status, int32_t *host_done, int32_t layers,
+                               cudaStream_t s) {
+  void *dparams[] = {&status, &host_done, &layers};
   return launch_pdl(reinterpret_cast<const void *>(stream_done_kernel), dim3(1), dim3(1), dparams, s);
 }
 

@@ -154,6 +154,9 @@ _SIGS = {
                            ctypes.POINTER(_I32)]),
     "kvx_reshard": (_I32, [ctypes.POINTER(_VP), _I32, _VP, ctypes.POINTER(_VP), _I32, _VP,
                            ctypes.POINTER(HeadPart), _I32, _I32, _VP, _SZ, _VP, _VP]),
+    "kvx_stream_reshard": (_I32, [ctypes.POINTER(_VP), _I32, _VP, ctypes.POINTER(_VP), _I32, _VP,
+                                  ctypes.POINTER(HeadPart), _I32, _I32, ctypes.POINTER(StreamCtl),
+                                  _VP, _SZ, _VP, _VP]),
     "kvx_plan": (_I32, [_I32, _VP, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _VP]),
     "kvx_plan_runs": (_I32, [_I32, _VP, _VP, _VP, _I32, _I32, _VP, _SZ, _VP, _VP]),
     "kvx_plan_batch": (_I32, [_VP, _VP, _VP, _I32, _I64, _VP, _I64, _VP, _I64, _SZ, _VP, _SZ,
@@ -462,6 +465,17 @@ def stream(op: int, src: Optional[Layout], src_slots, dst: Optional[Layout], dst
     ``layer_ready[l] >= ready_value`` and stops when ``epoch_word`` no longer holds ``epoch``
     or a layer's wait exceeds ``wait_ns``.  ``status`` is a device int32[4] (verdict, layers
     pending, internal, done).  Control words may be device tensors or pinned host tensors."""
+    ctl = _stream_ctl(layer_ready, ready_value, epoch_word, epoch, wait_ns, max_ctas, host_done,
+                      dst_page_epochs, epoch_page)
+    rc = lib().kvx_stream(op, _h(src), _ptr(src_slots), _h(dst), _ptr(dst_slots), n, _ptr(buf),
+                          _nbytes(buf) if buf_bytes is None else buf_bytes, ctypes.byref(ctl),
+                          _ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
+                          _ptr(status), _stream(stream))
+    _check(rc, "kvx_stream")
+
+
+def _stream_ctl(layer_ready, ready_value, epoch_word, epoch, wait_ns, max_ctas, host_done,
+                dst_page_epochs, epoch_page) -> StreamCtl:
     ctl = StreamCtl()
     ctl.layer_ready = _any_ptr(layer_ready)
     ctl.ready_value = ready_value
@@ -474,11 +488,30 @@ def stream(op: int, src: Optional[Layout], src_slots, dst: Optional[Layout], dst
     ctl.dst_page_epochs = _any_ptr(dst_page_epochs)
     ctl.epoch_page = epoch_page if dst_page_epochs is not None else 0
     ctl.reserved2 = 0
-    rc = lib().kvx_stream(op, _h(src), _ptr(src_slots), _h(dst), _ptr(dst_slots), n, _ptr(buf),
-                          _nbytes(buf) if buf_bytes is None else buf_bytes, ctypes.byref(ctl),
-                          _ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
-                          _ptr(status), _stream(stream))
-    _check(rc, "kvx_stream")
+    return ctl
+
+
+def stream_reshard(srcs: Sequence[Optional[Layout]], src_slots, dsts: Sequence[Optional[Layout]],
+                   dst_slots, parts, n: int, ws, status, layer_ready=None, ready_value: int = 1,
+                   epoch_word=None, epoch: int = 0, wait_ns: int = 100_000_000, host_done=None,
+                   dst_page_epochs=None, epoch_page: int = 1, ws_bytes=None,
+                   stream=None) -> None:
+    """kvx_stream_reshard: kvx_reshard moving layer l once ``layer_ready[l] >= ready_value``,
+    stopping on a changed epoch word or a wait past ``wait_ns``; ``status`` is a device
+    int32[4] as for stream()."""
+    ctl = _stream_ctl(layer_ready, ready_value, epoch_word, epoch, wait_ns, 0, host_done,
+                      dst_page_epochs, epoch_page)
+    sa = (_VP * max(1, len(srcs)))(*[_h(x) for x in srcs])
+    da = (_VP * max(1, len(dsts)))(*[_h(x) for x in dsts])
+    pa = (HeadPart * max(1, len(parts)))()
+    for k, q in enumerate(parts):
+        vals = tuple(int(x) for x in q)
+        pa[k] = HeadPart(*(vals + (0,) * (6 - len(vals))))
+    rc = lib().kvx_stream_reshard(sa, len(srcs), _ptr(src_slots), da, len(dsts),
+                                  _ptr(dst_slots), pa, len(parts), n, ctypes.byref(ctl),
+                                  _ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
+                                  _ptr(status), _stream(stream))
+    _check(rc, "kvx_stream_reshard")
 
 
 def _any_ptr(x) -> Optional[int]:

@@ -467,6 +467,24 @@ KVX_API kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src
                               void *d_ws, size_t ws_bytes, int32_t *d_status,
                               kvx_stream_t stream);
 
+/* kvx_reshard, layer-streamed and cancellable as kvx_stream ("DistServe 完全拆解", layer j
+ * pulled as soon as prefill has written it; [Mooncake] 7.7 异构TP for the parts): layer l of
+ * every part moves once ctl->layer_ready[l] >= ctl->ready_value (one word per layer for the
+ * whole source group: its ranks finish a layer together), the move stops when ctl->epoch_word
+ * no longer holds ctl->epoch or a wait runs past ctl->wait_ns, and with ctl->dst_page_epochs
+ * a row is written only while its destination page (slot / epoch_page, the same slot list for
+ * every destination) still holds ctl->epoch.  Arguments and host-side errors as kvx_reshard
+ * and kvx_stream; ctl->max_ctas must be 0 (one CTA per padded group of items, as kvx_stream's
+ * default grid), and a reshard whose padded items exceed 2^31 - 1 is KVX_ERR_INVALID_ARG.
+ * d_status: device int32[4], 16-byte aligned, with kvx_stream's meaning (verdict, layers
+ * pending, internal, "no further write"). */
+KVX_API kvx_status kvx_stream_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
+                                      const int32_t *d_src_slots, const kvx_layout_t *dsts,
+                                      int32_t n_dsts, const int32_t *d_dst_slots,
+                                      const kvx_head_part *parts, int32_t n_parts, int32_t n,
+                                      const kvx_stream_ctl *ctl, void *d_ws, size_t ws_bytes,
+                                      int32_t *d_status, kvx_stream_t stream);
+
 /* ---- misc ---------------------------------------------------------------------------- */
 
 /* Which kernel moves linear chunks (rows contiguous on both sides).  KVX_ENGINE_BULK uses the

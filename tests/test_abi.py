@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_misc(lib):
-    assert kvx.version() == 202
+    assert kvx.version() == 203
     assert kvx.status_str(kvx.OK) == "ok"
     assert "range" in kvx.status_str(kvx.ERR_OUT_OF_RANGE)
     ws = kvx.workspace_size(2048, 0)
@@ -281,6 +281,33 @@ def test_reshard_validation_before_cuda(lib):
     assert rs(p, d, good, ws=None) == kvx.ERR_NO_WORKSPACE
     assert rs(p, d, good, wsb=16) == kvx.ERR_NO_WORKSPACE
     assert rs(p, d, good, sl=None) == E
+
+
+def test_stream_reshard_validation_before_cuda(lib):
+    """kvx_stream_reshard refuses a persistent grid, a missing or malformed control block, a
+    status array that is not 16-byte aligned, and every malformed reshard kvx_reshard refuses."""
+    mk = lambda k, h: kvx.Layout(2, h, 64, kvx.F16, 1000, base=FAKE * k, plane_stride=1000 * h * 128)
+    p = [mk(1, 2), mk(2, 2)]
+    d = [mk(3, 4)]
+    WS, ST, SL = FAKE * 6, FAKE * 7, FAKE * 8
+    l = kvx.lib()
+
+    def rs(parts, ctl, st=ST, srcs=p):
+        sa = (ctypes.c_void_p * len(srcs))(*[x.handle for x in srcs])
+        da = (ctypes.c_void_p * 1)(d[0].handle)
+        pa = (kvx.HeadPart * max(1, len(parts)))(*[kvx.HeadPart(*q) for q in parts])
+        return l.kvx_stream_reshard(sa, len(srcs), SL, da, 1, SL, pa, len(parts), 10,
+                                    ctypes.byref(ctl) if ctl is not None else None, WS, 1 << 30,
+                                    st, None)
+
+    good = [(0, 0, 0, 0, 2), (1, 0, 0, 2, 2)]
+    ok = kvx._stream_ctl(None, 1, None, 0, 1000, 0, None, None, 1)
+    assert rs(good, None) == kvx.ERR_INVALID_ARG
+    assert rs(good, kvx._stream_ctl(None, 1, None, 0, 1000, 40, None, None, 1)) == kvx.ERR_INVALID_ARG
+    assert rs(good, kvx._stream_ctl(None, 1, None, 0, 0, 0, None, None, 1)) == kvx.ERR_INVALID_ARG
+    assert rs(good, ok, st=ST + 4) == kvx.ERR_INVALID_ARG
+    assert rs([(0, 0, 0, 0, 2), (1, 0, 0, 1, 2)], ok) == kvx.ERR_INVALID_ARG  # one head twice
+    assert rs(good, ok, srcs=[p[0], d[0]]) == kvx.ERR_INVALID_ARG            # sources differ
 
 
 def test_latent_plane_layouts(lib):
