@@ -6,7 +6,8 @@
 // in the widest access V (8, 4, 2 or 1 bytes; 16 when only the head vectors are narrow) that
 // every address of the call allows, which the host works out from the layouts.
 //
-// One warp per group of 1 << g tokens of one plane, as the row kernel of kvx_copy.cu: 32 >> g
+// One warp per group of 1 << g tokens of one plane (a power of two, unlike the row kernel of
+// kvx_copy.cu, which may give a token any number of lanes): 32 >> g
 // lanes per row, enough for the lane's kUnroll independent loads to cover the row
 // (narrow_group_shift).  One-shot calls read the slot lists, range-check them and load
 // before the planner's verdict; plans (one row per chunk, including a batch's request

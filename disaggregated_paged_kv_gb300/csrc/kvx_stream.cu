@@ -7,7 +7,8 @@
 // another request, and the sender may only acknowledge the abort once it can prove that no
 // write is still in flight.
 //
-// Items are (layer l, K/V, group of g tokens) in layer-major order: item i has
+// Items are (layer l, K/V, group of G tokens, m lanes each: the row kernel's shape for the
+// row length) in layer-major order: item i has
 // l = i / (kv_planes * groups); with one latent plane per layer (MLA) there is no K/V split.
 // Two grids move them:
 //
