@@ -68,8 +68,10 @@ def parse_args():
                          "the request itself is unchanged)")
     ap.add_argument("--fused-max", type=int, default=None,
                     help="kvx_set_fused_max_tokens for this run (0: planner + copy launches only)")
-    ap.add_argument("--workload", default="2",
-                    help="2 (default): the headline transfer; 1, 3, 4, 5: the other workloads; "
+    ap.add_argument("--workload", default="transfer",
+                    help="transfer (default): the 2048-token, 288 MiB pool-to-pool transfer; "
+                         "small_gather_scatter, fragmented, batch, hnd_permute: the other "
+                         "workloads of tests/inputs.py; "
                          "stream: the headline transfer through kvx_stream (layer-streamed); "
                          "tp: the headline request resharded between TP groups (kvx_reshard, and "
                          "kvx_move_heads pair by pair); "
@@ -113,7 +115,7 @@ def copy_source_sha256() -> str:
 def profile_traffic():
     """Per-launch DRAM bytes of the copy kernel from the committed ncu summary, if that summary
     was taken on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", "copy_row_kernel_cfg2_transfer.md")
+    path = os.path.join(ROOT, "profiles", "copy_row_kernel_transfer_2048_tokens.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -354,13 +356,14 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
 
 # ---------------------------------------------------------------------------------------
-# the other workloads (--workload 1, 3, 4, 5): same timing rules, one JSON line each
+# the other workloads (--workload small_gather_scatter, fragmented, batch, hnd_permute): same
+# timing rules, one JSON line each
 # ---------------------------------------------------------------------------------------
 
-def run_workload(args, cfg: int):
-    """Times every leg of workload cfg (gather + scatter-back, fragmented gather + scatter,
-    batch, fused-permute gather + rebuild).  Pools, slot lists and page tables come from the
-    same seeded recipe as the tests."""
+def run_workload(args, name: str):
+    """Times every leg of the named workload (gather + scatter-back, fragmented gather +
+    scatter, batch, fused-permute gather + rebuild).  Pools, slot lists and page tables come
+    from the same seeded recipe as the tests."""
     import numpy as np
     import torch
 
@@ -372,12 +375,13 @@ def run_workload(args, cfg: int):
     kvx.lib()
     stream = torch.cuda.Stream(device=dev)
     sp = int(stream.cuda_stream)
-    w = inputs.WORKLOADS[cfg]
+    w = inputs.WORKLOADS[name]
+    sid = w.seed_id
     Pw, Hw, Dw, Rw = w.planes, w.kv_heads, w.head_dim, w.row_bytes
     tdt = torch.float16 if w.dtype == "fp16" else torch.bfloat16
     kdt = kvx.F16 if w.dtype == "fp16" else kvx.BF16
     gen = torch.Generator(device=dev)
-    gen.manual_seed(inputs.seed(cfg, inputs.ROLE_VALUES))
+    gen.manual_seed(inputs.seed(sid, inputs.ROLE_VALUES))
     sentinel = 0x7E01 if w.dtype == "fp16" else 0x7FC1
 
     def randn(shape):
@@ -391,11 +395,11 @@ def run_workload(args, cfg: int):
     st = torch.zeros(65, dtype=torch.int32, device=dev)
     legs = []  # (name, fn, algorithmic bytes)
     requests = 1
-    if cfg == 1:
+    if name == "small_gather_scatter":
         pool = randn((w.num_slots, w.num_layers, 2, Hw, Dw))
         lay = kvx.Layout(w.num_layers, Hw, Dw, kdt, w.num_slots, base=pool, plane_stride=Rw,
                          slot_stride=Pw * Rw)
-        slots = torch.from_numpy(inputs.distinct_slots(inputs.rng(1, 1), w.n_tokens, w.num_slots)).to(dev)
+        slots = torch.from_numpy(inputs.distinct_slots(inputs.rng(sid, 1), w.n_tokens, w.num_slots)).to(dev)
         buf = torch.empty((Pw, w.n_tokens, Hw, Dw), dtype=tdt, device=dev)
         ws = torch.empty(kvx.workspace_size(w.n_tokens), dtype=torch.uint8, device=dev)
         nb = 2 * w.payload_bytes + 4 * w.n_tokens
@@ -405,11 +409,11 @@ def run_workload(args, cfg: int):
         desc = ("Qwen2.5-1.5B-shaped KV (28 x K/V x 2 x 128 fp16), slot-major pool of 4096 slots, "
                 "128 random slots: gather to a 3.5 MiB [layer][K/V][seq][head][dim] buffer, then "
                 "scatter back in place")
-    elif cfg == 3:
+    elif name == "fragmented":
         src_planes = [randn((w.num_slots, Hw, Dw)) for _ in range(Pw)]
         dst_planes = [sentinel_pool((w.num_slots, Hw, Dw)) for _ in range(Pw)]
-        s_np, runs = inputs.fragmented_slots(inputs.rng(3, 1), w.n_tokens, w.num_slots, 1.6)
-        d_np, _ = inputs.fragmented_slots(inputs.rng(3, 2), w.n_tokens, w.num_slots, 1.6)
+        s_np, runs = inputs.fragmented_slots(inputs.rng(sid, 1), w.n_tokens, w.num_slots, 1.6)
+        d_np, _ = inputs.fragmented_slots(inputs.rng(sid, 2), w.n_tokens, w.num_slots, 1.6)
         s_d, d_d = torch.from_numpy(s_np).to(dev), torch.from_numpy(d_np).to(dev)
         sl = kvx.Layout(w.num_layers, Hw, Dw, kdt, w.num_slots, plane_ptrs=src_planes)
         dl = kvx.Layout(w.num_layers, Hw, Dw, kdt, w.num_slots, plane_ptrs=dst_planes)
@@ -421,10 +425,10 @@ def run_workload(args, cfg: int):
         desc = (f"fragmented pools: 72 per-plane [131072][8][128] bf16 pools, 1536 tokens in "
                 f"{len(runs)} runs ~Geometric(1.6): gather to a 216 MiB buffer, then scatter into a "
                 f"fresh run layout")
-    elif cfg == 4:
+    elif name == "batch":
         lens = inputs.batch_lengths()
-        s_np, offs = inputs.paged_request_slots(inputs.rng(4, 1), lens, w.page_size, w.num_slots)
-        d_np, _ = inputs.paged_request_slots(inputs.rng(4, 2), lens, w.page_size, w.num_slots)
+        s_np, offs = inputs.paged_request_slots(inputs.rng(sid, 1), lens, w.page_size, w.num_slots)
+        d_np, _ = inputs.paged_request_slots(inputs.rng(sid, 2), lens, w.page_size, w.num_slots)
         src = randn((Pw, w.num_slots, Hw, Dw))
         dst = sentinel_pool((Pw, w.num_slots, Hw, Dw))
         sl = kvx.Layout(w.num_layers, Hw, Dw, kdt, w.num_slots, base=src, plane_stride=w.num_slots * Rw)
@@ -440,14 +444,14 @@ def run_workload(args, cfg: int):
                                              None, ws, st, buf_bytes=0, stream=sp), nb)]
         desc = (f"64 requests of U{{1000..2000}} tokens ({total} total), 36 x K/V x 8 x 128 bf16, "
                 f"token-paged pools of 262144 slots with page size 16: one kvx_batch")
-    elif cfg == 5:
+    elif name == "hnd_permute":
         ps = w.page_size
         pages = w.num_slots // ps
         n_pages = w.n_tokens // ps
         src = randn((Pw, pages, Hw, ps, Dw))
         dst = sentinel_pool((Pw, pages, Hw, ps, Dw))
-        pt = inputs.random_pages(inputs.rng(5, 1), n_pages, pages)
-        pt2 = inputs.random_pages(inputs.rng(5, 2), n_pages, pages)
+        pt = inputs.random_pages(inputs.rng(sid, 1), n_pages, pages)
+        pt2 = inputs.random_pages(inputs.rng(sid, 2), n_pages, pages)
         s_d = torch.from_numpy(inputs.page_table_slots(pt, w.n_tokens, ps)).to(dev)
         d_d = torch.from_numpy(inputs.page_table_slots(pt2, w.n_tokens, ps)).to(dev)
         sl = kvx.Layout(w.num_layers, Hw, Dw, kdt, w.num_slots, kind=kvx.HND_PAGED, page_size=ps,
@@ -463,7 +467,7 @@ def run_workload(args, cfg: int):
                 "(65536-page pools, random page tables): fused [heads,seq,dim] -> [seq,heads,dim] "
                 "gather to a 1.75 GiB buffer, then the inverse rebuild")
     else:
-        raise SystemExit(f"unknown workload {cfg}")
+        raise SystemExit(f"unknown workload {name}")
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
 
@@ -484,14 +488,14 @@ def run_workload(args, cfg: int):
 
     timed(max(3, args.warmup))
     assert int(st[0].item()) == kvx.OK, int(st[0].item())
-    K = max(3, min(args.steps, 200 if cfg in (4, 5) else args.steps))
+    K = max(3, min(args.steps, 200 if name in ("batch", "hnd_permute") else args.steps))
     res = timed(K)
     total_bytes = sum(b for _, _, b in legs)
     step_ms = statistics.mean(sum(r) for r in res)
     line = {"metric": METRIC, "value": total_bytes / (step_ms * 1e-3) / 1e9, "unit": UNIT,
             "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "dtype": "u8", "data": "synthetic",
-            "config": {"workload": f"cfg {cfg}: {desc}", "kv_dtype": w.dtype,
+            "config": {"workload": f"{name}: {desc}", "kv_dtype": w.dtype,
                        "alg_bytes_per_step": total_bytes, "requests_per_step": requests,
                        "us_per_request": step_ms * 1e3 / requests,
                        "l2": "flushed before every timed step (write of 2x L2, outside the events)"},
@@ -501,7 +505,7 @@ def run_workload(args, cfg: int):
     peaks, _ = measured_peaks()
     line["config"]["frac_of_measured_hbm"] = line["value"] / float(peaks["hbm_gbs"])
     line["config"]["frac_of_nominal_8tbs"] = line["value"] / NOMINAL_HBM_GBS
-    if cfg == 1:  # launch-bound and L2-resident when not flushed: report the warm figure too
+    if name == "small_gather_scatter":  # launch-bound, L2-resident unless flushed: warm too
         warm = timed(K, flush_l2=False)
         wm = statistics.mean(sum(r) for r in warm)
         line["warm_l2"] = {"value": total_bytes / (wm * 1e-3) / 1e9, "us_per_step": wm * 1e3}
@@ -1279,8 +1283,8 @@ def main():
     if args.workload == "comparators":
         run_comparators(args)
         return
-    if int(args.workload) != 2:
-        run_workload(args, int(args.workload))
+    if args.workload != "transfer":
+        run_workload(args, args.workload)
         return
     if world > 1:
         import torch

@@ -5,25 +5,27 @@ lists, page tables, run layouts and pool contents.  It holds none of the method'
 (no gather, no scatter, no address computation of a pool).
 
 The pages' workloads are production TTS traffic and public prompts, which are not used here;
-these shapes stand in for them:
+these shapes stand in for them (WORKLOADS, by name):
 
-  cfg 1  Qwen2.5-1.5B-shaped KV (28 layers, 2 kv heads, head_dim 128, fp16), slot-major pool
-         of 4096 slots, one request of 128 distinct random slots: gather, then scatter back.
-  cfg 2  36 layers x 8 kv heads x 128 bf16 (144 KiB/token), two pools of 65,536 slots,
+  small_gather_scatter  Qwen2.5-1.5B-shaped KV (28 layers, 2 kv heads, head_dim 128, fp16),
+         slot-major pool of 4096 slots, one request of 128 distinct random slots: gather,
+         then scatter back (3.5 MiB).
+  transfer  36 layers x 8 kv heads x 128 bf16 (144 KiB/token), two pools of 65,536 slots,
          2048 + 2048 distinct random slots: pool-to-pool transfer (288 MiB each way).
-  cfg 3  the cfg 2 shape on per-plane pools of 131,072 slots; one request of 1536 tokens in
-         runs of length ~Geometric(mean 1.6) placed at random non-overlapping starts with a
-         free slot between runs, in shuffled address order: gather, then scatter into a fresh
-         run layout.
-  cfg 4  64 requests of U{1000..2000} tokens, cfg 2 shape, token-paged pools of 262,144 slots
-         with page size 16 (distinct random pages, last page partial): one batch launch.
-  cfg 5  Qwen2.5-7B-shaped KV (28 layers, 4 kv heads, 128, bf16), seq 32,768, HND pages of
-         16 tokens in a 65,536-page pool with a random page table: fused permute gather, then
-         the inverse rebuild into a second pool under an independent page table.
+  fragmented  the transfer shape on per-plane pools of 131,072 slots; one request of 1536
+         tokens in runs of length ~Geometric(mean 1.6) placed at random non-overlapping starts
+         with a free slot between runs, in shuffled address order: gather, then scatter into a
+         fresh run layout.
+  batch  64 requests of U{1000..2000} tokens, the transfer shape, token-paged pools of 262,144
+         slots with page size 16 (distinct random pages, last page partial): one batch launch.
+  hnd_permute  Qwen2.5-7B-shaped KV (28 layers, 4 kv heads, 128, bf16), seq 32,768, HND pages
+         of 16 tokens in a 65,536-page pool with a random page table: fused permute gather,
+         then the inverse rebuild into a second pool under an independent page table.
 
 Values: elements ~N(0,1) (numpy PCG64, float64 draws rounded to float32 and then to the
 KV dtype with round-to-nearest-even).  Destinations and guard bands hold quiet-NaN payload
-patterns that N(0,1) never produces.  Seeds: 20261202 + 1000 * cfg + role.
+patterns that N(0,1) never produces.  Seeds: 20261202 + 1000 * group + role, the group
+being a workload's seed_id (1 to 5 in the order above) or a test's own number.
 """
 from __future__ import annotations
 
@@ -42,12 +44,12 @@ ROLE_LENGTHS = 3
 ROLE_DST_VALUES = 4
 
 
-def seed(cfg: int, role: int) -> int:
-    return SEED_BASE + 1000 * cfg + role
+def seed(group: int, role: int) -> int:
+    return SEED_BASE + 1000 * group + role
 
 
-def rng(cfg: int, role: int) -> np.random.Generator:
-    return np.random.Generator(np.random.PCG64(seed(cfg, role)))
+def rng(group: int, role: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(seed(group, role)))
 
 
 ELEM_BYTES = {"fp16": 2, "bf16": 2, "fp8": 1}
@@ -202,7 +204,7 @@ def page_table_slots(page_table: np.ndarray, seq_len: int, page_size: int) -> np
 
 @dataclass(frozen=True)
 class Workload:
-    cfg: int
+    seed_id: int  # seed group of its inputs
     name: str
     num_layers: int
     kv_heads: int
@@ -236,20 +238,26 @@ class Workload:
 
 
 WORKLOADS = {
-    1: Workload(1, "qwen2.5-1.5b gather+scatter-back, slot-major pool, 128 tokens", 28, 2, 128,
-                "fp16", "slot_major", 4096, 128),
-    2: Workload(2, "pool-to-pool transfer, 2048 random rows, 36x8x128 bf16 (288 MiB)", 36, 8, 128,
-                "bf16", "planes", 65536, 2048),
-    3: Workload(3, "fragmented gather+scatter, 1536 tokens in Geometric(1.6) runs", 36, 8, 128,
-                "bf16", "planes", 131072, 1536),
-    4: Workload(4, "batch of 64 requests U{1000..2000}, token-paged pools, page 16", 36, 8, 128,
-                "bf16", "planes", 262144, 0, page_size=16, n_requests=64),
-    5: Workload(5, "qwen2.5-7b fused HND->[S,H,D] gather + rebuild, seq 32768", 28, 4, 128,
-                "bf16", "hnd", 65536 * 16, 32768, page_size=16),
+    "small_gather_scatter": Workload(
+        1, "qwen2.5-1.5b gather+scatter-back, slot-major pool, 128 tokens", 28, 2, 128, "fp16",
+        "slot_major", 4096, 128),
+    "transfer": Workload(
+        2, "pool-to-pool transfer, 2048 random rows, 36x8x128 bf16 (288 MiB)", 36, 8, 128, "bf16",
+        "planes", 65536, 2048),
+    "fragmented": Workload(
+        3, "fragmented gather+scatter, 1536 tokens in Geometric(1.6) runs", 36, 8, 128, "bf16",
+        "planes", 131072, 1536),
+    "batch": Workload(
+        4, "batch of 64 requests U{1000..2000}, token-paged pools, page 16", 36, 8, 128, "bf16",
+        "planes", 262144, 0, page_size=16, n_requests=64),
+    "hnd_permute": Workload(
+        5, "qwen2.5-7b fused HND->[S,H,D] gather + rebuild, seq 32768", 28, 4, 128, "bf16", "hnd",
+        65536 * 16, 32768, page_size=16),
 }
 
 
-def batch_lengths(cfg: int = 4, n_requests: int = 64, lo: int = 1000, hi: int = 2000) -> List[int]:
-    """Prompt lengths U{lo..hi} inclusive."""
-    g = rng(cfg, ROLE_LENGTHS)
+def batch_lengths(group: int = 4, n_requests: int = 64, lo: int = 1000,
+                  hi: int = 2000) -> List[int]:
+    """Prompt lengths U{lo..hi} inclusive (the batch workload's by default)."""
+    g = rng(group, ROLE_LENGTHS)
     return [int(x) for x in g.integers(lo, hi + 1, size=n_requests)]

@@ -75,13 +75,13 @@ def _check_sampled_transfer(src, s, dst, d, sample):
     assert np.array_equal(got, dst_host), "sampled rows differ from the oracle"
 
 
-def test_cfg2_transfer_full_size():
-    w = inputs.WORKLOADS[2]
+def test_transfer_2048_tokens_full_size():
+    w = inputs.WORKLOADS["transfer"]
     P, S = w.planes, w.num_slots
-    src = _planes_pool(P, S, w.kv_heads, w.head_dim, w.dtype, "normal", inputs.seed(2, 0))
+    src = _planes_pool(P, S, w.kv_heads, w.head_dim, w.dtype, "normal", inputs.seed(w.seed_id, 0))
     dst = _planes_pool(P, S, w.kv_heads, w.head_dim, w.dtype, "sentinel", 0)
-    s = inputs.distinct_slots(inputs.rng(2, inputs.ROLE_SRC_SLOTS), w.n_tokens, S)
-    d = inputs.distinct_slots(inputs.rng(2, inputs.ROLE_DST_SLOTS), w.n_tokens, S)
+    s = inputs.distinct_slots(inputs.rng(w.seed_id, inputs.ROLE_SRC_SLOTS), w.n_tokens, S)
+    d = inputs.distinct_slots(inputs.rng(w.seed_id, inputs.ROLE_DST_SLOTS), w.n_tokens, S)
     R = w.row_bytes
     sl = kvx.Layout(w.num_layers, w.kv_heads, w.head_dim, kvx.BF16, S, base=src, plane_stride=S * R)
     dl = kvx.Layout(w.num_layers, w.kv_heads, w.head_dim, kvx.BF16, S, base=dst, plane_stride=S * R)
@@ -98,13 +98,13 @@ def test_cfg2_transfer_full_size():
     assert torch.equal(_changed_rows(dst, SENT), want), "rows other than the named ones changed"
 
 
-def test_cfg3_fragmented_gather_scatter_full_size():
-    w = inputs.WORKLOADS[3]
+def test_fragmented_gather_scatter_full_size():
+    w = inputs.WORKLOADS["fragmented"]
     P, S, H, D = w.planes, w.num_slots, w.kv_heads, w.head_dim
     R = w.row_bytes
     # per-layer separate K and V pools: one allocation per plane
-    src_planes = [_planes_pool(1, S, H, D, w.dtype, "normal", inputs.seed(3, 0) + p)[0] for p in range(P)]
-    s, runs = inputs.fragmented_slots(inputs.rng(3, inputs.ROLE_SRC_SLOTS), w.n_tokens, S, 1.6)
+    src_planes = [_planes_pool(1, S, H, D, w.dtype, "normal", inputs.seed(w.seed_id, 0) + p)[0] for p in range(P)]
+    s, runs = inputs.fragmented_slots(inputs.rng(w.seed_id, inputs.ROLE_SRC_SLOTS), w.n_tokens, S, 1.6)
     assert 900 <= len(runs) <= 1050
     sl = kvx.Layout(w.num_layers, H, D, kvx.BF16, S, plane_ptrs=src_planes)
     ws = torch.empty(kvx.workspace_size(w.n_tokens), dtype=torch.uint8, device="cuda")
@@ -123,7 +123,7 @@ def test_cfg3_fragmented_gather_scatter_full_size():
     assert np.array_equal(got, want)
     # scatter into a fresh destination run layout
     dst_planes = [_planes_pool(1, S, H, D, w.dtype, "sentinel", 0)[0] for _ in range(P)]
-    d, _ = inputs.fragmented_slots(inputs.rng(3, inputs.ROLE_DST_SLOTS), w.n_tokens, S, 1.6)
+    d, _ = inputs.fragmented_slots(inputs.rng(w.seed_id, inputs.ROLE_DST_SLOTS), w.n_tokens, S, 1.6)
     dl = kvx.Layout(w.num_layers, H, D, kvx.BF16, S, plane_ptrs=dst_planes)
     kvx.scatter(dl, torch.from_numpy(d).cuda(), w.n_tokens, buf, ws, st)
     torch.cuda.synchronize()
@@ -137,15 +137,15 @@ def test_cfg3_fragmented_gather_scatter_full_size():
         assert torch.equal(changed, want)
 
 
-def test_cfg4_batch_full_size():
-    w = inputs.WORKLOADS[4]
+def test_batch_64_requests_full_size():
+    w = inputs.WORKLOADS["batch"]
     P, S, H, D, ps = w.planes, w.num_slots, w.kv_heads, w.head_dim, w.page_size
     R = w.row_bytes
     lens = inputs.batch_lengths()
     assert len(lens) == 64 and 1000 <= min(lens) and max(lens) <= 2000
-    s, offs = inputs.paged_request_slots(inputs.rng(4, inputs.ROLE_SRC_SLOTS), lens, ps, S)
-    d, _ = inputs.paged_request_slots(inputs.rng(4, inputs.ROLE_DST_SLOTS), lens, ps, S)
-    src = _planes_pool(P, S, H, D, w.dtype, "normal", inputs.seed(4, 0))
+    s, offs = inputs.paged_request_slots(inputs.rng(w.seed_id, inputs.ROLE_SRC_SLOTS), lens, ps, S)
+    d, _ = inputs.paged_request_slots(inputs.rng(w.seed_id, inputs.ROLE_DST_SLOTS), lens, ps, S)
+    src = _planes_pool(P, S, H, D, w.dtype, "normal", inputs.seed(w.seed_id, 0))
     dst = _planes_pool(P, S, H, D, w.dtype, "sentinel", 0)
     sl = kvx.Layout(w.num_layers, H, D, kvx.BF16, S, base=src, plane_stride=S * R)
     dl = kvx.Layout(w.num_layers, H, D, kvx.BF16, S, base=dst, plane_stride=S * R)
@@ -172,17 +172,17 @@ def test_cfg4_batch_full_size():
     assert torch.equal(_changed_rows(dst, SENT), want)
 
 
-def test_cfg5_hnd_permute_gather_and_rebuild_full_size():
-    w = inputs.WORKLOADS[5]
+def test_hnd_permute_gather_and_rebuild_full_size():
+    w = inputs.WORKLOADS["hnd_permute"]
     P, H, D, ps = w.planes, w.kv_heads, w.head_dim, w.page_size
     pages = w.num_slots // ps
     seq = w.n_tokens
     n_pages = seq // ps
     R = w.row_bytes
     g = torch.Generator(device="cuda")
-    g.manual_seed(inputs.seed(5, 0))
+    g.manual_seed(inputs.seed(w.seed_id, 0))
     src = torch.randn((P, pages, H, ps, D), dtype=torch.bfloat16, device="cuda", generator=g)
-    pt = inputs.random_pages(inputs.rng(5, inputs.ROLE_SRC_SLOTS), n_pages, pages)
+    pt = inputs.random_pages(inputs.rng(w.seed_id, inputs.ROLE_SRC_SLOTS), n_pages, pages)
     slots = inputs.page_table_slots(pt, seq, ps)
     sl = kvx.Layout(w.num_layers, H, D, kvx.BF16, pages * ps, kind=kvx.HND_PAGED, page_size=ps,
                     base=src, plane_stride=pages * ps * R)
@@ -211,7 +211,7 @@ def test_cfg5_hnd_permute_gather_and_rebuild_full_size():
     # inverse rebuild into a second pool under an independent page table
     dst = torch.empty((P, pages, H, ps, D), dtype=torch.bfloat16, device="cuda")
     dst.view(torch.int16).fill_(SENT)
-    pt2 = inputs.random_pages(inputs.rng(5, inputs.ROLE_DST_SLOTS), n_pages, pages)
+    pt2 = inputs.random_pages(inputs.rng(w.seed_id, inputs.ROLE_DST_SLOTS), n_pages, pages)
     dl = kvx.Layout(w.num_layers, H, D, kvx.BF16, pages * ps, kind=kvx.HND_PAGED, page_size=ps,
                     base=dst, plane_stride=pages * ps * R)
     kvx.scatter(dl, torch.from_numpy(inputs.page_table_slots(pt2, seq, ps)).cuda(), seq, buf, ws, st)

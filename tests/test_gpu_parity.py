@@ -159,14 +159,14 @@ def test_transfer(src_kind, dst_kind, n, path):
     hz.assert_same_bytes(src.readback(), src.host, "source pool")
 
 
-def test_cfg1_gather_scatter_back_full_size(path):
+def test_small_gather_scatter_back_full_size(path):
     """Qwen2.5-1.5B shape (28 x 2 x 128 fp16), slot-major pool of 4096 slots, 128 random
     slots: gather, then scatter back into a sentinel copy and in place."""
-    w = inputs.WORKLOADS[1]
-    g = inputs.rng(1, inputs.ROLE_VALUES)
+    w = inputs.WORKLOADS["small_gather_scatter"]
+    g = inputs.rng(w.seed_id, inputs.ROLE_VALUES)
     src = hz.make_mirror("slot_major", w.num_layers, w.kv_heads, w.head_dim, w.dtype,
                          w.num_slots, 1, "normal", g).to_device()
-    slots = inputs.distinct_slots(inputs.rng(1, inputs.ROLE_SRC_SLOTS), w.n_tokens, w.num_slots)
+    slots = inputs.distinct_slots(inputs.rng(w.seed_id, inputs.ROLE_SRC_SLOTS), w.n_tokens, w.num_slots)
     rc, want, written = oracle.gather(hz.oracle_pool(src), slots)
     assert rc == oracle.OK and written == w.payload_bytes == 3670016
     buf = hz.make_mirror("buffer", w.num_layers, w.kv_heads, w.head_dim, w.dtype,
@@ -179,7 +179,7 @@ def test_cfg1_gather_scatter_back_full_size(path):
     exp = buf.host.copy()
     exp[hz.GUARD:hz.GUARD + len(want)] = want
     got = buf.readback()
-    hz.assert_same_bytes(got, exp, "cfg1 gather")
+    hz.assert_same_bytes(got, exp, "small gather")
     # scatter back into a sentinel copy
     sent = hz.make_mirror("slot_major", w.num_layers, w.kv_heads, w.head_dim, w.dtype,
                           w.num_slots, 1, "sentinel", salt=9).to_device()
@@ -189,12 +189,12 @@ def test_cfg1_gather_scatter_back_full_size(path):
     kvx.scatter(hz.kvx_layout(sent), hz.dev_i32(slots), w.n_tokens,
                 hz.GUARD + buf.dev.data_ptr(), ws, st, buf_bytes=w.payload_bytes)
     assert _sync_status(st) == [0]
-    hz.assert_same_bytes(sent.readback(), exp_sent.host, "cfg1 scatter into sentinel pool")
+    hz.assert_same_bytes(sent.readback(), exp_sent.host, "small scatter into sentinel pool")
     # scatter back in place: the pool is unchanged
     kvx.scatter(lay, hz.dev_i32(slots), w.n_tokens, hz.GUARD + buf.dev.data_ptr(), ws, st,
                 buf_bytes=w.payload_bytes)
     assert _sync_status(st) == [0]
-    hz.assert_same_bytes(src.readback(), src.host, "cfg1 in-place scatter-back")
+    hz.assert_same_bytes(src.readback(), src.host, "small in-place scatter-back")
 
 
 def test_hnd_page_table_gather_and_rebuild(path):
