@@ -849,13 +849,39 @@ kvx_status kvx_submit(int32_t op, kvx_layout_t src, const int32_t *h_src_slots,
   return e == cudaSuccess ? KVX_OK : cuda_fail(e);
 }
 
-// Device address of a control word: device memory as is, pinned host memory through its
-// device mapping; anything else (pageable memory, unknown pointers) gives nullptr.
-// Tags the mirror words of each kvx_stream call: an odd 64-bit start, one step per call.
+// Tags the mirror words of each streamed call: a Weyl sequence (odd step), so tags of nearby
+// calls differ in every bit range.
 std::atomic<uint64_t> g_stream_gen{0xD1B54A32D192ED03ull};
-static_assert(sizeof(kvx::Chunk) * kvx::kTile >= 8 * (2 + KVX_MAX_PLANES / 2),
+
+// The streamed kernels' device-memory mirror (in the workspace, where a plan's chunk table
+// would be) and the call's tag.  Words of earlier calls never match a new tag, so an eager call
+// needs no reset; a call being captured into a CUDA graph replays with the tag it was captured
+// with, so its mirror is cleared at the start of every replay (a zero word never matches a tag:
+// tags are non-zero with non-zero low 40 bits, which also keeps zero from reading as a stop).
+static kvx_status stream_mirror(void *d_ws, int64_t n, cudaStream_t s, kvx::StreamCtl *k) {
+  uint64_t gen;
+  do {
+    gen = g_stream_gen.fetch_add(0x9E3779B97F4A7C15ull, std::memory_order_relaxed);
+  } while ((gen & 0xFFFFFFFFFFull) == 0);
+  k->gen = gen;
+  k->mirror = nullptr;
+  if (n == 0) return KVX_OK;
+  k->mirror = reinterpret_cast<uint64_t *>(static_cast<char *>(d_ws) +
+                                           kvx::ws_layout(n, 0, false).chunks_off);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (cs != cudaStreamCaptureStatusNone) {
+    e = cudaMemsetAsync(k->mirror, 0, sizeof(uint64_t) * kvx::kMirrorWords, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return KVX_OK;
+}
+static_assert(sizeof(kvx::Chunk) * kvx::kTile >= sizeof(uint64_t) * kvx::kMirrorWords,
               "the stream mirror fits in one tile's chunk table");
 
+// Device address of a control word: device memory as is, pinned host memory through its
+// device mapping; anything else (pageable memory, unknown pointers) gives nullptr.
 static const void *device_word(const void *p, bool *in_device_memory = nullptr) {
   if (in_device_memory) *in_device_memory = false;
   if (!p) return nullptr;
@@ -927,6 +953,7 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
   if ((st = device_info(&di)) != KVX_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if ((st = stream_mirror(d_ws, n, s, &k)) != KVX_OK) return st;
   // status[0..3]: verdict, layers pending, CTAs finished, done.  A single-tile planner
   // writes all four itself; otherwise they are zeroed first and the planner's tiles raise [0].
   const bool direct = n > 0 && kvx::num_tiles(n) == 1;
@@ -946,11 +973,7 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
     }
     e = kvx::launch_plan(pa, s);
     if (e != cudaSuccess) return cuda_fail(e);
-    // the mirror lives where a plan's chunk table would be (unused by a validate-only plan)
-    k.mirror = reinterpret_cast<uint64_t *>(static_cast<char *>(d_ws) +
-                                            kvx::ws_layout(n, 0, false).chunks_off);
   }
-  k.gen = g_stream_gen.fetch_add(1, std::memory_order_relaxed);
   static thread_local kvx::CopyArgs a;  // ~4 KiB of plane pointers: keep it off the stack
   fill_copy_args(a, c, nullptr, d_buf, d_ws, d_status);
   a.spec_src = c.src ? d_src_slots : nullptr;
@@ -1238,6 +1261,7 @@ kvx_status kvx_stream_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
   if (!kvx::reshard_stream_fits(rc, k)) return KVX_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if ((st = stream_mirror(d_ws, n, s, &k)) != KVX_OK) return st;
   // status[0..3]: verdict, layers pending, stop code, done; as kvx_stream
   const bool direct = n > 0 && kvx::num_tiles(n) == 1;
   if (!direct) {
@@ -1256,11 +1280,7 @@ kvx_status kvx_stream_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
     }
     e = kvx::launch_plan(pa, s);
     if (e != cudaSuccess) return cuda_fail(e);
-    // the mirror lives where a plan's chunk table would be (unused by a validate-only plan)
-    k.mirror = reinterpret_cast<uint64_t *>(static_cast<char *>(d_ws) +
-                                            kvx::ws_layout(n, 0, false).chunks_off);
   }
-  k.gen = g_stream_gen.fetch_add(1, std::memory_order_relaxed);
   rc.status = d_status;
   e = kvx::launch_reshard_stream(rc, k, s);
   return e == cudaSuccess ? KVX_OK : cuda_fail(e);

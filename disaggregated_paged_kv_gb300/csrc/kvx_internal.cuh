@@ -175,6 +175,9 @@ struct CopyArgs {
   char *dst_planes[KVX_MAX_PLANES];
 };
 
+// Words of the streamed kernels' mirror: the cancel word, one word per layer, the stop word.
+constexpr int kMirrorWords = 2 + KVX_MAX_PLANES / 2;
+
 // kvx_stream's control words, as device addresses (pinned host words through their device
 // mapping).
 struct StreamCtl {
@@ -184,9 +187,9 @@ struct StreamCtl {
   // Device-memory copy of what some CTA has seen in the words above, in the workspace:
   // [0] == gen: cancelled (persistent grid); [1 + l] == gen: layer l ready;
   // [1 + KVX_MAX_PLANES / 2]: the row grid's stop word.  gen is a 64-bit tag new for every
-  // call, so words left by earlier calls (or any stale workspace bytes) do not match it and
-  // nothing needs resetting.
-  uint64_t *mirror;
+  // eager call, so words left by earlier calls (or any stale workspace bytes) do not match it;
+  // a call captured into a CUDA graph keeps its tag, so its mirror is zeroed on each replay.
+  uint64_t *mirror;  // kMirrorWords words
   uint64_t gen;
   int64_t wait_ns;
   int32_t ready_value;

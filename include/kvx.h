@@ -460,7 +460,10 @@ typedef struct kvx_stream_ctl {
  *       The receiving side may reuse cancelled pages after seeing it (or after the stream has
  *       passed the call).
  * The copy occupies up to ctl->max_ctas CTAs while it waits; every wait polls with back-off
- * and ends by ctl->wait_ns, so the kernel always finishes. */
+ * and ends by ctl->wait_ns, so the kernel always finishes.
+ * May be captured into a CUDA graph: every replay is a new call (it reads the slot lists,
+ * the control words and the workspace afresh and keeps nothing from an earlier replay); the
+ * host-side checks and the control block's values are those of the captured call. */
 KVX_API kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots,
                               kvx_layout_t dst, const int32_t *d_dst_slots, int32_t n,
                               void *d_buf, size_t buf_bytes, const kvx_stream_ctl *ctl,
@@ -477,7 +480,7 @@ KVX_API kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src
  * and kvx_stream; ctl->max_ctas must be 0 (one CTA per padded group of items, as kvx_stream's
  * default grid), and a reshard whose padded items exceed 2^31 - 1 is KVX_ERR_INVALID_ARG.
  * d_status: device int32[4], 16-byte aligned, with kvx_stream's meaning (verdict, layers
- * pending, internal, "no further write"). */
+ * pending, internal, "no further write").  May be captured into a CUDA graph, as kvx_stream. */
 KVX_API kvx_status kvx_stream_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
                                       const int32_t *d_src_slots, const kvx_layout_t *dsts,
                                       int32_t n_dsts, const int32_t *d_dst_slots,
