@@ -377,8 +377,11 @@ void fill_copy_args(kvx::CopyArgs &a, const Call &c, const kvx_request *d_reqs, 
   }
 }
 
+// engine: the call's KVX_ENGINE_* (read once per call, so that it matches what the planner
+// was told).
 kvx_status enqueue_copy(const Call &c, const kvx_request *d_reqs, void *d_buf, const void *d_ws,
-                        int32_t *d_status, cudaStream_t s, const int32_t *spec_src = nullptr,
+                        int32_t *d_status, cudaStream_t s, int32_t engine,
+                        const int32_t *spec_src = nullptr,
                         const int32_t *spec_dst = nullptr, int32_t *host_status = nullptr,
                         bool *host_status_written = nullptr) {
   if (host_status_written) *host_status_written = false;
@@ -395,25 +398,25 @@ kvx_status enqueue_copy(const Call &c, const kvx_request *d_reqs, void *d_buf, c
     const cudaError_t e = kvx::launch_narrow(a, s);
     return e == cudaSuccess ? KVX_OK : cuda_fail(e);
   }
-  if (kvx::copy_variant(a) == kvx::kVariantRow) {
+  const kvx::CopyVariant v = kvx::copy_variant(a, engine);
+  if (v == kvx::kVariantRow) {
     a.host_status = host_status;
     if (host_status_written) *host_status_written = host_status != nullptr;
     kvx::row_shape(a, &a.row_lanes, &a.rows_per_warp);
     const cudaError_t e = kvx::launch_copy(
-        a, (int)kvx::row_grid(c.n_tokens, c.planes, a.rows_per_warp), s);
+        a, v, (int)kvx::row_grid(c.n_tokens, c.planes, a.rows_per_warp), s);
     return e == cudaSuccess ? KVX_OK : cuda_fail(e);
   }
   a.spec_src = a.spec_dst = nullptr;  // the other kernels read the plan
   // one warp (register paths) or one thread (bulk path) per work item; at most n*P items
   const int64_t items = (int64_t)c.planes * c.n_tokens;
-  const kvx::CopyVariant v = kvx::copy_variant(a);
   const int64_t per_cta = v == kvx::kVariantBulk ? kvx::variant_threads(v) : kvx::kCopyThreads / 32;
   const bool small = kvx::num_tiles(c.n_tokens) <= kvx::kBulkSmallTiles;
   int64_t grid = (int64_t)di.sms * (small ? di.bps_small[v] : di.bps[v]);
   const int64_t need = (items + per_cta - 1) / per_cta;
   if (need < grid) grid = need;
   if (grid < 1) grid = 1;
-  cudaError_t e = kvx::launch_copy(a, (int)grid, s);
+  cudaError_t e = kvx::launch_copy(a, v, (int)grid, s);
   return e == cudaSuccess ? KVX_OK : cuda_fail(e);
 }
 
@@ -639,7 +642,8 @@ kvx_status kvx_execute(int32_t op, kvx_layout_t src, kvx_layout_t dst, const kvx
   if (n_tokens == 0) return KVX_OK;
   if ((st = check_ws(d_ws, ws_bytes, kvx::ws_layout(n_tokens, c.n_segs, false))) != KVX_OK)
     return st;
-  return enqueue_copy(c, d_reqs, d_buf, d_ws, d_status, reinterpret_cast<cudaStream_t>(stream));
+  return enqueue_copy(c, d_reqs, d_buf, d_ws, d_status, reinterpret_cast<cudaStream_t>(stream),
+                      kvx_get_copy_engine());
 }
 
 // gather / scatter / transfer of one slot-list request: one launch up to the fused limit,
@@ -661,6 +665,7 @@ static kvx_status run_call(const Call &c, const int32_t *d_src_slots, const int3
   kvx_status st;
   if (n > 0 && (st = check_ws(d_ws, ws_bytes, L)) != KVX_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int32_t engine = kvx_get_copy_engine();
   // Requests of up to the fused limit with rows under KVX_CHUNK_BYTES take the one-launch
   // path; the rest take the planner + row kernel (the row kernel overlaps the planner).
   const bool fused = call_chunk_rows(c) > 1 && !dup_check(c) &&
@@ -668,7 +673,7 @@ static kvx_status run_call(const Call &c, const int32_t *d_src_slots, const int3
   // small requests: one launch whose every CTA checks every index (no planner), unless the
   // duplicate check or the bulk engine was asked for
   const bool small = n > 0 && n <= kvx::kSmallMaxTokens && !fused && !dup_check(c) &&
-                     c.vec == 16 && kvx_get_copy_engine() != KVX_ENGINE_BULK;
+                     c.vec == 16 && engine != KVX_ENGINE_BULK;
   if (small) {
     static thread_local kvx::CopyArgs a;  // ~4 KiB of plane pointers: keep it off the stack
     fill_copy_args(a, c, nullptr, d_buf, d_ws, d_status);
@@ -684,11 +689,14 @@ static kvx_status run_call(const Call &c, const int32_t *d_src_slots, const int3
     kvx::PlanArgs a = plan_args(c, d_ws, d_status);
     a.src_idx = d_src_slots;
     a.dst_idx = d_dst_slots;
+    // The copy reads the slot lists itself (see CopyArgs::spec_src) and needs only the
+    // planner's verdict, except the TMA bulk kernel, which walks the plan's chunks.
+    a.validate_only = c.vec < 16 || engine != KVX_ENGINE_BULK;
     st = enqueue_plan(c, a, s);
     if (st != KVX_OK || n == 0) return st;
-    // the copy may read the slot lists itself (see CopyArgs::spec_src)
-    return enqueue_copy(c, nullptr, d_buf, d_ws, d_status, s, c.src ? d_src_slots : nullptr,
-                        c.dst ? d_dst_slots : nullptr, host_status, host_status_written);
+    return enqueue_copy(c, nullptr, d_buf, d_ws, d_status, s, engine,
+                        c.src ? d_src_slots : nullptr, c.dst ? d_dst_slots : nullptr,
+                        host_status, host_status_written);
   }
   return enqueue_fused(c, c.src ? d_src_slots : nullptr, c.dst ? d_dst_slots : nullptr, d_buf,
                        d_status, s);

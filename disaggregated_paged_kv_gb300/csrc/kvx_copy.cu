@@ -435,9 +435,9 @@ bool copy_is_linear(const CopyArgs &a) {
   return side_is_linear(a.src, a.row_bytes) && side_is_linear(a.dst, a.row_bytes);
 }
 
-CopyVariant copy_variant(const CopyArgs &a) {
+CopyVariant copy_variant(const CopyArgs &a, int32_t engine) {
   const bool linear = copy_is_linear(a);
-  if (linear && g_engine.load(std::memory_order_relaxed) == KVX_ENGINE_BULK) return kVariantBulk;
+  if (linear && engine == KVX_ENGINE_BULK) return kVariantBulk;
   // the row kernel takes every one-shot request (slot lists at hand) and every plan with
   // one-row chunks; multi-row plans keep the persistent kernels
   const bool spec = a.spec_src != nullptr || a.spec_dst != nullptr;
@@ -539,9 +539,8 @@ int variant_blocks_per_sm(CopyVariant v, int32_t n_tiles) {
   return nb;
 }
 
-cudaError_t launch_copy(const CopyArgs &a, int grid, cudaStream_t s) {
+cudaError_t launch_copy(const CopyArgs &a, CopyVariant v, int grid, cudaStream_t s) {
   const int32_t nt = (int32_t)num_tiles(a.n_tokens);
-  const CopyVariant v = copy_variant(a);
   void *args[] = {const_cast<CopyArgs *>(&a)};
   const void *fn = v == kVariantRow ? row_fn(a) : variant_fn(v);
   return launch_pdl(fn, dim3((unsigned)grid), dim3(variant_threads(v)), args, s,

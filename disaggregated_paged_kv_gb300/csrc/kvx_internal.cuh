@@ -131,7 +131,8 @@ struct PlanArgs {
   int32_t has_src, has_dst;
   int32_t status_direct;   // slots mode with a single tile: the CTA stores status[0] itself,
                            // and zeroes status[1 .. status_direct - 1]
-  int32_t validate_only;   // check the indices and write the status only (kvx_stream)
+  int32_t validate_only;   // check the indices and write the status only (no chunk table:
+                           // streamed calls, and one-shot calls whose copy reads the slot lists)
   // Duplicate-destination check (slots mode, destination pool): open-addressing table of
   // dup_mask + 1 words in the workspace, zeroed before the planner; entry = slot + 1.
   uint32_t *dup_table;     // nullptr: no check
@@ -210,12 +211,6 @@ struct StreamCtl {
   const int32_t *page_epochs;
 };
 
-// Launchers (enqueue only; return the launch's cudaError_t).
-cudaError_t launch_prefix(const PlanArgs &a, cudaStream_t s);
-cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
-cudaError_t launch_copy(const CopyArgs &a, int grid, cudaStream_t s);
-cudaError_t launch_export(const char *ws, WsLayout L, int64_t n_tokens, int32_t *out,
-                          int64_t max_chunks, int64_t *count, cudaStream_t s);
 // Copy kernel variants: row (non-persistent, one warp per group of tokens of one plane: every
 // one-shot request, and every plan with one-row chunks), lean (one request, linear multi-row
 // chunks, persistent, 32 registers), linear (batches of linear multi-row chunks), general
@@ -229,9 +224,18 @@ enum CopyVariant : int {
   kVariantRow,
   kNumVariants
 };
-CopyVariant copy_variant(const CopyArgs &a);
+
+// Launchers (enqueue only; return the launch's cudaError_t).
+cudaError_t launch_prefix(const PlanArgs &a, cudaStream_t s);
+cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
+// v: the variant copy_variant chose for these arguments and the call's engine.
+cudaError_t launch_copy(const CopyArgs &a, CopyVariant v, int grid, cudaStream_t s);
+cudaError_t launch_export(const char *ws, WsLayout L, int64_t n_tokens, int32_t *out,
+                          int64_t max_chunks, int64_t *count, cudaStream_t s);
+// engine: KVX_ENGINE_*, read once per call (kvx_get_copy_engine) so that the planner and the
+// copy of one call agree on it.
+CopyVariant copy_variant(const CopyArgs &a, int32_t engine);
 bool copy_is_linear(const CopyArgs &a);
-bool use_bulk(const CopyArgs &a);
 int variant_threads(CopyVariant v);
 int variant_blocks_per_sm(CopyVariant v, int32_t n_tiles);
 // Grid of the row variant: one warp per (group of rows_per_warp tokens, plane).
