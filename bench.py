@@ -76,7 +76,8 @@ def parse_args():
                          "tp: the headline request resharded between TP groups (kvx_reshard, and "
                          "kvx_move_heads pair by pair); "
                          "formats: MLA, fp8, narrow rows and cross-kind transcoding; "
-                         "comparators: other ways to move the headline bytes (context)")
+                         "comparators: other ways to move the headline bytes (context); "
+                         "sizes: the transfer time against the request size (T_setup + B/BW)")
     ap.add_argument("--check-duplicates", action="store_true",
                     help="kvx_set_check_duplicates(1) for this run (the planner also checks "
                          "every destination slot for repeats)")
@@ -471,7 +472,7 @@ def run_workload(args, name: str):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
 
-    def timed(K, flush_l2=True):
+    def timed(K, flush_l2=True, legs=legs):
         evs = []
         with torch.cuda.stream(stream):
             for i in range(K):
@@ -505,6 +506,25 @@ def run_workload(args, name: str):
     peaks, _ = measured_peaks()
     line["config"]["frac_of_measured_hbm"] = line["value"] / float(peaks["hbm_gbs"])
     line["config"]["frac_of_nominal_8tbs"] = line["value"] / NOMINAL_HBM_GBS
+    if name == "fragmented":
+        # the same request on the first 4 layers only (8 planes): ~7,700 fragments per direction
+        L4 = 4
+        sl4 = kvx.Layout(L4, Hw, Dw, kdt, w.num_slots, plane_ptrs=src_planes[:2 * L4])
+        dl4 = kvx.Layout(L4, Hw, Dw, kdt, w.num_slots, plane_ptrs=dst_planes[:2 * L4])
+        buf4 = buf[:2 * L4]
+        nb4 = 2 * 2 * L4 * w.n_tokens * Rw + 4 * w.n_tokens
+        legs4 = [("gather", lambda: kvx.gather(sl4, s_d, w.n_tokens, buf4, ws, st, stream=sp), nb4),
+                 ("scatter", lambda: kvx.scatter(dl4, d_d, w.n_tokens, buf4, ws, st, stream=sp), nb4)]
+        timed(3, legs=legs4)
+        assert int(st[0].item()) == kvx.OK, int(st[0].item())
+        r4 = timed(K, legs=legs4)
+        ms4 = statistics.mean(sum(r) for r in r4)
+        line["four_layers"] = {
+            "planes": 2 * L4, "fragments_per_direction": 2 * L4 * len(runs),
+            "us_per_step": ms4 * 1e3, "GBs": 2 * nb4 / (ms4 * 1e-3) / 1e9,
+            "frac_of_measured_hbm": 2 * nb4 / (ms4 * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
+            "legs_us": [statistics.mean(r[j] for r in r4) * 1e3 for j in range(2)],
+            "how": "the same 1536-token request on 4 layers (8 planes), gather then scatter"}
     if name == "small_gather_scatter":  # launch-bound, L2-resident unless flushed: warm too
         warm = timed(K, flush_l2=False)
         wm = statistics.mean(sum(r) for r in warm)
@@ -720,6 +740,98 @@ def run_comparators(args):
     print(json.dumps(line), flush=True)
 
 
+def run_sizes(args):
+    """The transfer-time model T = T_setup + B / BW_eff on this GPU: one-shot kvx_transfer of n
+    random tokens x 72 planes for n = 256 .. 16384, with 2 KiB rows (36 x K/V x 8 x 128 bf16)
+    and with 1 KiB rows (the same shape in fp8), between 65536-slot per-plane pools, beside a
+    contiguous device-to-device copy (torch copy_) of the same byte count.  L2 flushed before
+    every step; CUDA events on the launching stream.  The fit (least squares over n >= 1024)
+    splits each path's time into a fixed cost per call and a bandwidth."""
+    import numpy as np
+    import torch
+
+    from disaggregated_paged_kv_gb300 import kvx
+    from tests import inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kvx.lib()
+    stream = torch.cuda.Stream(device=dev)
+    sp = int(stream.cuda_stream)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    peaks, _ = measured_peaks()
+    NS, K = 65536, max(10, min(args.steps, 100))
+    sizes = [256, 512, 1024, 2048, 4096, 8192, 16384]
+
+    def timed(fn):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K + 3)]
+        with torch.cuda.stream(stream):
+            for i, (a, b) in enumerate(ev):
+                flush.fill_(i & 0xFF)
+                a.record(stream)
+                fn()
+                b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev[3:]) * 1e3  # us
+
+    def fit(pts):
+        x = np.array([b for b, _ in pts], dtype=np.float64)
+        y = np.array([t for _, t in pts], dtype=np.float64)
+        slope, icpt = np.polyfit(x, y, 1)
+        return {"t_setup_us": icpt, "bw_eff_gbs": 1e-3 / slope,
+                "bw_eff_frac_of_measured_hbm": 1e-3 / slope / float(peaks["hbm_gbs"])}
+
+    shapes = {"bf16_2KiB_rows": (2, kvx.BF16), "fp8_1KiB_rows": (1, kvx.FP8)}
+    results, copy_pts = {}, {}
+    for label, (e, dt) in shapes.items():
+        R = H * D * e
+        src = torch.randint(0, 255, (P * NS * R,), dtype=torch.uint8, device=dev)
+        dst = torch.zeros(P * NS * R, dtype=torch.uint8, device=dev)
+        sl = kvx.Layout(L, H, D, dt, NS, base=src, plane_stride=NS * R)
+        dl = kvx.Layout(L, H, D, dt, NS, base=dst, plane_stride=NS * R)
+        rows, pts = [], []
+        for n in sizes:
+            s_d = torch.from_numpy(inputs.distinct_slots(inputs.rng(2, inputs.ROLE_SRC_SLOTS), n, NS)).to(dev)
+            d_d = torch.from_numpy(inputs.distinct_slots(inputs.rng(2, inputs.ROLE_DST_SLOTS), n, NS)).to(dev)
+            ws = torch.empty(kvx.workspace_size(n, 0), dtype=torch.uint8, device=dev)
+            st = torch.zeros(1, dtype=torch.int32, device=dev)
+            us = timed(lambda: kvx.transfer(sl, s_d, dl, d_d, n, ws, st, stream=sp))
+            assert int(st.item()) == kvx.OK
+            alg = 2 * n * P * R + 8 * n
+            row = {"tokens": n, "alg_bytes": alg, "us": us, "GBs": alg / (us * 1e-6) / 1e9}
+            row["frac_of_measured_hbm"] = row["GBs"] / float(peaks["hbm_gbs"])
+            if n * P * R not in copy_pts:
+                nb = n * P * R
+                a, b = src[:nb], dst[:nb]
+                cu = timed(lambda: b.copy_(a))
+                copy_pts[nb] = cu
+            row["contiguous_copy_us"] = copy_pts[n * P * R]
+            rows.append(row)
+            if n >= 1024:
+                pts.append((alg, us))
+        results[label] = {"row_bytes": R, "points": rows, "fit": fit(pts)}
+        del src, dst, sl, dl
+        torch.cuda.empty_cache()
+    cfit = fit([(2 * nb, t) for nb, t in copy_pts.items() if nb >= 1024 * P * H * D])
+    head = next(r for r in results["bf16_2KiB_rows"]["points"] if r["tokens"] == N_TOK)
+    line = {
+        "metric": METRIC, "value": head["GBs"], "unit": UNIT, "n_gpus": 1, "steps": K,
+        "warmup": 3, "ms_per_step": head["us"] * 1e-3, "higher_is_better": True,
+        "dtype": "u8", "data": "synthetic (random bytes)",
+        "config": {"workload": "sizes: one-shot kvx_transfer of 256 .. 16384 random tokens x 72 "
+                               "planes (2 KiB bf16 and 1 KiB fp8 rows), 65536-slot per-plane "
+                               "pools, beside a contiguous copy of the same bytes; value = the "
+                               "2048-token 2 KiB-row point",
+                   "l2": "flushed before every timed step (write of 2x L2, outside the events)"},
+        "sizes": results,
+        "contiguous_copy_fit": cfit,
+        "gpu_launches": 2 * K * len(sizes) * len(shapes),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_formats(args):
     """Pool-to-pool transfers of one request of random slots in other layouts and dtypes, each
     timed like the headline (L2 flushed before every step, CUDA events around kvx_transfer):
@@ -729,6 +841,8 @@ def run_formats(args):
       gqa_fp8    the headline shape in fp8 (36 x K/V x 8 x 128: 1 KiB rows), 2048 tokens
       narrow     200-byte rows (one head of head_dim 100 fp16) through 8-byte accesses
       transcode  the headline shape from a slot-major pool into per-plane pools
+      slot_major the headline shape between two slot-major pools ([slot][36][K/V][8][128]: each
+                 token's 144 KiB contiguous)
     and, except the narrow rows, the same transfer through kvx_stream with every layer ready."""
     import numpy as np
     import torch
@@ -744,26 +858,31 @@ def run_formats(args):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     peaks, _ = measured_peaks()
-    # name: (layers, heads, head_dim, elem bytes, kv_planes, tokens, pool slots, src slot-major)
+    # name: (layers, heads, head_dim, elem bytes, kv_planes, tokens, pool slots,
+    #        source slot-major, destination slot-major)
     cases = {
-        "mla_bf16": (27, 1, 576, 2, 1, 16384, 65536, False),
-        "mla_fp8": (27, 1, 576, 1, 1, 16384, 65536, False),
-        "gqa_fp8": (36, 8, 128, 1, 2, 2048, 65536, False),
-        "narrow": (36, 1, 100, 2, 2, 16384, 65536, False),
-        "transcode": (36, 8, 128, 2, 2, 2048, 32768, True),
+        "mla_bf16": (27, 1, 576, 2, 1, 16384, 65536, False, False),
+        "mla_fp8": (27, 1, 576, 1, 1, 16384, 65536, False, False),
+        "gqa_fp8": (36, 8, 128, 1, 2, 2048, 65536, False, False),
+        "narrow": (36, 1, 100, 2, 2, 16384, 65536, False, False),
+        "transcode": (36, 8, 128, 2, 2, 2048, 32768, True, False),
+        "slot_major": (36, 8, 128, 2, 2, 2048, 32768, True, True),
     }
     dts = {1: kvx.FP8, 2: kvx.BF16}
     results = {}
-    for name, (Lc, Hc, Dc, e, kvp, n, NS, slot_major) in cases.items():
+    for name, (Lc, Hc, Dc, e, kvp, n, NS, src_sm, dst_sm) in cases.items():
         Pc, Rc = kvp * Lc, Hc * Dc * e
         src = torch.randint(0, 255, (Pc * NS * Rc,), dtype=torch.uint8, device=dev)
         dst = torch.zeros(Pc * NS * Rc, dtype=torch.uint8, device=dev)
-        if slot_major:
-            sl = kvx.Layout(Lc, Hc, Dc, dts[e], NS, base=src, plane_stride=Rc,
-                            slot_stride=Pc * Rc, kv_planes=kvp)
-        else:
-            sl = kvx.Layout(Lc, Hc, Dc, dts[e], NS, base=src, plane_stride=NS * Rc, kv_planes=kvp)
-        dl = kvx.Layout(Lc, Hc, Dc, dts[e], NS, base=dst, plane_stride=NS * Rc, kv_planes=kvp)
+
+        def layout(base, slot_major):
+            if slot_major:
+                return kvx.Layout(Lc, Hc, Dc, dts[e], NS, base=base, plane_stride=Rc,
+                                  slot_stride=Pc * Rc, kv_planes=kvp)
+            return kvx.Layout(Lc, Hc, Dc, dts[e], NS, base=base, plane_stride=NS * Rc,
+                              kv_planes=kvp)
+
+        sl, dl = layout(src, src_sm), layout(dst, dst_sm)
         s_d = torch.from_numpy(inputs.distinct_slots(inputs.rng(2, inputs.ROLE_SRC_SLOTS), n, NS)).to(dev)
         d_d = torch.from_numpy(inputs.distinct_slots(inputs.rng(2, inputs.ROLE_DST_SLOTS), n, NS)).to(dev)
         ws = torch.empty(kvx.workspace_size(n, 0), dtype=torch.uint8, device=dev)
@@ -780,8 +899,8 @@ def run_formats(args):
         assert int(st.item()) == kvx.OK
         # spot check token 7, plane 1: bytes equal
         k = 7
-        so = (int(s_d[k]) * Pc + 1) * Rc if slot_major else (NS + int(s_d[k])) * Rc
-        do = (NS + int(d_d[k])) * Rc
+        so = (int(s_d[k]) * Pc + 1) * Rc if src_sm else (NS + int(s_d[k])) * Rc
+        do = (int(d_d[k]) * Pc + 1) * Rc if dst_sm else (NS + int(d_d[k])) * Rc
         assert torch.equal(dst[do:do + Rc], src[so:so + Rc])
         K = args.steps
 
@@ -1282,6 +1401,9 @@ def main():
         return
     if args.workload == "comparators":
         run_comparators(args)
+        return
+    if args.workload == "sizes":
+        run_sizes(args)
         return
     if args.workload != "transfer":
         run_workload(args, args.workload)
