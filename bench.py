@@ -1208,7 +1208,18 @@ def run_stream(args):
     # every layer ready, through device ready words already raised; and on a persistent grid
     words = torch.ones(L, dtype=torch.int32, device=dev)
     words_ms = timed(layer_ready=words, ready_value=1)
-    persistent_ms = timed(max_ctas=2 * torch.cuda.get_device_properties(dev).multi_processor_count)
+    # persistent grids capped at a fraction of the SMs (the rest left to a producer), in the
+    # bulk (TMA) form and the register form
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    persistent = {"ctas": [], "registers_us": [], "bulk_us": []}
+    for ctas in (sms // 8, sms // 4, sms // 2, sms):
+        persistent["ctas"].append(ctas)
+        persistent["registers_us"].append(timed(max_ctas=ctas) * 1e3)
+        kvx.set_copy_engine(kvx.ENGINE_BULK)
+        try:
+            persistent["bulk_us"].append(timed(max_ctas=ctas) * 1e3)
+        finally:
+            kvx.set_copy_engine(kvx.ENGINE_AUTO)
 
     # epoch-fenced writes: the request's epoch word checked, or every destination page's owner
     # word checked (nothing cancelled or reassigned: the cost of the checks alone)
@@ -1299,7 +1310,10 @@ def run_stream(args):
                       "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
                       "includes": "planner + streamed copy + epilogue"},
         "all_ready_device_words_us": words_ms * 1e3,
-        "all_ready_persistent_2_per_sm_us": persistent_ms * 1e3,
+        "all_ready_persistent_grid": dict(persistent, how=(
+            "max_ctas CTAs for the whole move, one per SM at most; registers (the default): "
+            "32 warps per CTA; bulk (KVX_ENGINE_BULK): 96 threads per CTA, one 2 KiB "
+            "shared-memory stage each, TMA bulk copies")),
         "all_ready_request_epoch_checked_us": epoch_ms * 1e3,
         "all_ready_page_owners_checked_us": pages_ms * 1e3,
         "cancel_to_no_further_write_us": pct(cancels),

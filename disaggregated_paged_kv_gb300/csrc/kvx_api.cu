@@ -130,6 +130,7 @@ struct DeviceInfo {
   int bps_fused_linear = 0;               // one-launch path, linear rows
   int bps_fused_general = 0;              // one-launch path, general placement
   int bps_stream = 0;                     // layer-streamed copy
+  int bps_stream_bulk = 0;                // layer-streamed copy, bulk (TMA) form
 };
 
 std::atomic<int32_t> g_fused_max{0};  // measured: planner + row kernel is faster
@@ -160,7 +161,9 @@ kvx_status device_info(DeviceInfo *out) {
     d.bps_fused_linear = kvx::fused_blocks_per_sm(true);
     d.bps_fused_general = kvx::fused_blocks_per_sm(false);
     d.bps_stream = kvx::stream_blocks_per_sm();
-    if (d.bps_fused_linear <= 0 || d.bps_fused_general <= 0 || d.bps_stream <= 0) {
+    d.bps_stream_bulk = kvx::stream_bulk_blocks_per_sm();
+    if (d.bps_fused_linear <= 0 || d.bps_fused_general <= 0 || d.bps_stream <= 0 ||
+        d.bps_stream_bulk <= 0) {
       e = cudaGetLastError();
       return cuda_fail(e != cudaSuccess ? e : cudaErrorUnknown);
     }
@@ -993,15 +996,30 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
     return e == cudaSuccess ? KVX_OK : cuda_fail(e);
   }
   // persistent grid of at most max_ctas CTAs (at least one: it also runs the exit protocol)
+  if (kvx_get_copy_engine() == KVX_ENGINE_BULK) {
+    // bulk form: one thread per one-token item, a 2 KiB shared-memory stage each
+    kvx::stream_sizes(k, n, 1);
+    const int64_t per_cta = kvx::stream_bulk_threads();
+    int64_t grid = (int64_t)di.sms * di.bps_stream_bulk;
+    if (ctl->max_ctas < grid) grid = ctl->max_ctas;
+    const int64_t need = ((int64_t)k.items + per_cta - 1) / per_cta;
+    if (need < grid) grid = need;
+    if (grid < 1) grid = 1;
+    const int64_t per_thread = ((int64_t)k.items + grid * per_cta - 1) / (grid * per_cta);
+    k.block = (uint32_t)std::min<int64_t>(std::max<int64_t>(per_thread / 4, 1), 8);
+    e = kvx::launch_stream_bulk(a, k, (int)grid, s);
+    return e == cudaSuccess ? KVX_OK : cuda_fail(e);
+  }
   const int64_t warps = k.items;
   int64_t grid = (int64_t)di.sms * di.bps_stream;
   if (ctl->max_ctas < grid) grid = ctl->max_ctas;
-  const int64_t need = (warps + kvx::kCopyThreads / 32 - 1) / (kvx::kCopyThreads / 32);
+  const int64_t wpc = kvx::stream_threads() / 32;  // warps per CTA
+  const int64_t need = (warps + wpc - 1) / wpc;
   if (need < grid) grid = need;
   if (grid < 1) grid = 1;
   // about four blocks per warp: few layer entries per warp, yet each layer's items spread
   // over many warps (a late layer moves in a few row latencies)
-  const int64_t per_warp = (warps + grid * (kvx::kCopyThreads / 32) - 1) / (grid * (kvx::kCopyThreads / 32));
+  const int64_t per_warp = (warps + grid * wpc - 1) / (grid * wpc);
   k.block = (uint32_t)std::min<int64_t>(std::max<int64_t>(per_warp / 4, 1), 8);
   e = kvx::launch_stream(a, k, (int)grid, s);
   return e == cudaSuccess ? KVX_OK : cuda_fail(e);

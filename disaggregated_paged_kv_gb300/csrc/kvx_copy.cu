@@ -19,6 +19,7 @@
 // is the fused permute of "mini-infer系统实战-18-PD 解耦" (KV 序列化格式选择).
 #include <atomic>
 
+#include "kvx_bulk_ops.cuh"
 #include "kvx_copy_ops.cuh"
 #include "kvx_launch.cuh"
 
@@ -308,64 +309,11 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
 
 // ---- bulk (TMA) path ----------------------------------------------------------------------
 // For linear chunks only.  Every thread owns one kBulkStage-byte shared-memory stage and one
-// mbarrier: cp.async.bulk global -> shared (completion counted in bytes on the mbarrier), then
-// cp.async.bulk shared -> global, and the stage is reused once that store has read it.  Data
-// never passes through registers, so an SM keeps as many 2 KiB moves in flight as it has
-// stages.  Waits are bounded by %globaltimer: a wait that exceeds kWaitLimitNs (never expected)
-// sets KVX_ERR_TIMEOUT, drains this thread's transfers and ends the thread.
+// mbarrier: cp.async.bulk global -> shared, then shared -> global, and the stage is reused once
+// that store has read it (kvx_bulk_ops.cuh).  A wait that exceeds kBulkWaitLimitNs (never
+// expected) sets KVX_ERR_TIMEOUT, drains this thread's transfers and ends the thread.
 
-constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t *bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.b32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0; it < (1u << 30); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-  }
-  return false;
-}
-__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
-                                          uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-__device__ __forceinline__ void bulk_store(void *gdst, const void *smem_src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
-               "r"(smem_u32(smem_src)), "r"(bytes)
-               : "memory");
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
+using namespace bops;
 
 template <int kThreads, int kStage>
 __global__ void __launch_bounds__(kThreads) copy_bulk_kernel(const __grid_constant__ CopyArgs a) {
@@ -403,6 +351,7 @@ __global__ void __launch_bounds__(kThreads) copy_bulk_kernel(const __grid_consta
       }
       parity ^= 1u;
       bulk_store(const_cast<char *>(da.base) + off, stage, n);
+      bulk_commit();
     }
   }
   if (failed) {

@@ -257,8 +257,15 @@ constexpr int32_t kSmallMaxTokens = 512;
 cudaError_t launch_small(const CopyArgs &a, cudaStream_t s);
 // Layer-streamed copy (kvx_stream.cu): persistent grid over layer-major row groups.
 int stream_blocks_per_sm();
+int stream_threads();  // threads per CTA of the persistent grid
 void stream_sizes(StreamCtl &k, int64_t n_tokens, int32_t rows_per_warp);
 cudaError_t launch_stream(const CopyArgs &c, const StreamCtl &k, int grid, cudaStream_t s);
+// The same persistent grid moving whole one-token rows by TMA bulk copies (one shared-memory
+// stage per thread); sizes from stream_sizes(k, n, 1).  stream_bulk_blocks_per_sm also sets
+// the kernels' shared-memory limit (call it before the first launch).
+int stream_bulk_blocks_per_sm();
+int stream_bulk_threads();
+cudaError_t launch_stream_bulk(const CopyArgs &c, const StreamCtl &k, int grid, cudaStream_t s);
 // Row grid (one warp per item) and the epilogue that sets the "no further write" words.
 cudaError_t launch_stream_rows(const CopyArgs &c, const StreamCtl &k, cudaStream_t s);
 // One-launch path for single requests of up to KVX_FUSED_MAX_TOKENS tokens (kvx_fused.cu).

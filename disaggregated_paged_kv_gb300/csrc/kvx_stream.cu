@@ -40,6 +40,7 @@
 // them on every round and copies what it sees into the mirror.  Every wait is bounded by
 // wait_ns of %globaltimer and an iteration cap.  Waits only ever poll memory that the host or
 // another engine writes: no CTA waits for another CTA or another kernel.
+#include "kvx_bulk_ops.cuh"
 #include "kvx_copy_ops.cuh"
 #include "kvx_launch.cuh"
 #include "kvx_stream_ops.cuh"
@@ -49,8 +50,13 @@ namespace {
 
 using namespace ops;
 using namespace sops;
+using namespace bops;
 
 constexpr int kWarps = kCopyThreads / 32;
+// The persistent grid's CTAs: 32 warps, one CTA per SM, so that a grid capped at max_ctas
+// CTAs keeps 64 KiB of rows in flight on each of its SMs.
+constexpr int kPersistThreads = 1024;
+constexpr int kPersistWarps = kPersistThreads / 32;
 struct StreamArgs {
   CopyArgs c;   // sides, planes, buffer, status, slot lists (spec_src / spec_dst)
   StreamCtl k;
@@ -145,8 +151,34 @@ __device__ int32_t wait_layer(const StreamCtl &k, int32_t l, bool owner, CtaStat
   }
 }
 
+// Exit of a persistent grid's CTA (thread 0, once every thread of the CTA has made its last
+// write).  Warps of CTAs that started late may still be about to read the planner's verdict in
+// status[0], so no CTA writes its stop code there: the code goes into status[2] as a flag above
+// the count of finished CTAs, and the last CTA to finish folds the flags into status[0]
+// (CANCELLED over TIMEOUT) and sets the "no further write" words.
+constexpr int32_t kFinishedMask = (1 << 24) - 1;
+constexpr int32_t kTimeoutFlag = 1 << 24;
+constexpr int32_t kCancelledFlag = 1 << 25;
+
+__device__ void persistent_cta_exit(const CopyArgs &a, const StreamCtl &k, const CtaState &cs,
+                                    int32_t layers) {
+  if (cs.code) atomicOr(&a.status[2], cs.code == KVX_ERR_CANCELLED ? kCancelledFlag : kTimeoutFlag);
+  if (cs.stop < layers) atomicMax(&a.status[1], layers - cs.stop);
+  __threadfence_system();
+  const int32_t before = atomicAdd(&a.status[2], 1);
+  if ((before & kFinishedMask) == (int32_t)gridDim.x - 1) {
+    __threadfence_system();
+    const int32_t flags = atomicOr(&a.status[2], 0);  // every CTA set its flag before counting
+    if (flags & kCancelledFlag) atomicMax(&a.status[0], (int32_t)KVX_ERR_CANCELLED);
+    else if (flags & kTimeoutFlag) atomicMax(&a.status[0], (int32_t)KVX_ERR_TIMEOUT);
+    __threadfence_system();
+    st_release_sys(&a.status[3], 1);
+    if (k.host_done) st_release_sys(k.host_done, 1);
+  }
+}
+
 template <bool kSrcHnd, bool kDstHnd>
-__global__ void __launch_bounds__(kCopyThreads, 5) stream_kernel(const __grid_constant__ StreamArgs s) {
+__global__ void __launch_bounds__(kPersistThreads, 1) stream_kernel(const __grid_constant__ StreamArgs s) {
   __shared__ CtaState cs;
   const CopyArgs &a = s.c;
   const StreamCtl &k = s.k;
@@ -166,16 +198,16 @@ __global__ void __launch_bounds__(kCopyThreads, 5) stream_kernel(const __grid_co
   const int32_t rl = lane / m, li = lane - rl * m;
   const int32_t R = a.row_bytes, vpr = R >> 4;
   const bool sp = a.src.is_pool != 0, dp = a.dst.is_pool != 0;
-  // Blocks of kWarps * k.block consecutive items go to the CTAs in turn; warp w of a CTA takes
-  // items w, w + kWarps, ... of each of its blocks.  A warp's items still increase, and it
-  // enters a new layer about once per block rather than once per item.
-  const uint32_t bs = kWarps * k.block;
+  // Blocks of kPersistWarps * k.block consecutive items go to the CTAs in turn; warp w of a
+  // CTA takes items w, w + kPersistWarps, ... of each of its blocks.  A warp's items still
+  // increase, and it enters a new layer about once per block rather than once per item.
+  const uint32_t bs = kPersistWarps * k.block;
   const uint32_t stride = gridDim.x * bs;
   int32_t lcur = -1;
   bool verdict_ok = false;  // this warp has seen the planner's verdict (every index valid)
   uint32_t base = blockIdx.x * bs, j = 0;
   for (;; (++j == k.block) ? (j = 0, base += stride) : 0) {
-    const uint32_t i = base + j * kWarps + warp;
+    const uint32_t i = base + j * kPersistWarps + warp;
     if (i >= k.items) break;
     const int32_t l = (int32_t)(i / k.per_layer);
     if (l != lcur) {
@@ -237,16 +269,165 @@ __global__ void __launch_bounds__(kCopyThreads, 5) stream_kernel(const __grid_co
   pdl_wait();  // the planner's status words are written before any CTA reports
   __threadfence_system();
   __syncthreads();
-  if (threadIdx.x == 0) {
-    if (cs.code) atomicMax(&a.status[0], cs.code);
-    if (cs.stop < layers) atomicMax(&a.status[1], layers - cs.stop);
-    __threadfence_system();
-    if (atomicAdd(&a.status[2], 1) == (int32_t)gridDim.x - 1) {
-      __threadfence_system();
-      st_release_sys(&a.status[3], 1);
-      if (k.host_done) st_release_sys(k.host_done, 1);
-    }
+  if (threadIdx.x == 0) persistent_cta_exit(a, k, cs, layers);
+}
+
+// ---- persistent grid, bulk form ----------------------------------------------------------
+// The persistent grid's items with one token each, moved by TMA bulk copies instead of
+// registers (kvx_bulk_ops.cuh): every thread owns one kBulkStage-byte shared-memory stage and
+// one mbarrier and moves whole rows, global -> stage -> global, reusing its stage once the
+// previous store has read it.  A CTA of kBulkThreads threads keeps kBulkThreads stages in
+// flight (~192 KiB), where the register form keeps 16 KiB per CTA, so few SMs reach the copy
+// bandwidth: this is the form to leave most of the GPU to a producer.  Layer waits, stops,
+// page-owner checks and the exit protocol are the register form's.
+
+constexpr int kBulkThreads = 96;
+constexpr int kBulkStage = 2048;
+constexpr size_t kBulkSmem = (size_t)kBulkThreads * kBulkStage + 8 * kBulkThreads;
+
+// Bulk operations for bytes [x0, x0 + n) of a row of side s at `row` (row_base): one per
+// contiguous piece, i.e. the whole range, or on an HND pool side the part of each head vector
+// in the range.  Loads complete on bar; stores join the thread's open bulk async-group.
+template <bool kHnd, bool kLoad>
+__device__ __forceinline__ void bulk_row_range(const Side &s, bool pool, const char *row,
+                                               int32_t x0, int32_t n, unsigned char *stage,
+                                               uint64_t *bar) {
+  if (!kHnd || !pool) {
+    if constexpr (kLoad) bulk_load(stage, row + x0, (uint32_t)n, bar);
+    else bulk_store(const_cast<char *>(row) + x0, stage, (uint32_t)n);
+    return;
   }
+  const int32_t seg = s.seg_bytes, end = x0 + n;
+  for (int32_t x = x0; x < end;) {
+    const int32_t h = x / seg, off = x - h * seg;
+    const int32_t len = min(seg - off, end - x);
+    const char *g = row + (int64_t)h * s.page_size * seg + off;
+    if constexpr (kLoad) bulk_load(stage + (x - x0), g, (uint32_t)len, bar);
+    else bulk_store(const_cast<char *>(g), stage + (x - x0), (uint32_t)len);
+    x += len;
+  }
+}
+
+template <bool kSrcHnd, bool kDstHnd>
+__global__ void __launch_bounds__(kBulkThreads, 1)
+    stream_bulk_kernel(const __grid_constant__ StreamArgs s) {
+  extern __shared__ __align__(128) unsigned char smem[];  // stages | mbarriers
+  __shared__ CtaState cs;
+  const CopyArgs &a = s.c;
+  const StreamCtl &k = s.k;
+  const int32_t layers = k.layers;
+  unsigned char *stage = smem + threadIdx.x * kBulkStage;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + (size_t)kBulkThreads * kBulkStage) + threadIdx.x;
+  if (threadIdx.x < kReadyWords) {
+    cs.ready[threadIdx.x] = 0;
+    cs.polling[threadIdx.x] = 0;
+  }
+  if (threadIdx.x == 0) {
+    cs.stop = layers;
+    cs.code = 0;
+  }
+  mbar_init(bar);
+  __syncthreads();
+
+  const int32_t R = a.row_bytes;
+  const bool sp = a.src.is_pool != 0, dp = a.dst.is_pool != 0;
+  // Blocks of kBulkThreads * k.block consecutive items go to the CTAs in turn; thread x of a
+  // CTA takes items x, x + kBulkThreads, ... of each of its blocks, so its layers increase.
+  const uint32_t bs = kBulkThreads * k.block;
+  const uint32_t stride = gridDim.x * bs;
+  int32_t lcur = -1;
+  bool verdict_ok = false;  // this thread has seen the planner's verdict (every index valid)
+  bool stuck = false;       // a bulk load did not complete in time (never expected)
+  uint32_t parity = 0;
+  // The token of item i: the row of layer i / per_layer, K or V, token r mod groups.
+  auto token_of = [&](uint32_t i) -> int64_t {
+    const uint32_t r = i % k.per_layer;
+    return (int64_t)(r >= k.groups ? r - k.groups : r);
+  };
+  // Each item's slot indices are loaded one item ahead, while the previous row's bulk load is
+  // in flight, so that a thread's rows follow each other without an index round trip between.
+  uint32_t base = blockIdx.x * bs, j = 0;
+  uint32_t i = base + threadIdx.x;
+  int32_t si = 0, di = 0;
+  if (i < k.items) {
+    const int64_t t = token_of(i);
+    si = sp ? a.spec_src[t] : (int32_t)t;
+    di = dp ? a.spec_dst[t] : (int32_t)t;
+  }
+  while (i < k.items) {
+    if (++j == k.block) {
+      j = 0;
+      base += stride;
+    }
+    const uint32_t inext = base + j * kBulkThreads + threadIdx.x;
+    const int32_t l = (int32_t)(i / k.per_layer);
+    if (l != lcur) {
+      const bool owner = blockIdx.x == ((uint64_t)l * k.per_layer / bs) % gridDim.x;
+      if (!wait_layer(k, l, owner, &cs)) break;
+      fence_proxy_async_global();  // the layer's rows, seen by the acquire, reach the bulk loads
+      lcur = l;
+    }
+    const uint32_t r = i - (uint32_t)l * k.per_layer;
+    const int32_t p = k.kv_planes * l + (r >= k.groups ? 1 : 0);  // K or V (0 with MLA)
+    const bool ok = (!sp || (si >= 0 && (int64_t)si < a.src.num_slots)) &&
+                    (!dp || (di >= 0 && (int64_t)di < a.dst.num_slots));
+    if (!ok) {  // the planner refuses the request: nothing may be stored
+      pdl_wait();
+      atomicMin(&cs.stop, 0);
+      break;
+    }
+    const char *buf_plane = a.buf + (int64_t)p * a.n_tokens * R;
+    const char *srow = row_base<kSrcHnd>(a.src, sp, a.src_planes[p], buf_plane, si, R);
+    char *drow = const_cast<char *>(row_base<kDstHnd>(a.dst, dp, a.dst_planes[p], buf_plane, di, R));
+    const int32_t di_row = di;
+    bool drop = false, stop = false;
+    for (int32_t x0 = 0; x0 < R; x0 += kBulkStage) {
+      const int32_t n = min(kBulkStage, R - x0);
+      bulk_wait_read_all();  // the previous store has finished reading the stage
+      mbar_expect_tx(bar, (uint32_t)n);
+      bulk_row_range<kSrcHnd, true>(a.src, sp, srow, x0, n, stage, bar);
+      if (x0 == 0 && inext < k.items) {  // the next item's indices, under this load
+        const int64_t tn = token_of(inext);
+        si = sp ? a.spec_src[tn] : (int32_t)tn;
+        di = dp ? a.spec_dst[tn] : (int32_t)tn;
+      }
+      if (!verdict_ok) {  // the first row's load goes out before the planner's verdict
+        pdl_wait();       // the planner has checked every index and written status[0]
+        if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK) {
+          atomicMin(&cs.stop, 0);
+          stop = true;
+        }
+        verdict_ok = !stop;
+      }
+      if (!mbar_wait_bounded(bar, parity)) {
+        stuck = true;
+        give_up(&cs, l, KVX_ERR_TIMEOUT);
+        break;
+      }
+      parity ^= 1u;
+      if (stop) break;
+      if (x0 == 0 && dp && k.page_epochs && !page_owned(k, di_row)) {
+        // the page went to another request: the row is dropped and reported
+        drop = true;
+        atomicMax(&cs.code, (int32_t)KVX_ERR_CANCELLED);
+        atomicMax(&a.status[1], layers - l);
+      }
+      if (drop) break;
+      bulk_row_range<kDstHnd, false>(a.dst, dp, drow, x0, n, stage, bar);
+      bulk_commit();
+    }
+    if (stuck || stop) break;
+    i = inext;
+  }
+  if (stuck) (void)mbar_wait_bounded(bar, parity);  // let the late load land before leaving
+  bulk_wait_all();             // every store of this thread is complete
+  fence_proxy_async_global();  // ... and ordered before the generic-proxy release below
+
+  // every thread's writes before this CTA's report; the last CTA's release covers all CTAs
+  pdl_wait();  // the planner's status words are written before any CTA reports
+  __threadfence_system();
+  __syncthreads();
+  if (threadIdx.x == 0) persistent_cta_exit(a, k, cs, layers);
 }
 
 // ---- row grid ------------------------------------------------------------------------
@@ -365,12 +546,43 @@ const void *stream_fn(bool sh, bool dh) {
   return reinterpret_cast<const void *>(stream_kernel<false, false>);
 }
 
+const void *stream_bulk_fn(bool sh, bool dh) {
+  if (sh && dh) return reinterpret_cast<const void *>(stream_bulk_kernel<true, true>);
+  if (sh) return reinterpret_cast<const void *>(stream_bulk_kernel<true, false>);
+  if (dh) return reinterpret_cast<const void *>(stream_bulk_kernel<false, true>);
+  return reinterpret_cast<const void *>(stream_bulk_kernel<false, false>);
+}
+
 }  // namespace
+
+int stream_bulk_blocks_per_sm() {
+  for (int v = 0; v < 4; ++v)
+    if (cudaFuncSetAttribute(stream_bulk_fn(v & 1, v & 2), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kBulkSmem) != cudaSuccess)
+      return 0;
+  int nb = 0;
+  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &nb, stream_bulk_fn(false, false), kBulkThreads, kBulkSmem);
+  return e == cudaSuccess ? nb : 0;
+}
+
+int stream_bulk_threads() { return kBulkThreads; }
+int stream_threads() { return kPersistThreads; }
+
+cudaError_t launch_stream_bulk(const CopyArgs &c, const StreamCtl &k, int grid, cudaStream_t s) {
+  static thread_local StreamArgs args;  // ~4 KiB of plane pointers: keep it off the stack
+  args.c = c;
+  args.k = k;
+  const bool sh = c.src.hnd && c.src.is_pool, dh = c.dst.hnd && c.dst.is_pool;
+  void *params[] = {&args};
+  return launch_pdl(stream_bulk_fn(sh, dh), dim3((unsigned)grid), dim3(kBulkThreads), params, s,
+                    kBulkSmem);
+}
 
 int stream_blocks_per_sm() {
   int nb = 0;
   const cudaError_t e =
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, stream_kernel<false, false>, kCopyThreads, 0);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, stream_kernel<false, false>, kPersistThreads, 0);
   return e == cudaSuccess ? nb : 0;
 }
 
@@ -388,7 +600,7 @@ cudaError_t launch_stream(const CopyArgs &c, const StreamCtl &k, int grid, cudaS
   args.k = k;
   const bool sh = c.src.hnd && c.src.is_pool, dh = c.dst.hnd && c.dst.is_pool;
   void *params[] = {&args};
-  return launch_pdl(stream_fn(sh, dh), dim3((unsigned)grid), dim3(kCopyThreads), params, s);
+  return launch_pdl(stream_fn(sh, dh), dim3((unsigned)grid), dim3(kPersistThreads), params, s);
 }
 
 cudaError_t launch_stream_rows(const CopyArgs &c, const StreamCtl &k, cudaStream_t s) {

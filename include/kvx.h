@@ -423,9 +423,11 @@ typedef struct kvx_stream_ctl {
    * abnormal path needs a lease or a timeout). */
   int64_t wait_ns;
   /* 0: one warp per row (group) on as many CTAs as the request needs; CTAs waiting for a
-   * layer hold their SM slots.  > 0: a persistent grid of at most max_ctas CTAs (of 256
-   * threads) for the whole move, leaving the rest of the GPU to a producer running on the
-   * same GPU, which needs SMs to make progress. */
+   * layer hold their SM slots.  > 0: a persistent grid of at most max_ctas CTAs, at most one
+   * per SM (1024 threads moving rows through registers; with kvx_set_copy_engine(
+   * KVX_ENGINE_BULK), 96 threads moving rows by TMA bulk copies through shared memory), for
+   * the whole move, leaving the rest of the GPU to a producer running on the same GPU, which
+   * needs SMs to make progress. */
   int32_t max_ctas;
   int32_t reserved;  /* must be 0 */
   /* Pinned host int32 or NULL: set to 1 when d_status[3] is (see kvx_stream). */

@@ -11,6 +11,8 @@ What is checked:
     ends long before the wait bound with KVX_ERR_CANCELLED, layers below the waiting one moved
     and the rest untouched; a request cancelled before the launch moves nothing;
   * the "no further write" words (status[3] and the pinned host word) are set in every case.
+Each case runs on the default grid and on a persistent grid of 40 CTAs, in both of its forms
+(registers, and TMA bulk copies through shared-memory stages).
 
 Every failure is made on the host: a ready word that nothing raises, an epoch word the host
 changes.  Every device wait is bounded (wait_ns), so no case can hang the GPU.
@@ -41,10 +43,18 @@ def _cuda():
     yield
 
 
-# max_ctas: 0 = one warp per row group (default grid); 40 = a persistent grid of 40 CTAs
-@pytest.fixture(params=[0, 40], ids=["rowgrid", "persistent40"])
+# max_ctas: 0 = one warp per row group (default grid); 40 = a persistent grid of 40 CTAs,
+# in its register form (the default) and its bulk (TMA) form
+GRIDS = {"rowgrid": (0, kvx.ENGINE_AUTO), "persistent40": (40, kvx.ENGINE_AUTO),
+         "persistent40_bulk": (40, kvx.ENGINE_BULK)}
+
+
+@pytest.fixture(params=list(GRIDS))
 def grid(request):
-    return request.param
+    max_ctas, engine = GRIDS[request.param]
+    kvx.set_copy_engine(engine)
+    yield max_ctas
+    kvx.set_copy_engine(kvx.ENGINE_AUTO)
 
 
 def _rng(k):
@@ -148,18 +158,55 @@ def test_stream_gather_and_scatter(kind, grid):
     hz.assert_same_bytes(dst.readback(), exp.host, f"stream scatter {kind}")
 
 
-def test_stream_2k_rows_few_ctas():
-    """2 KiB rows (one token per warp) on a grid capped at 3 CTAs: every warp walks many
-    layers' items."""
+@pytest.mark.parametrize("engine", [kvx.ENGINE_AUTO, kvx.ENGINE_BULK], ids=["registers", "bulk"])
+def test_stream_2k_rows_few_ctas(engine):
+    """2 KiB rows (one token per warp) on a grid capped at 3 CTAs: every warp (every thread of
+    the bulk form) walks many layers' items."""
     n = 2048
     src, dst, s, d, exp = _transfer_case("planes", n, sh=SH2K, seed=90)
     st = _status()
     done = _pinned_i32([0])
-    _run_transfer(src, dst, s, d, n, st, max_ctas=3, host_done=done)
-    torch.cuda.synchronize()
+    kvx.set_copy_engine(engine)
+    try:
+        _run_transfer(src, dst, s, d, n, st, max_ctas=3, host_done=done)
+        torch.cuda.synchronize()
+    finally:
+        kvx.set_copy_engine(kvx.ENGINE_AUTO)
     assert st.cpu().tolist()[0:2] == [kvx.OK, 0] and st[3].item() == 1
     assert int(done[0]) == 1
     hz.assert_same_bytes(dst.readback(), exp.host, "stream 2k rows, 3 CTAs")
+
+
+SH_LONG = dict(L=3, H=3, D=768, dtype="bf16")  # 4608-byte rows of three 1536-byte head vectors
+
+
+@pytest.mark.parametrize("kinds", [("planes", "hnd"), ("hnd", "slot_major"), ("hnd", "hnd")])
+@pytest.mark.parametrize("max_ctas", [1, 8])
+@pytest.mark.parametrize("engine", [kvx.ENGINE_AUTO, kvx.ENGINE_BULK], ids=["registers", "bulk"])
+def test_stream_bulk_rows_longer_than_a_stage(kinds, max_ctas, engine):
+    """The bulk form's rows longer than its 2 KiB stage, in three pieces whose boundaries cut
+    head vectors (1536 bytes, not a power of two) on HND sides: every piece reaches the right
+    bytes of the right pages."""
+    n = 300
+    g = _rng(130 + max_ctas + len(kinds[0]) + 3 * len(kinds[1]))
+    src = _pool(kinds[0], "normal", g, num_slots=1024, sh=SH_LONG)
+    dst = _pool(kinds[1], "sentinel", salt=13, num_slots=1024, sh=SH_LONG)
+    exp = _expected_pool(kinds[1], 1024, 13, sh=SH_LONG)
+    s = _slots(131, n, 1024)
+    d = _slots(132, n, 1024)
+    assert oracle.transfer(hz.oracle_pool(src), s, hz.oracle_pool(exp), d)[0] == oracle.OK
+    st = _status()
+    ready = torch.ones(SH_LONG["L"], dtype=torch.int32, device="cuda")
+    kvx.set_copy_engine(engine)
+    try:
+        _run_transfer(src, dst, s, d, n, st, layer_ready=ready, ready_value=1, max_ctas=max_ctas)
+        torch.cuda.synchronize()
+    finally:
+        kvx.set_copy_engine(kvx.ENGINE_AUTO)
+    v = st.cpu().tolist()
+    assert v[0:2] == [kvx.OK, 0] and v[3] == 1, v
+    hz.assert_same_bytes(dst.readback(), exp.host, f"long rows {kinds}, {max_ctas} CTAs")
+    hz.assert_same_bytes(src.readback(), src.host, "source")
 
 
 def test_stream_n0_and_out_of_range(grid):
