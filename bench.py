@@ -1211,15 +1211,16 @@ def run_stream(args):
     # persistent grids capped at a fraction of the SMs (the rest left to a producer), in the
     # bulk (TMA) form and the register form
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    persistent = {"ctas": [], "registers_us": [], "bulk_us": []}
+    persistent = {"ctas": [], "mixed_us": [], "registers_us": [], "bulk_us": []}
     for ctas in (sms // 8, sms // 4, sms // 2, sms):
         persistent["ctas"].append(ctas)
-        persistent["registers_us"].append(timed(max_ctas=ctas) * 1e3)
-        kvx.set_copy_engine(kvx.ENGINE_BULK)
-        try:
-            persistent["bulk_us"].append(timed(max_ctas=ctas) * 1e3)
-        finally:
-            kvx.set_copy_engine(kvx.ENGINE_AUTO)
+        for key, engine in (("mixed_us", kvx.ENGINE_AUTO), ("registers_us", kvx.ENGINE_REGISTERS),
+                            ("bulk_us", kvx.ENGINE_BULK)):
+            kvx.set_copy_engine(engine)
+            try:
+                persistent[key].append(timed(max_ctas=ctas) * 1e3)
+            finally:
+                kvx.set_copy_engine(kvx.ENGINE_AUTO)
 
     # epoch-fenced writes: the request's epoch word checked, or every destination page's owner
     # word checked (nothing cancelled or reassigned: the cost of the checks alone)
@@ -1311,9 +1312,10 @@ def run_stream(args):
                       "includes": "planner + streamed copy + epilogue"},
         "all_ready_device_words_us": words_ms * 1e3,
         "all_ready_persistent_grid": dict(persistent, how=(
-            "max_ctas CTAs for the whole move, one per SM at most; registers (the default): "
-            "32 warps per CTA; bulk (KVX_ENGINE_BULK): 96 threads per CTA, one 2 KiB "
-            "shared-memory stage each, TMA bulk copies")),
+            "max_ctas CTAs for the whole move, one per SM at most; mixed (the default): 29 "
+            "register warps and 3 warps of TMA bulk-copy threads per CTA (one 2 KiB shared-"
+            "memory stage each); registers (KVX_ENGINE_REGISTERS): 32 register warps; bulk "
+            "(KVX_ENGINE_BULK): 96 TMA bulk-copy threads")),
         "all_ready_request_epoch_checked_us": epoch_ms * 1e3,
         "all_ready_page_owners_checked_us": pages_ms * 1e3,
         "cancel_to_no_further_write_us": pct(cancels),

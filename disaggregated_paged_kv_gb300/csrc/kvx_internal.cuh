@@ -263,6 +263,11 @@ cudaError_t launch_stream(const CopyArgs &c, const StreamCtl &k, int grid, cudaS
 // The same persistent grid moving whole one-token rows by TMA bulk copies (one shared-memory
 // stage per thread); sizes from stream_sizes(k, n, 1).  stream_bulk_blocks_per_sm also sets
 // the kernels' shared-memory limit (call it before the first launch).
+// Mixed form (the default when it fits): the register CTA with three warps of TMA bulk-copy
+// workers; for calls whose row groups fit one 2 KiB stage and one register pass.
+int stream_mixed_blocks_per_sm();
+bool stream_mixed_fits(const CopyArgs &c);
+cudaError_t launch_stream_mixed(const CopyArgs &c, const StreamCtl &k, int grid, cudaStream_t s);
 int stream_bulk_blocks_per_sm();
 int stream_bulk_threads();
 cudaError_t launch_stream_bulk(const CopyArgs &c, const StreamCtl &k, int grid, cudaStream_t s);

@@ -11,8 +11,8 @@ What is checked:
     ends long before the wait bound with KVX_ERR_CANCELLED, layers below the waiting one moved
     and the rest untouched; a request cancelled before the launch moves nothing;
   * the "no further write" words (status[3] and the pinned host word) are set in every case.
-Each case runs on the default grid and on a persistent grid of 40 CTAs, in both of its forms
-(registers, and TMA bulk copies through shared-memory stages).
+Each case runs on the default grid and on a persistent grid of 40 CTAs in its three forms
+(register and TMA bulk-copy warps mixed, registers only, TMA bulk copies only).
 
 Every failure is made on the host: a ready word that nothing raises, an epoch word the host
 changes.  Every device wait is bounded (wait_ns), so no case can hang the GPU.
@@ -43,10 +43,14 @@ def _cuda():
     yield
 
 
-# max_ctas: 0 = one warp per row group (default grid); 40 = a persistent grid of 40 CTAs,
-# in its register form (the default) and its bulk (TMA) form
+# max_ctas: 0 = one warp per row group (default grid); 40 = a persistent grid of 40 CTAs, in
+# its mixed form (the default: register warps and TMA bulk-copy warps), its register form and
+# its bulk (TMA) form
 GRIDS = {"rowgrid": (0, kvx.ENGINE_AUTO), "persistent40": (40, kvx.ENGINE_AUTO),
+         "persistent40_registers": (40, kvx.ENGINE_REGISTERS),
          "persistent40_bulk": (40, kvx.ENGINE_BULK)}
+ENGINES = dict(ids=["mixed", "registers", "bulk"])
+ENGINE_LIST = [kvx.ENGINE_AUTO, kvx.ENGINE_REGISTERS, kvx.ENGINE_BULK]
 
 
 @pytest.fixture(params=list(GRIDS))
@@ -158,7 +162,7 @@ def test_stream_gather_and_scatter(kind, grid):
     hz.assert_same_bytes(dst.readback(), exp.host, f"stream scatter {kind}")
 
 
-@pytest.mark.parametrize("engine", [kvx.ENGINE_AUTO, kvx.ENGINE_BULK], ids=["registers", "bulk"])
+@pytest.mark.parametrize("engine", ENGINE_LIST, **ENGINES)
 def test_stream_2k_rows_few_ctas(engine):
     """2 KiB rows (one token per warp) on a grid capped at 3 CTAs: every warp (every thread of
     the bulk form) walks many layers' items."""
@@ -184,6 +188,7 @@ SH_LONG = dict(L=3, H=3, D=768, dtype="bf16")  # 4608-byte rows of three 1536-by
 @pytest.mark.parametrize("max_ctas", [1, 8])
 @pytest.mark.parametrize("engine", [kvx.ENGINE_AUTO, kvx.ENGINE_BULK], ids=["registers", "bulk"])
 def test_stream_bulk_rows_longer_than_a_stage(kinds, max_ctas, engine):
+    # (rows longer than a stage take the register form under the default engine)
     """The bulk form's rows longer than its 2 KiB stage, in three pieces whose boundaries cut
     head vectors (1536 bytes, not a power of two) on HND sides: every piece reaches the right
     bytes of the right pages."""
