@@ -131,7 +131,6 @@ struct DeviceInfo {
   int bps_fused_general = 0;              // one-launch path, general placement
   int bps_stream = 0;                     // layer-streamed copy
   int bps_stream_bulk = 0;                // layer-streamed copy, bulk (TMA) form
-  int bps_stream_mixed = 0;               // layer-streamed copy, mixed form
 };
 
 std::atomic<int32_t> g_fused_max{0};  // measured: planner + row kernel is faster
@@ -163,9 +162,8 @@ kvx_status device_info(DeviceInfo *out) {
     d.bps_fused_general = kvx::fused_blocks_per_sm(false);
     d.bps_stream = kvx::stream_blocks_per_sm();
     d.bps_stream_bulk = kvx::stream_bulk_blocks_per_sm();
-    d.bps_stream_mixed = kvx::stream_mixed_blocks_per_sm();
     if (d.bps_fused_linear <= 0 || d.bps_fused_general <= 0 || d.bps_stream <= 0 ||
-        d.bps_stream_bulk <= 0 || d.bps_stream_mixed <= 0) {
+        d.bps_stream_bulk <= 0) {
       e = cudaGetLastError();
       return cuda_fail(e != cudaSuccess ? e : cudaErrorUnknown);
     }
@@ -1013,10 +1011,10 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
     return e == cudaSuccess ? KVX_OK : cuda_fail(e);
   }
   // register CTAs of 32 warps; with the default engine, three of the warps move their rows by
-  // TMA bulk copies where a row group fits one stage (the mixed form)
-  const bool mixed = kvx_get_copy_engine() == KVX_ENGINE_AUTO && kvx::stream_mixed_fits(a);
+  // TMA bulk copies where a row group fits one stage
+  const bool tma = kvx_get_copy_engine() == KVX_ENGINE_AUTO && kvx::stream_tma_fits(a);
   const int64_t warps = k.items;
-  int64_t grid = (int64_t)di.sms * (mixed ? di.bps_stream_mixed : di.bps_stream);
+  int64_t grid = (int64_t)di.sms * di.bps_stream;
   if (ctl->max_ctas < grid) grid = ctl->max_ctas;
   const int64_t wpc = kvx::stream_threads() / 32;  // warps per CTA
   const int64_t need = (warps + wpc - 1) / wpc;
@@ -1026,7 +1024,7 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
   // over many warps (a late layer moves in a few row latencies)
   const int64_t per_warp = (warps + grid * wpc - 1) / (grid * wpc);
   k.block = (uint32_t)std::min<int64_t>(std::max<int64_t>(per_warp / 4, 1), 8);
-  e = mixed ? kvx::launch_stream_mixed(a, k, (int)grid, s) : kvx::launch_stream(a, k, (int)grid, s);
+  e = kvx::launch_stream(a, k, (int)grid, tma, s);
   return e == cudaSuccess ? KVX_OK : cuda_fail(e);
 }
 

@@ -255,19 +255,18 @@ int32_t narrow_group_shift(int32_t row_bytes, int32_t vec_bytes);
 // One-launch path of small one-shot requests (kvx_small.cu): every CTA checks every index.
 constexpr int32_t kSmallMaxTokens = 512;
 cudaError_t launch_small(const CopyArgs &a, cudaStream_t s);
-// Layer-streamed copy (kvx_stream.cu): persistent grid over layer-major row groups.
+// Layer-streamed copy (kvx_stream.cu): persistent grid over layer-major row groups, one
+// 1024-thread CTA per SM; tma: three of its warps move row groups by TMA bulk copies (only
+// where stream_tma_fits).  stream_blocks_per_sm also sets the kernels' shared-memory limit.
 int stream_blocks_per_sm();
 int stream_threads();  // threads per CTA of the persistent grid
+bool stream_tma_fits(const CopyArgs &c);
 void stream_sizes(StreamCtl &k, int64_t n_tokens, int32_t rows_per_warp);
-cudaError_t launch_stream(const CopyArgs &c, const StreamCtl &k, int grid, cudaStream_t s);
-// The same persistent grid moving whole one-token rows by TMA bulk copies (one shared-memory
-// stage per thread); sizes from stream_sizes(k, n, 1).  stream_bulk_blocks_per_sm also sets
-// the kernels' shared-memory limit (call it before the first launch).
-// Mixed form (the default when it fits): the register CTA with three warps of TMA bulk-copy
-// workers; for calls whose row groups fit one 2 KiB stage and one register pass.
-int stream_mixed_blocks_per_sm();
-bool stream_mixed_fits(const CopyArgs &c);
-cudaError_t launch_stream_mixed(const CopyArgs &c, const StreamCtl &k, int grid, cudaStream_t s);
+cudaError_t launch_stream(const CopyArgs &c, const StreamCtl &k, int grid, bool tma,
+                          cudaStream_t s);
+// The same walk with one-token rows moved only by TMA bulk copies (one shared-memory stage per
+// thread, rows of any length in pieces); sizes from stream_sizes(k, n, 1).
+// stream_bulk_blocks_per_sm also sets the kernels' shared-memory limit.
 int stream_bulk_blocks_per_sm();
 int stream_bulk_threads();
 cudaError_t launch_stream_bulk(const CopyArgs &c, const StreamCtl &k, int grid, cudaStream_t s);

@@ -40,6 +40,8 @@
 // them on every round and copies what it sees into the mirror.  Every wait is bounded by
 // wait_ns of %globaltimer and an iteration cap.  Waits only ever poll memory that the host or
 // another engine writes: no CTA waits for another CTA or another kernel.
+#include <algorithm>
+
 #include "kvx_bulk_ops.cuh"
 #include "kvx_copy_ops.cuh"
 #include "kvx_launch.cuh"
@@ -175,101 +177,6 @@ __device__ void persistent_cta_exit(const CopyArgs &a, const StreamCtl &k, const
     st_release_sys(&a.status[3], 1);
     if (k.host_done) st_release_sys(k.host_done, 1);
   }
-}
-
-template <bool kSrcHnd, bool kDstHnd>
-__global__ void __launch_bounds__(kPersistThreads, 1) stream_kernel(const __grid_constant__ StreamArgs s) {
-  __shared__ CtaState cs;
-  const CopyArgs &a = s.c;
-  const StreamCtl &k = s.k;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int32_t layers = k.layers;
-  if (threadIdx.x < kReadyWords) {
-    cs.ready[threadIdx.x] = 0;
-    cs.polling[threadIdx.x] = 0;
-  }
-  if (threadIdx.x == 0) {
-    cs.stop = layers;
-    cs.code = 0;
-  }
-  __syncthreads();
-
-  const int32_t m = a.row_lanes, G = a.rows_per_warp;  // lanes per token, tokens per warp
-  const int32_t rl = lane / m, li = lane - rl * m;
-  const int32_t R = a.row_bytes, vpr = R >> 4;
-  const bool sp = a.src.is_pool != 0, dp = a.dst.is_pool != 0;
-  // Blocks of kPersistWarps * k.block consecutive items go to the CTAs in turn; warp w of a
-  // CTA takes items w, w + kPersistWarps, ... of each of its blocks.  A warp's items still
-  // increase, and it enters a new layer about once per block rather than once per item.
-  const uint32_t bs = kPersistWarps * k.block;
-  const uint32_t stride = gridDim.x * bs;
-  int32_t lcur = -1;
-  bool verdict_ok = false;  // this warp has seen the planner's verdict (every index valid)
-  uint32_t base = blockIdx.x * bs, j = 0;
-  for (;; (++j == k.block) ? (j = 0, base += stride) : 0) {
-    const uint32_t i = base + j * kPersistWarps + warp;
-    if (i >= k.items) break;
-    const int32_t l = (int32_t)(i / k.per_layer);
-    if (l != lcur) {
-      // the CTA whose block holds the layer's first item
-      const bool owner = blockIdx.x == ((uint64_t)l * k.per_layer / bs) % gridDim.x;
-      int32_t go = lane == 0 ? wait_layer(k, l, owner, &cs) : 0;
-      go = __shfl_sync(0xffffffffu, go, 0);
-      __syncwarp();  // lane 0's acquire orders every lane's loads of the layer
-      if (!go) break;
-      lcur = l;
-    }
-    const uint32_t r = i - (uint32_t)l * k.per_layer;
-    const int32_t kv = r >= k.groups ? 1 : 0;  // K or V (always 0 with one latent plane)
-    const int64_t t = (int64_t)(r - kv * k.groups) * G + rl;
-    const int32_t p = k.kv_planes * l + kv;
-    // The first item's loads go out before the planner's verdict, like the row kernel's; a
-    // lane range-checks its own indices first so that it never reads outside a pool.
-    bool ok = rl < G && t < a.n_tokens;
-    const int64_t tt = ok ? t : 0;
-    const int32_t si = sp ? a.spec_src[tt] : (int32_t)tt;
-    const int32_t di = dp ? a.spec_dst[tt] : (int32_t)tt;
-    ok = ok && (!sp || (si >= 0 && (int64_t)si < a.src.num_slots)) &&
-         (!dp || (di >= 0 && (int64_t)di < a.dst.num_slots));
-    const char *buf_plane = a.buf + (int64_t)p * a.n_tokens * R;
-    const char *srow = row_base<kSrcHnd>(a.src, sp, a.src_planes[p], buf_plane, si, R);
-    char *drow = const_cast<char *>(row_base<kDstHnd>(a.dst, dp, a.dst_planes[p], buf_plane, di, R));
-#pragma unroll 1
-    for (int32_t x0 = 0; x0 < vpr; x0 += kUnroll * m) {
-      uint4 v[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int32_t xv = x0 + li + u * m;
-        if (ok && xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
-      }
-      if (!verdict_ok) {
-        pdl_wait();  // the planner has checked every index and written status[0]
-        if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK) {
-          if (lane == 0) atomicMin(&cs.stop, 0);
-          break;
-        }
-        verdict_ok = true;
-      }
-      if (x0 == 0 && ok && dp && k.page_epochs && !page_owned(k, di)) {
-        // the page went to another request: the row is dropped and reported
-        ok = false;
-        atomicMax(&cs.code, (int32_t)KVX_ERR_CANCELLED);
-        atomicMax(&a.status[1], layers - l);
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int32_t xv = x0 + li + u * m;
-        if (ok && xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), v[u]);
-      }
-    }
-    if (!verdict_ok) break;
-  }
-
-  // every thread's writes before this CTA's report; the last CTA's release covers all CTAs
-  pdl_wait();  // the planner's status words are written before any CTA reports
-  __threadfence_system();
-  __syncthreads();
-  if (threadIdx.x == 0) persistent_cta_exit(a, k, cs, layers);
 }
 
 // ---- persistent grid, bulk form ----------------------------------------------------------
@@ -430,32 +337,33 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
   if (threadIdx.x == 0) persistent_cta_exit(a, k, cs, layers);
 }
 
-// ---- persistent grid, mixed form ---------------------------------------------------------
-// The register form's CTA with its first kMixedTmaWarps warps moving row groups by TMA bulk
-// copies (one 2 KiB stage and one mbarrier per thread) instead of registers.  The two are
-// bound by different limits of an SM -- the register warps by the rows they keep in flight,
-// the bulk copies by a cost per operation -- so together they move more per SM than either.
-// Workers (a register warp, or one thread of a TMA warp) take the CTA's items from a shared
-// counter, so the faster kind takes more; every worker's items still increase, so it enters
-// the layers in order.  Only for row groups of at most kBulkStage bytes.
+// ---- persistent grid ---------------------------------------------------------------------
+// One 1024-thread CTA per SM (32 warps, 64 KiB of rows in flight per SM: a grid capped at
+// max_ctas CTAs is bound by what each of its SMs keeps in flight).  Workers -- a warp moving a
+// row group through registers, or with kTma one thread of the first kTmaWarps warps moving it
+// by TMA bulk copies through its own 2 KiB shared-memory stage and mbarrier -- take the CTA's
+// items from a shared counter, so the faster kind takes more while every worker's items (and
+// so its layers) increase.  The two kinds are bound by different limits of an SM (rows in
+// flight; a cost per bulk operation), so mixing them moves a little more per SM than either.
+// kTma only for row groups of at most kBulkStage bytes moved in one register pass.
 
-constexpr int kMixedTmaWarps = 3;
-constexpr int kMixedTmaThreads = kMixedTmaWarps * 32;
-constexpr size_t kMixedSmem = (size_t)kMixedTmaThreads * kBulkStage + 8 * kMixedTmaThreads;
+constexpr int kTmaWarps = 3;
+constexpr int kTmaThreads = kTmaWarps * 32;
+constexpr size_t kTmaSmem = (size_t)kTmaThreads * kBulkStage + 8 * kTmaThreads;
 
-template <bool kSrcHnd, bool kDstHnd>
+template <bool kSrcHnd, bool kDstHnd, bool kTma>
 __global__ void __launch_bounds__(kPersistThreads, 1)
-    stream_mixed_kernel(const __grid_constant__ StreamArgs s) {
-  extern __shared__ __align__(128) unsigned char smem[];  // stages | mbarriers
+    stream_kernel(const __grid_constant__ StreamArgs s) {
+  extern __shared__ __align__(128) unsigned char smem[];  // kTma: stages | mbarriers
   __shared__ CtaState cs;
   __shared__ uint32_t next;  // the CTA's next item (in its own order)
   const CopyArgs &a = s.c;
   const StreamCtl &k = s.k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool tma = warp < kMixedTmaWarps;
+  const bool tma = kTma && warp < kTmaWarps;
   const int32_t layers = k.layers;
   unsigned char *stage = smem + threadIdx.x * kBulkStage;  // TMA threads only
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + (size_t)kMixedTmaThreads * kBulkStage) + threadIdx.x;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + (size_t)kTmaThreads * kBulkStage) + threadIdx.x;
   if (threadIdx.x < kReadyWords) {
     cs.ready[threadIdx.x] = 0;
     cs.polling[threadIdx.x] = 0;
@@ -465,7 +373,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
     cs.code = 0;
     next = 0;
   }
-  if (tma) mbar_init(bar);
+  if (tma) mbar_init(bar);  // (never with !kTma)
   __syncthreads();
 
   const int32_t m = a.row_lanes, G = a.rows_per_warp;  // lanes per token, tokens per group
@@ -480,75 +388,77 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
   bool verdict_ok = false;  // this worker has seen the planner's verdict (every index valid)
 
   if (tma) {
-    bool stuck = false;  // a bulk load did not complete in time (never expected)
-    uint32_t parity = 0;
-    for (;;) {
-      const uint32_t i = item_of(atomicAdd(&next, 1u));
-      if (i >= k.items) break;
-      const int32_t l = (int32_t)(i / k.per_layer);
-      if (l != lcur) {
-        const bool owner = blockIdx.x == ((uint64_t)l * k.per_layer / bs) % gridDim.x;
-        if (!wait_layer(k, l, owner, &cs)) break;
-        fence_proxy_async_global();  // the layer's rows, seen by the acquire, reach the loads
-        lcur = l;
-      }
-      const uint32_t r = i - (uint32_t)l * k.per_layer;
-      const int32_t kv = r >= k.groups ? 1 : 0;
-      const int32_t p = k.kv_planes * l + kv;
-      const int64_t t0 = (int64_t)(r - kv * k.groups) * G;
-      const int32_t gn = (int32_t)min((int64_t)G, a.n_tokens - t0);  // tokens in this group
-      const char *buf_plane = a.buf + (int64_t)p * a.n_tokens * R;
-      bool bad = false;
-      for (int32_t g = 0; g < gn; ++g) {
-        const int32_t si = sp ? a.spec_src[t0 + g] : (int32_t)(t0 + g);
-        const int32_t di = dp ? a.spec_dst[t0 + g] : (int32_t)(t0 + g);
-        bad |= (sp && (si < 0 || (int64_t)si >= a.src.num_slots)) ||
-               (dp && (di < 0 || (int64_t)di >= a.dst.num_slots));
-      }
-      if (bad) {  // the planner refuses the request: nothing may be stored
-        pdl_wait();
-        atomicMin(&cs.stop, 0);
-        break;
-      }
-      bulk_wait_read_all();  // the previous stores have finished reading the stage
-      mbar_expect_tx(bar, (uint32_t)(gn * R));
-      for (int32_t g = 0; g < gn; ++g) {
-        const int32_t si = sp ? a.spec_src[t0 + g] : (int32_t)(t0 + g);
-        const char *srow = row_base<kSrcHnd>(a.src, sp, a.src_planes[p], buf_plane, si, R);
-        bulk_row_range<kSrcHnd, true>(a.src, sp, srow, 0, R, stage + g * R, bar);
-      }
-      bool stop = false;
-      if (!verdict_ok) {  // the first group's loads go out before the planner's verdict
-        pdl_wait();
-        if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK) {
+    if constexpr (kTma) {  // (tma is false without kTma)
+      bool stuck = false;  // a bulk load did not complete in time (never expected)
+      uint32_t parity = 0;
+      for (;;) {
+        const uint32_t i = item_of(atomicAdd(&next, 1u));
+        if (i >= k.items) break;
+        const int32_t l = (int32_t)(i / k.per_layer);
+        if (l != lcur) {
+          const bool owner = blockIdx.x == ((uint64_t)l * k.per_layer / bs) % gridDim.x;
+          if (!wait_layer(k, l, owner, &cs)) break;
+          fence_proxy_async_global();  // the layer's rows, seen by the acquire, reach the loads
+          lcur = l;
+        }
+        const uint32_t r = i - (uint32_t)l * k.per_layer;
+        const int32_t kv = r >= k.groups ? 1 : 0;
+        const int32_t p = k.kv_planes * l + kv;
+        const int64_t t0 = (int64_t)(r - kv * k.groups) * G;
+        const int32_t gn = (int32_t)min((int64_t)G, a.n_tokens - t0);  // tokens in this group
+        const char *buf_plane = a.buf + (int64_t)p * a.n_tokens * R;
+        bool bad = false;
+        for (int32_t g = 0; g < gn; ++g) {
+          const int32_t si = sp ? a.spec_src[t0 + g] : (int32_t)(t0 + g);
+          const int32_t di = dp ? a.spec_dst[t0 + g] : (int32_t)(t0 + g);
+          bad |= (sp && (si < 0 || (int64_t)si >= a.src.num_slots)) ||
+                 (dp && (di < 0 || (int64_t)di >= a.dst.num_slots));
+        }
+        if (bad) {  // the planner refuses the request: nothing may be stored
+          pdl_wait();
           atomicMin(&cs.stop, 0);
-          stop = true;
+          break;
         }
-        verdict_ok = !stop;
-      }
-      if (!mbar_wait_bounded(bar, parity)) {
-        stuck = true;
-        give_up(&cs, l, KVX_ERR_TIMEOUT);
-        break;
-      }
-      parity ^= 1u;
-      if (stop) break;
-      for (int32_t g = 0; g < gn; ++g) {
-        const int32_t di = dp ? a.spec_dst[t0 + g] : (int32_t)(t0 + g);
-        if (dp && k.page_epochs && !page_owned(k, di)) {
-          // the page went to another request: the row is dropped and reported
-          atomicMax(&cs.code, (int32_t)KVX_ERR_CANCELLED);
-          atomicMax(&a.status[1], layers - l);
-          continue;
+        bulk_wait_read_all();  // the previous stores have finished reading the stage
+        mbar_expect_tx(bar, (uint32_t)(gn * R));
+        for (int32_t g = 0; g < gn; ++g) {
+          const int32_t si = sp ? a.spec_src[t0 + g] : (int32_t)(t0 + g);
+          const char *srow = row_base<kSrcHnd>(a.src, sp, a.src_planes[p], buf_plane, si, R);
+          bulk_row_range<kSrcHnd, true>(a.src, sp, srow, 0, R, stage + g * R, bar);
         }
-        char *drow = const_cast<char *>(row_base<kDstHnd>(a.dst, dp, a.dst_planes[p], buf_plane, di, R));
-        bulk_row_range<kDstHnd, false>(a.dst, dp, drow, 0, R, stage + g * R, bar);
+        bool stop = false;
+        if (!verdict_ok) {  // the first group's loads go out before the planner's verdict
+          pdl_wait();
+          if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK) {
+            atomicMin(&cs.stop, 0);
+            stop = true;
+          }
+          verdict_ok = !stop;
+        }
+        if (!mbar_wait_bounded(bar, parity)) {
+          stuck = true;
+          give_up(&cs, l, KVX_ERR_TIMEOUT);
+          break;
+        }
+        parity ^= 1u;
+        if (stop) break;
+        for (int32_t g = 0; g < gn; ++g) {
+          const int32_t di = dp ? a.spec_dst[t0 + g] : (int32_t)(t0 + g);
+          if (dp && k.page_epochs && !page_owned(k, di)) {
+            // the page went to another request: the row is dropped and reported
+            atomicMax(&cs.code, (int32_t)KVX_ERR_CANCELLED);
+            atomicMax(&a.status[1], layers - l);
+            continue;
+          }
+          char *drow = const_cast<char *>(row_base<kDstHnd>(a.dst, dp, a.dst_planes[p], buf_plane, di, R));
+          bulk_row_range<kDstHnd, false>(a.dst, dp, drow, 0, R, stage + g * R, bar);
+        }
+        bulk_commit();
       }
-      bulk_commit();
+      if (stuck) (void)mbar_wait_bounded(bar, parity);  // let the late load land before leaving
+      bulk_wait_all();             // every store of this thread is complete
+      fence_proxy_async_global();  // ... and ordered before the generic-proxy release below
     }
-    if (stuck) (void)mbar_wait_bounded(bar, parity);  // let the late load land before leaving
-    bulk_wait_all();             // every store of this thread is complete
-    fence_proxy_async_global();  // ... and ordered before the generic-proxy release below
   } else {
     const int32_t rl = lane / m, li = lane - rl * m;
     for (;;) {
@@ -578,30 +488,37 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
       const char *buf_plane = a.buf + (int64_t)p * a.n_tokens * R;
       const char *srow = row_base<kSrcHnd>(a.src, sp, a.src_planes[p], buf_plane, si, R);
       char *drow = const_cast<char *>(row_base<kDstHnd>(a.dst, dp, a.dst_planes[p], buf_plane, di, R));
-      uint4 v[kUnroll];
+      // The first item's loads go out before the planner's verdict, like the row kernel's; a
+      // lane range-checked its own indices above, so it never reads outside a pool.
+#pragma unroll 1
+      for (int32_t x0 = 0; x0 < vpr; x0 += kUnroll * m) {
+        uint4 v[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {  // one pass: a group is at most kBulkStage bytes
-        const int32_t xv = li + u * m;
-        if (ok && xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
-      }
-      if (!verdict_ok) {
-        pdl_wait();  // the planner has checked every index and written status[0]
-        if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK) {
-          if (lane == 0) atomicMin(&cs.stop, 0);
-          break;
+        for (int u = 0; u < kUnroll; ++u) {
+          const int32_t xv = x0 + li + u * m;
+          if (ok && xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
         }
-        verdict_ok = true;
-      }
-      if (ok && dp && k.page_epochs && !page_owned(k, di)) {
-        ok = false;
-        atomicMax(&cs.code, (int32_t)KVX_ERR_CANCELLED);
-        atomicMax(&a.status[1], layers - l);
-      }
+        if (!verdict_ok) {
+          pdl_wait();  // the planner has checked every index and written status[0]
+          if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK) {
+            if (lane == 0) atomicMin(&cs.stop, 0);
+            break;
+          }
+          verdict_ok = true;
+        }
+        if (x0 == 0 && ok && dp && k.page_epochs && !page_owned(k, di)) {
+          // the page went to another request: the row is dropped and reported
+          ok = false;
+          atomicMax(&cs.code, (int32_t)KVX_ERR_CANCELLED);
+          atomicMax(&a.status[1], layers - l);
+        }
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int32_t xv = li + u * m;
-        if (ok && xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), v[u]);
+        for (int u = 0; u < kUnroll; ++u) {
+          const int32_t xv = x0 + li + u * m;
+          if (ok && xv < vpr) st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, dp, drow, xv << 4)), v[u]);
+        }
       }
+      if (!verdict_ok) break;
     }
   }
 
@@ -721,11 +638,16 @@ const void *stream_row_fn_of(bool sh, bool dh) {
 }
 
 
-const void *stream_fn(bool sh, bool dh) {
-  if (sh && dh) return reinterpret_cast<const void *>(stream_kernel<true, true>);
-  if (sh) return reinterpret_cast<const void *>(stream_kernel<true, false>);
-  if (dh) return reinterpret_cast<const void *>(stream_kernel<false, true>);
-  return reinterpret_cast<const void *>(stream_kernel<false, false>);
+template <bool kTma>
+const void *stream_fn_of(bool sh, bool dh) {
+  if (sh && dh) return reinterpret_cast<const void *>(stream_kernel<true, true, kTma>);
+  if (sh) return reinterpret_cast<const void *>(stream_kernel<true, false, kTma>);
+  if (dh) return reinterpret_cast<const void *>(stream_kernel<false, true, kTma>);
+  return reinterpret_cast<const void *>(stream_kernel<false, false, kTma>);
+}
+
+const void *stream_fn(bool sh, bool dh, bool tma) {
+  return tma ? stream_fn_of<true>(sh, dh) : stream_fn_of<false>(sh, dh);
 }
 
 const void *stream_bulk_fn(bool sh, bool dh) {
@@ -735,39 +657,11 @@ const void *stream_bulk_fn(bool sh, bool dh) {
   return reinterpret_cast<const void *>(stream_bulk_kernel<false, false>);
 }
 
-const void *stream_mixed_fn(bool sh, bool dh) {
-  if (sh && dh) return reinterpret_cast<const void *>(stream_mixed_kernel<true, true>);
-  if (sh) return reinterpret_cast<const void *>(stream_mixed_kernel<true, false>);
-  if (dh) return reinterpret_cast<const void *>(stream_mixed_kernel<false, true>);
-  return reinterpret_cast<const void *>(stream_mixed_kernel<false, false>);
-}
-
 }  // namespace
 
-int stream_mixed_blocks_per_sm() {
-  for (int v = 0; v < 4; ++v)
-    if (cudaFuncSetAttribute(stream_mixed_fn(v & 1, v & 2),
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMixedSmem) != cudaSuccess)
-      return 0;
-  int nb = 0;
-  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &nb, stream_mixed_fn(false, false), kPersistThreads, kMixedSmem);
-  return e == cudaSuccess ? nb : 0;
-}
-
-bool stream_mixed_fits(const CopyArgs &c) {
+bool stream_tma_fits(const CopyArgs &c) {
   return (int64_t)c.rows_per_warp * c.row_bytes <= kBulkStage &&
          (c.row_bytes >> 4) <= kUnroll * c.row_lanes;  // one register pass per row
-}
-
-cudaError_t launch_stream_mixed(const CopyArgs &c, const StreamCtl &k, int grid, cudaStream_t s) {
-  static thread_local StreamArgs args;  // ~4 KiB of plane pointers: keep it off the stack
-  args.c = c;
-  args.k = k;
-  const bool sh = c.src.hnd && c.src.is_pool, dh = c.dst.hnd && c.dst.is_pool;
-  void *params[] = {&args};
-  return launch_pdl(stream_mixed_fn(sh, dh), dim3((unsigned)grid), dim3(kPersistThreads), params,
-                    s, kMixedSmem);
 }
 
 int stream_bulk_blocks_per_sm() {
@@ -795,10 +689,17 @@ cudaError_t launch_stream_bulk(const CopyArgs &c, const StreamCtl &k, int grid, 
 }
 
 int stream_blocks_per_sm() {
-  int nb = 0;
-  const cudaError_t e =
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, stream_kernel<false, false>, kPersistThreads, 0);
-  return e == cudaSuccess ? nb : 0;
+  for (int v = 0; v < 4; ++v)
+    if (cudaFuncSetAttribute(stream_fn(v & 1, v & 2, true),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmaSmem) != cudaSuccess)
+      return 0;
+  int nb = 0, nb_tma = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, stream_fn(false, false, false),
+                                                    kPersistThreads, 0) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb_tma, stream_fn(false, false, true),
+                                                    kPersistThreads, kTmaSmem) != cudaSuccess)
+    return 0;
+  return std::min(nb, nb_tma);
 }
 
 void stream_sizes(StreamCtl &k, int64_t n_tokens, int32_t rows_per_warp) {
@@ -809,13 +710,15 @@ void stream_sizes(StreamCtl &k, int64_t n_tokens, int32_t rows_per_warp) {
   k.per_layer_pad = (k.per_layer + kWarps - 1) / kWarps * kWarps;
 }
 
-cudaError_t launch_stream(const CopyArgs &c, const StreamCtl &k, int grid, cudaStream_t s) {
+cudaError_t launch_stream(const CopyArgs &c, const StreamCtl &k, int grid, bool tma,
+                          cudaStream_t s) {
   static thread_local StreamArgs args;  // ~4 KiB of plane pointers: keep it off the stack
   args.c = c;
   args.k = k;
   const bool sh = c.src.hnd && c.src.is_pool, dh = c.dst.hnd && c.dst.is_pool;
   void *params[] = {&args};
-  return launch_pdl(stream_fn(sh, dh), dim3((unsigned)grid), dim3(kPersistThreads), params, s);
+  return launch_pdl(stream_fn(sh, dh, tma), dim3((unsigned)grid), dim3(kPersistThreads), params,
+                    s, tma ? kTmaSmem : 0);
 }
 
 cudaError_t launch_stream_rows(const CopyArgs &c, const StreamCtl &k, cudaStream_t s) {
