@@ -24,14 +24,16 @@
 // kernel, launched behind the grid, folds the stop codes into the status and sets the
 // "no further write" words once every CTA has finished.
 //
-// Persistent grid (kvx_stream_ctl::max_ctas > 0): at most max_ctas CTAs, so that a producer
-// running on the same GPU keeps the rest of it.  Blocks of kWarps * block consecutive items
-// go to the CTAs in turn, so every warp reaches the layers in increasing order.  A warp
-// entering layer l checks, once per CTA and layer (the first warp to arrive polls, the others
-// read the CTA's shared bit of layer l), the epoch word and the ready word of layer l.  A CTA
-// that stops still finishes the layers its warps had already entered, so every layer below
-// the smallest stop layer of all CTAs holds every row.  On exit each CTA publishes its stop
-// layer and code, and the last CTA to finish sets the "no further write" words.
+// Persistent grid (kvx_stream_ctl::max_ctas > 0): at most max_ctas CTAs, one per SM, so that
+// a producer running on the same GPU keeps the rest of it.  Blocks of consecutive items go to
+// the CTAs in turn, and a CTA's workers (register warps; by default also TMA bulk-copy
+// threads) take its items in order from a shared counter, so every worker reaches the layers
+// in increasing order.  A worker entering layer l checks, once per CTA and layer (the first
+// to arrive polls, the others read the CTA's shared bit of layer l), the epoch word and the
+// ready word of layer l.  A CTA that stops still finishes the layers its workers had already
+// entered, so every layer below the smallest stop layer of all CTAs holds every row.  On exit
+// each CTA publishes its stop layer and flags its stop code, and the last CTA to finish folds
+// the codes into the verdict and sets the "no further write" words.
 //
 // In both, polling is shared out so that the words of a slow producer (often pinned host
 // memory, read over the CPU-GPU link) see few readers: pollers read the device-memory mirror
