@@ -1093,6 +1093,20 @@ def run_tp(args):
                 step_streamed()
         ms_streamed = timed(step_streamed)
         assert st4.tolist() == [kvx.OK, 0, 0, 1], st4.tolist()
+        # ... and on a persistent grid capped at half the SMs (the rest left to a producer)
+        half = torch.cuda.get_device_properties(dev).multi_processor_count // 2
+
+        def step_capped():
+            kvx.stream_reshard(p_l, s_dev, d_l, d_dev, plan, N_TOK, ws, st4, layer_ready=words,
+                               ready_value=1, max_ctas=half, stream=sp)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                flush.fill_(1)
+                step_capped()
+        ms_capped = timed(step_capped)
+        v4 = st4.tolist()
+        assert v4[0:2] == [kvx.OK, 0] and v4[3] == 1, v4
         alg = alg_bytes(N_TOK) + 8 * N_TOK * (len(plan) - 1)  # every pair reads both lists
         gbs = alg / (ms * 1e-3) / 1e9
         gbs_one = alg_bytes(N_TOK) / (ms_one * 1e-3) / 1e9
@@ -1104,6 +1118,7 @@ def run_tp(args):
             "us_per_reshard_one_call": ms_one * 1e3, "GBs_one_call": gbs_one,
             "frac_of_measured_hbm_one_call": gbs_one / float(peaks["hbm_gbs"]),
             "us_per_reshard_streamed_all_ready": ms_streamed * 1e3,
+            "us_per_reshard_streamed_half_the_sms": ms_capped * 1e3,
             "slice_bytes": plan[0][4] * D * 2}
         del p_pools, d_pools, p_l, d_l
         torch.cuda.empty_cache()

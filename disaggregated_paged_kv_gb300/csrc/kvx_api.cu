@@ -131,6 +131,7 @@ struct DeviceInfo {
   int bps_fused_general = 0;              // one-launch path, general placement
   int bps_stream = 0;                     // layer-streamed copy
   int bps_stream_bulk = 0;                // layer-streamed copy, bulk (TMA) form
+  int bps_reshard_persist = 0;            // layer-streamed reshard, capped persistent grid
 };
 
 std::atomic<int32_t> g_fused_max{0};  // measured: planner + row kernel is faster
@@ -162,8 +163,9 @@ kvx_status device_info(DeviceInfo *out) {
     d.bps_fused_general = kvx::fused_blocks_per_sm(false);
     d.bps_stream = kvx::stream_blocks_per_sm();
     d.bps_stream_bulk = kvx::stream_bulk_blocks_per_sm();
+    d.bps_reshard_persist = kvx::reshard_persist_blocks_per_sm();
     if (d.bps_fused_linear <= 0 || d.bps_fused_general <= 0 || d.bps_stream <= 0 ||
-        d.bps_stream_bulk <= 0) {
+        d.bps_stream_bulk <= 0 || d.bps_reshard_persist <= 0) {
       e = cudaGetLastError();
       return cuda_fail(e != cudaSuccess ? e : cudaErrorUnknown);
     }
@@ -1279,7 +1281,6 @@ kvx_status kvx_stream_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
                               const kvx_stream_ctl *ctl, void *d_ws, size_t ws_bytes,
                               int32_t *d_status, kvx_stream_t stream) {
   if (!d_status || !aligned(d_status, 16)) return KVX_ERR_INVALID_ARG;
-  if (ctl && ctl->max_ctas != 0) return KVX_ERR_INVALID_ARG;  // the row grid only
   Call c;
   static thread_local kvx::ReshardCall rc;  // ~30 KB: keep it off the stack
   kvx_status st = prepare_reshard(srcs, n_srcs, d_src_slots, dsts, n_dsts, d_dst_slots, parts,
@@ -1311,7 +1312,14 @@ kvx_status kvx_stream_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
     if (e != cudaSuccess) return cuda_fail(e);
   }
   rc.status = d_status;
-  e = kvx::launch_reshard_stream(rc, k, s);
+  if (ctl && ctl->max_ctas > 0) {  // capped persistent grid, one CTA per SM at most
+    DeviceInfo di;
+    if ((st = device_info(&di)) != KVX_OK) return st;
+    const int64_t cap = (int64_t)di.sms * di.bps_reshard_persist;
+    e = kvx::launch_reshard_stream_capped(rc, k, (int)std::min<int64_t>(ctl->max_ctas, cap), s);
+  } else {
+    e = kvx::launch_reshard_stream(rc, k, s);
+  }
   return e == cudaSuccess ? KVX_OK : cuda_fail(e);
 }
 

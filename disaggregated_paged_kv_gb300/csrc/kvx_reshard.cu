@@ -16,6 +16,8 @@
 // Grid rows (blockIdx.y) of 4096 token groups keep w small.
 // As in the row kernel of kvx_copy.cu, each lane range-checks its token and issues its loads
 // before the planner's verdict, and stores only after it (all-or-nothing).
+#include <algorithm>
+
 #include "kvx_copy_ops.cuh"
 #include "kvx_launch.cuh"
 #include "kvx_reshard.cuh"
@@ -221,6 +223,123 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
   }
 }
 
+// ---- layer-streamed reshard on a capped persistent grid -----------------------------------
+// kvx_stream's capped persistent grid over the streamed reshard's items (layer-major, parts
+// fastest within a layer, unpadded): at most max_ctas CTAs of 1024 threads, one per SM, whose
+// warps take the CTA's items from a shared counter, one poller per CTA and layer
+// (sops::wait_layer), and the last CTA to finish folds the stop codes into the verdict and
+// sets the "no further write" words (sops::persistent_cta_exit); no epilogue kernel.
+
+constexpr int kRsPersistThreads = 1024;
+constexpr int kRsPersistWarps = kRsPersistThreads / 32;
+
+template <bool kSrcHnd, bool kDstHnd, int kPtrs>
+__global__ void __launch_bounds__(kRsPersistThreads, 1)
+    reshard_persist_kernel(const __grid_constant__ ReshardStreamArgs<kPtrs> s) {
+  __shared__ sops::CtaState cs;
+  __shared__ uint32_t next;  // the CTA's next item (in its own order)
+  const ReshardArgs<kPtrs> &a = s.r;
+  const StreamCtl &k = s.k;
+  const int lane = threadIdx.x & 31;
+  const int32_t layers = k.layers;
+  if (threadIdx.x < sops::kReadyWords) {
+    cs.ready[threadIdx.x] = 0;
+    cs.polling[threadIdx.x] = 0;
+  }
+  if (threadIdx.x == 0) {
+    cs.stop = layers;
+    cs.code = 0;
+    next = 0;
+  }
+  __syncthreads();
+
+  const uint32_t J = (uint32_t)a.n_parts;
+  const int32_t m = a.lanes, G = a.rows;
+  const int32_t rl = lane / m, li = lane - rl * m;
+  const int32_t nt = (int32_t)a.n_tokens, R = a.row_bytes, vpr = R >> 4;
+  // Item q of this CTA: blocks of bs consecutive items go to the CTAs in turn.
+  const uint32_t bs = kRsPersistWarps * k.block;
+  auto item_of = [&](uint32_t q) -> uint32_t {
+    return ((q / bs) * gridDim.x + blockIdx.x) * bs + q % bs;
+  };
+  int32_t lcur = -1;
+  bool verdict_ok = false;  // this warp has seen the planner's verdict (both lists valid)
+  for (;;) {
+    uint32_t q = 0;
+    if (lane == 0) q = atomicAdd(&next, 1u);
+    const uint32_t i = item_of(__shfl_sync(0xffffffffu, q, 0));
+    if (i >= k.items) break;
+    const int32_t l = (int32_t)(i / k.per_layer);
+    if (l != lcur) {
+      const bool owner = blockIdx.x == ((uint64_t)l * k.per_layer / bs) % gridDim.x;
+      int32_t go = lane == 0 ? sops::wait_layer(k, l, owner, &cs) : 0;
+      go = __shfl_sync(0xffffffffu, go, 0);
+      __syncwarp();  // lane 0's acquire orders every lane's loads of the layer
+      if (!go) break;
+      lcur = l;
+    }
+    const uint32_t r = i - (uint32_t)l * k.per_layer;
+    const uint32_t qq = r / J;
+    const int32_t j = (int32_t)(r - qq * J);
+    const int32_t kv = qq >= k.groups ? 1 : 0;  // K or V (always 0 with one latent plane)
+    const int32_t t = (int32_t)(qq - (uint32_t)kv * k.groups) * G + rl;
+    bool ok = rl < G && t < nt;
+    const int32_t tt = ok ? t : 0;
+    const int32_t si = a.src_slots[tt], di = a.dst_slots[tt];
+    ok = ok && si >= 0 && (int64_t)si < a.src.num_slots && di >= 0 && (int64_t)di < a.dst.num_slots;
+    const int32_t p = k.kv_planes * l + kv;
+    const ReshardPart &pt = a.parts[j];
+    const char *srow =
+        row_base<kSrcHnd>(a.src, true, plane_addr(a, pt.src, p) + pt.src_off, nullptr, si, R);
+    char *drow = const_cast<char *>(
+        row_base<kDstHnd>(a.dst, true, plane_addr(a, pt.dst, p) + pt.dst_off, nullptr, di, R));
+#pragma unroll 1
+    for (int32_t x0 = 0; x0 < vpr; x0 += kUnroll * m) {
+      uint4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int32_t xv = x0 + li + u * m;
+        if (ok && xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, true, srow, xv << 4));
+      }
+      if (!verdict_ok) {
+        pdl_wait();  // the planner has checked both slot lists and written status[0]
+        if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK) {
+          if (lane == 0) atomicMin(&cs.stop, 0);
+          break;
+        }
+        verdict_ok = true;
+      }
+      if (x0 == 0 && ok && k.page_epochs && !sops::page_owned(k, di)) {
+        // the page went to another request: the piece is dropped and reported
+        ok = false;
+        atomicMax(&cs.code, (int32_t)KVX_ERR_CANCELLED);
+        atomicMax(&a.status[1], layers - l);
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int32_t xv = x0 + li + u * m;
+        if (ok && xv < vpr)
+          st_stream(const_cast<char *>(row_byte<kDstHnd>(a.dst, true, drow, xv << 4)), v[u]);
+      }
+    }
+    if (!verdict_ok) break;
+  }
+
+  // every thread's writes before this CTA's report; the last CTA's release covers all CTAs
+  pdl_wait();  // the planner's status words are written before any CTA reports
+  __threadfence_system();
+  __syncthreads();
+  if (threadIdx.x == 0) sops::persistent_cta_exit(a.status, k, cs, layers);
+}
+
+template <int kPtrs>
+const void *reshard_persist_fn(bool sh, bool dh) {
+  if (sh && dh) return reinterpret_cast<const void *>(reshard_persist_kernel<true, true, kPtrs>);
+  if (sh) return reinterpret_cast<const void *>(reshard_persist_kernel<true, false, kPtrs>);
+  if (dh) return reinterpret_cast<const void *>(reshard_persist_kernel<false, true, kPtrs>);
+  return reinterpret_cast<const void *>(reshard_persist_kernel<false, false, kPtrs>);
+}
+
 template <bool kTail, int kPtrs>
 const void *reshard_stream_fn(bool sh, bool dh) {
   if (sh && dh) return reinterpret_cast<const void *>(reshard_stream_kernel<true, true, kTail, kPtrs>);
@@ -242,6 +361,17 @@ RsSizes rs_sizes(const ReshardCall &c, const StreamCtl &k) {
   z.per_layer = (int64_t)k.kv_planes * z.groups * c.n_parts;
   z.per_layer_pad = (z.per_layer + kRsWarps - 1) / kRsWarps * kRsWarps;
   return z;
+}
+
+template <int kPtrs>
+cudaError_t launch_persist_with(const ReshardCall &c, const StreamCtl &k, const RsSizes &z,
+                                int grid, cudaStream_t s) {
+  static thread_local ReshardStreamArgs<kPtrs> args;  // up to ~29 KB: keep it off the stack
+  fill_args(args.r, c, z.m, z.G, 0);
+  args.k = k;
+  void *params[] = {&args};
+  return launch_pdl(reshard_persist_fn<kPtrs>(c.src.hnd != 0, c.dst.hnd != 0),
+                    dim3((unsigned)grid), dim3(kRsPersistThreads), params, s);
 }
 
 template <int kPtrs>
@@ -321,6 +451,31 @@ cudaError_t launch_reshard_stream(const ReshardCall &c, StreamCtl k, cudaStream_
                      : launch_stream_with<0>(c, k, z, s);
   if (e != cudaSuccess) return e;
   return launch_stream_done(c.status, k.host_done, k.layers, s);
+}
+
+int reshard_persist_blocks_per_sm() {
+  int nb = 0;
+  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &nb, reshard_persist_fn<kReshardMaxPtrs>(false, false), kRsPersistThreads, 0);
+  return e == cudaSuccess ? nb : 0;
+}
+
+cudaError_t launch_reshard_stream_capped(const ReshardCall &c, StreamCtl k, int max_grid,
+                                         cudaStream_t s) {
+  const RsSizes z = rs_sizes(c, k);
+  k.groups = (uint32_t)z.groups;
+  k.per_layer = (uint32_t)z.per_layer;
+  k.items = (uint32_t)(z.per_layer * k.layers);
+  if (k.items == 0)  // nothing to move: the epilogue alone writes the status words
+    return launch_stream_done(c.status, k.host_done, k.layers, s);
+  const int64_t warps = k.items;
+  int64_t grid = std::min<int64_t>(max_grid, (warps + kRsPersistWarps - 1) / kRsPersistWarps);
+  if (grid < 1) grid = 1;
+  // about four blocks per warp: few layer entries per warp, each layer spread over many warps
+  const int64_t per_warp = (warps + grid * kRsPersistWarps - 1) / (grid * kRsPersistWarps);
+  k.block = (uint32_t)std::min<int64_t>(std::max<int64_t>(per_warp / 4, 1), 8);
+  return c.n_ptrs > 0 ? launch_persist_with<kReshardMaxPtrs>(c, k, z, (int)grid, s)
+                      : launch_persist_with<0>(c, k, z, (int)grid, s);
 }
 
 cudaError_t launch_reshard(const ReshardCall &c, cudaStream_t s) {

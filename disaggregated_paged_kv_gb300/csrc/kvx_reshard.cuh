@@ -43,5 +43,10 @@ cudaError_t launch_reshard(const ReshardCall &c, cudaStream_t s);
 // control block, the mirror and its tag; the item counts are filled in here.
 bool reshard_stream_fits(const ReshardCall &c, const StreamCtl &k);
 cudaError_t launch_reshard_stream(const ReshardCall &c, StreamCtl k, cudaStream_t s);
+// The same on a capped persistent grid of at most max_grid CTAs (1024 threads, one per SM):
+// kvx_stream_ctl::max_ctas > 0.  Writes the status words itself (no epilogue kernel).
+int reshard_persist_blocks_per_sm();
+cudaError_t launch_reshard_stream_capped(const ReshardCall &c, StreamCtl k, int max_grid,
+                                         cudaStream_t s);
 
 }  // namespace kvx

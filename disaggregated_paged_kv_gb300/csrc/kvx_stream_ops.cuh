@@ -1,6 +1,7 @@
-// kvx_stream_ops.cuh -- the per-layer wait of the layer-streamed row grids (sm_103a): memory
-// ordering helpers, the owner-epoch check of a destination page, the tagged stop word and the
-// bounded wait of a CTA's thread 0 for its layer.  Shared by kvx_stream.cu and kvx_reshard.cu.
+// kvx_stream_ops.cuh -- the per-layer waits of the layer-streamed grids (sm_103a): memory
+// ordering helpers, the owner-epoch check of a destination page, the tagged stop word, the
+// bounded wait of a row-grid CTA's thread 0 for its layer, and the per-CTA layer state, wait
+// and exit protocol of the persistent grids.  Shared by kvx_stream.cu and kvx_reshard.cu.
 #pragma once
 
 #include "kvx_copy_ops.cuh"
@@ -110,6 +111,126 @@ __device__ inline int32_t row_wait(const StreamCtl &k, int32_t l, bool owner) {
     }
     __nanosleep(sleep_ns);
     if (sleep_ns < kMaxSleepNs) sleep_ns <<= 1;
+  }
+}
+
+// ---- persistent grids: per-CTA layer state, the shared wait, the exit protocol ------------
+// Used by the capped persistent grids of kvx_stream (kvx_stream.cu) and kvx_stream_reshard
+// (kvx_reshard.cu): a CTA's workers enter the layers in increasing order, one of them polls
+// per CTA and layer, the others read the CTA's shared bits.
+
+__device__ __forceinline__ int32_t ld_acquire_cta(const int32_t *smem) {
+  int32_t v;
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void or_release_cta(uint32_t *smem, uint32_t v) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("red.release.cta.shared::cta.or.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+constexpr int kReadyWords = KVX_MAX_PLANES / 2 / 32;
+static_assert(kReadyWords * 32 * 2 == KVX_MAX_PLANES, "one ready bit per layer");
+
+struct CtaState {
+  uint32_t ready[kReadyWords];    // bit l: layer l is known ready in this CTA
+  uint32_t polling[kReadyWords];  // bit l: one warp of this CTA polls for layer l
+  int32_t stop;                   // first layer this CTA does not start (num_layers: none)
+  int32_t code;                   // KVX_ERR_TIMEOUT / KVX_ERR_CANCELLED, or 0
+};
+
+__device__ __forceinline__ bool known_ready(CtaState *cs, int32_t l) {
+  return (ld_acquire_cta(reinterpret_cast<const int32_t *>(&cs->ready[l >> 5])) >> (l & 31)) & 1;
+}
+
+__device__ __forceinline__ int32_t stopped_before(CtaState *cs, int32_t l) {
+  return *reinterpret_cast<volatile int32_t *>(&cs->stop) <= l;
+}
+
+__device__ __forceinline__ int32_t give_up(CtaState *cs, int32_t l, int32_t code) {
+  atomicMin(&cs->stop, l);
+  atomicMax(&cs->code, code);
+  return 0;
+}
+
+// Lane 0 of a warp entering layer l: 1 to go on, 0 to stop.  Polling is shared out so that
+// the words of a slow producer (often pinned host memory, read over the CPU-GPU link) see
+// few readers: in each CTA one warp polls and the others watch the CTA's shared bit; the
+// polling warp reads the device-memory mirror on every round and the producer's words only
+// on its first round and every 16th, except in the CTA that owns the layer's first item,
+// which reads them on every round and copies what it sees into the mirror.
+__device__ inline int32_t wait_layer(const StreamCtl &k, int32_t l, bool owner, CtaState *cs) {
+  if (stopped_before(cs, l)) return 0;
+  if (known_ready(cs, l)) return 1;
+  const uint32_t bit = 1u << (l & 31);
+  if (!k.layer_ready && !k.epoch_word) {  // nothing to wait for
+    or_release_cta(&cs->ready[l >> 5], bit);
+    return 1;
+  }
+  if (k.words_local) {  // one round trip: the epoch and the ready word together
+    const int32_t e = k.epoch_word ? ld_relaxed_sys(k.epoch_word) : k.epoch;
+    const bool ready = !k.layer_ready || ld_acquire_sys(k.layer_ready + l) >= k.ready_value;
+    if (e == k.epoch && ready) {
+      or_release_cta(&cs->ready[l >> 5], bit);
+      return 1;
+    }
+  }
+  const bool poller = !(atomicOr(&cs->polling[l >> 5], bit) & bit);
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t sleep_ns = 32;
+  for (uint32_t it = 0;; ++it) {
+    if (poller) {
+      if (ld_acquire_gpu(k.mirror) == k.gen) return give_up(cs, l, KVX_ERR_CANCELLED);
+      if (ld_acquire_gpu(k.mirror + 1 + l) == k.gen) {
+        or_release_cta(&cs->ready[l >> 5], bit);
+        return 1;
+      }
+      if (owner || it == 0 || (it & 15) == 15) {
+        if (k.epoch_word && ld_acquire_sys(k.epoch_word) != k.epoch) {
+          st_release_gpu(k.mirror, k.gen);
+          return give_up(cs, l, KVX_ERR_CANCELLED);
+        }
+        if (!k.layer_ready || ld_acquire_sys(k.layer_ready + l) >= k.ready_value) {
+          st_release_gpu(k.mirror + 1 + l, k.gen);
+          or_release_cta(&cs->ready[l >> 5], bit);
+          return 1;
+        }
+      }
+    }
+    if (globaltimer_ns() - t0 >= (uint64_t)k.wait_ns || it >= kMaxPolls)
+      return give_up(cs, l, KVX_ERR_TIMEOUT);
+    __nanosleep(sleep_ns);
+    if (sleep_ns < kMaxSleepNs) sleep_ns <<= 1;
+    if (stopped_before(cs, l)) return 0;
+    if (known_ready(cs, l)) return 1;
+  }
+}
+
+// Exit of a persistent grid's CTA (thread 0, once every thread of the CTA has made its last
+// write).  Warps of CTAs that started late may still be about to read the planner's verdict in
+// status[0], so no CTA writes its stop code there: the code goes into status[2] as a flag above
+// the count of finished CTAs, and the last CTA to finish folds the flags into status[0]
+// (CANCELLED over TIMEOUT) and sets the "no further write" words.
+constexpr int32_t kFinishedMask = (1 << 24) - 1;
+constexpr int32_t kTimeoutFlag = 1 << 24;
+constexpr int32_t kCancelledFlag = 1 << 25;
+
+__device__ inline void persistent_cta_exit(int32_t *status, const StreamCtl &k, const CtaState &cs,
+                                           int32_t layers) {
+  if (cs.code) atomicOr(&status[2], cs.code == KVX_ERR_CANCELLED ? kCancelledFlag : kTimeoutFlag);
+  if (cs.stop < layers) atomicMax(&status[1], layers - cs.stop);
+  __threadfence_system();
+  const int32_t before = atomicAdd(&status[2], 1);
+  if ((before & kFinishedMask) == (int32_t)gridDim.x - 1) {
+    __threadfence_system();
+    const int32_t flags = atomicOr(&status[2], 0);  // every CTA set its flag before counting
+    if (flags & kCancelledFlag) atomicMax(&status[0], (int32_t)KVX_ERR_CANCELLED);
+    else if (flags & kTimeoutFlag) atomicMax(&status[0], (int32_t)KVX_ERR_TIMEOUT);
+    __threadfence_system();
+    st_release_sys(&status[3], 1);
+    if (k.host_done) st_release_sys(k.host_done, 1);
   }
 }
 

@@ -494,12 +494,12 @@ def _stream_ctl(layer_ready, ready_value, epoch_word, epoch, wait_ns, max_ctas, 
 def stream_reshard(srcs: Sequence[Optional[Layout]], src_slots, dsts: Sequence[Optional[Layout]],
                    dst_slots, parts, n: int, ws, status, layer_ready=None, ready_value: int = 1,
                    epoch_word=None, epoch: int = 0, wait_ns: int = 100_000_000, host_done=None,
-                   dst_page_epochs=None, epoch_page: int = 1, ws_bytes=None,
+                   dst_page_epochs=None, epoch_page: int = 1, max_ctas: int = 0, ws_bytes=None,
                    stream=None) -> None:
     """kvx_stream_reshard: kvx_reshard moving layer l once ``layer_ready[l] >= ready_value``,
     stopping on a changed epoch word or a wait past ``wait_ns``; ``status`` is a device
-    int32[4] as for stream()."""
-    ctl = _stream_ctl(layer_ready, ready_value, epoch_word, epoch, wait_ns, 0, host_done,
+    int32[4] as for stream(); ``max_ctas`` > 0 caps the grid as for stream()."""
+    ctl = _stream_ctl(layer_ready, ready_value, epoch_word, epoch, wait_ns, max_ctas, host_done,
                       dst_page_epochs, epoch_page)
     sa = (_VP * max(1, len(srcs)))(*[_h(x) for x in srcs])
     da = (_VP * max(1, len(dsts)))(*[_h(x) for x in dsts])

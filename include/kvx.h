@@ -479,8 +479,10 @@ KVX_API kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src
  * no longer holds ctl->epoch or a wait runs past ctl->wait_ns, and with ctl->dst_page_epochs
  * a row is written only while its destination page (slot / epoch_page, the same slot list for
  * every destination) still holds ctl->epoch.  Arguments and host-side errors as kvx_reshard
- * and kvx_stream; ctl->max_ctas must be 0 (one CTA per padded group of items, as kvx_stream's
- * default grid), and a reshard whose padded items exceed 2^31 - 1 is KVX_ERR_INVALID_ARG.
+ * and kvx_stream.  ctl->max_ctas == 0: one CTA per padded group of items, as kvx_stream's
+ * default grid; > 0: a persistent grid of at most max_ctas CTAs of 1024 threads, one per SM,
+ * leaving the rest of the GPU to a producer (as kvx_stream's, with registers only).  A reshard
+ * whose padded items exceed 2^31 - 1 is KVX_ERR_INVALID_ARG.
  * d_status: device int32[4], 16-byte aligned, with kvx_stream's meaning (verdict, layers
  * pending, internal, "no further write").  May be captured into a CUDA graph, as kvx_stream. */
 KVX_API kvx_status kvx_stream_reshard(const kvx_layout_t *srcs, int32_t n_srcs,

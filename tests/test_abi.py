@@ -284,7 +284,7 @@ def test_reshard_validation_before_cuda(lib):
 
 
 def test_stream_reshard_validation_before_cuda(lib):
-    """kvx_stream_reshard refuses a persistent grid, a missing or malformed control block, a
+    """kvx_stream_reshard refuses a negative CTA cap, a missing or malformed control block, a
     status array that is not 16-byte aligned, and every malformed reshard kvx_reshard refuses."""
     mk = lambda k, h: kvx.Layout(2, h, 64, kvx.F16, 1000, base=FAKE * k, plane_stride=1000 * h * 128)
     p = [mk(1, 2), mk(2, 2)]
@@ -303,7 +303,7 @@ def test_stream_reshard_validation_before_cuda(lib):
     good = [(0, 0, 0, 0, 2), (1, 0, 0, 2, 2)]
     ok = kvx._stream_ctl(None, 1, None, 0, 1000, 0, None, None, 1)
     assert rs(good, None) == kvx.ERR_INVALID_ARG
-    assert rs(good, kvx._stream_ctl(None, 1, None, 0, 1000, 40, None, None, 1)) == kvx.ERR_INVALID_ARG
+    assert rs(good, kvx._stream_ctl(None, 1, None, 0, 1000, -1, None, None, 1)) == kvx.ERR_INVALID_ARG
     assert rs(good, kvx._stream_ctl(None, 1, None, 0, 0, 0, None, None, 1)) == kvx.ERR_INVALID_ARG
     assert rs(good, ok, st=ST + 4) == kvx.ERR_INVALID_ARG
     assert rs([(0, 0, 0, 0, 2), (1, 0, 0, 1, 2)], ok) == kvx.ERR_INVALID_ARG  # one head twice

@@ -6,7 +6,8 @@ of the pools restricted to their first k layers (the plane lists cut after layer
 move stops at layer k, and of the token subset whose destination pages are still owned when
 pages are reassigned.  Every failure is made on the host (ready words nothing raises, an epoch
 word the host changes, owner words changed before or during the move), and every device wait
-is bounded, so no case can hang the GPU.
+is bounded, so no case can hang the GPU.  Each case runs on the row grid and on a capped
+persistent grid of 24 CTAs.
 """
 import time
 
@@ -35,6 +36,12 @@ def _cuda():
 
 def _rng(k):
     return np.random.Generator(np.random.PCG64(15000 + k))
+
+
+# max_ctas: 0 = the row grid (default); 24 = a capped persistent grid of 24 CTAs
+@pytest.fixture(params=[0, 24], ids=["rowgrid", "persistent24"])
+def grid(request):
+    return request.param
 
 
 def _pinned(values):
@@ -94,42 +101,45 @@ class Case:
 
 @pytest.mark.parametrize("p_tp,d_tp", [(8, 1), (4, 2), (1, 2), (2, 4)])
 @pytest.mark.parametrize("n", [1, 700, 2600])
-def test_all_layers_ready(p_tp, d_tp, n):
+def test_all_layers_ready(p_tp, d_tp, n, grid):
     c = Case(p_tp, d_tp, n, seed=p_tp * 10 + d_tp + n)
     c.expect()
     st = _status()
     words = torch.ones(L, dtype=torch.int32, device="cuda")
-    c.run(st, layer_ready=words, ready_value=1)
+    c.run(st, layer_ready=words, ready_value=1, max_ctas=grid)
     torch.cuda.synchronize()
-    assert st.cpu().tolist() == [kvx.OK, 0, 0, 1]
-    c.check(f"P TP {p_tp} -> D TP {d_tp}, n={n}")
+    v = st.cpu().tolist()
+    assert v[0:2] == [kvx.OK, 0] and v[3] == 1, v
+    c.check(f"P TP {p_tp} -> D TP {d_tp}, n={n}, {grid} CTAs")
 
 
-def test_layers_raised_late():
+def test_layers_raised_late(grid):
     c = Case(4, 2, 1500, seed=1)
     c.expect()
     ready, done = _pinned([0] * L), _pinned([0])
     st = _status()
     torch.cuda.synchronize()
-    c.run(st, layer_ready=ready, ready_value=1, wait_ns=2_000_000_000, host_done=done)
+    c.run(st, layer_ready=ready, ready_value=1, wait_ns=2_000_000_000, host_done=done,
+          max_ctas=grid)
     for layer in range(L):
         time.sleep(0.01)
         assert int(done[0]) == 0, f"finished before layer {layer} was raised"
         ready[layer] = 1
     torch.cuda.synchronize()
-    assert st.cpu().tolist() == [kvx.OK, 0, 0, 1]
+    v = st.cpu().tolist()
+    assert v[0:2] == [kvx.OK, 0] and v[3] == 1, v
     assert int(done[0]) == 1
     c.check("layers raised late")
 
 
 @pytest.mark.parametrize("k", [0, 3])
-def test_timeout_at_layer(k):
+def test_timeout_at_layer(k, grid):
     c = Case(8, 1, 900, seed=10 + k)
     c.expect(layers=k)
     ready, done = _pinned([1 if layer < k else 0 for layer in range(L)]), _pinned([0])
     st = _status()
     t0 = time.perf_counter()
-    c.run(st, layer_ready=ready, ready_value=1, wait_ns=30_000_000, host_done=done)
+    c.run(st, layer_ready=ready, ready_value=1, wait_ns=30_000_000, host_done=done, max_ctas=grid)
     torch.cuda.synchronize()
     elapsed = time.perf_counter() - t0
     v = st.cpu().tolist()
@@ -139,7 +149,7 @@ def test_timeout_at_layer(k):
     c.check(f"timeout at layer {k}")
 
 
-def test_cancel_while_waiting():
+def test_cancel_while_waiting(grid):
     k = 2
     c = Case(2, 4, 1200, seed=20)
     c.expect(layers=k)
@@ -148,7 +158,7 @@ def test_cancel_while_waiting():
     st = _status()
     torch.cuda.synchronize()
     c.run(st, layer_ready=ready, ready_value=1, epoch_word=epoch, epoch=5,
-          wait_ns=5_000_000_000, host_done=done)
+          wait_ns=5_000_000_000, host_done=done, max_ctas=grid)
     time.sleep(0.05)
     assert int(done[0]) == 0  # waiting for layer k
     epoch[0] = 6
@@ -162,11 +172,11 @@ def test_cancel_while_waiting():
     c.check("cancelled while waiting")
 
 
-def test_cancelled_before_launch_moves_nothing():
+def test_cancelled_before_launch_moves_nothing(grid):
     c = Case(8, 1, 600, seed=30)
     epoch = _pinned([9])
     st = _status()
-    c.run(st, epoch_word=epoch, epoch=8)
+    c.run(st, epoch_word=epoch, epoch=8, max_ctas=grid)
     torch.cuda.synchronize()
     v = st.cpu().tolist()
     assert v[0] == kvx.ERR_CANCELLED and v[1] == L and v[3] == 1, v
@@ -174,7 +184,7 @@ def test_cancelled_before_launch_moves_nothing():
 
 
 @pytest.mark.parametrize("when", ["before", "while_waiting"])
-def test_destination_pages_reassigned(when):
+def test_destination_pages_reassigned(when, grid):
     """Owner epochs per 16-slot destination page: rows into pages given to another request are
     dropped (KVX_ERR_CANCELLED), every other row moves."""
     k = 2
@@ -188,7 +198,7 @@ def test_destination_pages_reassigned(when):
     if when == "before":
         owners[torch.from_numpy(taken)] = 4
         c.expect(keep=keep)
-        c.run(st, dst_page_epochs=owners, epoch_page=16, epoch=3)
+        c.run(st, dst_page_epochs=owners, epoch_page=16, epoch=3, max_ctas=grid)
         torch.cuda.synchronize()
         v = st.cpu().tolist()
         assert v[0] == kvx.ERR_CANCELLED and v[3] == 1, v
@@ -202,7 +212,7 @@ def test_destination_pages_reassigned(when):
         assert rc == oracle.OK
         torch.cuda.synchronize()
         c.run(st, layer_ready=ready, ready_value=1, wait_ns=5_000_000_000, host_done=done,
-              dst_page_epochs=owners, epoch_page=16, epoch=3)
+              dst_page_epochs=owners, epoch_page=16, epoch=3, max_ctas=grid)
         time.sleep(0.05)
         owners[torch.from_numpy(taken)] = 4
         time.sleep(0.01)  # the owner words are visible before any later layer is raised
@@ -219,17 +229,17 @@ def test_destination_pages_reassigned(when):
     c.check(f"pages reassigned {when}")
 
 
-def test_n0_and_out_of_range():
+def test_n0_and_out_of_range(grid):
     c = Case(2, 1, 0, seed=50)
     st = _status()
-    c.run(st)
+    c.run(st, max_ctas=grid)
     torch.cuda.synchronize()
     assert st.cpu().tolist()[:2] == [kvx.OK, 0] and st.cpu().tolist()[3] == 1
     c = Case(2, 1, 800, seed=51)
     c.dslots[400] = c.num
     c.dd = hz.dev_i32(c.dslots)
     st = _status()
-    c.run(st)
+    c.run(st, max_ctas=grid)
     torch.cuda.synchronize()
     v = st.cpu().tolist()
     assert v[0] == kvx.ERR_OUT_OF_RANGE and v[1] == L and v[3] == 1, v
