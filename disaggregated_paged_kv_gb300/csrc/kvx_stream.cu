@@ -61,18 +61,19 @@ constexpr int kWarps = kCopyThreads / 32;
 // CTAs keeps 64 KiB of rows in flight on each of its SMs.
 constexpr int kPersistThreads = 1024;
 constexpr int kPersistWarps = kPersistThreads / 32;
+
 struct StreamArgs {
   CopyArgs c;   // sides, planes, buffer, status, slot lists (spec_src / spec_dst)
   StreamCtl k;
 };
 
 // ---- persistent grid, bulk form ----------------------------------------------------------
-// The persistent grid's items with one token each, moved by TMA bulk copies instead of
-// registers (kvx_bulk_ops.cuh): every thread owns one kBulkStage-byte shared-memory stage and
-// one mbarrier and moves whole rows, global -> stage -> global, reusing its stage once the
-// previous store has read it.  A CTA of kBulkThreads threads keeps kBulkThreads stages in
-// flight (~192 KiB), where the register form keeps 16 KiB per CTA, so few SMs reach the copy
-// bandwidth: this is the form to leave most of the GPU to a producer.  Layer waits, stops,
+// The persistent grid's items with one token each, moved only by TMA bulk copies
+// (kvx_bulk_ops.cuh), with kvx_set_copy_engine(KVX_ENGINE_BULK): every thread owns one
+// kBulkStage-byte shared-memory stage and one mbarrier and moves whole rows (longer rows in
+// pieces), global -> stage -> global, reusing its stage once the previous store has read it.
+// A CTA of kBulkThreads threads keeps ~192 KiB in flight, yet it moves less per SM than the
+// register form: each bulk operation has a fixed cost on the SM.  Layer waits, stops,
 // page-owner checks and the exit protocol are the register form's.
 
 constexpr int kBulkThreads = 96;
