@@ -54,10 +54,12 @@ def _changed(pool, slots_per_plane):
                         for p in range(pool.shape[0])])
 
 
-def test_stream_full_size_timeout_at_layer_20():
+@pytest.mark.parametrize("max_ctas", [0, 76], ids=["rowgrid", "capped76"])
+def test_stream_full_size_timeout_at_layer_20(max_ctas):
     """The headline request through kvx_stream with ready words in pinned host memory, layers
     0..19 raised and 20.. never: KVX_ERR_TIMEOUT, layers below 20 moved (sampled rows equal the
-    oracle's layer-range transfer), every row of the later layers untouched."""
+    oracle's layer-range transfer), every row of the later layers untouched; on the row grid and
+    on a persistent grid capped at half the SMs."""
     k = 20
     src = _pool((P, S, H, D), "normal", inputs.seed(2, 0))
     dst = _pool((P, S, H, D), "sentinel")
@@ -69,7 +71,8 @@ def test_stream_full_size_timeout_at_layer_20():
     st = torch.full((4,), -1, dtype=torch.int32, device="cuda")
     ws = torch.empty(kvx.workspace_size(N), dtype=torch.uint8, device="cuda")
     kvx.stream(kvx.OP_TRANSFER, sl, torch.from_numpy(s).cuda(), dl, torch.from_numpy(d).cuda(), N,
-               None, ws, st, layer_ready=ready, ready_value=1, wait_ns=50_000_000, buf_bytes=0)
+               None, ws, st, layer_ready=ready, ready_value=1, wait_ns=50_000_000, buf_bytes=0,
+               max_ctas=max_ctas)
     torch.cuda.synchronize()
     v = st.cpu().tolist()
     assert v[0] == kvx.ERR_TIMEOUT and v[1] == L - k and v[3] == 1, v
