@@ -424,10 +424,12 @@ typedef struct kvx_stream_ctl {
   int64_t wait_ns;
   /* 0: one warp per row (group) on as many CTAs as the request needs; CTAs waiting for a
    * layer hold their SM slots.  > 0: a persistent grid of at most max_ctas CTAs, at most one
-   * per SM (1024 threads moving rows through registers; with kvx_set_copy_engine(
-   * KVX_ENGINE_BULK), 96 threads moving rows by TMA bulk copies through shared memory), for
-   * the whole move, leaving the rest of the GPU to a producer running on the same GPU, which
-   * needs SMs to make progress. */
+   * per SM, for the whole move, leaving the rest of the GPU to a producer running on the same
+   * GPU, which needs SMs to make progress.  Its CTAs (see kvx_set_copy_engine): by default
+   * 1024 threads moving rows through registers, three of their warps by TMA bulk copies where
+   * a row group fits one 2 KiB stage; KVX_ENGINE_REGISTERS: registers only; KVX_ENGINE_BULK:
+   * 96 threads moving rows by TMA bulk copies only.  Every SM moves at most ~89 GB/s
+   * (read + write) in any form, so the HBM peak takes about half the SMs. */
   int32_t max_ctas;
   int32_t reserved;  /* must be 0 */
   /* Pinned host int32 or NULL: set to 1 when d_status[3] is (see kvx_stream). */
@@ -497,8 +499,9 @@ KVX_API kvx_status kvx_stream_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
 /* Which kernel moves linear chunks (rows contiguous on both sides).  KVX_ENGINE_BULK uses the
  * TMA bulk-copy kernel (cp.async.bulk through shared memory); KVX_ENGINE_AUTO (default) and
  * KVX_ENGINE_REGISTERS use 16-byte register loads and stores.  Both move the same bytes;
- * chunks that are not linear always take the register path.  Process-wide; returns
- * KVX_ERR_INVALID_ARG for an unknown value. */
+ * chunks that are not linear always take the register path.  It also picks the form of
+ * kvx_stream's capped persistent grid (kvx_stream_ctl::max_ctas).  Read once per call;
+ * process-wide; returns KVX_ERR_INVALID_ARG for an unknown value. */
 #define KVX_ENGINE_AUTO 0
 #define KVX_ENGINE_REGISTERS 1
 #define KVX_ENGINE_BULK 2
