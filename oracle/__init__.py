@@ -68,9 +68,9 @@ class Request(ctypes.Structure):
     ]
 
 
-class Chunk(ctypes.Structure):
+class Run(ctypes.Structure):
     _fields_ = [("req", ctypes.c_int32), ("src", ctypes.c_int32), ("dst", ctypes.c_int32),
-                ("rows", ctypes.c_int32)]
+                ("len", ctypes.c_int32)]
 
 
 class Part(ctypes.Structure):
@@ -122,10 +122,9 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
     lib.kvxo_hnd_rebuild.argtypes = [P(_Pool), i32p, ctypes.c_int64, u8p]
     lib.kvxo_batch.argtypes = [P(_Pool), P(_Pool), P(Request), ctypes.c_int32, i32p,
                                ctypes.c_int64, i32p, ctypes.c_int64, u8p, ctypes.c_int64, i32p]
-    lib.kvxo_plan.restype = ctypes.c_int64
-    lib.kvxo_plan.argtypes = [i32p, i32p, ctypes.c_int64, P(ctypes.c_int64), ctypes.c_int32,
-                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                              P(Chunk), ctypes.c_int64]
+    lib.kvxo_runs.restype = ctypes.c_int64
+    lib.kvxo_runs.argtypes = [i32p, i32p, ctypes.c_int64, P(ctypes.c_int64), ctypes.c_int32,
+                              P(Run), ctypes.c_int64]
     _lib_cache[path] = lib
     return lib
 
@@ -338,16 +337,16 @@ def batch(src: Optional[Pool], dst: Optional[Pool], reqs: Sequence[tuple], src_s
     return status
 
 
-def plan(src_idx, dst_idx, req_start, src_page_size: int, dst_page_size: int,
-         tile_tokens: int, chunk_rows: int, lib=None) -> np.ndarray:
-    """Run-length plan; returns an int32 array [n_chunks][4] = (req, src, dst, rows)."""
+def runs(src_idx, dst_idx, req_start=(0,), lib=None) -> np.ndarray:
+    """Run-length coalescing of two index lists (kvxo_runs); returns an int32 array
+    [n_runs][4] = (req, src, dst, len) in token order."""
     lib = lib or load()
     a, b = _i32(src_idx), _i32(dst_idx)
+    assert len(a) == len(b)
     rs = np.ascontiguousarray(np.asarray(req_start, dtype=np.int64))
     n = len(a)
-    out = (Chunk * max(1, n))()
-    cnt = lib.kvxo_plan(_i32p(a), _i32p(b), n, rs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
-                        len(rs), src_page_size, dst_page_size, tile_tokens, chunk_rows, out, n)
+    out = (Run * max(1, n))()
+    cnt = lib.kvxo_runs(_i32p(a), _i32p(b), n, rs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                        len(rs), out, n)
     assert 0 <= cnt <= n
-    res = np.frombuffer(out, dtype=np.int32).reshape(-1, 4)[:cnt].copy()
-    return res
+    return np.frombuffer(out, dtype=np.int32).reshape(-1, 4)[:cnt].copy()

@@ -441,54 +441,30 @@ int kvxo_batch(const kvxo_pool *src, const kvxo_pool *dst, const kvxo_request *r
   return status[0];
 }
 
-int64_t kvxo_plan(const int32_t *src_idx, const int32_t *dst_idx, int64_t n,
-                  const int64_t *req_start, int32_t n_reqs, int32_t src_page_size,
-                  int32_t dst_page_size, int32_t tile_tokens, int32_t chunk_rows,
-                  kvxo_chunk *out, int64_t max_chunks) {
-  /* [Mooncake] 7.6: consecutive blocks are merged into one descriptor.  Step 1 marks the
-   * tokens where a run must start; step 2 walks the runs and cuts each into pieces of at most
-   * chunk_rows rows. */
-  int32_t *req_of = NULL;
-  unsigned char *brk = NULL;
+int64_t kvxo_runs(const int32_t *src_idx, const int32_t *dst_idx, int64_t n,
+                  const int64_t *req_start, int32_t n_reqs, kvxo_run *out, int64_t max_runs) {
+  /* [Mooncake] 7.6 (_build_transfer_params): blocks whose addresses follow one another are
+   * merged into one descriptor (source start, destination start, length).  A run therefore
+   * goes on while both index sequences step up by exactly one; it ends where either one does
+   * not, and (a batch being a list of separate requests, [Mooncake] 6.1) where a new request
+   * starts.  Nothing else ends a run. */
   int64_t count = 0;
+  int32_t q = 0;
   if (n <= 0) return 0;
-  req_of = (int32_t *)malloc((size_t)n * sizeof(int32_t));
-  brk = (unsigned char *)calloc((size_t)n, 1);
-  if (!req_of || !brk) {
-    free(req_of);
-    free(brk);
-    return -1;
-  }
-  /* request of every token, and request starts */
-  for (int32_t q = 0; q < n_reqs; ++q) {
-    int64_t end = (q + 1 < n_reqs) ? req_start[q + 1] : n;
-    for (int64_t i = req_start[q]; i < end; ++i) req_of[i] = q;
-    if (req_start[q] < n) brk[req_start[q]] = 1;
-  }
-  /* step 1: run starts */
-  for (int64_t i = 0; i < n; ++i) {
-    if (i == 0 || i % tile_tokens == 0) brk[i] = 1;
-    if (i > 0 && src_idx[i] != src_idx[i - 1] + 1) brk[i] = 1;
-    if (i > 0 && dst_idx[i] != dst_idx[i - 1] + 1) brk[i] = 1;
-    if (src_page_size > 1 && src_idx[i] % src_page_size == 0) brk[i] = 1;
-    if (dst_page_size > 1 && dst_idx[i] % dst_page_size == 0) brk[i] = 1;
-  }
-  /* step 2: each run [a, b) becomes ceil((b - a) / chunk_rows) chunks */
   for (int64_t a = 0; a < n;) {
+    while (q + 1 < n_reqs && req_start[q + 1] <= a) ++q; /* request of token a */
+    const int64_t req_end = (q + 1 < n_reqs) ? req_start[q + 1] : n;
     int64_t b = a + 1;
-    while (b < n && !brk[b]) ++b;
-    for (int64_t j = 0; j < b - a; j += chunk_rows) {
-      if (count < max_chunks) {
-        out[count].req = req_of[a];
-        out[count].src = src_idx[a] + (int32_t)j;
-        out[count].dst = dst_idx[a] + (int32_t)j;
-        out[count].rows = (int32_t)((b - a - j) < chunk_rows ? (b - a - j) : chunk_rows);
-      }
-      ++count;
+    while (b < req_end && src_idx[b] == src_idx[b - 1] + 1 && dst_idx[b] == dst_idx[b - 1] + 1)
+      ++b;
+    if (count < max_runs) {
+      out[count].req = q;
+      out[count].src = src_idx[a];
+      out[count].dst = dst_idx[a];
+      out[count].len = (int32_t)(b - a);
     }
+    ++count;
     a = b;
   }
-  free(req_of);
-  free(brk);
   return count;
 }

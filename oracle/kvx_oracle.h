@@ -79,12 +79,12 @@ typedef struct kvxo_request {
   int64_t buf_off; /* byte offset of this request's [plane][token][head][dim] region */
 } kvxo_request;
 
-typedef struct kvxo_chunk {
-  int32_t req;  /* request the rows belong to */
-  int32_t src;  /* first source index (slot, or token for a buffer side) */
-  int32_t dst;  /* first destination index */
-  int32_t rows; /* consecutive rows covered */
-} kvxo_chunk;
+typedef struct kvxo_run {
+  int32_t req; /* request the rows belong to */
+  int32_t src; /* first source index (slot, or token for a buffer side) */
+  int32_t dst; /* first destination index */
+  int32_t len; /* consecutive tokens covered */
+} kvxo_run;
 
 /* B_KV per token = 2 * n_layer * n_kvhead * d_head * b   ([DistServe] KV Cache 跨实例传输). */
 int64_t kvxo_bytes_per_token(int32_t num_layers, int32_t kv_heads, int32_t head_dim,
@@ -197,17 +197,15 @@ int kvxo_batch(const kvxo_pool *src, const kvxo_pool *dst, const kvxo_request *r
                const int32_t *dst_slots, int64_t n_dst_slots, uint8_t *buf, int64_t buf_bytes,
                int32_t *status);
 
-/* Run-length plan ([Mooncake] 7.6: contiguous blocks coalesced into fewer descriptors).
- * src_idx / dst_idx give each token's source and destination index (slot, or the token's own
- * position for a buffer side).  req_start lists the first token of every request (ascending,
- * req_start[0] = 0).  A run ends where either index sequence stops increasing by one, at a
- * request start, at every multiple of tile_tokens, and at each page start of a side whose
- * page_size > 1.  Each run is cut into pieces of at most chunk_rows rows.
- * Writes up to max_chunks chunks and returns the number of chunks. */
-int64_t kvxo_plan(const int32_t *src_idx, const int32_t *dst_idx, int64_t n,
-                  const int64_t *req_start, int32_t n_reqs, int32_t src_page_size,
-                  int32_t dst_page_size, int32_t tile_tokens, int32_t chunk_rows,
-                  kvxo_chunk *out, int64_t max_chunks);
+/* Run-length coalescing ([Mooncake] 7.6: blocks at consecutive addresses are merged into one
+ * (source, destination, length) descriptor).  src_idx / dst_idx give each token's source and
+ * destination index (slot, or the token's own position for a buffer side).  req_start lists
+ * the first token of every request (ascending, req_start[0] = 0).  A run is a longest stretch
+ * of tokens of one request over which both index sequences step up by exactly one: it ends
+ * where either sequence does not, and at a request start; nothing else ends it.
+ * Writes up to max_runs runs in token order and returns the number of runs. */
+int64_t kvxo_runs(const int32_t *src_idx, const int32_t *dst_idx, int64_t n,
+                  const int64_t *req_start, int32_t n_reqs, kvxo_run *out, int64_t max_runs);
 
 #ifdef __cplusplus
 }

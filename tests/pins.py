@@ -592,67 +592,94 @@ def pin_batch(lib):
     assert list(st) == [1, 1, 1, 1, 1]
 
 
-def _expand(chunks):
+def _expand(runs):
     src, dst = [], []
-    for _, s, d, rows in chunks:
-        src.extend(range(s, s + rows))
-        dst.extend(range(d, d + rows))
+    for _, s, d, n in runs:
+        src.extend(range(s, s + n))
+        dst.extend(range(d, d + n))
     return src, dst
 
 
+def _coarsest_segmentation(src, dst, reqs):
+    """Brute force: among every way of cutting tokens 0..n-1 into consecutive pieces, keep the
+    cuttings whose pieces lie in one request and step up by one on both lists, and return the
+    one with the fewest pieces (as (req, src, dst, len) tuples).  [Mooncake] 7.6 merges every
+    block that follows the previous one, so the plan is the coarsest such cutting."""
+    n = len(src)
+    req_of = [max(q for q, r in enumerate(reqs) if r <= i) for i in range(n)]
+    best = None
+    for mask in range(1 << (n - 1)):
+        cuts = [0] + [i for i in range(1, n) if mask >> (i - 1) & 1] + [n]
+        pieces = []
+        ok = True
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            for i in range(a + 1, b):
+                if (src[i] != src[a] + (i - a) or dst[i] != dst[a] + (i - a)
+                        or req_of[i] != req_of[a]):
+                    ok = False
+            pieces.append((req_of[a], src[a], dst[a], b - a))
+        if ok and (best is None or len(pieces) < len(best)):
+            best = pieces
+    return best
+
+
 def pin_plan(lib):
-    """[Mooncake] 7.6 coalescing.  Invariants: expanding the chunks gives back the index lists;
-    a fully contiguous list within one tile is one run; the number of runs is 1 + the number of
-    places where either list stops increasing by one (plus forced breaks); no chunk crosses a
-    tile boundary, a request start, or a page start of a paged side; chunks are <= chunk_rows."""
+    """[Mooncake] 7.6 coalescing, by brute force: for every pair of index lists of up to three
+    tokens over four values and every request split, the oracle's runs are the coarsest
+    cutting of the tokens into pieces that stay in one request and step up by one on both
+    lists (found by trying every cutting); the same on random four- and five-token cases.
+    Invariants on long lists: the runs expand back to the index lists, the run count is
+    1 + the number of places where either list stops stepping by one or a request starts, and
+    a contiguous request of any length is a single run (nothing else, such as a tile or a page
+    boundary, ends a run)."""
+    import itertools
+    for n in (1, 2, 3):
+        lists = list(itertools.product(range(4), repeat=n))
+        splits = [[0] + list(c) for k in range(n) for c in itertools.combinations(range(1, n), k)]
+        for src in lists:
+            for dst in lists:
+                for reqs in splits:
+                    got = oracle.runs(src, dst, reqs, lib=lib)
+                    want = _coarsest_segmentation(src, dst, reqs)
+                    assert [tuple(r) for r in got.tolist()] == want, (src, dst, reqs)
     g = np.random.Generator(np.random.PCG64(23))
-    # contiguous: one run, split only by chunk_rows
-    n = 100
-    ch = oracle.plan(np.arange(5, 5 + n), np.arange(n), [0], 1, 1, 4096, 16, lib=lib)
-    assert len(ch) == (n + 15) // 16 and ch[:, 3].sum() == n
-    assert ch[0].tolist() == [0, 5, 0, 16]
-    ch = oracle.plan(np.arange(5, 5 + n), np.arange(n), [0], 1, 1, 4096, 1000, lib=lib)
-    assert len(ch) == 1
-    # random fragments with several requests, pages and tiles
-    for trial in range(30):
-        n = int(g.integers(1, 300))
-        def runs_of(hi):  # independent run structure for each side
+    for trial in range(400):
+        n = int(g.integers(4, 6))
+        base = g.integers(0, 3, 2)
+        src = (base[0] + np.cumsum(g.choice([0, 1, 1, 1, 2], n))).tolist()
+        dst = (base[1] + np.cumsum(g.choice([0, 1, 1, 1, -1], n))).tolist()
+        reqs = [0] + sorted(set(g.integers(1, n, int(g.integers(0, 3))).tolist()))
+        got = oracle.runs(src, dst, reqs, lib=lib)
+        assert [tuple(r) for r in got.tolist()] == _coarsest_segmentation(src, dst, reqs)
+    # a contiguous request is one run whatever its length (72 blocks on a fresh pool,
+    # "穷人版 PD 分离", 5090 section: one block per layer and K/V)
+    for n in (1, 2047, 2048, 2049, 100000):
+        got = oracle.runs(np.arange(7, 7 + n), np.arange(n), [0], lib=lib)
+        assert got.tolist() == [[0, 7, 0, n]]
+    # long random lists with several requests
+    for trial in range(40):
+        n = int(g.integers(1, 3000))
+        def runs_of(hi):  # an independent run structure for each list
             r = []
             while sum(r) < n:
                 r.append(int(g.integers(1, hi)))
             return np.concatenate([np.arange(s, s + k) for s, k in
                                    zip(g.integers(0, 1000, len(r)), r)])[:n]
         src = runs_of(6) if trial % 3 else np.arange(40, 40 + n)
-        dst = runs_of(6) if trial % 3 != 1 else np.arange(n)
-        reqs = sorted(set([0] + list(g.integers(0, n, int(g.integers(0, 4))))))
-        sps, dps = int(g.choice([1, 4])), int(g.choice([1, 8]))
-        tile, rows_max = int(g.choice([7, 64, 4096])), int(g.choice([1, 3, 16]))
-        ch = oracle.plan(src, dst, reqs, sps, dps, tile, rows_max, lib=lib)
-        s2, d2 = _expand(ch)
+        dst = runs_of(9) if trial % 3 != 1 else np.arange(n)
+        reqs = sorted(set([0] + list(g.integers(0, n, int(g.integers(0, 5))))))
+        got = oracle.runs(src, dst, reqs, lib=lib)
+        s2, d2 = _expand(got)
         assert s2 == src.tolist() and d2 == dst.tolist()
-        assert (ch[:, 3] >= 1).all() and (ch[:, 3] <= rows_max).all()
-        starts = np.concatenate([[0], np.cumsum(ch[:, 3])[:-1]])
-        for (q, s, d, rows), t0 in zip(ch, starts):
-            t1 = t0 + rows
-            assert t0 // tile == (t1 - 1) // tile
-            assert not any(t0 < r < t1 for r in reqs)
-            assert q == max(i for i, r in enumerate(reqs) if r <= t0)
-            if sps > 1:
-                assert not any((s + j) % sps == 0 for j in range(1, rows))
-            if dps > 1:
-                assert not any((d + j) % dps == 0 for j in range(1, rows))
-        # count of runs: a run boundary exists exactly at forced or natural breaks
+        assert (got[:, 3] >= 1).all()
         brk = np.zeros(n, bool)
         brk[0] = True
         brk[1:] |= (src[1:] != src[:-1] + 1) | (dst[1:] != dst[:-1] + 1)
-        brk[np.arange(n) % tile == 0] = True
         brk[reqs] = True
-        if sps > 1:
-            brk |= src % sps == 0
-        if dps > 1:
-            brk |= dst % dps == 0
-        run_len = np.diff(np.concatenate([np.flatnonzero(brk), [n]]))
-        assert len(ch) == int(((run_len + rows_max - 1) // rows_max).sum())
+        assert len(got) == 1 + int(brk[1:].sum())
+        starts = np.concatenate([[0], np.cumsum(got[:, 3])[:-1]])
+        for (q, _, _, _), t0 in zip(got, starts):
+            assert q == max(i for i, r in enumerate(reqs) if r <= t0)
 
 
 ALL_PINS = [pin_sizes, pin_bytes_written, pin_bruteforce_gather, pin_bruteforce_scatter,

@@ -355,8 +355,27 @@ def _export(ws, n):
     return out[:c].cpu().numpy()
 
 
+def _assert_refines(chunks, runs, max_rows):
+    """The kernel's plan refines the oracle's runs: every chunk lies inside one run, at the
+    matching offset on both index lists and in the same request, and every run boundary is a
+    chunk boundary, so the chunks, in order, concatenate to the runs.  How the kernel cuts a
+    run (tiles, page starts, chunk size) is its own choice; only max_rows bounds a chunk."""
+    assert len(chunks) >= len(runs)
+    assert (chunks[:, 3] >= 1).all() and (chunks[:, 3] <= max_rows).all()
+    ct = np.concatenate([[0], np.cumsum(chunks[:, 3].astype(np.int64))])
+    rt = np.concatenate([[0], np.cumsum(runs[:, 3].astype(np.int64))])
+    assert ct[-1] == rt[-1], "the chunks cover another number of tokens than the runs"
+    r = np.searchsorted(rt, ct[:-1], side="right") - 1
+    off = ct[:-1] - rt[r]
+    assert (ct[1:] <= rt[r + 1]).all(), "a chunk crosses a run boundary"
+    assert np.array_equal(chunks[:, 0], runs[r, 0]), "chunk request differs from its run's"
+    assert np.array_equal(chunks[:, 1], runs[r, 1] + off), "chunk source offset"
+    assert np.array_equal(chunks[:, 2], runs[r, 2] + off), "chunk destination offset"
+    assert np.isin(rt, ct).all(), "a run boundary is not a chunk boundary"
+
+
 @pytest.mark.parametrize("dst_kind", ["planes", "hnd"])
-def test_plan_matches_oracle(dst_kind):
+def test_plan_refines_oracle_runs(dst_kind):
     g = _rng(700)
     n = 6000
     src = _pool("planes", "normal", g, num_slots=40000)
@@ -369,12 +388,13 @@ def test_plan_matches_oracle(dst_kind):
              hz.dev_i32(d), n, ws, st)
     assert _sync_status(st) == [0]
     got = _export(ws, n)
-    rows = max(1, kvx.CHUNK_BYTES // src.R)
-    want = oracle.plan(s, d, [0], 1, 16 if dst_kind == "hnd" else 1, kvx.PLAN_TILE, rows)
-    assert got.shape == want.shape and np.array_equal(got, want)
+    want = oracle.runs(s, d, [0])
+    _assert_refines(got, want, max(1, kvx.CHUNK_BYTES // src.R))
+    if dst_kind == "hnd":  # a chunk is contiguous on an HND side only within one page
+        assert not any((c[2] % 16) + c[3] > 16 for c in got)
 
 
-def test_plan_batch_matches_oracle():
+def test_plan_batch_refines_oracle_runs():
     g = _rng(701)
     lens = [3000, 1, 0, 2500, 40]
     n = sum(lens)
@@ -394,8 +414,9 @@ def test_plan_batch_matches_oracle():
     assert _sync_status(st) == [0] * (len(reqs) + 1)
     got = _export(ws, n)
     starts = np.concatenate([[0], np.cumsum(lens)[:-1]])
-    want = oracle.plan(s, d, starts, 1, 1, kvx.PLAN_TILE, max(1, kvx.CHUNK_BYTES // src.R))
-    assert np.array_equal(got, want)
+    want = oracle.runs(s, d, starts)
+    assert want[:, 3].tolist() == [3000, 1, 2500, 40]  # one run per non-empty request
+    _assert_refines(got, want, max(1, kvx.CHUNK_BYTES // src.R))
 
 
 # ---------------------------------------------------------------------------------------

@@ -35,9 +35,10 @@ MUTANTS = {
     "permute_missing": ("memcpy(buf_vec(buf, src, p, seq_len, s, h), logical + ((int64_t)h * seq_len + s) * hb,",
                         "memcpy(buf_vec(buf, src, p, seq_len, s, h), logical + ((int64_t)s * H + h) * hb,"),
     "factor_two_dropped": ("return (int64_t)2 * num_layers", "return (int64_t)num_layers"),
-    "plan_dst_break_dropped": ("if (i > 0 && dst_idx[i] != dst_idx[i - 1] + 1) brk[i] = 1;", ""),
-    "plan_tile_break_dropped": ("if (i == 0 || i % tile_tokens == 0) brk[i] = 1;",
-                                "if (i == 0) brk[i] = 1;"),
+    "runs_dst_break_dropped": (" && dst_idx[b] == dst_idx[b - 1] + 1)", ")"),
+    "runs_request_break_dropped": ("const int64_t req_end = (q + 1 < n_reqs) ? req_start[q + 1] : n;",
+                                   "const int64_t req_end = n;"),
+    "runs_src_step_of_two": ("src_idx[b] == src_idx[b - 1] + 1 &&", "src_idx[b] >= src_idx[b - 1] + 1 &&"),
     "batch_status_not_per_request": ("status[1 + q] = rc;", "status[1 + q] = 0;"),
     "layers_one_short": ("for (int32_t layer = 0; layer < stop; ++layer)\n    for (int32_t kv = 0; kv < ppl; ++kv)\n      for (int64_t i = 0; i < n; ++i)\n        for",
                          "for (int32_t layer = 0; layer + 1 < stop; ++layer)\n    for (int32_t kv = 0; kv < ppl; ++kv)\n      for (int64_t i = 0; i < n; ++i)\n        for"),
