@@ -106,3 +106,27 @@ class Stager:
                 where = f" (row {i // row_bytes}, byte {i % row_bytes})" if row_bytes else ""
                 raise AssertionError(f"{what}: first difference at byte {i}{where}: device "
                                      f"{int(h[i - a])}, oracle {int(want[i])}")
+
+
+GUARD = 64 * 1024
+
+
+def guarded(shape, dtype, fill: str, sentinel16: int, seed: int = 0):
+    """A device tensor of `shape` and torch `dtype` between two 64 KiB guard bands holding the
+    16-bit sentinel: returns (the whole uint8 tensor, the tensor).  fill is "normal" (seeded
+    N(0,1)), "bytes" (seeded uniform bytes, for uint8 tensors) or "sentinel"."""
+    import torch
+
+    n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    whole = torch.empty(n + 2 * GUARD, dtype=torch.uint8, device="cuda")
+    whole.view(torch.int16).fill_(sentinel16 - 65536 if sentinel16 >= 32768 else sentinel16)
+    body = whole[GUARD: GUARD + n].view(dtype).view(shape)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    if fill == "normal":
+        torch.randn(shape, dtype=dtype, device="cuda", generator=g, out=body)
+    elif fill == "bytes":
+        torch.randint(0, 256, shape, dtype=dtype, device="cuda", generator=g, out=body)
+    else:
+        assert fill == "sentinel", fill
+    return whole, body

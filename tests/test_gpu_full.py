@@ -25,7 +25,7 @@ from disaggregated_paged_kv_gb300 import kvx  # noqa: E402
 
 SENT = {"bf16": 0x7FC1, "fp16": 0x7E01}  # quiet NaNs that N(0,1) never produces
 DT = {"bf16": torch.bfloat16, "fp16": torch.float16}
-GUARD = 64 * 1024
+GUARD = fullsize.GUARD
 
 
 @pytest.fixture(scope="module")
@@ -42,15 +42,7 @@ def _clean():
 
 def _guarded(shape, dtype, fill, seed=0):
     """A device pool of `shape` between two sentinel guard bands: (whole uint8 tensor, pool)."""
-    n = int(np.prod(shape)) * 2
-    whole = torch.empty(n + 2 * GUARD, dtype=torch.uint8, device="cuda")
-    whole.view(torch.int16).fill_(SENT[dtype])
-    body = whole[GUARD: GUARD + n].view(DT[dtype]).view(shape)
-    if fill == "normal":
-        g = torch.Generator(device="cuda")
-        g.manual_seed(seed)
-        torch.randn(shape, dtype=DT[dtype], device="cuda", generator=g, out=body)
-    return whole, body
+    return fullsize.guarded(shape, DT[dtype], fill, SENT[dtype], seed)
 
 
 def _rows_pool(w, arr, num_slots, at=0):
