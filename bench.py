@@ -5,8 +5,10 @@ Workload (a step = one pass of the whole hot path: index validation + run-length
 a 2048-token prompt, 36 layers x K/V x 8 kv heads x head_dim 128 bf16 (144 KiB/token, 288 MiB),
 moved pool-to-pool between two 65,536-slot token pools (72 per-plane tensors each, 9 GiB per
 pool) in one GB300's HBM; source and destination slot lists are 2048 distinct uniformly random
-slots each.  Inputs are resident in HBM before the timed region; L2 is flushed (a write of
-2x the L2 size) before every timed step, outside the step's CUDA events.
+slots each.  Inputs are resident in HBM before the timed region; L2 is flushed before every
+timed step, outside the step's CUDA events: a write of 2x the L2 size, then a read of another
+2x L2 buffer so that the flush's own dirty lines are written back before the step (the line
+also reports the step after a write-only flush, and back to back without any flush).
 
 Metric: GB/s moved = (payload read + payload written + index bytes) / device time per step.
 
@@ -19,6 +21,7 @@ replica on its own GPU (no data-path collective); rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -62,10 +65,18 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="headline line only: skip the other four workloads' summaries")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--pool-slots", type=int, default=SLOTS,
                     help="slots per plane of both pools (smaller pools for profiler captures; "
                          "the request itself is unchanged)")
+    ap.add_argument("--workload-slots", type=int, default=None,
+                    help="--workload fragmented|batch|hnd_permute: slots per plane of its pools "
+                         "(smaller pools for profiler captures; the request is unchanged)")
+    ap.add_argument("--batch-requests", type=int, default=None,
+                    help="--workload batch: only the first N of its 64 requests (profiler "
+                         "captures)")
     ap.add_argument("--fused-max", type=int, default=None,
                     help="kvx_set_fused_max_tokens for this run (0: planner + copy launches only)")
     ap.add_argument("--workload", default="transfer",
@@ -170,6 +181,35 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+class L2Flush:
+    """What runs on the stream between two timed steps so that no step finds the previous one's
+    data in L2: a write of a buffer of 2x the L2 size (every line the previous step left is
+    evicted), then a read of another 2x L2 buffer, so that the lines the write left dirty are
+    written back here, outside the timed region, instead of inside the next step.  `write_only`
+    keeps just the write (its dirty lines are then written back during the next step)."""
+
+    def __init__(self, dev, l2_bytes: int, write_only: bool = False):
+        import torch
+
+        n = max(2 * l2_bytes, 256 << 20)
+        self.w = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(n // 8, dtype=torch.int64, device=dev)
+        self.sink = torch.empty(1, dtype=torch.int64, device=dev)
+        self.write_only = write_only
+
+    def fill_(self, v: int):
+        import torch
+
+        self.w.fill_(v)
+        if not self.write_only:
+            torch.sum(self.r, dim=0, keepdim=True, out=self.sink)
+
+
+L2_NOTE = ("flushed before every timed step, outside the events: a write of 2x L2 (evicts the "
+           "previous step's lines) then a read of another 2x L2 (writes the flush's dirty lines "
+           "back before the step starts)")
+
+
 def step_percentiles(step_ms):
     """p10, median and p90 of per-step times, in us (CUDA event timestamps tick in ~1-2 us
     steps on this GPU, so these are coarse; the mean is the headline)."""
@@ -229,7 +269,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     ws = torch.empty(kvx.workspace_size(N_TOK, 0), dtype=torch.uint8, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, l2)
     torch.cuda.synchronize()
 
     def step():
@@ -255,6 +295,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     clocks = Clocks(local_rank, not args.no_clocks)
     time.sleep(0.3 if clocks.proc else 0)
     with torch.cuda.stream(stream):
+        for _ in range(3):  # untimed: the GPU back at full clocks after the pause above
+            flush.fill_(1)
+            step()
         for i in range(K):
             flush.fill_(i & 0xFF)
             ev[i][0].record(stream)
@@ -308,6 +351,24 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     graph_ms = statistics.mean(a.elapsed_time(b) for a, b in ev5)
     del graph
 
+    # ---- the same step after a write-only flush: L2 then holds up to its size in the flush's
+    # dirty lines, which the step itself has to write back ----
+    wflush = L2Flush(dev, l2, write_only=True)
+    ev6 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for i in range(K + 3):
+            wflush.fill_(i & 0xFF)
+            if i >= 3:
+                ev6[i - 3][0].record(stream)
+            step()
+            if i >= 3:
+                ev6[i - 3][1].record(stream)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvx.OK
+    write_only_ms = statistics.mean(a.elapsed_time(b) for a, b in ev6)
+    del wflush
+
     # ---- the copy kernel alone (plan and copy launched separately, same flushes) ----
     ev3 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
     with torch.cuda.stream(stream):
@@ -353,7 +414,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     total_ms = max_over_ranks(total_ms, device=dev)
     return dict(step_ms=step_ms, total_ms=total_ms, plan_ms=plan_ms, copy_ms=copy_ms, e2e=e2e,
                 clocks=clk, device=torch.cuda.get_device_name(dev), noflush_ms=noflush_ms,
-                graph_ms=graph_ms)
+                graph_ms=graph_ms, write_only_ms=write_only_ms)
 
 
 # ---------------------------------------------------------------------------------------
@@ -362,9 +423,14 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 # ---------------------------------------------------------------------------------------
 
 def run_workload(args, name: str):
+    print(json.dumps(measure_workload(args, name)), flush=True)
+
+
+def measure_workload(args, name: str, min_seconds: float = 0.25):
     """Times every leg of the named workload (gather + scatter-back, fragmented gather +
-    scatter, batch, fused-permute gather + rebuild).  Pools, slot lists and page tables come
-    from the same seeded recipe as the tests."""
+    scatter, batch, fused-permute gather + rebuild) and returns its JSON line.  Pools, slot
+    lists and page tables come from the same seeded recipe as the tests.  The timed steps are
+    repeated until they span at least min_seconds, with the SM clocks sampled meanwhile."""
     import numpy as np
     import torch
 
@@ -377,6 +443,8 @@ def run_workload(args, name: str):
     stream = torch.cuda.Stream(device=dev)
     sp = int(stream.cuda_stream)
     w = inputs.WORKLOADS[name]
+    if args.workload_slots and name in ("fragmented", "batch", "hnd_permute"):
+        w = dataclasses.replace(w, num_slots=args.workload_slots)
     sid = w.seed_id
     Pw, Hw, Dw, Rw = w.planes, w.kv_heads, w.head_dim, w.row_bytes
     tdt = torch.float16 if w.dtype == "fp16" else torch.bfloat16
@@ -427,7 +495,7 @@ def run_workload(args, name: str):
                 f"{len(runs)} runs ~Geometric(1.6): gather to a 216 MiB buffer, then scatter into a "
                 f"fresh run layout")
     elif name == "batch":
-        lens = inputs.batch_lengths()
+        lens = inputs.batch_lengths()[: args.batch_requests or None]
         s_np, offs = inputs.paged_request_slots(inputs.rng(sid, 1), lens, w.page_size, w.num_slots)
         d_np, _ = inputs.paged_request_slots(inputs.rng(sid, 2), lens, w.page_size, w.num_slots)
         src = randn((Pw, w.num_slots, Hw, Dw))
@@ -470,7 +538,7 @@ def run_workload(args, name: str):
     else:
         raise SystemExit(f"unknown workload {name}")
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, l2)
 
     def timed(K, flush_l2=True, legs=legs):
         evs = []
@@ -490,7 +558,15 @@ def run_workload(args, name: str):
     timed(max(3, args.warmup))
     assert int(st[0].item()) == kvx.OK, int(st[0].item())
     K = max(3, min(args.steps, 200 if name in ("batch", "hnd_permute") else args.steps))
-    res = timed(K)
+    clocks = Clocks(0, not args.no_clocks)
+    time.sleep(0.2 if clocks.proc else 0)
+    timed(3)  # untimed: the GPU back at full clocks after the pause above
+    res = []
+    t_start = time.perf_counter()
+    while not res or (time.perf_counter() - t_start < min_seconds and len(res) < 50 * K):
+        res += timed(K)
+    clk = clocks.stop()
+    K = len(res)
     total_bytes = sum(b for _, _, b in legs)
     step_ms = statistics.mean(sum(r) for r in res)
     line = {"metric": METRIC, "value": total_bytes / (step_ms * 1e-3) / 1e9, "unit": UNIT,
@@ -499,10 +575,11 @@ def run_workload(args, name: str):
             "config": {"workload": f"{name}: {desc}", "kv_dtype": w.dtype,
                        "alg_bytes_per_step": total_bytes, "requests_per_step": requests,
                        "us_per_request": step_ms * 1e3 / requests,
-                       "l2": "flushed before every timed step (write of 2x L2, outside the events)"},
+                       "l2": L2_NOTE},
             "legs": {name: {"us": statistics.mean(r[j] for r in res) * 1e3,
                             "GBs": b / (statistics.mean(r[j] for r in res) * 1e-3) / 1e9}
-                     for j, (name, _, b) in enumerate(legs)}}
+                     for j, (name, _, b) in enumerate(legs)},
+            "clocks": clk}
     peaks, _ = measured_peaks()
     line["config"]["frac_of_measured_hbm"] = line["value"] / float(peaks["hbm_gbs"])
     line["config"]["frac_of_nominal_8tbs"] = line["value"] / NOMINAL_HBM_GBS
@@ -559,7 +636,35 @@ def run_workload(args, name: str):
                               "warm_l2_value": total_bytes / (gw * 1e-6) / 1e9,
                               "how": "both legs captured once (one launch each: requests of up to 512 "
                                      "tokens skip the planner), replayed"}
-    print(json.dumps(line), flush=True)
+    return line
+
+
+OTHER_WORKLOADS = ("small_gather_scatter", "fragmented", "batch", "hnd_permute")
+
+
+def workload_summaries(args):
+    """The other four workloads, each timed as by --workload NAME, summarised for the headline
+    line (their pools are allocated and freed one workload at a time)."""
+    import torch
+
+    out = {}
+    for name in OTHER_WORKLOADS:
+        torch.cuda.empty_cache()
+        ln = measure_workload(args, name)
+        cfg = ln["config"]
+        out[name] = {"workload": cfg["workload"], "GBs": ln["value"],
+                     "us_per_request": cfg["us_per_request"],
+                     "us_per_step": ln["ms_per_step"] * 1e3,
+                     "requests_per_step": cfg["requests_per_step"],
+                     "alg_bytes_per_step": cfg["alg_bytes_per_step"],
+                     "frac_of_measured_hbm": cfg["frac_of_measured_hbm"],
+                     "frac_of_nominal_8tbs": cfg["frac_of_nominal_8tbs"],
+                     "legs": ln["legs"], "steps": ln["steps"], "clocks": ln["clocks"]}
+        for extra in ("four_layers", "warm_l2", "cuda_graph"):
+            if extra in ln:
+                out[name][extra] = ln[extra]
+    torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------------------------------
@@ -681,7 +786,7 @@ def run_comparators(args):
     s_dev = torch.from_numpy(s_np).to(dev).long()
     d_dev = torch.from_numpy(d_np).to(dev).long()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, l2)
     flat_src = src.view(-1)[: N_TOK * P * H * D]
     flat_dst = dst.view(-1)[: N_TOK * P * H * D]
 
@@ -732,7 +837,7 @@ def run_comparators(args):
         "value": res["contiguous_d2d_copy_us"], "unit": "us", "n_gpus": 1, "steps": args.steps,
         "warmup": 2, "higher_is_better": False, "dtype": "u8", "data": "synthetic",
         "config": {"workload": WORKLOAD, "value": "contiguous D2D copy of the same bytes, us",
-                   "l2": "flushed before every timed step (write of 2x L2, outside the events)"},
+                   "l2": L2_NOTE},
         "comparators": res,
         "GBs": {k: (nb / (v * 1e-6) / 1e9 if isinstance(v, float) and k.endswith("_us") else None)
                 for k, v in res.items()},
@@ -759,7 +864,7 @@ def run_sizes(args):
     stream = torch.cuda.Stream(device=dev)
     sp = int(stream.cuda_stream)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, l2)
     peaks, _ = measured_peaks()
     NS, K = 65536, max(10, min(args.steps, 100))
     sizes = [256, 512, 1024, 2048, 4096, 8192, 16384]
@@ -824,7 +929,7 @@ def run_sizes(args):
                                "planes (2 KiB bf16 and 1 KiB fp8 rows), 65536-slot per-plane "
                                "pools, beside a contiguous copy of the same bytes; value = the "
                                "2048-token 2 KiB-row point",
-                   "l2": "flushed before every timed step (write of 2x L2, outside the events)"},
+                   "l2": L2_NOTE},
         "sizes": results,
         "contiguous_copy_fit": cfit,
         "gpu_launches": 2 * K * len(sizes) * len(shapes),
@@ -856,7 +961,7 @@ def run_formats(args):
     stream = torch.cuda.Stream(device=dev)
     sp = int(stream.cuda_stream)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, l2)
     peaks, _ = measured_peaks()
     # name: (layers, heads, head_dim, elem bytes, kv_planes, tokens, pool slots,
     #        source slot-major, destination slot-major)
@@ -948,7 +1053,7 @@ def run_formats(args):
         "higher_is_better": True, "dtype": "u8", "data": "synthetic (random bytes)",
         "config": {"workload": "pool-to-pool transfers of random slots; value = MLA bf16 "
                                "(27 latent planes x 1152 B, 16384 tokens)",
-                   "l2": "flushed before every timed step (write of 2x L2, outside the events)"},
+                   "l2": L2_NOTE},
         "formats": results,
         "gpu_launches": 2 * args.steps,
     }
@@ -981,7 +1086,7 @@ def run_tp(args):
     ws = torch.empty(kvx.workspace_size(N_TOK, 0), dtype=torch.uint8, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, l2)
     peaks, _ = measured_peaks()
     results = {}
     for p_tp, d_tp in ((1, 2), (2, 1), (4, 2), (2, 4), (8, 1)):
@@ -1135,7 +1240,7 @@ def run_tp(args):
                                "(each D row merged from eight 256-byte pieces) in one call; "
                                "every plan also timed pair by pair (kvx_move_heads)",
                    "pool_slots": NS,
-                   "l2": "flushed before every timed step (write of 2x L2, outside the events)"},
+                   "l2": L2_NOTE},
         "reshards": results,
         "gpu_launches": 2 * args.steps,
     }
@@ -1175,7 +1280,7 @@ def run_stream(args):
     ws = torch.empty(kvx.workspace_size(N_TOK, 0), dtype=torch.uint8, device=dev)
     st = torch.zeros(4, dtype=torch.int32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, l2)
     ready = torch.zeros(L, dtype=torch.int32).pin_memory()
     done = torch.zeros(1, dtype=torch.int32).pin_memory()
 
@@ -1320,7 +1425,7 @@ def run_stream(args):
         "value": gbs, "unit": UNIT, "n_gpus": 1, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms, "higher_is_better": True, "dtype": "u8", "data": "synthetic",
         "config": {"workload": WORKLOAD + "; through kvx_stream", "pool_slots": NS,
-                   "l2": "flushed before every timed step (write of 2x L2, outside the events)"},
+                   "l2": L2_NOTE},
         "all_ready": {"us_per_request": step_ms * 1e3, "GBs": gbs,
                       "frac_of_measured_hbm": gbs / float(peaks["hbm_gbs"]),
                       "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
@@ -1471,7 +1576,7 @@ def main():
                    "frac_of_measured_hbm": value / hbm,
                    "frac_of_nominal_8tbs": value / NOMINAL_HBM_GBS,
                    "plan_us": res["plan_ms"] * 1e3, "copy_us": res["copy_ms"] * 1e3,
-                   "l2": "flushed before every timed step (write of 2x L2, outside the events)",
+                   "l2": L2_NOTE,
                    "steady_state_no_flush": {
                        "us_per_request": res["noflush_ms"] * 1e3,
                        "GBs": alg_bytes(N_TOK) / (res["noflush_ms"] * 1e-3) / 1e9,
@@ -1479,6 +1584,12 @@ def main():
                        / 1e9 / hbm,
                        "how": "back-to-back requests, no flush: inputs larger than L2 (288 MiB "
                               "each way per step), two sets of random slot lists in turn"},
+                   "write_only_flush": {
+                       "us_per_request": res["write_only_ms"] * 1e3,
+                       "GBs": alg_bytes(N_TOK) / (res["write_only_ms"] * 1e-3) / 1e9,
+                       "how": "the same step after a flush that only writes 2x L2: the step "
+                              "then also writes back the flush's dirty lines (up to the L2 "
+                              "size)"},
                    "cuda_graph_replay": {
                        "us_per_request": res["graph_ms"] * 1e3,
                        "GBs": alg_bytes(N_TOK) / (res["graph_ms"] * 1e-3) / 1e9,
@@ -1498,6 +1609,9 @@ def main():
                      "peak_kind": f"{peak_kind} (burst copy)",
                      "achieved_bytes_per_launch": copy_bytes},
     }
+    if world == 1 and not args.no_workloads:
+        del res
+        line["config"]["workloads"] = workload_summaries(args)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line), flush=True)

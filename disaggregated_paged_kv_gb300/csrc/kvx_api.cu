@@ -339,7 +339,7 @@ kvx_status enqueue_plan(const Call &c, kvx::PlanArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (c.mode == kvx::kModeSlots) {
-    if (kvx::num_tiles(c.n_tokens) == 1) {
+    if (kvx::validates_direct(c.n_tokens, a.validate_only != 0)) {
       a.status_direct = 1;
     } else {
       e = cudaMemsetAsync(a.status, 0, sizeof(int32_t), s);
@@ -408,8 +408,8 @@ kvx_status enqueue_copy(const Call &c, const kvx_request *d_reqs, void *d_buf, c
     a.host_status = host_status;
     if (host_status_written) *host_status_written = host_status != nullptr;
     kvx::row_shape(a, &a.row_lanes, &a.rows_per_warp);
-    const cudaError_t e = kvx::launch_copy(
-        a, v, (int)kvx::row_grid(c.n_tokens, c.planes, a.rows_per_warp), s);
+    const int64_t grid = kvx::row_grid(a);
+    const cudaError_t e = kvx::launch_copy(a, v, (int)grid, s);
     return e == cudaSuccess ? KVX_OK : cuda_fail(e);
   }
   a.spec_src = a.spec_dst = nullptr;  // the other kernels read the plan
@@ -967,9 +967,9 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if ((st = stream_mirror(d_ws, n, s, &k)) != KVX_OK) return st;
-  // status[0..3]: verdict, layers pending, CTAs finished, done.  A single-tile planner
+  // status[0..3]: verdict, layers pending, CTAs finished, done.  A one-CTA validation
   // writes all four itself; otherwise they are zeroed first and the planner's tiles raise [0].
-  const bool direct = n > 0 && kvx::num_tiles(n) == 1;
+  const bool direct = kvx::validates_direct(n, true);
   if (!direct) {
     e = cudaMemsetAsync(d_status, 0, 4 * sizeof(int32_t), s);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -1252,8 +1252,8 @@ kvx_status kvx_reshard(const kvx_layout_t *srcs, int32_t n_srcs, const int32_t *
     e = cudaMemsetAsync(d_status, 0, sizeof(int32_t), s);
     return e == cudaSuccess ? KVX_OK : cuda_fail(e);
   }
-  // the validating planner: a single tile writes the verdict itself, more tiles raise it
-  const bool direct = kvx::num_tiles(n) == 1;
+  // the validation: one CTA writes the verdict itself, a multi-tile planner raises it
+  const bool direct = kvx::validates_direct(n, true);
   if (!direct) {
     e = cudaMemsetAsync(d_status, 0, sizeof(int32_t), s);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -1293,7 +1293,7 @@ kvx_status kvx_stream_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
   cudaError_t e;
   if ((st = stream_mirror(d_ws, n, s, &k)) != KVX_OK) return st;
   // status[0..3]: verdict, layers pending, stop code, done; as kvx_stream
-  const bool direct = n > 0 && kvx::num_tiles(n) == 1;
+  const bool direct = kvx::validates_direct(n, true);
   if (!direct) {
     e = cudaMemsetAsync(d_status, 0, 4 * sizeof(int32_t), s);
     if (e != cudaSuccess) return cuda_fail(e);

@@ -188,8 +188,11 @@ __global__ void __launch_bounds__(kCopyThreads, 8)
   }
 }
 
-// Row path.  Non-persistent grid: one warp per (group of G consecutive tokens, plane), token
-// major, with m lanes per token (m * G <= 32; lanes past m * G idle).  Each lane moves vectors
+// Row path.  Non-persistent grid: one warp per (group of G consecutive tokens, plane), plane
+// major -- a CTA's warps take consecutive token groups of one plane and neighbouring CTAs the
+// next ones, so the grid streams through one plane's rows at a time (a buffer side is read or
+// written front to back; page runs of an HND side stay within one CTA) -- with m lanes per
+// token (m * G <= 32; lanes past m * G idle).  Each lane moves vectors
 // li, li + m, li + 2m, ... of its token's row, kUnroll of them in flight per pass.  The host
 // picks (m, G) for the row length (row_shape): as many row bytes in flight per pass as the
 // lanes allow, in as few passes as possible -- a 2 KiB row takes a whole warp (m = 32, one
@@ -224,10 +227,9 @@ template <bool kSrcHnd, bool kDstHnd, bool kSpec, bool kTail>
 __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 6 : 8)
     copy_row_kernel(const __grid_constant__ CopyArgs a) {
   const int lane = threadIdx.x & 31;
-  const uint32_t w = blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
-  const uint32_t P = (uint32_t)a.planes;
-  const uint32_t q = w / P;
-  const int32_t p = (int32_t)(w - q * P);
+  const uint32_t pc = blockIdx.x / a.row_blocks;  // plane-major (CopyArgs::row_blocks)
+  const int32_t p = (int32_t)pc;
+  const uint32_t q = (blockIdx.x - pc * a.row_blocks) * (kCopyThreads / 32) + (threadIdx.x >> 5);
   const int32_t m = a.row_lanes;      // lanes per token
   const int32_t G = a.rows_per_warp;  // tokens per warp
   const int64_t t0 = (int64_t)q * G;
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
   } else {
     pdl_wait();
     if (!header_matches(a)) {
-      if (w == 0 && lane == 0) atomicMax(&a.status[0], (int32_t)KVX_ERR_INVALID_ARG);
+      if (q == 0 && p == 0 && lane == 0) atomicMax(&a.status[0], (int32_t)KVX_ERR_INVALID_ARG);
       return;
     }
     const Chunk ch = reinterpret_cast<const Chunk *>(a.ws + a.L.chunks_off)[t0];  // G == 1
@@ -434,10 +436,11 @@ void row_shape_for(int64_t row_bytes, int32_t *lanes, int32_t *rows) {
   }
 }
 
-int64_t row_grid(int64_t n_tokens, int32_t planes, int32_t rows_per_warp) {
-  const int64_t warps = (n_tokens + rows_per_warp - 1) / rows_per_warp * planes;
+int64_t row_grid(CopyArgs &a) {
+  const int64_t groups = (a.n_tokens + a.rows_per_warp - 1) / a.rows_per_warp;
   const int64_t wpb = kCopyThreads / 32;
-  return (warps + wpb - 1) / wpb;
+  a.row_blocks = (uint32_t)((groups + wpb - 1) / wpb);
+  return (int64_t)a.row_blocks * a.planes;
 }
 
 template <bool kSpec, bool kTail>
