@@ -193,7 +193,30 @@ struct Call {
   // Widest access every row, head vector and plane of the call allows.  Below 16 bytes the
   // call takes the narrow row kernel with one row per plan chunk.
   int32_t vec = 16;
+  // The call's options (its flags word, or the process-wide settings for KVX_DEFAULTS).
+  bool check_dup = false;
+  int32_t engine = KVX_ENGINE_AUTO;
+  int32_t fused_max = 0;
 };
+
+// Resolves a call's flags word into c's options.  KVX_ERR_INVALID_ARG for unknown bits or both
+// engines at once.
+kvx_status apply_flags(Call &c, uint32_t flags) {
+  if (flags == KVX_DEFAULTS) {
+    c.check_dup = g_check_dup.load(std::memory_order_relaxed) != 0;
+    c.engine = kvx_get_copy_engine();
+    c.fused_max = g_fused_max.load(std::memory_order_relaxed);
+    return KVX_OK;
+  }
+  const uint32_t known = KVX_CHECK_DUP | KVX_USE_REGISTERS | KVX_USE_BULK | KVX_ONE_LAUNCH;
+  if ((flags & ~known) != 0 || ((flags & KVX_USE_REGISTERS) && (flags & KVX_USE_BULK)))
+    return KVX_ERR_INVALID_ARG;
+  c.check_dup = (flags & KVX_CHECK_DUP) != 0;
+  c.engine = (flags & KVX_USE_BULK) ? KVX_ENGINE_BULK
+             : (flags & KVX_USE_REGISTERS) ? KVX_ENGINE_REGISTERS : KVX_ENGINE_AUTO;
+  c.fused_max = (flags & KVX_ONE_LAUNCH) ? KVX_FUSED_MAX_TOKENS : 0;
+  return KVX_OK;
+}
 
 // The access width a pool side allows: its own, and its head vectors' (the per-head
 // placement of the fast kernels moves 16-byte pieces of head vectors).
@@ -215,12 +238,9 @@ int32_t call_chunk_rows(const Call &c) {
   return c.vec < 16 ? 1 : chunk_rows_for(c.row_bytes);
 }
 
-// Whether the planner checks this call's destination slots for repeats: slot-list calls into
-// a pool, with kvx_set_check_duplicates on.
-bool dup_check(const Call &c) {
-  return g_check_dup.load(std::memory_order_relaxed) != 0 && c.mode == kvx::kModeSlots &&
-         c.dst != nullptr && c.n_tokens > 0;
-}
+// Whether the planner checks this call's destination slots for repeats: calls that write
+// into a pool, with KVX_CHECK_DUP.
+bool dup_check(const Call &c) { return c.check_dup && c.dst != nullptr && c.n_tokens > 0; }
 
 // The workspace a slot-list call needs (the duplicate table included when it is checked).
 kvx::WsLayout slots_ws(const Call &c) { return kvx::ws_layout(c.n_tokens, 0, false, dup_check(c)); }
@@ -319,7 +339,8 @@ kvx::PlanArgs plan_args(const Call &c, void *d_ws, int32_t *d_status) {
   a.L = kvx::ws_layout(c.n_tokens, c.n_segs, false, dup_check(c));
   a.status = d_status;
   if (dup_check(c)) {
-    a.dup_table = reinterpret_cast<uint32_t *>(static_cast<char *>(d_ws) + a.L.dup_off);
+    a.dup_table =
+        reinterpret_cast<unsigned long long *>(static_cast<char *>(d_ws) + a.L.dup_off);
     a.dup_mask = (uint32_t)(a.L.dup_slots - 1);
     int32_t bits = 0;
     while (((int64_t)1 << bits) < a.L.dup_slots) ++bits;
@@ -335,7 +356,7 @@ kvx_status enqueue_plan(const Call &c, kvx::PlanArgs &a, cudaStream_t s) {
     return e == cudaSuccess ? KVX_OK : cuda_fail(e);
   }
   if (a.dup_table) {  // an empty duplicate table
-    e = cudaMemsetAsync(a.dup_table, 0, sizeof(uint32_t) * ((size_t)a.dup_mask + 1), s);
+    e = cudaMemsetAsync(a.dup_table, 0, sizeof(unsigned long long) * ((size_t)a.dup_mask + 1), s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (c.mode == kvx::kModeSlots) {
@@ -535,14 +556,15 @@ size_t kvx_workspace_size(int64_t max_tokens, int32_t max_requests) {
 
 kvx_status kvx_plan(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, kvx_layout_t dst,
                     const int32_t *d_dst_slots, int32_t n, void *d_ws, size_t ws_bytes,
-                    int32_t *d_status, kvx_stream_t stream) {
+                    int32_t *d_status, uint32_t flags, kvx_stream_t stream) {
   if (op < KVX_OP_GATHER || op > KVX_OP_TRANSFER || !valid_n(n)) return KVX_ERR_INVALID_ARG;
   if (!d_status || !aligned(d_status, 4)) return KVX_ERR_INVALID_ARG;
   Call c;
   c.mode = kvx::kModeSlots;
   c.op = op;
   c.n_tokens = n;
-  kvx_status st = bind_layouts(c, src, dst);
+  kvx_status st = apply_flags(c, flags);
+  if (st == KVX_OK) st = bind_layouts(c, src, dst);
   if (st != KVX_OK) return st;
   if (n > 0) {
     if (c.src && (!d_src_slots || !aligned(d_src_slots, 4))) return KVX_ERR_INVALID_ARG;
@@ -558,7 +580,7 @@ kvx_status kvx_plan(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, kv
 
 kvx_status kvx_plan_runs(int32_t op, kvx_layout_t src, kvx_layout_t dst, const int32_t *d_runs,
                          int32_t n_runs, int32_t n_tokens, void *d_ws, size_t ws_bytes,
-                         int32_t *d_status, kvx_stream_t stream) {
+                         int32_t *d_status, uint32_t flags, kvx_stream_t stream) {
   if (op < KVX_OP_GATHER || op > KVX_OP_TRANSFER || !valid_n(n_tokens) || n_runs < 0 ||
       n_runs > kvx::kMaxSegs)
     return KVX_ERR_INVALID_ARG;
@@ -569,10 +591,11 @@ kvx_status kvx_plan_runs(int32_t op, kvx_layout_t src, kvx_layout_t dst, const i
   c.op = op;
   c.n_tokens = n_tokens;
   c.n_segs = n_runs;
-  kvx_status st = bind_layouts(c, src, dst);
+  kvx_status st = apply_flags(c, flags);
+  if (st == KVX_OK) st = bind_layouts(c, src, dst);
   if (st != KVX_OK) return st;
   if (n_runs == 0 && n_tokens > 0) return KVX_ERR_INVALID_ARG;
-  const kvx::WsLayout L = kvx::ws_layout(n_tokens, n_runs, false);
+  const kvx::WsLayout L = kvx::ws_layout(n_tokens, n_runs, false, dup_check(c));
   if ((n_tokens > 0 || n_runs > 0) && (st = check_ws(d_ws, ws_bytes, L)) != KVX_OK) return st;
   kvx::PlanArgs a = plan_args(c, d_ws, d_status);
   a.runs = d_runs;
@@ -589,7 +612,7 @@ kvx_status kvx_plan_batch(kvx_layout_t src, kvx_layout_t dst, const kvx_request 
                           int32_t n_reqs, int64_t total_tokens, const int32_t *d_src_slots,
                           int64_t n_src_slots, const int32_t *d_dst_slots, int64_t n_dst_slots,
                           size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *d_status,
-                          kvx_stream_t stream) {
+                          uint32_t flags, kvx_stream_t stream) {
   if (!valid_n(total_tokens) || n_reqs < 0 || n_reqs > kvx::kMaxSegs || n_src_slots < 0 ||
       n_dst_slots < 0)
     return KVX_ERR_INVALID_ARG;
@@ -603,9 +626,10 @@ kvx_status kvx_plan_batch(kvx_layout_t src, kvx_layout_t dst, const kvx_request 
   c.n_tokens = total_tokens;
   c.n_segs = n_reqs;
   c.n_status = n_reqs + 1;
-  kvx_status st = bind_layouts(c, src, dst);
+  kvx_status st = apply_flags(c, flags);
+  if (st == KVX_OK) st = bind_layouts(c, src, dst);
   if (st != KVX_OK) return st;
-  const kvx::WsLayout L = kvx::ws_layout(total_tokens, n_reqs, false);
+  const kvx::WsLayout L = kvx::ws_layout(total_tokens, n_reqs, false, dup_check(c));
   if (n_reqs > 0 && (st = check_ws(d_ws, ws_bytes, L)) != KVX_OK) return st;
   kvx::PlanArgs a = plan_args(c, d_ws, d_status);
   a.src_idx = d_src_slots;
@@ -620,7 +644,12 @@ kvx_status kvx_plan_batch(kvx_layout_t src, kvx_layout_t dst, const kvx_request 
     cudaError_t e = cudaMemsetAsync(d_status, 0, sizeof(int32_t), s);
     return e == cudaSuccess ? KVX_OK : cuda_fail(e);
   }
-  cudaError_t e = kvx::launch_prefix(a, s);
+  cudaError_t e;
+  if (a.dup_table) {  // an empty duplicate table
+    e = cudaMemsetAsync(a.dup_table, 0, sizeof(unsigned long long) * ((size_t)a.dup_mask + 1), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  e = kvx::launch_prefix(a, s);
   if (e != cudaSuccess) return cuda_fail(e);
   if (total_tokens == 0) return KVX_OK;
   e = kvx::launch_plan(a, s);
@@ -629,7 +658,7 @@ kvx_status kvx_plan_batch(kvx_layout_t src, kvx_layout_t dst, const kvx_request 
 
 kvx_status kvx_execute(int32_t op, kvx_layout_t src, kvx_layout_t dst, const kvx_request *d_reqs,
                        int32_t n_reqs, int64_t n_tokens, void *d_buf, size_t buf_bytes,
-                       const void *d_ws, size_t ws_bytes, int32_t *d_status,
+                       const void *d_ws, size_t ws_bytes, int32_t *d_status, uint32_t flags,
                        kvx_stream_t stream) {
   if (op < KVX_OP_GATHER || op > KVX_OP_BATCH || !valid_n(n_tokens)) return KVX_ERR_INVALID_ARG;
   if (!d_status || !aligned(d_status, 4)) return KVX_ERR_INVALID_ARG;
@@ -641,14 +670,15 @@ kvx_status kvx_execute(int32_t op, kvx_layout_t src, kvx_layout_t dst, const kvx
     if (n_reqs < 0 || n_reqs > kvx::kMaxSegs || (n_reqs > 0 && !d_reqs)) return KVX_ERR_INVALID_ARG;
     c.n_segs = n_reqs;
   }
-  kvx_status st = bind_layouts(c, src, dst);
+  kvx_status st = apply_flags(c, flags);
+  if (st == KVX_OK) st = bind_layouts(c, src, dst);
   if (st != KVX_OK) return st;
   if ((st = check_buffer(c, d_buf, buf_bytes)) != KVX_OK) return st;
   if (n_tokens == 0) return KVX_OK;
   if ((st = check_ws(d_ws, ws_bytes, kvx::ws_layout(n_tokens, c.n_segs, false))) != KVX_OK)
     return st;
   return enqueue_copy(c, d_reqs, d_buf, d_ws, d_status, reinterpret_cast<cudaStream_t>(stream),
-                      kvx_get_copy_engine());
+                      c.engine);
 }
 
 // gather / scatter / transfer of one slot-list request: one launch up to the fused limit,
@@ -670,11 +700,10 @@ static kvx_status run_call(const Call &c, const int32_t *d_src_slots, const int3
   kvx_status st;
   if (n > 0 && (st = check_ws(d_ws, ws_bytes, L)) != KVX_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int32_t engine = kvx_get_copy_engine();
+  const int32_t engine = c.engine;
   // Requests of up to the fused limit with rows under KVX_CHUNK_BYTES take the one-launch
   // path; the rest take the planner + row kernel (the row kernel overlaps the planner).
-  const bool fused = call_chunk_rows(c) > 1 && !dup_check(c) &&
-                     n <= g_fused_max.load(std::memory_order_relaxed);
+  const bool fused = call_chunk_rows(c) > 1 && !dup_check(c) && n <= c.fused_max;
   // small requests: one launch whose every CTA checks every index (no planner), unless the
   // duplicate check or the bulk engine was asked for
   const bool small = n > 0 && n <= kvx::kSmallMaxTokens && !fused && !dup_check(c) &&
@@ -710,14 +739,15 @@ static kvx_status run_call(const Call &c, const int32_t *d_src_slots, const int3
 static kvx_status run_slots(int32_t op, kvx_layout_t src, const int32_t *d_src_slots,
                             kvx_layout_t dst, const int32_t *d_dst_slots, int32_t n, void *d_buf,
                             size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *d_status,
-                            kvx_stream_t stream, int32_t *host_status = nullptr,
+                            uint32_t flags, kvx_stream_t stream, int32_t *host_status = nullptr,
                             bool *host_status_written = nullptr) {
   if (host_status_written) *host_status_written = false;
   if (!valid_n(n)) return KVX_ERR_INVALID_ARG;
   Call c;
   c.op = op;
   c.n_tokens = n;
-  kvx_status st = bind_layouts(c, src, dst);
+  kvx_status st = apply_flags(c, flags);
+  if (st == KVX_OK) st = bind_layouts(c, src, dst);
   if (st == KVX_OK) st = check_buffer(c, d_buf, buf_bytes);
   if (st != KVX_OK) return st;
   return run_call(c, d_src_slots, d_dst_slots, d_buf, d_ws, ws_bytes, d_status, stream,
@@ -726,28 +756,29 @@ static kvx_status run_slots(int32_t op, kvx_layout_t src, const int32_t *d_src_s
 
 kvx_status kvx_gather(kvx_layout_t src, const int32_t *d_src_slots, int32_t n, void *d_buf,
                       size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *d_status,
-                      kvx_stream_t stream) {
+                      uint32_t flags, kvx_stream_t stream) {
   return run_slots(KVX_OP_GATHER, src, d_src_slots, nullptr, nullptr, n, d_buf, buf_bytes, d_ws,
-                   ws_bytes, d_status, stream);
+                   ws_bytes, d_status, flags, stream);
 }
 
 kvx_status kvx_scatter(kvx_layout_t dst, const int32_t *d_dst_slots, int32_t n,
                        const void *d_buf, size_t buf_bytes, void *d_ws, size_t ws_bytes,
-                       int32_t *d_status, kvx_stream_t stream) {
+                       int32_t *d_status, uint32_t flags, kvx_stream_t stream) {
   return run_slots(KVX_OP_SCATTER, nullptr, nullptr, dst, d_dst_slots, n,
-                   const_cast<void *>(d_buf), buf_bytes, d_ws, ws_bytes, d_status, stream);
+                   const_cast<void *>(d_buf), buf_bytes, d_ws, ws_bytes, d_status, flags, stream);
 }
 
 kvx_status kvx_transfer(kvx_layout_t src, const int32_t *d_src_slots, kvx_layout_t dst,
                         const int32_t *d_dst_slots, int32_t n, void *d_ws, size_t ws_bytes,
-                        int32_t *d_status, kvx_stream_t stream) {
+                        int32_t *d_status, uint32_t flags, kvx_stream_t stream) {
   return run_slots(KVX_OP_TRANSFER, src, d_src_slots, dst, d_dst_slots, n, nullptr, 0, d_ws,
-                   ws_bytes, d_status, stream);
+                   ws_bytes, d_status, flags, stream);
 }
 
 kvx_status kvx_gather_runs(kvx_layout_t src, const int32_t *d_runs, int32_t n_runs,
                            int32_t n_tokens, void *d_buf, size_t buf_bytes, void *d_ws,
-                           size_t ws_bytes, int32_t *d_status, kvx_stream_t stream) {
+                           size_t ws_bytes, int32_t *d_status, uint32_t flags,
+                           kvx_stream_t stream) {
   Call c;
   c.op = KVX_OP_GATHER;
   c.n_tokens = n_tokens;
@@ -755,15 +786,16 @@ kvx_status kvx_gather_runs(kvx_layout_t src, const int32_t *d_runs, int32_t n_ru
   if (st == KVX_OK && valid_n(n_tokens)) st = check_buffer(c, d_buf, buf_bytes);
   if (st != KVX_OK) return st;
   st = kvx_plan_runs(KVX_OP_GATHER, src, nullptr, d_runs, n_runs, n_tokens, d_ws, ws_bytes,
-                     d_status, stream);
+                     d_status, flags, stream);
   if (st != KVX_OK) return st;
   return kvx_execute(KVX_OP_GATHER, src, nullptr, nullptr, 0, n_tokens, d_buf, buf_bytes, d_ws,
-                     ws_bytes, d_status, stream);
+                     ws_bytes, d_status, flags, stream);
 }
 
 kvx_status kvx_scatter_runs(kvx_layout_t dst, const int32_t *d_runs, int32_t n_runs,
                             int32_t n_tokens, const void *d_buf, size_t buf_bytes, void *d_ws,
-                            size_t ws_bytes, int32_t *d_status, kvx_stream_t stream) {
+                            size_t ws_bytes, int32_t *d_status, uint32_t flags,
+                            kvx_stream_t stream) {
   Call c;
   c.op = KVX_OP_SCATTER;
   c.n_tokens = n_tokens;
@@ -771,38 +803,41 @@ kvx_status kvx_scatter_runs(kvx_layout_t dst, const int32_t *d_runs, int32_t n_r
   if (st == KVX_OK && valid_n(n_tokens)) st = check_buffer(c, d_buf, buf_bytes);
   if (st != KVX_OK) return st;
   st = kvx_plan_runs(KVX_OP_SCATTER, nullptr, dst, d_runs, n_runs, n_tokens, d_ws, ws_bytes,
-                     d_status, stream);
+                     d_status, flags, stream);
   if (st != KVX_OK) return st;
   return kvx_execute(KVX_OP_SCATTER, nullptr, dst, nullptr, 0, n_tokens,
-                     const_cast<void *>(d_buf), buf_bytes, d_ws, ws_bytes, d_status, stream);
+                     const_cast<void *>(d_buf), buf_bytes, d_ws, ws_bytes, d_status, flags,
+                     stream);
 }
 
 kvx_status kvx_transfer_runs(kvx_layout_t src, kvx_layout_t dst, const int32_t *d_runs,
                              int32_t n_runs, int32_t n_tokens, void *d_ws, size_t ws_bytes,
-                             int32_t *d_status, kvx_stream_t stream) {
+                             int32_t *d_status, uint32_t flags, kvx_stream_t stream) {
   kvx_status st = kvx_plan_runs(KVX_OP_TRANSFER, src, dst, d_runs, n_runs, n_tokens, d_ws,
-                                ws_bytes, d_status, stream);
+                                ws_bytes, d_status, flags, stream);
   if (st != KVX_OK) return st;
   return kvx_execute(KVX_OP_TRANSFER, src, dst, nullptr, 0, n_tokens, nullptr, 0, d_ws, ws_bytes,
-                     d_status, stream);
+                     d_status, flags, stream);
 }
 
 kvx_status kvx_batch(kvx_layout_t src, kvx_layout_t dst, const kvx_request *d_reqs,
                      int32_t n_reqs, int64_t total_tokens, const int32_t *d_src_slots,
                      int64_t n_src_slots, const int32_t *d_dst_slots, int64_t n_dst_slots,
                      void *d_buf, size_t buf_bytes, void *d_ws, size_t ws_bytes,
-                     int32_t *d_status, kvx_stream_t stream) {
+                     int32_t *d_status, uint32_t flags, kvx_stream_t stream) {
   Call c;
   c.op = KVX_OP_BATCH;
   c.mode = kvx::kModeBatch;
-  kvx_status st = bind_layouts(c, src, dst);
+  kvx_status st = apply_flags(c, flags);
+  if (st == KVX_OK) st = bind_layouts(c, src, dst);
   if (st == KVX_OK) st = check_buffer(c, d_buf, buf_bytes);
   if (st != KVX_OK) return st;
   st = kvx_plan_batch(src, dst, d_reqs, n_reqs, total_tokens, d_src_slots, n_src_slots,
-                      d_dst_slots, n_dst_slots, buf_bytes, d_ws, ws_bytes, d_status, stream);
+                      d_dst_slots, n_dst_slots, buf_bytes, d_ws, ws_bytes, d_status, flags,
+                      stream);
   if (st != KVX_OK) return st;
   return kvx_execute(KVX_OP_BATCH, src, dst, d_reqs, n_reqs, total_tokens, d_buf, buf_bytes,
-                     d_ws, ws_bytes, d_status, stream);
+                     d_ws, ws_bytes, d_status, flags, stream);
 }
 
 // Device address of a pinned (page-locked) host buffer, or nullptr for pageable memory.
@@ -819,13 +854,14 @@ static const void *pinned_alias(const void *h) {
 kvx_status kvx_submit(int32_t op, kvx_layout_t src, const int32_t *h_src_slots,
                       kvx_layout_t dst, const int32_t *h_dst_slots, int32_t n, void *d_buf,
                       size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *h_status,
-                      kvx_stream_t stream) {
+                      uint32_t flags, kvx_stream_t stream) {
   if (op < KVX_OP_GATHER || op > KVX_OP_TRANSFER || !valid_n(n) || !h_status)
     return KVX_ERR_INVALID_ARG;
   Call c;
   c.op = op;
   c.n_tokens = n;
-  kvx_status st = bind_layouts(c, src, dst);
+  kvx_status st = apply_flags(c, flags);
+  if (st == KVX_OK) st = bind_layouts(c, src, dst);
   if (st != KVX_OK) return st;
   if ((st = check_buffer(c, d_buf, buf_bytes)) != KVX_OK) return st;
   if (n > 0 && ((c.src && !h_src_slots) || (c.dst && !h_dst_slots))) return KVX_ERR_INVALID_ARG;
@@ -856,7 +892,7 @@ kvx_status kvx_submit(int32_t op, kvx_layout_t src, const int32_t *h_src_slots,
   }
   bool written = false;
   st = run_slots(op, src, c.src ? use_src : nullptr, dst, c.dst ? use_dst : nullptr, n, d_buf,
-                 buf_bytes, d_ws, ws_bytes, d_st, stream, z_status, &written);
+                 buf_bytes, d_ws, ws_bytes, d_st, flags, stream, z_status, &written);
   if (st != KVX_OK || written) return st;
   e = cudaMemcpyAsync(h_status, d_st, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
   return e == cudaSuccess ? KVX_OK : cuda_fail(e);
@@ -945,13 +981,14 @@ static kvx_status stream_ctl_of(const kvx_stream_ctl *ctl, int32_t op, const kvx
 kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, kvx_layout_t dst,
                       const int32_t *d_dst_slots, int32_t n, void *d_buf, size_t buf_bytes,
                       const kvx_stream_ctl *ctl, void *d_ws, size_t ws_bytes, int32_t *d_status,
-                      kvx_stream_t stream) {
+                      uint32_t flags, kvx_stream_t stream) {
   if (op < KVX_OP_GATHER || op > KVX_OP_TRANSFER || !valid_n(n)) return KVX_ERR_INVALID_ARG;
   if (!d_status || !aligned(d_status, 16)) return KVX_ERR_INVALID_ARG;
   Call c;
   c.op = op;
   c.n_tokens = n;
-  kvx_status st = bind_layouts(c, src, dst);
+  kvx_status st = apply_flags(c, flags);
+  if (st == KVX_OK) st = bind_layouts(c, src, dst);
   if (st == KVX_OK) st = check_buffer(c, d_buf, buf_bytes);
   if (st != KVX_OK) return st;
   if (c.vec < 16) return KVX_ERR_ALIGNMENT;  // the streamed kernels move 16-byte vectors
@@ -981,7 +1018,7 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
     pa.validate_only = 1;  // the streamed copy reads the slot lists itself
     if (direct) pa.status_direct = 4;
     if (pa.dup_table) {
-      e = cudaMemsetAsync(pa.dup_table, 0, sizeof(uint32_t) * ((size_t)pa.dup_mask + 1), s);
+      e = cudaMemsetAsync(pa.dup_table, 0, sizeof(unsigned long long) * ((size_t)pa.dup_mask + 1), s);
       if (e != cudaSuccess) return cuda_fail(e);
     }
     e = kvx::launch_plan(pa, s);
@@ -998,7 +1035,7 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
     return e == cudaSuccess ? KVX_OK : cuda_fail(e);
   }
   // persistent grid of at most max_ctas CTAs (at least one: it also runs the exit protocol)
-  if (kvx_get_copy_engine() == KVX_ENGINE_BULK) {
+  if (c.engine == KVX_ENGINE_BULK) {
     // bulk form: one thread per one-token item, a 2 KiB shared-memory stage each
     kvx::stream_sizes(k, n, 1);
     const int64_t per_cta = kvx::stream_bulk_threads();
@@ -1014,7 +1051,7 @@ kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, 
   }
   // register CTAs of 32 warps; with the default engine, three of the warps move their rows by
   // TMA bulk copies where a row group fits one stage
-  const bool tma = kvx_get_copy_engine() == KVX_ENGINE_AUTO && kvx::stream_tma_fits(a);
+  const bool tma = c.engine == KVX_ENGINE_AUTO && kvx::stream_tma_fits(a);
   const int64_t warps = k.items;
   int64_t grid = (int64_t)di.sms * di.bps_stream;
   if (ctl->max_ctas < grid) grid = ctl->max_ctas;
@@ -1073,12 +1110,13 @@ kvx_status kvx_move_heads(int32_t op, kvx_layout_t src, const int32_t *d_src_slo
                           int32_t src_head0, kvx_layout_t dst, const int32_t *d_dst_slots,
                           int32_t dst_head0, int32_t n_heads, int32_t n, void *d_buf,
                           size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *d_status,
-                          kvx_stream_t stream) {
+                          uint32_t flags, kvx_stream_t stream) {
   if (op < KVX_OP_GATHER || op > KVX_OP_TRANSFER || !valid_n(n) || n_heads < 1)
     return KVX_ERR_INVALID_ARG;
   const bool uses_src = op != KVX_OP_SCATTER, uses_dst = op != KVX_OP_GATHER;
   if ((uses_src && !src) || (uses_dst && !dst)) return KVX_ERR_INVALID_ARG;
   Call c;
+  if (apply_flags(c, flags) != KVX_OK) return KVX_ERR_INVALID_ARG;
   c.op = op;
   c.n_tokens = n;
   c.src = uses_src ? src : nullptr;
@@ -1239,9 +1277,10 @@ static kvx_status prepare_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
 kvx_status kvx_reshard(const kvx_layout_t *srcs, int32_t n_srcs, const int32_t *d_src_slots,
                        const kvx_layout_t *dsts, int32_t n_dsts, const int32_t *d_dst_slots,
                        const kvx_head_part *parts, int32_t n_parts, int32_t n, void *d_ws,
-                       size_t ws_bytes, int32_t *d_status, kvx_stream_t stream) {
+                       size_t ws_bytes, int32_t *d_status, uint32_t flags, kvx_stream_t stream) {
   if (!d_status || !aligned(d_status, 4)) return KVX_ERR_INVALID_ARG;
   Call c;
+  if (apply_flags(c, flags) != KVX_OK) return KVX_ERR_INVALID_ARG;
   static thread_local kvx::ReshardCall rc;  // ~30 KB: keep it off the stack
   kvx_status st = prepare_reshard(srcs, n_srcs, d_src_slots, dsts, n_dsts, d_dst_slots, parts,
                                   n_parts, n, d_ws, ws_bytes, c, rc);
@@ -1264,7 +1303,7 @@ kvx_status kvx_reshard(const kvx_layout_t *srcs, int32_t n_srcs, const int32_t *
   pa.validate_only = 1;
   if (direct) pa.status_direct = 1;
   if (pa.dup_table) {
-    e = cudaMemsetAsync(pa.dup_table, 0, sizeof(uint32_t) * ((size_t)pa.dup_mask + 1), s);
+    e = cudaMemsetAsync(pa.dup_table, 0, sizeof(unsigned long long) * ((size_t)pa.dup_mask + 1), s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   e = kvx::launch_plan(pa, s);
@@ -1279,9 +1318,10 @@ kvx_status kvx_stream_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
                               int32_t n_dsts, const int32_t *d_dst_slots,
                               const kvx_head_part *parts, int32_t n_parts, int32_t n,
                               const kvx_stream_ctl *ctl, void *d_ws, size_t ws_bytes,
-                              int32_t *d_status, kvx_stream_t stream) {
+                              int32_t *d_status, uint32_t flags, kvx_stream_t stream) {
   if (!d_status || !aligned(d_status, 16)) return KVX_ERR_INVALID_ARG;
   Call c;
+  if (apply_flags(c, flags) != KVX_OK) return KVX_ERR_INVALID_ARG;
   static thread_local kvx::ReshardCall rc;  // ~30 KB: keep it off the stack
   kvx_status st = prepare_reshard(srcs, n_srcs, d_src_slots, dsts, n_dsts, d_dst_slots, parts,
                                   n_parts, n, d_ws, ws_bytes, c, rc);
@@ -1305,7 +1345,7 @@ kvx_status kvx_stream_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
     pa.validate_only = 1;
     if (direct) pa.status_direct = 4;
     if (pa.dup_table) {
-      e = cudaMemsetAsync(pa.dup_table, 0, sizeof(uint32_t) * ((size_t)pa.dup_mask + 1), s);
+      e = cudaMemsetAsync(pa.dup_table, 0, sizeof(unsigned long long) * ((size_t)pa.dup_mask + 1), s);
       if (e != cudaSuccess) return cuda_fail(e);
     }
     e = kvx::launch_plan(pa, s);

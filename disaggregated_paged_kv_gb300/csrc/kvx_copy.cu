@@ -40,7 +40,7 @@ __device__ __forceinline__ int32_t copy_prologue(const CopyArgs &a, int32_t *s_t
   if (tid == 0) {
     int32_t ok = header_matches(a) ? 1 : 0;
     if (!ok && blockIdx.x == 0) atomicMax(&a.status[0], (int32_t)KVX_ERR_INVALID_ARG);
-    if (ok && a.mode != kModeBatch && a.status[0] != KVX_OK) ok = 0;
+    if (ok && a.mode != kModeBatch && load_status(a.status) != KVX_OK) ok = 0;
     *s_ok = ok;
   }
   __syncthreads();
@@ -93,7 +93,7 @@ __device__ __forceinline__ bool decode_item(const CopyArgs &a, uint32_t w,
   int64_t nreq = a.n_tokens;
   bool src_pool = a.src.is_pool, dst_pool = a.dst.is_pool;
   if (a.mode == kModeBatch) {
-    if (a.status[1 + ch.req] != KVX_OK) return false;
+    if (load_status(a.status + 1 + ch.req) != KVX_OK) return false;
     const kvx_request rq = a.reqs[ch.req];
     op = rq.op;
     bufp = a.buf + rq.buf_off;
@@ -257,13 +257,13 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
     }
     const Chunk ch = reinterpret_cast<const Chunk *>(a.ws + a.L.chunks_off)[t0];  // G == 1
     if (a.mode == kModeBatch) {
-      if (a.status[1 + ch.req] != KVX_OK) return;
+      if (load_status(a.status + 1 + ch.req) != KVX_OK) return;
       const kvx_request rq = a.reqs[ch.req];
       sp = (rq.op == KVX_OP_GATHER || rq.op == KVX_OP_TRANSFER);
       dp = (rq.op == KVX_OP_SCATTER || rq.op == KVX_OP_TRANSFER);
       bufp = a.buf + rq.buf_off;
       nreq = rq.n_tokens;
-    } else if (a.status[0] != KVX_OK) {
+    } else if (load_status(a.status) != KVX_OK) {
       return;
     }
     si = ch.src;
@@ -489,6 +489,23 @@ int variant_blocks_per_sm(CopyVariant v, int32_t n_tiles) {
                                                     variant_smem(v, n_tiles)) != cudaSuccess)
     return 0;
   return nb;
+}
+
+int copy_kernel_list(const void **out, int max) {
+  const void *k[20];
+  int n = 0;
+  for (int sh = 0; sh < 2; ++sh)
+    for (int dh = 0; dh < 2; ++dh) {
+      k[n++] = row_fn_of<true, false>(sh, dh);
+      k[n++] = row_fn_of<true, true>(sh, dh);
+      k[n++] = row_fn_of<false, false>(sh, dh);
+      k[n++] = row_fn_of<false, true>(sh, dh);
+    }
+  k[n++] = variant_fn(kVariantLean);
+  k[n++] = variant_fn(kVariantLinear);
+  k[n++] = variant_fn(kVariantGeneral);
+  k[n++] = variant_fn(kVariantBulk);
+  return kernel_list_out(k, n, out, max);
 }
 
 cudaError_t launch_copy(const CopyArgs &a, CopyVariant v, int grid, cudaStream_t s) {

@@ -230,6 +230,12 @@ int fused_blocks_per_sm(bool linear) {
   return e == cudaSuccess ? nb : 0;
 }
 
+int fused_kernel_list(const void **out, int max) {
+  const void *k[] = {reinterpret_cast<const void *>(fused_kernel<true>),
+                     reinterpret_cast<const void *>(fused_kernel<false>)};
+  return kernel_list_out(k, 2, out, max);
+}
+
 cudaError_t launch_fused(const CopyArgs &c, const int32_t *src_idx, const int32_t *dst_idx,
                          int32_t n, int32_t chunk_rows, int sms, int bps, cudaStream_t s) {
   static thread_local FusedArgs f;  // ~4 KiB of plane pointers: keep it off the stack

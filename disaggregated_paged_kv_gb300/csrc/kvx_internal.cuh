@@ -57,6 +57,12 @@ struct __align__(16) Chunk {
   int32_t rows;
 };
 
+// A status word that another kernel of the same call writes (the prefix kernel, the planner,
+// the duplicate check), read from L2.  A CTA that programmatic dependent launch started early
+// shares its SM's L1 with CTAs of those kernels, whose plain loads of the word can leave a copy
+// there that their later atomics (made in L2) do not refresh.
+__device__ __forceinline__ int32_t load_status(const int32_t *p) { return __ldcg(p); }
+
 // Byte offsets of the workspace sections; a pure function of the call's sizes, so the host
 // and every kernel agree on it.
 struct WsLayout {
@@ -65,22 +71,22 @@ struct WsLayout {
   int64_t chunks_off;  // Chunk[n_tiles][kTile]
   int64_t prefix_off;  // int64[n_segs + 1]: token offset of each run / request
   int64_t stage_off;   // kvx_submit: int32 src[n], int32 dst[n], int32 status
-  int64_t dup_off;     // duplicate-destination check: uint32[dup_slots] hash table
+  int64_t dup_off;     // duplicate-destination check: uint64[dup_slots] hash table
   int64_t dup_slots;   // power of two >= 2n
   int64_t total;       // bytes required
 };
 
-__host__ __device__ inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ constexpr int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline int64_t num_tiles(int64_t n_tokens) {
+__host__ __device__ constexpr int64_t num_tiles(int64_t n_tokens) {
   return (n_tokens + kTile - 1) / kTile;
 }
 
 // staging: kvx_submit's copies of host slot lists; dup: the duplicate-destination table
 // (after the staging area whether or not that is used, so every call agrees on its place).
-__host__ __device__ inline WsLayout ws_layout(int64_t n_tokens, int64_t n_segs, bool staging,
-                                              bool dup = false) {
-  WsLayout L;
+__host__ __device__ constexpr WsLayout ws_layout(int64_t n_tokens, int64_t n_segs, bool staging,
+                                                 bool dup = false) {
+  WsLayout L{};
   int64_t tiles = num_tiles(n_tokens);
   L.header_off = 0;
   L.tiles_off = 256;
@@ -90,7 +96,7 @@ __host__ __device__ inline WsLayout ws_layout(int64_t n_tokens, int64_t n_segs, 
   L.dup_off = align_up(L.stage_off + 8 * n_tokens + 16, 256);
   L.dup_slots = 64;
   while (L.dup_slots < 2 * n_tokens) L.dup_slots <<= 1;
-  if (dup) L.total = L.dup_off + 4 * L.dup_slots;
+  if (dup) L.total = L.dup_off + 8 * L.dup_slots;
   else L.total = staging ? L.dup_off : L.stage_off;
   return L;
 }
@@ -133,9 +139,10 @@ struct PlanArgs {
                            // stores status[0] itself and zeroes status[1 .. status_direct - 1]
   int32_t validate_only;   // check the indices and write the status only (no chunk table:
                            // streamed calls, and one-shot calls whose copy reads the slot lists)
-  // Duplicate-destination check (slots mode, destination pool): open-addressing table of
-  // dup_mask + 1 words in the workspace, zeroed before the planner; entry = slot + 1.
-  uint32_t *dup_table;     // nullptr: no check
+  // Duplicate-destination check (destination pool; slots, runs and batch modes): open-
+  // addressing table of dup_mask + 1 words in the workspace, zeroed before the planner;
+  // entry = (slot + 1) << 32 | request, so a batch knows both requests of a repeated slot.
+  unsigned long long *dup_table;  // nullptr: no check
   uint32_t dup_mask;
   int32_t dup_bits;        // log2 of the table size
   Side src, dst;           // batch: pool geometry of the two layouts (is_pool = 1)
@@ -232,6 +239,19 @@ enum CopyVariant : int {
 // Launchers (enqueue only; return the launch's cudaError_t).
 cudaError_t launch_prefix(const PlanArgs &a, cudaStream_t s);
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s);
+// Every kernel of one translation unit that a gather / scatter / transfer may launch: writes
+// at most max function pointers into out and returns how many it wrote (for loading them all
+// ahead of time, kvx_transfer_noalloc).
+int plan_kernel_list(const void **out, int max);
+int copy_kernel_list(const void **out, int max);
+int small_kernel_list(const void **out, int max);
+int narrow_kernel_list(const void **out, int max);
+int fused_kernel_list(const void **out, int max);
+inline int kernel_list_out(const void *const *k, int n, const void **out, int max) {
+  int c = 0;
+  for (; c < n && c < max; ++c) out[c] = k[c];
+  return c;
+}
 // Validate-only calls of up to this many tokens are checked by a single CTA (validate_kernel),
 // which stores the status words itself (status_direct), so no status memset is needed first.
 // Measured on GB300: 0.8-1.2 us faster than memset + multi-tile planner at 4096 and 8192

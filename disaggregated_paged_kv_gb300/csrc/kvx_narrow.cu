@@ -104,13 +104,13 @@ __global__ void __launch_bounds__(kCopyThreads) copy_narrow_kernel(const __grid_
     const Chunk ch = reinterpret_cast<const Chunk *>(a.ws + a.L.chunks_off)[tt];  // one row each
     if (batch) {
       // tokens of one warp may belong to different requests: each lane follows its own
-      if (a.status[1 + ch.req] != KVX_OK) ok = false;
+      if (load_status(a.status + 1 + ch.req) != KVX_OK) ok = false;
       const kvx_request rq = a.reqs[ch.req];
       sp = (rq.op == KVX_OP_GATHER || rq.op == KVX_OP_TRANSFER);
       dp = (rq.op == KVX_OP_SCATTER || rq.op == KVX_OP_TRANSFER);
       bufp = a.buf + rq.buf_off;
       nreq = rq.n_tokens;
-    } else if (a.status[0] != KVX_OK) {
+    } else if (load_status(a.status) != KVX_OK) {
       return;
     }
     si = ch.src;
@@ -139,6 +139,14 @@ int32_t narrow_group_shift(int32_t row_bytes, int32_t vec_bytes) {
   int32_t g = 0;
   while ((32 >> g) > lanes) ++g;
   return g;
+}
+
+int narrow_kernel_list(const void **out, int max) {
+  const void *k[] = {reinterpret_cast<const void *>(copy_narrow_kernel<true, true>),
+                     reinterpret_cast<const void *>(copy_narrow_kernel<true, false>),
+                     reinterpret_cast<const void *>(copy_narrow_kernel<false, true>),
+                     reinterpret_cast<const void *>(copy_narrow_kernel<false, false>)};
+  return kernel_list_out(k, 4, out, max);
 }
 
 cudaError_t launch_narrow(const CopyArgs &a, cudaStream_t s) {

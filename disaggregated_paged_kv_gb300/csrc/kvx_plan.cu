@@ -117,7 +117,7 @@ __device__ __forceinline__ Tok fetch(const PlanArgs &a, int64_t g, int32_t &seg)
     } else {
       t.req = seg;
       t.start = (off == 0);
-      if (a.status[1 + seg] != KVX_OK) {  // bad record: never read its index arrays
+      if (load_status(a.status + 1 + seg) != KVX_OK) {  // bad record: never read its indices
         t.s = t.d = off;
         t.live = false;
         return t;
@@ -473,33 +473,67 @@ cudaError_t launch_pdl(const void *fn, dim3 grid, dim3 block, void **args, cudaS
 
 namespace {
 
-// Duplicate-destination check (kvx_set_check_duplicates), behind the planner: one thread per
-// destination slot inserts it into an open-addressing table in the workspace (entry = slot + 1,
-// home bucket from a multiplicative hash, linear probing bounded by the table size; entries
-// only ever go from empty to a slot, and the table holds at most n < size of them).  Spread
-// over many CTAs because one SM keeps only a limited number of atomics in flight.  The inserts
-// go out before griddepcontrol.wait; the verdict is raised only once the planner, which writes
-// the status word, has finished.
+// Duplicate-destination check (KVX_CHECK_DUP), behind the planner: one thread per token
+// inserts the token's destination slot into an open-addressing table in the workspace
+// (entry = (slot + 1) << 32 | request, home bucket from a multiplicative hash, linear probing
+// bounded by the table size; entries only ever go from empty to a slot, and the table holds at
+// most n < size of them).  Spread over many CTAs because one SM keeps only a limited number of
+// atomics in flight.  Slot lists: the inserts go out before griddepcontrol.wait and the verdict
+// is raised once the planner, which writes the status word, has finished.  Runs and batches:
+// a token's run or request comes from the prefix kernel's offsets, and a batch request whose
+// record or indices the planner refused writes nothing, so its slots are not inserted; both
+// wait for the planner first.  A repeated slot in a batch fails every request naming it (the
+// one found in the table and the inserting one), each in its own status word.
 constexpr int kDupThreads = 128;
 
 __global__ void __launch_bounds__(kDupThreads) dup_kernel(const __grid_constant__ PlanArgs a) {
   pdl_trigger();
-  const int64_t i = (int64_t)blockIdx.x * kDupThreads + threadIdx.x;
-  bool dup = false;
-  if (i < a.n_tokens) {
-    const int32_t slot = __ldg(a.dst_idx + i);
-    if (slot >= 0 && (int64_t)slot < a.dst.num_slots) {  // the planner reports the others
-      const uint32_t tag = (uint32_t)slot + 1u;
-      uint32_t h = ((uint32_t)slot * 2654435761u) >> (32 - a.dup_bits);
-      for (uint32_t probe = 0; probe <= a.dup_mask; ++probe, h = (h + 1) & a.dup_mask) {
-        const uint32_t cur = atomicCAS(a.dup_table + h, 0u, tag);
-        if (cur == 0) break;  // claimed
-        if (cur == tag) {
-          dup = true;
-          break;
+  if (a.mode != kModeSlots) pdl_wait();
+  const int64_t g = (int64_t)blockIdx.x * kDupThreads + threadIdx.x;
+  int64_t slot = -1;
+  uint32_t req = 0;
+  if (g < a.n_tokens) {
+    if (a.mode == kModeSlots) {
+      slot = __ldg(a.dst_idx + g);
+    } else {
+      const int64_t *pre = reinterpret_cast<const int64_t *>(a.ws + a.L.prefix_off);
+      if (g < pre[a.n_segs]) {
+        const int32_t seg = seg_of(pre, a.n_segs, g);
+        const int64_t off = g - pre[seg];
+        if (a.mode == kModeRuns) {
+          slot = (int64_t)a.runs[3 * (int64_t)seg + 1] + off;
+        } else if (load_status(a.status + 1 + seg) == KVX_OK) {
+          const kvx_request r = a.reqs[seg];
+          if (uses_dst_pool(r.op)) {
+            slot = a.dst_idx[r.dst_off + off];
+            req = (uint32_t)seg;
+          }
         }
       }
     }
+  }
+  bool dup = false;
+  uint32_t other = 0;
+  if (slot >= 0 && slot < a.dst.num_slots) {  // the planner reports the others
+    const unsigned long long key = (unsigned long long)(slot + 1) << 32;
+    uint32_t h = ((uint32_t)slot * 2654435761u) >> (32 - a.dup_bits);
+    for (uint32_t probe = 0; probe <= a.dup_mask; ++probe, h = (h + 1) & a.dup_mask) {
+      const unsigned long long cur = atomicCAS(a.dup_table + h, 0ull, key | req);
+      if (cur == 0) break;  // claimed
+      if ((cur & 0xFFFFFFFF00000000ull) == key) {
+        dup = true;
+        other = (uint32_t)cur;
+        break;
+      }
+    }
+  }
+  if (a.mode == kModeBatch) {
+    if (dup) {
+      atomicMax(&a.status[1 + req], (int32_t)KVX_ERR_DUPLICATE_DST);
+      atomicMax(&a.status[1 + other], (int32_t)KVX_ERR_DUPLICATE_DST);
+      atomicMax(&a.status[0], (int32_t)KVX_ERR_DUPLICATE_DST);
+    }
+    return;
   }
   dup = __syncthreads_or(dup);
   pdl_wait();  // the planner's status words are written
@@ -610,6 +644,14 @@ cudaError_t launch_plan(const PlanArgs &a, cudaStream_t s) {
   const int64_t grid = (a.n_tokens + kDupThreads - 1) / kDupThreads;
   return launch_pdl(reinterpret_cast<const void *>(dup_kernel), dim3((unsigned)grid),
                     dim3(kDupThreads), args, s);
+}
+
+int plan_kernel_list(const void **out, int max) {
+  const void *k[] = {reinterpret_cast<const void *>(plan_kernel),
+                     reinterpret_cast<const void *>(validate_kernel),
+                     reinterpret_cast<const void *>(dup_kernel),
+                     reinterpret_cast<const void *>(prefix_kernel)};
+  return kernel_list_out(k, 4, out, max);
 }
 
 cudaError_t launch_export(const char *ws, WsLayout L, int64_t n_tokens, int32_t *out,

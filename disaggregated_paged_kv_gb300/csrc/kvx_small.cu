@@ -102,6 +102,17 @@ const void *small_fn_of(bool sh, bool dh) {
 
 }  // namespace
 
+int small_kernel_list(const void **out, int max) {
+  const void *k[8];
+  int n = 0;
+  for (int sh = 0; sh < 2; ++sh)
+    for (int dh = 0; dh < 2; ++dh) {
+      k[n++] = small_fn_of<false>(sh, dh);
+      k[n++] = small_fn_of<true>(sh, dh);
+    }
+  return kernel_list_out(k, n, out, max);
+}
+
 cudaError_t launch_small(const CopyArgs &a, cudaStream_t s) {
   const bool sh = a.src.hnd && a.src.is_pool, dh = a.dst.hnd && a.dst.is_pool;
   const bool tail = (a.row_bytes >> 4) > kUnroll * a.row_lanes;  // more than one pass

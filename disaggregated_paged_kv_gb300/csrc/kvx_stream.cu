@@ -508,8 +508,8 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
 // the verdict and the "no further write" words are set.
 __global__ void stream_done_kernel(int32_t *status, int32_t *host_done, int32_t layers) {
   pdl_wait();
-  if (status[0] != KVX_OK) status[1] = layers;  // the planner refused the request: nothing moved
-  const int32_t code = status[2];
+  if (load_status(status) != KVX_OK) status[1] = layers;  // refused by the planner: nothing moved
+  const int32_t code = load_status(status + 2);
   if (code) atomicMax(&status[0], code);
   status[2] = 0;
   __threadfence_system();

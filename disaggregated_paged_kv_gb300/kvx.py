@@ -40,6 +40,7 @@ PLAN_TILE = 2048
 MAX_TOKENS = PLAN_TILE * 4096
 CHUNK_BYTES = 2048
 NOALLOC_MAX_TOKENS = 16384
+NOALLOC_MAX_DUP_TOKENS = 8192
 
 ELEM_BYTES = {F16: 2, BF16: 2, F32: 4, FP8: 1}
 
@@ -127,6 +128,7 @@ _VP = ctypes.c_void_p
 _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
 _SZ = ctypes.c_size_t
+_U32 = ctypes.c_uint32
 
 _SIGS = {
     "kvx_layout_create": (_I32, [ctypes.POINTER(LayoutDesc), ctypes.POINTER(_VP)]),
@@ -134,34 +136,34 @@ _SIGS = {
     "kvx_layout_row_bytes": (_I64, [_VP]),
     "kvx_layout_num_planes": (_I32, [_VP]),
     "kvx_workspace_size": (_SZ, [_I64, _I32]),
-    "kvx_gather": (_I32, [_VP, _VP, _I32, _VP, _SZ, _VP, _SZ, _VP, _VP]),
-    "kvx_scatter": (_I32, [_VP, _VP, _I32, _VP, _SZ, _VP, _SZ, _VP, _VP]),
-    "kvx_transfer": (_I32, [_VP, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _VP]),
-    "kvx_transfer_noalloc": (_I32, [_VP, _VP, _VP, _VP, _I32, _VP, _VP]),
-    "kvx_gather_runs": (_I32, [_VP, _VP, _I32, _I32, _VP, _SZ, _VP, _SZ, _VP, _VP]),
-    "kvx_scatter_runs": (_I32, [_VP, _VP, _I32, _I32, _VP, _SZ, _VP, _SZ, _VP, _VP]),
-    "kvx_transfer_runs": (_I32, [_VP, _VP, _VP, _I32, _I32, _VP, _SZ, _VP, _VP]),
+    "kvx_gather": (_I32, [_VP, _VP, _I32, _VP, _SZ, _VP, _SZ, _VP, _U32, _VP]),
+    "kvx_scatter": (_I32, [_VP, _VP, _I32, _VP, _SZ, _VP, _SZ, _VP, _U32, _VP]),
+    "kvx_transfer": (_I32, [_VP, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _U32, _VP]),
+    "kvx_transfer_noalloc": (_I32, [_VP, _VP, _VP, _VP, _I32, _VP, _U32, _VP]),
+    "kvx_gather_runs": (_I32, [_VP, _VP, _I32, _I32, _VP, _SZ, _VP, _SZ, _VP, _U32, _VP]),
+    "kvx_scatter_runs": (_I32, [_VP, _VP, _I32, _I32, _VP, _SZ, _VP, _SZ, _VP, _U32, _VP]),
+    "kvx_transfer_runs": (_I32, [_VP, _VP, _VP, _I32, _I32, _VP, _SZ, _VP, _U32, _VP]),
     "kvx_batch": (_I32, [_VP, _VP, _VP, _I32, _I64, _VP, _I64, _VP, _I64, _VP, _SZ, _VP, _SZ,
-                         _VP, _VP]),
-    "kvx_submit": (_I32, [_I32, _VP, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _SZ, _VP, _VP]),
+                         _VP, _U32, _VP]),
+    "kvx_submit": (_I32, [_I32, _VP, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _SZ, _VP, _U32, _VP]),
     "kvx_stream": (_I32, [_I32, _VP, _VP, _VP, _VP, _I32, _VP, _SZ, ctypes.POINTER(StreamCtl),
-                          _VP, _SZ, _VP, _VP]),
+                          _VP, _SZ, _VP, _U32, _VP]),
     "kvx_tp_slice": (_I32, [_I32, _I32, _I32, _I32, _I32, ctypes.POINTER(_I32),
                             ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "kvx_move_heads": (_I32, [_I32, _VP, _VP, _I32, _VP, _VP, _I32, _I32, _I32, _VP, _SZ, _VP,
-                              _SZ, _VP, _VP]),
+                              _SZ, _VP, _U32, _VP]),
     "kvx_tp_plan": (_I32, [_I32, _I32, _I32, ctypes.POINTER(HeadPart), _I32,
                            ctypes.POINTER(_I32)]),
     "kvx_reshard": (_I32, [ctypes.POINTER(_VP), _I32, _VP, ctypes.POINTER(_VP), _I32, _VP,
-                           ctypes.POINTER(HeadPart), _I32, _I32, _VP, _SZ, _VP, _VP]),
+                           ctypes.POINTER(HeadPart), _I32, _I32, _VP, _SZ, _VP, _U32, _VP]),
     "kvx_stream_reshard": (_I32, [ctypes.POINTER(_VP), _I32, _VP, ctypes.POINTER(_VP), _I32, _VP,
                                   ctypes.POINTER(HeadPart), _I32, _I32, ctypes.POINTER(StreamCtl),
-                                  _VP, _SZ, _VP, _VP]),
-    "kvx_plan": (_I32, [_I32, _VP, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _VP]),
-    "kvx_plan_runs": (_I32, [_I32, _VP, _VP, _VP, _I32, _I32, _VP, _SZ, _VP, _VP]),
+                                  _VP, _SZ, _VP, _U32, _VP]),
+    "kvx_plan": (_I32, [_I32, _VP, _VP, _VP, _VP, _I32, _VP, _SZ, _VP, _U32, _VP]),
+    "kvx_plan_runs": (_I32, [_I32, _VP, _VP, _VP, _I32, _I32, _VP, _SZ, _VP, _U32, _VP]),
     "kvx_plan_batch": (_I32, [_VP, _VP, _VP, _I32, _I64, _VP, _I64, _VP, _I64, _SZ, _VP, _SZ,
-                              _VP, _VP]),
-    "kvx_execute": (_I32, [_I32, _VP, _VP, _VP, _I32, _I64, _VP, _SZ, _VP, _SZ, _VP, _VP]),
+                              _VP, _U32, _VP]),
+    "kvx_execute": (_I32, [_I32, _VP, _VP, _VP, _I32, _I64, _VP, _SZ, _VP, _SZ, _VP, _U32, _VP]),
     "kvx_plan_export": (_I32, [_VP, _SZ, _I64, _VP, _I64, _VP, _VP]),
     "kvx_status_str": (ctypes.c_char_p, [_I32]),
     "kvx_last_cuda_error": (_I32, []),
@@ -221,6 +223,11 @@ def _stream(stream) -> Optional[int]:
     return int(stream.cuda_stream) or None
 
 
+def _flags(flags) -> int:
+    """A call's flags word: None means DEFAULTS (the process-wide settings)."""
+    return DEFAULTS if flags is None else int(flags)
+
+
 def _check(rc: int, where: str) -> None:
     if rc != OK:
         raise KvxError(rc, where)
@@ -239,6 +246,13 @@ def version() -> int:
 
 
 ENGINE_AUTO, ENGINE_REGISTERS, ENGINE_BULK = 0, 1, 2
+
+# per-call options (the flags argument of every call that moves rows)
+DEFAULTS = 0xFFFFFFFF
+CHECK_DUP = 0x1
+USE_REGISTERS = 0x2
+USE_BULK = 0x4
+ONE_LAUNCH = 0x8
 
 
 def set_copy_engine(engine: int) -> None:
@@ -324,85 +338,85 @@ def _h(layout: Optional[Layout]) -> Optional[int]:
 
 
 def gather(src: Layout, src_slots, n: int, buf, ws, status, buf_bytes=None, ws_bytes=None,
-           stream=None) -> None:
+           flags=None, stream=None) -> None:
     rc = lib().kvx_gather(_h(src), _ptr(src_slots), n, _ptr(buf),
                           _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
                           _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
-                          _stream(stream))
+                          _flags(flags), _stream(stream))
     _check(rc, "kvx_gather")
 
 
 def scatter(dst: Layout, dst_slots, n: int, buf, ws, status, buf_bytes=None, ws_bytes=None,
-            stream=None) -> None:
+            flags=None, stream=None) -> None:
     rc = lib().kvx_scatter(_h(dst), _ptr(dst_slots), n, _ptr(buf),
                            _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
                            _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
-                           _stream(stream))
+                           _flags(flags), _stream(stream))
     _check(rc, "kvx_scatter")
 
 
 def transfer(src: Layout, src_slots, dst: Layout, dst_slots, n: int, ws, status,
-             ws_bytes=None, stream=None) -> None:
+             ws_bytes=None, flags=None, stream=None) -> None:
     rc = lib().kvx_transfer(_h(src), _ptr(src_slots), _h(dst), _ptr(dst_slots), n, _ptr(ws),
                             _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
-                            _stream(stream))
+                            _flags(flags), _stream(stream))
     _check(rc, "kvx_transfer")
 
 
 def transfer_noalloc(src: Layout, src_slots, dst: Layout, dst_slots, n: int, status,
-                     stream=None) -> None:
+                     flags=None, stream=None) -> None:
     """kvx_transfer without a workspace, for callers that cannot allocate device memory when
     KV has to move (the planner's scratch is a fixed array inside libkvx; n is at most
     NOALLOC_MAX_TOKENS, and calls that overlap on the GPU must not share it)."""
     rc = lib().kvx_transfer_noalloc(_h(src), _ptr(src_slots), _h(dst), _ptr(dst_slots), n,
-                                    _ptr(status), _stream(stream))
+                                    _ptr(status), _flags(flags), _stream(stream))
     _check(rc, "kvx_transfer_noalloc")
 
 
 def gather_runs(src: Layout, runs, n_runs: int, n_tokens: int, buf, ws, status, buf_bytes=None,
-                ws_bytes=None, stream=None) -> None:
+                ws_bytes=None, flags=None, stream=None) -> None:
     rc = lib().kvx_gather_runs(_h(src), _ptr(runs), n_runs, n_tokens, _ptr(buf),
                                _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
                                _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
-                               _stream(stream))
+                               _flags(flags), _stream(stream))
     _check(rc, "kvx_gather_runs")
 
 
 def scatter_runs(dst: Layout, runs, n_runs: int, n_tokens: int, buf, ws, status,
-                 buf_bytes=None, ws_bytes=None, stream=None) -> None:
+                 buf_bytes=None, ws_bytes=None, flags=None, stream=None) -> None:
     rc = lib().kvx_scatter_runs(_h(dst), _ptr(runs), n_runs, n_tokens, _ptr(buf),
                                 _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
                                 _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
-                                _stream(stream))
+                                _flags(flags), _stream(stream))
     _check(rc, "kvx_scatter_runs")
 
 
 def transfer_runs(src: Layout, dst: Layout, runs, n_runs: int, n_tokens: int, ws, status,
-                  ws_bytes=None, stream=None) -> None:
+                  ws_bytes=None, flags=None, stream=None) -> None:
     rc = lib().kvx_transfer_runs(_h(src), _h(dst), _ptr(runs), n_runs, n_tokens, _ptr(ws),
                                  _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
-                                 _stream(stream))
+                                 _flags(flags), _stream(stream))
     _check(rc, "kvx_transfer_runs")
 
 
 def batch(src: Optional[Layout], dst: Optional[Layout], reqs, n_reqs: int, total_tokens: int,
           src_slots, n_src_slots: int, dst_slots, n_dst_slots: int, buf, ws, status,
-          buf_bytes=None, ws_bytes=None, stream=None) -> None:
+          buf_bytes=None, ws_bytes=None, flags=None, stream=None) -> None:
     rc = lib().kvx_batch(_h(src), _h(dst), _ptr(reqs), n_reqs, total_tokens, _ptr(src_slots),
                          n_src_slots, _ptr(dst_slots), n_dst_slots, _ptr(buf),
                          _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
                          _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
-                         _stream(stream))
+                         _flags(flags), _stream(stream))
     _check(rc, "kvx_batch")
 
 
 def submit(op: int, src: Optional[Layout], h_src_slots, dst: Optional[Layout], h_dst_slots,
-           n: int, buf, ws, h_status, buf_bytes=None, ws_bytes=None, stream=None) -> None:
+           n: int, buf, ws, h_status, buf_bytes=None, ws_bytes=None, flags=None, stream=None) -> None:
     """Host slot lists (pinned tensors or numpy arrays) and a host status word."""
     rc = lib().kvx_submit(op, _h(src), _host_ptr(h_src_slots), _h(dst), _host_ptr(h_dst_slots),
                           n, _ptr(buf), _nbytes(buf) if buf_bytes is None else buf_bytes,
                           _ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
-                          _host_ptr(h_status), _stream(stream))
+                          _host_ptr(h_status), _flags(flags), _stream(stream))
     _check(rc, "kvx_submit")
 
 
@@ -415,37 +429,37 @@ def _host_ptr(x) -> Optional[int]:
 
 
 def plan(op: int, src: Optional[Layout], src_slots, dst: Optional[Layout], dst_slots, n: int,
-         ws, status, ws_bytes=None, stream=None) -> None:
+         ws, status, ws_bytes=None, flags=None, stream=None) -> None:
     rc = lib().kvx_plan(op, _h(src), _ptr(src_slots), _h(dst), _ptr(dst_slots), n, _ptr(ws),
                         _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
-                        _stream(stream))
+                        _flags(flags), _stream(stream))
     _check(rc, "kvx_plan")
 
 
 def plan_runs(op: int, src: Optional[Layout], dst: Optional[Layout], runs, n_runs: int,
-              n_tokens: int, ws, status, ws_bytes=None, stream=None) -> None:
+              n_tokens: int, ws, status, ws_bytes=None, flags=None, stream=None) -> None:
     rc = lib().kvx_plan_runs(op, _h(src), _h(dst), _ptr(runs), n_runs, n_tokens, _ptr(ws),
                              _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
-                             _stream(stream))
+                             _flags(flags), _stream(stream))
     _check(rc, "kvx_plan_runs")
 
 
 def plan_batch(src: Optional[Layout], dst: Optional[Layout], reqs, n_reqs: int,
                total_tokens: int, src_slots, n_src_slots: int, dst_slots, n_dst_slots: int,
-               buf_bytes: int, ws, status, ws_bytes=None, stream=None) -> None:
+               buf_bytes: int, ws, status, ws_bytes=None, flags=None, stream=None) -> None:
     rc = lib().kvx_plan_batch(_h(src), _h(dst), _ptr(reqs), n_reqs, total_tokens,
                               _ptr(src_slots), n_src_slots, _ptr(dst_slots), n_dst_slots,
                               buf_bytes, _ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
-                              _ptr(status), _stream(stream))
+                              _ptr(status), _flags(flags), _stream(stream))
     _check(rc, "kvx_plan_batch")
 
 
 def execute(op: int, src: Optional[Layout], dst: Optional[Layout], reqs, n_reqs: int,
-            n_tokens: int, buf, ws, status, buf_bytes=None, ws_bytes=None, stream=None) -> None:
+            n_tokens: int, buf, ws, status, buf_bytes=None, ws_bytes=None, flags=None, stream=None) -> None:
     rc = lib().kvx_execute(op, _h(src), _h(dst), _ptr(reqs), n_reqs, n_tokens, _ptr(buf),
                            _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
                            _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
-                           _stream(stream))
+                           _flags(flags), _stream(stream))
     _check(rc, "kvx_execute")
 
 
@@ -460,7 +474,7 @@ def stream(op: int, src: Optional[Layout], src_slots, dst: Optional[Layout], dst
            buf, ws, status, layer_ready=None, ready_value: int = 1, epoch_word=None,
            epoch: int = 0, wait_ns: int = 100_000_000, max_ctas: int = 0, host_done=None,
            dst_page_epochs=None, epoch_page: int = 1, buf_bytes=None, ws_bytes=None,
-           stream=None) -> None:
+           flags=None, stream=None) -> None:
     """kvx_stream: a gather / scatter / transfer that moves layer l once
     ``layer_ready[l] >= ready_value`` and stops when ``epoch_word`` no longer holds ``epoch``
     or a layer's wait exceeds ``wait_ns``.  ``status`` is a device int32[4] (verdict, layers
@@ -470,7 +484,7 @@ def stream(op: int, src: Optional[Layout], src_slots, dst: Optional[Layout], dst
     rc = lib().kvx_stream(op, _h(src), _ptr(src_slots), _h(dst), _ptr(dst_slots), n, _ptr(buf),
                           _nbytes(buf) if buf_bytes is None else buf_bytes, ctypes.byref(ctl),
                           _ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
-                          _ptr(status), _stream(stream))
+                          _ptr(status), _flags(flags), _stream(stream))
     _check(rc, "kvx_stream")
 
 
@@ -495,7 +509,7 @@ def stream_reshard(srcs: Sequence[Optional[Layout]], src_slots, dsts: Sequence[O
                    dst_slots, parts, n: int, ws, status, layer_ready=None, ready_value: int = 1,
                    epoch_word=None, epoch: int = 0, wait_ns: int = 100_000_000, host_done=None,
                    dst_page_epochs=None, epoch_page: int = 1, max_ctas: int = 0, ws_bytes=None,
-                   stream=None) -> None:
+                   flags=None, stream=None) -> None:
     """kvx_stream_reshard: kvx_reshard moving layer l once ``layer_ready[l] >= ready_value``,
     stopping on a changed epoch word or a wait past ``wait_ns``; ``status`` is a device
     int32[4] as for stream(); ``max_ctas`` > 0 caps the grid as for stream()."""
@@ -510,7 +524,7 @@ def stream_reshard(srcs: Sequence[Optional[Layout]], src_slots, dsts: Sequence[O
     rc = lib().kvx_stream_reshard(sa, len(srcs), _ptr(src_slots), da, len(dsts),
                                   _ptr(dst_slots), pa, len(parts), n, ctypes.byref(ctl),
                                   _ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
-                                  _ptr(status), _stream(stream))
+                                  _ptr(status), _flags(flags), _stream(stream))
     _check(rc, "kvx_stream_reshard")
 
 
@@ -545,7 +559,7 @@ def tp_plan(kv_heads: int, src_tp: int, dst_tp: int):
 
 
 def reshard(srcs: Sequence[Optional[Layout]], src_slots, dsts: Sequence[Optional[Layout]],
-            dst_slots, parts, n: int, ws, status, ws_bytes=None, stream=None) -> None:
+            dst_slots, parts, n: int, ws, status, ws_bytes=None, flags=None, stream=None) -> None:
     """kvx_reshard: every part (src, dst, src_head0, dst_head0, n_heads) of a reshard between
     the pools of two TP groups, in one planner + one copy launch."""
     sa = (_VP * max(1, len(srcs)))(*[_h(x) for x in srcs])
@@ -556,18 +570,18 @@ def reshard(srcs: Sequence[Optional[Layout]], src_slots, dsts: Sequence[Optional
         pa[k] = HeadPart(*(vals + (0,) * (6 - len(vals))))
     rc = lib().kvx_reshard(sa, len(srcs), _ptr(src_slots), da, len(dsts), _ptr(dst_slots), pa,
                            len(parts), n, _ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
-                           _ptr(status), _stream(stream))
+                           _ptr(status), _flags(flags), _stream(stream))
     _check(rc, "kvx_reshard")
 
 
 def move_heads(op: int, src: Optional[Layout], src_slots, src_head0: int, dst: Optional[Layout],
                dst_slots, dst_head0: int, n_heads: int, n: int, buf, ws, status, buf_bytes=None,
-               ws_bytes=None, stream=None) -> None:
+               ws_bytes=None, flags=None, stream=None) -> None:
     """kvx_move_heads: heads [src_head0, src_head0 + n_heads) of each source row to heads
     [dst_head0, ...) of each destination row (layouts may have different kv_heads)."""
     rc = lib().kvx_move_heads(op, _h(src), _ptr(src_slots), src_head0, _h(dst), _ptr(dst_slots),
                               dst_head0, n_heads, n, _ptr(buf),
                               _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
                               _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
-                              _stream(stream))
+                              _flags(flags), _stream(stream))
     _check(rc, "kvx_move_heads")

@@ -75,7 +75,7 @@ typedef enum kvx_status {
   KVX_ERR_ALIGNMENT = 2,     /* pointer or row size not 16-byte aligned */
   KVX_ERR_OUT_OF_RANGE = 3,  /* a slot / page index outside the pool (device status) */
   KVX_ERR_DUPLICATE_DST = 4, /* a destination slot named twice (device status; only checked
-                                with kvx_set_check_duplicates(1)) */
+                                with KVX_CHECK_DUP) */
   KVX_ERR_OVERLAP = 5,       /* source and destination memory overlap */
   KVX_ERR_CUDA = 6,          /* a CUDA runtime call failed; see kvx_last_cuda_error() */
   KVX_ERR_NO_WORKSPACE = 7,  /* workspace too small or misaligned */
@@ -110,6 +110,36 @@ typedef enum kvx_op {
   KVX_OP_TRANSFER = 2, /* pool rows -> pool rows */
   KVX_OP_BATCH = 3     /* kvx_execute only: the plan came from kvx_plan_batch */
 } kvx_op;
+
+/* Per-call options: the `flags` argument of every call that moves rows (the one before the
+ * stream).  KVX_DEFAULTS takes the process-wide settings (kvx_set_check_duplicates,
+ * kvx_set_copy_engine, kvx_set_fused_max_tokens).  Any other value is the call's complete
+ * option set, a combination of the bits below (0: no duplicate check, the automatic engine,
+ * the planner path): two threads may then move KV on two streams with different options
+ * without touching each other's.  Unknown bits, or both engines, are KVX_ERR_INVALID_ARG.
+ *  KVX_CHECK_DUP      also check that no destination slot is named twice: the planner inserts
+ *                     every destination slot into a hash table in the workspace (8 bytes per
+ *                     slot of a power of two >= 2n, beyond the plan: kvx_workspace_size
+ *                     covers it, plus a memset per call).  A repeat gives
+ *                     KVX_ERR_DUPLICATE_DST with nothing moved.  A list with both a repeated
+ *                     and an out-of-range slot may report either error.  In a batch the check
+ *                     covers the destination slots of every scatter and transfer request the
+ *                     planner accepted (requests refused for a bad record or index write
+ *                     nothing and keep their own error): every request naming a slot that
+ *                     appears twice among them fails with KVX_ERR_DUPLICATE_DST and moves
+ *                     nothing, the others move.  Without the check a repeated destination ends
+ *                     up holding one of its source rows, which one unspecified.
+ *  KVX_USE_REGISTERS  linear chunks moved by 16-byte register loads and stores (what the
+ *                     automatic choice does too); KVX_USE_BULK: by the TMA bulk-copy kernel
+ *                     (see kvx_set_copy_engine).  Also the form of a capped kvx_stream grid.
+ *  KVX_ONE_LAUNCH     the one-launch path of kvx_set_fused_max_tokens for requests of up to
+ *                     KVX_FUSED_MAX_TOKENS tokens whose rows are shorter than KVX_CHUNK_BYTES
+ *                     (not with KVX_CHECK_DUP). */
+#define KVX_DEFAULTS 0xFFFFFFFFu
+#define KVX_CHECK_DUP 0x1u
+#define KVX_USE_REGISTERS 0x2u
+#define KVX_USE_BULK 0x4u
+#define KVX_ONE_LAUNCH 0x8u
 
 /* Most planes a layout may have (128 layers x K/V). */
 #define KVX_MAX_PLANES 256
@@ -195,14 +225,14 @@ KVX_API size_t kvx_workspace_size(int64_t max_tokens, int32_t max_requests);
  * d_status: device int32[1]; KVX_OK or KVX_ERR_OUT_OF_RANGE after the stream reaches it. */
 KVX_API kvx_status kvx_gather(kvx_layout_t src, const int32_t *d_src_slots, int32_t n, void *d_buf,
                       size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *d_status,
-                      kvx_stream_t stream);
+                      uint32_t flags, kvx_stream_t stream);
 
 /* Scatter ([PD-budget] 5090 section: D scatters the staged rows into its own pages):
  *   row(dst, p, dst_slots[i]) = buf[p][i].  Slots not named keep their bytes.  Naming a slot
  * twice leaves either of the two rows there (unspecified which). */
 KVX_API kvx_status kvx_scatter(kvx_layout_t dst, const int32_t *d_dst_slots, int32_t n,
                        const void *d_buf, size_t buf_bytes, void *d_ws, size_t ws_bytes,
-                       int32_t *d_status, kvx_stream_t stream);
+                       int32_t *d_status, uint32_t flags, kvx_stream_t stream);
 
 /* Pool-to-pool transfer ([PD-budget] B300 section; [Mooncake] 7.6):
  *   row(dst, p, dst_slots[i]) = row(src, p, src_slots[i]).
@@ -210,7 +240,7 @@ KVX_API kvx_status kvx_scatter(kvx_layout_t dst, const int32_t *d_dst_slots, int
  * not share memory (KVX_ERR_OVERLAP). */
 KVX_API kvx_status kvx_transfer(kvx_layout_t src, const int32_t *d_src_slots, kvx_layout_t dst,
                         const int32_t *d_dst_slots, int32_t n, void *d_ws, size_t ws_bytes,
-                        int32_t *d_status, kvx_stream_t stream);
+                        int32_t *d_status, uint32_t flags, kvx_stream_t stream);
 
 /* Run-list forms ([Mooncake] 7.6 src/dst/length descriptors).  d_runs: device int32[n_runs][3]
  * = {src_start, dst_start, len}; run r names rows src_start .. src_start+len-1 and
@@ -219,13 +249,13 @@ KVX_API kvx_status kvx_transfer(kvx_layout_t src, const int32_t *d_src_slots, kv
  * device: KVX_ERR_INVALID_ARG in the status word). */
 KVX_API kvx_status kvx_gather_runs(kvx_layout_t src, const int32_t *d_runs, int32_t n_runs,
                            int32_t n_tokens, void *d_buf, size_t buf_bytes, void *d_ws,
-                           size_t ws_bytes, int32_t *d_status, kvx_stream_t stream);
+                           size_t ws_bytes, int32_t *d_status, uint32_t flags, kvx_stream_t stream);
 KVX_API kvx_status kvx_scatter_runs(kvx_layout_t dst, const int32_t *d_runs, int32_t n_runs,
                             int32_t n_tokens, const void *d_buf, size_t buf_bytes, void *d_ws,
-                            size_t ws_bytes, int32_t *d_status, kvx_stream_t stream);
+                            size_t ws_bytes, int32_t *d_status, uint32_t flags, kvx_stream_t stream);
 KVX_API kvx_status kvx_transfer_runs(kvx_layout_t src, kvx_layout_t dst, const int32_t *d_runs,
                              int32_t n_runs, int32_t n_tokens, void *d_ws, size_t ws_bytes,
-                             int32_t *d_status, kvx_stream_t stream);
+                             int32_t *d_status, uint32_t flags, kvx_stream_t stream);
 
 /* Batch of requests in one plan + one copy launch ([Mooncake] 6.1).  d_reqs: device
  * kvx_request[n_reqs].  total_tokens must equal the sum of n_tokens.  src / dst may be NULL
@@ -236,7 +266,7 @@ KVX_API kvx_status kvx_batch(kvx_layout_t src, kvx_layout_t dst, const kvx_reque
                      int32_t n_reqs, int64_t total_tokens, const int32_t *d_src_slots,
                      int64_t n_src_slots, const int32_t *d_dst_slots, int64_t n_dst_slots,
                      void *d_buf, size_t buf_bytes, void *d_ws, size_t ws_bytes,
-                     int32_t *d_status, kvx_stream_t stream);
+                     int32_t *d_status, uint32_t flags, kvx_stream_t stream);
 
 /* Host-index submission ([Mooncake] 6.1 submitTransfer + getTransferStatus): like
  * kvx_gather / kvx_scatter / kvx_transfer, but the slot lists and the status word are host
@@ -247,26 +277,33 @@ KVX_API kvx_status kvx_batch(kvx_layout_t src, kvx_layout_t dst, const kvx_reque
 KVX_API kvx_status kvx_submit(int32_t op, kvx_layout_t src, const int32_t *h_src_slots,
                       kvx_layout_t dst, const int32_t *h_dst_slots, int32_t n, void *d_buf,
                       size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *h_status,
-                      kvx_stream_t stream);
+                      uint32_t flags, kvx_stream_t stream);
 
 /* Pool-to-pool transfer without a workspace argument.  The pages have no counterpart to this
  * call: it exists for callers that cannot allocate device memory when KV has to move -- an
  * engine that reserved nearly all HBM for its KV pool at start-up has none left for a
  * workspace, and cudaMalloc would synchronise the device between decode steps.  Same
  * arguments, results and errors as kvx_transfer, except that the planner's scratch is one
- * fixed array per device inside libkvx:
- *  - n may be at most KVX_NOALLOC_MAX_TOKENS; a larger n returns KVX_ERR_NO_WORKSPACE with
- *    nothing enqueued;
- *  - the array's device address is looked up on the first call made while a device is
- *    current; make that first call on each device before any stream capture;
+ * fixed array per device inside libkvx (about 321 KiB, held by every GPU that loads the
+ * library until the process exits):
+ *  - n may be at most KVX_NOALLOC_MAX_TOKENS, and with the duplicate check (KVX_CHECK_DUP, or
+ *    the process default) at most KVX_NOALLOC_MAX_DUP_TOKENS; a larger n returns
+ *    KVX_ERR_NO_WORKSPACE with nothing enqueued;
+ *  - CUDA loads the array, and each of libkvx's kernels, into device memory when it is first
+ *    used.  The first call on a device -- n = 0 is enough -- loads the array and every kernel
+ *    this call can launch, so that no later call needs device memory.  Make that first call on
+ *    each device before the KV pool takes the device's free memory and before any stream
+ *    capture (after a device reset, make it again);
  *  - all calls share the array, so calls whose work overlaps on the GPU (other streams, other
  *    host threads without ordering) race and may corrupt each other; calls in one stream are
  *    safe.  Nothing in it needs to be cleared between calls.
- * It allocates nothing and calls no allocating library routine. */
+ * After the first call per device it allocates nothing and calls no allocating library
+ * routine. */
 #define KVX_NOALLOC_MAX_TOKENS 16384
+#define KVX_NOALLOC_MAX_DUP_TOKENS 8192
 KVX_API kvx_status kvx_transfer_noalloc(kvx_layout_t src, const int32_t *d_src_slots,
                                         kvx_layout_t dst, const int32_t *d_dst_slots, int32_t n,
-                                        int32_t *d_status, kvx_stream_t stream);
+                                        int32_t *d_status, uint32_t flags, kvx_stream_t stream);
 
 /* ---- two-phase form: the plan (validation + run-length planning) and the copy -------- */
 
@@ -274,15 +311,15 @@ KVX_API kvx_status kvx_transfer_noalloc(kvx_layout_t src, const int32_t *d_src_s
  * op is KVX_OP_GATHER, KVX_OP_SCATTER or KVX_OP_TRANSFER; unused side arguments are NULL. */
 KVX_API kvx_status kvx_plan(int32_t op, kvx_layout_t src, const int32_t *d_src_slots, kvx_layout_t dst,
                     const int32_t *d_dst_slots, int32_t n, void *d_ws, size_t ws_bytes,
-                    int32_t *d_status, kvx_stream_t stream);
+                    int32_t *d_status, uint32_t flags, kvx_stream_t stream);
 KVX_API kvx_status kvx_plan_runs(int32_t op, kvx_layout_t src, kvx_layout_t dst, const int32_t *d_runs,
                          int32_t n_runs, int32_t n_tokens, void *d_ws, size_t ws_bytes,
-                         int32_t *d_status, kvx_stream_t stream);
+                         int32_t *d_status, uint32_t flags, kvx_stream_t stream);
 KVX_API kvx_status kvx_plan_batch(kvx_layout_t src, kvx_layout_t dst, const kvx_request *d_reqs,
                           int32_t n_reqs, int64_t total_tokens, const int32_t *d_src_slots,
                           int64_t n_src_slots, const int32_t *d_dst_slots, int64_t n_dst_slots,
                           size_t buf_bytes, void *d_ws, size_t ws_bytes, int32_t *d_status,
-                          kvx_stream_t stream);
+                          uint32_t flags, kvx_stream_t stream);
 
 /* Runs the copy the plan in d_ws describes.  op, layouts, n_tokens (the planned token count:
  * n, the runs' total, or total_tokens) and, for KVX_OP_BATCH, d_reqs / n_reqs must be those
@@ -293,7 +330,7 @@ KVX_API kvx_status kvx_plan_batch(kvx_layout_t src, kvx_layout_t dst, const kvx_
 KVX_API kvx_status kvx_execute(int32_t op, kvx_layout_t src, kvx_layout_t dst, const kvx_request *d_reqs,
                        int32_t n_reqs, int64_t n_tokens, void *d_buf, size_t buf_bytes,
                        const void *d_ws, size_t ws_bytes, int32_t *d_status,
-                       kvx_stream_t stream);
+                       uint32_t flags, kvx_stream_t stream);
 
 /* Copies the plan's chunks out of the workspace, in plan order, as device int32[4] records
  * {request, src_index, dst_index, rows}; *d_count (device int64) gets the total, and at most
@@ -335,7 +372,7 @@ KVX_API kvx_status kvx_move_heads(int32_t op, kvx_layout_t src, const int32_t *d
                                   const int32_t *d_dst_slots, int32_t dst_head0,
                                   int32_t n_heads, int32_t n, void *d_buf, size_t buf_bytes,
                                   void *d_ws, size_t ws_bytes, int32_t *d_status,
-                                  kvx_stream_t stream);
+                                  uint32_t flags, kvx_stream_t stream);
 
 /* One part of a reshard (kvx_reshard): heads src_head0 .. src_head0 + n_heads - 1 of layout
  * srcs[src] go to heads dst_head0 .. dst_head0 + n_heads - 1 of layout dsts[dst].  Host
@@ -389,13 +426,13 @@ KVX_API kvx_status kvx_tp_plan(int32_t kv_heads, int32_t src_tp, int32_t dst_tp,
  * (a part's bytes do not start and end on 16-byte boundaries within rows); KVX_ERR_NO_WORKSPACE
  * (d_ws as kvx_transfer: kvx_workspace_size(n, 0) bytes).  On the stream: *d_status = KVX_OK,
  * or KVX_ERR_OUT_OF_RANGE (a slot outside [0, num_slots)) or KVX_ERR_DUPLICATE_DST (with
- * kvx_set_check_duplicates on), with nothing written. */
+ * KVX_CHECK_DUP), with nothing written. */
 KVX_API kvx_status kvx_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
                                const int32_t *d_src_slots, const kvx_layout_t *dsts,
                                int32_t n_dsts, const int32_t *d_dst_slots,
                                const kvx_head_part *parts, int32_t n_parts, int32_t n,
                                void *d_ws, size_t ws_bytes, int32_t *d_status,
-                               kvx_stream_t stream);
+                               uint32_t flags, kvx_stream_t stream);
 
 /* ---- layer-streamed, cancellable copy ------------------------------------------------- */
 
@@ -472,7 +509,7 @@ KVX_API kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src
                               kvx_layout_t dst, const int32_t *d_dst_slots, int32_t n,
                               void *d_buf, size_t buf_bytes, const kvx_stream_ctl *ctl,
                               void *d_ws, size_t ws_bytes, int32_t *d_status,
-                              kvx_stream_t stream);
+                              uint32_t flags, kvx_stream_t stream);
 
 /* kvx_reshard, layer-streamed and cancellable as kvx_stream ("DistServe 完全拆解", layer j
  * pulled as soon as prefill has written it; [Mooncake] 7.7 异构TP for the parts): layer l of
@@ -492,7 +529,7 @@ KVX_API kvx_status kvx_stream_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
                                       int32_t n_dsts, const int32_t *d_dst_slots,
                                       const kvx_head_part *parts, int32_t n_parts, int32_t n,
                                       const kvx_stream_ctl *ctl, void *d_ws, size_t ws_bytes,
-                                      int32_t *d_status, kvx_stream_t stream);
+                                      int32_t *d_status, uint32_t flags, kvx_stream_t stream);
 
 /* ---- misc ---------------------------------------------------------------------------- */
 
@@ -500,8 +537,9 @@ KVX_API kvx_status kvx_stream_reshard(const kvx_layout_t *srcs, int32_t n_srcs,
  * TMA bulk-copy kernel (cp.async.bulk through shared memory); KVX_ENGINE_AUTO (default) and
  * KVX_ENGINE_REGISTERS use 16-byte register loads and stores.  Both move the same bytes;
  * chunks that are not linear always take the register path.  It also picks the form of
- * kvx_stream's capped persistent grid (kvx_stream_ctl::max_ctas).  Read once per call;
- * process-wide; returns KVX_ERR_INVALID_ARG for an unknown value. */
+ * kvx_stream's capped persistent grid (kvx_stream_ctl::max_ctas).  A process-wide default read
+ * once per call made with flags = KVX_DEFAULTS (KVX_USE_REGISTERS / KVX_USE_BULK choose it per
+ * call); returns KVX_ERR_INVALID_ARG for an unknown value. */
 #define KVX_ENGINE_AUTO 0
 #define KVX_ENGINE_REGISTERS 1
 #define KVX_ENGINE_BULK 2
@@ -514,22 +552,15 @@ KVX_API int32_t kvx_get_copy_engine(void);
  * stays all-or-nothing), planning the runs of its own slice and copying it.  Otherwise the
  * planner launch and the row copy kernel run (the copy overlaps the planner).  Both reach the
  * same bytes.  The default is 0 (off: on GB300 the two launches measured faster at every size);
- * the most is KVX_FUSED_MAX_TOKENS.  Process-wide. */
+ * the most is KVX_FUSED_MAX_TOKENS.  A process-wide default for calls made with flags =
+ * KVX_DEFAULTS; a call's own flags choose it with KVX_ONE_LAUNCH (limit KVX_FUSED_MAX_TOKENS). */
 #define KVX_FUSED_MAX_TOKENS 8192
 KVX_API kvx_status kvx_set_fused_max_tokens(int32_t max_tokens);
 KVX_API int32_t kvx_get_fused_max_tokens(void);
 
-/* Duplicate-destination check (process-wide, off by default).  With 1, every slot-list call
- * that writes into a pool (kvx_scatter, kvx_transfer, kvx_submit, kvx_stream,
- * kvx_move_heads, kvx_plan for those ops) also makes the planner insert each destination slot
- * into a hash table in the workspace; a slot named twice gives KVX_ERR_DUPLICATE_DST in the
- * status and nothing moves.  (Without the check a repeated destination ends up holding one of
- * its source rows, which one unspecified.)  The table needs the workspace kvx_workspace_size
- * returns (4 bytes per slot of a power of two >= 2n, beyond the plan), and a memset per call;
- * the one-launch fused path is not used while the check is on.  Run lists and batches are not
- * checked, and kvx_transfer_noalloc's fixed scratch holds the table only for requests of up to
- * about half its token limit (KVX_ERR_NO_WORKSPACE beyond that while the check is on).  A list with both a repeated and an
- * out-of-range slot may report either error.  KVX_ERR_INVALID_ARG for values other than 0 / 1. */
+/* Process-wide default of the duplicate-destination check (KVX_CHECK_DUP), off at start: calls
+ * made with flags = KVX_DEFAULTS check for repeats while it is 1.  Calls with their own flags
+ * word are not affected.  KVX_ERR_INVALID_ARG for values other than 0 / 1. */
 KVX_API kvx_status kvx_set_check_duplicates(int32_t on);
 KVX_API int32_t kvx_get_check_duplicates(void);
 

@@ -121,7 +121,8 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
     lib.kvxo_hnd_gather.argtypes = [P(_Pool), i32p, ctypes.c_int64, u8p]
     lib.kvxo_hnd_rebuild.argtypes = [P(_Pool), i32p, ctypes.c_int64, u8p]
     lib.kvxo_batch.argtypes = [P(_Pool), P(_Pool), P(Request), ctypes.c_int32, i32p,
-                               ctypes.c_int64, i32p, ctypes.c_int64, u8p, ctypes.c_int64, i32p]
+                               ctypes.c_int64, i32p, ctypes.c_int64, u8p, ctypes.c_int64,
+                               ctypes.c_int, i32p]
     lib.kvxo_runs.restype = ctypes.c_int64
     lib.kvxo_runs.argtypes = [i32p, i32p, ctypes.c_int64, P(ctypes.c_int64), ctypes.c_int32,
                               P(Run), ctypes.c_int64]
@@ -322,7 +323,7 @@ def hnd_rebuild(pool: Pool, page_table, seq_len: int, buf: np.ndarray, lib=None)
 
 
 def batch(src: Optional[Pool], dst: Optional[Pool], reqs: Sequence[tuple], src_slots,
-          dst_slots, buf: np.ndarray, lib=None) -> np.ndarray:
+          dst_slots, buf: np.ndarray, check_dup: bool = False, lib=None) -> np.ndarray:
     """reqs: sequence of (op, n_tokens, src_off, dst_off, buf_off).  Returns status[n+1]."""
     lib = lib or load()
     arr = (Request * max(1, len(reqs)))(*[Request(*r) for r in reqs])
@@ -333,7 +334,7 @@ def batch(src: Optional[Pool], dst: Optional[Pool], reqs: Sequence[tuple], src_s
     buf = buf.view(np.uint8)
     lib.kvxo_batch(ctypes.byref(s1) if s1 else None, ctypes.byref(s2) if s2 else None, arr,
                    len(reqs), _i32p(a), len(a), _i32p(b), len(b), buf.ctypes.data, buf.nbytes,
-                   _i32p(status))
+                   int(check_dup), _i32p(status))
     return status
 
 

@@ -414,7 +414,7 @@ static int check_request(const kvxo_pool *src, const kvxo_pool *dst, const kvxo_
 int kvxo_batch(const kvxo_pool *src, const kvxo_pool *dst, const kvxo_request *reqs,
                int32_t n_reqs, const int32_t *src_slots, int64_t n_src_slots,
                const int32_t *dst_slots, int64_t n_dst_slots, uint8_t *buf, int64_t buf_bytes,
-               int32_t *status) {
+               int check_dup, int32_t *status) {
   /* [Mooncake] 6.1: a batch of non-contiguous transfers submitted together; each is its own
    * request with its own status. */
   status[0] = KVXO_OK;
@@ -422,10 +422,37 @@ int kvxo_batch(const kvxo_pool *src, const kvxo_pool *dst, const kvxo_request *r
     for (int32_t q = 0; q <= n_reqs; ++q) status[q] = KVXO_ERR_INVALID_ARG;
     return KVXO_ERR_INVALID_ARG;
   }
+  /* each request's own checks: its record and its indices */
+  for (int32_t q = 0; q < n_reqs; ++q)
+    status[1 + q] = check_request(src, dst, &reqs[q], n_src_slots, n_dst_slots, buf_bytes,
+                                  src_slots, dst_slots);
+  /* the duplicate check (asked for by the caller; the pages are silent on repeats): count
+   * every destination slot of the accepted requests that write into the pool; a request
+   * naming a slot counted more than once fails and writes nothing */
+  if (check_dup && dst) {
+    int32_t *count = (int32_t *)calloc((size_t)dst->num_slots, sizeof(int32_t));
+    if (!count) return KVXO_ERR_INVALID_ARG;
+    for (int32_t q = 0; q < n_reqs; ++q) {
+      const kvxo_request *r = &reqs[q];
+      const int counted = status[1 + q] == KVXO_OK && r->op != KVXO_OP_GATHER;
+      if (counted)
+        for (int32_t i = 0; i < r->n_tokens; ++i) ++count[dst_slots[r->dst_off + i]];
+    }
+    for (int32_t q = 0; q < n_reqs; ++q) {
+      const kvxo_request *r = &reqs[q];
+      if (status[1 + q] != KVXO_OK || r->op == KVXO_OP_GATHER) continue;
+      for (int32_t i = 0; i < r->n_tokens; ++i)
+        if (count[dst_slots[r->dst_off + i]] > 1) {
+          status[1 + q] = KVXO_ERR_DUPLICATE_DST;
+          break;
+        }
+    }
+    free(count);
+  }
+  /* the accepted requests, one by one in index order */
   for (int32_t q = 0; q < n_reqs; ++q) {
     const kvxo_request *r = &reqs[q];
-    int rc = check_request(src, dst, r, n_src_slots, n_dst_slots, buf_bytes, src_slots,
-                           dst_slots);
+    int rc = status[1 + q];
     if (rc == KVXO_OK) {
       if (r->op == KVXO_OP_GATHER)
         rc = kvxo_gather(src, src_slots + r->src_off, r->n_tokens, buf + r->buf_off, NULL);

@@ -191,11 +191,13 @@ int kvxo_hnd_rebuild(const kvxo_pool *dst, const int32_t *page_table, int64_t se
 /* Batch: every request applied in index order ([Mooncake] 6.1 BatchTransfer).
  * status[0] = largest code of any request, status[1 + q] = code of request q.  A failing
  * request writes nothing; the others still run.  The buffer region of request q is
- * buf + buf_off laid out [plane][n_tokens][head][dim]. */
+ * buf + buf_off laid out [plane][n_tokens][head][dim].  With check_dup, a destination slot
+ * named more than once among the scatter and transfer requests that passed their own checks
+ * fails every such request naming it (KVXO_ERR_DUPLICATE_DST). */
 int kvxo_batch(const kvxo_pool *src, const kvxo_pool *dst, const kvxo_request *reqs,
                int32_t n_reqs, const int32_t *src_slots, int64_t n_src_slots,
                const int32_t *dst_slots, int64_t n_dst_slots, uint8_t *buf, int64_t buf_bytes,
-               int32_t *status);
+               int check_dup, int32_t *status);
 
 /* Run-length coalescing ([Mooncake] 7.6: blocks at consecutive addresses are merged into one
  * (source, destination, length) descriptor).  src_idx / dst_idx give each token's source and

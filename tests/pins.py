@@ -592,6 +592,89 @@ def pin_batch(lib):
     assert list(st) == [1, 1, 1, 1, 1]
 
 
+def pin_batch_duplicates(lib):
+    """The duplicate check of a batch, against a brute-force model written from its rule: the
+    requests that pass their own checks and write into the pool are compared pairwise (and each
+    with itself) for a shared destination slot; every request in such a pair fails with
+    DUPLICATE_DST and moves nothing; the remaining requests are applied one by one with the
+    element model.  Statuses, the destination pool and the buffer must all agree, on a fixed
+    case (two transfers sharing a slot, a transfer repeating a slot, a refused transfer sharing
+    a slot with one that must still move) and on random batches over a 12-slot pool."""
+    g = np.random.Generator(np.random.PCG64(29))
+    R = H * D * 2
+    P = 2 * L
+
+    def model(src, dst0, reqs, ss, ds, buf0):
+        ok = []
+        for op, n, so, do, bo in reqs:
+            s_ok = op == oracle.OP_SCATTER or all(0 <= x < src.num_slots for x in ss[so:so + n])
+            d_ok = op == oracle.OP_GATHER or all(0 <= x < dst0.num_slots for x in ds[do:do + n])
+            ok.append(oracle.OK if (s_ok and d_ok) else oracle.ERR_OUT_OF_RANGE)
+        writes = [q for q, r in enumerate(reqs) if ok[q] == oracle.OK and r[0] != oracle.OP_GATHER]
+        dset = {q: list(ds[reqs[q][3]: reqs[q][3] + reqs[q][1]]) for q in writes}
+        for a in writes:
+            if len(set(dset[a])) < len(dset[a]):
+                ok[a] = oracle.ERR_DUPLICATE_DST
+            for b in writes:
+                if a != b and set(dset[a]) & set(dset[b]):
+                    ok[a] = oracle.ERR_DUPLICATE_DST
+        dst, buf = dst0.copy(), buf0.copy()
+        for q, (op, n, so, do, bo) in enumerate(reqs):
+            if ok[q] != oracle.OK:
+                continue
+            if op == oracle.OP_TRANSFER:
+                dst = bf.transfer(src, ss[so:so + n], dst, ds[do:do + n])
+            elif op == oracle.OP_GATHER:
+                buf[bo: bo + P * n * R] = _bytes_of(bf.gather(src, ss[so:so + n]))
+            else:
+                rows = buf[bo: bo + P * n * R].view(np.uint16).reshape(L, 2, n, H, D)
+                dst = bf.scatter(dst, ds[do:do + n], rows)
+        return [max(ok + [0])] + ok, dst, buf
+
+    def check(src, dst0, reqs, ss, ds, buf0):
+        dst, buf = dst0.copy(), buf0.copy()
+        st = oracle.batch(bf.to_oracle(src), bf.to_oracle(dst), reqs, ss, ds, buf, check_dup=True,
+                          lib=lib)
+        want_st, want_dst, want_buf = model(src, dst0, reqs, ss, ds, buf0)
+        assert list(st) == want_st, (list(st), want_st, reqs)
+        assert np.array_equal(dst.data, want_dst.data)
+        assert np.array_equal(buf, want_buf)
+        return list(st)
+
+    src = bf.make_pool("planes", L, H, D, 12, lambda n: g.integers(0, 0x7C00, n))
+    dst0 = bf.make_pool("planes", L, H, D, 12, _sentinel_fill)
+    buf0 = g.integers(0, 255, 4 * P * 3 * R, dtype=np.uint8)
+    T, G, S = oracle.OP_TRANSFER, oracle.OP_GATHER, oracle.OP_SCATTER
+    ss = np.array([0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 99, 1, 2, 3], dtype=np.int32)
+    ds = np.array([0, 1, 2, 2, 3, 4, 5, 6, 6, 7, 8, 9, 10, 11, 9], dtype=np.int32)
+    reqs = [(T, 3, 0, 0, 0),       # dst 0 1 2: shares 2 with the next one
+            (T, 3, 3, 3, 0),       # dst 2 3 4
+            (T, 3, 6, 6, 0),       # dst 5 6 6: repeats a slot of its own
+            (T, 3, 9, 9, 0),       # src 9 10 99 out of range; dst 7 8 9
+            (S, 2, 0, 12, 0),      # dst 10 11
+            (T, 1, 12, 14, 0),     # dst 9: shared only with the refused request, so it moves
+            (G, 2, 13, 0, P * 2 * R)]
+    st = check(src, dst0, reqs, ss, ds, buf0)
+    D_, O_ = oracle.ERR_DUPLICATE_DST, oracle.ERR_OUT_OF_RANGE
+    assert st == [D_, D_, D_, D_, O_, 0, 0, 0]
+    # without the check every accepted request moves
+    st = oracle.batch(bf.to_oracle(src), bf.to_oracle(dst0.copy()), reqs, ss, ds, buf0.copy(),
+                      lib=lib)
+    assert list(st) == [O_, 0, 0, 0, O_, 0, 0, 0]
+    for trial in range(150):
+        nreq = int(g.integers(1, 5))
+        reqs, ss_l, ds_l, bo = [], [], [], 0
+        for _ in range(nreq):
+            op = int(g.choice([T, T, S, G]))
+            n = int(g.integers(1, 4))
+            reqs.append((op, n, len(ss_l), len(ds_l), bo))
+            ss_l += list(g.integers(0, 13 if g.random() < 0.15 else 12, n))
+            ds_l += list(g.integers(0, 12, n))
+            bo += P * n * R
+        buf0 = g.integers(0, 255, max(bo, 16), dtype=np.uint8)
+        check(src, dst0, reqs, np.array(ss_l, np.int32), np.array(ds_l, np.int32), buf0)
+
+
 def _expand(runs):
     src, dst = [], []
     for _, s, d, n in runs:
@@ -688,4 +771,4 @@ ALL_PINS = [pin_sizes, pin_bytes_written, pin_bruteforce_gather, pin_bruteforce_
             pin_move_heads_full_range_is_transfer, pin_tp_slice, pin_mla, pin_bruteforce_hnd,
             pin_roundtrip,
             pin_transfer_is_scatter_of_gather, pin_hnd_roundtrip, pin_plane_locality,
-            pin_numpy_special_cases, pin_validation, pin_batch, pin_plan]
+            pin_numpy_special_cases, pin_validation, pin_batch, pin_batch_duplicates, pin_plan]

@@ -107,26 +107,51 @@ def test_call_validation_before_cuda(lib):
     big = 1 << 30
     l = kvx.lib()
     # transfer: mismatched shapes, overlap, null status, negative n
-    assert l.kvx_transfer(src.handle, SL, other.handle, SL, 10, WS, big, ST, None) == kvx.ERR_INVALID_ARG
-    assert l.kvx_transfer(src.handle, SL, src.handle, SL, 10, WS, big, ST, None) == kvx.ERR_OVERLAP
-    assert l.kvx_transfer(src.handle, SL, dst.handle, SL, 10, WS, big, None, None) == kvx.ERR_INVALID_ARG
-    assert l.kvx_transfer(src.handle, SL, dst.handle, SL, -1, WS, big, ST, None) == kvx.ERR_INVALID_ARG
-    assert l.kvx_transfer(src.handle, None, dst.handle, SL, 10, WS, big, ST, None) == kvx.ERR_INVALID_ARG
-    assert l.kvx_transfer(src.handle, SL, dst.handle, SL, 10, WS + 16, big, ST, None) == kvx.ERR_NO_WORKSPACE
-    assert l.kvx_transfer(src.handle, SL, dst.handle, SL, 10, WS, 512, ST, None) == kvx.ERR_NO_WORKSPACE
-    assert l.kvx_transfer(None, SL, dst.handle, SL, 10, WS, big, ST, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_transfer(src.handle, SL, other.handle, SL, 10, WS, big, ST, kvx.DEFAULTS, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_transfer(src.handle, SL, src.handle, SL, 10, WS, big, ST, kvx.DEFAULTS, None) == kvx.ERR_OVERLAP
+    assert l.kvx_transfer(src.handle, SL, dst.handle, SL, 10, WS, big, None, kvx.DEFAULTS, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_transfer(src.handle, SL, dst.handle, SL, -1, WS, big, ST, kvx.DEFAULTS, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_transfer(src.handle, None, dst.handle, SL, 10, WS, big, ST, kvx.DEFAULTS, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_transfer(src.handle, SL, dst.handle, SL, 10, WS + 16, big, ST, kvx.DEFAULTS, None) == kvx.ERR_NO_WORKSPACE
+    assert l.kvx_transfer(src.handle, SL, dst.handle, SL, 10, WS, 512, ST, kvx.DEFAULTS, None) == kvx.ERR_NO_WORKSPACE
+    assert l.kvx_transfer(None, SL, dst.handle, SL, 10, WS, big, ST, kvx.DEFAULTS, None) == kvx.ERR_INVALID_ARG
     # gather: buffer checks
     need = 4 * 10 * 256
-    assert l.kvx_gather(src.handle, SL, 10, None, need, WS, big, ST, None) == kvx.ERR_INVALID_ARG
-    assert l.kvx_gather(src.handle, SL, 10, BUF + 4, need, WS, big, ST, None) == kvx.ERR_ALIGNMENT
-    assert l.kvx_gather(src.handle, SL, 10, BUF, need - 16, WS, big, ST, None) == kvx.ERR_INVALID_ARG
-    assert l.kvx_gather(src.handle, SL, 10, FAKE + 256, need, WS, big, ST, None) == kvx.ERR_OVERLAP
+    assert l.kvx_gather(src.handle, SL, 10, None, need, WS, big, ST, kvx.DEFAULTS, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_gather(src.handle, SL, 10, BUF + 4, need, WS, big, ST, kvx.DEFAULTS, None) == kvx.ERR_ALIGNMENT
+    assert l.kvx_gather(src.handle, SL, 10, BUF, need - 16, WS, big, ST, kvx.DEFAULTS, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_gather(src.handle, SL, 10, FAKE + 256, need, WS, big, ST, kvx.DEFAULTS, None) == kvx.ERR_OVERLAP
     # execute / plan argument checks
-    assert l.kvx_execute(9, src.handle, dst.handle, None, 0, 10, None, 0, WS, big, ST, None) == kvx.ERR_INVALID_ARG
-    assert l.kvx_plan(kvx.OP_BATCH, src.handle, SL, dst.handle, SL, 10, WS, big, ST, None) == kvx.ERR_INVALID_ARG
-    assert l.kvx_plan_runs(kvx.OP_TRANSFER, src.handle, dst.handle, None, 3, 10, WS, big, ST, None) == kvx.ERR_INVALID_ARG
-    assert l.kvx_plan_batch(src.handle, dst.handle, None, 2, 10, SL, 10, SL, 10, 0, WS, big, ST, None) == kvx.ERR_INVALID_ARG
-    assert l.kvx_submit(kvx.OP_TRANSFER, src.handle, None, dst.handle, None, 10, None, 0, WS, big, ctypes.c_void_p(0), None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_execute(9, src.handle, dst.handle, None, 0, 10, None, 0, WS, big, ST, kvx.DEFAULTS, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_plan(kvx.OP_BATCH, src.handle, SL, dst.handle, SL, 10, WS, big, ST, kvx.DEFAULTS, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_plan_runs(kvx.OP_TRANSFER, src.handle, dst.handle, None, 3, 10, WS, big, ST, kvx.DEFAULTS, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_plan_batch(src.handle, dst.handle, None, 2, 10, SL, 10, SL, 10, 0, WS, big, ST, kvx.DEFAULTS, None) == kvx.ERR_INVALID_ARG
+    assert l.kvx_submit(kvx.OP_TRANSFER, src.handle, None, dst.handle, None, 10, None, 0, WS, big, ctypes.c_void_p(0), kvx.DEFAULTS, None) == kvx.ERR_INVALID_ARG
+
+
+def test_call_flags_checked_before_cuda(lib):
+    """A call's flags word: unknown bits or both engines are refused on the host; the
+    duplicate check needs its table in the workspace (kvx_workspace_size covers it)."""
+    src = kvx.Layout(2, 2, 64, kvx.F16, 1000, base=FAKE, plane_stride=1000 * 256)
+    dst = kvx.Layout(2, 2, 64, kvx.F16, 1000, base=FAKE * 2, plane_stride=1000 * 256)
+    WS, ST, SL = FAKE * 4, FAKE * 5, FAKE * 6
+    l = kvx.lib()
+    big = 1 << 30
+
+    def tr(flags, ws_bytes=big):
+        return l.kvx_transfer(src.handle, SL, dst.handle, SL, 3000, WS, ws_bytes, ST, flags, None)
+
+    for bad in (0x10, 0x80000000, kvx.USE_REGISTERS | kvx.USE_BULK, 0xFFFFFFFE):
+        assert tr(bad) == kvx.ERR_INVALID_ARG, hex(bad)
+        assert l.kvx_batch(src.handle, dst.handle, FAKE * 8, 1, 10, SL, 10, SL, 10, None, 0, WS,
+                           big, ST, bad, None) == kvx.ERR_INVALID_ARG
+        assert l.kvx_stream(kvx.OP_TRANSFER, src.handle, SL, dst.handle, SL, 10, None, 0, None, WS,
+                            big, ST, bad, None) == kvx.ERR_INVALID_ARG
+    # 100,000 bytes hold the plan of 3000 tokens (two tiles of 32 KiB chunk tables) but not
+    # the duplicate table after it (8 bytes x 8192 slots); kvx_workspace_size covers both
+    assert kvx.workspace_size(3000) > 100_000
+    assert tr(kvx.CHECK_DUP, 100_000) == kvx.ERR_NO_WORKSPACE
+    assert tr(kvx.CHECK_DUP | kvx.USE_BULK, 100_000) == kvx.ERR_NO_WORKSPACE
 
 
 def test_stream_validation_before_cuda(lib):
@@ -139,7 +164,7 @@ def test_stream_validation_before_cuda(lib):
 
     def call(ctl, status=ST, op=kvx.OP_TRANSFER, n=10, s=src, d=dst):
         return l.kvx_stream(op, s.handle, SL, d.handle, SL, n, None, 0,
-                            None if ctl is None else ctypes.byref(ctl), WS, big, status, None)
+                            None if ctl is None else ctypes.byref(ctl), WS, big, status, kvx.DEFAULTS, None)
 
     def ctl(**kw):
         c = kvx.StreamCtl()
@@ -189,7 +214,7 @@ def test_move_heads_validation_before_cuda(lib):
 
     def mv(op, s, h0, d, g0, nh, n=10, buf=None, bb=0):
         return l.kvx_move_heads(op, s and s.handle, SL, h0, d and d.handle, SL, g0, nh, n, buf, bb,
-                                WS, big, ST, None)
+                                WS, big, ST, kvx.DEFAULTS, None)
 
     T, G, S = kvx.OP_TRANSFER, kvx.OP_GATHER, kvx.OP_SCATTER
     assert mv(T, src, 3, dst, 0, 2) == kvx.ERR_INVALID_ARG      # source range past kv_heads
@@ -248,7 +273,7 @@ def test_reshard_validation_before_cuda(lib):
         sa = (ctypes.c_void_p * max(1, len(srcs)))(*[x.handle for x in srcs])
         da = (ctypes.c_void_p * max(1, len(dsts)))(*[x.handle for x in dsts])
         pa = (kvx.HeadPart * max(1, len(parts)))(*[kvx.HeadPart(*q) for q in parts])
-        return l.kvx_reshard(sa, len(srcs), sl, da, len(dsts), sl, pa, len(parts), n, ws, wsb, st,
+        return l.kvx_reshard(sa, len(srcs), sl, da, len(dsts), sl, pa, len(parts), n, ws, wsb, st, kvx.DEFAULTS,
                              None)
 
     E, O, A = kvx.ERR_INVALID_ARG, kvx.ERR_OVERLAP, kvx.ERR_ALIGNMENT
@@ -298,7 +323,7 @@ def test_stream_reshard_validation_before_cuda(lib):
         pa = (kvx.HeadPart * max(1, len(parts)))(*[kvx.HeadPart(*q) for q in parts])
         return l.kvx_stream_reshard(sa, len(srcs), SL, da, 1, SL, pa, len(parts), 10,
                                     ctypes.byref(ctl) if ctl is not None else None, WS, 1 << 30,
-                                    st, None)
+                                    st, kvx.DEFAULTS, None)
 
     good = [(0, 0, 0, 0, 2), (1, 0, 0, 2, 2)]
     ok = kvx._stream_ctl(None, 1, None, 0, 1000, 0, None, None, 1)
@@ -324,7 +349,7 @@ def test_latent_plane_layouts(lib):
     kvx.Layout(200, 1, 64, kvx.BF16, 10, base=FAKE, plane_stride=4096, kv_planes=1).close()
     l = kvx.lib()
     assert l.kvx_transfer(mla.handle, FAKE * 6, kv.handle, FAKE * 6, 10, FAKE * 4, 1 << 30,
-                          FAKE * 5, None) == kvx.ERR_INVALID_ARG
+                          FAKE * 5, kvx.DEFAULTS, None) == kvx.ERR_INVALID_ARG
 
 
 def test_stream_refuses_narrow_rows(lib):
@@ -335,7 +360,7 @@ def test_stream_refuses_narrow_rows(lib):
     c = kvx.StreamCtl()
     c.wait_ns = 1000
     rc = kvx.lib().kvx_stream(kvx.OP_TRANSFER, src.handle, FAKE * 6, dst.handle, FAKE * 6, 10,
-                              None, 0, ctypes.byref(c), FAKE * 4, 1 << 30, FAKE * 5, None)
+                              None, 0, ctypes.byref(c), FAKE * 4, 1 << 30, FAKE * 5, kvx.DEFAULTS, None)
     assert rc == kvx.ERR_ALIGNMENT
 
 
@@ -357,7 +382,8 @@ def test_stream_page_epochs_validation(lib):
     c.epoch_page = 0  # page size missing
     l = kvx.lib()
     args = lambda op, s, d: (op, s and s.handle, FAKE * 6, d and d.handle, FAKE * 6, 10, FAKE * 7,
-                             10 * 4 * 256, ctypes.byref(c), FAKE * 4, 1 << 30, FAKE * 5, None)
+                             10 * 4 * 256, ctypes.byref(c), FAKE * 4, 1 << 30, FAKE * 5,
+                             kvx.DEFAULTS, None)
     assert l.kvx_stream(*args(kvx.OP_TRANSFER, src, dst)) == kvx.ERR_INVALID_ARG
     c.epoch_page = 16
     assert l.kvx_stream(*args(kvx.OP_GATHER, src, None)) == kvx.ERR_INVALID_ARG  # no destination pool

@@ -40,6 +40,11 @@ MUTANTS = {
                                    "const int64_t req_end = n;"),
     "runs_src_step_of_two": ("src_idx[b] == src_idx[b - 1] + 1 &&", "src_idx[b] >= src_idx[b - 1] + 1 &&"),
     "batch_status_not_per_request": ("status[1 + q] = rc;", "status[1 + q] = 0;"),
+    "batch_dup_pairs_missed": ("if (count[dst_slots[r->dst_off + i]] > 1) {",
+                               "if (count[dst_slots[r->dst_off + i]] > 2) {"),
+    "batch_dup_counts_refused_requests": ("const int counted = status[1 + q] == KVXO_OK && r->op != KVXO_OP_GATHER;",
+                                          "const int counted = r->op != KVXO_OP_GATHER;"),
+    "batch_dup_check_ignored": ("if (check_dup && dst) {", "if (0 && dst) {"),
     "layers_one_short": ("for (int32_t layer = 0; layer < stop; ++layer)\n    for (int32_t kv = 0; kv < ppl; ++kv)\n      for (int64_t i = 0; i < n; ++i)\n        for",
                          "for (int32_t layer = 0; layer + 1 < stop; ++layer)\n    for (int32_t kv = 0; kv < ppl; ++kv)\n      for (int64_t i = 0; i < n; ++i)\n        for"),
     "layers_v_plane_dropped": ("    for (int32_t kv = 0; kv < ppl; ++kv)\n      for (int64_t i = 0; i < n; ++i)\n        for",
