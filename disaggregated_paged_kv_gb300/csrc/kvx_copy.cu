@@ -40,7 +40,7 @@ __device__ __forceinline__ int32_t copy_prologue(const CopyArgs &a, int32_t *s_t
   if (tid == 0) {
     int32_t ok = header_matches(a) ? 1 : 0;
     if (!ok && blockIdx.x == 0) atomicMax(&a.status[0], (int32_t)KVX_ERR_INVALID_ARG);
-    if (ok && a.mode != kModeBatch && load_status(a.status) != KVX_OK) ok = 0;
+    if (ok && a.mode != kModeBatch && a.status[0] != KVX_OK) ok = 0;
     *s_ok = ok;
   }
   __syncthreads();
@@ -93,7 +93,7 @@ __device__ __forceinline__ bool decode_item(const CopyArgs &a, uint32_t w,
   int64_t nreq = a.n_tokens;
   bool src_pool = a.src.is_pool, dst_pool = a.dst.is_pool;
   if (a.mode == kModeBatch) {
-    if (load_status(a.status + 1 + ch.req) != KVX_OK) return false;
+    if (a.status[1 + ch.req] != KVX_OK) return false;
     const kvx_request rq = a.reqs[ch.req];
     op = rq.op;
     bufp = a.buf + rq.buf_off;
@@ -257,13 +257,13 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
     }
     const Chunk ch = reinterpret_cast<const Chunk *>(a.ws + a.L.chunks_off)[t0];  // G == 1
     if (a.mode == kModeBatch) {
-      if (load_status(a.status + 1 + ch.req) != KVX_OK) return;
+      if (a.status[1 + ch.req] != KVX_OK) return;
       const kvx_request rq = a.reqs[ch.req];
       sp = (rq.op == KVX_OP_GATHER || rq.op == KVX_OP_TRANSFER);
       dp = (rq.op == KVX_OP_SCATTER || rq.op == KVX_OP_TRANSFER);
       bufp = a.buf + rq.buf_off;
       nreq = rq.n_tokens;
-    } else if (load_status(a.status) != KVX_OK) {
+    } else if (a.status[0] != KVX_OK) {
       return;
     }
     si = ch.src;
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
   }
   if constexpr (kSpec) {
     pdl_wait();  // the planner has checked every index of the request
-    const int32_t verdict = *reinterpret_cast<volatile const int32_t *>(a.status);
+    const int32_t verdict = a.status[0];
     if (verdict != KVX_OK) {
       if (reports(a)) report_host_status(a.host_status, verdict);
       return;

@@ -57,12 +57,6 @@ struct __align__(16) Chunk {
   int32_t rows;
 };
 
-// A status word that another kernel of the same call writes (the prefix kernel, the planner,
-// the duplicate check), read from L2.  A CTA that programmatic dependent launch started early
-// shares its SM's L1 with CTAs of those kernels, whose plain loads of the word can leave a copy
-// there that their later atomics (made in L2) do not refresh.
-__device__ __forceinline__ int32_t load_status(const int32_t *p) { return __ldcg(p); }
-
 // Byte offsets of the workspace sections; a pure function of the call's sizes, so the host
 // and every kernel agree on it.
 struct WsLayout {

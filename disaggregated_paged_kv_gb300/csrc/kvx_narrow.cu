@@ -49,7 +49,7 @@ __device__ __forceinline__ void move_rows(const CopyArgs &a, bool sp, const char
   }
   if (spec) {
     pdl_wait();  // the planner has checked every index of the request
-    if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK) return;
+    if (a.status[0] != KVX_OK) return;
   }
   if (!ok) return;
   for (int32_t v0 = li;;) {
@@ -104,13 +104,13 @@ __global__ void __launch_bounds__(kCopyThreads) copy_narrow_kernel(const __grid_
     const Chunk ch = reinterpret_cast<const Chunk *>(a.ws + a.L.chunks_off)[tt];  // one row each
     if (batch) {
       // tokens of one warp may belong to different requests: each lane follows its own
-      if (load_status(a.status + 1 + ch.req) != KVX_OK) ok = false;
+      if (a.status[1 + ch.req] != KVX_OK) ok = false;
       const kvx_request rq = a.reqs[ch.req];
       sp = (rq.op == KVX_OP_GATHER || rq.op == KVX_OP_TRANSFER);
       dp = (rq.op == KVX_OP_SCATTER || rq.op == KVX_OP_TRANSFER);
       bufp = a.buf + rq.buf_off;
       nreq = rq.n_tokens;
-    } else if (load_status(a.status) != KVX_OK) {
+    } else if (a.status[0] != KVX_OK) {
       return;
     }
     si = ch.src;

@@ -117,7 +117,7 @@ __device__ __forceinline__ Tok fetch(const PlanArgs &a, int64_t g, int32_t &seg)
     } else {
       t.req = seg;
       t.start = (off == 0);
-      if (load_status(a.status + 1 + seg) != KVX_OK) {  // bad record: never read its indices
+      if (a.status[1 + seg] != KVX_OK) {  // bad record: never read its indices
         t.s = t.d = off;
         t.live = false;
         return t;
@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(kDupThreads) dup_kernel(const __grid_constant_
         const int64_t off = g - pre[seg];
         if (a.mode == kModeRuns) {
           slot = (int64_t)a.runs[3 * (int64_t)seg + 1] + off;
-        } else if (load_status(a.status + 1 + seg) == KVX_OK) {
+        } else if (a.status[1 + seg] == KVX_OK) {
           const kvx_request r = a.reqs[seg];
           if (uses_dst_pool(r.op)) {
             slot = a.dst_idx[r.dst_off + off];

@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
     if (ok && xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, true, srow, xv << 4));
   }
   pdl_wait();  // the planner has checked both slot lists
-  if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK) return;
+  if (a.status[0] != KVX_OK) return;
   if (!ok) return;
   char *drow = const_cast<char *>(row_base<kDstHnd>(
       a.dst, true, plane_addr(a, a.parts[j].dst, p) + a.parts[j].dst_off, nullptr, di, R));
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
     if (ok && xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, true, srow, xv << 4));
   }
   pdl_wait();  // the planner has checked both slot lists and written status[0]
-  if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK || !ok) return;
+  if (a.status[0] != KVX_OK || !ok) return;
   if (k.page_epochs && !sops::page_owned(k, di)) {
     // the page went to another request: the row is dropped and reported
     atomicMax(&a.status[2], (int32_t)KVX_ERR_CANCELLED);
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kRsPersistThreads, 1)
       }
       if (!verdict_ok) {
         pdl_wait();  // the planner has checked both slot lists and written status[0]
-        if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK) {
+        if (a.status[0] != KVX_OK) {
           if (lane == 0) atomicMin(&cs.stop, 0);
           break;
         }

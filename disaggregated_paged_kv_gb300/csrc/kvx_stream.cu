@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
       }
       if (!verdict_ok) {  // the first row's load goes out before the planner's verdict
         pdl_wait();       // the planner has checked every index and written status[0]
-        if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK) {
+        if (a.status[0] != KVX_OK) {
           atomicMin(&cs.stop, 0);
           stop = true;
         }
@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
         bool stop = false;
         if (!verdict_ok) {  // the first group's loads go out before the planner's verdict
           pdl_wait();
-          if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK) {
+          if (a.status[0] != KVX_OK) {
             atomicMin(&cs.stop, 0);
             stop = true;
           }
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
         }
         if (!verdict_ok) {
           pdl_wait();  // the planner has checked every index and written status[0]
-          if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK) {
+          if (a.status[0] != KVX_OK) {
             if (lane == 0) atomicMin(&cs.stop, 0);
             break;
           }
@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
     if (ok && xv < vpr) v[u] = ld_stream(row_byte<kSrcHnd>(a.src, sp, srow, xv << 4));
   }
   pdl_wait();  // the planner has checked every index and written status[0]
-  if (*reinterpret_cast<volatile const int32_t *>(a.status) != KVX_OK || !ok) return;
+  if (a.status[0] != KVX_OK || !ok) return;
   if (dp && k.page_epochs && !page_owned(k, di)) {
     // the page went to another request: the row is dropped and reported
     atomicMax(&a.status[2], (int32_t)KVX_ERR_CANCELLED);
@@ -508,8 +508,8 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
 // the verdict and the "no further write" words are set.
 __global__ void stream_done_kernel(int32_t *status, int32_t *host_done, int32_t layers) {
   pdl_wait();
-  if (load_status(status) != KVX_OK) status[1] = layers;  // refused by the planner: nothing moved
-  const int32_t code = load_status(status + 2);
+  if (status[0] != KVX_OK) status[1] = layers;  // refused by the planner: nothing moved
+  const int32_t code = status[2];
   if (code) atomicMax(&status[0], code);
   status[2] = 0;
   __threadfence_system();
