@@ -169,7 +169,7 @@ struct CopyArgs {
   int32_t row_group_shift;  // narrow kernel: log2 of the tokens one warp moves
   int32_t row_lanes;        // row and streamed kernels: lanes per token (1 .. 32)
   int32_t rows_per_warp;    // tokens per warp (row_lanes * rows_per_warp <= 32)
-  // Row kernel order (plane-major): CTA c works on plane c / row_blocks, its warps on the
+  // Row and narrow kernel order (plane-major): CTA c works on plane c / row_blocks, its warps on the
   // consecutive token groups (c % row_blocks) * (kCopyThreads / 32) + warp, so neighbouring
   // CTAs stream through one plane's rows and a buffer side is read or written front to back.
   uint32_t row_blocks;      // CTAs per plane
@@ -276,7 +276,7 @@ constexpr int kBulkSmallTiles = 256;  // occupancy is cached for <= this many ti
 // Records e as this thread's kvx_last_cuda_error().
 void record_cuda_error(cudaError_t e);
 // Rows that do not allow 16-byte accesses (kvx_narrow.cu): one warp per (token, plane) row.
-cudaError_t launch_narrow(const CopyArgs &a, cudaStream_t s);
+cudaError_t launch_narrow(CopyArgs &a, cudaStream_t s);  // sets a.row_blocks
 // log2 of the tokens one warp of the narrow kernel moves (CopyArgs::row_group_shift).
 int32_t narrow_group_shift(int32_t row_bytes, int32_t vec_bytes);
 // One-launch path of small one-shot requests (kvx_small.cu): every CTA checks every index.

@@ -7,7 +7,9 @@
 // every address of the call allows, which the host works out from the layouts.
 //
 // One warp per group of 1 << g tokens of one plane (a power of two, unlike the row kernel of
-// kvx_copy.cu, which may give a token any number of lanes): 32 >> g
+// kvx_copy.cu, which may give a token any number of lanes), CTAs in plane-major order as the
+// row kernel's (measured on 200-byte rows of 16,384 random tokens: 159.3 -> 132.9 us; with all
+// writes in flight inside one plane, neighbouring rows' partial sectors meet in L2): 32 >> g
 // lanes per row, enough for the lane's kUnroll independent loads to cover the row
 // (narrow_group_shift).  One-shot calls read the slot lists, range-check them and load
 // before the planner's verdict; plans (one row per chunk, including a batch's request
@@ -72,10 +74,10 @@ __device__ __forceinline__ void move_rows(const CopyArgs &a, bool sp, const char
 template <bool kSrcHnd, bool kDstHnd>
 __global__ void __launch_bounds__(kCopyThreads) copy_narrow_kernel(const __grid_constant__ CopyArgs a) {
   const int lane = threadIdx.x & 31;
-  const uint32_t w = blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5);
-  const uint32_t P = (uint32_t)a.planes;
-  const uint32_t q = w / P;
-  const int32_t p = (int32_t)(w - q * P);
+  // plane-major CTAs, as the row kernel: CTA c works on plane c / row_blocks
+  const uint32_t pc = blockIdx.x / a.row_blocks;
+  const int32_t p = (int32_t)pc;
+  const uint32_t q = (blockIdx.x - pc * a.row_blocks) * (kCopyThreads / 32) + (threadIdx.x >> 5);
   const int32_t gsh = a.row_group_shift;  // 1 << gsh tokens per warp
   const int32_t lsh = 5 - gsh;            // 1 << lsh lanes per token
   const int64_t t0 = (int64_t)q << gsh;
@@ -98,7 +100,7 @@ __global__ void __launch_bounds__(kCopyThreads) copy_narrow_kernel(const __grid_
     pdl_wait();  // the plan is complete
     const bool batch = a.mode == kModeBatch;
     if (!header_matches(a)) {
-      if (w == 0 && lane == 0) atomicMax(&a.status[0], (int32_t)KVX_ERR_INVALID_ARG);
+      if (q == 0 && p == 0 && lane == 0) atomicMax(&a.status[0], (int32_t)KVX_ERR_INVALID_ARG);
       return;
     }
     const Chunk ch = reinterpret_cast<const Chunk *>(a.ws + a.L.chunks_off)[tt];  // one row each
@@ -149,7 +151,7 @@ int narrow_kernel_list(const void **out, int max) {
   return kernel_list_out(k, 4, out, max);
 }
 
-cudaError_t launch_narrow(const CopyArgs &a, cudaStream_t s) {
+cudaError_t launch_narrow(CopyArgs &a, cudaStream_t s) {
   // an HND side only matters where the request uses it as a pool
   const bool sh = a.src.hnd && (a.src.is_pool || a.mode == kModeBatch);
   const bool dh = a.dst.hnd && (a.dst.is_pool || a.mode == kModeBatch);
@@ -158,8 +160,9 @@ cudaError_t launch_narrow(const CopyArgs &a, cudaStream_t s) {
                  : dh       ? reinterpret_cast<const void *>(copy_narrow_kernel<false, true>)
                             : reinterpret_cast<const void *>(copy_narrow_kernel<false, false>);
   const int64_t groups = (a.n_tokens + (1 << a.row_group_shift) - 1) >> a.row_group_shift;
-  const int64_t warps = groups * a.planes;
-  const int64_t grid = (warps + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+  const int64_t wpb = kCopyThreads / 32;
+  a.row_blocks = (uint32_t)((groups + wpb - 1) / wpb);
+  const int64_t grid = (int64_t)a.row_blocks * a.planes;
   void *args[] = {const_cast<CopyArgs *>(&a)};
   return launch_pdl(fn, dim3((unsigned)grid), dim3(kCopyThreads), args, s);
 }
