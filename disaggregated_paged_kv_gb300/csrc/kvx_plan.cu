@@ -502,7 +502,10 @@ __global__ void __launch_bounds__(kDupThreads) dup_kernel(const __grid_constant_
         const int64_t off = g - pre[seg];
         if (a.mode == kModeRuns) {
           slot = (int64_t)a.runs[3 * (int64_t)seg + 1] + off;
-        } else if (a.status[1 + seg] == KVX_OK) {
+        } else if (const int32_t st = a.status[1 + seg];
+                   st == KVX_OK || st == KVX_ERR_DUPLICATE_DST) {
+          // accepted by the planner (a duplicate raised by this kernel meanwhile does not
+          // take a request's slots out of the check: the other requests naming them still fail)
           const kvx_request r = a.reqs[seg];
           if (uses_dst_pool(r.op)) {
             slot = a.dst_idx[r.dst_off + off];

@@ -240,3 +240,26 @@ def test_batch_duplicate_check_random(trial):
         if op != T:
             bo += n * R
     _check_batch(reqs, np.array(ss, np.int32), np.array(ds, np.int32), 600 + trial, num=300)
+
+
+@pytest.mark.parametrize("trial", range(8))
+def test_batch_duplicate_check_many_overlapping_requests(trial):
+    """Many requests whose destination slots overlap in chains (a request sharing one slot with
+    one request and another slot with a third), so that the check's inserts race with the
+    statuses it raises; statuses, pool and buffer against the oracle.  With requests of up to 200
+    tokens on 3000 slots nearly every request meets another; with up to 50 tokens on 20000
+    slots about a third of them move."""
+    g = _rng(700 + trial)
+    T, G, S = kvx.OP_TRANSFER, kvx.OP_GATHER, kvx.OP_SCATTER
+    R = 2 * SH["L"] * SH["H"] * SH["D"] * 2
+    num, longest = (3000, 200) if trial % 2 == 0 else (20000, 50)
+    reqs, ss, ds, bo = [], [], [], 0
+    for _ in range(40):
+        op = int(g.choice([T, T, T, S, G]))
+        n = int(g.integers(1, longest))
+        reqs.append((op, n, len(ss), len(ds), bo if op != T else 0))
+        ss += list(g.integers(0, num + (20 if g.random() < 0.05 else 0), n))
+        ds += list(g.choice(num, n, replace=False))
+        if op != T:
+            bo += n * R
+    _check_batch(reqs, np.array(ss, np.int32), np.array(ds, np.int32), 800 + trial, num=num)
