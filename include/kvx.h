@@ -72,7 +72,7 @@ typedef struct CUstream_st *kvx_stream_t;
 typedef enum kvx_status {
   KVX_OK = 0,
   KVX_ERR_INVALID_ARG = 1,   /* bad size, null pointer, inconsistent layouts or request */
-  KVX_ERR_ALIGNMENT = 2,     /* pointer or row size not 16-byte aligned */
+  KVX_ERR_ALIGNMENT = 2,     /* a pointer or size not aligned as the call needs */
   KVX_ERR_OUT_OF_RANGE = 3,  /* a slot / page index outside the pool (device status) */
   KVX_ERR_DUPLICATE_DST = 4, /* a destination slot named twice (device status; only checked
                                 with KVX_CHECK_DUP) */
@@ -162,12 +162,15 @@ typedef struct kvx_layout_desc {
   int64_t num_slots;  /* token slots per plane; HND: a multiple of page_size */
   /* Plane addresses: either plane_ptrs (host array of P = kv_planes * L device pointers, read
    * during kvx_layout_create and not kept) or, when plane_ptrs is NULL, plane p at
-   * base + p * plane_stride.  Every plane address must be 16-byte aligned. */
+   * base + p * plane_stride.  Every plane address must be a multiple of the element size.
+   * Rows move in the widest access (16, 8, 4, 2 or 1 bytes) that divides R, every plane
+   * address, the slot stride (KVX_NHD) and the head vector (KVX_HND_PAGED): 16 for the usual
+   * shapes; kvx_stream, kvx_stream_reshard, kvx_move_heads and kvx_reshard need 16. */
   void *const *plane_ptrs;
   void *base;
   int64_t plane_stride;
-  /* KVX_NHD: bytes from slot s to slot s+1 within a plane; 0 means R (dense rows).  Must be a
-   * multiple of 16 and >= R.  KVX_HND_PAGED: must be 0. */
+  /* KVX_NHD: bytes from slot s to slot s+1 within a plane; 0 means R (dense rows).  Must be
+   * >= R.  KVX_HND_PAGED: must be 0. */
   int64_t slot_stride;
   /* Planes per layer: 2 (K and V; 0 also means 2) or 1 -- one latent vector per layer and
    * token (MLA: [mini-infer] "KV 传输大小", latent + rope in a single plane).  With 1, plane p
@@ -198,8 +201,8 @@ typedef struct kvx_request {
 /* ---- layouts ------------------------------------------------------------------------ */
 
 /* Validates desc and creates a host-only handle (no device memory).  Errors:
- * KVX_ERR_INVALID_ARG (bad field), KVX_ERR_ALIGNMENT (R, head bytes for HND, slot stride or a
- * plane address not a multiple of 16). */
+ * KVX_ERR_INVALID_ARG (bad field), KVX_ERR_ALIGNMENT (a plane address not a multiple of the
+ * element size). */
 KVX_API kvx_status kvx_layout_create(const kvx_layout_desc *desc, kvx_layout_t *out);
 KVX_API kvx_status kvx_layout_destroy(kvx_layout_t layout);
 /* R, the bytes of one (plane, token) row; -1 for a NULL handle. */
@@ -504,7 +507,9 @@ typedef struct kvx_stream_ctl {
  * and ends by ctl->wait_ns, so the kernel always finishes.
  * May be captured into a CUDA graph: every replay is a new call (it reads the slot lists,
  * the control words and the workspace afresh and keeps nothing from an earlier replay); the
- * host-side checks and the control block's values are those of the captured call. */
+ * host-side checks and the control block's values are those of the captured call.
+ * Layouts whose rows do not move in 16-byte accesses (see kvx_layout_desc) are
+ * KVX_ERR_ALIGNMENT. */
 KVX_API kvx_status kvx_stream(int32_t op, kvx_layout_t src, const int32_t *d_src_slots,
                               kvx_layout_t dst, const int32_t *d_dst_slots, int32_t n,
                               void *d_buf, size_t buf_bytes, const kvx_stream_ctl *ctl,
