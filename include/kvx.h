@@ -165,7 +165,7 @@ typedef struct kvx_layout_desc {
    * base + p * plane_stride.  Every plane address must be a multiple of the element size.
    * Rows move in the widest access (16, 8, 4, 2 or 1 bytes) that divides R, every plane
    * address, the slot stride (KVX_NHD) and the head vector (KVX_HND_PAGED): 16 for the usual
-   * shapes; kvx_stream, kvx_stream_reshard, kvx_move_heads and kvx_reshard need 16. */
+   * shapes; kvx_stream, kvx_reshard and kvx_stream_reshard need 16. */
   void *const *plane_ptrs;
   void *base;
   int64_t plane_stride;
@@ -368,8 +368,8 @@ KVX_API kvx_status kvx_tp_slice(int32_t kv_heads, int32_t src_tp, int32_t src_ra
  * [head_dim] (buf_bytes >= P * n * n_heads * head_dim * elem); a scatter reads that form.
  * Arguments, workspace, status and errors otherwise as kvx_gather / kvx_scatter /
  * kvx_transfer (src_head0 is ignored by a scatter, dst_head0 by a gather); a head range outside
- * a layout's kv_heads is KVX_ERR_INVALID_ARG, and a range whose bytes do not start and end on
- * 16-byte boundaries within a row is KVX_ERR_ALIGNMENT. */
+ * a layout's kv_heads is KVX_ERR_INVALID_ARG.  A range whose bytes do not start and end on
+ * 16-byte boundaries within a row moves in the widest access its offsets and length allow. */
 KVX_API kvx_status kvx_move_heads(int32_t op, kvx_layout_t src, const int32_t *d_src_slots,
                                   int32_t src_head0, kvx_layout_t dst,
                                   const int32_t *d_dst_slots, int32_t dst_head0,

@@ -361,3 +361,287 @@ def test_fuzz_case(k):
         hz.assert_same_bytes(src.readback(), src.host, what + ": source pool")
     if uses_buf:
         hz.assert_same_bytes(buf.cpu().numpy(), exp_buf, what + ": buffer")
+
+
+# ---------------------------------------------------------------------------------------
+# the layer-streamed and head-range calls
+# ---------------------------------------------------------------------------------------
+# kvx_stream and kvx_stream_reshard with every layer ready (ready words already raised in
+# device or pinned host memory, or none), live epoch words and owned pages, on the row grid or
+# a persistent grid capped at 1 ... 152 CTAs; kvx_move_heads between layouts of different head
+# counts (narrow head slices included); kvx_reshard between random TP groups.  A call that
+# waits on nothing unraised is deterministic, so it is compared like the one-shot calls.
+
+N_LAYERED = 240
+LCALLS = ["stream", "move_heads", "reshard", "stream_reshard"]
+LCALL_P = [0.4, 0.25, 0.2, 0.15]
+GRIDS = [0, 0, 1, 3, 19, 76, 152]
+TPS = [1, 2, 4, 8]
+
+
+@dataclass
+class LCase:
+    k: int
+    dtype: str
+    L: int
+    D: int
+    kvp: int
+    call: str
+    op: str
+    flags: Optional[int]
+    defaults: tuple
+    heads: tuple             # (source kv_heads, destination kv_heads) of every pool
+    src: Optional[Side]      # a kind and slot count shared by every source pool
+    dst: Optional[Side]
+    s: np.ndarray
+    d: np.ndarray
+    plant: str
+    h0: int = 0              # move_heads: the head range
+    g0: int = 0
+    nh: int = 0
+    tp: tuple = (1, 1)       # reshard: (P group size, D group size)
+    H: int = 0               # reshard: the kv heads the TP groups shard
+    ctl: dict = field(default_factory=dict)
+
+    @property
+    def n(self) -> int:
+        return len(self.s) if self.op != "scatter" else len(self.d)
+
+    @property
+    def check_dup(self) -> bool:
+        return bool(self.defaults[0]) if self.flags is None else bool(self.flags & CHECK_DUP)
+
+
+def _shard_heads(heads, t):
+    return heads // t if t <= heads else 1
+
+
+def draw_layered(k: int) -> LCase:
+    g = np.random.Generator(np.random.PCG64(51000 + k))
+    dtype = str(g.choice(["fp8", "fp16", "bf16"]))
+    e = inputs.ELEM_BYTES[dtype]
+    call = str(g.choice(LCALLS, p=LCALL_P))
+    # whole 16-byte head vectors, except for the head-range move, which also takes narrow ones
+    Ds = [8, 16, 24, 36, 64, 100, 128] if call == "move_heads" else \
+        [d for d in (8, 16, 24, 32, 64, 128) if d * e % 16 == 0]
+    D = int(g.choice(Ds))
+    L = int(g.choice([1, 2, 3, 5]))
+    kvp = 1 if g.random() < 0.25 else 2
+    op = str(g.choice(["gather", "scatter", "transfer"])) if call in ("stream", "move_heads") \
+        else "transfer"
+    flags = [None, 0, 1, 2, 4, 1 | 2, 1 | 4][int(g.integers(0, 7))]
+    defaults = (int(g.integers(0, 2)), int(g.integers(0, 3)), 0)
+    tp = (1, 1)
+    h0 = g0 = nh = 0
+    if call in ("reshard", "stream_reshard"):
+        H = int(g.choice([1, 2, 4, 8]))
+        tp = (int(g.choice(TPS)), int(g.choice(TPS)))
+        heads = (_shard_heads(H, tp[0]), _shard_heads(H, tp[1]))
+        pools = tp[0] + tp[1]
+    elif call == "move_heads":
+        heads = (int(g.integers(1, 9)), int(g.integers(1, 9)))
+        nh = int(g.integers(1, min(heads) + 1)) if op == "transfer" else \
+            int(g.integers(1, (heads[0] if op == "gather" else heads[1]) + 1))
+        h0 = int(g.integers(0, heads[0] - nh + 1)) if op != "scatter" else 0
+        g0 = int(g.integers(0, heads[1] - nh + 1)) if op != "gather" else 0
+        pools = 2
+    else:
+        H = int(g.choice([1, 2, 4, 8]))
+        heads = (H, H)
+        pools = 2
+    R = max(heads) * D * e
+    cap_slots = max(64, (POOL_CAP // pools) // (kvp * L * R))
+    bucket = g.choice(["zero", "tiny", "small", "mid", "large"], p=[0.03, 0.17, 0.3, 0.3, 0.2])
+    n = {"zero": 0, "tiny": int(g.integers(1, 17)), "small": int(g.integers(17, 513)),
+         "mid": int(g.integers(513, 2100)), "large": int(g.integers(2100, 5000))}[bucket]
+    n = min(n, cap_slots // 2 - 8)
+    num = int(min(cap_slots, max(64, int(n * g.uniform(2.0, 4.0)) + 16)))
+    num -= num % 16
+    src = Side(str(g.choice(KINDS)), num, 16) if op != "scatter" else None
+    dst = Side(str(g.choice(KINDS)), num, int(g.choice([1, 4, 16]))) if op != "gather" else None
+    if src is not None and src.kind != "hnd":
+        src.ps = 1
+    if dst is not None and dst.kind != "hnd":
+        dst.ps = 1
+    c = LCase(k, dtype, L, D, kvp, call, op, flags, defaults, heads, src, dst,
+              np.zeros(0, np.int32), np.zeros(0, np.int32), "none", h0, g0, nh, tp,
+              H if call in ("reshard", "stream_reshard") else 0)
+    if src is not None:
+        c.s = _slots(g, n, num, distinct=g.random() < 0.85)
+    if dst is not None:
+        c.d = _slots(g, n, num)
+    if call in ("stream", "stream_reshard"):
+        c.ctl = dict(ready=str(g.choice(["none", "device", "pinned"])),
+                     ready_value=int(g.integers(1, 6)),
+                     epoch=str(g.choice(["none", "device", "pinned"])),
+                     epoch_value=int(g.integers(0, 1000)),
+                     owners=str(g.choice(["none", "device"])) if dst is not None else "none",
+                     epoch_page=int(g.choice([1, 16, 64])),
+                     done=bool(g.random() < 0.5),
+                     max_ctas=int(g.choice(GRIDS)))
+    if n > 0:
+        u = g.random()
+        if u < 0.15:
+            c.plant = "oor"
+        elif u < 0.5 and c.check_dup and dst is not None and n >= 2:
+            c.plant = "dup"
+    _plant(g, c)
+    return c
+
+
+def test_fuzz_layered_cases_draw():
+    """Every layered case draws well formed: streamed and reshard cases on whole 16-byte head
+    vectors, head ranges inside both layouts, distinct destination slots unless a duplicate is
+    planted under the check."""
+    calls = set()
+    for k in range(N_LAYERED):
+        c = draw_layered(k)
+        calls.add(c.call)
+        e = inputs.ELEM_BYTES[c.dtype]
+        if c.call != "move_heads":
+            assert c.D * e % 16 == 0
+        else:
+            if c.op != "scatter":
+                assert 0 <= c.h0 and c.h0 + c.nh <= c.heads[0]
+            if c.op != "gather":
+                assert 0 <= c.g0 and c.g0 + c.nh <= c.heads[1]
+        if c.dst is not None and c.plant != "dup":
+            inr = c.d[(c.d >= 0) & (c.d < c.dst.num)]
+            assert len(np.unique(inr)) == len(inr), k
+        for side in (c.src, c.dst):
+            if side is not None:
+                assert side.num % side.ps == 0
+    assert calls == set(LCALLS)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("k", range(N_LAYERED))
+def test_fuzz_layered_case(k):
+    torch = pytest.importorskip("torch")
+    from disaggregated_paged_kv_gb300 import kvx
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    c = draw_layered(k)
+    g = np.random.Generator(np.random.PCG64(61000 + k))
+    n, e = c.n, inputs.ELEM_BYTES[c.dtype]
+    P = c.kvp * c.L
+
+    def mirror(side, H, fill, salt):
+        return hz.make_mirror(side.kind, c.L, H, c.D, c.dtype, side.num, side.ps, fill,
+                              g if fill == "normal" else None, salt=salt, kvp=c.kvp)
+
+    resh = c.call in ("reshard", "stream_reshard")
+    n_src = c.tp[0] if resh else (1 if c.src else 0)
+    n_dst = c.tp[1] if resh else (1 if c.dst else 0)
+    srcs = [mirror(c.src, c.heads[0], "normal", 0).to_device() for _ in range(n_src)]
+    dsts = [mirror(c.dst, c.heads[1], "sentinel", 5 + r).to_device() for r in range(n_dst)]
+    exps = [mirror(c.dst, c.heads[1], "sentinel", 5 + r) for r in range(n_dst)]
+    rows = c.nh if c.call == "move_heads" else c.heads[0] if c.op != "scatter" else c.heads[1]
+    uses_buf = c.op != "transfer"
+    buf_n = P * n * rows * c.D * e if uses_buf else 0
+    buf = exp_buf = bufp = None
+    if uses_buf:
+        raw = g.integers(0, 256, 2 * hz.GUARD + max(16, buf_n), dtype=np.uint8)
+        buf = torch.from_numpy(raw).cuda()
+        exp_buf = raw.copy()
+        bufp = hz.GUARD + buf.data_ptr()
+    body = exp_buf[hz.GUARD:hz.GUARD + max(16, buf_n)] if uses_buf else None
+    parts = kvx.tp_plan(c.H, c.tp[0], c.tp[1]) if resh else []
+
+    # the oracle's result.  A planted repeat (always under the check) must fail with nothing
+    # moved: the oracle's head-range and reshard moves have no duplicate check, so that case
+    # expects untouched destinations without running them.
+    op_code = OP[c.op]
+    if c.plant == "dup":
+        rc = kvx.ERR_DUPLICATE_DST
+    elif resh:
+        rc = oracle.reshard([hz.oracle_pool(m) for m in srcs], c.s,
+                            [hz.oracle_pool(m) for m in exps], c.d, parts, n)[0]
+    elif c.call == "move_heads":
+        sp = hz.oracle_pool(srcs[0]) if srcs else None
+        dp = hz.oracle_pool(exps[0]) if dsts else None
+        rc, out, _ = oracle.move_heads(op_code, sp, c.s if len(c.s) else None, c.h0, dp,
+                                       c.d if len(c.d) else None, c.g0, c.nh, n,
+                                       buf=body if c.op == "scatter" else None)
+        if c.op == "gather" and rc == oracle.OK and n:
+            exp_buf[hz.GUARD:hz.GUARD + buf_n] = out[:buf_n]
+    elif c.op == "gather":
+        rc, out, _ = oracle.gather(hz.oracle_pool(srcs[0]), c.s)
+        if rc == oracle.OK and n:
+            exp_buf[hz.GUARD:hz.GUARD + buf_n] = out
+    elif c.op == "scatter":
+        rc = oracle.scatter(hz.oracle_pool(exps[0]), c.d, body)[0]
+    else:
+        rc = oracle.transfer(hz.oracle_pool(srcs[0]), c.s, hz.oracle_pool(exps[0]), c.d)[0]
+    if n == 0:
+        rc = kvx.OK
+
+    if c.flags is None:
+        kvx.set_check_duplicates(bool(c.defaults[0]))
+        kvx.set_copy_engine(c.defaults[1])
+    keep = []
+    try:
+        sls = [hz.kvx_layout(m) for m in srcs]
+        dls = [hz.kvx_layout(m) for m in dsts]
+        s_d = hz.dev_i32(c.s) if len(c.s) else None
+        d_d = hz.dev_i32(c.d) if len(c.d) else None
+        ws = hz.workspace(n)
+        f = c.flags
+        streamed = c.call in ("stream", "stream_reshard")
+        st = hz.status(4 if streamed else 1)
+        kw = {}
+        if streamed:
+            ct = c.ctl
+
+            def word(where, values):
+                t = torch.tensor(values, dtype=torch.int32)
+                t = t.cuda() if where == "device" else t.pin_memory()
+                keep.append(t)
+                return t
+
+            if ct["ready"] != "none":
+                kw["layer_ready"] = word(ct["ready"], [ct["ready_value"]] * c.L)
+                kw["ready_value"] = ct["ready_value"]
+            if ct["epoch"] != "none":
+                kw["epoch_word"] = word(ct["epoch"], [ct["epoch_value"]])
+            kw["epoch"] = ct["epoch_value"]
+            if ct["owners"] != "none":
+                pages = -(-c.dst.num // ct["epoch_page"])
+                kw["dst_page_epochs"] = word("device", [ct["epoch_value"]] * pages)
+                kw["epoch_page"] = ct["epoch_page"]
+            if ct["done"]:
+                kw["host_done"] = word("pinned", [0])
+            kw["max_ctas"] = ct["max_ctas"]
+            kw["wait_ns"] = 2_000_000_000
+        if c.call == "stream":
+            kvx.stream(op_code, sls[0] if sls else None, s_d, dls[0] if dls else None, d_d, n,
+                       bufp, ws, st, buf_bytes=buf_n, flags=f, **kw)
+        elif c.call == "stream_reshard":
+            kvx.stream_reshard(sls, s_d, dls, d_d, parts, n, ws, st, flags=f, **kw)
+        elif c.call == "reshard":
+            kvx.reshard(sls, s_d, dls, d_d, parts, n, ws, st, flags=f)
+        else:
+            kvx.move_heads(op_code, sls[0] if sls else None, s_d, c.h0, dls[0] if dls else None,
+                           d_d, c.g0, c.nh, n, bufp, ws, st, buf_bytes=buf_n, flags=f)
+        torch.cuda.synchronize()
+        got = st.cpu().numpy().tolist()
+    finally:
+        kvx.set_check_duplicates(False)
+        kvx.set_copy_engine(kvx.ENGINE_AUTO)
+
+    what = f"case {k}: {c.call} {c.op} {c.dtype} L{c.L} D{c.D} heads {c.heads} kvp{c.kvp} " \
+           f"n{n} flags {c.flags} plant {c.plant} tp {c.tp} heads {c.h0}/{c.g0}/{c.nh} " \
+           f"src {c.src} dst {c.dst} ctl {c.ctl}"
+    if streamed:
+        assert got[0] == rc and got[3] == 1, (got, rc, what)
+        assert got[1] == (0 if rc == kvx.OK else c.L), (got, rc, what)
+        if c.ctl.get("done"):
+            assert int(kw["host_done"][0]) == 1, what
+    else:
+        assert got == [rc], (got, rc, what)
+    for r, (m, x) in enumerate(zip(dsts, exps)):
+        hz.assert_same_bytes(m.readback(), x.host, f"{what}: destination pool {r}")
+    for r, m in enumerate(srcs):
+        hz.assert_same_bytes(m.readback(), m.host, f"{what}: source pool {r}")
+    if uses_buf:
+        hz.assert_same_bytes(buf.cpu().numpy(), exp_buf, what + ": buffer")
