@@ -614,6 +614,23 @@ def measure_workload(args, name: str, min_seconds: float = 0.25):
     cres = timed(max(3, min(K, 200)), legs=copy_leg)
     line["contiguous_copy_us_per_leg"] = statistics.mean(r[0] for r in cres) * 1e3
     del ca, cb
+    if name == "small_gather_scatter":
+        # a launch-bound leg's floors under the same timing: an elementwise kernel reading and
+        # writing the leg's bytes (the device copy above goes through the copy engine, whose
+        # setup alone is longer here), and a kernel that touches one element
+        ka = torch.zeros(payload // 2, dtype=torch.float16, device=dev)
+        kb = torch.empty_like(ka)
+        one = torch.zeros(1, dtype=torch.float32, device=dev)
+        floors = {}
+        for fname, fn in (("kernel_copy", lambda: torch.add(ka, 0, out=kb)),
+                          ("one_element_kernel", lambda: one.add_(1))):
+            leg = [(fname, fn, 0)]
+            timed(3, legs=leg)
+            floors[fname + "_us"] = statistics.mean(r[0] for r in timed(max(3, min(K, 200)), legs=leg)) * 1e3
+        floors["how"] = ("event-to-event time of one torch kernel per step after the same flush: "
+                         "an elementwise copy of one leg's bytes, and a one-element add")
+        line["launch_floor_per_leg"] = floors
+        del ka, kb, one
     if name == "fragmented":
         # the same request on the first 4 layers only (8 planes): ~7,700 fragments per direction
         L4 = 4
@@ -692,7 +709,7 @@ def workload_summaries(args):
                      "frac_of_nominal_8tbs": cfg["frac_of_nominal_8tbs"],
                      "legs": ln["legs"], "steps": ln["steps"], "clocks": ln["clocks"],
                      "contiguous_copy_us_per_leg": ln["contiguous_copy_us_per_leg"]}
-        for extra in ("four_layers", "warm_l2", "cuda_graph"):
+        for extra in ("four_layers", "warm_l2", "cuda_graph", "launch_floor_per_leg"):
             if extra in ln:
                 out[name][extra] = ln[extra]
     torch.cuda.empty_cache()
