@@ -512,9 +512,7 @@ __global__ void stream_done_kernel(int32_t *status, int32_t *host_done, int32_t 
   const int32_t code = status[2];
   if (code) atomicMax(&status[0], code);
   status[2] = 0;
-  __threadfence_system();
-  st_release_sys(&status[3], 1);
-  if (host_done) st_release_sys(host_done, 1);
+  publish_done(&status[3], host_done);
 }
 
 template <bool kTail>
