@@ -6,6 +6,8 @@
   source row, on the device -- plus the gather of the same request.
 - KVX_MAX_PLANES (256) planes, as 128 layers x K/V and as 256 latent planes: whole pools.
 - A reshard whose layouts bring exactly KVX_RESHARD_MAX_PLANE_TABLE uneven plane addresses.
+- The last slots of the largest pool a layout may describe (INT32_MAX slots of 16 bytes, token
+  rows and HND pages), and the first slot past them.
 """
 import numpy as np
 import pytest
@@ -137,3 +139,84 @@ def test_reshard_full_plane_table():
     with pytest.raises(kvx.KvxError):
         kvx.reshard([hz.kvx_layout(x) for x in srcs + [extra]], hz.dev_i32(s),
                     [hz.kvx_layout(dst)], hz.dev_i32(d), parts, n, hz.workspace(n), hz.status())
+
+
+def _sampled_oracle_rows(src, s, m_idx, R):
+    """The oracle's transfer of the sampled tokens m_idx between mini pools built from the
+    sampled source rows (the pools themselves are too large to mirror on the host)."""
+    rows = src[torch.from_numpy(s[m_idx]).long().cuda()].cpu().numpy().view(np.uint8).reshape(-1)
+    m = len(m_idx)
+    out = np.full(m * R, 0xFF, dtype=np.uint8)
+    sp = oracle.Pool(1, 1, R // 2, 2, oracle.TOKEN_ROWS, m, [(rows, 0)], R, kv_planes=1)
+    dp = oracle.Pool(1, 1, R // 2, 2, oracle.TOKEN_ROWS, m, [(out, 0)], R, kv_planes=1)
+    assert oracle.transfer(sp, np.arange(m), dp, np.arange(m))[0] == oracle.OK
+    return out
+
+
+@pytest.mark.parametrize("kind", ["planes", "hnd"])
+def test_top_slot_of_the_largest_pool(kind):
+    """A pool of the most slots a layout may have (num_slots = INT32_MAX, or the largest
+    multiple of the page size below it for HND pages of 16): 16-byte rows, one plane of 32 GiB
+    per side.  The request names the last slots of both pools (byte offsets past 2^35), slot 0
+    and random slots; every destination row is checked on the device (the moved rows equal
+    their source rows, every other row keeps its sentinel), sampled rows against the oracle,
+    and the gather of the same slots.  Slot INT32_MAX itself is one past the end: refused,
+    nothing moved."""
+    ps = 16 if kind == "hnd" else 1
+    num = (2 ** 31 - 1) // ps * ps
+    R = 16
+    n = 4096
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    src = torch.randint(-2 ** 31, 2 ** 31 - 1, (num, R // 4), dtype=torch.int32, device="cuda",
+                        generator=g)
+    dst = torch.full((num, R // 4), -1, dtype=torch.int32, device="cuda")
+    rng = _rng(40 + ps)
+    top = np.arange(num - 8, num, dtype=np.int64)  # the last eight slots, and slot 0
+    s = rng.permutation(np.concatenate([top, [0], rng.integers(0, num, n - 9)])).astype(np.int32)
+    others = rng.permutation(np.unique(rng.integers(1, num - 8, 2 * n)))[:n - 9]
+    d = rng.permutation(np.concatenate([top, [0], others])).astype(np.int32)
+    assert len(d) == n and len(np.unique(d)) == n and d.max() == num - 1 and s.max() == num - 1
+
+    def layout(t):
+        if kind == "hnd":
+            return kvx.Layout(1, 1, 8, kvx.F16, num, kind=kvx.HND_PAGED, page_size=ps, base=t,
+                              plane_stride=num * R, kv_planes=1)
+        return kvx.Layout(1, 1, 8, kvx.F16, num, base=t, plane_stride=num * R, kv_planes=1)
+
+    sl, dl = layout(src), layout(dst)
+    s_d, d_d = torch.from_numpy(s).cuda(), torch.from_numpy(d).cuda()
+    ws = torch.empty(kvx.workspace_size(n, 0), dtype=torch.uint8, device="cuda")
+    st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    kvx.transfer(sl, s_d, dl, d_d, n, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvx.OK
+    # with one head and one plane, a slot's row is contiguous in both kinds: HND page p holds
+    # tokens p*16 .. p*16+15 one after another (one head), so row i of the tensor is slot i
+    assert torch.equal(dst[d_d.long()], src[s_d.long()])
+    moved = dst[d_d.long()].clone()
+    dst[d_d.long()] = -1
+    assert bool((dst == -1).all()), "a row outside the request changed"
+    dst[d_d.long()] = moved
+    samp = np.unique(np.concatenate([np.flatnonzero(s >= num - 8), np.flatnonzero(d >= num - 8),
+                                     rng.choice(n, 300, replace=False)]))
+    want = _sampled_oracle_rows(src, s, samp, R)
+    got = dst[torch.from_numpy(d[samp]).long().cuda()].cpu().numpy().view(np.uint8).reshape(-1)
+    assert np.array_equal(got, want)
+    # the gather of the same slots: buffer row i is source row s[i]
+    buf = torch.empty((n, R // 4), dtype=torch.int32, device="cuda")
+    kvx.gather(sl, s_d, n, buf, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvx.OK
+    assert torch.equal(buf, src[s_d.long()])
+    # one past the end (INT32_MAX for token rows): refused, nothing moved
+    bad = d.copy()
+    bad[n // 2] = num
+    before = dst[d_d.long()].clone()
+    dst2_rows = torch.from_numpy(bad).cuda()
+    kvx.transfer(sl, s_d, dl, dst2_rows, n, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvx.ERR_OUT_OF_RANGE
+    assert torch.equal(dst[d_d.long()], before)
+    del src, dst, buf
+    torch.cuda.empty_cache()
