@@ -22,9 +22,10 @@ from tests import inputs
 N_CASES = 600
 POOL_CAP = 24 << 20  # bytes per pool
 KINDS = ["planes", "planes_rotated", "slot_major", "hnd"]
-CALLS = ["gather", "scatter", "transfer", "gather_runs", "scatter_runs", "transfer_runs",
-         "batch", "plan_execute", "submit", "noalloc"]
-CALL_P = [0.12, 0.12, 0.16, 0.07, 0.07, 0.08, 0.14, 0.1, 0.07, 0.07]
+# oneshot: kvx_gather / kvx_scatter / kvx_transfer by the case's op
+CALLS = ["oneshot", "gather_runs", "scatter_runs", "transfer_runs", "batch", "plan_execute",
+         "submit", "noalloc"]
+CALL_P = [0.40, 0.07, 0.07, 0.08, 0.14, 0.10, 0.07, 0.07]
 # per-call option words (None: KVX_DEFAULTS with random process-wide defaults)
 FLAG_CHOICES = [None, 0, 1, 2, 4, 8, 1 | 2, 1 | 4, 1 | 8, 2 | 8, 4 | 8]
 CHECK_DUP = 1
@@ -114,7 +115,7 @@ def draw(k: int) -> Case:
     g = np.random.Generator(np.random.PCG64(31000 + k))
     dtype = str(g.choice(["fp8", "fp16", "bf16"]))
     H = int(g.choice([1, 2, 3, 4, 8]))
-    D = int(g.choice([8, 16, 24, 36, 64, 100, 128]))
+    D = int(g.choice([1, 3, 8, 16, 24, 36, 64, 100, 128]))  # rows of 1 byte to 2 KiB
     L = int(g.choice([1, 2, 3, 5]))
     kvp = 1 if g.random() < 0.25 else 2
     call = str(g.choice(CALLS, p=CALL_P))
@@ -306,7 +307,7 @@ def test_fuzz_case(k):
         nst = len(c.reqs) + 1 if c.call == "batch" else 1
         st = hz.status(nst)
         f = c.flags
-        if c.call in ("gather", "scatter", "transfer"):
+        if c.call == "oneshot":
             ws = hz.workspace(n)
             if c.op == "gather":
                 kvx.gather(sl, s_d, n, bufp, ws, st, buf_bytes=buf_n, flags=f)
