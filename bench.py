@@ -14,6 +14,11 @@ Metric: GB/s moved = (payload read + payload written + index bytes) / device tim
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+At N = 1 the line also summarises, each with its own clock record, the other workloads
+(`config.workloads`: small gather + scatter-back, fragmented pools, a 64-request batch, the HND
+permute and rebuild) and the streamed move, the TP reshards and the other formats
+(`config.next_rows`); --workload NAME prints any one of them alone.
+
 --impl reference times the CPU oracle (single-threaded, as it stands) on a bounded sample of
 the same workload on the host cores.  Under torchrun (N > 1) every rank runs an independent
 replica on its own GPU (no data-path collective); rank 0 prints one JSON line.
@@ -67,6 +72,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
                     help="headline line only: skip the other four workloads' summaries")
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="skip the summaries of the streamed, TP-reshard and format workloads")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--pool-slots", type=int, default=SLOTS,
                     help="slots per plane of both pools (smaller pools for profiler captures; "
@@ -991,6 +998,10 @@ def run_sizes(args):
 
 
 def run_formats(args):
+    print(json.dumps(measure_formats(args)), flush=True)
+
+
+def measure_formats(args):
     """Pool-to-pool transfers of one request of random slots in other layouts and dtypes, each
     timed like the headline (L2 flushed before every step, CUDA events around kvx_transfer):
       mla_bf16   DeepSeek-V2-Lite-shaped MLA latent rows (27 layers x 576 bf16 = 1152 B),
@@ -1126,10 +1137,14 @@ def run_formats(args):
         "formats": results,
         "gpu_launches": 2 * args.steps,
     }
-    print(json.dumps(line), flush=True)
+    return line
 
 
 def run_tp(args):
+    print(json.dumps(measure_tp(args)), flush=True)
+
+
+def measure_tp(args):
     """The headline request (2048 random tokens, 36 layers x K/V x 8 kv heads x 128 bf16) moved
     between tensor-parallel groups of different sizes: for every (P rank, D rank) pair the heads
     kvx_tp_slice assigns it, one kvx_move_heads transfer each, each pair on its own stream
@@ -1313,10 +1328,14 @@ def run_tp(args):
         "reshards": results,
         "gpu_launches": 2 * args.steps,
     }
-    print(json.dumps(line), flush=True)
+    return line
 
 
 def run_stream(args):
+    print(json.dumps(measure_stream(args)), flush=True)
+
+
+def measure_stream(args):
     """The headline transfer through kvx_stream.  (1) Every layer ready: device time of
     memset + planner + streamed copy per step, L2 flushed before each step.  (2) Layers raised
     by the host at a fixed cadence (an emulated prefill producing one layer every --layer-us):
@@ -1518,7 +1537,58 @@ def run_stream(args):
         "clocks": clk,
         "gpu_launches": 3 * K,  # validating planner, streamed row grid, epilogue
     }
-    print(json.dumps(line), flush=True)
+    return line
+
+
+def next_row_summaries(args):
+    """The layer-streamed move, the TP reshards and the other formats, each measured as by
+    --workload stream / tp / formats (at most 200 timed steps per measurement), with the SM
+    clocks sampled over each, and summarised for the headline line."""
+    import torch
+
+    sub = argparse.Namespace(**vars(args))
+    sub.steps = min(args.steps, 200)
+    sub.warmup = max(3, min(args.warmup, 10))
+    out = {}
+    for name, fn in (("stream", measure_stream), ("tp", measure_tp), ("formats", measure_formats)):
+        torch.cuda.empty_cache()
+        clocks = Clocks(0, not args.no_clocks)
+        ln = fn(sub)
+        clk = clocks.stop()
+        if name == "stream":
+            ar = ln["all_ready"]
+            pg = ln["all_ready_persistent_grid"]
+            out[name] = {
+                "all_ready_us": ar["us_per_request"], "GBs": ar["GBs"],
+                "frac_of_measured_hbm": ar["frac_of_measured_hbm"],
+                "all_ready_device_words_us": ln["all_ready_device_words_us"],
+                "persistent_grid_mixed_us": dict(zip(map(str, pg["ctas"]), pg["mixed_us"])),
+                "request_epoch_checked_us": ln["all_ready_request_epoch_checked_us"],
+                "page_owners_checked_us": ln["all_ready_page_owners_checked_us"],
+                "tail_after_last_layer_us": ln["streamed_tail_us"],
+                "unstreamed_us": ln["unstreamed_us"],
+                "cancel_to_no_further_write_us": ln["cancel_to_no_further_write_us"],
+                "workload": ln["config"]["workload"]}
+        elif name == "tp":
+            out[name] = {k: {"one_call_us": v["us_per_reshard_one_call"],
+                             "one_call_frac_of_measured_hbm": v["frac_of_measured_hbm_one_call"],
+                             "pairs_us": v["us_per_reshard"],
+                             "streamed_all_ready_us": v["us_per_reshard_streamed_all_ready"],
+                             "streamed_half_the_sms_us": v["us_per_reshard_streamed_half_the_sms"]}
+                         for k, v in ln["reshards"].items()}
+            out[name]["workload"] = ln["config"]["workload"]
+        else:
+            out[name] = {k: {"row_bytes": v["row_bytes"], "us": v["us_per_request"],
+                             "frac_of_measured_hbm": v["frac_of_measured_hbm"],
+                             "frac_of_measured_hbm_sector_rounded":
+                                 v["frac_of_measured_hbm_sector_rounded"],
+                             **({"streamed_us": v["streamed_us_per_request"]}
+                                if "streamed_us_per_request" in v else {})}
+                         for k, v in ln["formats"].items()}
+        out[name]["steps"] = sub.steps
+        out[name]["clocks"] = clk
+    torch.cuda.empty_cache()
+    return out
 
 
 def host_description():
@@ -1686,6 +1756,8 @@ def main():
     if world == 1 and not args.no_workloads:
         del res
         line["config"]["workloads"] = workload_summaries(args)
+    if world == 1 and not args.no_next_rows:
+        line["config"]["next_rows"] = next_row_summaries(args)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line), flush=True)
