@@ -14,6 +14,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
 from typing import Optional, Sequence
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -585,3 +586,73 @@ def move_heads(op: int, src: Optional[Layout], src_slots, src_head0: int, dst: O
                               _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
                               _flags(flags), _stream(stream))
     _check(rc, "kvx_move_heads")
+
+
+# ---- checked calls -------------------------------------------------------------------------
+# The one-shot moves in the short form: gather(layout, slots, buf) and its siblings with the
+# workspace and the status word supplied here, the stream synchronised after the call, and a
+# device-side error (an index out of range, a repeated destination under KVX_CHECK_DUP)
+# raised as KvxError.  Each host thread keeps its own workspace and status word per device,
+# grown as needed, so threads on different streams do not share them.  The caller's buffers
+# and slot lists are torch tensors on the same device.
+
+
+_scratch = threading.local()
+
+
+def _scratch_for(device, n_tokens: int):
+    import torch
+    per = getattr(_scratch, "by_device", None)
+    if per is None:
+        per = _scratch.by_device = {}
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    need = workspace_size(max(1, n_tokens), 0)
+    ws, st = per.get(idx, (None, None))
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(need, dtype=torch.uint8, device=torch.device("cuda", idx))
+        st = torch.empty(4, dtype=torch.int32, device=torch.device("cuda", idx))
+        per[idx] = (ws, st)
+    return ws, st
+
+
+def _sync_and_raise(st, stream, where: str) -> None:
+    import torch
+    if stream is None:
+        torch.cuda.current_stream(st.device).synchronize()
+    elif isinstance(stream, int):
+        torch.cuda.ExternalStream(stream, device=st.device).synchronize()
+    else:
+        stream.synchronize()
+    code = int(st[0].item())
+    if code != OK:
+        raise KvxError(code, where + " (device status)")
+
+
+def gather_sync(src: Layout, slots, buf, flags=None, stream=None) -> None:
+    """buf[p][i] = row(src, p, slots[i]) for the n = slots.numel() tokens; raises KvxError if
+    any slot is out of range (nothing is written then)."""
+    n = int(slots.numel())
+    ws, st = _scratch_for(slots.device, n)
+    gather(src, slots, n, buf, ws, st, flags=flags, stream=stream)
+    _sync_and_raise(st, stream, "kvx_gather")
+
+
+def scatter_sync(dst: Layout, slots, buf, flags=None, stream=None) -> None:
+    """row(dst, p, slots[i]) = buf[p][i]; raises KvxError on a bad slot (or, with CHECK_DUP, a
+    repeated one), with nothing written."""
+    n = int(slots.numel())
+    ws, st = _scratch_for(slots.device, n)
+    scatter(dst, slots, n, buf, ws, st, flags=flags, stream=stream)
+    _sync_and_raise(st, stream, "kvx_scatter")
+
+
+def transfer_sync(src: Layout, src_slots, dst: Layout, dst_slots, flags=None,
+                  stream=None) -> None:
+    """row(dst, p, dst_slots[i]) = row(src, p, src_slots[i]); raises KvxError on a bad slot
+    (or, with CHECK_DUP, a repeated destination), with nothing written."""
+    n = int(src_slots.numel())
+    if int(dst_slots.numel()) != n:
+        raise ValueError("the two slot lists differ in length")
+    ws, st = _scratch_for(src_slots.device, n)
+    transfer(src, src_slots, dst, dst_slots, n, ws, st, flags=flags, stream=stream)
+    _sync_and_raise(st, stream, "kvx_transfer")
