@@ -1410,6 +1410,6 @@ kvx_status kvx_set_check_duplicates(int32_t on) {
 
 int32_t kvx_get_check_duplicates(void) { return g_check_dup.load(std::memory_order_relaxed); }
 
-int32_t kvx_version(void) { return 203; }
+int32_t kvx_version(void) { return 300; }
 
 }  // extern "C"

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_misc(lib):
-    assert kvx.version() == 203
+    assert kvx.version() == 300
     assert kvx.status_str(kvx.OK) == "ok"
     assert "range" in kvx.status_str(kvx.ERR_OUT_OF_RANGE)
     ws = kvx.workspace_size(2048, 0)
