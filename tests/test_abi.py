@@ -389,3 +389,20 @@ def test_stream_page_epochs_validation(lib):
     assert l.kvx_stream(*args(kvx.OP_GATHER, src, None)) == kvx.ERR_INVALID_ARG  # no destination pool
     c.reserved2 = 1
     assert l.kvx_stream(*args(kvx.OP_TRANSFER, src, dst)) == kvx.ERR_INVALID_ARG
+
+
+def test_header_compiles_as_strict_c99_and_cpp17(tmp_path):
+    """kvx.h alone, as C99 and as C++17, with every warning an error."""
+    c = tmp_path / "h.c"
+    c.write_text('#include "kvx.h"\nint main(void) { return kvx_version() > 0 ? 0 : 1; }\n')
+    for cmd in (["gcc", "-std=c99"], ["g++", "-std=c++17", "-x", "c++"]):
+        subprocess.run(cmd + ["-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only",
+                              "-I", os.path.dirname(HEADER), str(c)], check=True)
+
+
+def test_c_program_builds_against_the_library(lib, tmp_path):
+    """The plain-C transfer program (run on the GPU by tests/test_gpu_c_abi.py) compiles as
+    strict C99 and links against libkvx.so."""
+    from tests.cprog import build_c_program
+    exe = build_c_program(str(tmp_path / "transfer_from_c"))
+    assert os.path.exists(exe)
