@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
       const int32_t code = sops::row_wait(k, l, owner);
       if (code) {
         go = 0;
+        pdl_wait();  // after the planner's status words (as kvx_stream's row grid)
         atomicMax(&a.status[2], code);
         atomicMax(&a.status[1], k.layers - l);
       }

@@ -456,6 +456,10 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
       const int32_t code = row_wait(k, l, owner);
       if (code) {
         go = 0;
+        // The stop is recorded only once the planner has finished: a one-CTA validation
+        // stores all four status words and would otherwise overwrite it.  This also keeps the
+        // grid from completing before the planner, so the epilogue reads the final verdict.
+        pdl_wait();
         atomicMax(&a.status[2], code);
         atomicMax(&a.status[1], k.layers - l);
       }
@@ -463,7 +467,7 @@ __global__ void __launch_bounds__(kCopyThreads, kTail && (kSrcHnd || kDstHnd) ? 
     s_stop = go;
   }
   __syncthreads();  // thread 0's acquire of the layer orders every thread's row loads
-  if (!s_stop) return;  // stopped: this CTA writes nothing, so it need not wait for the planner
+  if (!s_stop) return;  // stopped: this CTA writes no row
   const int32_t p = k.kv_planes * l + kv;
   const int32_t R = a.row_bytes, vpr = R >> 4;
   const int32_t li = lane - rl * m;

@@ -406,3 +406,27 @@ def test_stream_all_pages_owned_moves_everything(grid):
     v = st.cpu().tolist()
     assert v[0] == kvx.OK and v[1] == 0 and v[3] == 1, v
     hz.assert_same_bytes(dst.readback(), exp.host, "every page owned")
+
+
+@pytest.mark.parametrize("n", [2048, 8192])
+def test_stream_cancelled_before_launch_while_validating(n, grid):
+    """The epoch word changed before the call: every CTA stops at its first look, often while the
+    one-CTA validation (which initialises all four status words) is still running.  Over 100
+    calls each must report CANCELLED with every layer pending and the done word set, and leave
+    the pool untouched."""
+    g = _rng(210)
+    src = _pool("planes", "normal", g, num_slots=16384)
+    dst = _pool("planes", "sentinel", salt=5, num_slots=16384)
+    s, d = _slots(211, n, 16384), _slots(212, n, 16384)
+    before = dst.readback()
+    epoch = torch.tensor([7], dtype=torch.int32, device="cuda")
+    sd, dd, ws = hz.dev_i32(s), hz.dev_i32(d), hz.workspace(n)
+    sts = [_status() for _ in range(100)]
+    for st in sts:
+        kvx.stream(kvx.OP_TRANSFER, hz.kvx_layout(src), sd, hz.kvx_layout(dst), dd, n, None, ws,
+                   st, epoch_word=epoch, epoch=6, max_ctas=grid, buf_bytes=0)
+    torch.cuda.synchronize()
+    got = [st.cpu().tolist() for st in sts]
+    bad = [v for v in got if not (v[0] == kvx.ERR_CANCELLED and v[1] == SH["L"] and v[3] == 1)]
+    assert not bad, (len(bad), bad[:5])
+    hz.assert_same_bytes(dst.readback(), before, "cancelled before launch: nothing moved")
