@@ -330,17 +330,28 @@ def test_fuzz_case(k):
                 b"".join(bytes(kvx.Request(*r)) for r in c.reqs) or bytes(32),
                 dtype=np.uint8).copy()).cuda()
             ws = hz.workspace(n, len(c.reqs))
-            kvx.batch(sl, dl, dreq, len(c.reqs), n, s_d, len(c.s), d_d, len(c.d), bufp, ws, st,
-                      buf_bytes=buf_n, flags=f)
+            if k % 2 == 0:
+                kvx.batch(sl, dl, dreq, len(c.reqs), n, s_d, len(c.s), d_d, len(c.d), bufp, ws,
+                          st, buf_bytes=buf_n, flags=f)
+            else:  # the same batch as plan + execute
+                kvx.plan_batch(sl, dl, dreq, len(c.reqs), n, s_d, len(c.s), d_d, len(c.d), buf_n,
+                               ws, st, flags=f)
+                kvx.execute(kvx.OP_BATCH, sl, dl, dreq, len(c.reqs), n, bufp, ws, st,
+                            buf_bytes=buf_n, flags=f)
         elif c.call == "plan_execute":
             ws = hz.workspace(n)
             kvx.plan(OP[c.op], sl, s_d, dl, d_d, n, ws, st, flags=f)
             kvx.execute(OP[c.op], sl, dl, None, 0, n, bufp, ws, st, buf_bytes=buf_n, flags=f)
         elif c.call == "submit":
             ws = hz.workspace(n)
-            hs = torch.from_numpy(c.s.copy()).pin_memory() if len(c.s) else None
-            hd = torch.from_numpy(c.d.copy()).pin_memory() if len(c.d) else None
-            hst = torch.full((1,), -1, dtype=torch.int32).pin_memory()
+            if k % 3:  # pinned lists and status word, read in place by the kernels
+                hs = torch.from_numpy(c.s.copy()).pin_memory() if len(c.s) else None
+                hd = torch.from_numpy(c.d.copy()).pin_memory() if len(c.d) else None
+                hst = torch.full((1,), -1, dtype=torch.int32).pin_memory()
+            else:  # pageable ones, staged by the call
+                hs = c.s.copy() if len(c.s) else None
+                hd = c.d.copy() if len(c.d) else None
+                hst = np.full(1, -1, dtype=np.int32)
             kvx.submit(OP[c.op], sl, hs, dl, hd, n, bufp, ws, hst, buf_bytes=buf_n, flags=f)
         else:  # noalloc
             kvx.transfer_noalloc(sl, s_d, dl, d_d, n, st, flags=f)
