@@ -47,6 +47,8 @@ ELEM_BYTES = {F16: 2, BF16: 2, F32: 4, FP8: 1}
 
 
 class KvxError(RuntimeError):
+    """A non-OK kvx_status: `code` is the status, the message names the call."""
+
     def __init__(self, code: int, where: str):
         self.code = code
         msg = status_str(code)
@@ -56,6 +58,7 @@ class KvxError(RuntimeError):
 
 
 class LayoutDesc(ctypes.Structure):
+    """kvx_layout_desc (kvx.h), as given to kvx_layout_create."""
     _fields_ = [
         ("num_layers", ctypes.c_int32),
         ("kv_heads", ctypes.c_int32),
@@ -74,6 +77,7 @@ class LayoutDesc(ctypes.Structure):
 
 
 class Request(ctypes.Structure):
+    """kvx_request (kvx.h): one request of a batch, 32 bytes."""
     _fields_ = [
         ("op", ctypes.c_int32),
         ("n_tokens", ctypes.c_int32),
@@ -196,6 +200,7 @@ def lib() -> ctypes.CDLL:
 
 
 def exported_names() -> Sequence[str]:
+    """The C entry points this binding declares (every KVX_API function of kvx.h)."""
     return tuple(_SIGS)
 
 
@@ -235,14 +240,17 @@ def _check(rc: int, where: str) -> None:
 
 
 def status_str(code: int) -> str:
+    """kvx_status_str: the status code's name."""
     return lib().kvx_status_str(code).decode()
 
 
 def last_cuda_error() -> int:
+    """kvx_last_cuda_error: the cudaError_t behind this thread's last KVX_ERR_CUDA."""
     return int(lib().kvx_last_cuda_error())
 
 
 def version() -> int:
+    """kvx_version: major * 10000 + minor * 100 + patch."""
     return int(lib().kvx_version())
 
 
@@ -257,10 +265,12 @@ ONE_LAUNCH = 0x8
 
 
 def set_copy_engine(engine: int) -> None:
+    """Process-wide default copy engine (ENGINE_AUTO / _REGISTERS / _BULK) for flags=None."""
     _check(lib().kvx_set_copy_engine(engine), "kvx_set_copy_engine")
 
 
 def get_copy_engine() -> int:
+    """The process-wide default copy engine."""
     return int(lib().kvx_get_copy_engine())
 
 
@@ -268,22 +278,28 @@ FUSED_MAX_TOKENS = 8192
 
 
 def set_fused_max_tokens(max_tokens: int) -> None:
+    """Process-wide default limit of the one-launch path (0: off) for flags=None."""
     _check(lib().kvx_set_fused_max_tokens(max_tokens), "kvx_set_fused_max_tokens")
 
 
 def get_fused_max_tokens() -> int:
+    """The process-wide default limit of the one-launch path."""
     return int(lib().kvx_get_fused_max_tokens())
 
 
 def set_check_duplicates(on: bool) -> None:
+    """Process-wide default of the duplicate-destination check for flags=None."""
     _check(lib().kvx_set_check_duplicates(1 if on else 0), "kvx_set_check_duplicates")
 
 
 def get_check_duplicates() -> bool:
+    """The process-wide default of the duplicate-destination check."""
     return bool(lib().kvx_get_check_duplicates())
 
 
 def workspace_size(max_tokens: int, max_requests: int = 0) -> int:
+    """kvx_workspace_size: bytes of workspace for calls of up to max_tokens rows per plane and
+    max_requests requests (batches) or runs (run lists)."""
     return int(lib().kvx_workspace_size(max_tokens, max_requests))
 
 
@@ -340,6 +356,8 @@ def _h(layout: Optional[Layout]) -> Optional[int]:
 
 def gather(src: Layout, src_slots, n: int, buf, ws, status, buf_bytes=None, ws_bytes=None,
            flags=None, stream=None) -> None:
+    """kvx_gather: buf[p][i] = row(src, p, src_slots[i]) for i < n; the device status word
+    (status) gets KVX_OK or KVX_ERR_OUT_OF_RANGE (nothing written)."""
     rc = lib().kvx_gather(_h(src), _ptr(src_slots), n, _ptr(buf),
                           _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
                           _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
@@ -349,6 +367,7 @@ def gather(src: Layout, src_slots, n: int, buf, ws, status, buf_bytes=None, ws_b
 
 def scatter(dst: Layout, dst_slots, n: int, buf, ws, status, buf_bytes=None, ws_bytes=None,
             flags=None, stream=None) -> None:
+    """kvx_scatter: row(dst, p, dst_slots[i]) = buf[p][i]; rows of other slots keep their bytes."""
     rc = lib().kvx_scatter(_h(dst), _ptr(dst_slots), n, _ptr(buf),
                            _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
                            _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
@@ -358,6 +377,7 @@ def scatter(dst: Layout, dst_slots, n: int, buf, ws, status, buf_bytes=None, ws_
 
 def transfer(src: Layout, src_slots, dst: Layout, dst_slots, n: int, ws, status,
              ws_bytes=None, flags=None, stream=None) -> None:
+    """kvx_transfer: row(dst, p, dst_slots[i]) = row(src, p, src_slots[i]) for i < n."""
     rc = lib().kvx_transfer(_h(src), _ptr(src_slots), _h(dst), _ptr(dst_slots), n, _ptr(ws),
                             _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
                             _flags(flags), _stream(stream))
@@ -376,6 +396,8 @@ def transfer_noalloc(src: Layout, src_slots, dst: Layout, dst_slots, n: int, sta
 
 def gather_runs(src: Layout, runs, n_runs: int, n_tokens: int, buf, ws, status, buf_bytes=None,
                 ws_bytes=None, flags=None, stream=None) -> None:
+    """kvx_gather_runs: runs is a device int32[n_runs][3] of (src_start, dst_start, len);
+    the buffer fills in run order (its start field ignored)."""
     rc = lib().kvx_gather_runs(_h(src), _ptr(runs), n_runs, n_tokens, _ptr(buf),
                                _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
                                _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
@@ -385,6 +407,7 @@ def gather_runs(src: Layout, runs, n_runs: int, n_tokens: int, buf, ws, status, 
 
 def scatter_runs(dst: Layout, runs, n_runs: int, n_tokens: int, buf, ws, status,
                  buf_bytes=None, ws_bytes=None, flags=None, stream=None) -> None:
+    """kvx_scatter_runs: the runs' destination slots take consecutive buffer rows."""
     rc = lib().kvx_scatter_runs(_h(dst), _ptr(runs), n_runs, n_tokens, _ptr(buf),
                                 _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
                                 _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
@@ -394,6 +417,7 @@ def scatter_runs(dst: Layout, runs, n_runs: int, n_tokens: int, buf, ws, status,
 
 def transfer_runs(src: Layout, dst: Layout, runs, n_runs: int, n_tokens: int, ws, status,
                   ws_bytes=None, flags=None, stream=None) -> None:
+    """kvx_transfer_runs: rows src_start.. of each run to dst_start.. of the same run."""
     rc = lib().kvx_transfer_runs(_h(src), _h(dst), _ptr(runs), n_runs, n_tokens, _ptr(ws),
                                  _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
                                  _flags(flags), _stream(stream))
@@ -403,6 +427,8 @@ def transfer_runs(src: Layout, dst: Layout, runs, n_runs: int, n_tokens: int, ws
 def batch(src: Optional[Layout], dst: Optional[Layout], reqs, n_reqs: int, total_tokens: int,
           src_slots, n_src_slots: int, dst_slots, n_dst_slots: int, buf, ws, status,
           buf_bytes=None, ws_bytes=None, flags=None, stream=None) -> None:
+    """kvx_batch: the requests (device array of Request) in one plan + one copy; status has
+    n_reqs + 1 words (overall, then each request's own)."""
     rc = lib().kvx_batch(_h(src), _h(dst), _ptr(reqs), n_reqs, total_tokens, _ptr(src_slots),
                          n_src_slots, _ptr(dst_slots), n_dst_slots, _ptr(buf),
                          _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
@@ -431,6 +457,7 @@ def _host_ptr(x) -> Optional[int]:
 
 def plan(op: int, src: Optional[Layout], src_slots, dst: Optional[Layout], dst_slots, n: int,
          ws, status, ws_bytes=None, flags=None, stream=None) -> None:
+    """kvx_plan: validate and plan a slot-list move into ws (run it with execute)."""
     rc = lib().kvx_plan(op, _h(src), _ptr(src_slots), _h(dst), _ptr(dst_slots), n, _ptr(ws),
                         _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
                         _flags(flags), _stream(stream))
@@ -439,6 +466,7 @@ def plan(op: int, src: Optional[Layout], src_slots, dst: Optional[Layout], dst_s
 
 def plan_runs(op: int, src: Optional[Layout], dst: Optional[Layout], runs, n_runs: int,
               n_tokens: int, ws, status, ws_bytes=None, flags=None, stream=None) -> None:
+    """kvx_plan_runs: the plan of a run-list move."""
     rc = lib().kvx_plan_runs(op, _h(src), _h(dst), _ptr(runs), n_runs, n_tokens, _ptr(ws),
                              _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
                              _flags(flags), _stream(stream))
@@ -448,6 +476,7 @@ def plan_runs(op: int, src: Optional[Layout], dst: Optional[Layout], runs, n_run
 def plan_batch(src: Optional[Layout], dst: Optional[Layout], reqs, n_reqs: int,
                total_tokens: int, src_slots, n_src_slots: int, dst_slots, n_dst_slots: int,
                buf_bytes: int, ws, status, ws_bytes=None, flags=None, stream=None) -> None:
+    """kvx_plan_batch: the plan of a batch (execute it with op OP_BATCH)."""
     rc = lib().kvx_plan_batch(_h(src), _h(dst), _ptr(reqs), n_reqs, total_tokens,
                               _ptr(src_slots), n_src_slots, _ptr(dst_slots), n_dst_slots,
                               buf_bytes, _ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
@@ -457,6 +486,8 @@ def plan_batch(src: Optional[Layout], dst: Optional[Layout], reqs, n_reqs: int,
 
 def execute(op: int, src: Optional[Layout], dst: Optional[Layout], reqs, n_reqs: int,
             n_tokens: int, buf, ws, status, buf_bytes=None, ws_bytes=None, flags=None, stream=None) -> None:
+    """kvx_execute: the copy of the plan in ws; sizes must match the plan's (else
+    KVX_ERR_INVALID_ARG on the device)."""
     rc = lib().kvx_execute(op, _h(src), _h(dst), _ptr(reqs), n_reqs, n_tokens, _ptr(buf),
                            _nbytes(buf) if buf_bytes is None else buf_bytes, _ptr(ws),
                            _nbytes(ws) if ws_bytes is None else ws_bytes, _ptr(status),
@@ -466,6 +497,8 @@ def execute(op: int, src: Optional[Layout], dst: Optional[Layout], reqs, n_reqs:
 
 def plan_export(ws, n_tokens: int, out, max_chunks: int, count, ws_bytes=None,
                 stream=None) -> None:
+    """kvx_plan_export: the plan's chunks as int32[count][4] (request, source offset,
+    destination offset, rows), for inspection."""
     rc = lib().kvx_plan_export(_ptr(ws), _nbytes(ws) if ws_bytes is None else ws_bytes,
                                n_tokens, _ptr(out), max_chunks, _ptr(count), _stream(stream))
     _check(rc, "kvx_plan_export")
