@@ -28,9 +28,10 @@
  * Conventions used by every call:
  *  - A layout has P = 2 * num_layers planes, plane p = 2*layer + kv with K = 0, V = 1 (or, with
  *    kv_planes = 1 for MLA, P = num_layers latent planes, plane p = layer).
- *  - A row is one (plane, token): kv_heads * head_dim elements, R bytes.  R must be a multiple
- *    of 16.  Values are never interpreted: every operation is an exact byte copy, so NaN
- *    payloads and any bit pattern survive.
+ *  - A row is one (plane, token): kv_heads * head_dim elements, R bytes (any R; rows that are
+ *    not 16-byte multiples move in narrower accesses, see kvx_layout_desc).  Values are never
+ *    interpreted: every operation is an exact byte copy, so NaN payloads and any bit pattern
+ *    survive.
  *  - A contiguous transfer buffer holding n tokens is [plane][n][kv_heads][head_dim], i.e.
  *    [layer][K/V][seq][head][dim]: row (p, i) starts at byte (p * n + i) * R.
  *  - Slots and page-table entries are int32.  Byte offsets are 64-bit.
