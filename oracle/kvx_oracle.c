@@ -482,7 +482,9 @@ int64_t kvxo_runs(const int32_t *src_idx, const int32_t *dst_idx, int64_t n,
     while (q + 1 < n_reqs && req_start[q + 1] <= a) ++q; /* request of token a */
     const int64_t req_end = (q + 1 < n_reqs) ? req_start[q + 1] : n;
     int64_t b = a + 1;
-    while (b < req_end && src_idx[b] == src_idx[b - 1] + 1 && dst_idx[b] == dst_idx[b - 1] + 1)
+    /* the step test in 64 bits: an index list may hold INT32_MAX */
+    while (b < req_end && (int64_t)src_idx[b] == (int64_t)src_idx[b - 1] + 1 &&
+           (int64_t)dst_idx[b] == (int64_t)dst_idx[b - 1] + 1)
       ++b;
     if (count < max_runs) {
       out[count].req = q;

@@ -710,7 +710,8 @@ def pin_plan(lib):
     """[Mooncake] 7.6 coalescing, by brute force: for every pair of index lists of up to three
     tokens over four values and every request split, the oracle's runs are the coarsest
     cutting of the tokens into pieces that stay in one request and step up by one on both
-    lists (found by trying every cutting); the same on random four- and five-token cases.
+    lists (found by trying every cutting); the same on random four- and five-token cases and
+    on lists holding INT32_MAX next to INT32_MIN.
     Invariants on long lists: the runs expand back to the index lists, the run count is
     1 + the number of places where either list stops stepping by one or a request starts, and
     a contiguous request of any length is a single run (nothing else, such as a tile or a page
@@ -734,6 +735,13 @@ def pin_plan(lib):
         reqs = [0] + sorted(set(g.integers(1, n, int(g.integers(0, 3))).tolist()))
         got = oracle.runs(src, dst, reqs, lib=lib)
         assert [tuple(r) for r in got.tolist()] == _coarsest_segmentation(src, dst, reqs)
+    # the extremes of int32: INT32_MAX followed by INT32_MIN does not step up by one (a step
+    # test in wrapping 32-bit arithmetic would merge them)
+    big, small = 2 ** 31 - 1, -2 ** 31
+    for src, dst in (([big - 1, big, small], [0, 1, 2]), ([0, 1, 2], [big - 1, big, small]),
+                     ([big, small, small + 1], [big, small, small + 1])):
+        got = oracle.runs(src, dst, [0], lib=lib)
+        assert [tuple(r) for r in got.tolist()] == _coarsest_segmentation(src, dst, [0])
     # a contiguous request is one run whatever its length (72 blocks on a fresh pool,
     # "穷人版 PD 分离", 5090 section: one block per layer and K/V)
     for n in (1, 2047, 2048, 2049, 100000):

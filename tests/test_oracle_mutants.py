@@ -35,10 +35,13 @@ MUTANTS = {
     "permute_missing": ("memcpy(buf_vec(buf, src, p, seq_len, s, h), logical + ((int64_t)h * seq_len + s) * hb,",
                         "memcpy(buf_vec(buf, src, p, seq_len, s, h), logical + ((int64_t)s * H + h) * hb,"),
     "factor_two_dropped": ("return (int64_t)2 * num_layers", "return (int64_t)num_layers"),
-    "runs_dst_break_dropped": (" && dst_idx[b] == dst_idx[b - 1] + 1)", ")"),
+    "runs_dst_break_dropped": (" &&\n           (int64_t)dst_idx[b] == (int64_t)dst_idx[b - 1] + 1)", ")"),
     "runs_request_break_dropped": ("const int64_t req_end = (q + 1 < n_reqs) ? req_start[q + 1] : n;",
                                    "const int64_t req_end = n;"),
-    "runs_src_step_of_two": ("src_idx[b] == src_idx[b - 1] + 1 &&", "src_idx[b] >= src_idx[b - 1] + 1 &&"),
+    "runs_src_step_of_two": ("(int64_t)src_idx[b] == (int64_t)src_idx[b - 1] + 1 &&",
+                             "(int64_t)src_idx[b] >= (int64_t)src_idx[b - 1] + 1 &&"),
+    "runs_step_in_32_bits": ("(int64_t)src_idx[b] == (int64_t)src_idx[b - 1] + 1 &&",
+                             "(uint32_t)src_idx[b] == (uint32_t)src_idx[b - 1] + 1u &&"),
     "batch_status_not_per_request": ("status[1 + q] = rc;", "status[1 + q] = 0;"),
     "batch_dup_pairs_missed": ("if (count[dst_slots[r->dst_off + i]] > 1) {",
                                "if (count[dst_slots[r->dst_off + i]] > 2) {"),
