@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kFThreads, kLinear ? 8 : 4)
       if (j < cnt) {
         sv[k] = src_of(ta + j);
         dv[k] = dst_of(ta + j);
-        brk[k] = j == 0 || sv[k] != ps + 1 || dv[k] != pd + 1 ||
+        brk[k] = j == 0 || (int64_t)sv[k] != (int64_t)ps + 1 || (int64_t)dv[k] != (int64_t)pd + 1 ||
                  (sp && a.src.hnd && sv[k] % a.src.page_size == 0) ||
                  (dp && a.dst.hnd && dv[k] % a.dst.page_size == 0);
         ps = sv[k];

@@ -138,7 +138,8 @@ __device__ __forceinline__ Tok fetch(const PlanArgs &a, int64_t g, int32_t &seg)
 __device__ __forceinline__ bool starts_run(const PlanArgs &a, const Tok &t, const Tok &prev,
                                            bool first_in_tile) {
   if (first_in_tile || t.start || t.req != prev.req) return true;
-  if (t.s != prev.s + 1 || t.d != prev.d + 1) return true;
+  // 64-bit steps: an index list may hold INT32_MAX (refused later, but never overflowed here)
+  if ((int64_t)t.s != (int64_t)prev.s + 1 || (int64_t)t.d != (int64_t)prev.d + 1) return true;
   const bool sp = (a.mode == kModeBatch) ? uses_src_pool(t.op) : (bool)a.src.is_pool;
   const bool dp = (a.mode == kModeBatch) ? uses_dst_pool(t.op) : (bool)a.dst.is_pool;
   if (sp && a.src.hnd && t.s % a.src.page_size == 0) return true;
